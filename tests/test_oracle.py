@@ -1,0 +1,315 @@
+"""Pins of the CPU oracle against things other than itself (no GPU)."""
+
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import gpt_oracle as O
+from persistent_gpt_step_gb300 import inputs as I
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+TINY = I.CONFIGS["tiny"]
+# an even smaller model for the exhaustive checks
+MICRO = TINY.replace(name="micro", n_layer=2, d_model=16, n_head=2, d_mlp=32, vocab=11,
+                     seq_len=6, batch=2)
+
+
+def _tiny_inputs(cfg, seed=7, step=0):
+    params = I.init_params(O.param_table(cfg), seed).astype(np.float64)
+    tok, tgt = I.batch(cfg, seed, step)
+    return params, tok, tgt
+
+
+def _read_kv(path):
+    out = {}
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        k, v = line.split(None, 1)
+        out[k] = v
+    return out
+
+
+# ----------------------------------------------------------------- page values
+
+def test_param_counts_match_pages():
+    for line in open(os.path.join(GOLD, "param_counts.txt")):
+        if not line.strip() or line.startswith("#"):
+            continue
+        name, L, C, H, F, V, T, lb, nb, count = line.split()
+        cfg = TINY.replace(n_layer=int(L), d_model=int(C), n_head=int(H), d_mlp=int(F),
+                           vocab=int(V), seq_len=int(T), linear_bias=bool(int(lb)),
+                           ln_bias=bool(int(nb)))
+        assert O.num_params(cfg) == int(count), name
+
+
+def test_param_count_closed_form():
+    for cfg in I.CONFIGS.values():
+        L, C, V, T, F = cfg.n_layer, cfg.d_model, cfg.vocab, cfg.seq_len, cfg.d_mlp
+        per_layer = 4 * C + (3 * C * C + 3 * C) + (C * C + C) + (F * C + F) + (C * F + C)
+        assert O.num_params(cfg) == L * per_layer + 2 * V * C + T * C + 2 * C
+
+
+def test_know_nothing_loss_is_ln_vocab():
+    g = _read_kv(os.path.join(GOLD, "know_nothing_loss.txt"))
+    V = int(g["vocab"])
+    cfg = MICRO.replace(vocab=V, seq_len=8, batch=2)
+    rng = np.random.default_rng(0)
+    params = rng.normal(0, 0.02, O.num_params(cfg))
+    O.param_views(cfg, params)["w_lm"][...] = 0.0       # every token equally likely
+    tok = rng.integers(0, V, (2, 8))
+    tgt = rng.integers(0, V, (2, 8))
+    loss, _ = O.forward(cfg, params, tok, tgt)
+    assert round(loss, int(g["decimals"])) == float(g["loss"])
+    assert abs(loss - math.log(V)) < 1e-12
+
+
+def test_initial_loss_near_ln_vocab_uniform_tokens():
+    params, tok, tgt = _tiny_inputs(TINY)
+    loss, _ = O.forward(TINY, params, tok, tgt)
+    assert abs(loss - math.log(TINY.vocab)) < 0.05
+
+
+# ----------------------------------------------------------------- invariants
+
+def test_softmax_rows_sum_to_one_and_dz_rows_to_zero():
+    rng = np.random.default_rng(1)
+    z = rng.normal(0, 3, (64, 300))
+    p = O.softmax_rows(z)
+    assert np.abs(p.sum(1) - 1).max() < 1e-6
+    t = rng.integers(0, 300, 64)
+    loss, rows, dz = O.cross_entropy(z, t)
+    assert np.abs(dz.sum(1)).max() < 1e-12
+    # the row loss is -log p[target]
+    assert np.allclose(rows, -np.log(p[np.arange(64), t]), rtol=1e-12)
+
+
+def test_cross_entropy_matches_logsumexp_definition():
+    rng = np.random.default_rng(2)
+    z = rng.normal(0, 2, (5, 7))
+    t = rng.integers(0, 7, 5)
+    loss, rows, _ = O.cross_entropy(z, t)
+    ref = [math.log(sum(math.exp(v) for v in z[i])) - z[i, t[i]] for i in range(5)]
+    assert np.allclose(rows, ref, rtol=1e-13)
+    assert abs(loss - sum(ref) / 5) < 1e-13
+
+
+def test_causality():
+    params, tok, tgt = _tiny_inputs(TINY)
+    _, c0 = O.forward(TINY, params, tok, tgt)
+    tok2 = tok.copy()
+    t = 37
+    tok2[:, t] = (tok2[:, t] + 101) % TINY.vocab
+    _, c1 = O.forward(TINY, params, tok2, tgt)
+    z0 = c0["z"].reshape(TINY.batch, TINY.seq_len, -1)
+    z1 = c1["z"].reshape(TINY.batch, TINY.seq_len, -1)
+    assert np.array_equal(z0[:, :t], z1[:, :t])
+    assert not np.allclose(z0[:, t:], z1[:, t:])
+
+
+def test_attention_single_position_returns_v():
+    rng = np.random.default_rng(3)
+    q, k, v = (rng.normal(size=(2, 3, 1, 8)) for _ in range(3))
+    o, p = O.causal_attention(q, k, v)
+    assert np.array_equal(p, np.ones_like(p))
+    assert np.allclose(o, v, rtol=0, atol=0)
+
+
+def test_attention_matches_per_row_loop():
+    rng = np.random.default_rng(4)
+    q, k, v = (rng.normal(size=(1, 1, 5, 4)) for _ in range(3))
+    o, _ = O.causal_attention(q, k, v)
+    for i in range(5):
+        s = [float(q[0, 0, i] @ k[0, 0, j]) / 2.0 for j in range(i + 1)]
+        w = np.exp(np.array(s) - max(s))
+        w /= w.sum()
+        assert np.allclose(o[0, 0, i], (w[:, None] * v[0, 0, :i + 1]).sum(0), rtol=1e-13)
+
+
+def test_layernorm_moments():
+    rng = np.random.default_rng(5)
+    x = rng.normal(3, 7, (10, 64))
+    y, xhat, _ = O.layernorm(x, np.ones(64), np.zeros(64), 1e-5)
+    assert np.abs(xhat.mean(1)).max() < 1e-12
+    assert np.abs(xhat.var(1) - 1).max() < 1e-5     # eps shifts the variance by ~eps/49
+    assert np.array_equal(y, xhat)
+
+
+def test_gelu_special_values():
+    x = np.linspace(-6, 6, 2001)
+    assert O.gelu(np.array([0.0]))[0] == 0.0
+    assert abs(O.gelu_grad(np.array([0.0]))[0] - 0.5) < 1e-15
+    # the tanh form approximates the erf form within 1e-3 everywhere
+    assert np.abs(O.gelu(x, True) - O.gelu(x, False)).max() < 1e-3
+    assert abs(O.gelu(np.array([30.0]))[0] - 30.0) < 1e-12
+    # derivative against central differences
+    h = 1e-6
+    fd = (O.gelu(x + h) - O.gelu(x - h)) / (2 * h)
+    assert np.abs(fd - O.gelu_grad(x)).max() < 1e-8
+    fd = (O.gelu(x + h, False) - O.gelu(x - h, False)) / (2 * h)
+    assert np.abs(fd - O.gelu_grad(x, False)).max() < 1e-8
+
+
+# ----------------------------------------------------------------- gradients
+
+def _loss(cfg, params, tok, tgt):
+    return O.forward(cfg, params, tok, tgt, keep=False)[0]
+
+
+def _one_blas_thread():
+    try:
+        from threadpoolctl import threadpool_limits
+        return threadpool_limits(1)
+    except ImportError:          # not installed everywhere; only slower without it
+        import contextlib
+        return contextlib.nullcontext()
+
+
+def test_finite_differences_tiny_fp64():
+    """Central differences on >=200 scalars per tensor (all of the small ones)."""
+    with _one_blas_thread():
+        _finite_differences_tiny_fp64()
+
+
+def _finite_differences_tiny_fp64():
+    cfg = TINY
+    params, tok, tgt = _tiny_inputs(cfg, seed=11)
+    # non-trivial LN/bias values so their gradients are exercised
+    rng = np.random.default_rng(12)
+    views = O.param_views(cfg, params)
+    for name, arr in views.items():
+        if name.endswith(("_b", "_g", "b_qkv", "b_o", "b_1", "b_2")):
+            arr += rng.normal(0, 0.1, arr.shape)
+    _, cache = O.forward(cfg, params, tok, tgt)
+    grad = O.backward(cfg, params, cache)
+    gv = O.param_views(cfg, grad)
+    off = 0
+    for name, shape, _ in O.param_table(cfg):
+        n = int(np.prod(shape))
+        idx = np.arange(n) if n <= 256 else rng.choice(n, 200, replace=False)
+        if name == "wte":   # rows of tokens that occur (the others have zero gradient)
+            rows = np.unique(tok)[:40]
+            idx = np.unique(np.concatenate([idx, (rows[:, None] * shape[1] + np.arange(5)).ravel()]))
+        fd = np.empty(len(idx))
+        for j, e in enumerate(idx):
+            p0 = params[off + e]
+            h = 1e-6 * max(1.0, abs(p0))
+            params[off + e] = p0 + h
+            lp = _loss(cfg, params, tok, tgt)
+            params[off + e] = p0 - h
+            lm = _loss(cfg, params, tok, tgt)
+            params[off + e] = p0
+            fd[j] = (lp - lm) / (2 * h)
+        an = gv[name].reshape(-1)[idx]
+        scale = max(np.abs(an).max(), 1e-12)
+        err = np.abs(fd - an).max() / scale
+        assert err <= 1e-4, (name, err)
+        off += n
+
+
+def _torch_loss(cfg, params, tok, tgt):
+    """Independent re-statement with PyTorch CPU library operators (float64)."""
+    import torch
+    import torch.nn.functional as F
+    t = torch.tensor(params, dtype=torch.float64, requires_grad=True)
+    views, off = {}, 0
+    for name, shape, _ in O.param_table(cfg):
+        n = int(np.prod(shape))
+        views[name] = t[off:off + n].view(*shape)
+        off += n
+    B, T = tok.shape
+    C, H = cfg.d_model, cfg.n_head
+    tk = torch.tensor(tok, dtype=torch.long)
+    x = F.embedding(tk, views["wte"]) + views["wpe"][:T][None]
+    for l in range(cfg.n_layer):
+        p = f"h{l}."
+        a = F.layer_norm(x, (C,), views[p + "ln1_g"], views.get(p + "ln1_b"), cfg.ln_eps)
+        qkv = F.linear(a, views[p + "w_qkv"], views.get(p + "b_qkv"))
+        q, k, v = qkv.split(C, dim=-1)
+        q, k, v = (u.view(B, T, H, C // H).transpose(1, 2) for u in (q, k, v))
+        o = F.scaled_dot_product_attention(q, k, v, is_causal=True)
+        o = o.transpose(1, 2).reshape(B, T, C)
+        x = x + F.linear(o, views[p + "w_o"], views.get(p + "b_o"))
+        a = F.layer_norm(x, (C,), views[p + "ln2_g"], views.get(p + "ln2_b"), cfg.ln_eps)
+        h = F.gelu(F.linear(a, views[p + "w_1"], views.get(p + "b_1")),
+                   approximate="tanh" if cfg.gelu_tanh else "none")
+        x = x + F.linear(h, views[p + "w_2"], views.get(p + "b_2"))
+    x = F.layer_norm(x, (C,), views["lnf_g"], views.get("lnf_b"), cfg.ln_eps)
+    z = F.linear(x, views["w_lm"])
+    loss = F.cross_entropy(z.view(B * T, -1), torch.tensor(tgt, dtype=torch.long).view(-1))
+    loss.backward()
+    return float(loss), t.grad.numpy()
+
+
+@pytest.mark.parametrize("variant", ["tiny", "nobias_erf"])
+def test_against_torch_autograd_fp64(variant):
+    cfg = TINY if variant == "tiny" else TINY.replace(linear_bias=False, ln_bias=False,
+                                                      gelu_tanh=False)
+    params, tok, tgt = _tiny_inputs(cfg, seed=5)
+    rng = np.random.default_rng(6)
+    params = params + rng.normal(0, 0.05, params.shape)   # move LN / biases off their init
+    loss, cache = O.forward(cfg, params, tok, tgt)
+    grad = O.backward(cfg, params, cache)
+    tl, tg = _torch_loss(cfg, params, tok, tgt)
+    assert abs(loss - tl) < 1e-12 * abs(tl)
+    assert np.abs(grad - tg).max() < 1e-10 * np.abs(tg).max()
+
+
+# ----------------------------------------------------------------- AdamW
+
+def test_adamw_first_two_steps_closed_form():
+    cfg = MICRO
+    rng = np.random.default_rng(8)
+    n = O.num_params(cfg)
+    p0 = rng.normal(0, 1, n)
+    g1, g2 = rng.normal(0, 1e-2, n), rng.normal(0, 1e-2, n)
+    lr, wd, b1, b2, eps = cfg.lr, cfg.weight_decay, cfg.beta1, cfg.beta2, cfg.eps
+    dec = O.decay_mask(cfg)
+    p, m, v = p0.copy(), np.zeros(n), np.zeros(n)
+    O.adamw(cfg, p, g1, m, v, 1)
+    # bias correction cancels on the first step: update = g / (|g| + eps)
+    p1 = p0 * (1 - lr * wd * dec) - lr * g1 / (np.abs(g1) + eps)
+    assert np.allclose(p, p1, rtol=1e-14, atol=1e-16)
+    O.adamw(cfg, p, g2, m, v, 2)
+    m2 = b1 * (1 - b1) * g1 + (1 - b1) * g2
+    v2 = b2 * (1 - b2) * g1 ** 2 + (1 - b2) * g2 ** 2
+    p2 = p1 * (1 - lr * wd * dec) - lr * (m2 / (1 - b1 ** 2)) / (np.sqrt(v2 / (1 - b2 ** 2)) + eps)
+    assert np.allclose(p, p2, rtol=1e-13, atol=1e-16)
+
+
+def test_decay_mask_is_two_dimensional_tensors():
+    cfg = MICRO
+    mask = O.decay_mask(cfg)
+    off = 0
+    for name, shape, _ in O.param_table(cfg):
+        n = int(np.prod(shape))
+        assert (mask[off:off + n] == (1.0 if len(shape) == 2 else 0.0)).all(), name
+        off += n
+    assert (O.decay_mask(cfg.replace(wd_on_1d=True)) == 1).all()
+
+
+def test_train_step_decreases_loss_on_repeated_batch():
+    cfg = MICRO.replace(lr=1e-2)
+    params, tok, tgt = _tiny_inputs(cfg, seed=9)
+    st = O.OracleState(cfg, params)
+    losses = [O.train_step(st, tok, tgt) for _ in range(20)]
+    assert losses[-1] < losses[0] - 0.5
+
+
+def test_fp32_oracle_tracks_fp64_within_tolerance_tiny():
+    """The fp32 tolerance (loss 1e-4 relative, params 1e-4 max-abs over 10 steps) is
+    reachable by a correct fp32 implementation: the fp32 oracle meets it."""
+    cfg = TINY
+    params = I.init_params(O.param_table(cfg), 1234)
+    s64 = O.OracleState(cfg, params, dtype=np.float64)
+    s32 = O.OracleState(cfg, params, dtype=np.float32)
+    for step in range(cfg.steps):
+        tok, tgt = I.batch(cfg, 1234, step)
+        l64 = O.train_step(s64, tok, tgt)
+        l32 = O.train_step(s32, tok, tgt)
+        assert abs(l32 - l64) <= 1e-4 * abs(l64)
+    assert np.abs(s32.params - s64.params).max() <= 1e-4

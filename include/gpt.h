@@ -1,0 +1,257 @@
+/*
+ * gpt.h — C ABI of the persistent GPT training-step library (libgpt.so).
+ *
+ * One call of gpt_train_step runs one full training step of a GPT language
+ * model — token/position embedding, pre-LN transformer blocks (causal
+ * multi-head attention, GELU MLP), final LayerNorm, LM head, mean softmax
+ * cross-entropy, the backward pass and an AdamW update of every parameter — as
+ * ONE persistent CUDA kernel launch.  Inside that launch resident thread blocks
+ * claim tasks (GEMM tiles, attention blocks, row blocks, optimizer chunks) from
+ * a ticket counter and order dependent tasks with release/acquire completion
+ * counters, so the host launches nothing between the operations of a step.
+ *
+ * Sources of the method (web pages; cited by title and section):
+ *  - "Open Flapping Airplanes" experiment record (A100 reproduction), section
+ *    "What ran": one persistent kernel whose resident blocks repeatedly take
+ *    tasks from a scheduler; the training role runs "forward pass, backward
+ *    pass, and weight updates" of a 12-layer, width-768, 12-head GPT on 8 x 512
+ *    tokens a step with AdamW from seeded initial weights.  Section "A longer
+ *    run exposed a scheduler overflow": a task budget computed as a 32-bit
+ *    product wrapped; every counter here is 64-bit.
+ *  - "How one persistent kernel runs three jobs" (review): training claims
+ *    tasks through ticket counters; completed phases publish their writes with
+ *    a memory fence before incrementing counters, dependents use acquire reads
+ *    and wait; forward releases backward without host launches.
+ *  - "Coppelius training on the RTX 3090": loss = mean cross-entropy over the
+ *    step's rows (figure "Loss"); per-invocation exit status, error notifier and
+ *    finite-loss check (section "Channel health"); checkpoints (section
+ *    "Checkpoint lineage").
+ *
+ * Conventions for every function:
+ *  - Return 0 on success or a negative GPT_ERR_* code; gpt_last_error() gives
+ *    the text of the handle's last error.  No C++ exception crosses the ABI.
+ *  - A handle is not thread-safe: one host thread at a time.
+ *  - "device" pointers are CUDA device addresses on the handle's device;
+ *    "host" pointers are ordinary host memory (pageable or pinned).  The caller
+ *    owns every buffer it passes; the library never frees or retains them past
+ *    the call.
+ *  - Flat parameter-sized vectors use the canonical order: wte [V,C], wpe [T,C],
+ *    then per layer ln1_g, ln1_b, w_qkv [3C,C], b_qkv [3C], w_o [C,C], b_o [C],
+ *    ln2_g, ln2_b, w_1 [F,C], b_1 [F], w_2 [C,F], b_2 [C]; then lnf_g, lnf_b,
+ *    w_lm [V,C] (biases present only when the config enables them).  Matrices
+ *    are row-major [out_features, in_features]; y = x W^T + b.
+ */
+#ifndef GPT_H_
+#define GPT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+#define GPT_OK               0
+#define GPT_ERR_INVALID_ARG (-1)  /* bad config, pointer, size or index            */
+#define GPT_ERR_CUDA        (-2)  /* a CUDA runtime/driver call failed              */
+#define GPT_ERR_OOM         (-3)  /* device or host allocation failed               */
+#define GPT_ERR_TIMEOUT     (-4)  /* a device wait gave up; the handle is poisoned  */
+#define GPT_ERR_NONFINITE   (-5)  /* the step's loss is NaN or infinite             */
+#define GPT_ERR_BAD_TOKEN   (-6)  /* a token or target id outside [0, vocab)        */
+#define GPT_ERR_POISONED    (-7)  /* an earlier timeout left the handle unusable    */
+#define GPT_ERR_UNSUPPORTED (-8)  /* shape not supported by the compiled kernels    */
+
+/* Arithmetic of a handle. */
+#define GPT_DTYPE_FP32 0  /* every tensor and every operation in fp32 (SIMT)          */
+#define GPT_DTYPE_BF16 1  /* bf16 GEMM/attention operands and stored activations,
+                             fp32 accumulation, statistics, residual stream, grads,
+                             master weights and AdamW moments                       */
+
+/*
+ * Model and optimizer configuration.  Architecture: "What ran" (model shape);
+ * the choices the pages leave open are fields here with these defaults:
+ * linear_bias 1 (biases on QKV, attention-out and both MLP linears; never on
+ * the LM head), ln_bias 1, tie_embeddings 0 (the only value supported),
+ * gelu_tanh 1 (tanh approximation; 0 = erf form), eps 1e-8, ln_eps 1e-5,
+ * wd_on_1d 0 (weight decay on 2-D tensors only), constant learning rate.
+ * Limits: d_model = n_head * head_dim with head_dim 16 or 64 (bf16: 64);
+ * seq_len <= 1024; for GPT_DTYPE_BF16 d_model, d_mlp and 3*d_model must be
+ * multiples of 64 and batch*seq_len a multiple of 128.
+ */
+typedef struct gpt_config {
+  int32_t n_layer, d_model, n_head, d_mlp, vocab, seq_len, batch;
+  int32_t dtype;             /* GPT_DTYPE_FP32 or GPT_DTYPE_BF16                    */
+  int32_t linear_bias, ln_bias, tie_embeddings, gelu_tanh;
+  float   lr, beta1, beta2, eps, weight_decay, ln_eps;
+  int32_t wd_on_1d;
+  uint32_t wait_timeout_ms;  /* bound of every in-kernel wait; 0 = default 2000 ms  */
+  int32_t deterministic;     /* accepted for compatibility: every reduction of this
+                                library has a fixed order, so steps are always
+                                bitwise repeatable                                  */
+} gpt_config;
+
+typedef struct gpt gpt;  /* opaque handle; owns every device buffer it allocates */
+
+/* Fills *cfg with the defaults above for the 162M model (12L/768/12H, F 3072,
+ * V 50304, T 512, B 8, bf16, lr 6e-4, betas 0.9/0.95, wd 0.1). */
+void gpt_default_config(gpt_config* cfg);
+
+/* Bytes of device memory a handle with this config needs (its arena). 0 on an
+ * invalid config. */
+size_t gpt_arena_bytes(const gpt_config* cfg);
+
+/*
+ * Creates a handle on the current CUDA device.  Weights are initialised on the
+ * host from `seed` ("What ran": seeded initial weights; "Reproduce the run":
+ * initial weights generated on the CPU): matrices and embeddings N(0, 0.02)
+ * drawn from SplitMix64 + Box-Muller per the specification in the package's
+ * inputs module, biases and LayerNorm biases 0, LayerNorm gains 1; AdamW
+ * moments 0, step count 0.
+ *   cuda_stream: cudaStream_t the handle launches on (NULL = legacy default).
+ *   arena/arena_bytes: optional caller-owned device allocation of at least
+ *     gpt_arena_bytes(cfg) bytes, 256-byte aligned, that must outlive the
+ *     handle; NULL/0 = the library allocates (and frees) its own.
+ *   out: receives the handle; unchanged on failure.
+ * Errors: INVALID_ARG (bad config, NULL out, arena too small or misaligned),
+ * UNSUPPORTED, OOM, CUDA.
+ */
+int gpt_create(const gpt_config* cfg, uint64_t seed, void* cuda_stream,
+               void* arena, size_t arena_bytes, gpt** out);
+
+/*
+ * One training step: forward, backward and AdamW, as one persistent kernel
+ * launch on the handle's stream; returns after the step completed (the call
+ * synchronises the stream).
+ *   tokens, targets: DEVICE int32 [batch, seq_len], row-major, ids in
+ *     [0, vocab); targets[b,t] is the id that should follow tokens[b,t].
+ *   loss: HOST float*, receives the mean cross-entropy of this step's forward
+ *     pass (before the update).  May be NULL.
+ * Errors: INVALID_ARG (NULL tokens/targets), BAD_TOKEN, NONFINITE, TIMEOUT
+ * (handle poisoned), POISONED, CUDA.  On BAD_TOKEN (out-of-range ids are
+ * clamped for the computation) and NONFINITE the launch still runs to its
+ * end, but every AdamW task sees the flag and skips its update: parameters,
+ * moments and the step count are left as they were before the call.
+ */
+int gpt_train_step(gpt* h, const int32_t* tokens, const int32_t* targets, float* loss);
+
+/*
+ * Same step with HOST token/target buffers: the call copies them to the
+ * handle's device staging buffers on its stream, runs the step and reads the
+ * loss back.  tokens/targets: HOST int32 [batch, seq_len].
+ */
+int gpt_train_step_host(gpt* h, const int32_t* tokens, const int32_t* targets, float* loss);
+
+/* Number of parameters (length of every flat parameter-sized vector). */
+size_t gpt_num_params(const gpt* h);
+
+/* Number of tensors in the canonical order. */
+int gpt_num_tensors(const gpt* h);
+
+/*
+ * Describes tensor i of the canonical order: *name (static storage of the
+ * handle), shape[0..1] (shape[1] = 1 for vectors) and *offset (element offset
+ * in the flat vector).  Any output pointer may be NULL.  INVALID_ARG if i is
+ * out of range.
+ */
+int gpt_tensor_info(const gpt* h, int i, const char** name, int64_t shape[2], size_t* offset);
+
+/* Copies the fp32 master parameters to HOST dst[0..n), n == gpt_num_params. */
+int gpt_get_params(gpt* h, float* dst, size_t n);
+
+/* Overwrites the fp32 master parameters (and the bf16 copies the kernels read)
+ * from HOST src[0..n).  Optimizer state is unchanged. */
+int gpt_set_params(gpt* h, const float* src, size_t n);
+
+/* Copies the gradient computed by the last step (fp32, canonical order) to
+ * HOST dst[0..n). */
+int gpt_get_grads(gpt* h, float* dst, size_t n);
+
+/* AdamW state: first and second moments (HOST float[n] each, either may be
+ * NULL) and the number of updates applied so far. */
+int gpt_get_opt_state(gpt* h, float* m, float* v, int64_t* step);
+int gpt_set_opt_state(gpt* h, const float* m, const float* v, int64_t step);
+
+/*
+ * Test hook: gpt_debug_skip_release(h, k) makes the next step's task number k
+ * (ticket order) skip its completion release, so that its dependents' bounded
+ * waits expire and the step returns GPT_ERR_TIMEOUT without hanging; -1 turns
+ * it off.  After such a timeout gpt_reset() clears the poisoned state.
+ */
+int gpt_debug_skip_release(gpt* h, int64_t task_index);
+
+/* Clears counters, the ticket and the error word after a timeout; parameters
+ * and optimizer state are kept. */
+int gpt_reset(gpt* h);
+
+/* Size of the step's task graph: number of tasks, and the grid (resident
+ * blocks) the persistent kernel is launched with.  Any pointer may be NULL. */
+int gpt_graph_info(const gpt* h, int64_t* n_tasks, int32_t* grid, int32_t* block);
+
+/* Device time of the last step's kernel launch in milliseconds, from CUDA
+ * events the library records on the handle's stream around the launch. */
+int gpt_last_kernel_ms(const gpt* h, float* ms);
+
+/* Text of the handle's last error ("" if none).  h may be NULL (last create
+ * error of this thread). */
+const char* gpt_last_error(const gpt* h);
+
+/* Releases every resource of the handle.  gpt_destroy(NULL) is a no-op. */
+void gpt_destroy(gpt* h);
+
+/*
+ * 64-bit task budget of a workload that runs `iterations` rounds of
+ * `tasks_per_iteration` tasks ("A longer run exposed a scheduler overflow":
+ * the 32-bit product 4,194,304 x 2,225 wrapped).  Returns the product, or -1
+ * if it does not fit in int64.
+ */
+int64_t gpt_task_budget(int64_t iterations, int64_t tasks_per_iteration);
+
+/*
+ * Host-only: fills HOST dst[0..n) (n == the parameter count of cfg) with the
+ * seeded initial weights gpt_create(cfg, seed) would start from.  Needs no GPU.
+ */
+int gpt_init_params_host(const gpt_config* cfg, uint64_t seed, float* dst, size_t n);
+
+/* One task of the step's graph as gpt_graph_describe reports it. */
+typedef struct gpt_task_info {
+  int32_t op;            /* operation (completion counter) the task belongs to   */
+  int32_t idx;           /* index of the task within its operation               */
+  int32_t nwait;         /* number of dependencies (<= 3)                         */
+  int32_t wait_op[3];    /* operations whose counters it waits on (-1 unused)    */
+  int32_t wait_need[3];  /* per-step count each counter must reach (its tasks)   */
+} gpt_task_info;
+
+/*
+ * Host-only: builds the step's task graph for cfg (as if on a GPU with num_sms
+ * SMs; <= 0 means 148) without device memory, and reports it: *n_tasks tasks in
+ * ticket order (the first max_tasks copied to HOST tasks[], may be NULL) and
+ * *n_ops operations (type and task count of the first max_ops into HOST
+ * op_types[] / op_tasks[], may be NULL).  Operation types are the kernel's
+ * OpType values (0 embed, 1 LN forward, 2 GEMM, 3 attention forward, 4 cross-
+ * entropy, 5 loss, 6 LN backward, 7 column sum, 8 attention backward,
+ * 9 token-embedding backward, 10 position-embedding backward, 11 AdamW).
+ */
+int gpt_graph_describe(const gpt_config* cfg, int32_t num_sms, int64_t* n_tasks, int32_t* n_ops,
+                       gpt_task_info* tasks, int64_t max_tasks, int32_t* op_types, int32_t* op_tasks,
+                       int32_t max_ops);
+
+/*
+ * Test hook: one GEMM C[M,N] = sum_k A(m,k) B(n,k), fp32 output, run as a
+ * one-task graph of the same persistent kernel (SIMT fp32 path for
+ * GPT_DTYPE_FP32, tcgen05/TMA path for GPT_DTYPE_BF16).  A, B, C are DEVICE
+ * pointers; A(m,k) = A[m*lda + k] (a_mn = 0, K-major) or A[k*lda + m] (a_mn = 1,
+ * MN-major), likewise B with ldb/b_mn; C[m*ldc + n], or with ksplit > 1 split s
+ * writes its partial sum to C + s*M*ldc.  Runs on cuda_stream and synchronises.
+ * bf16 requires K % (64 ksplit) == 0, N % 64 == 0, lda and ldb multiples of 8.
+ * Errors: INVALID_ARG, UNSUPPORTED, OOM, CUDA, TIMEOUT; text via
+ * gpt_last_error(NULL).
+ */
+int gpt_test_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, int32_t a_mn,
+                  const void* B, int64_t ldb, int32_t b_mn, float* C, int64_t ldc, int32_t ksplit,
+                  void* cuda_stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GPT_H_ */

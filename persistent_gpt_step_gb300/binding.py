@@ -1,0 +1,323 @@
+"""ctypes binding of libgpt.so: the gpt.h calls with the same names, argument
+marshalling only.  Every step of the training path runs in the library's CUDA
+kernel; there is no Python or CPU fallback — if the library is missing or
+cannot be loaded this module raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import (POINTER, byref, c_char_p, c_float, c_int, c_int32, c_int64, c_size_t,
+                    c_uint32, c_uint64, c_void_p)
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libgpt.so")
+
+GPT_OK = 0
+ERRORS = {
+    -1: "INVALID_ARG", -2: "CUDA", -3: "OOM", -4: "TIMEOUT", -5: "NONFINITE",
+    -6: "BAD_TOKEN", -7: "POISONED", -8: "UNSUPPORTED",
+}
+DTYPE_FP32, DTYPE_BF16 = 0, 1
+
+
+class GptError(RuntimeError):
+    """A negative status of a gpt_* call; ``code`` is the GPT_ERR_* value."""
+
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"GPT_ERR_{ERRORS.get(code, code)}: {msg}")
+        self.code = code
+        self.name = ERRORS.get(code, str(code))
+
+
+class gpt_config(ctypes.Structure):
+    _fields_ = [
+        ("n_layer", c_int32), ("d_model", c_int32), ("n_head", c_int32), ("d_mlp", c_int32),
+        ("vocab", c_int32), ("seq_len", c_int32), ("batch", c_int32),
+        ("dtype", c_int32),
+        ("linear_bias", c_int32), ("ln_bias", c_int32), ("tie_embeddings", c_int32),
+        ("gelu_tanh", c_int32),
+        ("lr", c_float), ("beta1", c_float), ("beta2", c_float), ("eps", c_float),
+        ("weight_decay", c_float), ("ln_eps", c_float),
+        ("wd_on_1d", c_int32), ("wait_timeout_ms", c_uint32), ("deterministic", c_int32),
+    ]
+
+
+class gpt_task_info(ctypes.Structure):
+    _fields_ = [("op", c_int32), ("idx", c_int32), ("nwait", c_int32),
+                ("wait_op", c_int32 * 3), ("wait_need", c_int32 * 3)]
+
+
+_lib = None
+
+# (name, restype, argtypes) of every function gpt.h declares
+SIGNATURES = [
+    ("gpt_default_config", None, [POINTER(gpt_config)]),
+    ("gpt_arena_bytes", c_size_t, [POINTER(gpt_config)]),
+    ("gpt_create", c_int, [POINTER(gpt_config), c_uint64, c_void_p, c_void_p, c_size_t, POINTER(c_void_p)]),
+    ("gpt_train_step", c_int, [c_void_p, c_void_p, c_void_p, POINTER(c_float)]),
+    ("gpt_train_step_host", c_int, [c_void_p, c_void_p, c_void_p, POINTER(c_float)]),
+    ("gpt_num_params", c_size_t, [c_void_p]),
+    ("gpt_num_tensors", c_int, [c_void_p]),
+    ("gpt_tensor_info", c_int, [c_void_p, c_int, POINTER(c_char_p), POINTER(c_int64), POINTER(c_size_t)]),
+    ("gpt_get_params", c_int, [c_void_p, c_void_p, c_size_t]),
+    ("gpt_set_params", c_int, [c_void_p, c_void_p, c_size_t]),
+    ("gpt_get_grads", c_int, [c_void_p, c_void_p, c_size_t]),
+    ("gpt_get_opt_state", c_int, [c_void_p, c_void_p, c_void_p, POINTER(c_int64)]),
+    ("gpt_set_opt_state", c_int, [c_void_p, c_void_p, c_void_p, c_int64]),
+    ("gpt_debug_skip_release", c_int, [c_void_p, c_int64]),
+    ("gpt_reset", c_int, [c_void_p]),
+    ("gpt_graph_info", c_int, [c_void_p, POINTER(c_int64), POINTER(c_int32), POINTER(c_int32)]),
+    ("gpt_last_kernel_ms", c_int, [c_void_p, POINTER(c_float)]),
+    ("gpt_last_error", c_char_p, [c_void_p]),
+    ("gpt_destroy", None, [c_void_p]),
+    ("gpt_task_budget", c_int64, [c_int64, c_int64]),
+    ("gpt_init_params_host", c_int, [POINTER(gpt_config), c_uint64, c_void_p, c_size_t]),
+    ("gpt_graph_describe", c_int, [POINTER(gpt_config), c_int32, POINTER(c_int64), POINTER(c_int32),
+                                   POINTER(gpt_task_info), c_int64, POINTER(c_int32), POINTER(c_int32),
+                                   c_int32]),
+    ("gpt_test_gemm", c_int, [c_int32, c_int32, c_int32, c_int32, c_void_p, c_int64, c_int32,
+                              c_void_p, c_int64, c_int32, c_void_p, c_int64, c_int32, c_void_p]),
+]
+
+
+def load(path: str = LIB_PATH):
+    """Loads libgpt.so (built in-tree by build.py); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           "`python -m persistent_gpt_step_gb300.build` (no fallback exists)")
+    lib = ctypes.CDLL(path)
+    for name, res, args in SIGNATURES:
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def make_config(cfg, wait_timeout_ms: int = 2000) -> gpt_config:
+    """gpt_config from a workload definition (inputs.GPTConfig or any object
+    with the same attribute names)."""
+    c = gpt_config()
+    load().gpt_default_config(byref(c))
+    for f in ("n_layer", "d_model", "n_head", "d_mlp", "vocab", "seq_len", "batch"):
+        setattr(c, f, int(getattr(cfg, f)))
+    c.dtype = DTYPE_FP32 if getattr(cfg, "dtype", "bf16") == "fp32" else DTYPE_BF16
+    c.linear_bias = int(bool(getattr(cfg, "linear_bias", True)))
+    c.ln_bias = int(bool(getattr(cfg, "ln_bias", True)))
+    c.gelu_tanh = int(bool(getattr(cfg, "gelu_tanh", True)))
+    for f in ("lr", "beta1", "beta2", "eps", "weight_decay", "ln_eps"):
+        if hasattr(cfg, f):
+            setattr(c, f, float(getattr(cfg, f)))
+    c.wd_on_1d = int(bool(getattr(cfg, "wd_on_1d", False)))
+    c.wait_timeout_ms = int(wait_timeout_ms)
+    return c
+
+
+def _ptr(t) -> int:
+    """Address of a torch tensor or numpy array."""
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+class GPT:
+    """One handle of the library: a GPT model with its optimizer state on the GPU.
+
+    ``cfg`` is a workload definition (see ``inputs.CONFIGS``).  The device arena
+    is a torch allocation (PyTorch supplies device memory and the stream); every
+    computation runs in the library's persistent kernel.
+    """
+
+    def __init__(self, cfg, seed: int = 1234, stream=None, wait_timeout_ms: int = 2000,
+                 torch_arena: bool = True):
+        import torch
+        lib = load()
+        self.cfg = cfg
+        self._c = make_config(cfg, wait_timeout_ms)
+        self._torch = torch
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        nbytes = lib.gpt_arena_bytes(byref(self._c))
+        if nbytes == 0:
+            raise GptError(-1, "invalid or unsupported config")
+        self._arena = torch.empty(nbytes, dtype=torch.uint8, device="cuda") if torch_arena else None
+        h = c_void_p()
+        rc = lib.gpt_create(byref(self._c), c_uint64(seed), c_void_p(self.stream.cuda_stream),
+                            c_void_p(self._arena.data_ptr() if torch_arena else 0),
+                            c_size_t(nbytes if torch_arena else 0), byref(h))
+        if rc != GPT_OK:
+            raise GptError(rc, lib.gpt_last_error(None).decode())
+        self._h = h
+        self._lib = lib
+        self.n_params = int(lib.gpt_num_params(h))
+
+    # -- helpers ------------------------------------------------------------
+    def _check(self, rc):
+        if rc != GPT_OK:
+            raise GptError(rc, self._lib.gpt_last_error(self._h).decode())
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.gpt_destroy(self._h)
+            self._h = None
+            self._arena = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    # -- the step -------------------------------------------------------------
+    def train_step(self, tokens, targets) -> float:
+        """One training step; returns the pre-update mean loss.
+
+        tokens, targets: int32 [batch, seq_len]; CUDA tensors are passed as
+        device pointers, numpy arrays / CPU tensors go through the host entry
+        point (copied to the device by the library on its stream).
+        """
+        loss = c_float()
+        is_dev = hasattr(tokens, "is_cuda") and tokens.is_cuda
+        if is_dev:
+            assert tokens.dtype == self._torch.int32 and targets.dtype == self._torch.int32
+            assert tokens.is_contiguous() and targets.is_contiguous()
+            rc = self._lib.gpt_train_step(self._h, c_void_p(tokens.data_ptr()),
+                                          c_void_p(targets.data_ptr()), byref(loss))
+        else:
+            tok = tokens.numpy() if hasattr(tokens, "numpy") else tokens
+            tgt = targets.numpy() if hasattr(targets, "numpy") else targets
+            tok = np.ascontiguousarray(tok, dtype=np.int32)
+            tgt = np.ascontiguousarray(tgt, dtype=np.int32)
+            rc = self._lib.gpt_train_step_host(self._h, c_void_p(tok.ctypes.data),
+                                               c_void_p(tgt.ctypes.data), byref(loss))
+        self._check(rc)
+        return float(loss.value)
+
+    # -- state ----------------------------------------------------------------
+    def params(self) -> np.ndarray:
+        out = np.empty(self.n_params, np.float32)
+        self._check(self._lib.gpt_get_params(self._h, c_void_p(out.ctypes.data), self.n_params))
+        return out
+
+    def set_params(self, p: np.ndarray):
+        p = np.ascontiguousarray(p, dtype=np.float32)
+        assert p.size == self.n_params
+        self._check(self._lib.gpt_set_params(self._h, c_void_p(p.ctypes.data), self.n_params))
+
+    def grads(self) -> np.ndarray:
+        out = np.empty(self.n_params, np.float32)
+        self._check(self._lib.gpt_get_grads(self._h, c_void_p(out.ctypes.data), self.n_params))
+        return out
+
+    def opt_state(self):
+        m = np.empty(self.n_params, np.float32)
+        v = np.empty(self.n_params, np.float32)
+        step = c_int64()
+        self._check(self._lib.gpt_get_opt_state(self._h, c_void_p(m.ctypes.data),
+                                                c_void_p(v.ctypes.data), byref(step)))
+        return m, v, int(step.value)
+
+    def set_opt_state(self, m, v, step: int):
+        m = np.ascontiguousarray(m, dtype=np.float32)
+        v = np.ascontiguousarray(v, dtype=np.float32)
+        self._check(self._lib.gpt_set_opt_state(self._h, c_void_p(m.ctypes.data),
+                                                c_void_p(v.ctypes.data), c_int64(step)))
+
+    def tensor_table(self):
+        """[(name, shape, offset)] in canonical order."""
+        out = []
+        name = c_char_p()
+        shape = (c_int64 * 2)()
+        off = c_size_t()
+        for i in range(self._lib.gpt_num_tensors(self._h)):
+            self._check(self._lib.gpt_tensor_info(self._h, i, byref(name), shape, byref(off)))
+            shp = (int(shape[0]),) if int(shape[1]) == 1 and not self._is_matrix(name.value) \
+                else (int(shape[0]), int(shape[1]))
+            out.append((name.value.decode(), shp, int(off.value)))
+        return out
+
+    @staticmethod
+    def _is_matrix(name: bytes) -> bool:
+        n = name.decode()
+        return n in ("wte", "wpe", "w_lm") or n.split(".")[-1].startswith("w_")
+
+    def graph_info(self):
+        n = c_int64()
+        g = c_int32()
+        b = c_int32()
+        self._check(self._lib.gpt_graph_info(self._h, byref(n), byref(g), byref(b)))
+        return int(n.value), int(g.value), int(b.value)
+
+    def last_kernel_ms(self) -> float:
+        ms = c_float()
+        self._check(self._lib.gpt_last_kernel_ms(self._h, byref(ms)))
+        return float(ms.value)
+
+    def debug_skip_release(self, task_index: int):
+        self._check(self._lib.gpt_debug_skip_release(self._h, c_int64(task_index)))
+
+    def reset(self):
+        self._check(self._lib.gpt_reset(self._h))
+
+
+def task_budget(iterations: int, tasks_per_iteration: int) -> int:
+    return int(load().gpt_task_budget(c_int64(iterations), c_int64(tasks_per_iteration)))
+
+
+def test_gemm(A, B, a_mn: bool, b_mn: bool, M: int, N: int, K: int, ksplit: int = 1, stream=None):
+    """Runs gpt_test_gemm on torch CUDA tensors; returns C (fp32 [ksplit, M, N])."""
+    import torch
+    lib = load()
+    dtype = DTYPE_BF16 if A.dtype == torch.bfloat16 else DTYPE_FP32
+    C = torch.full((ksplit, M, N), float("nan"), dtype=torch.float32, device=A.device)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    rc = lib.gpt_test_gemm(dtype, M, N, K, c_void_p(A.data_ptr()), A.stride(0), int(a_mn),
+                           c_void_p(B.data_ptr()), B.stride(0), int(b_mn), c_void_p(C.data_ptr()), N,
+                           ksplit, c_void_p(s.cuda_stream))
+    if rc != GPT_OK:
+        raise GptError(rc, lib.gpt_last_error(None).decode())
+    return C
+
+
+def init_params_host(cfg, seed: int, n: int) -> np.ndarray:
+    """The library's own (C++) seeded initial weights; no GPU needed."""
+    lib = load()
+    out = np.empty(n, np.float32)
+    c = make_config(cfg)
+    rc = lib.gpt_init_params_host(byref(c), c_uint64(seed), c_void_p(out.ctypes.data), n)
+    if rc != GPT_OK:
+        raise GptError(rc, lib.gpt_last_error(None).decode())
+    return out
+
+
+def describe_graph(cfg, num_sms: int = 148):
+    """(tasks, op_types, op_tasks) of the step's task graph, built on the host.
+
+    tasks: list of (op, idx, [(wait_op, need), ...]) in ticket order."""
+    lib = load()
+    c = make_config(cfg)
+    nt, no = c_int64(), c_int32()
+    rc = lib.gpt_graph_describe(byref(c), num_sms, byref(nt), byref(no), None, 0, None, None, 0)
+    if rc != GPT_OK:
+        raise GptError(rc, lib.gpt_last_error(None).decode())
+    tasks = (gpt_task_info * nt.value)()
+    types = (c_int32 * no.value)()
+    ntk = (c_int32 * no.value)()
+    rc = lib.gpt_graph_describe(byref(c), num_sms, byref(nt), byref(no), tasks, nt.value, types, ntk,
+                                no.value)
+    if rc != GPT_OK:
+        raise GptError(rc, lib.gpt_last_error(None).decode())
+    out = [(t.op, t.idx, [(t.wait_op[w], t.wait_need[w]) for w in range(t.nwait)]) for t in tasks]
+    return out, list(types), list(ntk)

@@ -1,0 +1,116 @@
+// device.cuh — device primitives of the persistent kernel: memory-ordering
+// operations on the completion counters, bounded waits, error reporting and
+// element conversions.
+#pragma once
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "graph.h"
+
+namespace pgs {
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_add_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
+  return *(volatile const uint32_t*)p;
+}
+
+// Orders this thread's generic-proxy global accesses with later async-proxy
+// (TMA) accesses: used by producers after their stores and by consumers after
+// their acquire, before tensor-core operand loads of data other blocks wrote.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void set_fatal(const KParams& kp, uint32_t code, uint32_t task,
+                                          uint32_t ctr) {
+  if (atomicCAS(&kp.err[0], 0u, code) == 0u) {
+    kp.err[2] = task;
+    kp.err[3] = ctr;
+  }
+}
+
+__device__ __forceinline__ void set_soft(const KParams& kp, uint32_t bits) {
+  atomicOr(&kp.err[1], bits);
+}
+
+// Spins (one thread) until counters[ctr] >= target.  Gives up after the
+// handle's timeout (globaltimer) or an iteration cap, whichever comes first,
+// recording a fatal error; also gives up when another block recorded one.
+__device__ __forceinline__ bool wait_counter(const KParams& kp, int32_t ctr,
+                                             unsigned long long target, uint32_t task) {
+  const unsigned long long* p = kp.counters + ctr;
+  if (ld_acquire_u64(p) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  // ~30 ns minimum per iteration (acquire load + sleep) bounds the count too.
+  const uint64_t max_iters = kp.timeout_ns / 30 + 1024;
+  uint32_t sleep = 32;
+  for (uint64_t it = 0; it < max_iters; ++it) {
+    __nanosleep(sleep);
+    if (sleep < 256) sleep <<= 1;
+    if (ld_acquire_u64(p) >= target) return true;
+    if ((it & 15) == 15) {
+      if (ld_volatile_u32(&kp.err[0]) != 0u) return false;
+      if (globaltimer_ns() - t0 > kp.timeout_ns) break;
+    }
+  }
+  set_fatal(kp, kFatalTimeout, task, (uint32_t)ctr);
+  return false;
+}
+
+// ---- element conversions (act_t = float or __nv_bfloat16) -------------------
+template <typename T> __device__ __forceinline__ float to_f(T v);
+template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) {
+  return __bfloat162float(v);
+}
+template <typename T> __device__ __forceinline__ T from_f(float v);
+template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// GELU, tanh form 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) or erf form.
+__device__ __forceinline__ float gelu_f(float x, bool tanh_form) {
+  if (tanh_form) {
+    const float k0 = 0.7978845608028654f;
+    return 0.5f * x * (1.0f + tanhf(k0 * (x + 0.044715f * x * x * x)));
+  }
+  return 0.5f * x * (1.0f + erff(x * 0.7071067811865476f));
+}
+__device__ __forceinline__ float gelu_grad_f(float x, bool tanh_form) {
+  if (tanh_form) {
+    const float k0 = 0.7978845608028654f;
+    float t = tanhf(k0 * (x + 0.044715f * x * x * x));
+    return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * k0 * (1.0f + 3.0f * 0.044715f * x * x);
+  }
+  return 0.5f * (1.0f + erff(x * 0.7071067811865476f)) +
+         x * expf(-0.5f * x * x) * 0.3989422804014327f;
+}
+
+}  // namespace pgs

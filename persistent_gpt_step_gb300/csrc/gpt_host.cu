@@ -1,0 +1,1144 @@
+// gpt_host.cu — host side of libgpt.so: configuration, parameter table, the
+// device arena, seeded initialisation, the task-graph builder, TMA tensor maps,
+// the per-step launch of the persistent kernel and the C ABI of gpt.h.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "../../include/gpt.h"
+#include "graph.h"
+#include "launch.h"
+
+using namespace pgs;
+
+namespace {
+
+thread_local std::string g_create_error;
+
+// ----------------------------------------------------------------------------
+// Seeded initial weights: SplitMix64 (Steele, Lea, Flood 2014) + Box-Muller.
+// Specification (shared with the test-side generator, implemented twice):
+//   out(s, n) = mix(s + (n + 1) * 0x9E3779B97F4A7C15); key_t = out(seed, t);
+//   u1 = (out(key_t, 2e) >> 11) 2^-53, u2 = (out(key_t, 2e+1) >> 11) 2^-53;
+//   w = fp32(0.02 * sqrt(-2 ln(1 - u1)) cos(2 pi u2)).
+// ----------------------------------------------------------------------------
+inline uint64_t sm64_mix(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+  return z ^ (z >> 31);
+}
+inline uint64_t sm64_out(uint64_t state, uint64_t n) {
+  return sm64_mix(state + (n + 1) * 0x9E3779B97F4A7C15ULL);
+}
+void normal_fill(float* dst, size_t n, uint64_t seed, uint64_t tensor_index) {
+  const uint64_t key = sm64_out(seed, tensor_index);
+  const double two_pi = 2.0 * 3.141592653589793;
+  auto work = [&](size_t lo, size_t hi) {
+    for (size_t e = lo; e < hi; ++e) {
+      const double u1 = (double)(sm64_out(key, 2 * e) >> 11) * 0x1p-53;
+      const double u2 = (double)(sm64_out(key, 2 * e + 1) >> 11) * 0x1p-53;
+      const double z = std::sqrt(-2.0 * std::log(1.0 - u1)) * std::cos(two_pi * u2);
+      dst[e] = (float)(0.02 * z);
+    }
+  };
+  const size_t nth = n < (1u << 16) ? 1 : std::max(1u, std::min(32u, std::thread::hardware_concurrency()));
+  if (nth == 1) { work(0, n); return; }
+  std::vector<std::thread> th;
+  for (size_t i = 0; i < nth; ++i) th.emplace_back(work, n * i / nth, n * (i + 1) / nth);
+  for (auto& t : th) t.join();
+}
+
+inline uint16_t f32_to_bf16_rne(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x40);  // NaN stays NaN
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+// ----------------------------------------------------------------------------
+// Parameter table (canonical order, see gpt.h)
+// ----------------------------------------------------------------------------
+enum InitKind { INIT_NORMAL, INIT_ZEROS, INIT_ONES };
+struct TensorInfo {
+  std::string name;
+  int64_t rows, cols;  // cols = 1 for vectors
+  int ndim;
+  size_t offset;
+  InitKind init;
+};
+
+struct TensorIds {  // indices into the table, per layer
+  int ln1_g, ln1_b, w_qkv, b_qkv, w_o, b_o, ln2_g, ln2_b, w_1, b_1, w_2, b_2;
+};
+
+struct Dims {
+  int L, C, H, d, F, V, T, B, N;
+};
+
+}  // namespace
+
+// ----------------------------------------------------------------------------
+// The handle
+// ----------------------------------------------------------------------------
+struct gpt {
+  gpt_config cfg;
+  Dims D;
+  int device = 0, num_sms = 0;
+  cudaStream_t stream = nullptr;
+  std::vector<TensorInfo> tensors;
+  std::vector<TensorIds> lid;
+  int t_wte = 0, t_wpe = 0, t_lnf_g = 0, t_lnf_b = -1, t_wlm = 0;
+  size_t nparams = 0;
+
+  // device memory
+  uint8_t* arena = nullptr;
+  size_t arena_bytes = 0;
+  bool own_arena = false;
+  uint8_t* meta = nullptr;  // tasks, ops, tensor maps, counters, error words, staging
+  size_t meta_bytes = 0;
+
+  // arena views
+  float *params = nullptr, *grads = nullptr, *m = nullptr, *v = nullptr;
+  uint16_t* shadow = nullptr;
+  float* loss_dev = nullptr;
+
+  // graph
+  std::vector<OpDesc> ops;
+  std::vector<TaskDesc> tasks;
+  std::vector<std::vector<uint8_t>> tmaps;  // 128-byte CUtensorMaps
+  TaskDesc* d_tasks = nullptr;
+  OpDesc* d_ops = nullptr;
+  void* d_tmaps = nullptr;
+  unsigned long long* d_counters = nullptr;
+  unsigned long long* d_ticket = nullptr;
+  uint32_t* d_err = nullptr;
+  int32_t* d_tok_stage = nullptr;
+
+  // launch
+  const void* kernel = nullptr;
+  int grid = 0;
+  size_t smem_bytes = 0;
+  uint64_t launches = 0;     // completed launches since the last reset
+  int64_t opt_step = 0;      // AdamW updates applied
+  int64_t skip_release = -1;
+  bool poisoned = false;
+  bool describe_only = false;  // build the graph without device memory or tensor maps
+
+  cudaEvent_t ev0 = nullptr, ev1 = nullptr;  // bracket the kernel of the last step
+  float last_kernel_ms = 0.f;
+  // host staging (pinned) for the per-step status
+  struct Status { uint32_t err[4]; float loss; uint32_t pad[3]; };
+  Status* h_status = nullptr;
+  std::string err;
+};
+
+namespace {
+
+int fail(gpt* h, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (h) h->err = buf; else g_create_error = buf;
+  return code;
+}
+
+#define CUDA_TRY(h, call)                                                                    \
+  do {                                                                                       \
+    cudaError_t e_ = (call);                                                                 \
+    if (e_ != cudaSuccess)                                                                   \
+      return fail((h), GPT_ERR_CUDA, "%s failed: %s", #call, cudaGetErrorString(e_));        \
+  } while (0)
+
+bool is_bf16(const gpt_config& c) { return c.dtype == GPT_DTYPE_BF16; }
+
+int validate(const gpt_config& c, std::string* why) {
+  auto bad = [&](const char* s) { *why = s; return GPT_ERR_INVALID_ARG; };
+  if (c.n_layer < 1 || c.d_model < 1 || c.n_head < 1 || c.d_mlp < 1 || c.vocab < 2 || c.seq_len < 1 ||
+      c.batch < 1)
+    return bad("every size must be positive (vocab >= 2)");
+  if (c.dtype != GPT_DTYPE_FP32 && c.dtype != GPT_DTYPE_BF16) return bad("dtype must be 0 (fp32) or 1 (bf16)");
+  if (c.tie_embeddings) { *why = "tied embeddings are not supported"; return GPT_ERR_UNSUPPORTED; }
+  if (c.d_model % c.n_head) return bad("d_model must be a multiple of n_head");
+  const int hd = c.d_model / c.n_head;
+  if (c.d_model % 64 || c.d_model > 1024) { *why = "d_model must be a multiple of 64 and <= 1024"; return GPT_ERR_UNSUPPORTED; }
+  if (c.d_mlp % 64) { *why = "d_mlp must be a multiple of 64"; return GPT_ERR_UNSUPPORTED; }
+  if (hd > 128) { *why = "head_dim must be <= 128"; return GPT_ERR_UNSUPPORTED; }
+  if (c.seq_len > 1024) { *why = "seq_len must be <= 1024"; return GPT_ERR_UNSUPPORTED; }
+  if ((int64_t)c.batch * c.seq_len > 8192) { *why = "batch * seq_len must be <= 8192"; return GPT_ERR_UNSUPPORTED; }
+  if (is_bf16(c)) {
+    if (((int64_t)c.batch * c.seq_len) % 128) { *why = "bf16: batch * seq_len must be a multiple of 128"; return GPT_ERR_UNSUPPORTED; }
+    if (c.vocab % 64) { *why = "bf16: vocab must be a multiple of 64"; return GPT_ERR_UNSUPPORTED; }
+  }
+  if (!(c.lr >= 0.f) || !(c.beta1 >= 0.f && c.beta1 < 1.f) || !(c.beta2 >= 0.f && c.beta2 < 1.f) ||
+      !(c.eps > 0.f) || !(c.ln_eps > 0.f) || !(c.weight_decay >= 0.f))
+    return bad("bad optimizer / LayerNorm constants");
+  return GPT_OK;
+}
+
+void build_table(gpt* h) {
+  const gpt_config& c = h->cfg;
+  const int64_t C = c.d_model, F = c.d_mlp, V = c.vocab, T = c.seq_len;
+  auto add = [&](const std::string& name, int64_t r, int64_t cc, int nd, InitKind k) {
+    TensorInfo t{name, r, cc, nd, h->nparams, k};
+    h->nparams += (size_t)(r * cc);
+    h->tensors.push_back(t);
+    return (int)h->tensors.size() - 1;
+  };
+  h->t_wte = add("wte", V, C, 2, INIT_NORMAL);
+  h->t_wpe = add("wpe", T, C, 2, INIT_NORMAL);
+  for (int l = 0; l < c.n_layer; ++l) {
+    const std::string p = "h" + std::to_string(l) + ".";
+    TensorIds id{};
+    id.ln1_g = add(p + "ln1_g", C, 1, 1, INIT_ONES);
+    id.ln1_b = c.ln_bias ? add(p + "ln1_b", C, 1, 1, INIT_ZEROS) : -1;
+    id.w_qkv = add(p + "w_qkv", 3 * C, C, 2, INIT_NORMAL);
+    id.b_qkv = c.linear_bias ? add(p + "b_qkv", 3 * C, 1, 1, INIT_ZEROS) : -1;
+    id.w_o = add(p + "w_o", C, C, 2, INIT_NORMAL);
+    id.b_o = c.linear_bias ? add(p + "b_o", C, 1, 1, INIT_ZEROS) : -1;
+    id.ln2_g = add(p + "ln2_g", C, 1, 1, INIT_ONES);
+    id.ln2_b = c.ln_bias ? add(p + "ln2_b", C, 1, 1, INIT_ZEROS) : -1;
+    id.w_1 = add(p + "w_1", F, C, 2, INIT_NORMAL);
+    id.b_1 = c.linear_bias ? add(p + "b_1", F, 1, 1, INIT_ZEROS) : -1;
+    id.w_2 = add(p + "w_2", C, F, 2, INIT_NORMAL);
+    id.b_2 = c.linear_bias ? add(p + "b_2", C, 1, 1, INIT_ZEROS) : -1;
+    h->lid.push_back(id);
+  }
+  h->t_lnf_g = add("lnf_g", C, 1, 1, INIT_ONES);
+  h->t_lnf_b = c.ln_bias ? add("lnf_b", C, 1, 1, INIT_ZEROS) : -1;
+  h->t_wlm = add("w_lm", V, C, 2, INIT_NORMAL);
+}
+
+// ----------------------------------------------------------------------------
+// Arena layout: every buffer 256-byte aligned.  Per-layer activations are kept
+// for the backward pass; every buffer has a single writer per step.
+// ----------------------------------------------------------------------------
+struct Bump {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    off = (off + 255) & ~(size_t)255;
+    size_t r = off;
+    off += bytes;
+    return r;
+  }
+};
+
+struct Layout {
+  size_t params, grads, m, v, shadow;
+  std::vector<size_t> x, xm, ln1, ln1_mu, ln1_rs, qkv, atto, lse, ln2, ln2_mu, ln2_rs, hpre, gact;
+  size_t lnf, lnf_mu, lnf_rs, logits, row_loss, loss;
+  size_t daf;
+  std::vector<size_t> dx, dx_act, dxm, dxm_act, dh, da2, dO, dqkv, da1, att_scr;
+  std::vector<size_t> ln1_gp, ln1_bp, ln2_gp, ln2_bp;
+  size_t lnf_gp, lnf_bp;
+  size_t total;
+};
+
+constexpr int kRowsLn = 32;       // rows per LayerNorm task
+constexpr int kRowsCe = 8;        // rows per cross-entropy task
+constexpr int kRowsEmb = 32;      // rows per embedding task
+constexpr int kVocabRows = 64;    // vocabulary rows per embedding-backward task
+constexpr int kColsColsum = 64;   // columns per column-sum task
+constexpr int64_t kAdamChunk = 65536;
+
+int ln_tasks(int N) { return (N + kRowsLn - 1) / kRowsLn; }
+
+Layout make_layout(const gpt_config& c, size_t nparams, int lm_ksplit) {
+  Layout Lo;
+  Bump b;
+  const size_t N = (size_t)c.batch * c.seq_len, C = c.d_model, F = c.d_mlp, V = c.vocab;
+  const size_t act = is_bf16(c) ? 2 : 4;
+  const int L = c.n_layer;
+  const size_t BHT = (size_t)c.batch * c.n_head * c.seq_len;
+  const size_t nrb = ln_tasks((int)N);
+  Lo.params = b.take(nparams * 4);
+  Lo.grads = b.take(nparams * 4);
+  Lo.m = b.take(nparams * 4);
+  Lo.v = b.take(nparams * 4);
+  Lo.shadow = is_bf16(c) ? b.take(nparams * 2) : 0;
+  for (int l = 0; l <= L; ++l) Lo.x.push_back(b.take(N * C * 4));
+  for (int l = 0; l < L; ++l) {
+    Lo.xm.push_back(b.take(N * C * 4));
+    Lo.ln1.push_back(b.take(N * C * act));
+    Lo.ln1_mu.push_back(b.take(N * 4));
+    Lo.ln1_rs.push_back(b.take(N * 4));
+    Lo.qkv.push_back(b.take(N * 3 * C * act));
+    Lo.atto.push_back(b.take(N * C * act));
+    Lo.lse.push_back(b.take(BHT * 4));
+    Lo.ln2.push_back(b.take(N * C * act));
+    Lo.ln2_mu.push_back(b.take(N * 4));
+    Lo.ln2_rs.push_back(b.take(N * 4));
+    Lo.hpre.push_back(b.take(N * F * act));
+    Lo.gact.push_back(b.take(N * F * act));
+  }
+  Lo.lnf = b.take(N * C * act);
+  Lo.lnf_mu = b.take(N * 4);
+  Lo.lnf_rs = b.take(N * 4);
+  Lo.logits = b.take(N * V * act);
+  Lo.row_loss = b.take(N * 4);
+  Lo.loss = b.take(256);
+  Lo.daf = b.take((size_t)lm_ksplit * N * C * 4);
+  for (int l = 0; l <= L; ++l) {
+    Lo.dx.push_back(b.take(N * C * 4));
+    Lo.dx_act.push_back(b.take(N * C * act));
+  }
+  for (int l = 0; l < L; ++l) {
+    Lo.dxm.push_back(b.take(N * C * 4));
+    Lo.dxm_act.push_back(b.take(N * C * act));
+    Lo.dh.push_back(b.take(N * F * act));
+    Lo.da2.push_back(b.take(N * C * 4));
+    Lo.dO.push_back(b.take(N * C * act));
+    Lo.dqkv.push_back(b.take(N * 3 * C * act));
+    Lo.da1.push_back(b.take(N * C * 4));
+    Lo.att_scr.push_back(b.take((size_t)c.batch * c.n_head * 2 * c.seq_len * (C / c.n_head) * 4));
+    Lo.ln1_gp.push_back(b.take(nrb * C * 4));
+    Lo.ln1_bp.push_back(b.take(nrb * C * 4));
+    Lo.ln2_gp.push_back(b.take(nrb * C * 4));
+    Lo.ln2_bp.push_back(b.take(nrb * C * 4));
+  }
+  Lo.lnf_gp = b.take(nrb * C * 4);
+  Lo.lnf_bp = b.take(nrb * C * 4);
+  Lo.total = (b.off + 255) & ~(size_t)255;
+  return Lo;
+}
+
+// ----------------------------------------------------------------------------
+// TMA tensor maps (driver entry point fetched through the runtime)
+// ----------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)p;
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor [outer][inner] (row pitch ld elements); box = 64 x box_outer, 128-byte swizzle.
+int make_tmap(gpt* h, const void* base, int64_t inner, int64_t outer, int64_t ld, int box_outer) {
+  if (h->describe_only) {
+    h->tmaps.push_back(std::vector<uint8_t>(128, 0));
+    return (int)h->tmaps.size() - 1;
+  }
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return -1;
+  std::vector<uint8_t> buf(128, 0);
+  CUtensorMap* m = reinterpret_cast<CUtensorMap*>(buf.data());
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return -1;
+  h->tmaps.push_back(buf);
+  return (int)h->tmaps.size() - 1;
+}
+
+// ----------------------------------------------------------------------------
+// Graph builder
+// ----------------------------------------------------------------------------
+struct Builder {
+  gpt* h;
+  int add(const OpDesc& op, std::initializer_list<int> deps) {
+    const int id = (int)h->ops.size();
+    h->ops.push_back(op);
+    int dl[kMaxWaits], nd = 0;
+    for (int d : deps) {
+      if (d < 0) continue;
+      bool dup = false;
+      for (int i = 0; i < nd; ++i) dup |= dl[i] == d;
+      if (!dup) dl[nd++] = d;
+    }
+    for (int i = 0; i < op.ntasks; ++i) {
+      TaskDesc t{};
+      t.op = id;
+      t.idx = i;
+      t.nwait = nd;
+      for (int w = 0; w < nd; ++w) {
+        t.wait_ctr[w] = dl[w];
+        t.wait_need[w] = (uint32_t)h->ops[dl[w]].ntasks;
+      }
+      h->tasks.push_back(t);
+    }
+    return id;
+  }
+};
+
+// One GEMM operand: element (mn, k) of a row-major 2-D tensor with row pitch ld;
+// K-major = stored [mn][k], MN-major = stored [k][mn].
+struct Operand {
+  const void* p;
+  int64_t ld;
+  bool mn_major;
+};
+
+int pick_bn(int M, int N, int num_sms) {
+  // prefer wide tiles, but not at the price of badly filled waves
+  const int tm = (M + kTcBM - 1) / kTcBM;
+  int best = 64;
+  double best_eff = -1;
+  for (int bn : {256, 128, 64}) {
+    if (N % 64) continue;
+    const int tiles = tm * ((N + bn - 1) / bn);
+    const int waves = (tiles + num_sms - 1) / num_sms;
+    double eff = (double)tiles / ((double)waves * num_sms) * (bn == 256 ? 1.0 : bn == 128 ? 0.92 : 0.75);
+    eff *= (double)N / ((double)((N + bn - 1) / bn) * bn);  // ragged last tile
+    if (eff > best_eff + 1e-9) { best_eff = eff; best = bn; }
+  }
+  return best;
+}
+
+int gemm_op(gpt* h, OpDesc* op, int M, int N, int K, Operand A, Operand B, int epi, int ksplit) {
+  GemmArgs& g = op->gemm;
+  std::memset(op, 0, sizeof(OpDesc));
+  op->type = OP_GEMM;
+  g.M = M; g.N = N; g.K = K;
+  g.A = A.p; g.B = B.p;
+  g.sam = A.mn_major ? 1 : A.ld; g.sak = A.mn_major ? A.ld : 1;
+  g.sbn = B.mn_major ? 1 : B.ld; g.sbk = B.mn_major ? B.ld : 1;
+  g.a_mn = A.mn_major; g.b_mn = B.mn_major;
+  g.epi = epi;
+  g.ksplit = ksplit;
+  g.a_map = g.b_map = -1;
+  if (is_bf16(h->cfg)) {
+    g.BM = kTcBM;
+    g.BN = pick_bn(M, N, h->num_sms);
+    g.BK = kTcBK;
+    g.a_map = A.mn_major ? make_tmap(h, A.p, M, K, A.ld, 64) : make_tmap(h, A.p, K, M, A.ld, kTcBM);
+    g.b_map = B.mn_major ? make_tmap(h, B.p, N, K, B.ld, 64) : make_tmap(h, B.p, K, N, B.ld, g.BN);
+    if (g.a_map < 0 || g.b_map < 0) return fail(h, GPT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  } else {
+    g.BM = kSimtTile; g.BN = kSimtTile; g.BK = 16;
+  }
+  g.tiles_n = (N + g.BN - 1) / g.BN;
+  const int tiles_m = (M + g.BM - 1) / g.BM;
+  op->ntasks = tiles_m * g.tiles_n * ksplit;
+  return GPT_OK;
+}
+
+OpDesc blank(int type, int ntasks) {
+  OpDesc o;
+  std::memset(&o, 0, sizeof o);
+  o.type = type;
+  o.ntasks = ntasks;
+  return o;
+}
+
+int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
+  const gpt_config& c = h->cfg;
+  const Dims& D = h->D;
+  uint8_t* A = h->arena;
+  auto F32 = [&](size_t off) { return reinterpret_cast<float*>(A + off); };
+  auto ACT = [&](size_t off) { return reinterpret_cast<void*>(A + off); };
+  const bool bf = is_bf16(c);
+  // weights as GEMM operands: bf16 copies on the tensor-core path, fp32 master otherwise
+  auto W = [&](int t) -> const void* {
+    const size_t off = h->tensors[t].offset;
+    return bf ? (const void*)(h->shadow + off) : (const void*)(h->params + off);
+  };
+  auto P = [&](int t) -> float* { return t < 0 ? nullptr : h->params + h->tensors[t].offset; };
+  auto G = [&](int t) -> float* { return t < 0 ? nullptr : h->grads + h->tensors[t].offset; };
+  Builder bld{h};
+  const int N = D.N, C = D.C, F = D.F, V = D.V, L = D.L;
+  int rc;
+
+  // ---------------- forward ----------------
+  OpDesc o = blank(OP_EMBED, (N + kRowsEmb - 1) / kRowsEmb);
+  o.emb = EmbedArgs{P(h->t_wte), P(h->t_wpe), F32(Lo.x[0]), nullptr, nullptr, nullptr,
+                    N, D.B, D.T, C, V, kRowsEmb};
+  int prev = bld.add(o, {});
+  std::vector<int> op_ln1(L), op_qkv(L), op_attn(L), op_atto(L), op_ln2(L), op_up(L), op_down(L);
+  const int qblock = D.T <= 512 ? 64 : 32;
+  for (int l = 0; l < L; ++l) {
+    const TensorIds& id = h->lid[l];
+    o = blank(OP_LN_FWD, ln_tasks(N));
+    o.lnf = LnFwdArgs{F32(Lo.x[l]), P(id.ln1_g), P(id.ln1_b), ACT(Lo.ln1[l]), F32(Lo.ln1_mu[l]),
+                      F32(Lo.ln1_rs[l]), N, C, kRowsLn, c.ln_eps};
+    op_ln1[l] = bld.add(o, {prev});
+    // qkv = ln1 . Wqkv^T + b
+    if ((rc = gemm_op(h, &o, N, 3 * C, C, {ACT(Lo.ln1[l]), C, false}, {W(id.w_qkv), C, false}, EPI_STORE, 1)))
+      return rc;
+    o.gemm.out = ACT(Lo.qkv[l]); o.gemm.ldo = 3 * C; o.gemm.bias = P(id.b_qkv);
+    op_qkv[l] = bld.add(o, {op_ln1[l]});
+    o = blank(OP_ATTN_FWD, D.B * D.H * ((D.T + qblock - 1) / qblock));
+    o.attn = AttnArgs{ACT(Lo.qkv[l]), ACT(Lo.atto[l]), F32(Lo.lse[l]), nullptr, nullptr, nullptr,
+                      D.B, D.T, D.H, D.d, C, qblock, 1.0f / std::sqrt((float)D.d)};
+    op_attn[l] = bld.add(o, {op_qkv[l]});
+    // xm = x + o . Wo^T + b
+    if ((rc = gemm_op(h, &o, N, C, C, {ACT(Lo.atto[l]), C, false}, {W(id.w_o), C, false}, EPI_RESID, 1)))
+      return rc;
+    o.gemm.out = F32(Lo.xm[l]); o.gemm.ldo = C; o.gemm.bias = P(id.b_o);
+    o.gemm.resid = F32(Lo.x[l]); o.gemm.ldr = C;
+    op_atto[l] = bld.add(o, {op_attn[l]});
+    o = blank(OP_LN_FWD, ln_tasks(N));
+    o.lnf = LnFwdArgs{F32(Lo.xm[l]), P(id.ln2_g), P(id.ln2_b), ACT(Lo.ln2[l]), F32(Lo.ln2_mu[l]),
+                      F32(Lo.ln2_rs[l]), N, C, kRowsLn, c.ln_eps};
+    op_ln2[l] = bld.add(o, {op_atto[l]});
+    // h = ln2 . W1^T + b1 ; g = GELU(h)
+    if ((rc = gemm_op(h, &o, N, F, C, {ACT(Lo.ln2[l]), C, false}, {W(id.w_1), C, false}, EPI_GELU, 1)))
+      return rc;
+    o.gemm.out = ACT(Lo.hpre[l]); o.gemm.ldo = F; o.gemm.out2 = ACT(Lo.gact[l]); o.gemm.ldo2 = F;
+    o.gemm.bias = P(id.b_1);
+    op_up[l] = bld.add(o, {op_ln2[l]});
+    // x_{l+1} = xm + g . W2^T + b2
+    if ((rc = gemm_op(h, &o, N, C, F, {ACT(Lo.gact[l]), F, false}, {W(id.w_2), F, false}, EPI_RESID, 1)))
+      return rc;
+    o.gemm.out = F32(Lo.x[l + 1]); o.gemm.ldo = C; o.gemm.bias = P(id.b_2);
+    o.gemm.resid = F32(Lo.xm[l]); o.gemm.ldr = C;
+    op_down[l] = prev = bld.add(o, {op_up[l]});
+  }
+  o = blank(OP_LN_FWD, ln_tasks(N));
+  o.lnf = LnFwdArgs{F32(Lo.x[L]), P(h->t_lnf_g), P(h->t_lnf_b), ACT(Lo.lnf), F32(Lo.lnf_mu), F32(Lo.lnf_rs),
+                    N, C, kRowsLn, c.ln_eps};
+  const int op_lnf = bld.add(o, {prev});
+  // logits = lnf . Wlm^T
+  if ((rc = gemm_op(h, &o, N, V, C, {ACT(Lo.lnf), C, false}, {W(h->t_wlm), C, false}, EPI_STORE, 1))) return rc;
+  o.gemm.out = ACT(Lo.logits); o.gemm.ldo = V;
+  const int op_lm = bld.add(o, {op_lnf});
+  o = blank(OP_CE, (N + kRowsCe - 1) / kRowsCe);
+  o.ce = CeArgs{ACT(Lo.logits), F32(Lo.row_loss), N, V, kRowsCe};
+  const int op_ce = bld.add(o, {op_lm});
+  o = blank(OP_LOSS, 1);
+  o.loss = LossArgs{F32(Lo.row_loss), F32(Lo.loss), N};
+  const int op_loss = bld.add(o, {op_ce});
+
+  // ---------------- backward ----------------
+  auto adam = [&](int t, std::initializer_list<int> deps) {
+    const TensorInfo& ti = h->tensors[t];
+    const int64_t n = ti.rows * ti.cols;
+    OpDesc a = blank(OP_ADAMW, (int)((n + kAdamChunk - 1) / kAdamChunk));
+    a.adam = AdamArgs{h->params + ti.offset, h->grads + ti.offset, h->m + ti.offset, h->v + ti.offset,
+                      bf ? h->shadow + ti.offset : nullptr, n, kAdamChunk,
+                      (ti.ndim == 2 || c.wd_on_1d) ? 1.0f : 0.0f};
+    std::vector<int> dl(deps);
+    dl.push_back(op_loss);
+    if (dl.size() == 2) bld.add(a, {dl[0], dl[1]});
+    else bld.add(a, {dl[0], dl[1], dl[2]});
+  };
+  auto colsum = [&](const void* src, bool f32, int64_t ld, int rows, int cols, float* dst, int dep) {
+    OpDesc s = blank(OP_COLSUM, (cols + kColsColsum - 1) / kColsColsum);
+    s.colsum = ColsumArgs{src, f32 ? 1 : 0, ld, rows, cols, kColsColsum, dst};
+    return bld.add(s, {dep});
+  };
+  // LM head: daf = dz . Wlm ; dWlm = dz^T . lnf
+  if ((rc = gemm_op(h, &o, N, C, V, {ACT(Lo.logits), V, false}, {W(h->t_wlm), C, true}, EPI_F32, lm_ksplit)))
+    return rc;
+  o.gemm.out = F32(Lo.daf); o.gemm.ldo = C; o.gemm.split_stride = (int64_t)N * C;
+  const int op_lm_dx = bld.add(o, {op_ce});
+  if ((rc = gemm_op(h, &o, V, C, N, {ACT(Lo.logits), V, true}, {ACT(Lo.lnf), C, true}, EPI_F32, 1))) return rc;
+  o.gemm.out = G(h->t_wlm); o.gemm.ldo = C;
+  const int op_lm_dw = bld.add(o, {op_ce});
+  adam(h->t_wlm, {op_lm_dw, op_lm_dx});
+  // final LayerNorm backward
+  const int nrb = ln_tasks(N);
+  o = blank(OP_LN_BWD, nrb);
+  o.lnb = LnBwdArgs{F32(Lo.daf), lm_ksplit, (int64_t)N * C, F32(Lo.x[L]), F32(Lo.lnf_mu), F32(Lo.lnf_rs),
+                    P(h->t_lnf_g), nullptr, F32(Lo.dx[L]), ACT(Lo.dx_act[L]), F32(Lo.lnf_gp),
+                    h->t_lnf_b >= 0 ? F32(Lo.lnf_bp) : nullptr, N, C, kRowsLn};
+  int op_dres = bld.add(o, {op_lm_dx});
+  {
+    const int r1 = colsum(F32(Lo.lnf_gp), true, C, nrb, C, G(h->t_lnf_g), op_dres);
+    adam(h->t_lnf_g, {r1});
+    if (h->t_lnf_b >= 0) {
+      const int r2 = colsum(F32(Lo.lnf_bp), true, C, nrb, C, G(h->t_lnf_b), op_dres);
+      adam(h->t_lnf_b, {r2});
+    }
+  }
+  for (int l = L - 1; l >= 0; --l) {
+    const TensorIds& id = h->lid[l];
+    // MLP down: dg = dx . W2 (then * GELU'(h)) ; dW2 = dx^T . g ; db2 = colsum(dx)
+    if ((rc = gemm_op(h, &o, N, F, C, {ACT(Lo.dx_act[l + 1]), C, false}, {W(id.w_2), F, true}, EPI_GELU_BWD, 1)))
+      return rc;
+    o.gemm.out = ACT(Lo.dh[l]); o.gemm.ldo = F; o.gemm.aux = ACT(Lo.hpre[l]); o.gemm.ldaux = F;
+    const int op_down_dx = bld.add(o, {op_dres});
+    if ((rc = gemm_op(h, &o, C, F, N, {ACT(Lo.dx_act[l + 1]), C, true}, {ACT(Lo.gact[l]), F, true}, EPI_F32, 1)))
+      return rc;
+    o.gemm.out = G(id.w_2); o.gemm.ldo = F;
+    const int op_down_dw = bld.add(o, {op_dres});
+    if (id.b_2 >= 0) adam(id.b_2, {colsum(F32(Lo.dx[l + 1]), true, C, N, C, G(id.b_2), op_dres)});
+    adam(id.w_2, {op_down_dw, op_down_dx});
+    // MLP up: da2 = dh . W1 ; dW1 = dh^T . ln2 ; db1 = colsum(dh)
+    if ((rc = gemm_op(h, &o, N, C, F, {ACT(Lo.dh[l]), F, false}, {W(id.w_1), C, true}, EPI_F32, 1))) return rc;
+    o.gemm.out = F32(Lo.da2[l]); o.gemm.ldo = C;
+    const int op_up_dx = bld.add(o, {op_down_dx});
+    if ((rc = gemm_op(h, &o, F, C, N, {ACT(Lo.dh[l]), F, true}, {ACT(Lo.ln2[l]), C, true}, EPI_F32, 1)))
+      return rc;
+    o.gemm.out = G(id.w_1); o.gemm.ldo = C;
+    const int op_up_dw = bld.add(o, {op_down_dx});
+    if (id.b_1 >= 0) adam(id.b_1, {colsum(ACT(Lo.dh[l]), false, F, N, F, G(id.b_1), op_down_dx)});
+    adam(id.w_1, {op_up_dw, op_up_dx});
+    // LN2 backward: dxm = dx + LN2'(da2)
+    o = blank(OP_LN_BWD, nrb);
+    o.lnb = LnBwdArgs{F32(Lo.da2[l]), 1, 0, F32(Lo.xm[l]), F32(Lo.ln2_mu[l]), F32(Lo.ln2_rs[l]), P(id.ln2_g),
+                      F32(Lo.dx[l + 1]), F32(Lo.dxm[l]), ACT(Lo.dxm_act[l]), F32(Lo.ln2_gp[l]),
+                      id.ln2_b >= 0 ? F32(Lo.ln2_bp[l]) : nullptr, N, C, kRowsLn};
+    const int op_ln2b = bld.add(o, {op_up_dx, op_dres});
+    adam(id.ln2_g, {colsum(F32(Lo.ln2_gp[l]), true, C, nrb, C, G(id.ln2_g), op_ln2b)});
+    if (id.ln2_b >= 0) adam(id.ln2_b, {colsum(F32(Lo.ln2_bp[l]), true, C, nrb, C, G(id.ln2_b), op_ln2b)});
+    // attention out: dO = dxm . Wo ; dWo = dxm^T . o ; dbo = colsum(dxm)
+    if ((rc = gemm_op(h, &o, N, C, C, {ACT(Lo.dxm_act[l]), C, false}, {W(id.w_o), C, true}, EPI_STORE, 1)))
+      return rc;
+    o.gemm.out = ACT(Lo.dO[l]); o.gemm.ldo = C;
+    const int op_atto_dx = bld.add(o, {op_ln2b});
+    if ((rc = gemm_op(h, &o, C, C, N, {ACT(Lo.dxm_act[l]), C, true}, {ACT(Lo.atto[l]), C, true}, EPI_F32, 1)))
+      return rc;
+    o.gemm.out = G(id.w_o); o.gemm.ldo = C;
+    const int op_atto_dw = bld.add(o, {op_ln2b});
+    if (id.b_o >= 0) adam(id.b_o, {colsum(F32(Lo.dxm[l]), true, C, N, C, G(id.b_o), op_ln2b)});
+    adam(id.w_o, {op_atto_dw, op_atto_dx});
+    // attention backward -> dqkv
+    o = blank(OP_ATTN_BWD, D.B * D.H);
+    o.attn = AttnArgs{ACT(Lo.qkv[l]), ACT(Lo.atto[l]), F32(Lo.lse[l]), ACT(Lo.dO[l]), ACT(Lo.dqkv[l]),
+                      F32(Lo.att_scr[l]), D.B, D.T, D.H, D.d, C, qblock, 1.0f / std::sqrt((float)D.d)};
+    const int op_attb = bld.add(o, {op_atto_dx});
+    // QKV: da1 = dqkv . Wqkv ; dWqkv = dqkv^T . ln1 ; dbqkv = colsum(dqkv)
+    if ((rc = gemm_op(h, &o, N, C, 3 * C, {ACT(Lo.dqkv[l]), 3 * C, false}, {W(id.w_qkv), C, true}, EPI_F32, 1)))
+      return rc;
+    o.gemm.out = F32(Lo.da1[l]); o.gemm.ldo = C;
+    const int op_qkv_dx = bld.add(o, {op_attb});
+    if ((rc = gemm_op(h, &o, 3 * C, C, N, {ACT(Lo.dqkv[l]), 3 * C, true}, {ACT(Lo.ln1[l]), C, true}, EPI_F32, 1)))
+      return rc;
+    o.gemm.out = G(id.w_qkv); o.gemm.ldo = C;
+    const int op_qkv_dw = bld.add(o, {op_attb});
+    if (id.b_qkv >= 0) adam(id.b_qkv, {colsum(ACT(Lo.dqkv[l]), false, 3 * C, N, 3 * C, G(id.b_qkv), op_attb)});
+    adam(id.w_qkv, {op_qkv_dw, op_qkv_dx});
+    // LN1 backward: dx_l = dxm + LN1'(da1)
+    o = blank(OP_LN_BWD, nrb);
+    o.lnb = LnBwdArgs{F32(Lo.da1[l]), 1, 0, F32(Lo.x[l]), F32(Lo.ln1_mu[l]), F32(Lo.ln1_rs[l]), P(id.ln1_g),
+                      F32(Lo.dxm[l]), F32(Lo.dx[l]), ACT(Lo.dx_act[l]), F32(Lo.ln1_gp[l]),
+                      id.ln1_b >= 0 ? F32(Lo.ln1_bp[l]) : nullptr, N, C, kRowsLn};
+    op_dres = bld.add(o, {op_qkv_dx, op_ln2b});
+    adam(id.ln1_g, {colsum(F32(Lo.ln1_gp[l]), true, C, nrb, C, G(id.ln1_g), op_dres)});
+    if (id.ln1_b >= 0) adam(id.ln1_b, {colsum(F32(Lo.ln1_bp[l]), true, C, nrb, C, G(id.ln1_b), op_dres)});
+  }
+  // embeddings
+  o = blank(OP_EMBED_BWD_WTE, (V + kVocabRows - 1) / kVocabRows);
+  o.emb = EmbedArgs{nullptr, nullptr, nullptr, F32(Lo.dx[0]), G(h->t_wte), G(h->t_wpe), N, D.B, D.T, C, V,
+                    kVocabRows};
+  const int op_wte = bld.add(o, {op_dres});
+  adam(h->t_wte, {op_wte});
+  o = blank(OP_EMBED_BWD_WPE, (D.T + kRowsEmb - 1) / kRowsEmb);
+  o.emb = EmbedArgs{nullptr, nullptr, nullptr, F32(Lo.dx[0]), G(h->t_wte), G(h->t_wpe), N, D.B, D.T, C, V,
+                    kRowsEmb};
+  const int op_wpe = bld.add(o, {op_dres});
+  adam(h->t_wpe, {op_wpe});
+  (void)op_lm; (void)op_qkv; (void)op_attn; (void)op_atto; (void)op_ln2; (void)op_up; (void)op_down;
+  return GPT_OK;
+}
+
+size_t smem_needed(const gpt* h) {
+  const Dims& D = h->D;
+  const int qblock = D.T <= 512 ? 64 : 32;
+  size_t s = 0;
+  s = std::max(s, (size_t)(2 * 16 * (kSimtTile + 4) * 4));                     // SIMT GEMM
+  s = std::max(s, (size_t)(2 * kWarps * D.C * 4));                             // LN backward partials
+  s = std::max(s, (size_t)D.N * 4);                                            // token ids
+  s = std::max(s, (size_t)(qblock * D.d + 64 * (D.d + 1) + qblock * D.T) * 4); // attention forward
+  s = std::max(s, (size_t)(2 * qblock * D.d + 64 * (D.d + 1) + qblock * D.T + qblock) * 4);  // backward
+  s = std::max(s, (size_t)kThreads * 4);
+  if (is_bf16(h->cfg)) s = std::max(s, (size_t)kTcSmemBytes);
+  return s + 1024;  // 1024-byte alignment slack
+}
+
+int fill_shadow_and_upload(gpt* h, const float* host_params) {
+  CUDA_TRY(h, cudaMemcpyAsync(h->params, host_params, h->nparams * 4, cudaMemcpyHostToDevice, h->stream));
+  if (is_bf16(h->cfg)) {
+    std::vector<uint16_t> sh(h->nparams);
+    for (size_t i = 0; i < h->nparams; ++i) sh[i] = f32_to_bf16_rne(host_params[i]);
+    CUDA_TRY(h, cudaMemcpyAsync(h->shadow, sh.data(), h->nparams * 2, cudaMemcpyHostToDevice, h->stream));
+    CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  } else {
+    CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  }
+  return GPT_OK;
+}
+
+int reset_counters(gpt* h) {
+  const size_t nctr = h->ops.size();
+  CUDA_TRY(h, cudaMemsetAsync(h->d_counters, 0, nctr * sizeof(unsigned long long), h->stream));
+  CUDA_TRY(h, cudaMemsetAsync(h->d_ticket, 0, sizeof(unsigned long long), h->stream));
+  CUDA_TRY(h, cudaMemsetAsync(h->d_err, 0, 4 * sizeof(uint32_t), h->stream));
+  CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  h->launches = 0;
+  h->poisoned = false;
+  return GPT_OK;
+}
+
+int launch_step(gpt* h, const int32_t* tokens, const int32_t* targets, float* loss) {
+  if (h->poisoned) return fail(h, GPT_ERR_POISONED, "handle poisoned by an earlier timeout; call gpt_reset");
+  KParams kp;
+  std::memset(&kp, 0, sizeof kp);
+  kp.tasks = h->d_tasks;
+  kp.ntasks = (int64_t)h->tasks.size();
+  kp.ops = h->d_ops;
+  kp.counters = h->d_counters;
+  kp.ticket = h->d_ticket;
+  kp.ticket_base = (unsigned long long)h->launches * (unsigned long long)(h->tasks.size() + h->grid);
+  kp.epoch = h->launches + 1;
+  kp.err = h->d_err;
+  kp.timeout_ns = (uint64_t)(h->cfg.wait_timeout_ms ? h->cfg.wait_timeout_ms : 2000) * 1000000ull;
+  kp.skip_release = h->skip_release;
+  kp.tmaps = h->d_tmaps;
+  kp.tokens = tokens;
+  kp.targets = targets;
+  kp.lr = h->cfg.lr; kp.beta1 = h->cfg.beta1; kp.beta2 = h->cfg.beta2; kp.eps = h->cfg.eps;
+  kp.wd = h->cfg.weight_decay;
+  const double t = (double)(h->opt_step + 1);
+  kp.bc1 = (float)(1.0 - std::pow((double)h->cfg.beta1, t));
+  kp.bc2 = (float)(1.0 - std::pow((double)h->cfg.beta2, t));
+  int32_t gelu_tanh = h->cfg.gelu_tanh;
+  void* args[2] = {&kp, &gelu_tanh};
+  h->skip_release = -1;
+  if (h->ev0) CUDA_TRY(h, cudaEventRecord(h->ev0, h->stream));
+  cudaError_t e = cudaLaunchCooperativeKernel(h->kernel, dim3(h->grid), dim3(kThreads), args, h->smem_bytes,
+                                              h->stream);
+  if (e != cudaSuccess) return fail(h, GPT_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+  if (h->ev1) CUDA_TRY(h, cudaEventRecord(h->ev1, h->stream));
+  CUDA_TRY(h, cudaMemcpyAsync(h->h_status->err, h->d_err, 4 * sizeof(uint32_t), cudaMemcpyDeviceToHost, h->stream));
+  CUDA_TRY(h, cudaMemcpyAsync(&h->h_status->loss, h->loss_dev, sizeof(float), cudaMemcpyDeviceToHost, h->stream));
+  CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  if (h->ev0 && h->ev1) cudaEventElapsedTime(&h->last_kernel_ms, h->ev0, h->ev1);
+  const uint32_t fatal = h->h_status->err[0], soft = h->h_status->err[1];
+  if (fatal) {
+    h->poisoned = true;
+    return fail(h, GPT_ERR_TIMEOUT, "device wait timed out (code %u, task %u, counter/barrier %u)", fatal,
+                h->h_status->err[2], h->h_status->err[3]);
+  }
+  h->launches++;
+  if (loss) *loss = h->h_status->loss;
+  if (soft) {
+    CUDA_TRY(h, cudaMemsetAsync(h->d_err + 1, 0, sizeof(uint32_t), h->stream));
+    CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+    if (soft & kSoftBadToken) return fail(h, GPT_ERR_BAD_TOKEN, "token or target id outside [0, vocab)");
+    return fail(h, GPT_ERR_NONFINITE, "non-finite loss %g", (double)h->h_status->loss);
+  }
+  h->opt_step++;
+  h->err.clear();
+  return GPT_OK;
+}
+
+}  // namespace
+
+// ============================================================================
+// C ABI
+// ============================================================================
+extern "C" {
+
+void gpt_default_config(gpt_config* c) {
+  if (!c) return;
+  std::memset(c, 0, sizeof *c);
+  c->n_layer = 12; c->d_model = 768; c->n_head = 12; c->d_mlp = 3072; c->vocab = 50304;
+  c->seq_len = 512; c->batch = 8; c->dtype = GPT_DTYPE_BF16;
+  c->linear_bias = 1; c->ln_bias = 1; c->tie_embeddings = 0; c->gelu_tanh = 1;
+  c->lr = 6e-4f; c->beta1 = 0.9f; c->beta2 = 0.95f; c->eps = 1e-8f; c->weight_decay = 0.1f; c->ln_eps = 1e-5f;
+  c->wd_on_1d = 0; c->wait_timeout_ms = 2000; c->deterministic = 1;
+}
+
+static int lm_ksplit_for(const gpt_config& c, int num_sms) {
+  if (!is_bf16(c)) return 1;
+  // the vocabulary-long reduction of the LM-head input gradient is split so
+  // that its tiles fill at least one wave
+  const int N = c.batch * c.seq_len;
+  const int tiles = (N / kTcBM) * ((c.d_model + 255) / 256);
+  int ks = 1;
+  while (tiles * ks < num_sms && ks < 8 && (c.vocab / kTcBK) % (ks * 2) == 0) ks *= 2;
+  return ks;
+}
+
+size_t gpt_arena_bytes(const gpt_config* cfg) {
+  if (!cfg) return 0;
+  std::string why;
+  if (validate(*cfg, &why) != GPT_OK) return 0;
+  gpt tmp;
+  tmp.cfg = *cfg;
+  build_table(&tmp);
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return make_layout(*cfg, tmp.nparams, lm_ksplit_for(*cfg, sms)).total;
+}
+
+int gpt_create(const gpt_config* cfg, uint64_t seed, void* cuda_stream, void* arena, size_t arena_bytes, gpt** out) {
+  g_create_error.clear();
+  if (!cfg || !out) return fail(nullptr, GPT_ERR_INVALID_ARG, "cfg and out must be non-NULL");
+  std::string why;
+  int rc = validate(*cfg, &why);
+  if (rc != GPT_OK) return fail(nullptr, rc, "invalid config: %s", why.c_str());
+  gpt* h = new (std::nothrow) gpt();
+  if (!h) return fail(nullptr, GPT_ERR_OOM, "host allocation failed");
+  h->cfg = *cfg;
+  if (!h->cfg.wait_timeout_ms) h->cfg.wait_timeout_ms = 2000;
+  const gpt_config& c = h->cfg;
+  h->D = Dims{c.n_layer, c.d_model, c.n_head, c.d_model / c.n_head, c.d_mlp, c.vocab, c.seq_len, c.batch,
+              c.batch * c.seq_len};
+  h->stream = (cudaStream_t)cuda_stream;
+  auto bail = [&](int code) {
+    std::string msg = h->err;
+    gpt_destroy(h);
+    g_create_error = msg;
+    return code;
+  };
+  if (cudaGetDevice(&h->device) != cudaSuccess) { fail(h, GPT_ERR_CUDA, "no CUDA device"); return bail(GPT_ERR_CUDA); }
+  cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device);
+  int cc_major = 0, cc_minor = 0;
+  cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, h->device);
+  cudaDeviceGetAttribute(&cc_minor, cudaDevAttrComputeCapabilityMinor, h->device);
+  if (cc_major != 10 || cc_minor != 3) {
+    fail(h, GPT_ERR_UNSUPPORTED, "compiled for sm_103a; device is sm_%d%d", cc_major, cc_minor);
+    return bail(GPT_ERR_UNSUPPORTED);
+  }
+  build_table(h);
+  const int lm_ks = lm_ksplit_for(c, h->num_sms);
+  const Layout Lo = make_layout(c, h->nparams, lm_ks);
+  // arena
+  if (arena) {
+    if (arena_bytes < Lo.total || (reinterpret_cast<uintptr_t>(arena) & 255)) {
+      fail(h, GPT_ERR_INVALID_ARG, "arena must be 256-byte aligned and >= %zu bytes", Lo.total);
+      return bail(GPT_ERR_INVALID_ARG);
+    }
+    h->arena = static_cast<uint8_t*>(arena);
+  } else {
+    if (cudaMalloc(&h->arena, Lo.total) != cudaSuccess) {
+      cudaGetLastError();
+      fail(h, GPT_ERR_OOM, "cudaMalloc of %zu arena bytes failed", Lo.total);
+      return bail(GPT_ERR_OOM);
+    }
+    h->own_arena = true;
+  }
+  h->arena_bytes = Lo.total;
+  h->params = reinterpret_cast<float*>(h->arena + Lo.params);
+  h->grads = reinterpret_cast<float*>(h->arena + Lo.grads);
+  h->m = reinterpret_cast<float*>(h->arena + Lo.m);
+  h->v = reinterpret_cast<float*>(h->arena + Lo.v);
+  h->shadow = is_bf16(c) ? reinterpret_cast<uint16_t*>(h->arena + Lo.shadow) : nullptr;
+  h->loss_dev = reinterpret_cast<float*>(h->arena + Lo.loss);
+  // graph
+  rc = build_graph(h, Lo, lm_ks);
+  if (rc != GPT_OK) return bail(rc);
+  // metadata allocation: tasks | ops | tensor maps | counters | ticket | err | token staging
+  Bump mb;
+  const size_t o_tasks = mb.take(h->tasks.size() * sizeof(TaskDesc));
+  const size_t o_ops = mb.take(h->ops.size() * sizeof(OpDesc));
+  const size_t o_maps = mb.take(std::max<size_t>(1, h->tmaps.size()) * 128);
+  const size_t o_ctr = mb.take(h->ops.size() * sizeof(unsigned long long));
+  const size_t o_tic = mb.take(sizeof(unsigned long long));
+  const size_t o_err = mb.take(4 * sizeof(uint32_t));
+  const size_t o_tok = mb.take(2 * (size_t)h->D.N * sizeof(int32_t));
+  h->meta_bytes = mb.off;
+  if (cudaMalloc(&h->meta, h->meta_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    fail(h, GPT_ERR_OOM, "cudaMalloc of graph metadata failed");
+    return bail(GPT_ERR_OOM);
+  }
+  h->d_tasks = reinterpret_cast<TaskDesc*>(h->meta + o_tasks);
+  h->d_ops = reinterpret_cast<OpDesc*>(h->meta + o_ops);
+  h->d_tmaps = h->meta + o_maps;
+  h->d_counters = reinterpret_cast<unsigned long long*>(h->meta + o_ctr);
+  h->d_ticket = reinterpret_cast<unsigned long long*>(h->meta + o_tic);
+  h->d_err = reinterpret_cast<uint32_t*>(h->meta + o_err);
+  h->d_tok_stage = reinterpret_cast<int32_t*>(h->meta + o_tok);
+  if (cudaMallocHost(&h->h_status, sizeof(gpt::Status)) != cudaSuccess) {
+    cudaGetLastError();
+    fail(h, GPT_ERR_OOM, "pinned host allocation failed");
+    return bail(GPT_ERR_OOM);
+  }
+#define CREATE_TRY(call)                                                                       \
+  do {                                                                                         \
+    cudaError_t e_ = (call);                                                                   \
+    if (e_ != cudaSuccess) {                                                                   \
+      fail(h, GPT_ERR_CUDA, "%s failed: %s", #call, cudaGetErrorString(e_));                   \
+      return bail(GPT_ERR_CUDA);                                                               \
+    }                                                                                          \
+  } while (0)
+  CREATE_TRY(cudaMemcpyAsync(h->d_tasks, h->tasks.data(), h->tasks.size() * sizeof(TaskDesc),
+                             cudaMemcpyHostToDevice, h->stream));
+  CREATE_TRY(cudaMemcpyAsync(h->d_ops, h->ops.data(), h->ops.size() * sizeof(OpDesc), cudaMemcpyHostToDevice,
+                             h->stream));
+  for (size_t i = 0; i < h->tmaps.size(); ++i)
+    CREATE_TRY(cudaMemcpyAsync(static_cast<uint8_t*>(h->d_tmaps) + 128 * i, h->tmaps[i].data(), 128,
+                               cudaMemcpyHostToDevice, h->stream));
+  // seeded initial weights on the host; m = v = 0; grads = 0
+  {
+    std::vector<float> hp(h->nparams);
+    for (size_t t = 0; t < h->tensors.size(); ++t) {
+      const TensorInfo& ti = h->tensors[t];
+      const size_t n = (size_t)(ti.rows * ti.cols);
+      float* dst = hp.data() + ti.offset;
+      if (ti.init == INIT_NORMAL) normal_fill(dst, n, seed, t);
+      else std::fill(dst, dst + n, ti.init == INIT_ONES ? 1.0f : 0.0f);
+    }
+    rc = fill_shadow_and_upload(h, hp.data());
+    if (rc != GPT_OK) return bail(rc);
+  }
+  CREATE_TRY(cudaMemsetAsync(h->grads, 0, h->nparams * 4, h->stream));
+  CREATE_TRY(cudaMemsetAsync(h->m, 0, h->nparams * 4, h->stream));
+  CREATE_TRY(cudaMemsetAsync(h->v, 0, h->nparams * 4, h->stream));
+  // kernel + grid: every block must be resident (cooperative launch checks it)
+  h->kernel = is_bf16(c) ? step_kernel_bf16() : step_kernel_fp32();
+  h->smem_bytes = smem_needed(h);
+  CREATE_TRY(cudaFuncSetAttribute(h->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem_bytes));
+  int per_sm = 0;
+  CREATE_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, h->kernel, kThreads, h->smem_bytes));
+  if (per_sm < 1) {
+    fail(h, GPT_ERR_UNSUPPORTED, "kernel does not fit on an SM (%zu bytes shared memory)", h->smem_bytes);
+    return bail(GPT_ERR_UNSUPPORTED);
+  }
+  h->grid = h->num_sms * std::min(per_sm, 1);
+  CREATE_TRY(cudaEventCreate(&h->ev0));
+  CREATE_TRY(cudaEventCreate(&h->ev1));
+  if (reset_counters(h) != GPT_OK) return bail(GPT_ERR_CUDA);
+#undef CREATE_TRY
+  *out = h;
+  return GPT_OK;
+}
+
+int gpt_train_step(gpt* h, const int32_t* tokens, const int32_t* targets, float* loss) {
+  if (!h) return GPT_ERR_INVALID_ARG;
+  if (!tokens || !targets) return fail(h, GPT_ERR_INVALID_ARG, "tokens and targets must be device pointers");
+  return launch_step(h, tokens, targets, loss);
+}
+
+int gpt_train_step_host(gpt* h, const int32_t* tokens, const int32_t* targets, float* loss) {
+  if (!h) return GPT_ERR_INVALID_ARG;
+  if (!tokens || !targets) return fail(h, GPT_ERR_INVALID_ARG, "tokens and targets must be host pointers");
+  const size_t n = (size_t)h->D.N;
+  CUDA_TRY(h, cudaMemcpyAsync(h->d_tok_stage, tokens, n * 4, cudaMemcpyHostToDevice, h->stream));
+  CUDA_TRY(h, cudaMemcpyAsync(h->d_tok_stage + n, targets, n * 4, cudaMemcpyHostToDevice, h->stream));
+  return launch_step(h, h->d_tok_stage, h->d_tok_stage + n, loss);
+}
+
+size_t gpt_num_params(const gpt* h) { return h ? h->nparams : 0; }
+int gpt_num_tensors(const gpt* h) { return h ? (int)h->tensors.size() : 0; }
+
+int gpt_tensor_info(const gpt* h, int i, const char** name, int64_t shape[2], size_t* offset) {
+  if (!h || i < 0 || i >= (int)h->tensors.size()) return GPT_ERR_INVALID_ARG;
+  const TensorInfo& t = h->tensors[i];
+  if (name) *name = t.name.c_str();
+  if (shape) { shape[0] = t.rows; shape[1] = t.cols; }
+  if (offset) *offset = t.offset;
+  return GPT_OK;
+}
+
+static int copy_out(gpt* h, float* dst, const float* src, size_t n) {
+  if (!h || !dst) return GPT_ERR_INVALID_ARG;
+  if (n != h->nparams) return fail(h, GPT_ERR_INVALID_ARG, "n must equal gpt_num_params (%zu)", h->nparams);
+  CUDA_TRY(h, cudaMemcpyAsync(dst, src, n * 4, cudaMemcpyDeviceToHost, h->stream));
+  CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  return GPT_OK;
+}
+
+int gpt_get_params(gpt* h, float* dst, size_t n) { return h ? copy_out(h, dst, h->params, n) : GPT_ERR_INVALID_ARG; }
+int gpt_get_grads(gpt* h, float* dst, size_t n) { return h ? copy_out(h, dst, h->grads, n) : GPT_ERR_INVALID_ARG; }
+
+int gpt_set_params(gpt* h, const float* src, size_t n) {
+  if (!h || !src) return GPT_ERR_INVALID_ARG;
+  if (n != h->nparams) return fail(h, GPT_ERR_INVALID_ARG, "n must equal gpt_num_params (%zu)", h->nparams);
+  return fill_shadow_and_upload(h, src);
+}
+
+int gpt_get_opt_state(gpt* h, float* m, float* v, int64_t* step) {
+  if (!h) return GPT_ERR_INVALID_ARG;
+  if (m) CUDA_TRY(h, cudaMemcpyAsync(m, h->m, h->nparams * 4, cudaMemcpyDeviceToHost, h->stream));
+  if (v) CUDA_TRY(h, cudaMemcpyAsync(v, h->v, h->nparams * 4, cudaMemcpyDeviceToHost, h->stream));
+  CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  if (step) *step = h->opt_step;
+  return GPT_OK;
+}
+
+int gpt_set_opt_state(gpt* h, const float* m, const float* v, int64_t step) {
+  if (!h || step < 0) return GPT_ERR_INVALID_ARG;
+  if (m) CUDA_TRY(h, cudaMemcpyAsync(h->m, m, h->nparams * 4, cudaMemcpyHostToDevice, h->stream));
+  if (v) CUDA_TRY(h, cudaMemcpyAsync(h->v, v, h->nparams * 4, cudaMemcpyHostToDevice, h->stream));
+  CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  h->opt_step = step;
+  return GPT_OK;
+}
+
+int gpt_debug_skip_release(gpt* h, int64_t task_index) {
+  if (!h || task_index < -1 || task_index >= (int64_t)h->tasks.size()) return GPT_ERR_INVALID_ARG;
+  h->skip_release = task_index;
+  return GPT_OK;
+}
+
+int gpt_reset(gpt* h) {
+  if (!h) return GPT_ERR_INVALID_ARG;
+  return reset_counters(h);
+}
+
+int gpt_graph_info(const gpt* h, int64_t* n_tasks, int32_t* grid, int32_t* block) {
+  if (!h) return GPT_ERR_INVALID_ARG;
+  if (n_tasks) *n_tasks = (int64_t)h->tasks.size();
+  if (grid) *grid = h->grid;
+  if (block) *block = kThreads;
+  return GPT_OK;
+}
+
+int gpt_last_kernel_ms(const gpt* h, float* ms) {
+  if (!h || !ms) return GPT_ERR_INVALID_ARG;
+  *ms = h->last_kernel_ms;
+  return GPT_OK;
+}
+
+const char* gpt_last_error(const gpt* h) { return h ? h->err.c_str() : g_create_error.c_str(); }
+
+void gpt_destroy(gpt* h) {
+  if (!h) return;
+  if (h->stream || h->meta || h->arena) cudaStreamSynchronize(h->stream);
+  if (h->meta) cudaFree(h->meta);
+  if (h->own_arena && h->arena) cudaFree(h->arena);
+  if (h->h_status) cudaFreeHost(h->h_status);
+  if (h->ev0) cudaEventDestroy(h->ev0);
+  if (h->ev1) cudaEventDestroy(h->ev1);
+  delete h;
+}
+
+int gpt_test_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, int32_t a_mn,
+                  const void* B, int64_t ldb, int32_t b_mn, float* C, int64_t ldc, int32_t ksplit,
+                  void* cuda_stream) {
+  g_create_error.clear();
+  if (!A || !B || !C || M < 1 || N < 1 || K < 1 || ksplit < 1 || (dtype != GPT_DTYPE_FP32 && dtype != GPT_DTYPE_BF16))
+    return fail(nullptr, GPT_ERR_INVALID_ARG, "bad GEMM test arguments");
+  if (dtype == GPT_DTYPE_BF16 && (K % (kTcBK * ksplit) || N % 64 || lda % 8 || ldb % 8 || ldc % 4))
+    return fail(nullptr, GPT_ERR_UNSUPPORTED, "bf16 GEMM test: K %% (64 ksplit), N %% 64, lda/ldb %% 8 must be 0");
+  gpt h;
+  gpt_default_config(&h.cfg);
+  h.cfg.dtype = dtype;
+  h.stream = (cudaStream_t)cuda_stream;
+  cudaGetDevice(&h.device);
+  cudaDeviceGetAttribute(&h.num_sms, cudaDevAttrMultiProcessorCount, h.device);
+  OpDesc o;
+  int rc = gemm_op(&h, &o, M, N, K, {A, lda, a_mn != 0}, {B, ldb, b_mn != 0}, EPI_F32, ksplit);
+  if (rc != GPT_OK) { g_create_error = h.err; return rc; }
+  o.gemm.out = C; o.gemm.ldo = ldc; o.gemm.split_stride = (int64_t)M * ldc;
+  Builder bld{&h};
+  bld.add(o, {});
+  h.D = Dims{1, 64, 1, 64, 64, 64, 1, 1, 1};
+  Bump mb;
+  const size_t o_tasks = mb.take(h.tasks.size() * sizeof(TaskDesc));
+  const size_t o_ops = mb.take(sizeof(OpDesc));
+  const size_t o_maps = mb.take(std::max<size_t>(1, h.tmaps.size()) * 128);
+  const size_t o_ctr = mb.take(sizeof(unsigned long long));
+  const size_t o_tic = mb.take(sizeof(unsigned long long));
+  const size_t o_err = mb.take(4 * sizeof(uint32_t));
+  const size_t o_loss = mb.take(sizeof(float));
+  h.meta_bytes = mb.off;
+  if (cudaMalloc(&h.meta, h.meta_bytes) != cudaSuccess) { cudaGetLastError(); h.meta = nullptr; return fail(nullptr, GPT_ERR_OOM, "cudaMalloc failed"); }
+  h.d_tasks = reinterpret_cast<TaskDesc*>(h.meta + o_tasks);
+  h.d_ops = reinterpret_cast<OpDesc*>(h.meta + o_ops);
+  h.d_tmaps = h.meta + o_maps;
+  h.d_counters = reinterpret_cast<unsigned long long*>(h.meta + o_ctr);
+  h.d_ticket = reinterpret_cast<unsigned long long*>(h.meta + o_tic);
+  h.d_err = reinterpret_cast<uint32_t*>(h.meta + o_err);
+  h.loss_dev = reinterpret_cast<float*>(h.meta + o_loss);
+  int result = GPT_OK;
+  do {
+    if (cudaMallocHost(&h.h_status, sizeof(gpt::Status)) != cudaSuccess) { result = GPT_ERR_OOM; break; }
+    if (cudaMemcpyAsync(h.d_tasks, h.tasks.data(), h.tasks.size() * sizeof(TaskDesc), cudaMemcpyHostToDevice, h.stream) ||
+        cudaMemcpyAsync(h.d_ops, h.ops.data(), sizeof(OpDesc), cudaMemcpyHostToDevice, h.stream)) { result = GPT_ERR_CUDA; break; }
+    bool bad = false;
+    for (size_t i = 0; i < h.tmaps.size(); ++i)
+      bad |= cudaMemcpyAsync(static_cast<uint8_t*>(h.d_tmaps) + 128 * i, h.tmaps[i].data(), 128, cudaMemcpyHostToDevice, h.stream) != cudaSuccess;
+    if (bad) { result = GPT_ERR_CUDA; break; }
+    h.kernel = dtype == GPT_DTYPE_BF16 ? step_kernel_bf16() : step_kernel_fp32();
+    h.smem_bytes = dtype == GPT_DTYPE_BF16 ? (size_t)kTcSmemBytes + 1024 : (size_t)(2 * 16 * (kSimtTile + 4) * 4) + 1024;
+    if (cudaFuncSetAttribute(h.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h.smem_bytes)) { result = GPT_ERR_CUDA; break; }
+    h.grid = h.num_sms;
+    if (reset_counters(&h) != GPT_OK) { result = GPT_ERR_CUDA; break; }
+    const int32_t dummy_tok = 0;
+    (void)dummy_tok;
+    result = launch_step(&h, reinterpret_cast<const int32_t*>(h.meta), reinterpret_cast<const int32_t*>(h.meta), nullptr);
+  } while (0);
+  if (result != GPT_OK) g_create_error = h.err.empty() ? std::string("GEMM test failed") : h.err;
+  cudaStreamSynchronize(h.stream);
+  cudaFree(h.meta);
+  h.meta = nullptr;
+  if (h.h_status) cudaFreeHost(h.h_status);
+  h.h_status = nullptr;
+  return result;
+}
+
+int gpt_init_params_host(const gpt_config* cfg, uint64_t seed, float* dst, size_t n) {
+  if (!cfg || !dst) return fail(nullptr, GPT_ERR_INVALID_ARG, "cfg and dst must be non-NULL");
+  std::string why;
+  int rc = validate(*cfg, &why);
+  if (rc != GPT_OK) return fail(nullptr, rc, "invalid config: %s", why.c_str());
+  gpt h;
+  h.cfg = *cfg;
+  build_table(&h);
+  if (n != h.nparams) return fail(nullptr, GPT_ERR_INVALID_ARG, "n must be %zu", h.nparams);
+  for (size_t t = 0; t < h.tensors.size(); ++t) {
+    const TensorInfo& ti = h.tensors[t];
+    const size_t cnt = (size_t)(ti.rows * ti.cols);
+    float* d = dst + ti.offset;
+    if (ti.init == INIT_NORMAL) normal_fill(d, cnt, seed, t);
+    else std::fill(d, d + cnt, ti.init == INIT_ONES ? 1.0f : 0.0f);
+  }
+  return GPT_OK;
+}
+
+int gpt_graph_describe(const gpt_config* cfg, int32_t num_sms, int64_t* n_tasks, int32_t* n_ops,
+                       gpt_task_info* tasks, int64_t max_tasks, int32_t* op_types, int32_t* op_tasks,
+                       int32_t max_ops) {
+  if (!cfg || !n_tasks || !n_ops) return fail(nullptr, GPT_ERR_INVALID_ARG, "NULL argument");
+  std::string why;
+  int rc = validate(*cfg, &why);
+  if (rc != GPT_OK) return fail(nullptr, rc, "invalid config: %s", why.c_str());
+  gpt h;
+  h.cfg = *cfg;
+  h.describe_only = true;
+  h.num_sms = num_sms > 0 ? num_sms : 148;
+  h.D = Dims{cfg->n_layer, cfg->d_model, cfg->n_head, cfg->d_model / cfg->n_head, cfg->d_mlp, cfg->vocab,
+             cfg->seq_len, cfg->batch, cfg->batch * cfg->seq_len};
+  build_table(&h);
+  const int ks = lm_ksplit_for(*cfg, h.num_sms);
+  const Layout Lo = make_layout(*cfg, h.nparams, ks);
+  h.params = h.grads = h.m = h.v = nullptr;  // addresses are never dereferenced here
+  rc = build_graph(&h, Lo, ks);
+  if (rc != GPT_OK) { g_create_error = h.err; return rc; }
+  *n_tasks = (int64_t)h.tasks.size();
+  *n_ops = (int32_t)h.ops.size();
+  if (tasks)
+    for (int64_t i = 0; i < std::min<int64_t>(max_tasks, (int64_t)h.tasks.size()); ++i) {
+      const TaskDesc& t = h.tasks[i];
+      tasks[i].op = t.op;
+      tasks[i].idx = t.idx;
+      tasks[i].nwait = t.nwait;
+      for (int w = 0; w < 3; ++w) {
+        tasks[i].wait_op[w] = w < t.nwait ? t.wait_ctr[w] : -1;
+        tasks[i].wait_need[w] = w < t.nwait ? (int32_t)t.wait_need[w] : 0;
+      }
+    }
+  for (int32_t i = 0; i < std::min<int32_t>(max_ops, (int32_t)h.ops.size()); ++i) {
+    if (op_types) op_types[i] = h.ops[i].type;
+    if (op_tasks) op_tasks[i] = h.ops[i].ntasks;
+  }
+  return GPT_OK;
+}
+
+int64_t gpt_task_budget(int64_t iterations, int64_t tasks_per_iteration) {
+  if (iterations < 0 || tasks_per_iteration < 0) return -1;
+  if (tasks_per_iteration != 0 && iterations > INT64_MAX / tasks_per_iteration) return -1;
+  return iterations * tasks_per_iteration;
+}
+
+}  // extern "C"

@@ -1,0 +1,177 @@
+// graph.h — task-graph descriptors shared by the host graph builder and the
+// persistent kernel.  Plain structs of device pointers and sizes.
+//
+// The step is a list of tasks in a topological (ticket) order.  A task names an
+// operation (an "op": one GEMM, one LayerNorm, the attention of one layer ...)
+// and its tile / block index within that op.  Every op owns a 64-bit completion
+// counter; a task may wait for up to kMaxWaits counters to reach
+// epoch * need (need = the producing op's task count), then runs, then adds 1
+// to its own op's counter with release semantics.  Dependencies only point to
+// earlier tickets, so with every block resident the graph cannot deadlock
+// ("How one persistent kernel runs three jobs": ticket counters, release
+// fences before the counter increments, acquire waits by dependents).
+#pragma once
+#include <stdint.h>
+
+namespace pgs {
+
+constexpr int kMaxWaits = 3;
+// tile shapes shared by the host graph builder and the kernels
+constexpr int kSimtTile = 64;             // SIMT GEMM: 64 x 64 tiles
+constexpr int kTcBM = 128;                // tensor-core GEMM: 128-row tiles
+constexpr int kTcBK = 64;                 // one 128-byte swizzle row of bf16
+constexpr int kTcStages = 4;
+constexpr int kTcStageA = kTcBM * kTcBK * 2;          // 16 KB
+constexpr int kTcStageB = 256 * kTcBK * 2;            // 32 KB (BN <= 256)
+constexpr int kTcStageBytes = kTcStageA + kTcStageB;  // 48 KB
+constexpr int kTcSmemBytes = kTcStages * kTcStageBytes;
+constexpr int kTmemCols = 256;            // one fp32 accumulator of up to 128 x 256
+constexpr int kThreads = 256;     // threads of every persistent block
+constexpr int kWarps = kThreads / 32;
+
+enum OpType : int32_t {
+  OP_EMBED = 0,      // x0 = wte[tok] + wpe[t]                       tasks: row blocks
+  OP_LN_FWD,         // y = LN(x); mean, rstd                        tasks: row blocks
+  OP_GEMM,           // C = A . B^T (+ epilogue)                     tasks: tiles
+  OP_ATTN_FWD,       // causal softmax(q k^T / sqrt d) v, LSE        tasks: (b, h, q block)
+  OP_CE,             // per-row loss; logits -> dlogits in place     tasks: row blocks
+  OP_LOSS,           // mean of the row losses                       tasks: 1
+  OP_LN_BWD,         // dres_out = dres_in + LN'(dy); dg/db partials tasks: row blocks
+  OP_COLSUM,         // dst[c] = sum_r src[r, c] (fixed order)        tasks: column chunks
+  OP_ATTN_BWD,       // dq, dk, dv of the causal attention           tasks: (b, h)
+  OP_EMBED_BWD_WTE,  // dwte[v] = sum_{n: tok[n] = v} dx0[n]         tasks: vocab blocks
+  OP_EMBED_BWD_WPE,  // dwpe[t] = sum_b dx0[b, t]                    tasks: position blocks
+  OP_ADAMW,          // AdamW on a contiguous parameter range        tasks: chunks
+  OP_NOP,            // scheduler test: no work                      tasks: any
+  OP_NUM_TYPES
+};
+
+enum Epilogue : int32_t {
+  EPI_STORE = 0,     // out(act)  = acc (+ bias)
+  EPI_RESID,         // out(f32)  = resid(f32) + acc (+ bias)
+  EPI_GELU,          // out(act)  = acc + bias ; out2(act) = GELU(acc + bias)
+  EPI_F32,           // out(f32)  = acc                   (dX partials, weight gradients)
+  EPI_GELU_BWD,      // out(act)  = acc * GELU'(aux(act))
+};
+
+struct GemmArgs {
+  int32_t M, N, K;          // C[M, N] = sum_k A(m, k) B(n, k)
+  int32_t BM, BN, BK;       // tile shape of one task
+  int32_t tiles_n, ksplit;  // tasks = tiles_m * tiles_n * ksplit
+  // element access for the SIMT path: A(m,k) = A[m*sam + k*sak], B(n,k) = B[n*sbn + k*sbk]
+  const void* A; int64_t sam, sak;
+  const void* B; int64_t sbn, sbk;
+  // tensor-core path: tensor-map indices and operand majorness (1 = MN-major)
+  int32_t a_map, b_map, a_mn, b_mn;
+  int32_t epi;
+  void* out;  int64_t ldo;   // with ksplit > 1 split s writes out + s * split_stride
+  int64_t split_stride;
+  void* out2; int64_t ldo2;
+  const float* bias;         // [N] or null
+  const float* resid; int64_t ldr;
+  const void* aux; int64_t ldaux;
+};
+
+struct LnFwdArgs {
+  const float* x; const float* g; const float* b;  // b may be null
+  void* y; float* mean; float* rstd;
+  int32_t rows, C, rows_per_task;
+  float eps;
+};
+
+struct LnBwdArgs {
+  const float* dy; int32_t dy_splits; int64_t dy_split_stride;  // dy = sum of splits
+  const float* x; const float* mean; const float* rstd; const float* g;
+  const float* dres_in;       // may be null
+  float* dres_out; void* dres_act;
+  float* dg_part; float* db_part;   // [tasks, C]; db_part may be null
+  int32_t rows, C, rows_per_task;
+};
+
+struct AttnArgs {
+  const void* qkv;  // act [B*T, 3C]: q | k | v, head h at columns h*d
+  void* o;          // act [B*T, C]
+  float* lse;       // [B, H, T]
+  const void* dout; // act [B*T, C]   (backward)
+  void* dqkv;       // act [B*T, 3C]  (backward)
+  float* scratch;   // backward accumulators
+  int32_t B, T, H, d, C, q_block;
+  float scale;
+};
+
+struct CeArgs {
+  void* logits;              // act [N, V], overwritten by dlogits
+  float* row_loss;           // [N]
+  int32_t N, V, rows_per_task;
+};
+
+struct LossArgs {
+  const float* row_loss; float* loss; int32_t N;
+};
+
+struct ColsumArgs {
+  const void* src; int32_t src_f32; int64_t ld;
+  int32_t rows, cols, cols_per_task;
+  float* dst;
+};
+
+struct EmbedArgs {
+  const float* wte; const float* wpe; float* x0;
+  const float* dx0; float* dwte; float* dwpe;
+  int32_t N, B, T, C, V, rows_per_task;
+};
+
+struct AdamArgs {
+  float* p; const float* g; float* m; float* v; uint16_t* shadow;  // shadow may be null
+  int64_t n; int64_t chunk;
+  float decay;   // 1 = apply weight decay
+};
+
+struct OpDesc {
+  int32_t type;
+  int32_t ntasks;
+  union {
+    GemmArgs gemm;
+    LnFwdArgs lnf;
+    LnBwdArgs lnb;
+    AttnArgs attn;
+    CeArgs ce;
+    LossArgs loss;
+    ColsumArgs colsum;
+    EmbedArgs emb;
+    AdamArgs adam;
+  };
+};
+
+struct TaskDesc {
+  int32_t op;
+  int32_t idx;                     // task index within its op
+  int32_t nwait;
+  int32_t wait_ctr[kMaxWaits];     // counter (= op) indices
+  uint32_t wait_need[kMaxWaits];   // tasks of that op (per epoch)
+  int32_t pad;
+};
+
+// Soft error bits (the step runs to its end, AdamW skips its update).
+constexpr uint32_t kSoftBadToken = 1u;
+constexpr uint32_t kSoftNonFinite = 2u;
+// Fatal error codes (blocks drain and exit).
+constexpr uint32_t kFatalTimeout = 1u;
+constexpr uint32_t kFatalMbarTimeout = 2u;
+
+struct KParams {
+  const TaskDesc* tasks; int64_t ntasks;
+  const OpDesc* ops;
+  unsigned long long* counters;
+  unsigned long long* ticket;
+  unsigned long long ticket_base;
+  unsigned long long epoch;        // 1-based step number of this launch
+  uint32_t* err;                   // [0] fatal code, [1] soft bits, [2] task of a fatal error, [3] counter
+  uint64_t timeout_ns;
+  int64_t skip_release;            // test hook: this task skips its release (-1 = none)
+  const void* tmaps;               // CUtensorMap[] (tensor-core path)
+  const int32_t* tokens; const int32_t* targets;
+  float lr, beta1, beta2, eps, wd, bc1, bc2;
+};
+
+}  // namespace pgs

@@ -1,0 +1,387 @@
+// tasks_rows.cuh — row-parallel and elementwise task bodies of the persistent
+// kernel: embedding, LayerNorm forward/backward, softmax cross-entropy with its
+// gradient, the loss reduction, column sums, embedding backward and AdamW.
+// Every body is executed by all kThreads threads of one block and uses a fixed
+// summation order, so a step is bitwise repeatable.
+#pragma once
+#include "device.cuh"
+
+namespace pgs {
+
+// x0[n] = wte[tok[n]] + wpe[n mod T]  (token + learned position embedding).
+template <typename act_t>
+__device__ inline void task_embed(const KParams& kp, const EmbedArgs& a, int idx) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = idx * a.rows_per_task, r1 = min(r0 + a.rows_per_task, a.N);
+  for (int r = r0 + warp; r < r1; r += kWarps) {
+    int tok = kp.tokens[r];
+    if (tok < 0 || tok >= a.V) {
+      if (lane == 0) set_soft(kp, kSoftBadToken);
+      tok = tok < 0 ? 0 : a.V - 1;
+    }
+    const float4* we = reinterpret_cast<const float4*>(a.wte + (int64_t)tok * a.C);
+    const float4* pe = reinterpret_cast<const float4*>(a.wpe + (int64_t)(r % a.T) * a.C);
+    float4* xo = reinterpret_cast<float4*>(a.x0 + (int64_t)r * a.C);
+    for (int c = lane; c < a.C / 4; c += 32) {
+      float4 u = we[c], w = pe[c];
+      xo[c] = make_float4(u.x + w.x, u.y + w.y, u.z + w.z, u.w + w.w);
+    }
+  }
+}
+
+// LayerNorm forward, one warp per row; lane holds columns lane + 32 i.
+// mean = sum x / C, var = sum (x - mean)^2 / C (biased), y = xhat g + b.
+template <typename act_t>
+__device__ inline void task_ln_fwd(const LnFwdArgs& a, int idx) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = idx * a.rows_per_task, r1 = min(r0 + a.rows_per_task, a.rows);
+  const int nper = a.C >> 5;  // C <= 1024
+  act_t* y = reinterpret_cast<act_t*>(a.y);
+  for (int r = r0 + warp; r < r1; r += kWarps) {
+    const float* x = a.x + (int64_t)r * a.C;
+    float v[32];
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < nper) { v[i] = x[i * 32 + lane]; s += v[i]; }
+    const float mean = warp_sum(s) / (float)a.C;
+    float q = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < nper) { float d = v[i] - mean; q += d * d; }
+    const float rstd = rsqrtf(warp_sum(q) / (float)a.C + a.eps);
+    act_t* yr = y + (int64_t)r * a.C;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < nper) {
+        const int c = i * 32 + lane;
+        float o = (v[i] - mean) * rstd * a.g[c];
+        if (a.b) o += a.b[c];
+        yr[c] = from_f<act_t>(o);
+      }
+    if (lane == 0) { a.mean[r] = mean; a.rstd[r] = rstd; }
+  }
+}
+
+// LayerNorm backward for a block of rows:
+//   dxhat = dy g; dx = rstd (dxhat - mean(dxhat) - xhat mean(dxhat xhat));
+//   dres_out = dres_in + dx (fp32 and act copies);
+//   dg_part[task] = sum_rows dy xhat, db_part[task] = sum_rows dy.
+template <typename act_t>
+__device__ inline void task_ln_bwd(const LnBwdArgs& a, int idx, float* smem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = idx * a.rows_per_task, r1 = min(r0 + a.rows_per_task, a.rows);
+  const int nper = a.C >> 5;
+  float pg[32], pb[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) { pg[i] = 0.f; pb[i] = 0.f; }
+  act_t* dact = reinterpret_cast<act_t*>(a.dres_act);
+  const float invC = 1.0f / (float)a.C;
+  for (int r = r0 + warp; r < r1; r += kWarps) {
+    const float mean = a.mean[r], rstd = a.rstd[r];
+    const float* x = a.x + (int64_t)r * a.C;
+    float dy[32], xh[32];
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < nper) {
+        const int c = i * 32 + lane;
+        float d = 0.f;
+        for (int s = 0; s < a.dy_splits; ++s) d += a.dy[s * a.dy_split_stride + (int64_t)r * a.C + c];
+        dy[i] = d;
+        xh[i] = (x[c] - mean) * rstd;
+        const float dxh = d * a.g[c];
+        s1 += dxh;
+        s2 += dxh * xh[i];
+        pg[i] += d * xh[i];
+        pb[i] += d;
+      }
+    s1 = warp_sum(s1) * invC;
+    s2 = warp_sum(s2) * invC;
+    float* out = a.dres_out + (int64_t)r * a.C;
+    const float* din = a.dres_in ? a.dres_in + (int64_t)r * a.C : nullptr;
+    act_t* oa = dact + (int64_t)r * a.C;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < nper) {
+        const int c = i * 32 + lane;
+        float dx = rstd * (dy[i] * a.g[c] - s1 - xh[i] * s2);
+        if (din) dx += din[c];
+        out[c] = dx;
+        oa[c] = from_f<act_t>(dx);
+      }
+  }
+  // fixed-order reduction of the per-warp partial sums
+  float* sg = smem;                 // [kWarps][C]
+  float* sb = smem + kWarps * a.C;  // [kWarps][C]
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (i < nper) {
+      sg[warp * a.C + i * 32 + lane] = pg[i];
+      sb[warp * a.C + i * 32 + lane] = pb[i];
+    }
+  __syncthreads();
+  for (int c = threadIdx.x; c < a.C; c += kThreads) {
+    float g = 0.f, b = 0.f;
+    for (int w = 0; w < kWarps; ++w) { g += sg[w * a.C + c]; b += sb[w * a.C + c]; }
+    a.dg_part[(int64_t)idx * a.C + c] = g;
+    if (a.db_part) a.db_part[(int64_t)idx * a.C + c] = b;
+  }
+}
+
+// Softmax cross-entropy of a block of rows, one warp per row:
+// lse = log sum_j exp z_j (max subtracted), loss_n = lse - z[t_n],
+// dz_j = (exp(z_j - lse) - [j = t_n]) / N written over the logits.
+template <typename act_t>
+__device__ inline void task_ce(const KParams& kp, const CeArgs& a, int idx) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = idx * a.rows_per_task, r1 = min(r0 + a.rows_per_task, a.N);
+  act_t* L = reinterpret_cast<act_t*>(a.logits);
+  const float invN = 1.0f / (float)a.N;
+  for (int r = r0 + warp; r < r1; r += kWarps) {
+    act_t* z = L + (int64_t)r * a.V;
+    int t = kp.targets[r];
+    if (t < 0 || t >= a.V) {
+      if (lane == 0) set_soft(kp, kSoftBadToken);
+      t = t < 0 ? 0 : a.V - 1;
+    }
+    float m = -INFINITY, s = 0.f;
+    for (int j = lane; j < a.V; j += 32) {
+      const float x = to_f<act_t>(z[j]);
+      if (x > m) { s = s * expf(m - x) + 1.0f; m = x; }
+      else s += expf(x - m);
+    }
+    const float M = warp_max(m);
+    s = (m == -INFINITY) ? 0.f : s * expf(m - M);
+    const float S = warp_sum(s);
+    const float lse = M + logf(S);
+    const float zt = to_f<act_t>(z[t]);
+    __syncwarp();
+    if (lane == 0) a.row_loss[r] = lse - zt;
+    for (int j = lane; j < a.V; j += 32) {
+      const float x = to_f<act_t>(z[j]);
+      float p = expf(x - lse);
+      if (j == t) p -= 1.0f;
+      z[j] = from_f<act_t>(p * invN);
+    }
+  }
+}
+
+// Vectorised variant for bf16 logits with V % 8 == 0: 16-byte loads, 4 in flight.
+__device__ __forceinline__ void bf16x8_to_f(const uint4& u, float* f) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = __bfloat1622float2(h[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+__device__ __forceinline__ uint4 f_to_bf16x8(const float* f) {
+  uint4 u;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  return u;
+}
+
+__device__ inline void task_ce_bf16_vec(const KParams& kp, const CeArgs& a, int idx) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = idx * a.rows_per_task, r1 = min(r0 + a.rows_per_task, a.N);
+  const float invN = 1.0f / (float)a.N;
+  const int nvec = a.V >> 3;
+  for (int r = r0 + warp; r < r1; r += kWarps) {
+    __nv_bfloat16* zr = reinterpret_cast<__nv_bfloat16*>(a.logits) + (int64_t)r * a.V;
+    uint4* z = reinterpret_cast<uint4*>(zr);
+    int t = kp.targets[r];
+    if (t < 0 || t >= a.V) {
+      if (lane == 0) set_soft(kp, kSoftBadToken);
+      t = t < 0 ? 0 : a.V - 1;
+    }
+    float m = -INFINITY, s = 0.f;
+    int j = lane;
+    for (; j + 96 < nvec; j += 128) {
+      uint4 u[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) u[q] = z[j + 32 * q];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float f[8];
+        bf16x8_to_f(u[q], f);
+        float lm = f[0];
+#pragma unroll
+        for (int e = 1; e < 8; ++e) lm = fmaxf(lm, f[e]);
+        if (lm > m) { s *= expf(m - lm); m = lm; }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s += expf(f[e] - m);
+      }
+    }
+    for (; j < nvec; j += 32) {
+      float f[8];
+      bf16x8_to_f(z[j], f);
+      float lm = f[0];
+#pragma unroll
+      for (int e = 1; e < 8; ++e) lm = fmaxf(lm, f[e]);
+      if (lm > m) { s *= expf(m - lm); m = lm; }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s += expf(f[e] - m);
+    }
+    const float M = warp_max(m);
+    s = (m == -INFINITY) ? 0.f : s * expf(m - M);
+    const float lse = M + logf(warp_sum(s));
+    const float zt = __bfloat162float(zr[t]);
+    __syncwarp();
+    if (lane == 0) a.row_loss[r] = lse - zt;
+    for (j = lane; j < nvec; j += 32) {
+      float f[8];
+      bf16x8_to_f(z[j], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float p = expf(f[e] - lse);
+        if (j * 8 + e == t) p -= 1.0f;
+        f[e] = p * invN;
+      }
+      z[j] = f_to_bf16x8(f);
+    }
+  }
+}
+
+// loss = (1/N) sum_n row_loss[n], fixed order; flags a non-finite loss.
+__device__ inline void task_loss(const KParams& kp, const LossArgs& a, float* smem) {
+  float s = 0.f;
+  for (int i = threadIdx.x; i < a.N; i += kThreads) s += a.row_loss[i];
+  smem[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = kThreads / 2; w > 0; w >>= 1) {
+    if ((int)threadIdx.x < w) smem[threadIdx.x] += smem[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const float loss = smem[0] / (float)a.N;
+    *a.loss = loss;
+    if (!isfinite(loss)) set_soft(kp, kSoftNonFinite);
+  }
+}
+
+// dst[c] = sum_r src[r, c] for a chunk of columns; warp w sums rows w, w+8, ...,
+// then the warps' partials are added in warp order.
+template <typename act_t>
+__device__ inline void task_colsum(const ColsumArgs& a, int idx, float* smem) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c0 = idx * a.cols_per_task;
+  const int ncol = min(a.cols_per_task, a.cols - c0);  // <= 64
+  float acc0 = 0.f, acc1 = 0.f;
+  const bool has0 = lane < ncol, has1 = lane + 32 < ncol;
+  if (a.src_f32) {
+    const float* src = reinterpret_cast<const float*>(a.src) + c0;
+    for (int r = warp; r < a.rows; r += kWarps) {
+      const float* row = src + (int64_t)r * a.ld;
+      if (has0) acc0 += row[lane];
+      if (has1) acc1 += row[lane + 32];
+    }
+  } else {
+    const act_t* src = reinterpret_cast<const act_t*>(a.src) + c0;
+    for (int r = warp; r < a.rows; r += kWarps) {
+      const act_t* row = src + (int64_t)r * a.ld;
+      if (has0) acc0 += to_f<act_t>(row[lane]);
+      if (has1) acc1 += to_f<act_t>(row[lane + 32]);
+    }
+  }
+  smem[warp * 64 + lane] = acc0;
+  smem[warp * 64 + lane + 32] = acc1;
+  __syncthreads();
+  if ((int)threadIdx.x < ncol) {
+    float s = 0.f;
+    for (int w = 0; w < kWarps; ++w) s += smem[w * 64 + threadIdx.x];
+    a.dst[c0 + threadIdx.x] = s;
+  }
+}
+
+// dwte[v] = sum over positions n with tok[n] = v of dx0[n] (in increasing n),
+// for a block of vocabulary rows; rows no token hit are written as zeros.
+__device__ inline void task_embed_bwd_wte(const KParams& kp, const EmbedArgs& a, int idx, int* stok) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int n = threadIdx.x; n < a.N; n += kThreads) {
+    int t = kp.tokens[n];
+    stok[n] = t < 0 ? 0 : (t >= a.V ? a.V - 1 : t);
+  }
+  __syncthreads();
+  const int v0 = idx * a.rows_per_task, v1 = min(v0 + a.rows_per_task, a.V);
+  const int nper = a.C >> 5;
+  for (int v = v0 + warp; v < v1; v += kWarps) {
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+    for (int n0 = 0; n0 < a.N; n0 += 32) {
+      const int n = n0 + lane;
+      unsigned mask = __ballot_sync(0xffffffffu, n < a.N && stok[n] == v);
+      while (mask) {
+        const int hit = n0 + __ffs(mask) - 1;
+        mask &= mask - 1;
+        const float* src = a.dx0 + (int64_t)hit * a.C;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < nper) acc[i] += src[i * 32 + lane];
+      }
+    }
+    float* dst = a.dwte + (int64_t)v * a.C;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < nper) dst[i * 32 + lane] = acc[i];
+  }
+}
+
+// dwpe[t] = sum_b dx0[b, t] for a block of positions.
+__device__ inline void task_embed_bwd_wpe(const EmbedArgs& a, int idx) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = idx * a.rows_per_task, t1 = min(t0 + a.rows_per_task, a.T);
+  for (int t = t0 + warp; t < t1; t += kWarps) {
+    for (int c = lane; c < a.C; c += 32) {
+      float s = 0.f;
+      for (int b = 0; b < a.B; ++b) s += a.dx0[((int64_t)b * a.T + t) * a.C + c];
+      a.dwpe[(int64_t)t * a.C + c] = s;
+    }
+  }
+}
+
+// AdamW on one chunk of a parameter tensor (decoupled weight decay first):
+// p *= 1 - lr wd; m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2;
+// p -= lr (m / bc1) / (sqrt(v / bc2) + eps); bf16 copy of p written if requested.
+__device__ inline void task_adamw(const KParams& kp, const AdamArgs& a, int idx) {
+  if (ld_volatile_u32(&kp.err[1]) & (kSoftBadToken | kSoftNonFinite)) return;
+  const int64_t lo = (int64_t)idx * a.chunk;
+  const int64_t hi = min(lo + a.chunk, a.n);
+  const float decay = 1.0f - kp.lr * kp.wd * a.decay;
+  const float b1 = kp.beta1, b2 = kp.beta2, ib1 = 1.0f - kp.beta1, ib2 = 1.0f - kp.beta2;
+  const float rbc1 = 1.0f / kp.bc1, rbc2 = 1.0f / kp.bc2;
+  float4* P = reinterpret_cast<float4*>(a.p);
+  const float4* G = reinterpret_cast<const float4*>(a.g);
+  float4* Mo = reinterpret_cast<float4*>(a.m);
+  float4* Vo = reinterpret_cast<float4*>(a.v);
+  for (int64_t i = lo / 4 + threadIdx.x; i < hi / 4; i += kThreads) {
+    float4 p = P[i], g = G[i], m = Mo[i], v = Vo[i];
+    float pp[4] = {p.x, p.y, p.z, p.w}, gg[4] = {g.x, g.y, g.z, g.w};
+    float mm[4] = {m.x, m.y, m.z, m.w}, vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      pp[e] *= decay;
+      mm[e] = b1 * mm[e] + ib1 * gg[e];
+      vv[e] = b2 * vv[e] + ib2 * gg[e] * gg[e];
+      const float mh = mm[e] * rbc1, vh = vv[e] * rbc2;
+      pp[e] -= kp.lr * mh / (sqrtf(vh) + kp.eps);
+    }
+    P[i] = make_float4(pp[0], pp[1], pp[2], pp[3]);
+    Mo[i] = make_float4(mm[0], mm[1], mm[2], mm[3]);
+    Vo[i] = make_float4(vv[0], vv[1], vv[2], vv[3]);
+    if (a.shadow) {
+      __nv_bfloat162 lo2 = __floats2bfloat162_rn(pp[0], pp[1]);
+      __nv_bfloat162 hi2 = __floats2bfloat162_rn(pp[2], pp[3]);
+      uint2 u;
+      u.x = *reinterpret_cast<uint32_t*>(&lo2);
+      u.y = *reinterpret_cast<uint32_t*>(&hi2);
+      reinterpret_cast<uint2*>(a.shadow)[i] = u;
+    }
+  }
+}
+
+}  // namespace pgs

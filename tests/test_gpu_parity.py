@@ -1,0 +1,243 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle, on a GPU.
+
+Tolerances: fp32 tiny config — per-step loss within 1e-4 relative, parameters
+within 1e-4 max-abs after 10 steps; bf16 configs — step-1 loss within 2e-3
+relative, per-tensor gradient cosine similarity >= 0.999, loss curve within 1%
+of the oracle's over the first 50 steps.
+"""
+
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import gpt_oracle as O
+from persistent_gpt_step_gb300 import binding as B
+from persistent_gpt_step_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from persistent_gpt_step_gb300 import build
+    build.build()
+    B.load()
+    torch.backends.cuda.matmul.allow_tf32 = False
+    yield
+
+
+def _dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _cos(a, b):
+    a = a.astype(np.float64).ravel()
+    b = b.astype(np.float64).ravel()
+    na, nb = np.linalg.norm(a), np.linalg.norm(b)
+    if na == 0 and nb == 0:
+        return 1.0
+    return float(a @ b / (na * nb))
+
+
+# ----------------------------------------------------------------- GEMM unit tests
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 64), (256, 192, 320), (384, 512, 128), (100, 64, 48)])
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1)])
+def test_gemm_fp32_simt(M, N, K, a_mn, b_mn):
+    g = torch.Generator(device="cuda").manual_seed(M + N + K)
+    Am = torch.randn(M, K, device="cuda", generator=g)
+    Bm = torch.randn(N, K, device="cuda", generator=g)
+    A = Am.t().contiguous() if a_mn else Am
+    Bt = Bm.t().contiguous() if b_mn else Bm
+    C = B.test_gemm(A, Bt, a_mn, b_mn, M, N, K)[0]
+    ref = Am.double() @ Bm.double().t()
+    assert torch.allclose(C.double(), ref, rtol=1e-4, atol=1e-4 * math.sqrt(K))
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (256, 768, 768), (384, 320, 512), (128, 64, 4096),
+                                   (640, 2304, 768)])
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1)])
+def test_gemm_bf16_tcgen05(M, N, K, a_mn, b_mn):
+    g = torch.Generator(device="cuda").manual_seed(M * 7 + N + K)
+    Am = torch.randn(M, K, device="cuda", generator=g).bfloat16()
+    Bm = torch.randn(N, K, device="cuda", generator=g).bfloat16()
+    A = Am.t().contiguous() if a_mn else Am
+    Bt = Bm.t().contiguous() if b_mn else Bm
+    C = B.test_gemm(A, Bt, a_mn, b_mn, M, N, K)[0]
+    ref = Am.double() @ Bm.double().t()
+    err = (C.double() - ref).abs().max().item()
+    assert err <= 1e-3 * math.sqrt(K), err
+
+
+def test_gemm_bf16_ksplit():
+    M, N, K, ks = 256, 256, 1024, 4
+    g = torch.Generator(device="cuda").manual_seed(3)
+    Am = torch.randn(M, K, device="cuda", generator=g).bfloat16()
+    Bm = torch.randn(K, N, device="cuda", generator=g).bfloat16()   # MN-major B
+    C = B.test_gemm(Am, Bm, 0, 1, M, N, K, ksplit=ks)
+    ref = Am.double() @ Bm.double()
+    assert (C.double().sum(0) - ref).abs().max().item() <= 1e-3 * math.sqrt(K)
+
+
+# ----------------------------------------------------------------- model parity
+
+def test_create_initialises_from_spec():
+    cfg = I.CONFIGS["small"]
+    with B.GPT(cfg, seed=77) as m:
+        got = m.params()
+        table = m.tensor_table()
+    ref = I.init_params(O.param_table(cfg), 77)
+    assert (got != ref).sum() <= 2
+    assert [(n, tuple(s)) for n, s, _ in table] == [(n, tuple(s)) for n, s, _ in O.param_table(cfg)]
+
+
+def test_tiny_fp32_parity_10_steps():
+    cfg = I.CONFIGS["tiny"]
+    seed = 1234
+    params = I.init_params(O.param_table(cfg), seed)
+    st = O.OracleState(cfg, params, dtype=np.float64)
+    with B.GPT(cfg, seed=seed) as m:
+        m.set_params(params)
+        for step in range(cfg.steps):
+            tok, tgt = I.batch(cfg, seed, step)
+            loss = m.train_step(_dev(tok), _dev(tgt))
+            ref = O.train_step(st, tok, tgt)
+            assert abs(loss - ref) <= 1e-4 * abs(ref), (step, loss, ref)
+            if step == 0:
+                g = m.grads()
+                for (name, shape, _), a, b in zip(O.param_table(cfg),
+                                                  O.param_views(cfg, g).values(),
+                                                  O.param_views(cfg, st.last_grad).values()):
+                    scale = max(np.abs(b).max(), 1e-6)
+                    assert np.abs(a - b).max() <= 1e-3 * scale, name
+        p = m.params()
+        mom, vel, nstep = m.opt_state()
+    assert nstep == cfg.steps
+    assert np.abs(p - st.params).max() <= 1e-4
+    assert np.abs(mom - st.m).max() <= 1e-4
+
+
+def _bf16_parity(cfg, seed, steps, oracle_dtype=np.float64):
+    params = I.init_params(O.param_table(cfg), seed)
+    st = O.OracleState(cfg, params, dtype=oracle_dtype)
+    losses, refs = [], []
+    with B.GPT(cfg, seed=seed) as m:
+        m.set_params(params)
+        for step in range(steps):
+            tok, tgt = I.batch(cfg, seed, step)
+            losses.append(m.train_step(_dev(tok), _dev(tgt)))
+            refs.append(O.train_step(st, tok, tgt))
+            if step == 0:
+                assert abs(losses[0] - refs[0]) <= 2e-3 * abs(refs[0]), (losses[0], refs[0])
+                g = m.grads()
+                bad = []
+                for name, a, b in zip(O.param_views(cfg, g).keys(), O.param_views(cfg, g).values(),
+                                      O.param_views(cfg, st.last_grad).values()):
+                    c = _cos(a, b)
+                    if c < 0.999:
+                        bad.append((name, c))
+                assert not bad, bad
+    return np.array(losses), np.array(refs)
+
+
+def test_small_bf16_parity_50_steps():
+    cfg = I.CONFIGS["small"]
+    losses, refs = _bf16_parity(cfg, 1234, 50)
+    rel = np.abs(losses - refs) / np.abs(refs)
+    assert rel.max() <= 0.01, rel.max()
+    assert losses[-1] < losses[0]
+
+
+def test_main_bf16_parity_first_steps():
+    """The 162M workload, in the launch configuration the benchmark times: step-1
+    loss and per-tensor gradient cosine, then two more steps of the loss curve
+    (the oracle runs in fp32 here to bound its CPU time)."""
+    cfg = I.CONFIGS["main"]
+    losses, refs = _bf16_parity(cfg, 1234, 3, oracle_dtype=np.float32)
+    assert (np.abs(losses - refs) / np.abs(refs)).max() <= 0.01
+
+
+# ----------------------------------------------------------------- properties
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_steps_are_bitwise_repeatable(name):
+    cfg = I.CONFIGS[name]
+    runs = []
+    for _ in range(2):
+        with B.GPT(cfg, seed=5) as m:
+            ls = [m.train_step(*(_dev(x) for x in I.batch(cfg, 5, s))) for s in range(4)]
+            runs.append((ls, m.params()))
+    assert runs[0][0] == runs[1][0]
+    assert np.array_equal(runs[0][1], runs[1][1])
+
+
+def test_host_entry_point_matches_device_entry_point():
+    cfg = I.CONFIGS["tiny"]
+    tok, tgt = I.batch(cfg, 3, 0)
+    with B.GPT(cfg, seed=3) as a, B.GPT(cfg, seed=3) as b:
+        la = a.train_step(_dev(tok), _dev(tgt))
+        lb = b.train_step(tok, tgt)
+        assert la == lb
+        assert np.array_equal(a.params(), b.params())
+
+
+def test_checkpoint_resume_is_bitwise():
+    cfg = I.CONFIGS["small"]
+    seed = 11
+    batches = [I.batch(cfg, seed, s) for s in range(6)]
+    with B.GPT(cfg, seed=seed) as a:
+        la = [a.train_step(_dev(t), _dev(g)) for t, g in batches]
+        pa = a.params()
+    with B.GPT(cfg, seed=seed) as b:
+        lb = [b.train_step(_dev(t), _dev(g)) for t, g in batches[:3]]
+        p, (m, v, step) = b.params(), b.opt_state()
+    with B.GPT(cfg, seed=999) as c:
+        c.set_params(p)
+        c.set_opt_state(m, v, step)
+        lb += [c.train_step(_dev(t), _dev(g)) for t, g in batches[3:]]
+        pc = c.params()
+    assert la == lb
+    assert np.array_equal(pa, pc)
+
+
+def test_bad_token_skips_update():
+    cfg = I.CONFIGS["tiny"]
+    tok, tgt = I.batch(cfg, 1, 0)
+    tok = tok.copy()
+    tok[1, 5] = cfg.vocab + 3
+    with B.GPT(cfg, seed=1) as m:
+        p0 = m.params()
+        with pytest.raises(B.GptError) as e:
+            m.train_step(_dev(tok), _dev(tgt))
+        assert e.value.name == "BAD_TOKEN"
+        assert np.array_equal(m.params(), p0)
+        assert m.opt_state()[2] == 0
+        tok[1, 5] = 0
+        m.train_step(_dev(tok), _dev(tgt))      # the handle stays usable
+        assert m.opt_state()[2] == 1
+
+
+def test_skipped_release_times_out_without_hanging():
+    """Fault injection on the host side of the protocol: one task does not
+    publish its completion, so its dependents' bounded waits expire; the step
+    returns TIMEOUT, the context stays usable and gpt_reset recovers."""
+    cfg = I.CONFIGS["tiny"]
+    tok, tgt = I.batch(cfg, 2, 0)
+    with B.GPT(cfg, seed=2, wait_timeout_ms=200) as m:
+        m.debug_skip_release(0)
+        with pytest.raises(B.GptError) as e:
+            m.train_step(_dev(tok), _dev(tgt))
+        assert e.value.name == "TIMEOUT"
+        with pytest.raises(B.GptError) as e:
+            m.train_step(_dev(tok), _dev(tgt))
+        assert e.value.name == "POISONED"
+        m.reset()
+        loss = m.train_step(_dev(tok), _dev(tgt))
+        assert math.isfinite(loss)
+    torch.cuda.synchronize()

@@ -1,0 +1,231 @@
+"""Host-side tests of libgpt.so and the input generators (no GPU needed)."""
+
+import ctypes
+import os
+import random
+import re
+import threading
+import time
+
+import numpy as np
+import pytest
+
+from oracle import gpt_oracle as O
+from persistent_gpt_step_gb300 import binding as B
+from persistent_gpt_step_gb300 import build as build_mod
+from persistent_gpt_step_gb300 import inputs as I
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gpt.h")
+GOLD = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_mod.build()
+    return B.load()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(gpt_[a-z_0-9]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_every_declared_function_is_exported(lib):
+    names = _declared_functions()
+    assert len(names) >= 20
+    for n in names:
+        assert hasattr(lib, n), n
+    bound = {s[0] for s in B.SIGNATURES}
+    assert set(names) == bound, set(names) ^ bound
+
+
+def test_config_struct_matches_header(lib):
+    text = open(HEADER).read()
+    body = re.search(r"typedef struct gpt_config \{(.*?)\} gpt_config;", text, re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    fields = []
+    for decl in body.split(";"):
+        decl = decl.strip()
+        if not decl:
+            continue
+        typ, names = decl.split(None, 1)
+        fields += [(typ, n.strip()) for n in names.split(",")]
+    assert [n for _, n in fields] == [f[0] for f in B.gpt_config._fields_]
+    assert ctypes.sizeof(B.gpt_config) == 4 * len(fields)
+
+
+def test_default_config_is_main_workload(lib):
+    c = B.gpt_config()
+    lib.gpt_default_config(ctypes.byref(c))
+    main = I.CONFIGS["main"]
+    for f in ("n_layer", "d_model", "n_head", "d_mlp", "vocab", "seq_len", "batch"):
+        assert getattr(c, f) == getattr(main, f)
+    assert c.dtype == B.DTYPE_BF16 and c.tie_embeddings == 0 and c.gelu_tanh == 1
+    assert abs(c.lr - 6e-4) < 1e-9 and abs(c.beta2 - 0.95) < 1e-7 and abs(c.weight_decay - 0.1) < 1e-7
+
+
+def test_task_budget_overflow_golden(lib):
+    g = {}
+    for line in open(os.path.join(GOLD, "scheduler_overflow.txt")):
+        if line.strip() and not line.startswith("#"):
+            k, v = line.split()
+            g[k] = int(v)
+    prod = B.task_budget(g["iterations"], g["tasks_per_iteration"])
+    assert prod == g["product"]
+    # the page's 32-bit arithmetic, reproduced: this is the failure the 64-bit budget avoids
+    assert prod % (1 << 32) == g["wrapped"]
+    assert (prod % (1 << 32)) // g["tasks_per_iteration"] == g["tokens_before_stop"]
+    assert B.task_budget(1 << 62, 4) == -1
+    assert B.task_budget(-1, 3) == -1
+
+
+def test_arena_bytes_and_invalid_configs(lib):
+    for name in ("tiny", "small", "main"):
+        c = B.make_config(I.CONFIGS[name])
+        assert lib.gpt_arena_bytes(ctypes.byref(c)) > 0
+    bad = B.make_config(I.CONFIGS["tiny"].replace(d_model=63))
+    assert lib.gpt_arena_bytes(ctypes.byref(bad)) == 0
+    bad = B.make_config(I.CONFIGS["small"].replace(seq_len=100))  # bf16: B*T % 128
+    assert lib.gpt_arena_bytes(ctypes.byref(bad)) == 0
+
+
+def test_create_without_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    c = B.make_config(I.CONFIGS["tiny"])
+    h = ctypes.c_void_p()
+    rc = lib.gpt_create(ctypes.byref(c), 1, None, None, 0, ctypes.byref(h))
+    assert rc in (-2, -8)
+    assert h.value is None
+    assert lib.gpt_last_error(None)
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_library_tensor_table_and_host_init_match_spec(lib, name):
+    """The C++ implementation of the init spec equals the test-side one."""
+    cfg = I.CONFIGS[name]
+    n = O.num_params(cfg)
+    got = B.init_params_host(cfg, 1234, n)
+    ref = I.init_params(O.param_table(cfg), 1234)
+    diff = got != ref
+    # double-precision log/cos may differ in the last ulp between libm builds;
+    # that moves an fp32 weight by one ulp at most, and almost never
+    assert diff.sum() <= 2
+    if diff.any():
+        ulp = np.abs(got.view(np.int32)[diff].astype(np.int64) - ref.view(np.int32)[diff].astype(np.int64))
+        assert ulp.max() <= 1
+
+
+def test_init_statistics():
+    w = I.normal_fp32(42, 3, 200000)
+    assert abs(w.mean()) < 0.02 * 0.02
+    assert abs(w.std() - 0.02) < 0.02 * 0.01
+
+
+def test_splitmix64_published_vector():
+    lines = [l.strip() for l in open(os.path.join(GOLD, "splitmix64.txt"))
+             if l.strip() and not l.startswith("#")]
+    seed = int(lines[0].split()[1])
+    want = [int(x, 16) for x in lines[1:]]
+    got = [int(v) for v in I.splitmix64(seed, np.arange(len(want)))]
+    assert got == want
+
+
+def test_token_batches():
+    cfg = I.CONFIGS["small"]
+    tok, tgt = I.batch(cfg, 5, 3)
+    assert tok.shape == (cfg.batch, cfg.seq_len) and tok.dtype == np.int32
+    assert np.array_equal(tok[:, 1:], tgt[:, :-1])       # targets = inputs shifted by one
+    assert tok.min() >= 0 and tok.max() < cfg.vocab
+    t2, _ = I.batch(cfg, 5, 3)
+    assert np.array_equal(tok, t2)
+    t3, _ = I.batch(cfg, 5, 4)
+    assert not np.array_equal(tok, t3)
+
+
+def test_zipf_frequencies():
+    V, s = 1000, 1.1
+    blk = I.token_block(9, 0, 64, 4096, V, "zipf", s)
+    counts = np.bincount(blk.ravel(), minlength=V)[:10].astype(float)
+    w = np.arange(1, V + 1, dtype=float) ** -s
+    pmf = w / w.sum()
+    n = blk.size
+    assert np.all(np.abs(counts - n * pmf[:10]) < 5 * np.sqrt(n * pmf[:10]))
+    uni = I.token_block(9, 0, 64, 4096, V, "uniform")
+    assert abs(np.bincount(uni.ravel(), minlength=V).std() / (uni.size / V) - 1 / np.sqrt(uni.size / V)) < 0.05
+
+
+# ----------------------------------------------------------------- task graph
+
+@pytest.mark.parametrize("name", ["tiny", "small", "main"])
+def test_task_graph_is_topological(lib, name):
+    tasks, types, ntk = B.describe_graph(I.CONFIGS[name])
+    first = {}
+    counts = {}
+    for i, (op, idx, waits) in enumerate(tasks):
+        first.setdefault(op, i)
+        counts[op] = counts.get(op, 0) + 1
+        for wop, need in waits:
+            assert wop < op or first[wop] < first[op]
+            assert need == ntk[wop]
+    assert [counts[o] for o in range(len(types))] == ntk
+    # every parameter tensor gets exactly one AdamW op
+    n_adam = sum(1 for t in types if t == 11)
+    assert n_adam == len(O.param_table(I.CONFIGS[name]))
+
+
+def _simulate(tasks, ntk, n_blocks, skip=None, timeout=5.0, seed=0):
+    """Blocks as threads running the ticket loop with random delays."""
+    counters = [0] * len(ntk)
+    ticket = [0]
+    lock = threading.Lock()
+    done = []
+    failed = []
+    rng = random.Random(seed)
+
+    def block():
+        while True:
+            with lock:
+                t = ticket[0]
+                ticket[0] += 1
+            if t >= len(tasks) or failed:
+                return
+            op, idx, waits = tasks[t]
+            t0 = time.time()
+            for wop, need in waits:
+                while counters[wop] < need:
+                    if time.time() - t0 > timeout:
+                        failed.append(t)
+                        return
+                    time.sleep(0)
+            if rng.random() < 0.01:
+                time.sleep(0.001)
+            with lock:
+                done.append(t)
+                if t != skip:
+                    counters[op] += 1
+
+    th = [threading.Thread(target=block) for _ in range(n_blocks)]
+    for x in th:
+        x.start()
+    for x in th:
+        x.join()
+    return counters, done, failed
+
+
+def test_scheduler_simulation_completes_tiny(lib):
+    tasks, types, ntk = B.describe_graph(I.CONFIGS["tiny"])
+    counters, done, failed = _simulate(tasks, ntk, 16)
+    assert not failed
+    assert counters == ntk
+    assert sorted(done) == list(range(len(tasks)))
+
+
+def test_scheduler_simulation_skipped_release_times_out(lib):
+    tasks, types, ntk = B.describe_graph(I.CONFIGS["tiny"])
+    counters, done, failed = _simulate(tasks, ntk, 8, skip=0, timeout=0.5)
+    assert failed and counters[0] == ntk[0] - 1

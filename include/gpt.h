@@ -237,6 +237,38 @@ int gpt_graph_describe(const gpt_config* cfg, int32_t num_sms, int64_t* n_tasks,
                        int32_t max_ops);
 
 /*
+ * Training step that allocates nothing (the pages have no counterpart: this is
+ * an addition of this library).  It is meant for callers that cannot allocate
+ * device memory: code that issues the step while a stream is being captured
+ * into a CUDA graph, runtimes whose device memory belongs to a pool that does
+ * not allow side allocations, and hosts that must not allocate after start-up.
+ * The same persistent kernel runs the same task graph as gpt_train_step, with
+ * GPT_DTYPE_FP32 arithmetic; every piece of scratch (gradients, activations,
+ * the task graph, counters, error words) lives in one 16 MiB file-scope device
+ * array that every GPU which loads libgpt.so holds until the process exits.
+ * No cudaMalloc, cudaFree, pinned or library allocation is made; the task list
+ * is built in ordinary host heap memory and copied into the array.
+ *   cfg: GPT_DTYPE_FP32 only; models whose scratch exceeds 16 MiB (the tiny
+ *     configuration needs about 7 MiB) are rejected with GPT_ERR_INVALID_ARG
+ *     and a message giving the size they need.
+ *   params, m, v: DEVICE fp32 [gpt_num_params] in the canonical order: the
+ *     parameters and AdamW moments, read and updated in place.
+ *   step: AdamW updates applied so far (bias correction uses step + 1); on
+ *     GPT_OK the caller counts one more.
+ *   tokens, targets: DEVICE int32 [batch, seq_len]; loss: HOST float*, may be
+ *     NULL.  Runs on cuda_stream and synchronises it.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit: make that
+ * first call before any stream capture.  Every call shares the one array and
+ * starts by rewriting its graph and zeroing its counters, so calls whose work
+ * overlaps on the GPU (other threads, other streams) race and must not be made.
+ * Errors as gpt_train_step (BAD_TOKEN / NONFINITE leave params, m, v as they
+ * were), plus UNSUPPORTED for bf16; text via gpt_last_error(NULL).
+ */
+int gpt_train_step_static(const gpt_config* cfg, float* params, float* m, float* v, int64_t step,
+                          const int32_t* tokens, const int32_t* targets, float* loss, void* cuda_stream);
+
+/*
  * Test hook: one GEMM C[M,N] = sum_k A(m,k) B(n,k), fp32 output, run as a
  * one-task graph of the same persistent kernel (SIMT fp32 path for
  * GPT_DTYPE_FP32, tcgen05/TMA path for GPT_DTYPE_BF16).  A, B, C are DEVICE

@@ -79,6 +79,8 @@ SIGNATURES = [
     ("gpt_graph_describe", c_int, [POINTER(gpt_config), c_int32, POINTER(c_int64), POINTER(c_int32),
                                    POINTER(gpt_task_info), c_int64, POINTER(c_int32), POINTER(c_int32),
                                    c_int32]),
+    ("gpt_train_step_static", c_int, [POINTER(gpt_config), c_void_p, c_void_p, c_void_p, c_int64,
+                                      c_void_p, c_void_p, POINTER(c_float), c_void_p]),
     ("gpt_test_gemm", c_int, [c_int32, c_int32, c_int32, c_int32, c_void_p, c_int64, c_int32,
                               c_void_p, c_int64, c_int32, c_void_p, c_int64, c_int32, c_void_p]),
 ]
@@ -321,3 +323,19 @@ def describe_graph(cfg, num_sms: int = 148):
         raise GptError(rc, lib.gpt_last_error(None).decode())
     out = [(t.op, t.idx, [(t.wait_op[w], t.wait_need[w]) for w in range(t.nwait)]) for t in tasks]
     return out, list(types), list(ntk)
+
+
+def train_step_static(cfg, params, m, v, step: int, tokens, targets, stream=None,
+                      wait_timeout_ms: int = 2000) -> float:
+    """gpt_train_step_static on CUDA tensors (fp32 params/m/v updated in place)."""
+    import torch
+    lib = load()
+    c = make_config(cfg, wait_timeout_ms)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    loss = c_float()
+    rc = lib.gpt_train_step_static(byref(c), c_void_p(params.data_ptr()), c_void_p(m.data_ptr()),
+                                   c_void_p(v.data_ptr()), c_int64(step), c_void_p(tokens.data_ptr()),
+                                   c_void_p(targets.data_ptr()), byref(loss), c_void_p(s.cuda_stream))
+    if rc != GPT_OK:
+        raise GptError(rc, lib.gpt_last_error(None).decode())
+    return float(loss.value)

@@ -10,6 +10,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <thread>
 #include <vector>
@@ -1142,3 +1143,129 @@ int64_t gpt_task_budget(int64_t iterations, int64_t tasks_per_iteration) {
 }
 
 }  // extern "C"
+
+// ============================================================================
+// Training step without any allocation.
+//
+// For callers that cannot allocate device memory themselves or through us:
+// code that runs while a stream is being captured into a CUDA graph (where an
+// allocation would break or serialise the capture), runtimes whose memory is
+// owned by a pool that forbids side allocations, and embedded or real-time
+// hosts that must not allocate after start-up.  The step's scratch (gradients,
+// activations, the task graph, counters and error words) lives in one
+// file-scope device array; the caller passes parameters, AdamW moments, tokens
+// and targets.  Only the fp32 arithmetic is offered (the bf16 path would have to
+// rebuild its bf16 weight copy inside the array on every call), and only models
+// whose scratch fits in kStaticScratchBytes.
+// ============================================================================
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t)16 << 20;  // 16 MiB on every GPU that loads libgpt.so
+constexpr int kStaticMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mu;
+uint8_t* g_static_ptr[kStaticMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device (looked up once per
+// device; the host-side name of the array is not a device address).
+int static_scratch_address(int device, uint8_t** out) {
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[device]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(nullptr, GPT_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed: %s",
+                  cudaGetErrorString(e));
+    g_static_ptr[device] = static_cast<uint8_t*>(p);
+  }
+  *out = g_static_ptr[device];
+  return GPT_OK;
+}
+
+}  // namespace
+
+extern "C" int gpt_train_step_static(const gpt_config* cfg, float* params, float* m, float* v, int64_t step,
+                                     const int32_t* tokens, const int32_t* targets, float* loss,
+                                     void* cuda_stream) {
+  g_create_error.clear();
+  if (!cfg || !params || !m || !v || !tokens || !targets || step < 0)
+    return fail(nullptr, GPT_ERR_INVALID_ARG, "cfg, params, m, v, tokens, targets must be non-NULL; step >= 0");
+  std::string why;
+  int rc = validate(*cfg, &why);
+  if (rc != GPT_OK) return fail(nullptr, rc, "invalid config: %s", why.c_str());
+  if (cfg->dtype != GPT_DTYPE_FP32)
+    return fail(nullptr, GPT_ERR_UNSUPPORTED, "gpt_train_step_static supports GPT_DTYPE_FP32 only");
+  gpt h;
+  h.cfg = *cfg;
+  if (!h.cfg.wait_timeout_ms) h.cfg.wait_timeout_ms = 2000;
+  h.D = Dims{cfg->n_layer, cfg->d_model, cfg->n_head, cfg->d_model / cfg->n_head, cfg->d_mlp, cfg->vocab,
+             cfg->seq_len, cfg->batch, cfg->batch * cfg->seq_len};
+  h.stream = (cudaStream_t)cuda_stream;
+  if (cudaGetDevice(&h.device) != cudaSuccess) return fail(nullptr, GPT_ERR_CUDA, "no CUDA device");
+  if (h.device < 0 || h.device >= kStaticMaxDevices)
+    return fail(nullptr, GPT_ERR_UNSUPPORTED, "device ordinal %d >= %d", h.device, kStaticMaxDevices);
+  cudaDeviceGetAttribute(&h.num_sms, cudaDevAttrMultiProcessorCount, h.device);
+  build_table(&h);
+  const int lm_ks = lm_ksplit_for(h.cfg, h.num_sms);
+  const Layout Lo = make_layout(h.cfg, h.nparams, lm_ks);
+  uint8_t* scratch = nullptr;
+  rc = static_scratch_address(h.device, &scratch);
+  if (rc != GPT_OK) return rc;
+  // scratch: the arena layout (its params/m/v regions stay unused: the
+  // caller's buffers take their place), then the graph and the sync words
+  h.arena = scratch;
+  h.params = params;
+  h.m = m;
+  h.v = v;
+  h.grads = reinterpret_cast<float*>(scratch + Lo.grads);
+  h.loss_dev = reinterpret_cast<float*>(scratch + Lo.loss);
+  rc = build_graph(&h, Lo, lm_ks);
+  if (rc != GPT_OK) { g_create_error = h.err; return rc; }
+  Bump mb;
+  mb.off = Lo.total;
+  const size_t o_tasks = mb.take(h.tasks.size() * sizeof(TaskDesc));
+  const size_t o_ops = mb.take(h.ops.size() * sizeof(OpDesc));
+  const size_t o_ctr = mb.take(h.ops.size() * sizeof(unsigned long long));
+  const size_t o_tic = mb.take(sizeof(unsigned long long));
+  const size_t o_err = mb.take(4 * sizeof(uint32_t));
+  if (mb.off > kStaticScratchBytes)
+    return fail(nullptr, GPT_ERR_INVALID_ARG,
+                "gpt_train_step_static: this model needs %zu bytes of scratch, above the %zu-byte static maximum",
+                mb.off, kStaticScratchBytes);
+  h.d_tasks = reinterpret_cast<TaskDesc*>(scratch + o_tasks);
+  h.d_ops = reinterpret_cast<OpDesc*>(scratch + o_ops);
+  h.d_counters = reinterpret_cast<unsigned long long*>(scratch + o_ctr);
+  h.d_ticket = reinterpret_cast<unsigned long long*>(scratch + o_tic);
+  h.d_err = reinterpret_cast<uint32_t*>(scratch + o_err);
+  gpt::Status status{};
+  h.h_status = &status;  // pageable host memory: no pinned allocation
+  h.opt_step = step;
+  h.launches = 0;
+  h.kernel = step_kernel_fp32();
+  h.smem_bytes = smem_needed(&h);
+  int per_sm = 0;
+  cudaError_t e = cudaFuncSetAttribute(h.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h.smem_bytes);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, h.kernel, kThreads, h.smem_bytes);
+  if (e == cudaSuccess && per_sm < 1) e = cudaErrorInvalidConfiguration;
+  if (e == cudaSuccess) {
+    h.grid = h.num_sms;
+    // the array keeps the previous call's contents: the graph is rewritten and
+    // every counter, the ticket and the error words restart from zero
+    e = cudaMemcpyAsync(h.d_tasks, h.tasks.data(), h.tasks.size() * sizeof(TaskDesc), cudaMemcpyHostToDevice,
+                        h.stream);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(h.d_ops, h.ops.data(), h.ops.size() * sizeof(OpDesc), cudaMemcpyHostToDevice, h.stream);
+    if (e == cudaSuccess)
+      e = cudaMemsetAsync(scratch + o_ctr, 0, mb.off - o_ctr, h.stream);
+  }
+  if (e != cudaSuccess) {
+    h.h_status = nullptr;
+    return fail(nullptr, GPT_ERR_CUDA, "gpt_train_step_static set-up failed: %s", cudaGetErrorString(e));
+  }
+  rc = launch_step(&h, tokens, targets, loss);
+  if (rc != GPT_OK) g_create_error = h.err;
+  h.h_status = nullptr;
+  return rc;
+}

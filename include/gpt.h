@@ -75,9 +75,10 @@ extern "C" {
  * the LM head), ln_bias 1, tie_embeddings 0 (the only value supported),
  * gelu_tanh 1 (tanh approximation; 0 = erf form), eps 1e-8, ln_eps 1e-5,
  * wd_on_1d 0 (weight decay on 2-D tensors only), constant learning rate.
- * Limits: d_model = n_head * head_dim with head_dim 16 or 64 (bf16: 64);
- * seq_len <= 1024; for GPT_DTYPE_BF16 d_model, d_mlp and 3*d_model must be
- * multiples of 64 and batch*seq_len a multiple of 128.
+ * Limits: d_model a multiple of 64 and <= 1024, d_mlp a multiple of 64,
+ * head_dim = d_model / n_head <= 128, seq_len <= 1024, batch*seq_len <= 8192;
+ * for GPT_DTYPE_BF16 also head_dim == 64, seq_len a multiple of 128, vocab a
+ * multiple of 64 and batch*seq_len a multiple of 128.
  */
 typedef struct gpt_config {
   int32_t n_layer, d_model, n_head, d_mlp, vocab, seq_len, batch;
@@ -188,6 +189,19 @@ int gpt_reset(gpt* h);
  * blocks) the persistent kernel is launched with.  Any pointer may be NULL. */
 int gpt_graph_info(const gpt* h, int64_t* n_tasks, int32_t* grid, int32_t* block);
 
+/*
+ * In-kernel trace (observability, after the pages' per-launch device
+ * timestamps: "Coppelius training on the RTX 3090", section "Where a step's
+ * time goes").  gpt_trace_enable(h, 1) allocates a device buffer of 32 bytes
+ * per task; every later step records, per task (ticket order), four uint64:
+ * claim time, start time (after its dependency waits), end time (after its
+ * release), all %globaltimer nanoseconds, and the SM id that ran it.
+ * gpt_get_trace copies the last step's record to HOST dst[0..4*n_tasks).
+ * gpt_trace_enable(h, 0) frees the buffer.
+ */
+int gpt_trace_enable(gpt* h, int32_t on);
+int gpt_get_trace(gpt* h, uint64_t* dst, size_t n);
+
 /* Device time of the last step's kernel launch in milliseconds, from CUDA
  * events the library records on the handle's stream around the launch. */
 int gpt_last_kernel_ms(const gpt* h, float* ms);
@@ -230,7 +244,8 @@ typedef struct gpt_task_info {
  * op_types[] / op_tasks[], may be NULL).  Operation types are the kernel's
  * OpType values (0 embed, 1 LN forward, 2 GEMM, 3 attention forward, 4 cross-
  * entropy, 5 loss, 6 LN backward, 7 column sum, 8 attention backward,
- * 9 token-embedding backward, 10 position-embedding backward, 11 AdamW).
+ * 9 token-embedding backward, 10 position-embedding backward, 11 AdamW,
+ * 12 attention-backward pre-pass, 13 attention dK/dV, 14 attention dQ).
  */
 int gpt_graph_describe(const gpt_config* cfg, int32_t num_sms, int64_t* n_tasks, int32_t* n_ops,
                        gpt_task_info* tasks, int64_t max_tasks, int32_t* op_types, int32_t* op_tasks,
@@ -282,6 +297,19 @@ int gpt_train_step_static(const gpt_config* cfg, float* params, float* m, float*
 int gpt_test_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, int32_t a_mn,
                   const void* B, int64_t ldb, int32_t b_mn, float* C, int64_t ldc, int32_t ksplit,
                   void* cuda_stream);
+
+/*
+ * Test hook: causal multi-head attention forward and backward as a graph of
+ * the persistent kernel's attention tasks.  DEVICE buffers, token-major rows
+ * n = b*T + t: qkv [B*T, 3*H*d] (q | k | v, head h at columns h*d), o
+ * [B*T, H*d] output, lse float [B, H, T] output (natural-log LSE of the
+ * scaled scores), dout [B*T, H*d] input gradient of o, dqkv [B*T, 3*H*d]
+ * output, scratch float workspace of at least B*H*T floats (bf16) or
+ * B*H*2*T*d floats (fp32).  Element type bf16 (GPT_DTYPE_BF16: tensor cores,
+ * d == 64, T % 128 == 0) or fp32 (GPT_DTYPE_FP32: SIMT).  Scale 1/sqrt(d).
+ */
+int gpt_test_attention(int32_t dtype, int32_t B, int32_t T, int32_t H, int32_t d, const void* qkv, void* o,
+                       float* lse, const void* dout, void* dqkv, float* scratch, void* cuda_stream);
 
 #ifdef __cplusplus
 }

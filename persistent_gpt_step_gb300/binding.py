@@ -71,6 +71,8 @@ SIGNATURES = [
     ("gpt_debug_skip_release", c_int, [c_void_p, c_int64]),
     ("gpt_reset", c_int, [c_void_p]),
     ("gpt_graph_info", c_int, [c_void_p, POINTER(c_int64), POINTER(c_int32), POINTER(c_int32)]),
+    ("gpt_trace_enable", c_int, [c_void_p, c_int32]),
+    ("gpt_get_trace", c_int, [c_void_p, c_void_p, c_size_t]),
     ("gpt_last_kernel_ms", c_int, [c_void_p, POINTER(c_float)]),
     ("gpt_last_error", c_char_p, [c_void_p]),
     ("gpt_destroy", None, [c_void_p]),
@@ -81,6 +83,8 @@ SIGNATURES = [
                                    c_int32]),
     ("gpt_train_step_static", c_int, [POINTER(gpt_config), c_void_p, c_void_p, c_void_p, c_int64,
                                       c_void_p, c_void_p, POINTER(c_float), c_void_p]),
+    ("gpt_test_attention", c_int, [c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p,
+                                   c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     ("gpt_test_gemm", c_int, [c_int32, c_int32, c_int32, c_int32, c_void_p, c_int64, c_int32,
                               c_void_p, c_int64, c_int32, c_void_p, c_int64, c_int32, c_void_p]),
 ]
@@ -262,6 +266,16 @@ class GPT:
         self._check(self._lib.gpt_graph_info(self._h, byref(n), byref(g), byref(b)))
         return int(n.value), int(g.value), int(b.value)
 
+    def trace_enable(self, on: bool = True):
+        self._check(self._lib.gpt_trace_enable(self._h, int(on)))
+
+    def trace(self) -> np.ndarray:
+        """uint64 [n_tasks, 4]: claim, start, end (ns), SM id of the last step."""
+        n = self.graph_info()[0]
+        out = np.empty((n, 4), np.uint64)
+        self._check(self._lib.gpt_get_trace(self._h, c_void_p(out.ctypes.data), out.size))
+        return out
+
     def last_kernel_ms(self) -> float:
         ms = c_float()
         self._check(self._lib.gpt_last_kernel_ms(self._h, byref(ms)))
@@ -339,3 +353,22 @@ def train_step_static(cfg, params, m, v, step: int, tokens, targets, stream=None
     if rc != GPT_OK:
         raise GptError(rc, lib.gpt_last_error(None).decode())
     return float(loss.value)
+
+
+def test_attention(qkv, dout, B: int, T: int, H: int, d: int, stream=None):
+    """Runs gpt_test_attention on CUDA tensors; returns (o, lse, dqkv)."""
+    import torch
+    lib = load()
+    dtype = DTYPE_BF16 if qkv.dtype == torch.bfloat16 else DTYPE_FP32
+    C = H * d
+    o = torch.full((B * T, C), float("nan"), dtype=qkv.dtype, device=qkv.device)
+    dqkv = torch.full((B * T, 3 * C), float("nan"), dtype=qkv.dtype, device=qkv.device)
+    lse = torch.full((B, H, T), float("nan"), dtype=torch.float32, device=qkv.device)
+    scratch = torch.empty(B * H * 2 * T * d, dtype=torch.float32, device=qkv.device)
+    s = stream if stream is not None else torch.cuda.current_stream()
+    rc = lib.gpt_test_attention(dtype, B, T, H, d, c_void_p(qkv.data_ptr()), c_void_p(o.data_ptr()),
+                                c_void_p(lse.data_ptr()), c_void_p(dout.data_ptr()), c_void_p(dqkv.data_ptr()),
+                                c_void_p(scratch.data_ptr()), c_void_p(s.cuda_stream))
+    if rc != GPT_OK:
+        raise GptError(rc, lib.gpt_last_error(None).decode())
+    return o, lse, dqkv

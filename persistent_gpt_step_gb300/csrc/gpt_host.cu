@@ -137,6 +137,7 @@ struct gpt {
 
   cudaEvent_t ev0 = nullptr, ev1 = nullptr;  // bracket the kernel of the last step
   float last_kernel_ms = 0.f;
+  unsigned long long* d_trace = nullptr;  // optional per-task timestamps (gpt_trace_enable)
   // host staging (pinned) for the per-step status
   struct Status { uint32_t err[4]; float loss; uint32_t pad[3]; };
   Status* h_status = nullptr;
@@ -181,6 +182,8 @@ int validate(const gpt_config& c, std::string* why) {
   if (is_bf16(c)) {
     if (((int64_t)c.batch * c.seq_len) % 128) { *why = "bf16: batch * seq_len must be a multiple of 128"; return GPT_ERR_UNSUPPORTED; }
     if (c.vocab % 64) { *why = "bf16: vocab must be a multiple of 64"; return GPT_ERR_UNSUPPORTED; }
+    if (hd != 64) { *why = "bf16: head_dim must be 64"; return GPT_ERR_UNSUPPORTED; }
+    if (c.seq_len % 128) { *why = "bf16: seq_len must be a multiple of 128"; return GPT_ERR_UNSUPPORTED; }
   }
   if (!(c.lr >= 0.f) || !(c.beta1 >= 0.f && c.beta1 < 1.f) || !(c.beta2 >= 0.f && c.beta2 < 1.f) ||
       !(c.eps > 0.f) || !(c.ln_eps > 0.f) || !(c.weight_decay >= 0.f))
@@ -482,7 +485,7 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
       return rc;
     o.gemm.out = ACT(Lo.qkv[l]); o.gemm.ldo = 3 * C; o.gemm.bias = P(id.b_qkv);
     op_qkv[l] = bld.add(o, {op_ln1[l]});
-    o = blank(OP_ATTN_FWD, D.B * D.H * ((D.T + qblock - 1) / qblock));
+    o = blank(OP_ATTN_FWD, bf ? D.B * D.H * (D.T / 128) : D.B * D.H * ((D.T + qblock - 1) / qblock));
     o.attn = AttnArgs{ACT(Lo.qkv[l]), ACT(Lo.atto[l]), F32(Lo.lse[l]), nullptr, nullptr, nullptr,
                       D.B, D.T, D.H, D.d, C, qblock, 1.0f / std::sqrt((float)D.d)};
     op_attn[l] = bld.add(o, {op_qkv[l]});
@@ -537,10 +540,11 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
     if (dl.size() == 2) bld.add(a, {dl[0], dl[1]});
     else bld.add(a, {dl[0], dl[1], dl[2]});
   };
-  auto colsum = [&](const void* src, bool f32, int64_t ld, int rows, int cols, float* dst, int dep) {
+  auto colsum = [&](const void* src, bool f32, int64_t ld, int rows, int cols, float* dst, int dep,
+                    int dep2 = -1) {
     OpDesc s = blank(OP_COLSUM, (cols + kColsColsum - 1) / kColsColsum);
     s.colsum = ColsumArgs{src, f32 ? 1 : 0, ld, rows, cols, kColsColsum, dst};
-    return bld.add(s, {dep});
+    return bld.add(s, {dep, dep2});
   };
   // LM head: daf = dz . Wlm ; dWlm = dz^T . lnf
   if ((rc = gemm_op(h, &o, N, C, V, {ACT(Lo.logits), V, false}, {W(h->t_wlm), C, true}, EPI_F32, lm_ksplit)))
@@ -609,20 +613,35 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
     if (id.b_o >= 0) adam(id.b_o, {colsum(F32(Lo.dxm[l]), true, C, N, C, G(id.b_o), op_ln2b)});
     adam(id.w_o, {op_atto_dw, op_atto_dx});
     // attention backward -> dqkv
-    o = blank(OP_ATTN_BWD, D.B * D.H);
-    o.attn = AttnArgs{ACT(Lo.qkv[l]), ACT(Lo.atto[l]), F32(Lo.lse[l]), ACT(Lo.dO[l]), ACT(Lo.dqkv[l]),
-                      F32(Lo.att_scr[l]), D.B, D.T, D.H, D.d, C, qblock, 1.0f / std::sqrt((float)D.d)};
-    const int op_attb = bld.add(o, {op_atto_dx});
+    const AttnArgs att{ACT(Lo.qkv[l]), ACT(Lo.atto[l]), F32(Lo.lse[l]), ACT(Lo.dO[l]), ACT(Lo.dqkv[l]),
+                       F32(Lo.att_scr[l]), D.B, D.T, D.H, D.d, C, qblock, 1.0f / std::sqrt((float)D.d)};
+    int op_attb, op_attb2 = -1;
+    if (bf) {
+      o = blank(OP_ATTN_BWD_PRE, N / 64);
+      o.attn = att;
+      const int op_pre = bld.add(o, {op_atto_dx});
+      o = blank(OP_ATTN_BWD_KV, D.B * D.H * (D.T / 128));
+      o.attn = att;
+      op_attb = bld.add(o, {op_pre});
+      o = blank(OP_ATTN_BWD_Q, D.B * D.H * (D.T / 128));
+      o.attn = att;
+      op_attb2 = bld.add(o, {op_pre});
+    } else {
+      o = blank(OP_ATTN_BWD, D.B * D.H);
+      o.attn = att;
+      op_attb = bld.add(o, {op_atto_dx});
+    }
     // QKV: da1 = dqkv . Wqkv ; dWqkv = dqkv^T . ln1 ; dbqkv = colsum(dqkv)
     if ((rc = gemm_op(h, &o, N, C, 3 * C, {ACT(Lo.dqkv[l]), 3 * C, false}, {W(id.w_qkv), C, true}, EPI_F32, 1)))
       return rc;
     o.gemm.out = F32(Lo.da1[l]); o.gemm.ldo = C;
-    const int op_qkv_dx = bld.add(o, {op_attb});
+    const int op_qkv_dx = bld.add(o, {op_attb, op_attb2});
     if ((rc = gemm_op(h, &o, 3 * C, C, N, {ACT(Lo.dqkv[l]), 3 * C, true}, {ACT(Lo.ln1[l]), C, true}, EPI_F32, 1)))
       return rc;
     o.gemm.out = G(id.w_qkv); o.gemm.ldo = C;
-    const int op_qkv_dw = bld.add(o, {op_attb});
-    if (id.b_qkv >= 0) adam(id.b_qkv, {colsum(ACT(Lo.dqkv[l]), false, 3 * C, N, 3 * C, G(id.b_qkv), op_attb)});
+    const int op_qkv_dw = bld.add(o, {op_attb, op_attb2});
+    if (id.b_qkv >= 0)
+      adam(id.b_qkv, {colsum(ACT(Lo.dqkv[l]), false, 3 * C, N, 3 * C, G(id.b_qkv), op_attb, op_attb2)});
     adam(id.w_qkv, {op_qkv_dw, op_qkv_dx});
     // LN1 backward: dx_l = dxm + LN1'(da1)
     o = blank(OP_LN_BWD, nrb);
@@ -703,6 +722,7 @@ int launch_step(gpt* h, const int32_t* tokens, const int32_t* targets, float* lo
   kp.tmaps = h->d_tmaps;
   kp.tokens = tokens;
   kp.targets = targets;
+  kp.trace = h->d_trace;
   kp.lr = h->cfg.lr; kp.beta1 = h->cfg.beta1; kp.beta2 = h->cfg.beta2; kp.eps = h->cfg.eps;
   kp.wd = h->cfg.weight_decay;
   const double t = (double)(h->opt_step + 1);
@@ -994,6 +1014,34 @@ int gpt_graph_info(const gpt* h, int64_t* n_tasks, int32_t* grid, int32_t* block
   return GPT_OK;
 }
 
+int gpt_trace_enable(gpt* h, int32_t on) {
+  if (!h) return GPT_ERR_INVALID_ARG;
+  if (on && !h->d_trace) {
+    const size_t bytes = h->tasks.size() * 4 * sizeof(unsigned long long);
+    if (cudaMalloc(&h->d_trace, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      h->d_trace = nullptr;
+      return fail(h, GPT_ERR_OOM, "cudaMalloc of the trace buffer failed");
+    }
+    CUDA_TRY(h, cudaMemsetAsync(h->d_trace, 0, bytes, h->stream));
+    CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  } else if (!on && h->d_trace) {
+    cudaStreamSynchronize(h->stream);
+    cudaFree(h->d_trace);
+    h->d_trace = nullptr;
+  }
+  return GPT_OK;
+}
+
+int gpt_get_trace(gpt* h, uint64_t* dst, size_t n) {
+  if (!h || !dst) return GPT_ERR_INVALID_ARG;
+  if (!h->d_trace) return fail(h, GPT_ERR_INVALID_ARG, "tracing is off (gpt_trace_enable)");
+  if (n != h->tasks.size() * 4) return fail(h, GPT_ERR_INVALID_ARG, "n must be 4 * n_tasks");
+  CUDA_TRY(h, cudaMemcpyAsync(dst, h->d_trace, n * 8, cudaMemcpyDeviceToHost, h->stream));
+  CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  return GPT_OK;
+}
+
 int gpt_last_kernel_ms(const gpt* h, float* ms) {
   if (!h || !ms) return GPT_ERR_INVALID_ARG;
   *ms = h->last_kernel_ms;
@@ -1008,9 +1056,68 @@ void gpt_destroy(gpt* h) {
   if (h->meta) cudaFree(h->meta);
   if (h->own_arena && h->arena) cudaFree(h->arena);
   if (h->h_status) cudaFreeHost(h->h_status);
+  if (h->d_trace) cudaFree(h->d_trace);
   if (h->ev0) cudaEventDestroy(h->ev0);
   if (h->ev1) cudaEventDestroy(h->ev1);
   delete h;
+}
+
+// Runs the ops/tasks already built in h once (test hooks): graph metadata in a
+// temporary allocation, one launch of the persistent kernel, then freed.
+static int run_test_graph(gpt& h, int32_t dtype) {
+  Bump mb;
+  const size_t o_tasks = mb.take(h.tasks.size() * sizeof(TaskDesc));
+  const size_t o_ops = mb.take(h.ops.size() * sizeof(OpDesc));
+  const size_t o_maps = mb.take(std::max<size_t>(1, h.tmaps.size()) * 128);
+  const size_t o_ctr = mb.take(h.ops.size() * sizeof(unsigned long long));
+  const size_t o_tic = mb.take(sizeof(unsigned long long));
+  const size_t o_err = mb.take(4 * sizeof(uint32_t));
+  const size_t o_loss = mb.take(sizeof(float));
+  h.meta_bytes = mb.off;
+  if (cudaMalloc(&h.meta, h.meta_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    h.meta = nullptr;
+    return fail(nullptr, GPT_ERR_OOM, "cudaMalloc failed");
+  }
+  h.d_tasks = reinterpret_cast<TaskDesc*>(h.meta + o_tasks);
+  h.d_ops = reinterpret_cast<OpDesc*>(h.meta + o_ops);
+  h.d_tmaps = h.meta + o_maps;
+  h.d_counters = reinterpret_cast<unsigned long long*>(h.meta + o_ctr);
+  h.d_ticket = reinterpret_cast<unsigned long long*>(h.meta + o_tic);
+  h.d_err = reinterpret_cast<uint32_t*>(h.meta + o_err);
+  h.loss_dev = reinterpret_cast<float*>(h.meta + o_loss);
+  int result = GPT_OK;
+  do {
+    if (cudaMallocHost(&h.h_status, sizeof(gpt::Status)) != cudaSuccess) { result = GPT_ERR_OOM; break; }
+    if (cudaMemcpyAsync(h.d_tasks, h.tasks.data(), h.tasks.size() * sizeof(TaskDesc), cudaMemcpyHostToDevice,
+                        h.stream) ||
+        cudaMemcpyAsync(h.d_ops, h.ops.data(), h.ops.size() * sizeof(OpDesc), cudaMemcpyHostToDevice, h.stream)) {
+      result = GPT_ERR_CUDA;
+      break;
+    }
+    bool bad = false;
+    for (size_t i = 0; i < h.tmaps.size(); ++i)
+      bad |= cudaMemcpyAsync(static_cast<uint8_t*>(h.d_tmaps) + 128 * i, h.tmaps[i].data(), 128,
+                             cudaMemcpyHostToDevice, h.stream) != cudaSuccess;
+    if (bad) { result = GPT_ERR_CUDA; break; }
+    h.kernel = dtype == GPT_DTYPE_BF16 ? step_kernel_bf16() : step_kernel_fp32();
+    h.smem_bytes = dtype == GPT_DTYPE_BF16 ? (size_t)kTcSmemBytes + 1024 : smem_needed(&h);
+    if (cudaFuncSetAttribute(h.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h.smem_bytes)) {
+      result = GPT_ERR_CUDA;
+      break;
+    }
+    h.grid = h.num_sms;
+    if (reset_counters(&h) != GPT_OK) { result = GPT_ERR_CUDA; break; }
+    result = launch_step(&h, reinterpret_cast<const int32_t*>(h.meta), reinterpret_cast<const int32_t*>(h.meta),
+                         nullptr);
+  } while (0);
+  if (result != GPT_OK) g_create_error = h.err.empty() ? std::string("test graph failed") : h.err;
+  cudaStreamSynchronize(h.stream);
+  cudaFree(h.meta);
+  h.meta = nullptr;
+  if (h.h_status) cudaFreeHost(h.h_status);
+  h.h_status = nullptr;
+  return result;
 }
 
 int gpt_test_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, int32_t a_mn,
@@ -1027,55 +1134,56 @@ int gpt_test_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* A,
   h.stream = (cudaStream_t)cuda_stream;
   cudaGetDevice(&h.device);
   cudaDeviceGetAttribute(&h.num_sms, cudaDevAttrMultiProcessorCount, h.device);
+  h.D = Dims{1, 64, 1, 64, 64, 64, 1, 1, 1};
   OpDesc o;
   int rc = gemm_op(&h, &o, M, N, K, {A, lda, a_mn != 0}, {B, ldb, b_mn != 0}, EPI_F32, ksplit);
   if (rc != GPT_OK) { g_create_error = h.err; return rc; }
   o.gemm.out = C; o.gemm.ldo = ldc; o.gemm.split_stride = (int64_t)M * ldc;
   Builder bld{&h};
   bld.add(o, {});
-  h.D = Dims{1, 64, 1, 64, 64, 64, 1, 1, 1};
-  Bump mb;
-  const size_t o_tasks = mb.take(h.tasks.size() * sizeof(TaskDesc));
-  const size_t o_ops = mb.take(sizeof(OpDesc));
-  const size_t o_maps = mb.take(std::max<size_t>(1, h.tmaps.size()) * 128);
-  const size_t o_ctr = mb.take(sizeof(unsigned long long));
-  const size_t o_tic = mb.take(sizeof(unsigned long long));
-  const size_t o_err = mb.take(4 * sizeof(uint32_t));
-  const size_t o_loss = mb.take(sizeof(float));
-  h.meta_bytes = mb.off;
-  if (cudaMalloc(&h.meta, h.meta_bytes) != cudaSuccess) { cudaGetLastError(); h.meta = nullptr; return fail(nullptr, GPT_ERR_OOM, "cudaMalloc failed"); }
-  h.d_tasks = reinterpret_cast<TaskDesc*>(h.meta + o_tasks);
-  h.d_ops = reinterpret_cast<OpDesc*>(h.meta + o_ops);
-  h.d_tmaps = h.meta + o_maps;
-  h.d_counters = reinterpret_cast<unsigned long long*>(h.meta + o_ctr);
-  h.d_ticket = reinterpret_cast<unsigned long long*>(h.meta + o_tic);
-  h.d_err = reinterpret_cast<uint32_t*>(h.meta + o_err);
-  h.loss_dev = reinterpret_cast<float*>(h.meta + o_loss);
-  int result = GPT_OK;
-  do {
-    if (cudaMallocHost(&h.h_status, sizeof(gpt::Status)) != cudaSuccess) { result = GPT_ERR_OOM; break; }
-    if (cudaMemcpyAsync(h.d_tasks, h.tasks.data(), h.tasks.size() * sizeof(TaskDesc), cudaMemcpyHostToDevice, h.stream) ||
-        cudaMemcpyAsync(h.d_ops, h.ops.data(), sizeof(OpDesc), cudaMemcpyHostToDevice, h.stream)) { result = GPT_ERR_CUDA; break; }
-    bool bad = false;
-    for (size_t i = 0; i < h.tmaps.size(); ++i)
-      bad |= cudaMemcpyAsync(static_cast<uint8_t*>(h.d_tmaps) + 128 * i, h.tmaps[i].data(), 128, cudaMemcpyHostToDevice, h.stream) != cudaSuccess;
-    if (bad) { result = GPT_ERR_CUDA; break; }
-    h.kernel = dtype == GPT_DTYPE_BF16 ? step_kernel_bf16() : step_kernel_fp32();
-    h.smem_bytes = dtype == GPT_DTYPE_BF16 ? (size_t)kTcSmemBytes + 1024 : (size_t)(2 * 16 * (kSimtTile + 4) * 4) + 1024;
-    if (cudaFuncSetAttribute(h.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h.smem_bytes)) { result = GPT_ERR_CUDA; break; }
-    h.grid = h.num_sms;
-    if (reset_counters(&h) != GPT_OK) { result = GPT_ERR_CUDA; break; }
-    const int32_t dummy_tok = 0;
-    (void)dummy_tok;
-    result = launch_step(&h, reinterpret_cast<const int32_t*>(h.meta), reinterpret_cast<const int32_t*>(h.meta), nullptr);
-  } while (0);
-  if (result != GPT_OK) g_create_error = h.err.empty() ? std::string("GEMM test failed") : h.err;
-  cudaStreamSynchronize(h.stream);
-  cudaFree(h.meta);
-  h.meta = nullptr;
-  if (h.h_status) cudaFreeHost(h.h_status);
-  h.h_status = nullptr;
-  return result;
+  return run_test_graph(h, dtype);
+}
+
+int gpt_test_attention(int32_t dtype, int32_t B, int32_t T, int32_t H, int32_t d, const void* qkv, void* o,
+                       float* lse, const void* dout, void* dqkv, float* scratch, void* cuda_stream) {
+  g_create_error.clear();
+  if (!qkv || !o || !lse || !dout || !dqkv || !scratch || B < 1 || T < 1 || H < 1 || d < 1 ||
+      (dtype != GPT_DTYPE_FP32 && dtype != GPT_DTYPE_BF16))
+    return fail(nullptr, GPT_ERR_INVALID_ARG, "bad attention test arguments");
+  if (dtype == GPT_DTYPE_BF16 && (d != 64 || T % 128))
+    return fail(nullptr, GPT_ERR_UNSUPPORTED, "bf16 attention needs head_dim 64 and T %% 128 == 0");
+  if (dtype == GPT_DTYPE_FP32 && (T > 1024 || d > 128))
+    return fail(nullptr, GPT_ERR_UNSUPPORTED, "fp32 attention needs T <= 1024 and head_dim <= 128");
+  gpt h;
+  gpt_default_config(&h.cfg);
+  h.cfg.dtype = dtype;
+  h.cfg.n_head = H; h.cfg.d_model = H * d; h.cfg.seq_len = T; h.cfg.batch = B;
+  h.stream = (cudaStream_t)cuda_stream;
+  cudaGetDevice(&h.device);
+  cudaDeviceGetAttribute(&h.num_sms, cudaDevAttrMultiProcessorCount, h.device);
+  h.D = Dims{1, H * d, H, d, 64, 64, T, B, B * T};
+  const int qblock = T <= 512 ? 64 : 32;
+  const AttnArgs att{qkv, o, lse, dout, dqkv, scratch, B, T, H, d, H * d, qblock, 1.0f / std::sqrt((float)d)};
+  Builder bld{&h};
+  OpDesc op = blank(OP_ATTN_FWD, dtype == GPT_DTYPE_BF16 ? B * H * (T / 128) : B * H * ((T + qblock - 1) / qblock));
+  op.attn = att;
+  const int f = bld.add(op, {});
+  if (dtype == GPT_DTYPE_BF16) {
+    op = blank(OP_ATTN_BWD_PRE, (B * T + 63) / 64);
+    op.attn = att;
+    const int pre = bld.add(op, {f});
+    op = blank(OP_ATTN_BWD_KV, B * H * (T / 128));
+    op.attn = att;
+    bld.add(op, {pre});
+    op = blank(OP_ATTN_BWD_Q, B * H * (T / 128));
+    op.attn = att;
+    bld.add(op, {pre});
+  } else {
+    op = blank(OP_ATTN_BWD, B * H);
+    op.attn = att;
+    bld.add(op, {f});
+  }
+  return run_test_graph(h, dtype);
 }
 
 int gpt_init_params_host(const gpt_config* cfg, uint64_t seed, float* dst, size_t n) {

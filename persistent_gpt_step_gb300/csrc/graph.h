@@ -42,6 +42,9 @@ enum OpType : int32_t {
   OP_EMBED_BWD_WTE,  // dwte[v] = sum_{n: tok[n] = v} dx0[n]         tasks: vocab blocks
   OP_EMBED_BWD_WPE,  // dwpe[t] = sum_b dx0[b, t]                    tasks: position blocks
   OP_ADAMW,          // AdamW on a contiguous parameter range        tasks: chunks
+  OP_ATTN_BWD_PRE,   // D = rowsum(dO * O) per head (tensor-core path) tasks: 64-row blocks
+  OP_ATTN_BWD_KV,    // dK, dV of the causal attention               tasks: (b, h, 128 keys)
+  OP_ATTN_BWD_Q,     // dQ of the causal attention                   tasks: (b, h, 128 queries)
   OP_NOP,            // scheduler test: no work                      tasks: any
   OP_NUM_TYPES
 };
@@ -94,7 +97,7 @@ struct AttnArgs {
   float* lse;       // [B, H, T]
   const void* dout; // act [B*T, C]   (backward)
   void* dqkv;       // act [B*T, 3C]  (backward)
-  float* scratch;   // backward accumulators
+  float* scratch;   // SIMT backward: dK/dV accumulators; tensor-core path: D [B, H, T]
   int32_t B, T, H, d, C, q_block;
   float scale;
 };
@@ -172,6 +175,7 @@ struct KParams {
   const void* tmaps;               // CUtensorMap[] (tensor-core path)
   const int32_t* tokens; const int32_t* targets;
   float lr, beta1, beta2, eps, wd, bc1, bc2;
+  unsigned long long* trace;       // optional [ntasks][4]: claim, start, end (globaltimer ns), SM id
 };
 
 }  // namespace pgs

@@ -13,6 +13,7 @@
 #include "tasks_rows.cuh"
 #include "tasks_simt.cuh"
 #include "tc_gemm.cuh"
+#include "attn_tc.cuh"
 
 namespace pgs {
 
@@ -56,10 +57,18 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
         t = (int64_t)(atomicAdd(kp.ticket, 1ull) - kp.ticket_base);
         if (t < kp.ntasks) {
           ok = 1;
+          const uint64_t t_claim = kp.trace ? globaltimer_ns() : 0;
           const TaskDesc& d = kp.tasks[t];
           for (int w = 0; w < d.nwait && ok; ++w)
             ok = wait_counter(kp, d.wait_ctr[w], kp.epoch * (unsigned long long)d.wait_need[w],
                               (uint32_t)t);
+          if (kp.trace) {
+            uint32_t smid;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+            kp.trace[4 * t + 0] = t_claim;
+            kp.trace[4 * t + 1] = globaltimer_ns();
+            kp.trace[4 * t + 3] = smid;
+          }
         }
       }
       sh.task = t;
@@ -83,7 +92,19 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
           task_gemm_simt<act_t>(op.gemm, idx, reinterpret_cast<float*>(smem), gelu_tanh != 0);
         }
         break;
-      case OP_ATTN_FWD: task_attn_fwd_simt<act_t>(op.attn, idx, reinterpret_cast<float*>(smem)); break;
+      case OP_ATTN_FWD:
+        if constexpr (kTC) task_attn_fwd_tc(op.attn, idx, smem);
+        else task_attn_fwd_simt<act_t>(op.attn, idx, reinterpret_cast<float*>(smem));
+        break;
+      case OP_ATTN_BWD_PRE:
+        if constexpr (kTC) task_attn_bwd_pre(op.attn, idx);
+        break;
+      case OP_ATTN_BWD_KV:
+        if constexpr (kTC) task_attn_bwd_kv_tc(op.attn, idx, smem);
+        break;
+      case OP_ATTN_BWD_Q:
+        if constexpr (kTC) task_attn_bwd_q_tc(op.attn, idx, smem);
+        break;
       case OP_CE:
         if constexpr (kTC) {
           if ((op.ce.V & 7) == 0) task_ce_bf16_vec(kp, op.ce, idx);
@@ -107,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
       fence_proxy_async_global();
       red_release_add_u64(kp.counters + d.op, 1ull);
     }
+    if (threadIdx.x == 0 && kp.trace) kp.trace[4 * t + 2] = globaltimer_ns();
   }
 
   if constexpr (kTC) {

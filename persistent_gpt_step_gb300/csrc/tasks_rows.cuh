@@ -29,37 +29,85 @@ __device__ inline void task_embed(const KParams& kp, const EmbedArgs& a, int idx
   }
 }
 
-// LayerNorm forward, one warp per row; lane holds columns lane + 32 i.
-// mean = sum x / C, var = sum (x - mean)^2 / C (biased), y = xhat g + b.
+// LayerNorm forward, one warp per row.  mean = sum x / C,
+// var = sum (x - mean)^2 / C (biased), y = (x - mean) rstd g + b.
+// NV > 0: C = 128 NV, lane holds float4 number lane + 32 i in registers;
+// NV = 0: any C (multiple of 32), three passes over the row (L1-resident).
 template <typename act_t>
-__device__ inline void task_ln_fwd(const LnFwdArgs& a, int idx) {
+__device__ __forceinline__ void store4(act_t* p, float a, float b, float c, float d);
+template <>
+__device__ __forceinline__ void store4<float>(float* p, float a, float b, float c, float d) {
+  *reinterpret_cast<float4*>(p) = make_float4(a, b, c, d);
+}
+template <>
+__device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float a, float b, float c, float d) {
+  __nv_bfloat162 lo = __floats2bfloat162_rn(a, b), hi = __floats2bfloat162_rn(c, d);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&lo);
+  u.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+template <typename act_t, int NV>
+__device__ __forceinline__ void ln_fwd_rows(const LnFwdArgs& a, int r0, int r1) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = idx * a.rows_per_task, r1 = min(r0 + a.rows_per_task, a.rows);
-  const int nper = a.C >> 5;  // C <= 1024
   act_t* y = reinterpret_cast<act_t*>(a.y);
+  const float invC = 1.0f / (float)a.C;
   for (int r = r0 + warp; r < r1; r += kWarps) {
     const float* x = a.x + (int64_t)r * a.C;
-    float v[32];
-    float s = 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (i < nper) { v[i] = x[i * 32 + lane]; s += v[i]; }
-    const float mean = warp_sum(s) / (float)a.C;
-    float q = 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (i < nper) { float d = v[i] - mean; q += d * d; }
-    const float rstd = rsqrtf(warp_sum(q) / (float)a.C + a.eps);
     act_t* yr = y + (int64_t)r * a.C;
+    float mean, rstd;
+    if constexpr (NV > 0) {
+      float4 v[NV];
+      float s = 0.f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (i < nper) {
-        const int c = i * 32 + lane;
-        float o = (v[i] - mean) * rstd * a.g[c];
+      for (int i = 0; i < NV; ++i) {
+        v[i] = reinterpret_cast<const float4*>(x)[lane + 32 * i];
+        s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+      }
+      mean = warp_sum(s) * invC;
+      float q = 0.f;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const float d0 = v[i].x - mean, d1 = v[i].y - mean, d2 = v[i].z - mean, d3 = v[i].w - mean;
+        q += (d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3);
+      }
+      rstd = rsqrtf(warp_sum(q) * invC + a.eps);
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int c = 4 * (lane + 32 * i);
+        const float4 g = *reinterpret_cast<const float4*>(a.g + c);
+        float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (a.b) b = *reinterpret_cast<const float4*>(a.b + c);
+        store4<act_t>(yr + c, (v[i].x - mean) * rstd * g.x + b.x, (v[i].y - mean) * rstd * g.y + b.y,
+                      (v[i].z - mean) * rstd * g.z + b.z, (v[i].w - mean) * rstd * g.w + b.w);
+      }
+    } else {
+      float s = 0.f;
+      for (int c = lane; c < a.C; c += 32) s += x[c];
+      mean = warp_sum(s) * invC;
+      float q = 0.f;
+      for (int c = lane; c < a.C; c += 32) { const float d = x[c] - mean; q += d * d; }
+      rstd = rsqrtf(warp_sum(q) * invC + a.eps);
+      for (int c = lane; c < a.C; c += 32) {
+        float o = (x[c] - mean) * rstd * a.g[c];
         if (a.b) o += a.b[c];
         yr[c] = from_f<act_t>(o);
       }
+    }
     if (lane == 0) { a.mean[r] = mean; a.rstd[r] = rstd; }
+  }
+}
+
+template <typename act_t>
+__device__ inline void task_ln_fwd(const LnFwdArgs& a, int idx) {
+  const int r0 = idx * a.rows_per_task, r1 = min(r0 + a.rows_per_task, a.rows);
+  switch ((a.C & 127) ? 0 : a.C >> 7) {
+    case 2: ln_fwd_rows<act_t, 2>(a, r0, r1); break;
+    case 4: ln_fwd_rows<act_t, 4>(a, r0, r1); break;
+    case 6: ln_fwd_rows<act_t, 6>(a, r0, r1); break;
+    case 8: ln_fwd_rows<act_t, 8>(a, r0, r1); break;
+    default: ln_fwd_rows<act_t, 0>(a, r0, r1); break;
   }
 }
 
@@ -67,59 +115,102 @@ __device__ inline void task_ln_fwd(const LnFwdArgs& a, int idx) {
 //   dxhat = dy g; dx = rstd (dxhat - mean(dxhat) - xhat mean(dxhat xhat));
 //   dres_out = dres_in + dx (fp32 and act copies);
 //   dg_part[task] = sum_rows dy xhat, db_part[task] = sum_rows dy.
-template <typename act_t>
-__device__ inline void task_ln_bwd(const LnBwdArgs& a, int idx, float* smem) {
+// Warp w adds its rows' dy xhat and dy, in row order, into its own shared-memory
+// rows; the warps' rows are then added in warp order (fixed summation order).
+template <typename act_t, int NV>
+__device__ __forceinline__ void ln_bwd_rows(const LnBwdArgs& a, int r0, int r1, float* sg, float* sb) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r0 = idx * a.rows_per_task, r1 = min(r0 + a.rows_per_task, a.rows);
-  const int nper = a.C >> 5;
-  float pg[32], pb[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) { pg[i] = 0.f; pb[i] = 0.f; }
   act_t* dact = reinterpret_cast<act_t*>(a.dres_act);
   const float invC = 1.0f / (float)a.C;
+  float* wg = sg + warp * a.C;
+  float* wb = sb + warp * a.C;
   for (int r = r0 + warp; r < r1; r += kWarps) {
     const float mean = a.mean[r], rstd = a.rstd[r];
     const float* x = a.x + (int64_t)r * a.C;
-    float dy[32], xh[32];
-    float s1 = 0.f, s2 = 0.f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (i < nper) {
-        const int c = i * 32 + lane;
-        float d = 0.f;
-        for (int s = 0; s < a.dy_splits; ++s) d += a.dy[s * a.dy_split_stride + (int64_t)r * a.C + c];
-        dy[i] = d;
-        xh[i] = (x[c] - mean) * rstd;
-        const float dxh = d * a.g[c];
-        s1 += dxh;
-        s2 += dxh * xh[i];
-        pg[i] += d * xh[i];
-        pb[i] += d;
-      }
-    s1 = warp_sum(s1) * invC;
-    s2 = warp_sum(s2) * invC;
     float* out = a.dres_out + (int64_t)r * a.C;
     const float* din = a.dres_in ? a.dres_in + (int64_t)r * a.C : nullptr;
     act_t* oa = dact + (int64_t)r * a.C;
+    if constexpr (NV > 0) {
+      float4 dy[NV], xh[NV];
+      float s1 = 0.f, s2 = 0.f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (i < nper) {
-        const int c = i * 32 + lane;
-        float dx = rstd * (dy[i] * a.g[c] - s1 - xh[i] * s2);
+      for (int i = 0; i < NV; ++i) {
+        const int c = 4 * (lane + 32 * i);
+        float4 d = *reinterpret_cast<const float4*>(a.dy + (int64_t)r * a.C + c);
+        for (int sp = 1; sp < a.dy_splits; ++sp) {
+          const float4 e = *reinterpret_cast<const float4*>(a.dy + sp * a.dy_split_stride + (int64_t)r * a.C + c);
+          d.x += e.x; d.y += e.y; d.z += e.z; d.w += e.w;
+        }
+        const float4 xv = *reinterpret_cast<const float4*>(x + c);
+        const float4 g = *reinterpret_cast<const float4*>(a.g + c);
+        dy[i] = d;
+        xh[i] = make_float4((xv.x - mean) * rstd, (xv.y - mean) * rstd, (xv.z - mean) * rstd, (xv.w - mean) * rstd);
+        const float a0 = d.x * g.x, a1 = d.y * g.y, a2 = d.z * g.z, a3 = d.w * g.w;
+        s1 += (a0 + a1) + (a2 + a3);
+        s2 += (a0 * xh[i].x + a1 * xh[i].y) + (a2 * xh[i].z + a3 * xh[i].w);
+        float4 pg = *reinterpret_cast<float4*>(wg + c);
+        pg.x += d.x * xh[i].x; pg.y += d.y * xh[i].y; pg.z += d.z * xh[i].z; pg.w += d.w * xh[i].w;
+        *reinterpret_cast<float4*>(wg + c) = pg;
+        float4 pb = *reinterpret_cast<float4*>(wb + c);
+        pb.x += d.x; pb.y += d.y; pb.z += d.z; pb.w += d.w;
+        *reinterpret_cast<float4*>(wb + c) = pb;
+      }
+      s1 = warp_sum(s1) * invC;
+      s2 = warp_sum(s2) * invC;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int c = 4 * (lane + 32 * i);
+        const float4 g = *reinterpret_cast<const float4*>(a.g + c);
+        float4 o = make_float4(rstd * (dy[i].x * g.x - s1 - xh[i].x * s2), rstd * (dy[i].y * g.y - s1 - xh[i].y * s2),
+                               rstd * (dy[i].z * g.z - s1 - xh[i].z * s2), rstd * (dy[i].w * g.w - s1 - xh[i].w * s2));
+        if (din) {
+          const float4 e = *reinterpret_cast<const float4*>(din + c);
+          o.x += e.x; o.y += e.y; o.z += e.z; o.w += e.w;
+        }
+        *reinterpret_cast<float4*>(out + c) = o;
+        store4<act_t>(oa + c, o.x, o.y, o.z, o.w);
+      }
+    } else {
+      float s1 = 0.f, s2 = 0.f;
+      for (int c = lane; c < a.C; c += 32) {
+        float d = 0.f;
+        for (int sp = 0; sp < a.dy_splits; ++sp) d += a.dy[sp * a.dy_split_stride + (int64_t)r * a.C + c];
+        const float xh = (x[c] - mean) * rstd;
+        const float dxh = d * a.g[c];
+        s1 += dxh;
+        s2 += dxh * xh;
+        wg[c] += d * xh;
+        wb[c] += d;
+      }
+      s1 = warp_sum(s1) * invC;
+      s2 = warp_sum(s2) * invC;
+      for (int c = lane; c < a.C; c += 32) {
+        float d = 0.f;
+        for (int sp = 0; sp < a.dy_splits; ++sp) d += a.dy[sp * a.dy_split_stride + (int64_t)r * a.C + c];
+        const float xh = (x[c] - mean) * rstd;
+        float dx = rstd * (d * a.g[c] - s1 - xh * s2);
         if (din) dx += din[c];
         out[c] = dx;
         oa[c] = from_f<act_t>(dx);
       }
+    }
   }
-  // fixed-order reduction of the per-warp partial sums
+}
+
+template <typename act_t>
+__device__ inline void task_ln_bwd(const LnBwdArgs& a, int idx, float* smem) {
+  const int r0 = idx * a.rows_per_task, r1 = min(r0 + a.rows_per_task, a.rows);
   float* sg = smem;                 // [kWarps][C]
   float* sb = smem + kWarps * a.C;  // [kWarps][C]
-#pragma unroll
-  for (int i = 0; i < 32; ++i)
-    if (i < nper) {
-      sg[warp * a.C + i * 32 + lane] = pg[i];
-      sb[warp * a.C + i * 32 + lane] = pb[i];
-    }
+  for (int e = threadIdx.x; e < 2 * kWarps * a.C; e += kThreads) smem[e] = 0.f;
+  __syncthreads();
+  switch ((a.C & 127) ? 0 : a.C >> 7) {
+    case 2: ln_bwd_rows<act_t, 2>(a, r0, r1, sg, sb); break;
+    case 4: ln_bwd_rows<act_t, 4>(a, r0, r1, sg, sb); break;
+    case 6: ln_bwd_rows<act_t, 6>(a, r0, r1, sg, sb); break;
+    case 8: ln_bwd_rows<act_t, 8>(a, r0, r1, sg, sb); break;
+    default: ln_bwd_rows<act_t, 0>(a, r0, r1, sg, sb); break;
+  }
   __syncthreads();
   for (int c = threadIdx.x; c < a.C; c += kThreads) {
     float g = 0.f, b = 0.f;

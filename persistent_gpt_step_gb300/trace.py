@@ -1,0 +1,80 @@
+"""Per-family time table of one training step from the in-kernel trace.
+
+python -m persistent_gpt_step_gb300.trace [--config main] [--steps 3]
+
+The kernel stamps every task's claim, start (after its dependency waits) and
+end (after its release) with %globaltimer.  Per operation family this prints
+the summed busy time (sum of end - start over its tasks, divided by the number
+of blocks: the family's share of the step if blocks never idled), the summed
+dependency-wait time and the wall-clock span from its first start to its last
+end — the shape of the per-family table on "Coppelius training on the RTX
+3090" (section "Where a step's time goes"), measured inside one launch.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import sys
+
+import numpy as np
+
+FAMILIES = ["embed", "layernorm-fwd", "gemm", "attention-fwd", "cross-entropy", "loss",
+            "layernorm-bwd", "column-sum", "attention-bwd", "embedding-bwd-wte",
+            "embedding-bwd-wpe", "adamw", "attention-bwd-pre", "attention-bwd-kv", "attention-bwd-q",
+            "nop"]
+
+
+def family_table(trace: np.ndarray, task_ops: np.ndarray, op_types, grid: int):
+    """Rows (family, tasks, busy_ms_per_block, wait_ms_per_block, span_ms)."""
+    claim = trace[:, 0].astype(np.int64)
+    start = trace[:, 1].astype(np.int64)
+    end = trace[:, 2].astype(np.int64)
+    t0 = start.min()
+    fam_of_task = np.asarray(op_types)[task_ops]
+    rows = []
+    for f in sorted(set(fam_of_task.tolist())):
+        sel = fam_of_task == f
+        busy = (end[sel] - start[sel]).sum() / 1e6 / grid
+        wait = (start[sel] - claim[sel]).sum() / 1e6 / grid
+        span = (end[sel].max() - start[sel].min()) / 1e6
+        rows.append((FAMILIES[f], int(sel.sum()), busy, wait, span,
+                     (start[sel].min() - t0) / 1e6, (end[sel].max() - t0) / 1e6))
+    total = (end.max() - claim.min()) / 1e6
+    return rows, total
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--config", default="main")
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--json", default=None)
+    args = ap.parse_args()
+    import torch
+
+    from . import binding as B
+    from . import inputs as I
+    cfg = I.CONFIGS[args.config]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tasks, op_types, _ = B.describe_graph(cfg, sms)
+    task_ops = np.array([t[0] for t in tasks])
+    with B.GPT(cfg, seed=1234) as m:
+        n, grid, _ = m.graph_info()
+        assert n == len(tasks), (n, len(tasks))
+        m.trace_enable(True)
+        for s in range(args.steps):
+            tok, tgt = I.batch(cfg, 1234, s)
+            m.train_step(torch.from_numpy(tok).cuda(), torch.from_numpy(tgt).cuda())
+        tr = m.trace()
+        kms = m.last_kernel_ms()
+    rows, total = family_table(tr, task_ops, op_types, grid)
+    print(f"config {args.config}: {n} tasks, grid {grid}, kernel {kms:.3f} ms, traced span {total:.3f} ms")
+    print(f"{'family':20s} {'tasks':>7s} {'busy ms':>9s} {'wait ms':>9s} {'span ms':>9s} {'first':>8s} {'last':>8s}")
+    for r in sorted(rows, key=lambda r: -r[2]):
+        print(f"{r[0]:20s} {r[1]:7d} {r[2]:9.3f} {r[3]:9.3f} {r[4]:9.3f} {r[5]:8.3f} {r[6]:8.3f}")
+    if args.json:
+        json.dump({"config": args.config, "kernel_ms": kms, "grid": grid, "rows": rows}, open(args.json, "w"))
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -85,6 +85,38 @@ def test_gemm_bf16_ksplit():
     assert (C.double().sum(0) - ref).abs().max().item() <= 1e-3 * math.sqrt(K)
 
 
+# ----------------------------------------------------------------- attention unit tests
+
+def _attn_reference(qkv, dout, B, T, H, d):
+    x = qkv.double().detach().requires_grad_(True)
+    C = H * d
+    q, k, v = (x[:, i * C:(i + 1) * C].reshape(B, T, H, d).transpose(1, 2) for i in range(3))
+    s = q @ k.transpose(-1, -2) / math.sqrt(d)
+    mask = torch.triu(torch.ones(T, T, dtype=torch.bool, device=qkv.device), 1)
+    s = s.masked_fill(mask, float("-inf"))
+    lse = torch.logsumexp(s, -1)
+    o = (torch.softmax(s, -1) @ v).transpose(1, 2).reshape(B * T, C)
+    o.backward(dout.double())
+    return o.detach(), lse.detach(), x.grad
+
+
+@pytest.mark.parametrize("dt,Bn,T,H,d", [("bf16", 2, 256, 3, 64), ("bf16", 1, 512, 2, 64),
+                                         ("bf16", 1, 1024, 1, 64), ("fp32", 2, 64, 4, 16),
+                                         ("fp32", 1, 192, 2, 64)])
+def test_attention_tasks_match_autograd(dt, Bn, T, H, d):
+    g = torch.Generator(device="cuda").manual_seed(T + H)
+    dtype = torch.bfloat16 if dt == "bf16" else torch.float32
+    qkv = torch.randn(Bn * T, 3 * H * d, device="cuda", generator=g).to(dtype)
+    dout = torch.randn(Bn * T, H * d, device="cuda", generator=g).to(dtype)
+    o, lse, dqkv = B.test_attention(qkv, dout, Bn, T, H, d)
+    ro, rlse, rd = _attn_reference(qkv, dout, Bn, T, H, d)
+    tol = 2e-2 if dt == "bf16" else 1e-5
+    for got, ref, name in ((o, ro, "o"), (lse, rlse, "lse"), (dqkv, rd, "dqkv")):
+        err = (got.double() - ref).norm().item() / ref.norm().item()
+        assert err <= tol, (name, err)
+        assert torch.isfinite(got).all()
+
+
 # ----------------------------------------------------------------- model parity
 
 def test_create_initialises_from_spec():

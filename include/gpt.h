@@ -241,7 +241,8 @@ typedef struct gpt_task_info {
  * SMs; <= 0 means 148) without device memory, and reports it: *n_tasks tasks in
  * ticket order (the first max_tasks copied to HOST tasks[], may be NULL) and
  * *n_ops operations (type and task count of the first max_ops into HOST
- * op_types[] / op_tasks[], may be NULL).  Operation types are the kernel's
+ * op_types[] / op_tasks[], and for GEMM operations M, N, K and the tile
+ * width into op_dims[4*i .. 4*i+3] (zeros otherwise); each may be NULL).  Operation types are the kernel's
  * OpType values (0 embed, 1 LN forward, 2 GEMM, 3 attention forward, 4 cross-
  * entropy, 5 loss, 6 LN backward, 7 column sum, 8 attention backward,
  * 9 token-embedding backward, 10 position-embedding backward, 11 AdamW,
@@ -249,7 +250,7 @@ typedef struct gpt_task_info {
  */
 int gpt_graph_describe(const gpt_config* cfg, int32_t num_sms, int64_t* n_tasks, int32_t* n_ops,
                        gpt_task_info* tasks, int64_t max_tasks, int32_t* op_types, int32_t* op_tasks,
-                       int32_t max_ops);
+                       int32_t* op_dims, int32_t max_ops);
 
 /*
  * Training step that allocates nothing (the pages have no counterpart: this is

@@ -80,7 +80,7 @@ SIGNATURES = [
     ("gpt_init_params_host", c_int, [POINTER(gpt_config), c_uint64, c_void_p, c_size_t]),
     ("gpt_graph_describe", c_int, [POINTER(gpt_config), c_int32, POINTER(c_int64), POINTER(c_int32),
                                    POINTER(gpt_task_info), c_int64, POINTER(c_int32), POINTER(c_int32),
-                                   c_int32]),
+                                   POINTER(c_int32), c_int32]),
     ("gpt_train_step_static", c_int, [POINTER(gpt_config), c_void_p, c_void_p, c_void_p, c_int64,
                                       c_void_p, c_void_p, POINTER(c_float), c_void_p]),
     ("gpt_test_attention", c_int, [c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p,
@@ -318,24 +318,28 @@ def init_params_host(cfg, seed: int, n: int) -> np.ndarray:
     return out
 
 
-def describe_graph(cfg, num_sms: int = 148):
-    """(tasks, op_types, op_tasks) of the step's task graph, built on the host.
+def describe_graph(cfg, num_sms: int = 148, dims: bool = False):
+    """(tasks, op_types, op_tasks[, op_dims]) of the step's task graph, built on the host.
 
-    tasks: list of (op, idx, [(wait_op, need), ...]) in ticket order."""
+    tasks: list of (op, idx, [(wait_op, need), ...]) in ticket order; op_dims:
+    per op (M, N, K, tile width) for GEMMs, zeros otherwise."""
     lib = load()
     c = make_config(cfg)
     nt, no = c_int64(), c_int32()
-    rc = lib.gpt_graph_describe(byref(c), num_sms, byref(nt), byref(no), None, 0, None, None, 0)
+    rc = lib.gpt_graph_describe(byref(c), num_sms, byref(nt), byref(no), None, 0, None, None, None, 0)
     if rc != GPT_OK:
         raise GptError(rc, lib.gpt_last_error(None).decode())
     tasks = (gpt_task_info * nt.value)()
     types = (c_int32 * no.value)()
     ntk = (c_int32 * no.value)()
+    odims = (c_int32 * (4 * no.value))()
     rc = lib.gpt_graph_describe(byref(c), num_sms, byref(nt), byref(no), tasks, nt.value, types, ntk,
-                                no.value)
+                                odims, no.value)
     if rc != GPT_OK:
         raise GptError(rc, lib.gpt_last_error(None).decode())
     out = [(t.op, t.idx, [(t.wait_op[w], t.wait_need[w]) for w in range(t.nwait)]) for t in tasks]
+    if dims:
+        return out, list(types), list(ntk), [tuple(odims[4 * i:4 * i + 4]) for i in range(no.value)]
     return out, list(types), list(ntk)
 
 

@@ -94,21 +94,29 @@ __device__ __forceinline__ void mma_abt(float (*acc)[4], const uint32_t (*af)[4]
     }
 }
 
-// acc[8][4] (16 x 64) += P (16 x 64 in accumulator layout, k = 64) * B
+// Packs a 16 x 64 fp32 accumulator tile into bf16 A fragments (4 k-steps of 16).
+__device__ __forceinline__ void pack_a(const float (*p)[4], uint32_t (*pa)[4]) {
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    pa[t][0] = pack_bf16x2(p[2 * t][0], p[2 * t][1]);
+    pa[t][1] = pack_bf16x2(p[2 * t][2], p[2 * t][3]);
+    pa[t][2] = pack_bf16x2(p[2 * t + 1][0], p[2 * t + 1][1]);
+    pa[t][3] = pack_bf16x2(p[2 * t + 1][2], p[2 * t + 1][3]);
+  }
+}
+
+// acc[8][4] (16 x 64) += A (16 x 64, packed bf16 fragments, k = 64) * B
 // with B stored [k][n] (64 k-rows x 64 n) in a swizzled tile.
-__device__ __forceinline__ void mma_pb(float (*acc)[4], const float (*p)[4], uint32_t sb) {
+__device__ __forceinline__ void mma_pb(float (*acc)[4], const uint32_t (*pa)[4], uint32_t sb) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
-    uint32_t a[4] = {pack_bf16x2(p[2 * t][0], p[2 * t][1]), pack_bf16x2(p[2 * t][2], p[2 * t][3]),
-                     pack_bf16x2(p[2 * t + 1][0], p[2 * t + 1][1]),
-                     pack_bf16x2(p[2 * t + 1][2], p[2 * t + 1][3])};
 #pragma unroll
     for (int np = 0; np < 4; ++np) {
       uint32_t b[4];
       ldsm_x4_t(sb + swz(t * 16 + (lane & 7) + (((lane >> 3) & 1) << 3), np * 2 + (lane >> 4)), b);
-      mma16816(acc[2 * np], a, b[0], b[1]);
-      mma16816(acc[2 * np + 1], a, b[2], b[3]);
+      mma16816(acc[2 * np], pa[t], b[0], b[1]);
+      mma16816(acc[2 * np + 1], pa[t], b[2], b[3]);
     }
   }
 }
@@ -188,7 +196,9 @@ __device__ inline void task_attn_fwd_tc(const AttnArgs& a, int idx, uint8_t* sme
         l0 += s[nt][0] + s[nt][1];
         l1 += s[nt][2] + s[nt][3];
       }
-      mma_pb(o, s, vb);
+      uint32_t pa[4][4];
+      pack_a(s, pa);
+      mma_pb(o, pa, vb);
     }
     __syncthreads();
   }
@@ -315,8 +325,11 @@ __device__ inline void task_attn_bwd_kv_tc(const AttnArgs& a, int idx, uint8_t* 
         dp[nt][2] = p[nt][2] * (dp[nt][2] - d0) * a.scale;
         dp[nt][3] = p[nt][3] * (dp[nt][3] - d1) * a.scale;
       }
-      mma_pb(dv, p, ob_s);   // dV += P^T dO
-      mma_pb(dk, dp, qb_s);  // dK += dS^T Q
+      uint32_t pa[4][4], pd[4][4];  // P^T and dS^T as bf16 fragments (the fp32 tiles die here)
+      pack_a(p, pa);
+      pack_a(dp, pd);
+      mma_pb(dv, pa, ob_s);  // dV += P^T dO
+      mma_pb(dk, pd, qb_s);  // dK += dS^T Q
     }
     __syncthreads();
   }
@@ -394,7 +407,9 @@ __device__ inline void task_attn_bwd_q_tc(const AttnArgs& a, int idx, uint8_t* s
         p[nt][2] *= (dp[nt][2] - db) * a.scale;
         p[nt][3] *= (dp[nt][3] - db) * a.scale;
       }
-      mma_pb(dq, p, kb);  // dQ += dS K
+      uint32_t pa[4][4];
+      pack_a(p, pa);
+      mma_pb(dq, pa, kb);  // dQ += dS K
     }
     __syncthreads();
   }

@@ -436,6 +436,7 @@ int gemm_op(gpt* h, OpDesc* op, int M, int N, int K, Operand A, Operand B, int e
     g.BM = kSimtTile; g.BN = kSimtTile; g.BK = 16;
   }
   g.tiles_n = (N + g.BN - 1) / g.BN;
+  g.m_fastest = N > M ? 1 : 0;  // consecutive tasks share the tile of the larger operand
   const int tiles_m = (M + g.BM - 1) / g.BM;
   op->ntasks = tiles_m * g.tiles_n * ksplit;
   return GPT_OK;
@@ -677,7 +678,7 @@ size_t smem_needed(const gpt* h) {
   s = std::max(s, (size_t)(qblock * D.d + 64 * (D.d + 1) + qblock * D.T) * 4); // attention forward
   s = std::max(s, (size_t)(2 * qblock * D.d + 64 * (D.d + 1) + qblock * D.T + qblock) * 4);  // backward
   s = std::max(s, (size_t)kThreads * 4);
-  if (is_bf16(h->cfg)) s = std::max(s, (size_t)kTcSmemBytes);
+  if (is_bf16(h->cfg)) s = std::max(s, (size_t)kTcSmemBytes + 4 * kEpiStageBytes);
   return s + 1024;  // 1024-byte alignment slack
 }
 
@@ -1101,7 +1102,7 @@ static int run_test_graph(gpt& h, int32_t dtype) {
                              cudaMemcpyHostToDevice, h.stream) != cudaSuccess;
     if (bad) { result = GPT_ERR_CUDA; break; }
     h.kernel = dtype == GPT_DTYPE_BF16 ? step_kernel_bf16() : step_kernel_fp32();
-    h.smem_bytes = dtype == GPT_DTYPE_BF16 ? (size_t)kTcSmemBytes + 1024 : smem_needed(&h);
+    h.smem_bytes = dtype == GPT_DTYPE_BF16 ? (size_t)kTcSmemBytes + 4 * kEpiStageBytes + 1024 : smem_needed(&h);
     if (cudaFuncSetAttribute(h.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h.smem_bytes)) {
       result = GPT_ERR_CUDA;
       break;
@@ -1207,7 +1208,7 @@ int gpt_init_params_host(const gpt_config* cfg, uint64_t seed, float* dst, size_
 
 int gpt_graph_describe(const gpt_config* cfg, int32_t num_sms, int64_t* n_tasks, int32_t* n_ops,
                        gpt_task_info* tasks, int64_t max_tasks, int32_t* op_types, int32_t* op_tasks,
-                       int32_t max_ops) {
+                       int32_t* op_dims, int32_t max_ops) {
   if (!cfg || !n_tasks || !n_ops) return fail(nullptr, GPT_ERR_INVALID_ARG, "NULL argument");
   std::string why;
   int rc = validate(*cfg, &why);
@@ -1240,6 +1241,12 @@ int gpt_graph_describe(const gpt_config* cfg, int32_t num_sms, int64_t* n_tasks,
   for (int32_t i = 0; i < std::min<int32_t>(max_ops, (int32_t)h.ops.size()); ++i) {
     if (op_types) op_types[i] = h.ops[i].type;
     if (op_tasks) op_tasks[i] = h.ops[i].ntasks;
+    if (op_dims) {
+      const bool g = h.ops[i].type == OP_GEMM;
+      const GemmArgs& a = h.ops[i].gemm;
+      const int32_t v[4] = {g ? a.M : 0, g ? a.N : 0, g ? a.K : 0, g ? a.BN : 0};
+      for (int k = 0; k < 4; ++k) op_dims[4 * i + k] = v[k];
+    }
   }
   return GPT_OK;
 }

@@ -25,7 +25,8 @@ constexpr int kTcStageA = kTcBM * kTcBK * 2;          // 16 KB
 constexpr int kTcStageB = 256 * kTcBK * 2;            // 32 KB (BN <= 256)
 constexpr int kTcStageBytes = kTcStageA + kTcStageB;  // 48 KB
 constexpr int kTcSmemBytes = kTcStages * kTcStageBytes;
-constexpr int kTmemCols = 256;            // one fp32 accumulator of up to 128 x 256
+constexpr int kEpiStageBytes = 32 * 64 * 4;            // per epilogue warp: 32 rows x 64 fp32
+constexpr int kTmemCols = 512;            // two fp32 accumulators of up to 128 x 256
 constexpr int kThreads = 256;     // threads of every persistent block
 constexpr int kWarps = kThreads / 32;
 
@@ -61,6 +62,7 @@ struct GemmArgs {
   int32_t M, N, K;          // C[M, N] = sum_k A(m, k) B(n, k)
   int32_t BM, BN, BK;       // tile shape of one task
   int32_t tiles_n, ksplit;  // tasks = tiles_m * tiles_n * ksplit
+  int32_t m_fastest;        // task order: 1 = M tiles vary fastest (B tile reused by consecutive tasks)
   // element access for the SIMT path: A(m,k) = A[m*sam + k*sak], B(n,k) = B[n*sbn + k*sbk]
   const void* A; int64_t sam, sak;
   const void* B; int64_t sbn, sbk;

@@ -18,7 +18,7 @@
 namespace pgs {
 
 struct KernelShared {
-  uint64_t bars[2 * kTcStages + 1];
+  GemmShared gemm;
   uint32_t tmem_base;
   int32_t ok;
   int64_t task;
@@ -36,10 +36,9 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
   if constexpr (kTC) {
     if (threadIdx.x == 0) {
       for (int i = 0; i < kTcStages; ++i) {
-        mbar_init(smem_u32(&sh.bars[i]), 1);               // full: producer arrive + tx bytes
-        mbar_init(smem_u32(&sh.bars[kTcStages + i]), 1);   // empty: one MMA commit
+        mbar_init(smem_u32(&sh.gemm.stage_full[i]), 1);   // producer arrive + tx bytes
+        mbar_init(smem_u32(&sh.gemm.stage_empty[i]), 1);  // one MMA commit
       }
-      mbar_init(smem_u32(&sh.bars[2 * kTcStages]), 1);     // accumulator ready
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -49,12 +48,13 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
     tc_fence_after();
   }
 
+  int64_t pending = -1;  // ticket claimed by a GEMM run, dependencies not yet waited
   for (;;) {
     if (threadIdx.x == 0) {
       int64_t t = kp.ntasks;
       int ok = 0;
       if (ld_volatile_u32(&kp.err[0]) == 0u) {
-        t = (int64_t)(atomicAdd(kp.ticket, 1ull) - kp.ticket_base);
+        t = pending >= 0 ? pending : (int64_t)(atomicAdd(kp.ticket, 1ull) - kp.ticket_base);
         if (t < kp.ntasks) {
           ok = 1;
           const uint64_t t_claim = kp.trace ? globaltimer_ns() : 0;
@@ -77,49 +77,59 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
     __syncthreads();
     const int64_t t = sh.task;
     if (!sh.ok || t >= kp.ntasks) break;
+    pending = -1;
     const TaskDesc& d = kp.tasks[t];
     const OpDesc& op = kp.ops[d.op];
     const int idx = d.idx;
+    if constexpr (kTC) {
+      if (op.type == OP_GEMM) {
+        pending = gemm_run(kp, t, sh.gemm, smem, sh.tmem_base, st, gelu_tanh != 0);
+        continue;  // the run released its tasks
+      }
+    }
     switch (op.type) {
-      case OP_EMBED: task_embed<act_t>(kp, op.emb, idx); break;
-      case OP_LN_FWD: task_ln_fwd<act_t>(op.lnf, idx); break;
+      case OP_EMBED: { const EmbedArgs a = op.emb; task_embed<act_t>(kp, a, idx); } break;
+      case OP_LN_FWD: { const LnFwdArgs a = op.lnf; task_ln_fwd<act_t>(a, idx); } break;
       case OP_GEMM:
-        if constexpr (kTC) {
-          if (threadIdx.x == 0) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncthreads();
-          task_gemm_tc(kp, op.gemm, idx, smem, sh.bars, sh.tmem_base, st, gelu_tanh != 0);
-        } else {
-          task_gemm_simt<act_t>(op.gemm, idx, reinterpret_cast<float*>(smem), gelu_tanh != 0);
+        if constexpr (!kTC) {
+          const GemmArgs a = op.gemm;
+          task_gemm_simt<act_t>(a, idx, reinterpret_cast<float*>(smem), gelu_tanh != 0);
         }
         break;
       case OP_ATTN_FWD:
-        if constexpr (kTC) task_attn_fwd_tc(op.attn, idx, smem);
-        else task_attn_fwd_simt<act_t>(op.attn, idx, reinterpret_cast<float*>(smem));
-        break;
-      case OP_ATTN_BWD_PRE:
-        if constexpr (kTC) task_attn_bwd_pre(op.attn, idx);
-        break;
-      case OP_ATTN_BWD_KV:
-        if constexpr (kTC) task_attn_bwd_kv_tc(op.attn, idx, smem);
-        break;
-      case OP_ATTN_BWD_Q:
-        if constexpr (kTC) task_attn_bwd_q_tc(op.attn, idx, smem);
-        break;
-      case OP_CE:
-        if constexpr (kTC) {
-          if ((op.ce.V & 7) == 0) task_ce_bf16_vec(kp, op.ce, idx);
-          else task_ce<act_t>(kp, op.ce, idx);
-        } else {
-          task_ce<act_t>(kp, op.ce, idx);
+        {
+          const AttnArgs a = op.attn;
+          if constexpr (kTC) task_attn_fwd_tc(a, idx, smem);
+          else task_attn_fwd_simt<act_t>(a, idx, reinterpret_cast<float*>(smem));
         }
         break;
-      case OP_LOSS: task_loss(kp, op.loss, reinterpret_cast<float*>(smem)); break;
-      case OP_LN_BWD: task_ln_bwd<act_t>(op.lnb, idx, reinterpret_cast<float*>(smem)); break;
-      case OP_COLSUM: task_colsum<act_t>(op.colsum, idx, reinterpret_cast<float*>(smem)); break;
-      case OP_ATTN_BWD: task_attn_bwd_simt<act_t>(op.attn, idx, reinterpret_cast<float*>(smem)); break;
-      case OP_EMBED_BWD_WTE: task_embed_bwd_wte(kp, op.emb, idx, reinterpret_cast<int*>(smem)); break;
-      case OP_EMBED_BWD_WPE: task_embed_bwd_wpe(op.emb, idx); break;
-      case OP_ADAMW: task_adamw(kp, op.adam, idx); break;
+      case OP_ATTN_BWD_PRE:
+        if constexpr (kTC) { const AttnArgs a = op.attn; task_attn_bwd_pre(a, idx); }
+        break;
+      case OP_ATTN_BWD_KV:
+        if constexpr (kTC) { const AttnArgs a = op.attn; task_attn_bwd_kv_tc(a, idx, smem); }
+        break;
+      case OP_ATTN_BWD_Q:
+        if constexpr (kTC) { const AttnArgs a = op.attn; task_attn_bwd_q_tc(a, idx, smem); }
+        break;
+      case OP_CE:
+        {
+          const CeArgs a = op.ce;
+          if constexpr (kTC) {
+            if ((a.V & 7) == 0) task_ce_bf16_vec(kp, a, idx);
+            else task_ce<act_t>(kp, a, idx);
+          } else {
+            task_ce<act_t>(kp, a, idx);
+          }
+        }
+        break;
+      case OP_LOSS: { const LossArgs a = op.loss; task_loss(kp, a, reinterpret_cast<float*>(smem)); } break;
+      case OP_LN_BWD: { const LnBwdArgs a = op.lnb; task_ln_bwd<act_t>(a, idx, reinterpret_cast<float*>(smem)); } break;
+      case OP_COLSUM: { const ColsumArgs a = op.colsum; task_colsum<act_t>(a, idx, reinterpret_cast<float*>(smem)); } break;
+      case OP_ATTN_BWD: { const AttnArgs a = op.attn; task_attn_bwd_simt<act_t>(a, idx, reinterpret_cast<float*>(smem)); } break;
+      case OP_EMBED_BWD_WTE: { const EmbedArgs a = op.emb; task_embed_bwd_wte(kp, a, idx, reinterpret_cast<int*>(smem)); } break;
+      case OP_EMBED_BWD_WPE: { const EmbedArgs a = op.emb; task_embed_bwd_wpe(a, idx); } break;
+      case OP_ADAMW: { const AdamArgs a = op.adam; task_adamw(kp, a, idx); } break;
       default: break;
     }
     __syncthreads();

@@ -6,6 +6,16 @@
 
 namespace pgs {
 
+// Tile of GEMM task idx: split-major, then M- or N-fastest as the host chose.
+__device__ __forceinline__ void gemm_coords(const GemmArgs& g, int idx, int& tm, int& tn, int& split) {
+  const int tiles_m = (g.M + g.BM - 1) / g.BM;
+  const int per_split = tiles_m * g.tiles_n;
+  split = idx / per_split;
+  const int r = idx - split * per_split;
+  if (g.m_fastest) { tm = r % tiles_m; tn = r / tiles_m; }
+  else { tn = r % g.tiles_n; tm = r / g.tiles_n; }
+}
+
 // ---- GEMM epilogue, one element ----------------------------------------------
 template <typename act_t>
 __device__ __forceinline__ void epilogue_one(const GemmArgs& g, int split, int m, int n, float acc,
@@ -39,10 +49,8 @@ constexpr int kSimtBM = kSimtTile, kSimtBN = kSimtTile, kSimtBK = 16;
 
 template <typename act_t>
 __device__ inline void task_gemm_simt(const GemmArgs& g, int idx, float* smem, bool gelu_tanh) {
-  const int tiles_m = (g.M + g.BM - 1) / g.BM;
-  const int tn = idx % g.tiles_n;
-  const int tm = (idx / g.tiles_n) % tiles_m;
-  const int split = idx / (g.tiles_n * tiles_m);
+  int tm, tn, split;
+  gemm_coords(g, idx, tm, tn, split);
   const int kchunk = (g.K + g.ksplit - 1) / g.ksplit;
   const int k0 = split * kchunk, k1 = min(g.K, k0 + kchunk);
   const int m0 = tm * kSimtBM, n0 = tn * kSimtBN;

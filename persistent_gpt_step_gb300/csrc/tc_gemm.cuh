@@ -11,6 +11,7 @@
 //   weight grad   C = dY^T X   A = dY [K,M] MN-major,  B = X [K,N] MN-major
 #pragma once
 #include "device.cuh"
+#include "tasks_simt.cuh"
 
 namespace pgs {
 
@@ -113,6 +114,26 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// Issue-only variant: the registers are valid after tmem_ld_wait16 on them.
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15},"
+      " [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+// Waits for this thread's outstanding tcgen05.ld; the register operands tie
+// every later use of r to the wait, so no use is scheduled before it.
+__device__ __forceinline__ void tmem_ld_wait16(uint32_t* r) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+}
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and
 // stride byte offsets (>> 4), fixed version 1 at bit 46, 128-byte swizzle (2) at bits 61-63.
@@ -127,7 +148,26 @@ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn)
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// ---- epilogue on 16 consecutive columns of one row ------------------------------------
+// ---- epilogue on 64 consecutive columns of one row ------------------------------------
+// GELU on the bf16 path uses the SFU tanh (tanh.approx.f32, relative error about
+// 2^-11), below the bf16 rounding of the stored result.
+__device__ __forceinline__ float tanh_sfu(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float gelu_bf(float x, bool tanh_form) {
+  if (!tanh_form) return gelu_f(x, false);
+  const float k0 = 0.7978845608028654f;
+  return 0.5f * x * (1.0f + tanh_sfu(k0 * (x + 0.044715f * x * x * x)));
+}
+__device__ __forceinline__ float gelu_grad_bf(float x, bool tanh_form) {
+  if (!tanh_form) return gelu_grad_f(x, false);
+  const float k0 = 0.7978845608028654f;
+  const float t = tanh_sfu(k0 * (x + 0.044715f * x * x * x));
+  return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * k0 * (1.0f + 3.0f * 0.044715f * x * x);
+}
+
 __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float* v) {
   uint4 u0, u1;
   __nv_bfloat162* h0 = reinterpret_cast<__nv_bfloat162*>(&u0);
@@ -141,137 +181,337 @@ __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float* v
   reinterpret_cast<uint4*>(dst)[1] = u1;
 }
 
-__device__ __forceinline__ void epilogue16(const GemmArgs& g, int split, int m, int n, float* v,
-                                           bool gelu_tanh) {
-  if (g.bias && g.epi != EPI_F32 && g.epi != EPI_GELU_BWD) {
-    const float4* b4 = reinterpret_cast<const float4*>(g.bias + n);
+// One epilogue warp's part of a finished tile: TMEM lane quarter (32 rows from
+// row0), all BN columns, in 64-column groups.  The accumulators go TMEM ->
+// registers -> a per-warp 32 x 64 fp32 staging tile in shared memory (16-byte
+// chunks XOR-swizzled by row) -> back to registers in a row-contiguous layout:
+// thread u owns columns 4 (u mod 16) .. +3 of rows 2i + u / 16, so bias,
+// residual, GELU and the stores touch whole 256-byte row segments.
+struct EpiPtrs {
+  void* out; int64_t ldo;      // EPI_F32: already offset to the split's partial
+  void* out2; int64_t ldo2;
+  const float* bias;
+  const float* resid; int64_t ldr;
+  const __nv_bfloat16* aux; int64_t ldaux;
+};
+
+template <int EPI>
+static __device__ __noinline__ void epi_tile(const int M, const int N, const int BN, const int row0, const int n0,
+                                             const uint32_t tbase, uint8_t* stage, void* const out,
+                                             const int64_t ldo, void* const out2, const int64_t ldo2,
+                                             const float* const bias, const void* const src, const int64_t lds,
+                                             const bool gelu_tanh) {
+  const int lane = threadIdx.x & 31;
+  const int cu = 4 * (lane & 15);  // this thread's first column within the group
+  const int ru = lane >> 4;        // row parity
+  for (int c = 0; c < BN; c += 64) {  // N is a multiple of 64: groups are all in or all out
+    const int n = n0 + c;
+    if (n >= N) break;
+    {
+      uint32_t r[4][16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float4 b = b4[i];
-      v[4 * i] += b.x; v[4 * i + 1] += b.y; v[4 * i + 2] += b.z; v[4 * i + 3] += b.w;
+      for (int j = 0; j < 4; ++j) tmem_ld16_issue(tbase + (uint32_t)(c + 16 * j), r[j]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) tmem_ld_wait16(r[j]);
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int ch = 4 * j + h;  // 16-byte chunk of this thread's row
+          *reinterpret_cast<uint4*>(stage + lane * 256 + ((ch ^ (lane & 15)) << 4)) =
+              make_uint4(r[j][4 * h], r[j][4 * h + 1], r[j][4 * h + 2], r[j][4 * h + 3]);
+        }
+      __syncwarp();
     }
-  }
-  switch (g.epi) {
-    case EPI_STORE:
-      store_bf16x16(reinterpret_cast<__nv_bfloat16*>(g.out) + (int64_t)m * g.ldo + n, v);
-      break;
-    case EPI_RESID: {
-      const float4* r4 = reinterpret_cast<const float4*>(g.resid + (int64_t)m * g.ldr + n);
-      float4* o4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(g.out) + (int64_t)m * g.ldo + n);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float4 r = r4[i];
-        o4[i] = make_float4(r.x + v[4 * i], r.y + v[4 * i + 1], r.z + v[4 * i + 2], r.w + v[4 * i + 3]);
+    const int col = n + cu;
+    float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (EPI != EPI_F32 && EPI != EPI_GELU_BWD && bias) b = *reinterpret_cast<const float4*>(bias + col);
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+      const int rl = ru + 2 * i;
+      const int m = row0 + rl;
+      if (m >= M) break;  // rows ascend with i
+      float4 v = *reinterpret_cast<const float4*>(stage + rl * 256 + (((lane & 15) ^ (rl & 15)) << 4));
+      v.x += b.x; v.y += b.y; v.z += b.z; v.w += b.w;
+      if constexpr (EPI == EPI_STORE || EPI == EPI_GELU) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + (int64_t)m * ldo + col) =
+            make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+        if constexpr (EPI == EPI_GELU) {
+          lo = __floats2bfloat162_rn(gelu_bf(v.x, gelu_tanh), gelu_bf(v.y, gelu_tanh));
+          hi = __floats2bfloat162_rn(gelu_bf(v.z, gelu_tanh), gelu_bf(v.w, gelu_tanh));
+          *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out2) + (int64_t)m * ldo2 + col) =
+              make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+        }
+      } else if constexpr (EPI == EPI_RESID) {
+        const float4 rr = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + (int64_t)m * lds + col);
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (int64_t)m * ldo + col) =
+            make_float4(rr.x + v.x, rr.y + v.y, rr.z + v.z, rr.w + v.w);
+      } else if constexpr (EPI == EPI_F32) {
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (int64_t)m * ldo + col) = v;
+      } else if constexpr (EPI == EPI_GELU_BWD) {
+        const uint2 hv = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(src) +
+                                                         (int64_t)m * lds + col);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hv.x));
+        const float2 e = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hv.y));
+        __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * gelu_grad_bf(a.x, gelu_tanh), v.y * gelu_grad_bf(a.y, gelu_tanh));
+        __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * gelu_grad_bf(e.x, gelu_tanh), v.w * gelu_grad_bf(e.y, gelu_tanh));
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + (int64_t)m * ldo + col) =
+            make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
       }
-    } break;
-    case EPI_GELU: {
-      store_bf16x16(reinterpret_cast<__nv_bfloat16*>(g.out) + (int64_t)m * g.ldo + n, v);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] = gelu_f(v[i], gelu_tanh);
-      store_bf16x16(reinterpret_cast<__nv_bfloat16*>(g.out2) + (int64_t)m * g.ldo2 + n, v);
-    } break;
-    case EPI_F32: {
-      float4* o4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(g.out) + split * g.split_stride +
-                                             (int64_t)m * g.ldo + n);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-    } break;
-    case EPI_GELU_BWD: {
-      const uint4* h4 = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(g.aux) +
-                                                       (int64_t)m * g.ldaux + n);
-      uint4 hu[2] = {h4[0], h4[1]};
-      const __nv_bfloat16* hb = reinterpret_cast<const __nv_bfloat16*>(hu);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) v[i] *= gelu_grad_f(__bfloat162float(hb[i]), gelu_tanh);
-      store_bf16x16(reinterpret_cast<__nv_bfloat16*>(g.out) + (int64_t)m * g.ldo + n, v);
-    } break;
+    }
   }
 }
 
-// ---- the GEMM task -----------------------------------------------------------------------
-// smem_tiles: 1024-byte aligned ring of kTcStages stages; bars: full[S], empty[S], acc.
-__device__ inline void task_gemm_tc(const KParams& kp, const GemmArgs& g, int idx, uint8_t* smem_tiles,
-                             uint64_t* bars, uint32_t tmem_base, TcState& st, bool gelu_tanh) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tiles_m = (g.M + kTcBM - 1) / kTcBM;
-  const int tn = idx % g.tiles_n;
-  const int tm = (idx / g.tiles_n) % tiles_m;
-  const int split = idx / (g.tiles_n * tiles_m);
-  const int BN = g.BN;
-  const int kchunk = (g.K + g.ksplit - 1) / g.ksplit;  // multiple of kTcBK (host checks)
-  const int k0 = split * kchunk;
-  const int nkb = (min(g.K, k0 + kchunk) - k0 + kTcBK - 1) / kTcBK;
-  const int m0 = tm * kTcBM, n0 = tn * BN;
-  const uint8_t* maps = reinterpret_cast<const uint8_t*>(kp.tmaps);  // 128-byte CUtensorMaps
-  const void* amap = maps + 128 * g.a_map;
-  const void* bmap = maps + 128 * g.b_map;
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kTcStages),
-                 accb = smem_u32(bars + 2 * kTcStages);
-  const uint32_t tiles0 = smem_u32(smem_tiles);
-  const uint32_t bytes = kTcStageA + (uint32_t)BN * kTcBK * 2;
+__device__ __forceinline__ void epilogue_tile(const GemmArgs& g, int split, int row0, int n0, uint32_t tbase,
+                                              uint8_t* stage, bool gelu_tanh) {
+  switch (g.epi) {
+    case EPI_STORE:
+      epi_tile<EPI_STORE>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, g.bias, nullptr, 0,
+                          gelu_tanh);
+      break;
+    case EPI_RESID:
+      epi_tile<EPI_RESID>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, g.bias, g.resid, g.ldr,
+                          gelu_tanh);
+      break;
+    case EPI_GELU:
+      epi_tile<EPI_GELU>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, g.out2, g.ldo2, g.bias, nullptr, 0,
+                         gelu_tanh);
+      break;
+    case EPI_F32:
+      epi_tile<EPI_F32>(g.M, g.N, g.BN, row0, n0, tbase, stage,
+                        reinterpret_cast<float*>(g.out) + split * g.split_stride, g.ldo, nullptr, 0, nullptr,
+                        nullptr, 0, gelu_tanh);
+      break;
+    case EPI_GELU_BWD:
+      epi_tile<EPI_GELU_BWD>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, nullptr, g.aux,
+                             g.ldaux, gelu_tanh);
+      break;
+  }
+}
 
-  if (warp == 0 && lane == 0) {
-    // ---- producer: TMA loads of A and B k-blocks into the ring ----
-    fence_proxy_async_global();  // operands written by other blocks' generic stores
-    for (int kb = 0; kb < nkb; ++kb) {
-      if (!mbar_wait(kp, empty0 + 8 * st.prod_stage, st.prod_phase ^ 1u)) break;
-      const uint32_t full = full0 + 8 * st.prod_stage;
-      mbar_arrive_expect_tx(full, bytes);
-      const uint32_t sa = tiles0 + st.prod_stage * kTcStageBytes;
-      const uint32_t sb = sa + kTcStageA;
-      const int kk = k0 + kb * kTcBK;
-      if (!g.a_mn) {
-        tma_load_2d(sa, amap, kk, m0, full);
-      } else {
-        tma_load_2d(sa, amap, m0, kk, full);
-        tma_load_2d(sa + 8192, amap, m0 + 64, kk, full);
-      }
-      if (!g.b_mn) {
-        tma_load_2d(sb, bmap, kk, n0, full);
-      } else {
-        for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + 8192 * j, bmap, n0 + 64 * j, kk, full);
-      }
-      if (++st.prod_stage == kTcStages) { st.prod_stage = 0; st.prod_phase ^= 1u; }
+// ---- GEMM runs: warp-specialised pipeline over consecutive GEMM tasks ---------------
+//
+// While a block's current task is a GEMM, its warps split into roles that each
+// loop over the same sequence of GEMM tasks:
+//   warp 2 lane 0  scheduler: claims the next ticket ahead of time, waits for
+//                  its dependencies, hands it over through a 2-slot queue;
+//   warp 0 lane 0  TMA producer: k-blocks of A and B into the stage ring;
+//   warp 1 lane 0  MMA issuer: tcgen05.mma into one of two TMEM accumulators;
+//   warps 4..7     epilogue: TMEM -> registers -> fused epilogue -> global,
+//                  then the task's release.
+// Tile i+1's loads and MMAs therefore overlap tile i's epilogue.  The run ends
+// when the scheduler claims a task that is not a GEMM (or the graph ends); that
+// ticket goes back to the main loop, dependencies not yet waited.
+struct GemmShared {
+  uint64_t stage_full[kTcStages], stage_empty[kTcStages];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t q_full[2], q_empty[2];
+  int64_t q_task[2];
+  int64_t next;
+};
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void epi_bar_sync() {  // the four epilogue warps
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+__device__ __forceinline__ bool gemm_task_ready(const KParams& kp, int64_t t) {
+  const TaskDesc& d = kp.tasks[t];
+  bool ok = true;
+  for (int w = 0; w < d.nwait && ok; ++w)
+    ok = wait_counter(kp, d.wait_ctr[w], kp.epoch * (unsigned long long)d.wait_need[w], (uint32_t)t);
+  return ok;
+}
+
+// Runs GEMM tasks starting with t_first (claimed, dependencies satisfied) and
+// returns the next claimed ticket (not a GEMM, or >= ntasks).
+__device__ inline int64_t gemm_run(const KParams& kp, int64_t t_first, GemmShared& gs, uint8_t* smem_tiles,
+                                   uint32_t tmem_base, TcState& st, bool gelu_tanh) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t q_full0 = smem_u32(&gs.q_full[0]), q_empty0 = smem_u32(&gs.q_empty[0]);
+  const uint32_t acc_full0 = smem_u32(&gs.acc_full[0]), acc_empty0 = smem_u32(&gs.acc_empty[0]);
+  const uint32_t full0 = smem_u32(&gs.stage_full[0]), empty0 = smem_u32(&gs.stage_empty[0]);
+  const uint32_t tiles0 = smem_u32(smem_tiles);
+  const uint8_t* maps = reinterpret_cast<const uint8_t*>(kp.tmaps);  // 128-byte CUtensorMaps
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(q_full0 + 8 * i, 1);
+      mbar_init(q_empty0 + 8 * i, 3);    // producer, MMA, epilogue leader
+      mbar_init(acc_full0 + 8 * i, 1);   // MMA commit
+      mbar_init(acc_empty0 + 8 * i, 4);  // one arrive per epilogue warp
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer ----
-    const uint32_t idesc = idesc_bf16(kTcBM, BN, g.a_mn, g.b_mn);
-    for (int kb = 0; kb < nkb; ++kb) {
-      if (!mbar_wait(kp, full0 + 8 * st.mma_stage, st.mma_phase)) break;
-      tc_fence_after();
-      const uint32_t sa = tiles0 + st.mma_stage * kTcStageBytes;
-      const uint32_t sb = sa + kTcStageA;
+    gs.q_task[0] = t_first;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == 2) {
+    if (lane == 0) {
+      // ---- scheduler ----
+      mbar_arrive(q_full0);  // fill 0 = t_first
+      for (uint32_t i = 1;; ++i) {
+        int64_t t = kp.ntasks;
+        bool gemm = false;
+        if (ld_volatile_u32(&kp.err[0]) == 0u) {
+          t = (int64_t)(atomicAdd(kp.ticket, 1ull) - kp.ticket_base);
+          if (t < kp.ntasks && kp.ops[kp.tasks[t].op].type == OP_GEMM) {
+            const uint64_t t_claim = kp.trace ? globaltimer_ns() : 0;
+            gemm = gemm_task_ready(kp, t);
+            if (!gemm) t = kp.ntasks;  // a wait failed: stop the run, the main loop drains
+            else if (kp.trace) {
+              kp.trace[4 * t + 0] = t_claim;
+              kp.trace[4 * t + 1] = globaltimer_ns();
+              uint32_t smid;
+              asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+              kp.trace[4 * t + 3] = smid;
+            }
+          }
+        }
+        const uint32_t slot = i & 1;
+        if (i >= 2 && !mbar_wait(kp, q_empty0 + 8 * slot, ((i >> 1) - 1) & 1)) {
+          gs.next = kp.ntasks;
+          break;
+        }
+        gs.q_task[slot] = gemm ? t : -2 - t;
+        mbar_arrive(q_full0 + 8 * slot);
+        if (!gemm) {
+          gs.next = t;
+          break;
+        }
+      }
+    }
+  } else if (warp == 0) {
+    if (lane == 0) {
+      // ---- TMA producer ----
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // smem last written by generic stores
+      for (uint32_t i = 0;; ++i) {
+        const uint32_t slot = i & 1;
+        if (!mbar_wait(kp, q_full0 + 8 * slot, (i >> 1) & 1)) break;
+        const int64_t t = gs.q_task[slot];
+        mbar_arrive(q_empty0 + 8 * slot);
+        if (t < 0) break;
+        fence_proxy_async_global();  // operands written by other blocks' generic stores
+        const GemmArgs g = kp.ops[kp.tasks[t].op].gemm;
+        int tm, tn, split;
+        gemm_coords(g, kp.tasks[t].idx, tm, tn, split);
+        const int kchunk = (g.K + g.ksplit - 1) / g.ksplit;
+        const int k0 = split * kchunk;
+        const int nkb = (min(g.K, k0 + kchunk) - k0 + kTcBK - 1) / kTcBK;
+        const int m0 = tm * kTcBM, n0 = tn * g.BN;
+        const void* amap = maps + 128 * g.a_map;
+        const void* bmap = maps + 128 * g.b_map;
+        const uint32_t bytes = kTcStageA + (uint32_t)g.BN * kTcBK * 2;
+        bool ok = true;
+        for (int kb = 0; kb < nkb && ok; ++kb) {
+          ok = mbar_wait(kp, empty0 + 8 * st.prod_stage, st.prod_phase ^ 1u);
+          if (!ok) break;
+          const uint32_t full = full0 + 8 * st.prod_stage;
+          mbar_arrive_expect_tx(full, bytes);
+          const uint32_t sa = tiles0 + st.prod_stage * kTcStageBytes;
+          const uint32_t sb = sa + kTcStageA;
+          const int kk = k0 + kb * kTcBK;
+          if (!g.a_mn) {
+            tma_load_2d(sa, amap, kk, m0, full);
+          } else {
+            tma_load_2d(sa, amap, m0, kk, full);
+            tma_load_2d(sa + 8192, amap, m0 + 64, kk, full);
+          }
+          if (!g.b_mn) {
+            tma_load_2d(sb, bmap, kk, n0, full);
+          } else {
+            for (int j = 0; j < g.BN / 64; ++j) tma_load_2d(sb + 8192 * j, bmap, n0 + 64 * j, kk, full);
+          }
+          if (++st.prod_stage == kTcStages) { st.prod_stage = 0; st.prod_phase ^= 1u; }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer ----
+      for (uint32_t i = 0;; ++i) {
+        const uint32_t slot = i & 1;
+        if (!mbar_wait(kp, q_full0 + 8 * slot, (i >> 1) & 1)) break;
+        const int64_t t = gs.q_task[slot];
+        mbar_arrive(q_empty0 + 8 * slot);
+        if (t < 0) break;
+        const uint32_t buf = i & 1;  // i counts this run's GEMM tasks (stop comes last)
+        if (i >= 2 && !mbar_wait(kp, acc_empty0 + 8 * buf, ((i >> 1) - 1) & 1)) break;
+        tc_fence_after();
+        const GemmArgs g = kp.ops[kp.tasks[t].op].gemm;
+        int tm, tn, split;
+        gemm_coords(g, kp.tasks[t].idx, tm, tn, split);
+        const int kchunk = (g.K + g.ksplit - 1) / g.ksplit;
+        const int k0 = split * kchunk;
+        const int nkb = (min(g.K, k0 + kchunk) - k0 + kTcBK - 1) / kTcBK;
+        const uint32_t idesc = idesc_bf16(kTcBM, g.BN, g.a_mn, g.b_mn);
+        const uint32_t d_tmem = tmem_base + buf * 256;
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          ok = mbar_wait(kp, full0 + 8 * st.mma_stage, st.mma_phase);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t sa = tiles0 + st.mma_stage * kTcStageBytes;
+          const uint32_t sb = sa + kTcStageA;
 #pragma unroll
-      for (int k = 0; k < kTcBK / 16; ++k) {
-        const uint64_t ad = g.a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
-                                   : smem_desc_sw128(sa + k * 32, 16, 1024);
-        const uint64_t bd = g.b_mn ? smem_desc_sw128(sb + k * 2048, 8192, 1024)
-                                   : smem_desc_sw128(sb + k * 32, 16, 1024);
-        tc_mma(tmem_base, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < kTcBK / 16; ++k) {
+            const uint64_t ad = g.a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
+                                       : smem_desc_sw128(sa + k * 32, 16, 1024);
+            const uint64_t bd = g.b_mn ? smem_desc_sw128(sb + k * 2048, 8192, 1024)
+                                       : smem_desc_sw128(sb + k * 32, 16, 1024);
+            tc_mma(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(empty0 + 8 * st.mma_stage);  // frees the stage once these MMAs have read it
+          if (++st.mma_stage == kTcStages) { st.mma_stage = 0; st.mma_phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(acc_full0 + 8 * buf);  // accumulator complete
       }
-      tc_commit(empty0 + 8 * st.mma_stage);  // frees the stage once these MMAs have read it
-      if (++st.mma_stage == kTcStages) { st.mma_stage = 0; st.mma_phase ^= 1u; }
     }
-    tc_commit(accb);  // accumulator complete
+  } else if (warp >= 4) {
+    // ---- epilogue (warps 4..7 read TMEM lane quarters 0..3) ----
+    const int q = warp & 3;
+    for (uint32_t i = 0;; ++i) {
+      const uint32_t slot = i & 1;
+      if (!mbar_wait(kp, q_full0 + 8 * slot, (i >> 1) & 1)) break;
+      const int64_t t = gs.q_task[slot];
+      if (t < 0) {
+        epi_bar_sync();
+        if (warp == 4 && lane == 0) mbar_arrive(q_empty0 + 8 * slot);
+        break;
+      }
+      const uint32_t buf = i & 1;
+      const bool ok = mbar_wait(kp, acc_full0 + 8 * buf, (i >> 1) & 1);
+      tc_fence_after();
+      const GemmArgs g = kp.ops[kp.tasks[t].op].gemm;
+      int tm, tn, split;
+      gemm_coords(g, kp.tasks[t].idx, tm, tn, split);
+      if (ok)
+        epilogue_tile(g, split, tm * kTcBM + q * 32, tn * g.BN, tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256,
+                      smem_tiles + kTcSmemBytes + (warp - 4) * kEpiStageBytes, gelu_tanh);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty0 + 8 * buf);
+      epi_bar_sync();
+      if (warp == 4 && lane == 0) {
+        mbar_arrive(q_empty0 + 8 * slot);
+        if (t != kp.skip_release) {
+          __threadfence();
+          fence_proxy_async_global();
+          red_release_add_u64(kp.counters + kp.tasks[t].op, 1ull);
+        }
+        if (kp.trace) kp.trace[4 * t + 2] = globaltimer_ns();
+      }
+      if (!ok) break;
+    }
   }
   __syncwarp();
-
-  // ---- epilogue: all 8 warps; warp w reads TMEM lanes 32 (w % 4).., column half w / 4 ----
-  const bool ok = mbar_wait(kp, accb, st.acc_phase);
-  st.acc_phase ^= 1u;
-  tc_fence_after();
-  if (ok) {
-    const int q = warp & 3, half = warp >> 2;
-    const int row = m0 + q * 32 + lane;
-    const int cbeg = half * (BN / 2), cend = cbeg + BN / 2;
-    for (int c = cbeg; c < cend; c += 16) {
-      float v[16];
-      tmem_ld16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)c, v);
-      const int n = n0 + c;
-      if (row < g.M && n < g.N) epilogue16(g, split, row, n, v, gelu_tanh);
-    }
-  }
-  tc_fence_before();
+  __syncthreads();
+  return gs.next;
 }
 
 }  // namespace pgs

@@ -56,7 +56,7 @@ def main():
     from . import inputs as I
     cfg = I.CONFIGS[args.config]
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    tasks, op_types, _ = B.describe_graph(cfg, sms)
+    tasks, op_types, op_ntasks, op_dims = B.describe_graph(cfg, sms, dims=True)
     task_ops = np.array([t[0] for t in tasks])
     with B.GPT(cfg, seed=1234) as m:
         n, grid, _ = m.graph_info()
@@ -72,6 +72,20 @@ def main():
     print(f"{'family':20s} {'tasks':>7s} {'busy ms':>9s} {'wait ms':>9s} {'span ms':>9s} {'first':>8s} {'last':>8s}")
     for r in sorted(rows, key=lambda r: -r[2]):
         print(f"{r[0]:20s} {r[1]:7d} {r[2]:9.3f} {r[3]:9.3f} {r[4]:9.3f} {r[5]:8.3f} {r[6]:8.3f}")
+    # per-op spans of the GEMMs (first start to last end), with their achieved rate
+    start = tr[:, 1].astype(np.int64)
+    end = tr[:, 2].astype(np.int64)
+    t0 = start.min()
+    print(f"\n{'gemm op':>7s} {'M':>6s} {'N':>6s} {'K':>6s} {'BN':>4s} {'tiles':>6s} {'span us':>8s} {'TF/s':>7s} "
+          f"{'begin':>8s}")
+    for o, ty in enumerate(op_types):
+        if ty != 2:
+            continue
+        sel = task_ops == o
+        span = (end[sel].max() - start[sel].min()) / 1e3
+        M, N, K, BN = op_dims[o]
+        print(f"{o:7d} {M:6d} {N:6d} {K:6d} {BN:4d} {op_ntasks[o]:6d} {span:8.1f} "
+              f"{2.0 * M * N * K / span / 1e6:7.1f} {(start[sel].min() - t0) / 1e6:8.3f}")
     if args.json:
         json.dump({"config": args.config, "kernel_ms": kms, "grid": grid, "rows": rows}, open(args.json, "w"))
 

@@ -292,12 +292,14 @@ int gpt_train_step_static(const gpt_config* cfg, float* params, float* m, float*
  * MN-major), likewise B with ldb/b_mn; C[m*ldc + n], or with ksplit > 1 split s
  * writes its partial sum to C + s*M*ldc.  Runs on cuda_stream and synchronises.
  * bf16 requires K % (64 ksplit) == 0, N % 64 == 0, lda and ldb multiples of 8.
+ * kernel_ms: HOST float*, receives the kernel's device time (CUDA events
+ * around the launch); may be NULL.
  * Errors: INVALID_ARG, UNSUPPORTED, OOM, CUDA, TIMEOUT; text via
  * gpt_last_error(NULL).
  */
 int gpt_test_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, int32_t a_mn,
                   const void* B, int64_t ldb, int32_t b_mn, float* C, int64_t ldc, int32_t ksplit,
-                  void* cuda_stream);
+                  void* cuda_stream, float* kernel_ms);
 
 /*
  * Test hook: causal multi-head attention forward and backward as a graph of

@@ -86,7 +86,8 @@ SIGNATURES = [
     ("gpt_test_attention", c_int, [c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p, c_void_p,
                                    c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     ("gpt_test_gemm", c_int, [c_int32, c_int32, c_int32, c_int32, c_void_p, c_int64, c_int32,
-                              c_void_p, c_int64, c_int32, c_void_p, c_int64, c_int32, c_void_p]),
+                              c_void_p, c_int64, c_int32, c_void_p, c_int64, c_int32, c_void_p,
+                              POINTER(c_float)]),
 ]
 
 
@@ -292,19 +293,22 @@ def task_budget(iterations: int, tasks_per_iteration: int) -> int:
     return int(load().gpt_task_budget(c_int64(iterations), c_int64(tasks_per_iteration)))
 
 
-def test_gemm(A, B, a_mn: bool, b_mn: bool, M: int, N: int, K: int, ksplit: int = 1, stream=None):
-    """Runs gpt_test_gemm on torch CUDA tensors; returns C (fp32 [ksplit, M, N])."""
+def test_gemm(A, B, a_mn: bool, b_mn: bool, M: int, N: int, K: int, ksplit: int = 1, stream=None,
+              timing: bool = False):
+    """Runs gpt_test_gemm on torch CUDA tensors; returns C (fp32 [ksplit, M, N]),
+    and with timing=True (C, kernel milliseconds)."""
     import torch
     lib = load()
     dtype = DTYPE_BF16 if A.dtype == torch.bfloat16 else DTYPE_FP32
     C = torch.full((ksplit, M, N), float("nan"), dtype=torch.float32, device=A.device)
     s = stream if stream is not None else torch.cuda.current_stream()
+    ms = c_float()
     rc = lib.gpt_test_gemm(dtype, M, N, K, c_void_p(A.data_ptr()), A.stride(0), int(a_mn),
                            c_void_p(B.data_ptr()), B.stride(0), int(b_mn), c_void_p(C.data_ptr()), N,
-                           ksplit, c_void_p(s.cuda_stream))
+                           ksplit, c_void_p(s.cuda_stream), byref(ms))
     if rc != GPT_OK:
         raise GptError(rc, lib.gpt_last_error(None).decode())
-    return C
+    return (C, float(ms.value)) if timing else C
 
 
 def init_params_host(cfg, seed: int, n: int) -> np.ndarray:

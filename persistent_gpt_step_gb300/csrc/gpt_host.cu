@@ -1123,7 +1123,7 @@ static int run_test_graph(gpt& h, int32_t dtype) {
 
 int gpt_test_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, int32_t a_mn,
                   const void* B, int64_t ldb, int32_t b_mn, float* C, int64_t ldc, int32_t ksplit,
-                  void* cuda_stream) {
+                  void* cuda_stream, float* kernel_ms) {
   g_create_error.clear();
   if (!A || !B || !C || M < 1 || N < 1 || K < 1 || ksplit < 1 || (dtype != GPT_DTYPE_FP32 && dtype != GPT_DTYPE_BF16))
     return fail(nullptr, GPT_ERR_INVALID_ARG, "bad GEMM test arguments");
@@ -1142,7 +1142,18 @@ int gpt_test_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* A,
   o.gemm.out = C; o.gemm.ldo = ldc; o.gemm.split_stride = (int64_t)M * ldc;
   Builder bld{&h};
   bld.add(o, {});
-  return run_test_graph(h, dtype);
+  if (kernel_ms) {
+    cudaEventCreate(&h.ev0);
+    cudaEventCreate(&h.ev1);
+  }
+  rc = run_test_graph(h, dtype);
+  if (kernel_ms) {
+    *kernel_ms = h.last_kernel_ms;
+    cudaEventDestroy(h.ev0);
+    cudaEventDestroy(h.ev1);
+    h.ev0 = h.ev1 = nullptr;
+  }
+  return rc;
 }
 
 int gpt_test_attention(int32_t dtype, int32_t B, int32_t T, int32_t H, int32_t d, const void* qkv, void* o,

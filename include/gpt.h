@@ -229,11 +229,14 @@ int gpt_init_params_host(const gpt_config* cfg, uint64_t seed, float* dst, size_
 
 /* One task of the step's graph as gpt_graph_describe reports it. */
 typedef struct gpt_task_info {
-  int32_t op;            /* operation (completion counter) the task belongs to   */
+  int32_t op;            /* operation the task belongs to                         */
   int32_t idx;           /* index of the task within its operation               */
-  int32_t nwait;         /* number of dependencies (<= 3)                         */
-  int32_t wait_op[3];    /* operations whose counters it waits on (-1 unused)    */
-  int32_t wait_need[3];  /* per-step count each counter must reach (its tasks)   */
+  int32_t sig;           /* completion counter the task increments when done     */
+  int32_t sig2;          /* op-level counter it also increments (-1: none)      */
+  int32_t nwait;         /* number of dependency ranges (<= 3)                    */
+  int32_t wait_first[3]; /* first counter of each range (-1 unused)               */
+  int32_t wait_count[3]; /* counters in each range                                */
+  int32_t wait_need[3];  /* per-step count each counter of the range must reach  */
 } gpt_task_info;
 
 /*
@@ -241,12 +244,17 @@ typedef struct gpt_task_info {
  * SMs; <= 0 means 148) without device memory, and reports it: *n_tasks tasks in
  * ticket order (the first max_tasks copied to HOST tasks[], may be NULL) and
  * *n_ops operations (type and task count of the first max_ops into HOST
- * op_types[] / op_tasks[], and for GEMM operations M, N, K and the tile
- * width into op_dims[4*i .. 4*i+3] (zeros otherwise); each may be NULL).  Operation types are the kernel's
+ * op_types[] / op_tasks[], and into op_dims[6*i .. 6*i+5]: for GEMM
+ * operations M, N, K and the tile width (zeros otherwise), then the op's first
+ * completion counter and its number of counters (one per 128-row block of the
+ * token dimension for ops with token-major output on the bf16 path plus one
+ * op-level counter that every task of the op also increments, else 1);
+ * each may be NULL).  Tasks are reported in ticket order.  Operation types are the kernel's
  * OpType values (0 embed, 1 LN forward, 2 GEMM, 3 attention forward, 4 cross-
  * entropy, 5 loss, 6 LN backward, 7 column sum, 8 attention backward,
  * 9 token-embedding backward, 10 position-embedding backward, 11 AdamW,
- * 12 attention-backward pre-pass, 13 attention dK/dV, 14 attention dQ).
+ * 12 attention-backward pre-pass, 13 attention dK/dV, 14 attention dQ,
+ * 15 token sort).
  */
 int gpt_graph_describe(const gpt_config* cfg, int32_t num_sms, int64_t* n_tasks, int32_t* n_ops,
                        gpt_task_info* tasks, int64_t max_tasks, int32_t* op_types, int32_t* op_tasks,

@@ -47,8 +47,8 @@ class gpt_config(ctypes.Structure):
 
 
 class gpt_task_info(ctypes.Structure):
-    _fields_ = [("op", c_int32), ("idx", c_int32), ("nwait", c_int32),
-                ("wait_op", c_int32 * 3), ("wait_need", c_int32 * 3)]
+    _fields_ = [("op", c_int32), ("idx", c_int32), ("sig", c_int32), ("sig2", c_int32), ("nwait", c_int32),
+                ("wait_first", c_int32 * 3), ("wait_count", c_int32 * 3), ("wait_need", c_int32 * 3)]
 
 
 _lib = None
@@ -323,10 +323,11 @@ def init_params_host(cfg, seed: int, n: int) -> np.ndarray:
 
 
 def describe_graph(cfg, num_sms: int = 148, dims: bool = False):
-    """(tasks, op_types, op_tasks[, op_dims]) of the step's task graph, built on the host.
+    """The step's task graph, built on the host.
 
-    tasks: list of (op, idx, [(wait_op, need), ...]) in ticket order; op_dims:
-    per op (M, N, K, tile width) for GEMMs, zeros otherwise."""
+    Returns (tasks, op_types, op_tasks[, op_dims]): tasks in ticket order as
+    (op, idx, sig, [(first_counter, n_counters, need), ...], sig2); op_dims per op:
+    (M, N, K, tile width) for GEMMs (zeros otherwise), first counter, counters."""
     lib = load()
     c = make_config(cfg)
     nt, no = c_int64(), c_int32()
@@ -336,14 +337,15 @@ def describe_graph(cfg, num_sms: int = 148, dims: bool = False):
     tasks = (gpt_task_info * nt.value)()
     types = (c_int32 * no.value)()
     ntk = (c_int32 * no.value)()
-    odims = (c_int32 * (4 * no.value))()
+    odims = (c_int32 * (6 * no.value))()
     rc = lib.gpt_graph_describe(byref(c), num_sms, byref(nt), byref(no), tasks, nt.value, types, ntk,
                                 odims, no.value)
     if rc != GPT_OK:
         raise GptError(rc, lib.gpt_last_error(None).decode())
-    out = [(t.op, t.idx, [(t.wait_op[w], t.wait_need[w]) for w in range(t.nwait)]) for t in tasks]
+    out = [(t.op, t.idx, t.sig, [(t.wait_first[w], t.wait_count[w], t.wait_need[w]) for w in range(t.nwait)],
+            t.sig2) for t in tasks]
     if dims:
-        return out, list(types), list(ntk), [tuple(odims[4 * i:4 * i + 4]) for i in range(no.value)]
+        return out, list(types), list(ntk), [tuple(odims[6 * i:6 * i + 6]) for i in range(no.value)]
     return out, list(types), list(ntk)
 
 

@@ -72,6 +72,27 @@ __device__ __forceinline__ bool wait_counter(const KParams& kp, int32_t ctr,
   return false;
 }
 
+// Waits (one thread) for every dependency range of task t.
+__device__ __forceinline__ bool task_ready(const KParams& kp, int64_t t) {
+  const TaskDesc& d = kp.tasks[t];
+  for (int w = 0; w < d.nwait; ++w) {
+    const WaitSpec ws = d.wait[w];
+    const unsigned long long target = kp.epoch * (unsigned long long)ws.need;
+    for (int c = 0; c < ws.count; ++c)
+      if (!wait_counter(kp, ws.first + c, target, (uint32_t)t)) return false;
+  }
+  return true;
+}
+
+// Claims the next ticket (one thread): the index of a task in kp.tasks, or
+// kp.ntasks when the graph is exhausted or a fatal error was recorded.  Tickets
+// are a 64-bit counter per launch parity; the previous launch zeroed this one.
+__device__ __forceinline__ int64_t claim_task(const KParams& kp) {
+  if (ld_volatile_u32(&kp.err[0]) != 0u) return kp.ntasks;
+  const int64_t t = (int64_t)atomicAdd(kp.tickets + (kp.epoch & 1ull), 1ull);
+  return t < kp.ntasks ? t : kp.ntasks;
+}
+
 // ---- element conversions (act_t = float or __nv_bfloat16) -------------------
 template <typename T> __device__ __forceinline__ float to_f(T v);
 template <> __device__ __forceinline__ float to_f<float>(float v) { return v; }

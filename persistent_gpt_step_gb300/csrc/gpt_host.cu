@@ -9,8 +9,10 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <queue>
 #include <string>
 #include <thread>
 #include <vector>
@@ -134,6 +136,8 @@ struct gpt {
   int64_t skip_release = -1;
   bool poisoned = false;
   bool describe_only = false;  // build the graph without device memory or tensor maps
+  int n_counters = 0;          // completion counters of the graph
+  std::vector<int> op_ctr0, op_nblk;  // first counter and counter count of each op
 
   cudaEvent_t ev0 = nullptr, ev1 = nullptr;  // bracket the kernel of the last step
   float last_kernel_ms = 0.f;
@@ -246,6 +250,7 @@ struct Layout {
   std::vector<size_t> dx, dx_act, dxm, dxm_act, dh, da2, dO, dqkv, da1, att_scr;
   std::vector<size_t> ln1_gp, ln1_bp, ln2_gp, ln2_bp;
   size_t lnf_gp, lnf_bp;
+  size_t sorted_tok, sorted_pos, block_start;
   size_t total;
 };
 
@@ -254,7 +259,7 @@ constexpr int kRowsCe = 8;        // rows per cross-entropy task
 constexpr int kRowsEmb = 32;      // rows per embedding task
 constexpr int kVocabRows = 64;    // vocabulary rows per embedding-backward task
 constexpr int kColsColsum = 64;   // columns per column-sum task
-constexpr int64_t kAdamChunk = 65536;
+constexpr int64_t kAdamChunk = 32768;
 
 int ln_tasks(int N) { return (N + kRowsLn - 1) / kRowsLn; }
 
@@ -313,6 +318,9 @@ Layout make_layout(const gpt_config& c, size_t nparams, int lm_ksplit) {
   }
   Lo.lnf_gp = b.take(nrb * C * 4);
   Lo.lnf_bp = b.take(nrb * C * 4);
+  Lo.sorted_tok = b.take(N * 4);
+  Lo.sorted_pos = b.take(N * 4);
+  Lo.block_start = b.take((V / 64 + 2) * 4);
   Lo.total = (b.off + 255) & ~(size_t)255;
   return Lo;
 }
@@ -362,8 +370,92 @@ int make_tmap(gpt* h, const void* base, int64_t inner, int64_t outer, int64_t ld
 // ----------------------------------------------------------------------------
 // Graph builder
 // ----------------------------------------------------------------------------
+// Host copy of the kernel's GEMM tile order (split-major, then M- or N-fastest).
+void gemm_coords_host(const GemmArgs& g, int idx, int& tm, int& tn, int& split) {
+  const int tiles_m = (g.M + g.BM - 1) / g.BM;
+  const int per_split = tiles_m * g.tiles_n;
+  split = idx / per_split;
+  const int r = idx - split * per_split;
+  if (g.m_fastest) { tm = r % tiles_m; tn = r / tiles_m; }
+  else { tn = r % g.tiles_n; tm = r / g.tiles_n; }
+}
+
+// Builds the task list op by op.  On the tensor-core path every op whose output
+// is token-major gets one completion counter per kRowBlock rows, and a task of
+// such an op waits only for the row blocks it reads (the same rows, or for
+// attention the prefix / suffix of its sequence); weight-gradient GEMMs, column
+// sums, the loss, embedding gradients and AdamW read every row and wait for
+// whole ops.  finish() then re-orders the tickets by list scheduling.
+constexpr int kRowBlock = 128;
+
 struct Builder {
   gpt* h;
+  struct OpInfo {
+    int ctr0, nblk, per_block;
+    int op_ctr, ntasks;  // op-level counter (blocks > 1), counts every task
+  };
+  std::vector<OpInfo> info;
+  std::vector<double> cost;  // estimated microseconds per task (ticket order of construction)
+  int nctr = 0;
+
+  // block of task i of op o, the row-block range [lo, hi] it reads (lo < 0: all
+  // rows), and its estimated time
+  void shape(const OpDesc& o, int i, int& blk, int& lo, int& hi, double& us) const {
+    const Dims& D = h->D;
+    const bool rowed = is_bf16(h->cfg);
+    const double bw = 40e3;     // bytes per microsecond one SM streams
+    blk = 0; lo = -1; hi = -1;
+    us = 1.0;
+    auto rows_task = [&](int rows_per_task, double bytes_per_row) {
+      if (rowed) { blk = i * rows_per_task / kRowBlock; lo = hi = blk; }
+      us = 1.0 + rows_per_task * bytes_per_row / bw;
+    };
+    const int nqb = D.T / 128;
+    switch (o.type) {
+      case OP_EMBED: rows_task(o.emb.rows_per_task, 12.0 * D.C); break;
+      case OP_LN_FWD: rows_task(o.lnf.rows_per_task, 6.0 * D.C); break;
+      case OP_LN_BWD: rows_task(o.lnb.rows_per_task, 18.0 * D.C); break;
+      case OP_CE: rows_task(o.ce.rows_per_task, 6.0 * D.V); break;
+      case OP_ATTN_BWD_PRE: rows_task(64, 4.0 * D.C); break;
+      case OP_GEMM: {
+        const GemmArgs& g = o.gemm;
+        int tm, tn, sp;
+        gemm_coords_host(g, i, tm, tn, sp);
+        const double k = (double)g.K / g.ksplit;
+        us = 1.5 + 2.0 * g.BM * g.BN * k / 7e6;
+        if (rowed && !g.a_mn && g.M == D.N) { blk = tm; lo = hi = tm; }  // token-major output rows
+      } break;
+      case OP_ATTN_FWD:
+      case OP_ATTN_BWD_Q:
+        if (rowed) {
+          const int qb = nqb - 1 - i % nqb, b = i / (nqb * D.H);
+          blk = (b * D.T + qb * 128) / kRowBlock;
+          lo = o.type == OP_ATTN_FWD ? b * D.T / kRowBlock : blk;
+          hi = blk;
+          us = 1.0 + (o.type == OP_ATTN_FWD ? 4.0 : 6.0) * 128.0 * (qb * 128 + 128) * D.d / 3e6;
+        } else {
+          us = 1.0 + 4.0 * D.T * D.T * D.d / 1e5;
+        }
+        break;
+      case OP_ATTN_BWD_KV:
+        if (rowed) {
+          const int kb = i % nqb, b = i / (nqb * D.H);
+          blk = (b * D.T + kb * 128) / kRowBlock;
+          lo = blk;
+          hi = (b * D.T + D.T) / kRowBlock - 1;
+          us = 1.0 + 8.0 * 128.0 * (D.T - kb * 128) * D.d / 3e6;
+        }
+        break;
+      case OP_ATTN_BWD: us = 1.0 + 12.0 * D.T * D.T * D.d / 1e5; break;
+      case OP_COLSUM: us = 1.0 + (double)o.colsum.rows * o.colsum.cols_per_task * 4.0 / bw; break;
+      case OP_ADAMW: us = 1.0 + std::min<double>(o.adam.chunk, (double)o.adam.n) * 30.0 / bw; break;
+      case OP_EMBED_BWD_WTE: us = 2.0 + o.emb.rows_per_task * 4.0 * D.C / bw; break;
+      case OP_TOKEN_SORT: us = 5.0 + D.N / 8.0; break;
+      case OP_EMBED_BWD_WPE: us = 1.0 + o.emb.rows_per_task * 4.0 * D.C * D.B / bw; break;
+      default: break;
+    }
+  }
+
   int add(const OpDesc& op, std::initializer_list<int> deps) {
     const int id = (int)h->ops.size();
     h->ops.push_back(op);
@@ -374,18 +466,130 @@ struct Builder {
       for (int i = 0; i < nd; ++i) dup |= dl[i] == d;
       if (!dup) dl[nd++] = d;
     }
+    // block structure of this op
+    int nblk = 1;
+    if (is_bf16(h->cfg)) {
+      int b, lo, hi;
+      double us;
+      for (int i = 0; i < op.ntasks; ++i) {
+        shape(op, i, b, lo, hi, us);
+        nblk = std::max(nblk, b + 1);
+      }
+    }
+    OpInfo oi{nctr, nblk, 0, nblk > 1 ? nctr + nblk : nctr, op.ntasks};
+    std::vector<int> per(nblk, 0);
     for (int i = 0; i < op.ntasks; ++i) {
       TaskDesc t{};
+      int b, lo, hi;
+      double us;
+      shape(op, i, b, lo, hi, us);
       t.op = id;
       t.idx = i;
+      t.sig = nctr + b;
+      t.sig2 = nblk > 1 ? nctr + nblk : -1;
+      per[b]++;
       t.nwait = nd;
       for (int w = 0; w < nd; ++w) {
-        t.wait_ctr[w] = dl[w];
-        t.wait_need[w] = (uint32_t)h->ops[dl[w]].ntasks;
+        const OpInfo& pi = info[dl[w]];
+        if (pi.nblk == 1 || lo < 0) {
+          t.wait[w] = WaitSpec{pi.op_ctr, 1, (uint32_t)pi.ntasks};  // whole op: one counter
+        } else {
+          t.wait[w] = WaitSpec{pi.ctr0 + lo, hi - lo + 1, (uint32_t)pi.per_block};
+        }
       }
       h->tasks.push_back(t);
+      cost.push_back(us);
     }
+    for (int b = 0; b < nblk; ++b)
+      if (per[b] != per[0]) {
+        fprintf(stderr, "libgpt: op %d has uneven row blocks\n", id);
+        std::abort();
+      }
+    oi.per_block = per[0];
+    info.push_back(oi);
+    nctr += nblk > 1 ? nblk + 1 : 1;
     return id;
+  }
+
+  // Ticket order by list scheduling: simulate the graph on `workers` blocks with
+  // the cost model, always starting the ready task with the longest remaining
+  // path (bottom level) first; the start order becomes the ticket order.  A task
+  // starts only after every task it waits for has finished, so dependencies
+  // still point to earlier tickets.
+  void finish(int workers) {
+    const int T = (int)h->tasks.size();
+    std::vector<int> remaining(nctr, 0);
+    std::vector<std::vector<int>> waiters(nctr);
+    std::vector<int> unmet(T, 0);
+    for (int t = 0; t < T; ++t) {
+      const TaskDesc& d = h->tasks[t];
+      remaining[d.sig]++;
+      if (d.sig2 >= 0) remaining[d.sig2]++;
+      for (int w = 0; w < d.nwait; ++w)
+        for (int c = 0; c < d.wait[w].count; ++c) {
+          waiters[d.wait[w].first + c].push_back(t);
+          unmet[t]++;
+        }
+    }
+    // bottom levels, in reverse construction order (a topological order)
+    std::vector<double> bl(T, 0.0), blc(nctr, 0.0);
+    for (int t = T - 1; t >= 0; --t) {
+      const TaskDesc& d = h->tasks[t];
+      bl[t] = cost[t] + std::max(blc[d.sig], d.sig2 >= 0 ? blc[d.sig2] : 0.0);
+      for (int w = 0; w < d.nwait; ++w)
+        for (int c = 0; c < d.wait[w].count; ++c) {
+          double& x = blc[d.wait[w].first + c];
+          x = std::max(x, bl[t]);
+        }
+    }
+    // priority = bottom level (critical path first).  Measured on the 162M step,
+    // raising the priority of tasks that have waited long (to pull AdamW and
+    // column sums forward into the backward) only made the step slower.
+    auto cmp = [&](int a, int b) { return bl[a] < bl[b] || (bl[a] == bl[b] && a > b); };
+    std::priority_queue<int, std::vector<int>, decltype(cmp)> ready(cmp);
+    double now = 0.0;
+    auto make_ready = [&](int t) { ready.push(t); };
+    for (int t = 0; t < T; ++t)
+      if (unmet[t] == 0) make_ready(t);
+    typedef std::pair<double, int> Ev;
+    std::priority_queue<Ev, std::vector<Ev>, std::greater<Ev>> running;
+    std::vector<int> order;
+    order.reserve(T);
+    int idle = std::max(1, workers);
+    while ((int)order.size() < T) {
+      while (idle > 0 && !ready.empty()) {
+        const int t = ready.top();
+        ready.pop();
+        order.push_back(t);
+        running.push(Ev(now + cost[t], t));
+        --idle;
+      }
+      if (running.empty()) break;  // cannot happen for a valid graph
+      const Ev e = running.top();
+      running.pop();
+      now = e.first;
+      ++idle;
+      for (const int c : {h->tasks[e.second].sig, h->tasks[e.second].sig2}) {
+        if (c < 0) continue;
+        if (--remaining[c] == 0)
+          for (int w : waiters[c])
+            if (--unmet[w] == 0) make_ready(w);
+      }
+    }
+    if ((int)order.size() != T) {
+      fprintf(stderr, "libgpt: task graph has a cycle\n");
+      std::abort();
+    }
+    std::vector<TaskDesc> sorted(T);
+    for (int i = 0; i < T; ++i) sorted[i] = h->tasks[order[i]];
+    h->tasks.swap(sorted);
+    h->n_counters = nctr;
+    h->op_ctr0.clear();
+    h->op_nblk.clear();
+    for (const OpInfo& oi : info) {
+      h->op_ctr0.push_back(oi.ctr0);
+      h->op_nblk.push_back(oi.nblk > 1 ? oi.nblk + 1 : 1);  // block counters + the op counter
+    }
   }
 };
 
@@ -471,7 +675,7 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
   // ---------------- forward ----------------
   OpDesc o = blank(OP_EMBED, (N + kRowsEmb - 1) / kRowsEmb);
   o.emb = EmbedArgs{P(h->t_wte), P(h->t_wpe), F32(Lo.x[0]), nullptr, nullptr, nullptr,
-                    N, D.B, D.T, C, V, kRowsEmb};
+                    N, D.B, D.T, C, V, kRowsEmb, nullptr, nullptr, nullptr};
   int prev = bld.add(o, {});
   std::vector<int> op_ln1(L), op_qkv(L), op_attn(L), op_atto(L), op_ln2(L), op_up(L), op_down(L);
   const int qblock = D.T <= 512 ? 64 : 32;
@@ -536,10 +740,12 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
     a.adam = AdamArgs{h->params + ti.offset, h->grads + ti.offset, h->m + ti.offset, h->v + ti.offset,
                       bf ? h->shadow + ti.offset : nullptr, n, kAdamChunk,
                       (ti.ndim == 2 || c.wd_on_1d) ? 1.0f : 0.0f};
+    // the gradient producers depend (through the backward) on every cross-entropy
+    // row, whose task flags a non-finite loss, so AdamW sees that flag and the
+    // bad-token flag without waiting for the loss reduction
     std::vector<int> dl(deps);
-    dl.push_back(op_loss);
-    if (dl.size() == 2) bld.add(a, {dl[0], dl[1]});
-    else bld.add(a, {dl[0], dl[1], dl[2]});
+    if (dl.size() == 1) bld.add(a, {dl[0]});
+    else bld.add(a, {dl[0], dl[1]});
   };
   auto colsum = [&](const void* src, bool f32, int64_t ld, int rows, int cols, float* dst, int dep,
                     int dep2 = -1) {
@@ -653,17 +859,25 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
     adam(id.ln1_g, {colsum(F32(Lo.ln1_gp[l]), true, C, nrb, C, G(id.ln1_g), op_dres)});
     if (id.ln1_b >= 0) adam(id.ln1_b, {colsum(F32(Lo.ln1_bp[l]), true, C, nrb, C, G(id.ln1_b), op_dres)});
   }
-  // embeddings
+  // embeddings: sort (token, position) pairs, then one task per block of vocabulary rows
+  int32_t* stok = reinterpret_cast<int32_t*>(A + Lo.sorted_tok);
+  int32_t* spos = reinterpret_cast<int32_t*>(A + Lo.sorted_pos);
+  int32_t* bstart = reinterpret_cast<int32_t*>(A + Lo.block_start);
+  o = blank(OP_TOKEN_SORT, 1);
+  o.emb = EmbedArgs{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, N, D.B, D.T, C, V, kVocabRows,
+                    stok, spos, bstart};
+  const int op_sort = bld.add(o, {});
   o = blank(OP_EMBED_BWD_WTE, (V + kVocabRows - 1) / kVocabRows);
   o.emb = EmbedArgs{nullptr, nullptr, nullptr, F32(Lo.dx[0]), G(h->t_wte), G(h->t_wpe), N, D.B, D.T, C, V,
-                    kVocabRows};
-  const int op_wte = bld.add(o, {op_dres});
+                    kVocabRows, stok, spos, bstart};
+  const int op_wte = bld.add(o, {op_dres, op_sort});
   adam(h->t_wte, {op_wte});
   o = blank(OP_EMBED_BWD_WPE, (D.T + kRowsEmb - 1) / kRowsEmb);
   o.emb = EmbedArgs{nullptr, nullptr, nullptr, F32(Lo.dx[0]), G(h->t_wte), G(h->t_wpe), N, D.B, D.T, C, V,
-                    kRowsEmb};
+                    kRowsEmb, nullptr, nullptr, nullptr};
   const int op_wpe = bld.add(o, {op_dres});
   adam(h->t_wpe, {op_wpe});
+  bld.finish(h->num_sms > 0 ? h->num_sms : 148);
   (void)op_lm; (void)op_qkv; (void)op_attn; (void)op_atto; (void)op_ln2; (void)op_up; (void)op_down;
   return GPT_OK;
 }
@@ -674,10 +888,11 @@ size_t smem_needed(const gpt* h) {
   size_t s = 0;
   s = std::max(s, (size_t)(2 * 16 * (kSimtTile + 4) * 4));                     // SIMT GEMM
   s = std::max(s, (size_t)(2 * kWarps * D.C * 4));                             // LN backward partials
-  s = std::max(s, (size_t)D.N * 4);                                            // token ids
+  s = std::max(s, (size_t)D.N * 16 + 256 * 4);                                 // token sort
   s = std::max(s, (size_t)(qblock * D.d + 64 * (D.d + 1) + qblock * D.T) * 4); // attention forward
   s = std::max(s, (size_t)(2 * qblock * D.d + 64 * (D.d + 1) + qblock * D.T + qblock) * 4);  // backward
   s = std::max(s, (size_t)kThreads * 4);
+  s = std::max(s, (size_t)kAdamStages * kAdamStageBytes);          // AdamW staging
   if (is_bf16(h->cfg)) s = std::max(s, (size_t)kTcSmemBytes + 4 * kEpiStageBytes);
   return s + 1024;  // 1024-byte alignment slack
 }
@@ -696,9 +911,9 @@ int fill_shadow_and_upload(gpt* h, const float* host_params) {
 }
 
 int reset_counters(gpt* h) {
-  const size_t nctr = h->ops.size();
+  const size_t nctr = (size_t)h->n_counters;
   CUDA_TRY(h, cudaMemsetAsync(h->d_counters, 0, nctr * sizeof(unsigned long long), h->stream));
-  CUDA_TRY(h, cudaMemsetAsync(h->d_ticket, 0, sizeof(unsigned long long), h->stream));
+  CUDA_TRY(h, cudaMemsetAsync(h->d_ticket, 0, 2 * sizeof(unsigned long long), h->stream));
   CUDA_TRY(h, cudaMemsetAsync(h->d_err, 0, 4 * sizeof(uint32_t), h->stream));
   CUDA_TRY(h, cudaStreamSynchronize(h->stream));
   h->launches = 0;
@@ -714,8 +929,7 @@ int launch_step(gpt* h, const int32_t* tokens, const int32_t* targets, float* lo
   kp.ntasks = (int64_t)h->tasks.size();
   kp.ops = h->d_ops;
   kp.counters = h->d_counters;
-  kp.ticket = h->d_ticket;
-  kp.ticket_base = (unsigned long long)h->launches * (unsigned long long)(h->tasks.size() + h->grid);
+  kp.tickets = h->d_ticket;
   kp.epoch = h->launches + 1;
   kp.err = h->d_err;
   kp.timeout_ns = (uint64_t)(h->cfg.wait_timeout_ms ? h->cfg.wait_timeout_ms : 2000) * 1000000ull;
@@ -862,8 +1076,8 @@ int gpt_create(const gpt_config* cfg, uint64_t seed, void* cuda_stream, void* ar
   const size_t o_tasks = mb.take(h->tasks.size() * sizeof(TaskDesc));
   const size_t o_ops = mb.take(h->ops.size() * sizeof(OpDesc));
   const size_t o_maps = mb.take(std::max<size_t>(1, h->tmaps.size()) * 128);
-  const size_t o_ctr = mb.take(h->ops.size() * sizeof(unsigned long long));
-  const size_t o_tic = mb.take(sizeof(unsigned long long));
+  const size_t o_ctr = mb.take((size_t)h->n_counters * sizeof(unsigned long long));
+  const size_t o_tic = mb.take(2 * sizeof(unsigned long long));
   const size_t o_err = mb.take(4 * sizeof(uint32_t));
   const size_t o_tok = mb.take(2 * (size_t)h->D.N * sizeof(int32_t));
   h->meta_bytes = mb.off;
@@ -1070,8 +1284,8 @@ static int run_test_graph(gpt& h, int32_t dtype) {
   const size_t o_tasks = mb.take(h.tasks.size() * sizeof(TaskDesc));
   const size_t o_ops = mb.take(h.ops.size() * sizeof(OpDesc));
   const size_t o_maps = mb.take(std::max<size_t>(1, h.tmaps.size()) * 128);
-  const size_t o_ctr = mb.take(h.ops.size() * sizeof(unsigned long long));
-  const size_t o_tic = mb.take(sizeof(unsigned long long));
+  const size_t o_ctr = mb.take((size_t)h.n_counters * sizeof(unsigned long long));
+  const size_t o_tic = mb.take(2 * sizeof(unsigned long long));
   const size_t o_err = mb.take(4 * sizeof(uint32_t));
   const size_t o_loss = mb.take(sizeof(float));
   h.meta_bytes = mb.off;
@@ -1142,6 +1356,7 @@ int gpt_test_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* A,
   o.gemm.out = C; o.gemm.ldo = ldc; o.gemm.split_stride = (int64_t)M * ldc;
   Builder bld{&h};
   bld.add(o, {});
+  bld.finish(h.num_sms);
   if (kernel_ms) {
     cudaEventCreate(&h.ev0);
     cudaEventCreate(&h.ev1);
@@ -1195,6 +1410,7 @@ int gpt_test_attention(int32_t dtype, int32_t B, int32_t T, int32_t H, int32_t d
     op.attn = att;
     bld.add(op, {f});
   }
+  bld.finish(h.num_sms);
   return run_test_graph(h, dtype);
 }
 
@@ -1243,10 +1459,13 @@ int gpt_graph_describe(const gpt_config* cfg, int32_t num_sms, int64_t* n_tasks,
       const TaskDesc& t = h.tasks[i];
       tasks[i].op = t.op;
       tasks[i].idx = t.idx;
+      tasks[i].sig = t.sig;
+      tasks[i].sig2 = t.sig2;
       tasks[i].nwait = t.nwait;
       for (int w = 0; w < 3; ++w) {
-        tasks[i].wait_op[w] = w < t.nwait ? t.wait_ctr[w] : -1;
-        tasks[i].wait_need[w] = w < t.nwait ? (int32_t)t.wait_need[w] : 0;
+        tasks[i].wait_first[w] = w < t.nwait ? t.wait[w].first : -1;
+        tasks[i].wait_count[w] = w < t.nwait ? t.wait[w].count : 0;
+        tasks[i].wait_need[w] = w < t.nwait ? (int32_t)t.wait[w].need : 0;
       }
     }
   for (int32_t i = 0; i < std::min<int32_t>(max_ops, (int32_t)h.ops.size()); ++i) {
@@ -1255,8 +1474,8 @@ int gpt_graph_describe(const gpt_config* cfg, int32_t num_sms, int64_t* n_tasks,
     if (op_dims) {
       const bool g = h.ops[i].type == OP_GEMM;
       const GemmArgs& a = h.ops[i].gemm;
-      const int32_t v[4] = {g ? a.M : 0, g ? a.N : 0, g ? a.K : 0, g ? a.BN : 0};
-      for (int k = 0; k < 4; ++k) op_dims[4 * i + k] = v[k];
+      const int32_t v[6] = {g ? a.M : 0, g ? a.N : 0, g ? a.K : 0, g ? a.BN : 0, h.op_ctr0[i], h.op_nblk[i]};
+      for (int k = 0; k < 6; ++k) op_dims[6 * i + k] = v[k];
     }
   }
   return GPT_OK;
@@ -1353,8 +1572,8 @@ extern "C" int gpt_train_step_static(const gpt_config* cfg, float* params, float
   mb.off = Lo.total;
   const size_t o_tasks = mb.take(h.tasks.size() * sizeof(TaskDesc));
   const size_t o_ops = mb.take(h.ops.size() * sizeof(OpDesc));
-  const size_t o_ctr = mb.take(h.ops.size() * sizeof(unsigned long long));
-  const size_t o_tic = mb.take(sizeof(unsigned long long));
+  const size_t o_ctr = mb.take((size_t)h.n_counters * sizeof(unsigned long long));
+  const size_t o_tic = mb.take(2 * sizeof(unsigned long long));
   const size_t o_err = mb.take(4 * sizeof(uint32_t));
   if (mb.off > kStaticScratchBytes)
     return fail(nullptr, GPT_ERR_INVALID_ARG,

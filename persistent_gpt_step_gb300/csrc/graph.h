@@ -3,11 +3,13 @@
 //
 // The step is a list of tasks in a topological (ticket) order.  A task names an
 // operation (an "op": one GEMM, one LayerNorm, the attention of one layer ...)
-// and its tile / block index within that op.  Every op owns a 64-bit completion
-// counter; a task may wait for up to kMaxWaits counters to reach
-// epoch * need (need = the producing op's task count), then runs, then adds 1
-// to its own op's counter with release semantics.  Dependencies only point to
-// earlier tickets, so with every block resident the graph cannot deadlock
+// and its tile / block index within that op.  Every op owns 64-bit completion
+// counters: one per 128-row block of the token dimension for ops whose output
+// is token-major, else one.  A task may wait for up to kMaxWaits ranges of
+// counters to reach epoch * need (need = the producer's tasks per counter),
+// then runs, then adds 1 to its own counter with release semantics.
+// Dependencies only point to earlier tickets, so with every block resident the
+// graph cannot deadlock
 // ("How one persistent kernel runs three jobs": ticket counters, release
 // fences before the counter increments, acquire waits by dependents).
 #pragma once
@@ -27,6 +29,9 @@ constexpr int kTcStageBytes = kTcStageA + kTcStageB;  // 48 KB
 constexpr int kTcSmemBytes = kTcStages * kTcStageBytes;
 constexpr int kEpiStageBytes = 32 * 64 * 4;            // per epilogue warp: 32 rows x 64 fp32
 constexpr int kTmemCols = 512;            // two fp32 accumulators of up to 128 x 256
+constexpr int kAdamSub = 2048;            // AdamW: parameters per bulk-copied sub-chunk
+constexpr int kAdamStages = 4;            // AdamW: sub-chunks in flight
+constexpr int kAdamStageBytes = kAdamSub * (4 * 4 + 2);  // p, g, m, v fp32 + bf16 copy
 constexpr int kThreads = 256;     // threads of every persistent block
 constexpr int kWarps = kThreads / 32;
 
@@ -46,6 +51,7 @@ enum OpType : int32_t {
   OP_ATTN_BWD_PRE,   // D = rowsum(dO * O) per head (tensor-core path) tasks: 64-row blocks
   OP_ATTN_BWD_KV,    // dK, dV of the causal attention               tasks: (b, h, 128 keys)
   OP_ATTN_BWD_Q,     // dQ of the causal attention                   tasks: (b, h, 128 queries)
+  OP_TOKEN_SORT,     // (token, position) pairs sorted by token      tasks: 1
   OP_NOP,            // scheduler test: no work                      tasks: any
   OP_NUM_TYPES
 };
@@ -124,6 +130,8 @@ struct EmbedArgs {
   const float* wte; const float* wpe; float* x0;
   const float* dx0; float* dwte; float* dwpe;
   int32_t N, B, T, C, V, rows_per_task;
+  int32_t* sorted_tok; int32_t* sorted_pos;   // token ids in increasing order, stable
+  int32_t* block_start;  // [V / rows_per_task + 1]: first sorted entry of each vocabulary block
 };
 
 struct AdamArgs {
@@ -148,13 +156,20 @@ struct OpDesc {
   };
 };
 
+// A task waits until counters[first .. first+count) each reach epoch * need.
+struct WaitSpec {
+  int32_t first, count;
+  uint32_t need;
+};
+
 struct TaskDesc {
   int32_t op;
   int32_t idx;                     // task index within its op
+  int32_t sig;                     // counter this task adds 1 to when done
+  int32_t sig2;                    // op-level counter also added to (-1: none)
   int32_t nwait;
-  int32_t wait_ctr[kMaxWaits];     // counter (= op) indices
-  uint32_t wait_need[kMaxWaits];   // tasks of that op (per epoch)
-  int32_t pad;
+  WaitSpec wait[kMaxWaits];
+  int32_t pad[2];
 };
 
 // Soft error bits (the step runs to its end, AdamW skips its update).
@@ -168,8 +183,7 @@ struct KParams {
   const TaskDesc* tasks; int64_t ntasks;
   const OpDesc* ops;
   unsigned long long* counters;
-  unsigned long long* ticket;
-  unsigned long long ticket_base;
+  unsigned long long* tickets;     // [2]: ticket counter of even / odd launches (this one: epoch & 1)
   unsigned long long epoch;        // 1-based step number of this launch
   uint32_t* err;                   // [0] fatal code, [1] soft bits, [2] task of a fatal error, [3] counter
   uint64_t timeout_ns;

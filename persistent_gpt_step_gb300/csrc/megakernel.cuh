@@ -19,6 +19,8 @@ namespace pgs {
 
 struct KernelShared {
   GemmShared gemm;
+  uint64_t adam_bars[kAdamStages];
+  uint32_t adam_iter;
   uint32_t tmem_base;
   int32_t ok;
   int64_t task;
@@ -33,6 +35,13 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
                                              ~(uintptr_t)1023);
   const int warp = threadIdx.x >> 5;
   TcState st = {0u, 0u, 0u, 0u, 0u};
+  if (blockIdx.x == 0 && threadIdx.x == 0) kp.tickets[(kp.epoch + 1ull) & 1ull] = 0ull;  // next launch's
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kAdamStages; ++i) mbar_init(smem_u32(&sh.adam_bars[i]), 1);
+    sh.adam_iter = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
   if constexpr (kTC) {
     if (threadIdx.x == 0) {
       for (int i = 0; i < kTcStages; ++i) {
@@ -54,14 +63,11 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
       int64_t t = kp.ntasks;
       int ok = 0;
       if (ld_volatile_u32(&kp.err[0]) == 0u) {
-        t = pending >= 0 ? pending : (int64_t)(atomicAdd(kp.ticket, 1ull) - kp.ticket_base);
+        t = pending >= 0 ? pending : claim_task(kp);
         if (t < kp.ntasks) {
           ok = 1;
           const uint64_t t_claim = kp.trace ? globaltimer_ns() : 0;
-          const TaskDesc& d = kp.tasks[t];
-          for (int w = 0; w < d.nwait && ok; ++w)
-            ok = wait_counter(kp, d.wait_ctr[w], kp.epoch * (unsigned long long)d.wait_need[w],
-                              (uint32_t)t);
+          ok = task_ready(kp, t);
           if (kp.trace) {
             uint32_t smid;
             asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
@@ -129,18 +135,24 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
       case OP_ATTN_BWD: { const AttnArgs a = op.attn; task_attn_bwd_simt<act_t>(a, idx, reinterpret_cast<float*>(smem)); } break;
       case OP_EMBED_BWD_WTE: { const EmbedArgs a = op.emb; task_embed_bwd_wte(kp, a, idx, reinterpret_cast<int*>(smem)); } break;
       case OP_EMBED_BWD_WPE: { const EmbedArgs a = op.emb; task_embed_bwd_wpe(a, idx); } break;
-      case OP_ADAMW: { const AdamArgs a = op.adam; task_adamw(kp, a, idx); } break;
+      case OP_TOKEN_SORT: { const EmbedArgs a = op.emb; task_token_sort(kp, a, reinterpret_cast<int*>(smem)); } break;
+      case OP_ADAMW: {
+        const AdamArgs a = op.adam;
+        task_adamw(kp, a, idx, smem, sh.adam_bars, &sh.adam_iter);
+      } break;
       default: break;
     }
     __syncthreads();
     if (threadIdx.x == 0 && t != kp.skip_release) {
       __threadfence();
       fence_proxy_async_global();
-      red_release_add_u64(kp.counters + d.op, 1ull);
+      red_release_add_u64(kp.counters + d.sig, 1ull);
+      if (d.sig2 >= 0) red_release_add_u64(kp.counters + d.sig2, 1ull);
     }
     if (threadIdx.x == 0 && kp.trace) kp.trace[4 * t + 2] = globaltimer_ns();
   }
 
+  if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   if constexpr (kTC) {
     tc_fence_before();
     __syncthreads();

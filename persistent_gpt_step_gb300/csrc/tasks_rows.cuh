@@ -5,6 +5,7 @@
 // summation order, so a step is bitwise repeatable.
 #pragma once
 #include "device.cuh"
+#include "tc_gemm.cuh"
 
 namespace pgs {
 
@@ -248,7 +249,10 @@ __device__ inline void task_ce(const KParams& kp, const CeArgs& a, int idx) {
     const float lse = M + logf(S);
     const float zt = to_f<act_t>(z[t]);
     __syncwarp();
-    if (lane == 0) a.row_loss[r] = lse - zt;
+    if (lane == 0) {
+      a.row_loss[r] = lse - zt;
+      if (!isfinite(lse - zt)) set_soft(kp, kSoftNonFinite);
+    }
     for (int j = lane; j < a.V; j += 32) {
       const float x = to_f<act_t>(z[j]);
       float p = expf(x - lse);
@@ -322,17 +326,29 @@ __device__ inline void task_ce_bf16_vec(const KParams& kp, const CeArgs& a, int 
     const float lse = M + logf(warp_sum(s));
     const float zt = __bfloat162float(zr[t]);
     __syncwarp();
-    if (lane == 0) a.row_loss[r] = lse - zt;
-    for (j = lane; j < nvec; j += 32) {
-      float f[8];
-      bf16x8_to_f(z[j], f);
+    if (lane == 0) {
+      a.row_loss[r] = lse - zt;
+      if (!isfinite(lse - zt)) set_soft(kp, kSoftNonFinite);
+    }
+    for (j = lane; j < nvec; j += 128) {  // four 16-byte loads in flight per lane
+      uint4 u[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        float p = expf(f[e] - lse);
-        if (j * 8 + e == t) p -= 1.0f;
-        f[e] = p * invN;
+      for (int q = 0; q < 4; ++q)
+        if (j + 32 * q < nvec) u[q] = z[j + 32 * q];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int jq = j + 32 * q;
+        if (jq >= nvec) continue;
+        float f[8];
+        bf16x8_to_f(u[q], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float p = expf(f[e] - lse);
+          if (jq * 8 + e == t) p -= 1.0f;
+          f[e] = p * invN;
+        }
+        z[jq] = f_to_bf16x8(f);
       }
-      z[j] = f_to_bf16x8(f);
     }
   }
 }
@@ -363,16 +379,41 @@ __device__ inline void task_colsum(const ColsumArgs& a, int idx, float* smem) {
   const int ncol = min(a.cols_per_task, a.cols - c0);  // <= 64
   float acc0 = 0.f, acc1 = 0.f;
   const bool has0 = lane < ncol, has1 = lane + 32 < ncol;
+  constexpr int U = 8;  // rows of one warp in flight
   if (a.src_f32) {
     const float* src = reinterpret_cast<const float*>(a.src) + c0;
-    for (int r = warp; r < a.rows; r += kWarps) {
+    int r = warp;
+    for (; r + (U - 1) * kWarps < a.rows; r += U * kWarps) {
+      float x0[U], x1[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const float* row = src + (int64_t)(r + u * kWarps) * a.ld;
+        x0[u] = has0 ? row[lane] : 0.f;
+        x1[u] = has1 ? row[lane + 32] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) { acc0 += x0[u]; acc1 += x1[u]; }
+    }
+    for (; r < a.rows; r += kWarps) {
       const float* row = src + (int64_t)r * a.ld;
       if (has0) acc0 += row[lane];
       if (has1) acc1 += row[lane + 32];
     }
   } else {
     const act_t* src = reinterpret_cast<const act_t*>(a.src) + c0;
-    for (int r = warp; r < a.rows; r += kWarps) {
+    int r = warp;
+    for (; r + (U - 1) * kWarps < a.rows; r += U * kWarps) {
+      float x0[U], x1[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const act_t* row = src + (int64_t)(r + u * kWarps) * a.ld;
+        x0[u] = has0 ? to_f<act_t>(row[lane]) : 0.f;
+        x1[u] = has1 ? to_f<act_t>(row[lane + 32]) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) { acc0 += x0[u]; acc1 += x1[u]; }
+    }
+    for (; r < a.rows; r += kWarps) {
       const act_t* row = src + (int64_t)r * a.ld;
       if (has0) acc0 += to_f<act_t>(row[lane]);
       if (has1) acc1 += to_f<act_t>(row[lane + 32]);
@@ -388,37 +429,128 @@ __device__ inline void task_colsum(const ColsumArgs& a, int idx, float* smem) {
   }
 }
 
-// dwte[v] = sum over positions n with tok[n] = v of dx0[n] (in increasing n),
-// for a block of vocabulary rows; rows no token hit are written as zeros.
-__device__ inline void task_embed_bwd_wte(const KParams& kp, const EmbedArgs& a, int idx, int* stok) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int n = threadIdx.x; n < a.N; n += kThreads) {
+// Stable sort of the step's (token, position) pairs by token id, one block:
+// least-significant-digit radix sort with 8-bit digits in shared memory.  The
+// digit counts come from shared-memory atomics (order-free); the scatter walks
+// the elements in order on one warp, ranking equal digits with __match_any_sync,
+// so equal tokens keep increasing positions.
+__device__ inline void task_token_sort(const KParams& kp, const EmbedArgs& a, int* smem) {
+  const int N = a.N;
+  int* ka = smem;
+  int* va = ka + N;
+  int* kb = va + N;
+  int* vb = kb + N;
+  int* hist = vb + N;  // [256]
+  for (int n = threadIdx.x; n < N; n += kThreads) {
     int t = kp.tokens[n];
-    stok[n] = t < 0 ? 0 : (t >= a.V ? a.V - 1 : t);
+    ka[n] = t < 0 ? 0 : (t >= a.V ? a.V - 1 : t);
+    va[n] = n;
   }
-  __syncthreads();
-  const int v0 = idx * a.rows_per_task, v1 = min(v0 + a.rows_per_task, a.V);
-  const int nper = a.C >> 5;
-  for (int v = v0 + warp; v < v1; v += kWarps) {
-    float acc[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-    for (int n0 = 0; n0 < a.N; n0 += 32) {
-      const int n = n0 + lane;
-      unsigned mask = __ballot_sync(0xffffffffu, n < a.N && stok[n] == v);
-      while (mask) {
-        const int hit = n0 + __ffs(mask) - 1;
-        mask &= mask - 1;
-        const float* src = a.dx0 + (int64_t)hit * a.C;
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          if (i < nper) acc[i] += src[i * 32 + lane];
+  const int passes = a.V <= 256 ? 1 : (a.V <= 65536 ? 2 : 3);
+  for (int pass = 0; pass < passes; ++pass) {
+    const int shift = 8 * pass;
+    for (int i = threadIdx.x; i < 256; i += kThreads) hist[i] = 0;
+    __syncthreads();
+    for (int n = threadIdx.x; n < N; n += kThreads) atomicAdd(&hist[(ka[n] >> shift) & 255], 1);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int run = 0;
+      for (int i = 0; i < 256; ++i) { const int c = hist[i]; hist[i] = run; run += c; }
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      const unsigned lt = (1u << lane) - 1u;
+      for (int c0 = 0; c0 < N; c0 += 32) {
+        const int n = c0 + lane;
+        const bool live = n < N;
+        const int key = live ? ka[n] : 0;
+        const int d = live ? (key >> shift) & 255 : 256 + lane;  // dead lanes never match
+        const unsigned peers = __match_any_sync(0xffffffffu, d);
+        const int rank = __popc(peers & lt);
+        const int base = live ? hist[d] : 0;
+        __syncwarp();
+        if (live) {
+          kb[base + rank] = key;
+          vb[base + rank] = va[n];
+          if (rank == 0) hist[d] = base + __popc(peers);
+        }
+        __syncwarp();
       }
     }
-    float* dst = a.dwte + (int64_t)v * a.C;
+    __syncthreads();
+    int* t0 = ka; ka = kb; kb = t0;
+    int* t1 = va; va = vb; vb = t1;
+  }
+  for (int n = threadIdx.x; n < N; n += kThreads) {
+    a.sorted_tok[n] = ka[n];
+    a.sorted_pos[n] = va[n];
+  }
+  // first sorted entry of every block of rows_per_task vocabulary rows
+  const int nblk = (a.V + a.rows_per_task - 1) / a.rows_per_task;
+  for (int n = threadIdx.x; n <= N; n += kThreads) {
+    const int bprev = n == 0 ? -1 : ka[n - 1] / a.rows_per_task;
+    const int bcur = n == N ? nblk : ka[n] / a.rows_per_task;
+    for (int b = bprev + 1; b <= bcur; ++b) a.block_start[b] = n;
+  }
+}
+
+// dwte[v] = sum over positions n with tok[n] = v of dx0[n] (in increasing n),
+// for a block of vocabulary rows; rows no token hit are written as zeros.  The
+// block's entries of the sorted token list are found by binary search.
+__device__ __forceinline__ int lower_bound_i32(const int* a, int n, int key) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (a[mid] < key) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+template <int NV>
+__device__ __forceinline__ void wte_rows(const EmbedArgs& a, int v0, int v1, int i0, const int* stok, int nseg) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int v = v0 + warp; v < v1; v += kWarps) {
+    float4 acc[NV > 0 ? NV : 1];
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (i < nper) dst[i * 32 + lane] = acc[i];
+    for (int i = 0; i < (NV > 0 ? NV : 1); ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    int j = lower_bound_i32(stok, nseg, v);
+    float* dst = a.dwte + (int64_t)v * a.C;
+    if constexpr (NV > 0) {
+      for (; j < nseg && stok[j] == v; ++j) {
+        const float4* src = reinterpret_cast<const float4*>(a.dx0 + (int64_t)a.sorted_pos[i0 + j] * a.C);
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+          const float4 x = src[lane + 32 * i];
+          acc[i].x += x.x; acc[i].y += x.y; acc[i].z += x.z; acc[i].w += x.w;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < NV; ++i) reinterpret_cast<float4*>(dst)[lane + 32 * i] = acc[i];
+    } else {
+      const int jb = j;
+      for (int c = lane; c < a.C; c += 32) {
+        float s = 0.f;
+        for (j = jb; j < nseg && stok[j] == v; ++j) s += a.dx0[(int64_t)a.sorted_pos[i0 + j] * a.C + c];
+        dst[c] = s;
+      }
+    }
+  }
+}
+
+__device__ inline void task_embed_bwd_wte(const KParams& kp, const EmbedArgs& a, int idx, int* smem) {
+  (void)kp;
+  const int v0 = idx * a.rows_per_task, v1 = min(v0 + a.rows_per_task, a.V);
+  const int i0 = a.block_start[idx], nseg = a.block_start[idx + 1] - i0;
+  int* stok = smem;
+  for (int j = threadIdx.x; j < nseg; j += kThreads) stok[j] = a.sorted_tok[i0 + j];
+  __syncthreads();
+  switch ((a.C & 127) ? 0 : a.C >> 7) {
+    case 2: wte_rows<2>(a, v0, v1, i0, stok, nseg); break;
+    case 4: wte_rows<4>(a, v0, v1, i0, stok, nseg); break;
+    case 6: wte_rows<6>(a, v0, v1, i0, stok, nseg); break;
+    case 8: wte_rows<8>(a, v0, v1, i0, stok, nseg); break;
+    default: wte_rows<0>(a, v0, v1, i0, stok, nseg); break;
   }
 }
 
@@ -438,40 +570,115 @@ __device__ inline void task_embed_bwd_wpe(const EmbedArgs& a, int idx) {
 // AdamW on one chunk of a parameter tensor (decoupled weight decay first):
 // p *= 1 - lr wd; m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2;
 // p -= lr (m / bc1) / (sqrt(v / bc2) + eps); bf16 copy of p written if requested.
-__device__ inline void task_adamw(const KParams& kp, const AdamArgs& a, int idx) {
+// The chunk streams through shared memory in sub-chunks of kAdamSub parameters:
+// one thread issues 1-D bulk copies (cp.async.bulk, completion counted on an
+// mbarrier) of p, g, m and v for up to kAdamStages sub-chunks ahead, all threads
+// update a staged sub-chunk in place, and bulk stores write p, m, v and the bf16
+// copy back — about 128 KB in flight per SM without spending registers on it.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// iter: this block's count of sub-chunks so far (stage = iter mod kAdamStages,
+// phase = (iter / kAdamStages) mod 2), shared by the block's threads.
+__device__ inline void task_adamw(const KParams& kp, const AdamArgs& a, int idx, uint8_t* smem, uint64_t* bars,
+                                  uint32_t* iter) {
   if (ld_volatile_u32(&kp.err[1]) & (kSoftBadToken | kSoftNonFinite)) return;
   const int64_t lo = (int64_t)idx * a.chunk;
   const int64_t hi = min(lo + a.chunk, a.n);
+  const int nsub = (int)((hi - lo + kAdamSub - 1) / kAdamSub);
+  const uint32_t it0 = *iter;
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
+  const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(bars);
+  auto stage_of = [&](int s) { return (it0 + (uint32_t)s) % kAdamStages; };
+  auto count_of = [&](int s) {
+    const int64_t rest = hi - (lo + (int64_t)s * kAdamSub);
+    return (int)(rest < kAdamSub ? rest : (int64_t)kAdamSub);
+  };
+  auto issue = [&](int s) {  // one thread
+    const uint32_t st = stage_of(s);
+    const int64_t base = lo + (int64_t)s * kAdamSub;
+    const uint32_t bytes = (uint32_t)count_of(s) * 4u;
+    const uint32_t buf = sbase + st * kAdamStageBytes;
+    const uint32_t bar = bar0 + 8 * st;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(4 * bytes) : "memory");
+    bulk_load(buf, a.p + base, bytes, bar);
+    bulk_load(buf + kAdamSub * 4, a.g + base, bytes, bar);
+    bulk_load(buf + kAdamSub * 8, a.m + base, bytes, bar);
+    bulk_load(buf + kAdamSub * 12, a.v + base, bytes, bar);
+  };
+  if (threadIdx.x == 0) {
+    bulk_wait_read_all();  // earlier bulk stores have finished reading these buffers
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    for (int s = 0; s < min(nsub, kAdamStages); ++s) issue(s);
+  }
   const float decay = 1.0f - kp.lr * kp.wd * a.decay;
   const float b1 = kp.beta1, b2 = kp.beta2, ib1 = 1.0f - kp.beta1, ib2 = 1.0f - kp.beta2;
   const float rbc1 = 1.0f / kp.bc1, rbc2 = 1.0f / kp.bc2;
-  float4* P = reinterpret_cast<float4*>(a.p);
-  const float4* G = reinterpret_cast<const float4*>(a.g);
-  float4* Mo = reinterpret_cast<float4*>(a.m);
-  float4* Vo = reinterpret_cast<float4*>(a.v);
-  for (int64_t i = lo / 4 + threadIdx.x; i < hi / 4; i += kThreads) {
-    float4 p = P[i], g = G[i], m = Mo[i], v = Vo[i];
-    float pp[4] = {p.x, p.y, p.z, p.w}, gg[4] = {g.x, g.y, g.z, g.w};
-    float mm[4] = {m.x, m.y, m.z, m.w}, vv[4] = {v.x, v.y, v.z, v.w};
+  for (int s = 0; s < nsub; ++s) {
+    const uint32_t st = stage_of(s);
+    const uint32_t phase = ((it0 + (uint32_t)s) / kAdamStages) & 1u;
+    if (!mbar_wait(kp, bar0 + 8 * st, phase)) return;
+    uint8_t* buf = smem + st * kAdamStageBytes;
+    float4* P = reinterpret_cast<float4*>(buf);
+    const float4* G = reinterpret_cast<const float4*>(buf + kAdamSub * 4);
+    float4* Mo = reinterpret_cast<float4*>(buf + kAdamSub * 8);
+    float4* Vo = reinterpret_cast<float4*>(buf + kAdamSub * 12);
+    uint2* S = reinterpret_cast<uint2*>(buf + kAdamSub * 16);
+    const int cnt4 = count_of(s) / 4;
+    for (int i = threadIdx.x; i < cnt4; i += kThreads) {
+      const float4 p = P[i], g = G[i], m = Mo[i], v = Vo[i];
+      float pp[4] = {p.x, p.y, p.z, p.w}, gg[4] = {g.x, g.y, g.z, g.w};
+      float mm[4] = {m.x, m.y, m.z, m.w}, vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      pp[e] *= decay;
-      mm[e] = b1 * mm[e] + ib1 * gg[e];
-      vv[e] = b2 * vv[e] + ib2 * gg[e] * gg[e];
-      const float mh = mm[e] * rbc1, vh = vv[e] * rbc2;
-      pp[e] -= kp.lr * mh / (sqrtf(vh) + kp.eps);
+      for (int e = 0; e < 4; ++e) {
+        pp[e] *= decay;
+        mm[e] = b1 * mm[e] + ib1 * gg[e];
+        vv[e] = b2 * vv[e] + ib2 * gg[e] * gg[e];
+        const float mh = mm[e] * rbc1, vh = vv[e] * rbc2;
+        pp[e] -= kp.lr * mh / (sqrtf(vh) + kp.eps);
+      }
+      P[i] = make_float4(pp[0], pp[1], pp[2], pp[3]);
+      Mo[i] = make_float4(mm[0], mm[1], mm[2], mm[3]);
+      Vo[i] = make_float4(vv[0], vv[1], vv[2], vv[3]);
+      if (a.shadow) {
+        __nv_bfloat162 lo2 = __floats2bfloat162_rn(pp[0], pp[1]);
+        __nv_bfloat162 hi2 = __floats2bfloat162_rn(pp[2], pp[3]);
+        S[i] = make_uint2(*reinterpret_cast<uint32_t*>(&lo2), *reinterpret_cast<uint32_t*>(&hi2));
+      }
     }
-    P[i] = make_float4(pp[0], pp[1], pp[2], pp[3]);
-    Mo[i] = make_float4(mm[0], mm[1], mm[2], mm[3]);
-    Vo[i] = make_float4(vv[0], vv[1], vv[2], vv[3]);
-    if (a.shadow) {
-      __nv_bfloat162 lo2 = __floats2bfloat162_rn(pp[0], pp[1]);
-      __nv_bfloat162 hi2 = __floats2bfloat162_rn(pp[2], pp[3]);
-      uint2 u;
-      u.x = *reinterpret_cast<uint32_t*>(&lo2);
-      u.y = *reinterpret_cast<uint32_t*>(&hi2);
-      reinterpret_cast<uint2*>(a.shadow)[i] = u;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic smem writes -> bulk stores
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int64_t base = lo + (int64_t)s * kAdamSub;
+      const uint32_t bytes = (uint32_t)count_of(s) * 4u;
+      const uint32_t sb = sbase + st * kAdamStageBytes;
+      bulk_store(a.p + base, sb, bytes);
+      bulk_store(a.m + base, sb + kAdamSub * 8, bytes);
+      bulk_store(a.v + base, sb + kAdamSub * 12, bytes);
+      if (a.shadow) bulk_store(a.shadow + base, sb + kAdamSub * 16, bytes / 2);
+      bulk_commit();
+      if (s + kAdamStages < nsub) {
+        bulk_wait_read_all();  // this stage's stores have read the buffer
+        issue(s + kAdamStages);
+      }
     }
+  }
+  if (threadIdx.x == 0) {
+    bulk_wait_all();  // writes complete before the task's release
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    *iter = it0 + (uint32_t)nsub;
   }
 }
 

@@ -319,14 +319,6 @@ __device__ __forceinline__ void epi_bar_sync() {  // the four epilogue warps
   asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
-__device__ __forceinline__ bool gemm_task_ready(const KParams& kp, int64_t t) {
-  const TaskDesc& d = kp.tasks[t];
-  bool ok = true;
-  for (int w = 0; w < d.nwait && ok; ++w)
-    ok = wait_counter(kp, d.wait_ctr[w], kp.epoch * (unsigned long long)d.wait_need[w], (uint32_t)t);
-  return ok;
-}
-
 // Runs GEMM tasks starting with t_first (claimed, dependencies satisfied) and
 // returns the next claimed ticket (not a GEMM, or >= ntasks).
 __device__ inline int64_t gemm_run(const KParams& kp, int64_t t_first, GemmShared& gs, uint8_t* smem_tiles,
@@ -357,10 +349,10 @@ __device__ inline int64_t gemm_run(const KParams& kp, int64_t t_first, GemmShare
         int64_t t = kp.ntasks;
         bool gemm = false;
         if (ld_volatile_u32(&kp.err[0]) == 0u) {
-          t = (int64_t)(atomicAdd(kp.ticket, 1ull) - kp.ticket_base);
+          t = claim_task(kp);
           if (t < kp.ntasks && kp.ops[kp.tasks[t].op].type == OP_GEMM) {
             const uint64_t t_claim = kp.trace ? globaltimer_ns() : 0;
-            gemm = gemm_task_ready(kp, t);
+            gemm = task_ready(kp, t);
             if (!gemm) t = kp.ntasks;  // a wait failed: stop the run, the main loop drains
             else if (kp.trace) {
               kp.trace[4 * t + 0] = t_claim;
@@ -502,7 +494,8 @@ __device__ inline int64_t gemm_run(const KParams& kp, int64_t t_first, GemmShare
         if (t != kp.skip_release) {
           __threadfence();
           fence_proxy_async_global();
-          red_release_add_u64(kp.counters + kp.tasks[t].op, 1ull);
+          red_release_add_u64(kp.counters + kp.tasks[t].sig, 1ull);
+          if (kp.tasks[t].sig2 >= 0) red_release_add_u64(kp.counters + kp.tasks[t].sig2, 1ull);
         }
         if (kp.trace) kp.trace[4 * t + 2] = globaltimer_ns();
       }

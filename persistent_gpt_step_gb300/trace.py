@@ -22,7 +22,7 @@ import numpy as np
 FAMILIES = ["embed", "layernorm-fwd", "gemm", "attention-fwd", "cross-entropy", "loss",
             "layernorm-bwd", "column-sum", "attention-bwd", "embedding-bwd-wte",
             "embedding-bwd-wpe", "adamw", "attention-bwd-pre", "attention-bwd-kv", "attention-bwd-q",
-            "nop"]
+            "token-sort", "nop"]
 
 
 def family_table(trace: np.ndarray, task_ops: np.ndarray, op_types, grid: int):
@@ -49,6 +49,7 @@ def main():
     ap.add_argument("--config", default="main")
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--json", default=None)
+    ap.add_argument("--ops", action="store_true", help="print every op's first start / last end")
     args = ap.parse_args()
     import torch
 
@@ -83,9 +84,18 @@ def main():
             continue
         sel = task_ops == o
         span = (end[sel].max() - start[sel].min()) / 1e3
-        M, N, K, BN = op_dims[o]
+        M, N, K, BN = op_dims[o][:4]
         print(f"{o:7d} {M:6d} {N:6d} {K:6d} {BN:4d} {op_ntasks[o]:6d} {span:8.1f} "
               f"{2.0 * M * N * K / span / 1e6:7.1f} {(start[sel].min() - t0) / 1e6:8.3f}")
+    if args.ops:
+        print(f"\n{'op':>5s} {'family':20s} {'tasks':>6s} {'start':>8s} {'end':>8s} {'busy/blk':>9s}")
+        rows = []
+        for o, ty in enumerate(op_types):
+            sel = task_ops == o
+            rows.append(((start[sel].min() - t0) / 1e6, o, ty, int(sel.sum()), (end[sel].max() - t0) / 1e6,
+                         (end[sel] - start[sel]).sum() / 1e6 / grid))
+        for st, o, ty, nt, en, busy in sorted(rows):
+            print(f"{o:5d} {FAMILIES[ty]:20s} {nt:6d} {st:8.3f} {en:8.3f} {busy:9.4f}")
     if args.json:
         json.dump({"config": args.config, "kernel_ms": kms, "grid": grid, "rows": rows}, open(args.json, "w"))
 

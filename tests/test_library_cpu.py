@@ -161,26 +161,43 @@ def test_zipf_frequencies():
 
 # ----------------------------------------------------------------- task graph
 
-@pytest.mark.parametrize("name", ["tiny", "small", "main"])
+@pytest.mark.parametrize("name", ["tiny", "small", "main", "350m"])
 def test_task_graph_is_topological(lib, name):
-    tasks, types, ntk = B.describe_graph(I.CONFIGS[name])
-    first = {}
-    counts = {}
-    for i, (op, idx, waits) in enumerate(tasks):
-        first.setdefault(op, i)
-        counts[op] = counts.get(op, 0) + 1
-        for wop, need in waits:
-            assert wop < op or first[wop] < first[op]
-            assert need == ntk[wop]
-    assert [counts[o] for o in range(len(types))] == ntk
+    """Every counter a task waits on is signalled only by earlier tickets, as
+    many times as the wait needs (the no-deadlock condition of the ticket loop)."""
+    from collections import Counter
+    tasks, types, ntk, dims = B.describe_graph(I.CONFIGS[name], dims=True)
+    sig_count = Counter(t[2] for t in tasks) + Counter(t[4] for t in tasks if t[4] >= 0)
+    seen = Counter()
+    for op, idx, sig, waits, sig2 in tasks:
+        ctr0, nblk = dims[op][4], dims[op][5]
+        assert ctr0 <= sig < ctr0 + nblk
+        assert sig2 == (ctr0 + nblk - 1 if nblk > 1 else -1)
+        for first, count, need in waits:
+            for c in range(first, first + count):
+                assert sig_count[c] == need
+                assert seen[c] == sig_count[c]       # all signallers are earlier tickets
+        seen[sig] += 1
+        if sig2 >= 0:
+            seen[sig2] += 1
+    assert sorted(Counter(t[0] for t in tasks).items()) == list(enumerate(ntk))
     # every parameter tensor gets exactly one AdamW op
-    n_adam = sum(1 for t in types if t == 11)
-    assert n_adam == len(O.param_table(I.CONFIGS[name]))
+    assert sum(1 for t in types if t == 11) == len(O.param_table(I.CONFIGS[name]))
 
 
-def _simulate(tasks, ntk, n_blocks, skip=None, timeout=5.0, seed=0):
+def test_row_blocks_make_the_forward_a_wavefront(lib):
+    """On the bf16 path a QKV tile waits only for its own 128-row block of LN1."""
+    tasks, types, ntk, dims = B.describe_graph(I.CONFIGS["main"], dims=True)
+    gemm_row_ops = [o for o, t in enumerate(types) if t == 2 and dims[o][5] > 1]
+    assert gemm_row_ops
+    o = gemm_row_ops[0]
+    waits = [w for (op, _, _, ws, _) in tasks if op == o for w in ws]
+    assert all(count == 1 for _, count, _ in waits)
+
+
+def _simulate(tasks, n_counters, n_blocks, skip=None, timeout=5.0, seed=0):
     """Blocks as threads running the ticket loop with random delays."""
-    counters = [0] * len(ntk)
+    counters = [0] * n_counters
     ticket = [0]
     lock = threading.Lock()
     done = []
@@ -194,20 +211,23 @@ def _simulate(tasks, ntk, n_blocks, skip=None, timeout=5.0, seed=0):
                 ticket[0] += 1
             if t >= len(tasks) or failed:
                 return
-            op, idx, waits = tasks[t]
+            op, idx, sig, waits, sig2 = tasks[t]
             t0 = time.time()
-            for wop, need in waits:
-                while counters[wop] < need:
-                    if time.time() - t0 > timeout:
-                        failed.append(t)
-                        return
-                    time.sleep(0)
+            for first, count, need in waits:
+                for c in range(first, first + count):
+                    while counters[c] < need:
+                        if time.time() - t0 > timeout:
+                            failed.append(t)
+                            return
+                        time.sleep(0)
             if rng.random() < 0.01:
                 time.sleep(0.001)
             with lock:
                 done.append(t)
                 if t != skip:
-                    counters[op] += 1
+                    counters[sig] += 1
+                    if sig2 >= 0:
+                        counters[sig2] += 1
 
     th = [threading.Thread(target=block) for _ in range(n_blocks)]
     for x in th:
@@ -217,15 +237,22 @@ def _simulate(tasks, ntk, n_blocks, skip=None, timeout=5.0, seed=0):
     return counters, done, failed
 
 
-def test_scheduler_simulation_completes_tiny(lib):
-    tasks, types, ntk = B.describe_graph(I.CONFIGS["tiny"])
-    counters, done, failed = _simulate(tasks, ntk, 16)
+def _n_counters(dims):
+    return max(d[4] + d[5] for d in dims)
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_scheduler_simulation_completes(lib, name):
+    tasks, types, ntk, dims = B.describe_graph(I.CONFIGS[name], dims=True)
+    counters, done, failed = _simulate(tasks, _n_counters(dims), 16)
     assert not failed
-    assert counters == ntk
     assert sorted(done) == list(range(len(tasks)))
+    from collections import Counter
+    want = Counter(t[2] for t in tasks) + Counter(t[4] for t in tasks if t[4] >= 0)
+    assert counters == [want[c] for c in range(_n_counters(dims))]
 
 
 def test_scheduler_simulation_skipped_release_times_out(lib):
-    tasks, types, ntk = B.describe_graph(I.CONFIGS["tiny"])
-    counters, done, failed = _simulate(tasks, ntk, 8, skip=0, timeout=0.5)
-    assert failed and counters[0] == ntk[0] - 1
+    tasks, types, ntk, dims = B.describe_graph(I.CONFIGS["tiny"], dims=True)
+    counters, done, failed = _simulate(tasks, _n_counters(dims), 8, skip=0, timeout=0.5)
+    assert failed

@@ -207,12 +207,12 @@ __device__ inline void task_attn_fwd_tc(const AttnArgs& a, int idx, uint8_t* sme
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
   const float i0 = 1.0f / l0, i1 = 1.0f / l1;
-  __nv_bfloat16* O = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)b * a.T * a.C + h * 64;
+  __nv_bfloat16* O = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)b * a.T * a.ld_o + h * 64;
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
     const int c = nt * 8 + 2 * (lane & 3);
-    *reinterpret_cast<uint32_t*>(O + (int64_t)ra * a.C + c) = pack_bf16x2(o[nt][0] * i0, o[nt][1] * i0);
-    *reinterpret_cast<uint32_t*>(O + (int64_t)rb * a.C + c) = pack_bf16x2(o[nt][2] * i1, o[nt][3] * i1);
+    *reinterpret_cast<uint32_t*>(O + (int64_t)ra * a.ld_o + c) = pack_bf16x2(o[nt][0] * i0, o[nt][1] * i0);
+    *reinterpret_cast<uint32_t*>(O + (int64_t)rb * a.ld_o + c) = pack_bf16x2(o[nt][2] * i1, o[nt][3] * i1);
   }
   if ((lane & 3) == 0) {
     float* L = a.lse + ((int64_t)b * a.H + h) * a.T;
@@ -237,7 +237,7 @@ __device__ inline void task_attn_bwd_pre(const AttnArgs& a, int idx) {
       float s = 0.f;
       if (h < a.H) {
         const uint4 u = *reinterpret_cast<const uint4*>(dO + (int64_t)r * a.C + h * 64 + sub * 8);
-        const uint4 v = *reinterpret_cast<const uint4*>(O + (int64_t)r * a.C + h * 64 + sub * 8);
+        const uint4 v = *reinterpret_cast<const uint4*>(O + (int64_t)r * a.ld_o + h * 64 + sub * 8);
         float fu[8], fv[8];
         bf16x8_to_f(u, fu);
         bf16x8_to_f(v, fv);

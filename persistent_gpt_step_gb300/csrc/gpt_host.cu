@@ -243,6 +243,7 @@ struct Bump {
 };
 
 struct Layout {
+  size_t ldc, ldf;  // row pitch (elements) of the padded C- and F-wide activations
   size_t params, grads, m, v, shadow;
   std::vector<size_t> x, xm, ln1, ln1_mu, ln1_rs, qkv, atto, lse, ln2, ln2_mu, ln2_rs, hpre, gact;
   size_t lnf, lnf_mu, lnf_rs, logits, row_loss, loss;
@@ -271,6 +272,11 @@ Layout make_layout(const gpt_config& c, size_t nparams, int lm_ksplit) {
   const int L = c.n_layer;
   const size_t BHT = (size_t)c.batch * c.n_head * c.seq_len;
   const size_t nrb = ln_tasks((int)N);
+  // activations a weight-gradient GEMM reads as its second operand carry a
+  // 64-column pad whose first column is 1 (bias gradients come out of the GEMM)
+  const size_t pad = c.linear_bias ? 64 : 0;
+  Lo.ldc = C + pad;
+  Lo.ldf = F + pad;
   Lo.params = b.take(nparams * 4);
   Lo.grads = b.take(nparams * 4);
   Lo.m = b.take(nparams * 4);
@@ -279,17 +285,17 @@ Layout make_layout(const gpt_config& c, size_t nparams, int lm_ksplit) {
   for (int l = 0; l <= L; ++l) Lo.x.push_back(b.take(N * C * 4));
   for (int l = 0; l < L; ++l) {
     Lo.xm.push_back(b.take(N * C * 4));
-    Lo.ln1.push_back(b.take(N * C * act));
+    Lo.ln1.push_back(b.take(N * Lo.ldc * act));
     Lo.ln1_mu.push_back(b.take(N * 4));
     Lo.ln1_rs.push_back(b.take(N * 4));
     Lo.qkv.push_back(b.take(N * 3 * C * act));
-    Lo.atto.push_back(b.take(N * C * act));
+    Lo.atto.push_back(b.take(N * Lo.ldc * act));
     Lo.lse.push_back(b.take(BHT * 4));
-    Lo.ln2.push_back(b.take(N * C * act));
+    Lo.ln2.push_back(b.take(N * Lo.ldc * act));
     Lo.ln2_mu.push_back(b.take(N * 4));
     Lo.ln2_rs.push_back(b.take(N * 4));
     Lo.hpre.push_back(b.take(N * F * act));
-    Lo.gact.push_back(b.take(N * F * act));
+    Lo.gact.push_back(b.take(N * Lo.ldf * act));
   }
   Lo.lnf = b.take(N * C * act);
   Lo.lnf_mu = b.take(N * 4);
@@ -628,6 +634,8 @@ int gemm_op(gpt* h, OpDesc* op, int M, int N, int K, Operand A, Operand B, int e
   g.a_mn = A.mn_major; g.b_mn = B.mn_major;
   g.epi = epi;
   g.ksplit = ksplit;
+  g.n_real = N;
+  g.bias_grad = nullptr;
   g.a_map = g.b_map = -1;
   if (is_bf16(h->cfg)) {
     g.BM = kTcBM;
@@ -670,6 +678,7 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
   auto G = [&](int t) -> float* { return t < 0 ? nullptr : h->grads + h->tensors[t].offset; };
   Builder bld{h};
   const int N = D.N, C = D.C, F = D.F, V = D.V, L = D.L;
+  const int LDC = (int)Lo.ldc, LDF = (int)Lo.ldf;  // padded pitches (bias-gradient column)
   int rc;
 
   // ---------------- forward ----------------
@@ -683,35 +692,35 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
     const TensorIds& id = h->lid[l];
     o = blank(OP_LN_FWD, ln_tasks(N));
     o.lnf = LnFwdArgs{F32(Lo.x[l]), P(id.ln1_g), P(id.ln1_b), ACT(Lo.ln1[l]), F32(Lo.ln1_mu[l]),
-                      F32(Lo.ln1_rs[l]), N, C, kRowsLn, c.ln_eps};
+                      F32(Lo.ln1_rs[l]), N, C, kRowsLn, c.ln_eps, LDC};
     op_ln1[l] = bld.add(o, {prev});
     // qkv = ln1 . Wqkv^T + b
-    if ((rc = gemm_op(h, &o, N, 3 * C, C, {ACT(Lo.ln1[l]), C, false}, {W(id.w_qkv), C, false}, EPI_STORE, 1)))
+    if ((rc = gemm_op(h, &o, N, 3 * C, C, {ACT(Lo.ln1[l]), LDC, false}, {W(id.w_qkv), C, false}, EPI_STORE, 1)))
       return rc;
     o.gemm.out = ACT(Lo.qkv[l]); o.gemm.ldo = 3 * C; o.gemm.bias = P(id.b_qkv);
     op_qkv[l] = bld.add(o, {op_ln1[l]});
     o = blank(OP_ATTN_FWD, bf ? D.B * D.H * (D.T / 128) : D.B * D.H * ((D.T + qblock - 1) / qblock));
     o.attn = AttnArgs{ACT(Lo.qkv[l]), ACT(Lo.atto[l]), F32(Lo.lse[l]), nullptr, nullptr, nullptr,
-                      D.B, D.T, D.H, D.d, C, qblock, 1.0f / std::sqrt((float)D.d)};
+                      D.B, D.T, D.H, D.d, C, qblock, 1.0f / std::sqrt((float)D.d), LDC};
     op_attn[l] = bld.add(o, {op_qkv[l]});
     // xm = x + o . Wo^T + b
-    if ((rc = gemm_op(h, &o, N, C, C, {ACT(Lo.atto[l]), C, false}, {W(id.w_o), C, false}, EPI_RESID, 1)))
+    if ((rc = gemm_op(h, &o, N, C, C, {ACT(Lo.atto[l]), LDC, false}, {W(id.w_o), C, false}, EPI_RESID, 1)))
       return rc;
     o.gemm.out = F32(Lo.xm[l]); o.gemm.ldo = C; o.gemm.bias = P(id.b_o);
     o.gemm.resid = F32(Lo.x[l]); o.gemm.ldr = C;
     op_atto[l] = bld.add(o, {op_attn[l]});
     o = blank(OP_LN_FWD, ln_tasks(N));
     o.lnf = LnFwdArgs{F32(Lo.xm[l]), P(id.ln2_g), P(id.ln2_b), ACT(Lo.ln2[l]), F32(Lo.ln2_mu[l]),
-                      F32(Lo.ln2_rs[l]), N, C, kRowsLn, c.ln_eps};
+                      F32(Lo.ln2_rs[l]), N, C, kRowsLn, c.ln_eps, LDC};
     op_ln2[l] = bld.add(o, {op_atto[l]});
     // h = ln2 . W1^T + b1 ; g = GELU(h)
-    if ((rc = gemm_op(h, &o, N, F, C, {ACT(Lo.ln2[l]), C, false}, {W(id.w_1), C, false}, EPI_GELU, 1)))
+    if ((rc = gemm_op(h, &o, N, F, C, {ACT(Lo.ln2[l]), LDC, false}, {W(id.w_1), C, false}, EPI_GELU, 1)))
       return rc;
-    o.gemm.out = ACT(Lo.hpre[l]); o.gemm.ldo = F; o.gemm.out2 = ACT(Lo.gact[l]); o.gemm.ldo2 = F;
+    o.gemm.out = ACT(Lo.hpre[l]); o.gemm.ldo = F; o.gemm.out2 = ACT(Lo.gact[l]); o.gemm.ldo2 = LDF;
     o.gemm.bias = P(id.b_1);
     op_up[l] = bld.add(o, {op_ln2[l]});
     // x_{l+1} = xm + g . W2^T + b2
-    if ((rc = gemm_op(h, &o, N, C, F, {ACT(Lo.gact[l]), F, false}, {W(id.w_2), F, false}, EPI_RESID, 1)))
+    if ((rc = gemm_op(h, &o, N, C, F, {ACT(Lo.gact[l]), LDF, false}, {W(id.w_2), F, false}, EPI_RESID, 1)))
       return rc;
     o.gemm.out = F32(Lo.x[l + 1]); o.gemm.ldo = C; o.gemm.bias = P(id.b_2);
     o.gemm.resid = F32(Lo.xm[l]); o.gemm.ldr = C;
@@ -719,7 +728,7 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
   }
   o = blank(OP_LN_FWD, ln_tasks(N));
   o.lnf = LnFwdArgs{F32(Lo.x[L]), P(h->t_lnf_g), P(h->t_lnf_b), ACT(Lo.lnf), F32(Lo.lnf_mu), F32(Lo.lnf_rs),
-                    N, C, kRowsLn, c.ln_eps};
+                    N, C, kRowsLn, c.ln_eps, C};
   const int op_lnf = bld.add(o, {prev});
   // logits = lnf . Wlm^T
   if ((rc = gemm_op(h, &o, N, V, C, {ACT(Lo.lnf), C, false}, {W(h->t_wlm), C, false}, EPI_STORE, 1))) return rc;
@@ -779,26 +788,28 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
   }
   for (int l = L - 1; l >= 0; --l) {
     const TensorIds& id = h->lid[l];
-    // MLP down: dg = dx . W2 (then * GELU'(h)) ; dW2 = dx^T . g ; db2 = colsum(dx)
+    // MLP down: dg = dx . W2 (then * GELU'(h)) ; dW2 = dx^T . g ; db2 = dx^T . 1
     if ((rc = gemm_op(h, &o, N, F, C, {ACT(Lo.dx_act[l + 1]), C, false}, {W(id.w_2), F, true}, EPI_GELU_BWD, 1)))
       return rc;
     o.gemm.out = ACT(Lo.dh[l]); o.gemm.ldo = F; o.gemm.aux = ACT(Lo.hpre[l]); o.gemm.ldaux = F;
     const int op_down_dx = bld.add(o, {op_dres});
-    if ((rc = gemm_op(h, &o, C, F, N, {ACT(Lo.dx_act[l + 1]), C, true}, {ACT(Lo.gact[l]), F, true}, EPI_F32, 1)))
+    // [dW2 | db2] = dx^T . [g | 1]
+    if ((rc = gemm_op(h, &o, C, LDF, N, {ACT(Lo.dx_act[l + 1]), C, true}, {ACT(Lo.gact[l]), LDF, true}, EPI_F32, 1)))
       return rc;
-    o.gemm.out = G(id.w_2); o.gemm.ldo = F;
+    o.gemm.out = G(id.w_2); o.gemm.ldo = F; o.gemm.n_real = F; o.gemm.bias_grad = G(id.b_2);
     const int op_down_dw = bld.add(o, {op_dres});
-    if (id.b_2 >= 0) adam(id.b_2, {colsum(F32(Lo.dx[l + 1]), true, C, N, C, G(id.b_2), op_dres)});
+    if (id.b_2 >= 0) adam(id.b_2, {op_down_dw});
     adam(id.w_2, {op_down_dw, op_down_dx});
-    // MLP up: da2 = dh . W1 ; dW1 = dh^T . ln2 ; db1 = colsum(dh)
+    // MLP up: da2 = dh . W1 ; dW1 = dh^T . ln2 ; db1 = dh^T . 1
     if ((rc = gemm_op(h, &o, N, C, F, {ACT(Lo.dh[l]), F, false}, {W(id.w_1), C, true}, EPI_F32, 1))) return rc;
     o.gemm.out = F32(Lo.da2[l]); o.gemm.ldo = C;
     const int op_up_dx = bld.add(o, {op_down_dx});
-    if ((rc = gemm_op(h, &o, F, C, N, {ACT(Lo.dh[l]), F, true}, {ACT(Lo.ln2[l]), C, true}, EPI_F32, 1)))
+    // [dW1 | db1] = dh^T . [ln2 | 1]
+    if ((rc = gemm_op(h, &o, F, LDC, N, {ACT(Lo.dh[l]), F, true}, {ACT(Lo.ln2[l]), LDC, true}, EPI_F32, 1)))
       return rc;
-    o.gemm.out = G(id.w_1); o.gemm.ldo = C;
+    o.gemm.out = G(id.w_1); o.gemm.ldo = C; o.gemm.n_real = C; o.gemm.bias_grad = G(id.b_1);
     const int op_up_dw = bld.add(o, {op_down_dx});
-    if (id.b_1 >= 0) adam(id.b_1, {colsum(ACT(Lo.dh[l]), false, F, N, F, G(id.b_1), op_down_dx)});
+    if (id.b_1 >= 0) adam(id.b_1, {op_up_dw});
     adam(id.w_1, {op_up_dw, op_up_dx});
     // LN2 backward: dxm = dx + LN2'(da2)
     o = blank(OP_LN_BWD, nrb);
@@ -808,20 +819,21 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
     const int op_ln2b = bld.add(o, {op_up_dx, op_dres});
     adam(id.ln2_g, {colsum(F32(Lo.ln2_gp[l]), true, C, nrb, C, G(id.ln2_g), op_ln2b)});
     if (id.ln2_b >= 0) adam(id.ln2_b, {colsum(F32(Lo.ln2_bp[l]), true, C, nrb, C, G(id.ln2_b), op_ln2b)});
-    // attention out: dO = dxm . Wo ; dWo = dxm^T . o ; dbo = colsum(dxm)
+    // attention out: dO = dxm . Wo ; dWo = dxm^T . o ; dbo = dxm^T . 1
     if ((rc = gemm_op(h, &o, N, C, C, {ACT(Lo.dxm_act[l]), C, false}, {W(id.w_o), C, true}, EPI_STORE, 1)))
       return rc;
     o.gemm.out = ACT(Lo.dO[l]); o.gemm.ldo = C;
     const int op_atto_dx = bld.add(o, {op_ln2b});
-    if ((rc = gemm_op(h, &o, C, C, N, {ACT(Lo.dxm_act[l]), C, true}, {ACT(Lo.atto[l]), C, true}, EPI_F32, 1)))
+    // [dWo | dbo] = dxm^T . [o | 1]
+    if ((rc = gemm_op(h, &o, C, LDC, N, {ACT(Lo.dxm_act[l]), C, true}, {ACT(Lo.atto[l]), LDC, true}, EPI_F32, 1)))
       return rc;
-    o.gemm.out = G(id.w_o); o.gemm.ldo = C;
+    o.gemm.out = G(id.w_o); o.gemm.ldo = C; o.gemm.n_real = C; o.gemm.bias_grad = G(id.b_o);
     const int op_atto_dw = bld.add(o, {op_ln2b});
-    if (id.b_o >= 0) adam(id.b_o, {colsum(F32(Lo.dxm[l]), true, C, N, C, G(id.b_o), op_ln2b)});
+    if (id.b_o >= 0) adam(id.b_o, {op_atto_dw});
     adam(id.w_o, {op_atto_dw, op_atto_dx});
     // attention backward -> dqkv
     const AttnArgs att{ACT(Lo.qkv[l]), ACT(Lo.atto[l]), F32(Lo.lse[l]), ACT(Lo.dO[l]), ACT(Lo.dqkv[l]),
-                       F32(Lo.att_scr[l]), D.B, D.T, D.H, D.d, C, qblock, 1.0f / std::sqrt((float)D.d)};
+                       F32(Lo.att_scr[l]), D.B, D.T, D.H, D.d, C, qblock, 1.0f / std::sqrt((float)D.d), LDC};
     int op_attb, op_attb2 = -1;
     if (bf) {
       o = blank(OP_ATTN_BWD_PRE, N / 64);
@@ -838,17 +850,18 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
       o.attn = att;
       op_attb = bld.add(o, {op_atto_dx});
     }
-    // QKV: da1 = dqkv . Wqkv ; dWqkv = dqkv^T . ln1 ; dbqkv = colsum(dqkv)
+    // QKV: da1 = dqkv . Wqkv ; dWqkv = dqkv^T . ln1 ; dbqkv = dqkv^T . 1
     if ((rc = gemm_op(h, &o, N, C, 3 * C, {ACT(Lo.dqkv[l]), 3 * C, false}, {W(id.w_qkv), C, true}, EPI_F32, 1)))
       return rc;
     o.gemm.out = F32(Lo.da1[l]); o.gemm.ldo = C;
     const int op_qkv_dx = bld.add(o, {op_attb, op_attb2});
-    if ((rc = gemm_op(h, &o, 3 * C, C, N, {ACT(Lo.dqkv[l]), 3 * C, true}, {ACT(Lo.ln1[l]), C, true}, EPI_F32, 1)))
+    // [dWqkv | dbqkv] = dqkv^T . [ln1 | 1]
+    if ((rc = gemm_op(h, &o, 3 * C, LDC, N, {ACT(Lo.dqkv[l]), 3 * C, true}, {ACT(Lo.ln1[l]), LDC, true}, EPI_F32,
+                      1)))
       return rc;
-    o.gemm.out = G(id.w_qkv); o.gemm.ldo = C;
+    o.gemm.out = G(id.w_qkv); o.gemm.ldo = C; o.gemm.n_real = C; o.gemm.bias_grad = G(id.b_qkv);
     const int op_qkv_dw = bld.add(o, {op_attb, op_attb2});
-    if (id.b_qkv >= 0)
-      adam(id.b_qkv, {colsum(ACT(Lo.dqkv[l]), false, 3 * C, N, 3 * C, G(id.b_qkv), op_attb, op_attb2)});
+    if (id.b_qkv >= 0) adam(id.b_qkv, {op_qkv_dw});
     adam(id.w_qkv, {op_qkv_dw, op_qkv_dx});
     // LN1 backward: dx_l = dxm + LN1'(da1)
     o = blank(OP_LN_BWD, nrb);
@@ -895,6 +908,33 @@ size_t smem_needed(const gpt* h) {
   s = std::max(s, (size_t)kAdamStages * kAdamStageBytes);          // AdamW staging
   if (is_bf16(h->cfg)) s = std::max(s, (size_t)kTcSmemBytes + 4 * kEpiStageBytes);
   return s + 1024;  // 1024-byte alignment slack
+}
+
+// Writes the 64-column pad of every activation a weight-gradient GEMM reads as
+// its second operand: column 0 of the pad = 1 (so the GEMM also produces the
+// bias gradient), the rest 0.  Nothing else writes these columns.
+int init_bias_pads(gpt* h, const Layout& Lo) {
+  const Dims& D = h->D;
+  if (Lo.ldc == (size_t)D.C) return GPT_OK;
+  const bool bf = is_bf16(h->cfg);
+  const size_t es = bf ? 2 : 4, padc = 64;
+  std::vector<uint8_t> pad(D.N * padc * es, 0);
+  for (int r = 0; r < D.N; ++r) {
+    if (bf) { const uint16_t one = 0x3F80; std::memcpy(&pad[(size_t)r * padc * es], &one, 2); }
+    else { const float one = 1.0f; std::memcpy(&pad[(size_t)r * padc * es], &one, 4); }
+  }
+  auto put = [&](size_t off, size_t width, size_t ld) {
+    return cudaMemcpy2DAsync(h->arena + off + width * es, ld * es, pad.data(), padc * es, padc * es, D.N,
+                             cudaMemcpyHostToDevice, h->stream);
+  };
+  for (int l = 0; l < D.L; ++l) {
+    CUDA_TRY(h, put(Lo.ln1[l], D.C, Lo.ldc));
+    CUDA_TRY(h, put(Lo.ln2[l], D.C, Lo.ldc));
+    CUDA_TRY(h, put(Lo.atto[l], D.C, Lo.ldc));
+    CUDA_TRY(h, put(Lo.gact[l], D.F, Lo.ldf));
+  }
+  CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  return GPT_OK;
 }
 
 int fill_shadow_and_upload(gpt* h, const float* host_params) {
@@ -1126,6 +1166,7 @@ int gpt_create(const gpt_config* cfg, uint64_t seed, void* cuda_stream, void* ar
     rc = fill_shadow_and_upload(h, hp.data());
     if (rc != GPT_OK) return bail(rc);
   }
+  if (init_bias_pads(h, Lo) != GPT_OK) return bail(GPT_ERR_CUDA);
   CREATE_TRY(cudaMemsetAsync(h->grads, 0, h->nparams * 4, h->stream));
   CREATE_TRY(cudaMemsetAsync(h->m, 0, h->nparams * 4, h->stream));
   CREATE_TRY(cudaMemsetAsync(h->v, 0, h->nparams * 4, h->stream));
@@ -1390,7 +1431,8 @@ int gpt_test_attention(int32_t dtype, int32_t B, int32_t T, int32_t H, int32_t d
   cudaDeviceGetAttribute(&h.num_sms, cudaDevAttrMultiProcessorCount, h.device);
   h.D = Dims{1, H * d, H, d, 64, 64, T, B, B * T};
   const int qblock = T <= 512 ? 64 : 32;
-  const AttnArgs att{qkv, o, lse, dout, dqkv, scratch, B, T, H, d, H * d, qblock, 1.0f / std::sqrt((float)d)};
+  const AttnArgs att{qkv, o, lse, dout, dqkv, scratch, B, T, H, d, H * d, qblock, 1.0f / std::sqrt((float)d),
+                     H * d};
   Builder bld{&h};
   OpDesc op = blank(OP_ATTN_FWD, dtype == GPT_DTYPE_BF16 ? B * H * (T / 128) : B * H * ((T + qblock - 1) / qblock));
   op.attn = att;
@@ -1570,6 +1612,10 @@ extern "C" int gpt_train_step_static(const gpt_config* cfg, float* params, float
   if (rc != GPT_OK) { g_create_error = h.err; return rc; }
   Bump mb;
   mb.off = Lo.total;
+  if (mb.off <= kStaticScratchBytes && init_bias_pads(&h, Lo) != GPT_OK) {
+    g_create_error = h.err;
+    return GPT_ERR_CUDA;
+  }
   const size_t o_tasks = mb.take(h.tasks.size() * sizeof(TaskDesc));
   const size_t o_ops = mb.take(h.ops.size() * sizeof(OpDesc));
   const size_t o_ctr = mb.take((size_t)h.n_counters * sizeof(unsigned long long));

@@ -81,6 +81,12 @@ struct GemmArgs {
   const float* bias;         // [N] or null
   const float* resid; int64_t ldr;
   const void* aux; int64_t ldaux;
+  // weight gradient with the bias gradient folded in (EPI_F32): columns
+  // n >= n_real come from a padded operand whose column n_real is all ones, so
+  // column n_real of the product is the bias gradient, written to bias_grad[m];
+  // the other padded columns are dropped.  n_real = N when there is none.
+  int32_t n_real;
+  float* bias_grad;
 };
 
 struct LnFwdArgs {
@@ -88,6 +94,7 @@ struct LnFwdArgs {
   void* y; float* mean; float* rstd;
   int32_t rows, C, rows_per_task;
   float eps;
+  int32_t ldy;      // row pitch of y (>= C)
 };
 
 struct LnBwdArgs {
@@ -108,6 +115,7 @@ struct AttnArgs {
   float* scratch;   // SIMT backward: dK/dV accumulators; tensor-core path: D [B, H, T]
   int32_t B, T, H, d, C, q_block;
   float scale;
+  int32_t ld_o;     // row pitch of o (>= C)
 };
 
 struct CeArgs {

@@ -56,7 +56,7 @@ __device__ __forceinline__ void ln_fwd_rows(const LnFwdArgs& a, int r0, int r1) 
   const float invC = 1.0f / (float)a.C;
   for (int r = r0 + warp; r < r1; r += kWarps) {
     const float* x = a.x + (int64_t)r * a.C;
-    act_t* yr = y + (int64_t)r * a.C;
+    act_t* yr = y + (int64_t)r * a.ldy;
     float mean, rstd;
     if constexpr (NV > 0) {
       float4 v[NV];

@@ -35,6 +35,10 @@ __device__ __forceinline__ void epilogue_one(const GemmArgs& g, int split, int m
       reinterpret_cast<act_t*>(g.out2)[(int64_t)m * g.ldo2 + n] = from_f<act_t>(gelu_f(acc, gelu_tanh));
     } break;
     case EPI_F32: {
+      if (n >= g.n_real) {  // padded columns: the first one is the bias gradient
+        if (n == g.n_real && g.bias_grad) g.bias_grad[m] = acc;
+        break;
+      }
       reinterpret_cast<float*>(g.out)[split * g.split_stride + (int64_t)m * g.ldo + n] = acc;
     } break;
     case EPI_GELU_BWD: {
@@ -174,7 +178,7 @@ __device__ inline void task_attn_fwd_simt(const AttnArgs& a, int idx, float* sme
     const int i = e / d, c = e % d;
     float acc = 0.f;
     for (int j = 0; j <= q0 + i; ++j) acc = fmaf(S[i * a.T + j], qkv_at<act_t>(a, b, j, 2, h, c), acc);
-    O[((int64_t)b * a.T + q0 + i) * a.C + h * d + c] = from_f<act_t>(acc);
+    O[((int64_t)b * a.T + q0 + i) * a.ld_o + h * d + c] = from_f<act_t>(acc);
   }
 }
 
@@ -213,7 +217,7 @@ __device__ inline void task_attn_bwd_simt(const AttnArgs& a, int idx, float* sme
       float s = 0.f;
       for (int c = lane; c < d; c += 32)
         s += to_f<act_t>(dO[((int64_t)b * T + q0 + i) * a.C + h * d + c]) *
-             to_f<act_t>(Oa[((int64_t)b * T + q0 + i) * a.C + h * d + c]);
+             to_f<act_t>(Oa[((int64_t)b * T + q0 + i) * a.ld_o + h * d + c]);
       s = warp_sum(s);
       if (lane == 0) Ds[i] = s;
     }

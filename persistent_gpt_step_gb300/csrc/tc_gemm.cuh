@@ -200,7 +200,7 @@ static __device__ __noinline__ void epi_tile(const int M, const int N, const int
                                              const uint32_t tbase, uint8_t* stage, void* const out,
                                              const int64_t ldo, void* const out2, const int64_t ldo2,
                                              const float* const bias, const void* const src, const int64_t lds,
-                                             const bool gelu_tanh) {
+                                             const bool gelu_tanh, const int n_real, float* const bias_grad) {
   const int lane = threadIdx.x & 31;
   const int cu = 4 * (lane & 15);  // this thread's first column within the group
   const int ru = lane >> 4;        // row parity
@@ -249,7 +249,11 @@ static __device__ __noinline__ void epi_tile(const int M, const int N, const int
         *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (int64_t)m * ldo + col) =
             make_float4(rr.x + v.x, rr.y + v.y, rr.z + v.z, rr.w + v.w);
       } else if constexpr (EPI == EPI_F32) {
-        *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (int64_t)m * ldo + col) = v;
+        if (n >= n_real) {  // the padded group: its first column is the bias gradient
+          if (n == n_real && cu == 0 && bias_grad) bias_grad[m] = v.x;
+        } else {
+          *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (int64_t)m * ldo + col) = v;
+        }
       } else if constexpr (EPI == EPI_GELU_BWD) {
         const uint2 hv = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(src) +
                                                          (int64_t)m * lds + col);
@@ -269,24 +273,24 @@ __device__ __forceinline__ void epilogue_tile(const GemmArgs& g, int split, int 
   switch (g.epi) {
     case EPI_STORE:
       epi_tile<EPI_STORE>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, g.bias, nullptr, 0,
-                          gelu_tanh);
+                          gelu_tanh, g.N, nullptr);
       break;
     case EPI_RESID:
       epi_tile<EPI_RESID>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, g.bias, g.resid, g.ldr,
-                          gelu_tanh);
+                          gelu_tanh, g.N, nullptr);
       break;
     case EPI_GELU:
       epi_tile<EPI_GELU>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, g.out2, g.ldo2, g.bias, nullptr, 0,
-                         gelu_tanh);
+                         gelu_tanh, g.N, nullptr);
       break;
     case EPI_F32:
       epi_tile<EPI_F32>(g.M, g.N, g.BN, row0, n0, tbase, stage,
                         reinterpret_cast<float*>(g.out) + split * g.split_stride, g.ldo, nullptr, 0, nullptr,
-                        nullptr, 0, gelu_tanh);
+                        nullptr, 0, gelu_tanh, g.n_real, g.bias_grad);
       break;
     case EPI_GELU_BWD:
       epi_tile<EPI_GELU_BWD>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, nullptr, g.aux,
-                             g.ldaux, gelu_tanh);
+                             g.ldaux, gelu_tanh, g.N, nullptr);
       break;
   }
 }

@@ -43,20 +43,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait on an mbarrier phase; on expiry records a fatal error.
-__device__ __forceinline__ bool mbar_wait(const KParams& kp, uint32_t bar, uint32_t parity) {
+// Bounded wait on an mbarrier phase; on expiry records a fatal error in err
+// (the KParams error words: [0] code, [2] task, [3] counter).
+__device__ __forceinline__ bool mbar_wait_e(uint32_t* err, uint64_t timeout_ns, uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  const uint64_t max_iters = kp.timeout_ns / 20 + 1024;
+  const uint64_t max_iters = timeout_ns / 20 + 1024;
   for (uint64_t it = 0; it < max_iters; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63) == 63) {
-      if (ld_volatile_u32(&kp.err[0]) != 0u) return false;
-      if (globaltimer_ns() - t0 > kp.timeout_ns) break;
+      if (ld_volatile_u32(&err[0]) != 0u) return false;
+      if (globaltimer_ns() - t0 > timeout_ns) break;
     }
   }
-  set_fatal(kp, kFatalMbarTimeout, 0xffffffffu, bar);
+  if (atomicCAS(&err[0], 0u, kFatalMbarTimeout) == 0u) {
+    err[2] = 0xffffffffu;
+    err[3] = bar;
+  }
   return false;
+}
+__device__ __forceinline__ bool mbar_wait(const KParams& kp, uint32_t bar, uint32_t parity) {
+  return mbar_wait_e(kp.err, kp.timeout_ns, bar, parity);
 }
 
 // ---- TMA -------------------------------------------------------------------------
@@ -181,58 +188,93 @@ __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float* v
   reinterpret_cast<uint4*>(dst)[1] = u1;
 }
 
-// One epilogue warp's part of a finished tile: TMEM lane quarter (32 rows from
-// row0), all BN columns, in 64-column groups.  The accumulators go TMEM ->
-// registers -> a per-warp 32 x 64 fp32 staging tile in shared memory (16-byte
-// chunks XOR-swizzled by row) -> back to registers in a row-contiguous layout:
-// thread u owns columns 4 (u mod 16) .. +3 of rows 2i + u / 16, so bias,
-// residual, GELU and the stores touch whole 256-byte row segments.
-struct EpiPtrs {
-  void* out; int64_t ldo;      // EPI_F32: already offset to the split's partial
-  void* out2; int64_t ldo2;
-  const float* bias;
-  const float* resid; int64_t ldr;
-  const __nv_bfloat16* aux; int64_t ldaux;
+// One epilogue warp's part of a tile: TMEM lane quarter (32 rows from row0),
+// all BN columns, in 32-column groups.  The accumulators go TMEM -> registers
+// -> a per-warp 32 x 32 fp32 staging tile in shared memory (16-byte chunks
+// XOR-swizzled by row) -> back to registers in a row-contiguous layout: thread
+// u owns columns 4 (u mod 8) .. +3 of rows 4i + u / 8, so bias, residual,
+// GELU and the stores touch whole 64- or 128-byte row segments.
+//
+// An epilogue that reads a second operand (the residual stream, the GELU
+// pre-activation) issues all 8 of a group's loads at once: the first group's
+// before waiting for the accumulator (they land while the MMAs still run), each
+// next group's before the current one is processed, so a tile pays about one
+// memory latency instead of one per few rows.  Returns false when the wait for
+// the accumulator (acc_bar, parity) timed out or another block failed.
+template <int EPI>
+struct EpiSrc {
+  using T = uint2;  // EPI_GELU_BWD: four bf16 pre-activations
+};
+template <>
+struct EpiSrc<EPI_RESID> {
+  using T = float4;  // four fp32 residual-stream values
 };
 
 template <int EPI>
-static __device__ __noinline__ void epi_tile(const int M, const int N, const int BN, const int row0, const int n0,
+__device__ __forceinline__ void epi_load_src(typename EpiSrc<EPI>::T* dst, const void* src, int64_t lds, int M,
+                                             int r0, int col) {
+  using T = typename EpiSrc<EPI>::T;
+  const T* p = reinterpret_cast<const T*>(reinterpret_cast<const char*>(src) +
+                                          ((int64_t)r0 * lds + col) * (EPI == EPI_RESID ? 4 : 2));
+  const int64_t step = 4 * lds * (EPI == EPI_RESID ? 4 : 2) / (int64_t)sizeof(T);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (r0 + 4 * i < M) dst[i] = p[i * step];
+}
+
+template <int EPI>
+static __device__ __noinline__ bool epi_tile(const int M, const int N, const int BN, const int row0, const int n0,
                                              const uint32_t tbase, uint8_t* stage, void* const out,
                                              const int64_t ldo, void* const out2, const int64_t ldo2,
                                              const float* const bias, const void* const src, const int64_t lds,
-                                             const bool gelu_tanh, const int n_real, float* const bias_grad) {
+                                             const bool gelu_tanh, const int n_real, float* const bias_grad,
+                                             const uint32_t acc_bar, const uint32_t acc_parity, uint32_t* const err,
+                                             const uint64_t timeout_ns) {
+  constexpr bool kSrc = EPI == EPI_RESID || EPI == EPI_GELU_BWD;
+  using SrcT = typename EpiSrc<EPI>::T;
   const int lane = threadIdx.x & 31;
-  const int cu = 4 * (lane & 15);  // this thread's first column within the group
-  const int ru = lane >> 4;        // row parity
-  for (int c = 0; c < BN; c += 64) {  // N is a multiple of 64: groups are all in or all out
+  const int cu = 4 * (lane & 7);     // this thread's first column within the group
+  const int rq = lane >> 3;          // first row (of 4)
+  const int r0 = row0 + rq;
+  const int cend = min(BN, N - n0);  // N is a multiple of 64
+  SrcT nxt[kSrc ? 8 : 1];
+  if constexpr (kSrc) epi_load_src<EPI>(nxt, src, lds, M, r0, n0 + cu);
+  if (!mbar_wait_e(err, timeout_ns, acc_bar, acc_parity)) return false;
+  tc_fence_after();
+  for (int c = 0; c < cend; c += 32) {
     const int n = n0 + c;
-    if (n >= N) break;
     {
-      uint32_t r[4][16];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) tmem_ld16_issue(tbase + (uint32_t)(c + 16 * j), r[j]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) tmem_ld_wait16(r[j]);
+      uint32_t r[2][16];
+      tmem_ld16_issue(tbase + (uint32_t)c, r[0]);
+      tmem_ld16_issue(tbase + (uint32_t)(c + 16), r[1]);
+      tmem_ld_wait16(r[0]);
+      tmem_ld_wait16(r[1]);
       __syncwarp();
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
+      for (int j = 0; j < 2; ++j)
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           const int ch = 4 * j + h;  // 16-byte chunk of this thread's row
-          *reinterpret_cast<uint4*>(stage + lane * 256 + ((ch ^ (lane & 15)) << 4)) =
+          *reinterpret_cast<uint4*>(stage + lane * 128 + ((ch ^ (lane & 7)) << 4)) =
               make_uint4(r[j][4 * h], r[j][4 * h + 1], r[j][4 * h + 2], r[j][4 * h + 3]);
         }
       __syncwarp();
     }
+    SrcT cur[kSrc ? 8 : 1];
+    if constexpr (kSrc) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
+      if (c + 32 < cend) epi_load_src<EPI>(nxt, src, lds, M, r0, n + 32 + cu);
+    }
     const int col = n + cu;
     float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
     if (EPI != EPI_F32 && EPI != EPI_GELU_BWD && bias) b = *reinterpret_cast<const float4*>(bias + col);
-#pragma unroll 4
-    for (int i = 0; i < 16; ++i) {
-      const int rl = ru + 2 * i;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rl = rq + 4 * i;
       const int m = row0 + rl;
       if (m >= M) break;  // rows ascend with i
-      float4 v = *reinterpret_cast<const float4*>(stage + rl * 256 + (((lane & 15) ^ (rl & 15)) << 4));
+      float4 v = *reinterpret_cast<const float4*>(stage + rl * 128 + (((lane & 7) ^ (rl & 7)) << 4));
       v.x += b.x; v.y += b.y; v.z += b.z; v.w += b.w;
       if constexpr (EPI == EPI_STORE || EPI == EPI_GELU) {
         __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
@@ -245,18 +287,17 @@ static __device__ __noinline__ void epi_tile(const int M, const int N, const int
               make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
         }
       } else if constexpr (EPI == EPI_RESID) {
-        const float4 rr = *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(src) + (int64_t)m * lds + col);
+        const float4 rr = cur[i];
         *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (int64_t)m * ldo + col) =
             make_float4(rr.x + v.x, rr.y + v.y, rr.z + v.z, rr.w + v.w);
       } else if constexpr (EPI == EPI_F32) {
-        if (n >= n_real) {  // the padded group: its first column is the bias gradient
+        if (n >= n_real) {  // the padded columns: the first is the bias gradient
           if (n == n_real && cu == 0 && bias_grad) bias_grad[m] = v.x;
         } else {
           *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (int64_t)m * ldo + col) = v;
         }
       } else if constexpr (EPI == EPI_GELU_BWD) {
-        const uint2 hv = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(src) +
-                                                         (int64_t)m * lds + col);
+        const uint2 hv = cur[i];
         const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hv.x));
         const float2 e = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hv.y));
         __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * gelu_grad_bf(a.x, gelu_tanh), v.y * gelu_grad_bf(a.y, gelu_tanh));
@@ -266,32 +307,31 @@ static __device__ __noinline__ void epi_tile(const int M, const int N, const int
       }
     }
   }
+  return true;
 }
 
-__device__ __forceinline__ void epilogue_tile(const GemmArgs& g, int split, int row0, int n0, uint32_t tbase,
-                                              uint8_t* stage, bool gelu_tanh) {
+// Waits for the tile's accumulator and runs its epilogue (false: the wait failed).
+__device__ __forceinline__ bool epilogue_tile(const KParams& kp, const GemmArgs& g, int split, int row0, int n0,
+                                              uint32_t tbase, uint8_t* stage, bool gelu_tanh, uint32_t acc_bar,
+                                              uint32_t acc_parity) {
   switch (g.epi) {
     case EPI_STORE:
-      epi_tile<EPI_STORE>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, g.bias, nullptr, 0,
-                          gelu_tanh, g.N, nullptr);
-      break;
+      return epi_tile<EPI_STORE>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, g.bias, nullptr,
+                                 0, gelu_tanh, g.N, nullptr, acc_bar, acc_parity, kp.err, kp.timeout_ns);
     case EPI_RESID:
-      epi_tile<EPI_RESID>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, g.bias, g.resid, g.ldr,
-                          gelu_tanh, g.N, nullptr);
-      break;
+      return epi_tile<EPI_RESID>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, g.bias, g.resid,
+                                 g.ldr, gelu_tanh, g.N, nullptr, acc_bar, acc_parity, kp.err, kp.timeout_ns);
     case EPI_GELU:
-      epi_tile<EPI_GELU>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, g.out2, g.ldo2, g.bias, nullptr, 0,
-                         gelu_tanh, g.N, nullptr);
-      break;
+      return epi_tile<EPI_GELU>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, g.out2, g.ldo2, g.bias,
+                                nullptr, 0, gelu_tanh, g.N, nullptr, acc_bar, acc_parity, kp.err, kp.timeout_ns);
     case EPI_F32:
-      epi_tile<EPI_F32>(g.M, g.N, g.BN, row0, n0, tbase, stage,
-                        reinterpret_cast<float*>(g.out) + split * g.split_stride, g.ldo, nullptr, 0, nullptr,
-                        nullptr, 0, gelu_tanh, g.n_real, g.bias_grad);
-      break;
-    case EPI_GELU_BWD:
-      epi_tile<EPI_GELU_BWD>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, nullptr, g.aux,
-                             g.ldaux, gelu_tanh, g.N, nullptr);
-      break;
+      return epi_tile<EPI_F32>(g.M, g.N, g.BN, row0, n0, tbase, stage,
+                               reinterpret_cast<float*>(g.out) + split * g.split_stride, g.ldo, nullptr, 0, nullptr,
+                               nullptr, 0, gelu_tanh, g.n_real, g.bias_grad, acc_bar, acc_parity, kp.err,
+                               kp.timeout_ns);
+    default:
+      return epi_tile<EPI_GELU_BWD>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, nullptr, g.aux,
+                                    g.ldaux, gelu_tanh, g.N, nullptr, acc_bar, acc_parity, kp.err, kp.timeout_ns);
   }
 }
 
@@ -481,14 +521,13 @@ __device__ inline int64_t gemm_run(const KParams& kp, int64_t t_first, GemmShare
         break;
       }
       const uint32_t buf = i & 1;
-      const bool ok = mbar_wait(kp, acc_full0 + 8 * buf, (i >> 1) & 1);
-      tc_fence_after();
       const GemmArgs g = kp.ops[kp.tasks[t].op].gemm;
       int tm, tn, split;
       gemm_coords(g, kp.tasks[t].idx, tm, tn, split);
-      if (ok)
-        epilogue_tile(g, split, tm * kTcBM + q * 32, tn * g.BN, tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256,
-                      smem_tiles + kTcSmemBytes + (warp - 4) * kEpiStageBytes, gelu_tanh);
+      const bool ok = epilogue_tile(kp, g, split, tm * kTcBM + q * 32, tn * g.BN,
+                                    tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256,
+                                    smem_tiles + kTcSmemBytes + (warp - 4) * kEpiStageBytes, gelu_tanh,
+                                    acc_full0 + 8 * buf, (i >> 1) & 1);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty0 + 8 * buf);

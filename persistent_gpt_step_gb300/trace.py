@@ -50,6 +50,7 @@ def main():
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--json", default=None)
     ap.add_argument("--ops", action="store_true", help="print every op's first start / last end")
+    ap.add_argument("--save", default=None, help="write the raw trace and the task graph to this .npz")
     args = ap.parse_args()
     import torch
 
@@ -68,6 +69,15 @@ def main():
             m.train_step(torch.from_numpy(tok).cuda(), torch.from_numpy(tgt).cuda())
         tr = m.trace()
         kms = m.last_kernel_ms()
+    if args.save:
+        waits = np.full((len(tasks), 3, 3), -1, dtype=np.int64)
+        for i, t in enumerate(tasks):
+            for w, (first, count, need) in enumerate(t[3]):
+                waits[i, w] = (first, count, need)
+        np.savez_compressed(args.save, trace=tr, task_ops=task_ops, task_idx=np.array([t[1] for t in tasks]),
+                            task_sig=np.array([t[2] for t in tasks]), task_sig2=np.array([t[4] for t in tasks]),
+                            task_waits=waits, op_types=np.asarray(op_types), op_dims=np.asarray(op_dims),
+                            grid=grid, kernel_ms=kms)
     rows, total = family_table(tr, task_ops, op_types, grid)
     print(f"config {args.config}: {n} tasks, grid {grid}, kernel {kms:.3f} ms, traced span {total:.3f} ms")
     print(f"{'family':20s} {'tasks':>7s} {'busy ms':>9s} {'wait ms':>9s} {'span ms':>9s} {'first':>8s} {'last':>8s}")

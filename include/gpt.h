@@ -195,9 +195,17 @@ int gpt_graph_info(const gpt* h, int64_t* n_tasks, int32_t* grid, int32_t* block
  * time goes").  gpt_trace_enable(h, 1) allocates a device buffer of 32 bytes
  * per task; every later step records, per task (ticket order), four uint64:
  * claim time, start time (after its dependency waits), end time (after its
- * release), all %globaltimer nanoseconds, and the SM id that ran it.
- * gpt_get_trace copies the last step's record to HOST dst[0..4*n_tasks).
- * gpt_trace_enable(h, 0) frees the buffer.
+ * release), all %globaltimer nanoseconds, and the SM id (low 32 bits) and
+ * block index (high 32 bits) that ran it.
+ * gpt_get_trace copies the last step's record to HOST dst[0..4*n_tasks); with
+ * n = 4*n_tasks + 8*grid it also copies, per block, the last wait each GEMM
+ * role entered (scheduler, TMA producer, MMA issuer, four epilogue warps) as
+ * kind << 56 | (run-local task count mod 2^24) << 32 | task, and an eighth word
+ * holding the block's number of GEMM runs << 32 | the last run's first task; the
+ * kinds numbered 1..11 as: scheduler dependency wait, scheduler queue-slot
+ * wait, producer queue wait, producer stage wait, MMA queue wait, MMA
+ * accumulator wait, MMA stage wait, epilogue queue wait, epilogue tile,
+ * epilogue group sync, role finished.  gpt_trace_enable(h, 0) frees the buffer.
  */
 int gpt_trace_enable(gpt* h, int32_t on);
 int gpt_get_trace(gpt* h, uint64_t* dst, size_t n);

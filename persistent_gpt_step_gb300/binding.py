@@ -277,6 +277,13 @@ class GPT:
         self._check(self._lib.gpt_get_trace(self._h, c_void_p(out.ctypes.data), out.size))
         return out
 
+    def role_states(self) -> np.ndarray:
+        """uint64 [grid, 8]: the last wait each GEMM role entered in the last step."""
+        n, grid, _ = self.graph_info()
+        out = np.empty(4 * n + 8 * grid, np.uint64)
+        self._check(self._lib.gpt_get_trace(self._h, c_void_p(out.ctypes.data), out.size))
+        return out[4 * n:].reshape(grid, 8)
+
     def last_kernel_ms(self) -> float:
         ms = c_float()
         self._check(self._lib.gpt_last_kernel_ms(self._h, byref(ms)))

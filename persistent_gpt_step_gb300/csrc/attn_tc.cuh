@@ -224,30 +224,57 @@ __device__ inline void task_attn_fwd_tc(const AttnArgs& a, int idx, uint8_t* sme
 
 // ---- backward pre-pass: D = rowsum(dO * O) per (row, head) --------------------
 __device__ inline void task_attn_bwd_pre(const AttnArgs& a, int idx) {
+  // D[b, h, t] = sum_d dO[t, h d] O[t, h d]: 8 lanes per head (8 elements each),
+  // four heads per warp-wide pass.  A warp loads two rows' dO and O (every
+  // head) before reducing either, so its eight rows cost four memory latencies
+  // instead of one per row and head group.  Heads beyond 16 take a second round.
+  constexpr int kRG = 2, kHG = 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.B * a.T;
   const int r0 = idx * kAttSub, r1 = min(r0 + kAttSub, N);
-  const int sub = lane & 7;          // 8 lanes per head, 8 elements each
+  const int sub = lane & 7;
   const __nv_bfloat16* dO = reinterpret_cast<const __nv_bfloat16*>(a.dout);
   const __nv_bfloat16* O = reinterpret_cast<const __nv_bfloat16*>(a.o);
-  for (int r = r0 + warp; r < r1; r += kWarps) {
-    const int b = r / a.T, t = r % a.T;
-    for (int h0 = 0; h0 < a.H; h0 += 4) {
-      const int h = h0 + (lane >> 3);
-      float s = 0.f;
-      if (h < a.H) {
-        const uint4 u = *reinterpret_cast<const uint4*>(dO + (int64_t)r * a.C + h * 64 + sub * 8);
-        const uint4 v = *reinterpret_cast<const uint4*>(O + (int64_t)r * a.ld_o + h * 64 + sub * 8);
-        float fu[8], fv[8];
-        bf16x8_to_f(u, fu);
-        bf16x8_to_f(v, fv);
+  for (int rb = r0 + warp; rb < r1; rb += kRG * kWarps) {
+    for (int hb = 0; hb < a.H; hb += 4 * kHG) {
+      uint4 u[kRG][kHG], v[kRG][kHG];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) s += fu[e] * fv[e];
+      for (int i = 0; i < kRG; ++i) {
+        const int r = rb + i * kWarps;
+#pragma unroll
+        for (int j = 0; j < kHG; ++j) {
+          const int h = hb + 4 * j + (lane >> 3);
+          if (r < r1 && h < a.H) {
+            u[i][j] = *reinterpret_cast<const uint4*>(dO + (int64_t)r * a.C + h * 64 + sub * 8);
+            v[i][j] = *reinterpret_cast<const uint4*>(O + (int64_t)r * a.ld_o + h * 64 + sub * 8);
+          } else {
+            u[i][j] = make_uint4(0u, 0u, 0u, 0u);
+            v[i][j] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
       }
-      s += __shfl_xor_sync(0xffffffffu, s, 1);
-      s += __shfl_xor_sync(0xffffffffu, s, 2);
-      s += __shfl_xor_sync(0xffffffffu, s, 4);
-      if (sub == 0 && h < a.H) a.scratch[((int64_t)b * a.H + h) * a.T + t] = s;
+#pragma unroll
+      for (int i = 0; i < kRG; ++i) {
+        const int r = rb + i * kWarps;
+#pragma unroll
+        for (int j = 0; j < kHG; ++j) {
+          const int h = hb + 4 * j + (lane >> 3);
+          if (hb + 4 * j >= a.H) break;  // warp-uniform
+          float fu[8], fv[8];
+          bf16x8_to_f(u[i][j], fu);
+          bf16x8_to_f(v[i][j], fv);
+          float s = 0.f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) s += fu[e] * fv[e];
+          s += __shfl_xor_sync(0xffffffffu, s, 1);
+          s += __shfl_xor_sync(0xffffffffu, s, 2);
+          s += __shfl_xor_sync(0xffffffffu, s, 4);
+          if (sub == 0 && h < a.H && r < r1) {
+            const int b = r / a.T, t = r % a.T;
+            a.scratch[((int64_t)b * a.H + h) * a.T + t] = s;
+          }
+        }
+      }
     }
   }
 }

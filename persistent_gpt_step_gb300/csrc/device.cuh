@@ -36,6 +36,13 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Block-wide barrier in its non-aligned PTX form, for the end of a GEMM run,
+// where lane 0 of warps 0-2 leaves a long single-thread role loop while the
+// other lanes have long arrived: the non-aligned form counts every thread on
+// its own and does not rely on the warp having reconverged.  Everywhere else
+// the aligned __syncthreads() is used (it keeps more registers free).
+__device__ __forceinline__ void cta_sync() { asm volatile("barrier.sync 0;" ::: "memory"); }
+
 __device__ __forceinline__ void set_fatal(const KParams& kp, uint32_t code, uint32_t task,
                                           uint32_t ctr) {
   if (atomicCAS(&kp.err[0], 0u, code) == 0u) {

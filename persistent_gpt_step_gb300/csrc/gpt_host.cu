@@ -256,7 +256,14 @@ struct Layout {
 };
 
 constexpr int kRowsLn = 32;       // rows per LayerNorm task
-constexpr int kRowsCe = 8;        // rows per cross-entropy task
+constexpr int kRowsCe = 4;        // rows per cross-entropy task
+
+// The bf16 cross-entropy stages two whole rows of logits in shared memory when
+// they fit beside the GEMM pipeline's footprint (it reuses that space).
+bool ce_staged(const gpt_config& c) {
+  const size_t row = ((size_t)c.vocab * 2 + 127) & ~(size_t)127;
+  return c.dtype == GPT_DTYPE_BF16 && c.vocab % 8 == 0 && 2 * row + 64 <= (size_t)kTcSmemBytes + 4 * kEpiStageBytes;
+}
 constexpr int kRowsEmb = 32;      // rows per embedding task
 constexpr int kVocabRows = 64;    // vocabulary rows per embedding-backward task
 constexpr int kColsColsum = 64;   // columns per column-sum task
@@ -735,7 +742,7 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
   o.gemm.out = ACT(Lo.logits); o.gemm.ldo = V;
   const int op_lm = bld.add(o, {op_lnf});
   o = blank(OP_CE, (N + kRowsCe - 1) / kRowsCe);
-  o.ce = CeArgs{ACT(Lo.logits), F32(Lo.row_loss), N, V, kRowsCe};
+  o.ce = CeArgs{ACT(Lo.logits), F32(Lo.row_loss), N, V, kRowsCe, ce_staged(c) ? 1 : 0};
   const int op_ce = bld.add(o, {op_lm});
   o = blank(OP_LOSS, 1);
   o.loss = LossArgs{F32(Lo.row_loss), F32(Lo.loss), N};
@@ -1273,7 +1280,7 @@ int gpt_graph_info(const gpt* h, int64_t* n_tasks, int32_t* grid, int32_t* block
 int gpt_trace_enable(gpt* h, int32_t on) {
   if (!h) return GPT_ERR_INVALID_ARG;
   if (on && !h->d_trace) {
-    const size_t bytes = h->tasks.size() * 4 * sizeof(unsigned long long);
+    const size_t bytes = (h->tasks.size() * 4 + (size_t)h->grid * 8) * sizeof(unsigned long long);
     if (cudaMalloc(&h->d_trace, bytes) != cudaSuccess) {
       cudaGetLastError();
       h->d_trace = nullptr;
@@ -1292,7 +1299,8 @@ int gpt_trace_enable(gpt* h, int32_t on) {
 int gpt_get_trace(gpt* h, uint64_t* dst, size_t n) {
   if (!h || !dst) return GPT_ERR_INVALID_ARG;
   if (!h->d_trace) return fail(h, GPT_ERR_INVALID_ARG, "tracing is off (gpt_trace_enable)");
-  if (n != h->tasks.size() * 4) return fail(h, GPT_ERR_INVALID_ARG, "n must be 4 * n_tasks");
+  if (n != h->tasks.size() * 4 && n != h->tasks.size() * 4 + (size_t)h->grid * 8)
+    return fail(h, GPT_ERR_INVALID_ARG, "n must be 4 * n_tasks (+ 8 * grid for the GEMM role states)");
   CUDA_TRY(h, cudaMemcpyAsync(dst, h->d_trace, n * 8, cudaMemcpyDeviceToHost, h->stream));
   CUDA_TRY(h, cudaStreamSynchronize(h->stream));
   return GPT_OK;

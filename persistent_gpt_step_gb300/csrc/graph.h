@@ -122,6 +122,7 @@ struct CeArgs {
   void* logits;              // act [N, V], overwritten by dlogits
   float* row_loss;           // [N]
   int32_t N, V, rows_per_task;
+  int32_t staged;            // bf16: two whole rows fit in shared memory (bulk-copied)
 };
 
 struct LossArgs {

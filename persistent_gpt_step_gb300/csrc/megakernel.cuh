@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
   const int warp = threadIdx.x >> 5;
-  TcState st = {0u, 0u, 0u, 0u, 0u};
+  TcState st = {0u, 0u, 0u, 0u, 0u, 0u, 0u};
   if (blockIdx.x == 0 && threadIdx.x == 0) kp.tickets[(kp.epoch + 1ull) & 1ull] = 0ull;  // next launch's
   if (threadIdx.x == 0) {
     for (int i = 0; i < kAdamStages; ++i) mbar_init(smem_u32(&sh.adam_bars[i]), 1);
@@ -48,9 +48,17 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
         mbar_init(smem_u32(&sh.gemm.stage_full[i]), 1);   // producer arrive + tx bytes
         mbar_init(smem_u32(&sh.gemm.stage_empty[i]), 1);  // one MMA commit
       }
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(smem_u32(&sh.gemm.q_full[i]), 1);     // scheduler publishes a queue entry
+        mbar_init(smem_u32(&sh.gemm.q_empty[i]), 3);    // producer, MMA, epilogue leader took it
+        mbar_init(smem_u32(&sh.gemm.acc_full[i]), 1);   // MMA commit: accumulator complete
+        mbar_init(smem_u32(&sh.gemm.acc_empty[i]), 4);  // each epilogue warp drained it
+      }
+      mbar_init(smem_u32(&sh.gemm.epi_sync), 4);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
+    __syncwarp();  // tcgen05.alloc is warp-aligned
     if (warp == 0) tmem_alloc(smem_u32(&sh.tmem_base), kTmemCols);
     tc_fence_before();
     __syncthreads();
@@ -73,7 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
             asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
             kp.trace[4 * t + 0] = t_claim;
             kp.trace[4 * t + 1] = globaltimer_ns();
-            kp.trace[4 * t + 3] = smid;
+            kp.trace[4 * t + 3] = smid | ((unsigned long long)blockIdx.x << 32);
           }
         }
       }
@@ -81,8 +89,8 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
       sh.ok = ok;
     }
     __syncthreads();
-    const int64_t t = sh.task;
-    if (!sh.ok || t >= kp.ntasks) break;
+    const int64_t t = *reinterpret_cast<volatile int64_t*>(&sh.task);  // read once (thread 0 rewrites it next round)
+    if (!*reinterpret_cast<volatile int32_t*>(&sh.ok) || t >= kp.ntasks) break;
     pending = -1;
     const TaskDesc& d = kp.tasks[t];
     const OpDesc& op = kp.ops[d.op];
@@ -122,7 +130,8 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
         {
           const CeArgs a = op.ce;
           if constexpr (kTC) {
-            if ((a.V & 7) == 0) task_ce_bf16_vec(kp, a, idx);
+            if (a.staged) task_ce_bf16_staged(kp, a, idx, smem, sh.adam_bars, &sh.adam_iter);
+            else if ((a.V & 7) == 0) task_ce_bf16_vec(kp, a, idx);
             else task_ce<act_t>(kp, a, idx);
           } else {
             task_ce<act_t>(kp, a, idx);
@@ -157,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    __syncwarp();
     if (warp == 0) tmem_dealloc(sh.tmem_base, kTmemCols);
   }
 }

@@ -9,6 +9,23 @@
 
 namespace pgs {
 
+// ---- 1-D bulk copies (async proxy) between global and shared memory ----
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+
 // x0[n] = wte[tok[n]] + wpe[n mod T]  (token + learned position embedding).
 template <typename act_t>
 __device__ inline void task_embed(const KParams& kp, const EmbedArgs& a, int idx) {
@@ -54,49 +71,67 @@ __device__ __forceinline__ void ln_fwd_rows(const LnFwdArgs& a, int r0, int r1) 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   act_t* y = reinterpret_cast<act_t*>(a.y);
   const float invC = 1.0f / (float)a.C;
-  for (int r = r0 + warp; r < r1; r += kWarps) {
-    const float* x = a.x + (int64_t)r * a.C;
-    act_t* yr = y + (int64_t)r * a.ldy;
-    float mean, rstd;
-    if constexpr (NV > 0) {
+  if constexpr (NV > 0) {
+    // g and b are the same for every row; the next row's x is loaded while
+    // this one is reduced and written, so a warp waits about once per task.
+    float4 g[NV], bb[NV], nv[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int c = 4 * (lane + 32 * i);
+      g[i] = *reinterpret_cast<const float4*>(a.g + c);
+      bb[i] = a.b ? *reinterpret_cast<const float4*>(a.b + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    int r = r0 + warp;
+    if (r < r1) {
+#pragma unroll
+      for (int i = 0; i < NV; ++i) nv[i] = reinterpret_cast<const float4*>(a.x + (int64_t)r * a.C)[lane + 32 * i];
+    }
+    for (; r < r1; r += kWarps) {
       float4 v[NV];
+#pragma unroll
+      for (int i = 0; i < NV; ++i) v[i] = nv[i];
+      if (r + kWarps < r1) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+          nv[i] = reinterpret_cast<const float4*>(a.x + (int64_t)(r + kWarps) * a.C)[lane + 32 * i];
+      }
       float s = 0.f;
 #pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        v[i] = reinterpret_cast<const float4*>(x)[lane + 32 * i];
-        s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
-      }
-      mean = warp_sum(s) * invC;
+      for (int i = 0; i < NV; ++i) s += (v[i].x + v[i].y) + (v[i].z + v[i].w);
+      const float mean = warp_sum(s) * invC;
       float q = 0.f;
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         const float d0 = v[i].x - mean, d1 = v[i].y - mean, d2 = v[i].z - mean, d3 = v[i].w - mean;
         q += (d0 * d0 + d1 * d1) + (d2 * d2 + d3 * d3);
       }
-      rstd = rsqrtf(warp_sum(q) * invC + a.eps);
+      const float rstd = rsqrtf(warp_sum(q) * invC + a.eps);
+      act_t* yr = y + (int64_t)r * a.ldy;
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         const int c = 4 * (lane + 32 * i);
-        const float4 g = *reinterpret_cast<const float4*>(a.g + c);
-        float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (a.b) b = *reinterpret_cast<const float4*>(a.b + c);
-        store4<act_t>(yr + c, (v[i].x - mean) * rstd * g.x + b.x, (v[i].y - mean) * rstd * g.y + b.y,
-                      (v[i].z - mean) * rstd * g.z + b.z, (v[i].w - mean) * rstd * g.w + b.w);
+        store4<act_t>(yr + c, (v[i].x - mean) * rstd * g[i].x + bb[i].x, (v[i].y - mean) * rstd * g[i].y + bb[i].y,
+                      (v[i].z - mean) * rstd * g[i].z + bb[i].z, (v[i].w - mean) * rstd * g[i].w + bb[i].w);
       }
-    } else {
+      if (lane == 0) { a.mean[r] = mean; a.rstd[r] = rstd; }
+    }
+  } else {
+    for (int r = r0 + warp; r < r1; r += kWarps) {
+      const float* x = a.x + (int64_t)r * a.C;
+      act_t* yr = y + (int64_t)r * a.ldy;
       float s = 0.f;
       for (int c = lane; c < a.C; c += 32) s += x[c];
-      mean = warp_sum(s) * invC;
+      const float mean = warp_sum(s) * invC;
       float q = 0.f;
       for (int c = lane; c < a.C; c += 32) { const float d = x[c] - mean; q += d * d; }
-      rstd = rsqrtf(warp_sum(q) * invC + a.eps);
+      const float rstd = rsqrtf(warp_sum(q) * invC + a.eps);
       for (int c = lane; c < a.C; c += 32) {
         float o = (x[c] - mean) * rstd * a.g[c];
         if (a.b) o += a.b[c];
         yr[c] = from_f<act_t>(o);
       }
+      if (lane == 0) { a.mean[r] = mean; a.rstd[r] = rstd; }
     }
-    if (lane == 0) { a.mean[r] = mean; a.rstd[r] = rstd; }
   }
 }
 
@@ -119,34 +154,66 @@ __device__ inline void task_ln_fwd(const LnFwdArgs& a, int idx) {
 // Warp w adds its rows' dy xhat and dy, in row order, into its own shared-memory
 // rows; the warps' rows are then added in warp order (fixed summation order).
 template <typename act_t, int NV>
+__device__ __forceinline__ void ln_bwd_load(const LnBwdArgs& a, int r, int lane, float4* dy, float4* xv, float4* din,
+                                            float& mean, float& rstd) {
+  mean = a.mean[r];
+  rstd = a.rstd[r];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int64_t c = (int64_t)r * a.C + 4 * (lane + 32 * i);
+    dy[i] = *reinterpret_cast<const float4*>(a.dy + c);
+    xv[i] = *reinterpret_cast<const float4*>(a.x + c);
+    din[i] = a.dres_in ? *reinterpret_cast<const float4*>(a.dres_in + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int sp = 1; sp < a.dy_splits; ++sp) {  // split-K partials of dy (final LayerNorm only)
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const float4 e = *reinterpret_cast<const float4*>(a.dy + sp * a.dy_split_stride + (int64_t)r * a.C +
+                                                        4 * (lane + 32 * i));
+      dy[i].x += e.x; dy[i].y += e.y; dy[i].z += e.z; dy[i].w += e.w;
+    }
+  }
+}
+
+template <typename act_t, int NV>
 __device__ __forceinline__ void ln_bwd_rows(const LnBwdArgs& a, int r0, int r1, float* sg, float* sb) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   act_t* dact = reinterpret_cast<act_t*>(a.dres_act);
   const float invC = 1.0f / (float)a.C;
   float* wg = sg + warp * a.C;
   float* wb = sb + warp * a.C;
-  for (int r = r0 + warp; r < r1; r += kWarps) {
-    const float mean = a.mean[r], rstd = a.rstd[r];
-    const float* x = a.x + (int64_t)r * a.C;
-    float* out = a.dres_out + (int64_t)r * a.C;
-    const float* din = a.dres_in ? a.dres_in + (int64_t)r * a.C : nullptr;
-    act_t* oa = dact + (int64_t)r * a.C;
-    if constexpr (NV > 0) {
-      float4 dy[NV], xh[NV];
+  if constexpr (NV > 0) {
+    // dy, x and the incoming residual gradient of a row are loaded together, and
+    // (for C <= 768, where the registers allow) those of the warp's next row
+    // while this one is reduced and written: about one memory latency per task.
+    constexpr bool kPrefetch = NV <= 6;
+    float4 ndy[NV], nx[NV], ndin[NV];
+    float nmean = 0.f, nrstd = 0.f;
+    int r = r0 + warp;
+    if (kPrefetch && r < r1) ln_bwd_load<act_t, NV>(a, r, lane, ndy, nx, ndin, nmean, nrstd);
+    for (; r < r1; r += kWarps) {
+      float4 dy[NV], xh[NV], din[NV];
+      float mean, rstd;
+      if constexpr (kPrefetch) {
+        mean = nmean;
+        rstd = nrstd;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) { dy[i] = ndy[i]; xh[i] = nx[i]; din[i] = ndin[i]; }
+        if (r + kWarps < r1) ln_bwd_load<act_t, NV>(a, r + kWarps, lane, ndy, nx, ndin, nmean, nrstd);
+      } else {
+        ln_bwd_load<act_t, NV>(a, r, lane, dy, xh, din, mean, rstd);
+      }
+      float4 g[NV];
+#pragma unroll
+      for (int i = 0; i < NV; ++i) g[i] = *reinterpret_cast<const float4*>(a.g + 4 * (lane + 32 * i));
       float s1 = 0.f, s2 = 0.f;
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         const int c = 4 * (lane + 32 * i);
-        float4 d = *reinterpret_cast<const float4*>(a.dy + (int64_t)r * a.C + c);
-        for (int sp = 1; sp < a.dy_splits; ++sp) {
-          const float4 e = *reinterpret_cast<const float4*>(a.dy + sp * a.dy_split_stride + (int64_t)r * a.C + c);
-          d.x += e.x; d.y += e.y; d.z += e.z; d.w += e.w;
-        }
-        const float4 xv = *reinterpret_cast<const float4*>(x + c);
-        const float4 g = *reinterpret_cast<const float4*>(a.g + c);
-        dy[i] = d;
-        xh[i] = make_float4((xv.x - mean) * rstd, (xv.y - mean) * rstd, (xv.z - mean) * rstd, (xv.w - mean) * rstd);
-        const float a0 = d.x * g.x, a1 = d.y * g.y, a2 = d.z * g.z, a3 = d.w * g.w;
+        const float4 d = dy[i];
+        xh[i] = make_float4((xh[i].x - mean) * rstd, (xh[i].y - mean) * rstd, (xh[i].z - mean) * rstd,
+                            (xh[i].w - mean) * rstd);
+        const float a0 = d.x * g[i].x, a1 = d.y * g[i].y, a2 = d.z * g[i].z, a3 = d.w * g[i].w;
         s1 += (a0 + a1) + (a2 + a3);
         s2 += (a0 * xh[i].x + a1 * xh[i].y) + (a2 * xh[i].z + a3 * xh[i].w);
         float4 pg = *reinterpret_cast<float4*>(wg + c);
@@ -158,20 +225,26 @@ __device__ __forceinline__ void ln_bwd_rows(const LnBwdArgs& a, int r0, int r1, 
       }
       s1 = warp_sum(s1) * invC;
       s2 = warp_sum(s2) * invC;
+      float* out = a.dres_out + (int64_t)r * a.C;
+      act_t* oa = dact + (int64_t)r * a.C;
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         const int c = 4 * (lane + 32 * i);
-        const float4 g = *reinterpret_cast<const float4*>(a.g + c);
-        float4 o = make_float4(rstd * (dy[i].x * g.x - s1 - xh[i].x * s2), rstd * (dy[i].y * g.y - s1 - xh[i].y * s2),
-                               rstd * (dy[i].z * g.z - s1 - xh[i].z * s2), rstd * (dy[i].w * g.w - s1 - xh[i].w * s2));
-        if (din) {
-          const float4 e = *reinterpret_cast<const float4*>(din + c);
-          o.x += e.x; o.y += e.y; o.z += e.z; o.w += e.w;
-        }
+        const float4 o = make_float4(rstd * (dy[i].x * g[i].x - s1 - xh[i].x * s2) + din[i].x,
+                                     rstd * (dy[i].y * g[i].y - s1 - xh[i].y * s2) + din[i].y,
+                                     rstd * (dy[i].z * g[i].z - s1 - xh[i].z * s2) + din[i].z,
+                                     rstd * (dy[i].w * g[i].w - s1 - xh[i].w * s2) + din[i].w);
         *reinterpret_cast<float4*>(out + c) = o;
         store4<act_t>(oa + c, o.x, o.y, o.z, o.w);
       }
-    } else {
+    }
+  } else {
+    for (int r = r0 + warp; r < r1; r += kWarps) {
+      const float mean = a.mean[r], rstd = a.rstd[r];
+      const float* x = a.x + (int64_t)r * a.C;
+      float* out = a.dres_out + (int64_t)r * a.C;
+      const float* din = a.dres_in ? a.dres_in + (int64_t)r * a.C : nullptr;
+      act_t* oa = dact + (int64_t)r * a.C;
       float s1 = 0.f, s2 = 0.f;
       for (int c = lane; c < a.C; c += 32) {
         float d = 0.f;
@@ -281,6 +354,12 @@ __device__ __forceinline__ uint4 f_to_bf16x8(const float* f) {
 }
 
 __device__ inline void task_ce_bf16_vec(const KParams& kp, const CeArgs& a, int idx) {
+  // One warp per row; every lane keeps eight 16-byte loads in flight in both
+  // passes (a row of 50k logits is ~100 KB, mostly L2-resident right after the
+  // LM-head tiles that wrote it).  exp is the fast hardware form (__expf):
+  // its relative error (a few 1e-6 at these arguments) is far below the bf16
+  // rounding of the gradient it feeds.
+  constexpr int kU = 8;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r0 = idx * a.rows_per_task, r1 = min(r0 + a.rows_per_task, a.N);
   const float invN = 1.0f / (float)a.N;
@@ -294,35 +373,26 @@ __device__ inline void task_ce_bf16_vec(const KParams& kp, const CeArgs& a, int 
       t = t < 0 ? 0 : a.V - 1;
     }
     float m = -INFINITY, s = 0.f;
-    int j = lane;
-    for (; j + 96 < nvec; j += 128) {
-      uint4 u[4];
+    for (int j = lane; j < nvec; j += 32 * kU) {
+      uint4 u[kU];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) u[q] = z[j + 32 * q];
+      for (int q = 0; q < kU; ++q)
+        if (j + 32 * q < nvec) u[q] = z[j + 32 * q];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < kU; ++q) {
+        if (j + 32 * q >= nvec) break;
         float f[8];
         bf16x8_to_f(u[q], f);
         float lm = f[0];
 #pragma unroll
         for (int e = 1; e < 8; ++e) lm = fmaxf(lm, f[e]);
-        if (lm > m) { s *= expf(m - lm); m = lm; }
+        if (lm > m) { s *= __expf(m - lm); m = lm; }
 #pragma unroll
-        for (int e = 0; e < 8; ++e) s += expf(f[e] - m);
+        for (int e = 0; e < 8; ++e) s += __expf(f[e] - m);
       }
     }
-    for (; j < nvec; j += 32) {
-      float f[8];
-      bf16x8_to_f(z[j], f);
-      float lm = f[0];
-#pragma unroll
-      for (int e = 1; e < 8; ++e) lm = fmaxf(lm, f[e]);
-      if (lm > m) { s *= expf(m - lm); m = lm; }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) s += expf(f[e] - m);
-    }
     const float M = warp_max(m);
-    s = (m == -INFINITY) ? 0.f : s * expf(m - M);
+    s = (m == -INFINITY) ? 0.f : s * __expf(m - M);
     const float lse = M + logf(warp_sum(s));
     const float zt = __bfloat162float(zr[t]);
     __syncwarp();
@@ -330,20 +400,20 @@ __device__ inline void task_ce_bf16_vec(const KParams& kp, const CeArgs& a, int 
       a.row_loss[r] = lse - zt;
       if (!isfinite(lse - zt)) set_soft(kp, kSoftNonFinite);
     }
-    for (j = lane; j < nvec; j += 128) {  // four 16-byte loads in flight per lane
-      uint4 u[4];
+    for (int j = lane; j < nvec; j += 32 * kU) {
+      uint4 u[kU];
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
+      for (int q = 0; q < kU; ++q)
         if (j + 32 * q < nvec) u[q] = z[j + 32 * q];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < kU; ++q) {
         const int jq = j + 32 * q;
-        if (jq >= nvec) continue;
+        if (jq >= nvec) break;
         float f[8];
         bf16x8_to_f(u[q], f);
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          float p = expf(f[e] - lse);
+          float p = __expf(f[e] - lse);
           if (jq * 8 + e == t) p -= 1.0f;
           f[e] = p * invN;
         }
@@ -351,6 +421,103 @@ __device__ inline void task_ce_bf16_vec(const KParams& kp, const CeArgs& a, int 
       }
     }
   }
+}
+
+// Staged variant (bf16, two rows of V logits fit in shared memory): one thread
+// bulk-copies each row into one of two buffers, the next row while this one is
+// processed; the whole block reduces the row (online max / sum of exp, then a
+// fixed-order combination of the eight warps) and writes dz back with 16-byte
+// coalesced stores.  A logit is read from memory once instead of twice.
+// The row copies complete on the bars shared with AdamW (iter counts their
+// phases); every copy issued here is also waited for here.
+__device__ inline void task_ce_bf16_staged(const KParams& kp, const CeArgs& a, int idx, uint8_t* smem,
+                                           uint64_t* bars, uint32_t* iter) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = idx * a.rows_per_task, r1 = min(r0 + a.rows_per_task, a.N);
+  const int nrows = r1 - r0;
+  const float invN = 1.0f / (float)a.N;
+  const int nvec = a.V >> 3;
+  const uint32_t row_bytes = (uint32_t)a.V * 2u;
+  const uint32_t buf_stride = (row_bytes + 127u) & ~127u;
+  float2* red = reinterpret_cast<float2*>(smem + 2 * buf_stride);  // [kWarps] (max, sum)
+  const uint32_t it0 = *iter;
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(smem);
+  const uint32_t bar0 = (uint32_t)__cvta_generic_to_shared(bars);
+  const __nv_bfloat16* logits = reinterpret_cast<const __nv_bfloat16*>(a.logits);
+  auto issue = [&](int k) {  // one thread: row r0 + k into buffer k & 1
+    const uint32_t bar = bar0 + 8 * ((it0 + (uint32_t)k) % kAdamStages);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(row_bytes) : "memory");
+    bulk_load(sbase + (uint32_t)(k & 1) * buf_stride, logits + (int64_t)(r0 + k) * a.V, row_bytes, bar);
+  };
+  if (threadIdx.x == 0) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier generic use of the buffers
+    for (int k = 0; k < min(nrows, 2); ++k) issue(k);
+  }
+  for (int k = 0; k < nrows; ++k) {
+    const int r = r0 + k;
+    const uint32_t st = (it0 + (uint32_t)k) % kAdamStages;
+    const uint32_t phase = ((it0 + (uint32_t)k) / kAdamStages) & 1u;
+    // every thread leaves together when a wait fails (no thread may be left
+    // behind at a later barrier of this task)
+    if (!__syncthreads_and(mbar_wait(kp, bar0 + 8 * st, phase))) return;
+    const uint4* z = reinterpret_cast<const uint4*>(smem + (k & 1) * buf_stride);
+    int t = kp.targets[r];
+    if (t < 0 || t >= a.V) {
+      if (threadIdx.x == 0) set_soft(kp, kSoftBadToken);
+      t = t < 0 ? 0 : a.V - 1;
+    }
+    float m = -INFINITY, s = 0.f;
+    for (int j = threadIdx.x; j < nvec; j += kThreads) {
+      float f[8];
+      bf16x8_to_f(z[j], f);
+      float lm = f[0];
+#pragma unroll
+      for (int e = 1; e < 8; ++e) lm = fmaxf(lm, f[e]);
+      if (lm > m) { s *= __expf(m - lm); m = lm; }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s += __expf(f[e] - m);
+    }
+    // warp, then block: (m, s) pairs combined in a fixed order
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+      const float mm = fmaxf(m, m2);
+      s = (m == -INFINITY ? 0.f : s * __expf(m - mm)) + (m2 == -INFINITY ? 0.f : s2 * __expf(m2 - mm));
+      m = mm;
+    }
+    if (lane == 0) red[warp] = make_float2(m, s);
+    __syncthreads();
+    float M = red[0].x;
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) M = fmaxf(M, red[w].x);
+    float S = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) S += red[w].x == -INFINITY ? 0.f : red[w].y * __expf(red[w].x - M);
+    const float lse = M + logf(S);
+    if (threadIdx.x == 0) {
+      const float zt = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(z)[t]);
+      a.row_loss[r] = lse - zt;
+      if (!isfinite(lse - zt)) set_soft(kp, kSoftNonFinite);
+    }
+    uint4* dz = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.logits) + (int64_t)r * a.V);
+    for (int j = threadIdx.x; j < nvec; j += kThreads) {
+      float f[8];
+      bf16x8_to_f(z[j], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        float p = __expf(f[e] - lse);
+        if (j * 8 + e == t) p -= 1.0f;
+        f[e] = p * invN;
+      }
+      dz[j] = f_to_bf16x8(f);
+    }
+    __syncthreads();  // buffer k & 1 and red[] are free again
+    if (threadIdx.x == 0 && k + 2 < nrows) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issue(k + 2);
+    }
+  }
+  if (threadIdx.x == 0) *iter = it0 + (uint32_t)nrows;
 }
 
 // loss = (1/N) sum_n row_loss[n], fixed order; flags a non-finite loss.
@@ -575,26 +742,13 @@ __device__ inline void task_embed_bwd_wpe(const EmbedArgs& a, int idx) {
 // mbarrier) of p, g, m and v for up to kAdamStages sub-chunks ahead, all threads
 // update a staged sub-chunk in place, and bulk stores write p, m, v and the bf16
 // copy back — about 128 KB in flight per SM without spending registers on it.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_all() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 // iter: this block's count of sub-chunks so far (stage = iter mod kAdamStages,
 // phase = (iter / kAdamStages) mod 2), shared by the block's threads.
 __device__ inline void task_adamw(const KParams& kp, const AdamArgs& a, int idx, uint8_t* smem, uint64_t* bars,
                                   uint32_t* iter) {
-  if (ld_volatile_u32(&kp.err[1]) & (kSoftBadToken | kSoftNonFinite)) return;
+  // The loss task may raise the flag while this task runs: thread 0 reads it
+  // once for the whole block, so all threads take the same branch.
+  if (__syncthreads_or(threadIdx.x == 0 && (ld_volatile_u32(&kp.err[1]) & (kSoftBadToken | kSoftNonFinite)))) return;
   const int64_t lo = (int64_t)idx * a.chunk;
   const int64_t hi = min(lo + a.chunk, a.n);
   const int nsub = (int)((hi - lo + kAdamSub - 1) / kAdamSub);
@@ -629,7 +783,7 @@ __device__ inline void task_adamw(const KParams& kp, const AdamArgs& a, int idx,
   for (int s = 0; s < nsub; ++s) {
     const uint32_t st = stage_of(s);
     const uint32_t phase = ((it0 + (uint32_t)s) / kAdamStages) & 1u;
-    if (!mbar_wait(kp, bar0 + 8 * st, phase)) return;
+    if (!__syncthreads_and(mbar_wait(kp, bar0 + 8 * st, phase))) return;  // all threads leave together
     uint8_t* buf = smem + st * kAdamStageBytes;
     float4* P = reinterpret_cast<float4*>(buf);
     const float4* G = reinterpret_cast<const float4*>(buf + kAdamSub * 4);

@@ -15,10 +15,16 @@
 
 namespace pgs {
 
-struct TcState {          // pipeline state carried by the block across GEMM tasks
-  uint32_t prod_stage, prod_phase;   // producer thread
-  uint32_t mma_stage, mma_phase;     // MMA thread
-  uint32_t acc_phase;                // every thread
+// Pipeline state a block carries across its GEMM runs for the whole launch.
+// Each role thread keeps its own copy and advances only its own fields; the
+// queue, accumulator and epilogue-sync mbarriers are initialised once per
+// launch and these counts give every wait its slot and phase parity.
+struct TcState {
+  uint32_t prod_stage, prod_phase;   // producer thread: operand stage ring
+  uint32_t mma_stage, mma_phase;     // MMA thread: operand stage ring
+  uint32_t q_seq;                    // queue entries published (scheduler) / taken (consumers)
+  uint32_t acc_seq;                  // accumulators filled (MMA) / drained (epilogue)
+  uint32_t e_seq;                    // epilogue group syncs (epilogue warps)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -57,7 +63,7 @@ __device__ __forceinline__ bool mbar_wait_e(uint32_t* err, uint64_t timeout_ns, 
     }
   }
   if (atomicCAS(&err[0], 0u, kFatalMbarTimeout) == 0u) {
-    err[2] = 0xffffffffu;
+    err[2] = 0x80000000u | (threadIdx.x << 16) | blockIdx.x;  // which block and thread gave up
     err[3] = bar;
   }
   return false;
@@ -239,7 +245,9 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
   const int cend = min(BN, N - n0);  // N is a multiple of 64
   SrcT nxt[kSrc ? 8 : 1];
   if constexpr (kSrc) epi_load_src<EPI>(nxt, src, lds, M, r0, n0 + cu);
-  if (!mbar_wait_e(err, timeout_ns, acc_bar, acc_parity)) return false;
+  const bool acc_ok = mbar_wait_e(err, timeout_ns, acc_bar, acc_parity);
+  __syncwarp();  // lanes leave the poll loop separately; tcgen05.ld below is warp-aligned
+  if (!acc_ok) return false;
   tc_fence_after();
   for (int c = 0; c < cend; c += 32) {
     const int n = n0 + c;
@@ -352,6 +360,7 @@ struct GemmShared {
   uint64_t stage_full[kTcStages], stage_empty[kTcStages];
   uint64_t acc_full[2], acc_empty[2];
   uint64_t q_full[2], q_empty[2];
+  uint64_t epi_sync;  // the four epilogue warps meet here after each tile
   int64_t q_task[2];
   int64_t next;
 };
@@ -359,8 +368,39 @@ struct GemmShared {
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ void epi_bar_sync() {  // the four epilogue warps
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+// The four epilogue warps meet on an mbarrier (one arrival per warp) rather
+// than a named hardware barrier: the wait is bounded, so a warp that left its
+// loop after a failed wait cannot leave the other three blocked for good.
+// n counts this warp's syncs in the current run (the phase parity).
+__device__ __forceinline__ bool epi_group_sync(const KParams& kp, uint32_t bar, uint32_t& n) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+  const bool ok = mbar_wait(kp, bar, n & 1u);
+  ++n;
+  __syncwarp();
+  return ok;
+}
+
+// The queue slots are rewritten by the scheduler as soon as every role has
+// signalled "slot empty"; a role must therefore read its slot exactly once,
+// before that signal.  Volatile accesses keep the compiler from re-reading
+// the slot later (a plain load may legally be repeated under register
+// pressure, and a repeat after the signal would see the next task).
+__device__ __forceinline__ int64_t q_read(const int64_t* slot) { return *reinterpret_cast<const volatile int64_t*>(slot); }
+__device__ __forceinline__ void q_write(int64_t* slot, int64_t v) { *reinterpret_cast<volatile int64_t*>(slot) = v; }
+
+// With tracing on, each GEMM role keeps its current wait in a per-block record
+// after the per-task trace (8 words per block: scheduler, producer, MMA, the four
+// epilogue warps, spare): kind << 56 | (i mod 2^24) << 32 | task.  After a failed
+// step the host reads where every block's pipeline stopped.
+enum RoleWait : uint32_t {
+  RW_SCHED_READY = 1, RW_SCHED_QEMPTY, RW_PROD_QFULL, RW_PROD_STAGE, RW_MMA_QFULL, RW_MMA_ACC, RW_MMA_STAGE,
+  RW_EPI_QFULL, RW_EPI_TILE, RW_EPI_SYNC, RW_DONE
+};
+__device__ __forceinline__ void role_note(const KParams& kp, int role, uint32_t kind, uint32_t i, int64_t t) {
+  if (kp.trace)
+    kp.trace[4 * kp.ntasks + 8 * blockIdx.x + role] =
+        ((unsigned long long)kind << 56) | ((unsigned long long)(i & 0xffffffu) << 32) | (uint32_t)t;
 }
 
 // Runs GEMM tasks starting with t_first (claimed, dependencies satisfied) and
@@ -373,47 +413,46 @@ __device__ inline int64_t gemm_run(const KParams& kp, int64_t t_first, GemmShare
   const uint32_t full0 = smem_u32(&gs.stage_full[0]), empty0 = smem_u32(&gs.stage_empty[0]);
   const uint32_t tiles0 = smem_u32(smem_tiles);
   const uint8_t* maps = reinterpret_cast<const uint8_t*>(kp.tmaps);  // 128-byte CUtensorMaps
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(q_full0 + 8 * i, 1);
-      mbar_init(q_empty0 + 8 * i, 3);    // producer, MMA, epilogue leader
-      mbar_init(acc_full0 + 8 * i, 1);   // MMA commit
-      mbar_init(acc_empty0 + 8 * i, 4);  // one arrive per epilogue warp
-    }
-    gs.q_task[0] = t_first;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  if (kp.trace && threadIdx.x == 0) {  // spare role word: runs so far on this block and this run's first task
+    unsigned long long* w = kp.trace + 4 * kp.ntasks + 8 * blockIdx.x + 7;
+    *w = ((((*w >> 32) & 0xffffffull) + 1) << 32) | (uint32_t)t_first;
   }
-  __syncthreads();
 
   if (warp == 2) {
     if (lane == 0) {
-      // ---- scheduler ----
-      mbar_arrive(q_full0);  // fill 0 = t_first
-      for (uint32_t i = 1;; ++i) {
-        int64_t t = kp.ntasks;
-        bool gemm = false;
-        if (ld_volatile_u32(&kp.err[0]) == 0u) {
-          t = claim_task(kp);
-          if (t < kp.ntasks && kp.ops[kp.tasks[t].op].type == OP_GEMM) {
-            const uint64_t t_claim = kp.trace ? globaltimer_ns() : 0;
-            gemm = task_ready(kp, t);
-            if (!gemm) t = kp.ntasks;  // a wait failed: stop the run, the main loop drains
-            else if (kp.trace) {
-              kp.trace[4 * t + 0] = t_claim;
-              kp.trace[4 * t + 1] = globaltimer_ns();
-              uint32_t smid;
-              asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-              kp.trace[4 * t + 3] = smid;
+      // ---- scheduler: publishes t_first, then claims ahead ----
+      for (uint32_t i = 0;; ++i) {
+        int64_t t = t_first;
+        bool gemm = true;
+        if (i > 0) {
+          t = kp.ntasks;
+          gemm = false;
+          if (ld_volatile_u32(&kp.err[0]) == 0u) {
+            t = claim_task(kp);
+            if (t < kp.ntasks && kp.ops[kp.tasks[t].op].type == OP_GEMM) {
+              const uint64_t t_claim = kp.trace ? globaltimer_ns() : 0;
+              role_note(kp, 0, RW_SCHED_READY, i, t);
+              gemm = task_ready(kp, t);
+              if (!gemm) t = kp.ntasks;  // a wait failed: stop the run, the main loop drains
+              else if (kp.trace) {
+                kp.trace[4 * t + 0] = t_claim;
+                kp.trace[4 * t + 1] = globaltimer_ns();
+                uint32_t smid;
+                asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+                kp.trace[4 * t + 3] = smid | ((unsigned long long)blockIdx.x << 32);
+              }
             }
           }
         }
-        const uint32_t slot = i & 1;
-        if (i >= 2 && !mbar_wait(kp, q_empty0 + 8 * slot, ((i >> 1) - 1) & 1)) {
+        const uint32_t seq = st.q_seq, slot = seq & 1;
+        role_note(kp, 0, RW_SCHED_QEMPTY, i, t);
+        if (seq >= 2 && !mbar_wait(kp, q_empty0 + 8 * slot, ((seq >> 1) - 1) & 1)) {
           gs.next = kp.ntasks;
           break;
         }
-        gs.q_task[slot] = gemm ? t : -2 - t;
+        q_write(&gs.q_task[slot], gemm ? t : -2 - t);
         mbar_arrive(q_full0 + 8 * slot);
+        ++st.q_seq;
         if (!gemm) {
           gs.next = t;
           break;
@@ -425,11 +464,14 @@ __device__ inline int64_t gemm_run(const KParams& kp, int64_t t_first, GemmShare
       // ---- TMA producer ----
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // smem last written by generic stores
       for (uint32_t i = 0;; ++i) {
-        const uint32_t slot = i & 1;
-        if (!mbar_wait(kp, q_full0 + 8 * slot, (i >> 1) & 1)) break;
-        const int64_t t = gs.q_task[slot];
+        const uint32_t seq = st.q_seq, slot = seq & 1;
+        role_note(kp, 1, RW_PROD_QFULL, i, -1);
+        if (!mbar_wait(kp, q_full0 + 8 * slot, (seq >> 1) & 1)) break;
+        const int64_t t = q_read(&gs.q_task[slot]);
         mbar_arrive(q_empty0 + 8 * slot);
+        ++st.q_seq;
         if (t < 0) break;
+        role_note(kp, 1, RW_PROD_STAGE, i, t);
         fence_proxy_async_global();  // operands written by other blocks' generic stores
         const GemmArgs g = kp.ops[kp.tasks[t].op].gemm;
         int tm, tn, split;
@@ -470,13 +512,16 @@ __device__ inline int64_t gemm_run(const KParams& kp, int64_t t_first, GemmShare
     if (lane == 0) {
       // ---- MMA issuer ----
       for (uint32_t i = 0;; ++i) {
-        const uint32_t slot = i & 1;
-        if (!mbar_wait(kp, q_full0 + 8 * slot, (i >> 1) & 1)) break;
-        const int64_t t = gs.q_task[slot];
+        const uint32_t seq = st.q_seq, slot = seq & 1;
+        role_note(kp, 2, RW_MMA_QFULL, i, -1);
+        if (!mbar_wait(kp, q_full0 + 8 * slot, (seq >> 1) & 1)) break;
+        const int64_t t = q_read(&gs.q_task[slot]);
         mbar_arrive(q_empty0 + 8 * slot);
+        ++st.q_seq;
         if (t < 0) break;
-        const uint32_t buf = i & 1;  // i counts this run's GEMM tasks (stop comes last)
-        if (i >= 2 && !mbar_wait(kp, acc_empty0 + 8 * buf, ((i >> 1) - 1) & 1)) break;
+        role_note(kp, 2, RW_MMA_ACC, i, t);
+        const uint32_t acc = st.acc_seq, buf = acc & 1;
+        if (acc >= 2 && !mbar_wait(kp, acc_empty0 + 8 * buf, ((acc >> 1) - 1) & 1)) break;
         tc_fence_after();
         const GemmArgs g = kp.ops[kp.tasks[t].op].gemm;
         int tm, tn, split;
@@ -487,6 +532,7 @@ __device__ inline int64_t gemm_run(const KParams& kp, int64_t t_first, GemmShare
         const uint32_t idesc = idesc_bf16(kTcBM, g.BN, g.a_mn, g.b_mn);
         const uint32_t d_tmem = tmem_base + buf * 256;
         bool ok = true;
+        role_note(kp, 2, RW_MMA_STAGE, i, t);
         for (int kb = 0; kb < nkb; ++kb) {
           ok = mbar_wait(kp, full0 + 8 * st.mma_stage, st.mma_phase);
           if (!ok) break;
@@ -506,33 +552,40 @@ __device__ inline int64_t gemm_run(const KParams& kp, int64_t t_first, GemmShare
         }
         if (!ok) break;
         tc_commit(acc_full0 + 8 * buf);  // accumulator complete
+        ++st.acc_seq;
       }
     }
   } else if (warp >= 4) {
     // ---- epilogue (warps 4..7 read TMEM lane quarters 0..3) ----
     const int q = warp & 3;
+    const uint32_t esync = smem_u32(&gs.epi_sync);
     for (uint32_t i = 0;; ++i) {
-      const uint32_t slot = i & 1;
-      if (!mbar_wait(kp, q_full0 + 8 * slot, (i >> 1) & 1)) break;
-      const int64_t t = gs.q_task[slot];
+      const uint32_t seq = st.q_seq, slot = seq & 1;
+      if (lane == 0) role_note(kp, 3 + q, RW_EPI_QFULL, i, -1);
+      if (!mbar_wait(kp, q_full0 + 8 * slot, (seq >> 1) & 1)) break;
+      const int64_t t = q_read(&gs.q_task[slot]);
+      ++st.q_seq;
       if (t < 0) {
-        epi_bar_sync();
+        epi_group_sync(kp, esync, st.e_seq);
         if (warp == 4 && lane == 0) mbar_arrive(q_empty0 + 8 * slot);
         break;
       }
-      const uint32_t buf = i & 1;
+      const uint32_t acc = st.acc_seq, buf = acc & 1;
+      ++st.acc_seq;
       const GemmArgs g = kp.ops[kp.tasks[t].op].gemm;
       int tm, tn, split;
       gemm_coords(g, kp.tasks[t].idx, tm, tn, split);
+      if (lane == 0) role_note(kp, 3 + q, RW_EPI_TILE, i, t);
       const bool ok = epilogue_tile(kp, g, split, tm * kTcBM + q * 32, tn * g.BN,
                                     tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256,
                                     smem_tiles + kTcSmemBytes + (warp - 4) * kEpiStageBytes, gelu_tanh,
-                                    acc_full0 + 8 * buf, (i >> 1) & 1);
+                                    acc_full0 + 8 * buf, (acc >> 1) & 1);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty0 + 8 * buf);
-      epi_bar_sync();
-      if (warp == 4 && lane == 0) {
+      if (lane == 0) role_note(kp, 3 + q, RW_EPI_SYNC, i, t);
+      const bool synced = epi_group_sync(kp, esync, st.e_seq);
+      if (warp == 4 && lane == 0 && synced) {
         mbar_arrive(q_empty0 + 8 * slot);
         if (t != kp.skip_release) {
           __threadfence();
@@ -542,11 +595,13 @@ __device__ inline int64_t gemm_run(const KParams& kp, int64_t t_first, GemmShare
         }
         if (kp.trace) kp.trace[4 * t + 2] = globaltimer_ns();
       }
-      if (!ok) break;
+      if (!ok || !synced) break;
     }
   }
+  if (lane == 0 && warp != 3 && ld_volatile_u32(&kp.err[0]) == 0u)  // a failed role keeps its last wait
+    role_note(kp, warp < 3 ? (warp == 2 ? 0 : warp + 1) : 3 + (warp & 3), RW_DONE, 0, -1);
   __syncwarp();
-  __syncthreads();
+  cta_sync();
   return gs.next;
 }
 

@@ -318,6 +318,25 @@ int gpt_test_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* A,
                   void* cuda_stream, float* kernel_ms);
 
 /*
+ * Test hook: one bf16 tensor-core GEMM as in gpt_test_gemm (A, B bf16, same
+ * layouts), followed by one of the fused epilogues the training step uses on
+ * the accumulator acc[m, n] (fp32):
+ *   epi 0  store:         out bf16 [M, ldo] = acc + bias
+ *   epi 1  residual add:  out fp32 [M, ldo] = src fp32 [M, lds] + acc + bias
+ *   epi 2  GELU:          out bf16 = GELU'(acc + bias), out2 bf16 [M, ldo2] = GELU(acc + bias)
+ *   epi 4  GELU backward: out bf16 = acc * src bf16 [M, lds]  (src: a stored GELU')
+ * GELU is the tanh form when gelu_tanh != 0, else the erf form (the step's
+ * MLP activation).  bias fp32 [N] or NULL (ignored by epi 4).  All pointers DEVICE; out may alias src (epi 1).
+ * Requires K % 64 == 0, N % 64 == 0, lda, ldb % 8 == 0, ldo, ldo2, lds % 4 == 0.
+ * kernel_ms (HOST, may be NULL) receives the launch's device time.  Errors:
+ * INVALID_ARG, UNSUPPORTED, OOM, CUDA, TIMEOUT; text via gpt_last_error(NULL).
+ */
+int gpt_test_gemm_epilogue(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, int32_t a_mn,
+                           const void* B, int64_t ldb, int32_t b_mn, int32_t epi, int32_t gelu_tanh, void* out,
+                           int64_t ldo, void* out2, int64_t ldo2, const float* bias, const void* src, int64_t lds,
+                           void* cuda_stream, float* kernel_ms);
+
+/*
  * Test hook: causal multi-head attention forward and backward as a graph of
  * the persistent kernel's attention tasks.  DEVICE buffers, token-major rows
  * n = b*T + t: qkv [B*T, 3*H*d] (q | k | v, head h at columns h*d), o

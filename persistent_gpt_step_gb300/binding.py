@@ -88,6 +88,10 @@ SIGNATURES = [
     ("gpt_test_gemm", c_int, [c_int32, c_int32, c_int32, c_int32, c_void_p, c_int64, c_int32,
                               c_void_p, c_int64, c_int32, c_void_p, c_int64, c_int32, c_void_p,
                               POINTER(c_float)]),
+    ("gpt_test_gemm_epilogue", c_int, [c_int32, c_int32, c_int32, c_void_p, c_int64, c_int32,
+                                       c_void_p, c_int64, c_int32, c_int32, c_int32, c_void_p, c_int64,
+                                       c_void_p, c_int64, c_void_p, c_void_p, c_int64, c_void_p,
+                                       POINTER(c_float)]),
 ]
 
 
@@ -316,6 +320,35 @@ def test_gemm(A, B, a_mn: bool, b_mn: bool, M: int, N: int, K: int, ksplit: int 
     if rc != GPT_OK:
         raise GptError(rc, lib.gpt_last_error(None).decode())
     return (C, float(ms.value)) if timing else C
+
+
+EPI_STORE, EPI_RESID, EPI_GELU, EPI_GELU_BWD = 0, 1, 2, 4
+
+
+def test_gemm_epilogue(A, B, a_mn: bool, b_mn: bool, M: int, N: int, K: int, epi: int, bias=None, src=None,
+                       gelu_tanh: bool = True, stream=None, timing: bool = False):
+    """Runs gpt_test_gemm_epilogue on bf16 torch CUDA tensors A, B.  Returns
+    out (bf16, or fp32 for the residual epilogue; GELU' for the GELU
+    epilogue), plus out2 (GELU) for the GELU epilogue, plus kernel
+    milliseconds with timing=True."""
+    import torch
+    lib = load()
+    dev = A.device
+    out = torch.full((M, N), float("nan"), dtype=torch.float32 if epi == EPI_RESID else torch.bfloat16, device=dev)
+    out2 = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=dev) if epi == EPI_GELU else None
+    s = stream if stream is not None else torch.cuda.current_stream()
+    ms = c_float()
+    rc = lib.gpt_test_gemm_epilogue(M, N, K, c_void_p(A.data_ptr()), A.stride(0), int(a_mn),
+                                    c_void_p(B.data_ptr()), B.stride(0), int(b_mn), epi, int(gelu_tanh),
+                                    c_void_p(out.data_ptr()), N,
+                                    c_void_p(out2.data_ptr() if out2 is not None else None), N,
+                                    c_void_p(bias.data_ptr() if bias is not None else None),
+                                    c_void_p(src.data_ptr() if src is not None else None),
+                                    src.stride(0) if src is not None else 0, c_void_p(s.cuda_stream), byref(ms))
+    if rc != GPT_OK:
+        raise GptError(rc, lib.gpt_last_error(None).decode())
+    res = (out, out2) if epi == EPI_GELU else (out,)
+    return (*res, float(ms.value)) if timing else (res if len(res) > 1 else res[0])
 
 
 def init_params_host(cfg, seed: int, n: int) -> np.ndarray:

@@ -245,7 +245,7 @@ struct Bump {
 struct Layout {
   size_t ldc, ldf;  // row pitch (elements) of the padded C- and F-wide activations
   size_t params, grads, m, v, shadow;
-  std::vector<size_t> x, xm, ln1, ln1_mu, ln1_rs, qkv, atto, lse, ln2, ln2_mu, ln2_rs, hpre, gact;
+  std::vector<size_t> x, xm, ln1, ln1_mu, ln1_rs, qkv, atto, lse, ln2, ln2_mu, ln2_rs, dgelu, gact;
   size_t lnf, lnf_mu, lnf_rs, logits, row_loss, loss;
   size_t daf;
   std::vector<size_t> dx, dx_act, dxm, dxm_act, dh, da2, dO, dqkv, da1, att_scr;
@@ -301,7 +301,7 @@ Layout make_layout(const gpt_config& c, size_t nparams, int lm_ksplit) {
     Lo.ln2.push_back(b.take(N * Lo.ldc * act));
     Lo.ln2_mu.push_back(b.take(N * 4));
     Lo.ln2_rs.push_back(b.take(N * 4));
-    Lo.hpre.push_back(b.take(N * F * act));
+    Lo.dgelu.push_back(b.take(N * F * act));  // GELU'(pre-activation), for the backward
     Lo.gact.push_back(b.take(N * Lo.ldf * act));
   }
   Lo.lnf = b.take(N * C * act);
@@ -723,7 +723,7 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
     // h = ln2 . W1^T + b1 ; g = GELU(h)
     if ((rc = gemm_op(h, &o, N, F, C, {ACT(Lo.ln2[l]), LDC, false}, {W(id.w_1), C, false}, EPI_GELU, 1)))
       return rc;
-    o.gemm.out = ACT(Lo.hpre[l]); o.gemm.ldo = F; o.gemm.out2 = ACT(Lo.gact[l]); o.gemm.ldo2 = LDF;
+    o.gemm.out = ACT(Lo.dgelu[l]); o.gemm.ldo = F; o.gemm.out2 = ACT(Lo.gact[l]); o.gemm.ldo2 = LDF;
     o.gemm.bias = P(id.b_1);
     op_up[l] = bld.add(o, {op_ln2[l]});
     // x_{l+1} = xm + g . W2^T + b2
@@ -798,7 +798,7 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
     // MLP down: dg = dx . W2 (then * GELU'(h)) ; dW2 = dx^T . g ; db2 = dx^T . 1
     if ((rc = gemm_op(h, &o, N, F, C, {ACT(Lo.dx_act[l + 1]), C, false}, {W(id.w_2), F, true}, EPI_GELU_BWD, 1)))
       return rc;
-    o.gemm.out = ACT(Lo.dh[l]); o.gemm.ldo = F; o.gemm.aux = ACT(Lo.hpre[l]); o.gemm.ldaux = F;
+    o.gemm.out = ACT(Lo.dh[l]); o.gemm.ldo = F; o.gemm.aux = ACT(Lo.dgelu[l]); o.gemm.ldaux = F;
     const int op_down_dx = bld.add(o, {op_dres});
     // [dW2 | db2] = dx^T . [g | 1]
     if ((rc = gemm_op(h, &o, C, LDF, N, {ACT(Lo.dx_act[l + 1]), C, true}, {ACT(Lo.gact[l]), LDF, true}, EPI_F32, 1)))
@@ -1411,6 +1411,53 @@ int gpt_test_gemm(int32_t dtype, int32_t M, int32_t N, int32_t K, const void* A,
     cudaEventCreate(&h.ev1);
   }
   rc = run_test_graph(h, dtype);
+  if (kernel_ms) {
+    *kernel_ms = h.last_kernel_ms;
+    cudaEventDestroy(h.ev0);
+    cudaEventDestroy(h.ev1);
+    h.ev0 = h.ev1 = nullptr;
+  }
+  return rc;
+}
+
+int gpt_test_gemm_epilogue(int32_t M, int32_t N, int32_t K, const void* A, int64_t lda, int32_t a_mn,
+                           const void* B, int64_t ldb, int32_t b_mn, int32_t epi, int32_t gelu_tanh, void* out,
+                           int64_t ldo, void* out2, int64_t ldo2, const float* bias, const void* src, int64_t lds,
+                           void* cuda_stream, float* kernel_ms) {
+  g_create_error.clear();
+  if (!A || !B || !out || M < 1 || N < 1 || K < 1 || ldo < N)
+    return fail(nullptr, GPT_ERR_INVALID_ARG, "bad GEMM epilogue test arguments");
+  if (epi != EPI_STORE && epi != EPI_RESID && epi != EPI_GELU && epi != EPI_GELU_BWD)
+    return fail(nullptr, GPT_ERR_INVALID_ARG, "epi must be 0 (store), 1 (residual), 2 (GELU) or 4 (GELU backward)");
+  if ((epi == EPI_GELU && (!out2 || ldo2 < N || ldo2 % 4)) || ((epi == EPI_RESID || epi == EPI_GELU_BWD) &&
+                                                              (!src || lds < N || lds % 4)))
+    return fail(nullptr, GPT_ERR_INVALID_ARG, "missing or misaligned second output / source operand");
+  if (K % kTcBK || N % 64 || lda % 8 || ldb % 8 || ldo % 4)
+    return fail(nullptr, GPT_ERR_UNSUPPORTED, "GEMM epilogue test: K %% 64, N %% 64, lda/ldb %% 8, ldo %% 4 must be 0");
+  gpt h;
+  gpt_default_config(&h.cfg);
+  h.cfg.dtype = GPT_DTYPE_BF16;
+  h.cfg.gelu_tanh = gelu_tanh;
+  h.stream = (cudaStream_t)cuda_stream;
+  cudaGetDevice(&h.device);
+  cudaDeviceGetAttribute(&h.num_sms, cudaDevAttrMultiProcessorCount, h.device);
+  h.D = Dims{1, 64, 1, 64, 64, 64, 1, 1, 1};
+  OpDesc o;
+  int rc = gemm_op(&h, &o, M, N, K, {A, lda, a_mn != 0}, {B, ldb, b_mn != 0}, epi, 1);
+  if (rc != GPT_OK) { g_create_error = h.err; return rc; }
+  o.gemm.out = out; o.gemm.ldo = ldo;
+  o.gemm.out2 = out2; o.gemm.ldo2 = ldo2;
+  o.gemm.bias = epi == EPI_GELU_BWD ? nullptr : bias;
+  if (epi == EPI_RESID) { o.gemm.resid = static_cast<const float*>(src); o.gemm.ldr = lds; }
+  if (epi == EPI_GELU_BWD) { o.gemm.aux = src; o.gemm.ldaux = lds; }
+  Builder bld{&h};
+  bld.add(o, {});
+  bld.finish(h.num_sms);
+  if (kernel_ms) {
+    cudaEventCreate(&h.ev0);
+    cudaEventCreate(&h.ev1);
+  }
+  rc = run_test_graph(h, GPT_DTYPE_BF16);
   if (kernel_ms) {
     *kernel_ms = h.last_kernel_ms;
     cudaEventDestroy(h.ev0);

@@ -59,9 +59,9 @@ enum OpType : int32_t {
 enum Epilogue : int32_t {
   EPI_STORE = 0,     // out(act)  = acc (+ bias)
   EPI_RESID,         // out(f32)  = resid(f32) + acc (+ bias)
-  EPI_GELU,          // out(act)  = acc + bias ; out2(act) = GELU(acc + bias)
+  EPI_GELU,          // out(act)  = GELU'(acc + bias) ; out2(act) = GELU(acc + bias)
   EPI_F32,           // out(f32)  = acc                   (dX partials, weight gradients)
-  EPI_GELU_BWD,      // out(act)  = acc * GELU'(aux(act))
+  EPI_GELU_BWD,      // out(act)  = acc * aux(act)        (aux: the GELU' the forward stored)
 };
 
 struct GemmArgs {

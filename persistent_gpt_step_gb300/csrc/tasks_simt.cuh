@@ -31,7 +31,7 @@ __device__ __forceinline__ void epilogue_one(const GemmArgs& g, int split, int m
     } break;
     case EPI_GELU: {
       if (g.bias) acc += g.bias[n];
-      reinterpret_cast<act_t*>(g.out)[(int64_t)m * g.ldo + n] = from_f<act_t>(acc);
+      reinterpret_cast<act_t*>(g.out)[(int64_t)m * g.ldo + n] = from_f<act_t>(gelu_grad_f(acc, gelu_tanh));
       reinterpret_cast<act_t*>(g.out2)[(int64_t)m * g.ldo2 + n] = from_f<act_t>(gelu_f(acc, gelu_tanh));
     } break;
     case EPI_F32: {
@@ -42,8 +42,8 @@ __device__ __forceinline__ void epilogue_one(const GemmArgs& g, int split, int m
       reinterpret_cast<float*>(g.out)[split * g.split_stride + (int64_t)m * g.ldo + n] = acc;
     } break;
     case EPI_GELU_BWD: {
-      const float h = to_f<act_t>(reinterpret_cast<const act_t*>(g.aux)[(int64_t)m * g.ldaux + n]);
-      reinterpret_cast<act_t*>(g.out)[(int64_t)m * g.ldo + n] = from_f<act_t>(acc * gelu_grad_f(h, gelu_tanh));
+      const float dg = to_f<act_t>(reinterpret_cast<const act_t*>(g.aux)[(int64_t)m * g.ldaux + n]);
+      reinterpret_cast<act_t*>(g.out)[(int64_t)m * g.ldo + n] = from_f<act_t>(acc * dg);
     } break;
   }
 }

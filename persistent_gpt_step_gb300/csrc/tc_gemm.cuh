@@ -169,16 +169,21 @@ __device__ __forceinline__ float tanh_sfu(float x) {
   asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ float gelu_bf(float x, bool tanh_form) {
-  if (!tanh_form) return gelu_f(x, false);
+// GELU and its derivative at x together (one tanh for both in the tanh form):
+// GELU(x) = 0.5 x (1 + t), GELU'(x) = 0.5 (1 + t) + 0.5 x (1 - t^2) k0 (1 + 3 c x^2),
+// t = tanh(k0 (x + c x^3)), k0 = sqrt(2/pi), c = 0.044715; erf form otherwise.
+__device__ __forceinline__ void gelu_pair_bf(float x, bool tanh_form, float& g, float& dg) {
+  if (!tanh_form) {
+    g = gelu_f(x, false);
+    dg = gelu_grad_f(x, false);
+    return;
+  }
   const float k0 = 0.7978845608028654f;
-  return 0.5f * x * (1.0f + tanh_sfu(k0 * (x + 0.044715f * x * x * x)));
-}
-__device__ __forceinline__ float gelu_grad_bf(float x, bool tanh_form) {
-  if (!tanh_form) return gelu_grad_f(x, false);
-  const float k0 = 0.7978845608028654f;
-  const float t = tanh_sfu(k0 * (x + 0.044715f * x * x * x));
-  return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * k0 * (1.0f + 3.0f * 0.044715f * x * x);
+  const float x2 = x * x;
+  const float t = tanh_sfu(k0 * (x + 0.044715f * x2 * x));
+  const float h = 0.5f * x;
+  g = h + h * t;
+  dg = 0.5f + 0.5f * t + h * (1.0f - t * t) * k0 * (1.0f + 3.0f * 0.044715f * x2);
 }
 
 __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float* v) {
@@ -201,15 +206,15 @@ __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float* v
 // u owns columns 4 (u mod 8) .. +3 of rows 4i + u / 8, so bias, residual,
 // GELU and the stores touch whole 64- or 128-byte row segments.
 //
-// An epilogue that reads a second operand (the residual stream, the GELU
-// pre-activation) issues all 8 of a group's loads at once: the first group's
+// An epilogue that reads a second operand (the residual stream, the stored
+// GELU derivative) issues all 8 of a group's loads at once: the first group's
 // before waiting for the accumulator (they land while the MMAs still run), each
 // next group's before the current one is processed, so a tile pays about one
 // memory latency instead of one per few rows.  Returns false when the wait for
 // the accumulator (acc_bar, parity) timed out or another block failed.
 template <int EPI>
 struct EpiSrc {
-  using T = uint2;  // EPI_GELU_BWD: four bf16 pre-activations
+  using T = uint2;  // EPI_GELU_BWD: four bf16 GELU derivatives
 };
 template <>
 struct EpiSrc<EPI_RESID> {
@@ -277,23 +282,28 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
     const int col = n + cu;
     float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
     if (EPI != EPI_F32 && EPI != EPI_GELU_BWD && bias) b = *reinterpret_cast<const float4*>(bias + col);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    auto row = [&](const int i) {
       const int rl = rq + 4 * i;
       const int m = row0 + rl;
-      if (m >= M) break;  // rows ascend with i
       float4 v = *reinterpret_cast<const float4*>(stage + rl * 128 + (((lane & 7) ^ (rl & 7)) << 4));
       v.x += b.x; v.y += b.y; v.z += b.z; v.w += b.w;
-      if constexpr (EPI == EPI_STORE || EPI == EPI_GELU) {
+      if constexpr (EPI == EPI_STORE) {
         __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
         *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + (int64_t)m * ldo + col) =
             make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
-        if constexpr (EPI == EPI_GELU) {
-          lo = __floats2bfloat162_rn(gelu_bf(v.x, gelu_tanh), gelu_bf(v.y, gelu_tanh));
-          hi = __floats2bfloat162_rn(gelu_bf(v.z, gelu_tanh), gelu_bf(v.w, gelu_tanh));
-          *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out2) + (int64_t)m * ldo2 + col) =
-              make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
-        }
+      } else if constexpr (EPI == EPI_GELU) {  // out = GELU'(v) for the backward, out2 = GELU(v)
+        float g[4], dg[4];
+        gelu_pair_bf(v.x, gelu_tanh, g[0], dg[0]);
+        gelu_pair_bf(v.y, gelu_tanh, g[1], dg[1]);
+        gelu_pair_bf(v.z, gelu_tanh, g[2], dg[2]);
+        gelu_pair_bf(v.w, gelu_tanh, g[3], dg[3]);
+        __nv_bfloat162 lo = __floats2bfloat162_rn(dg[0], dg[1]), hi = __floats2bfloat162_rn(dg[2], dg[3]);
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + (int64_t)m * ldo + col) =
+            make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+        lo = __floats2bfloat162_rn(g[0], g[1]);
+        hi = __floats2bfloat162_rn(g[2], g[3]);
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out2) + (int64_t)m * ldo2 + col) =
+            make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
       } else if constexpr (EPI == EPI_RESID) {
         const float4 rr = cur[i];
         *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (int64_t)m * ldo + col) =
@@ -305,14 +315,22 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
           *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (int64_t)m * ldo + col) = v;
         }
       } else if constexpr (EPI == EPI_GELU_BWD) {
-        const uint2 hv = cur[i];
+        const uint2 hv = cur[i];  // GELU'(pre-activation), stored by the forward
         const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hv.x));
         const float2 e = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hv.y));
-        __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * gelu_grad_bf(a.x, gelu_tanh), v.y * gelu_grad_bf(a.y, gelu_tanh));
-        __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * gelu_grad_bf(e.x, gelu_tanh), v.w * gelu_grad_bf(e.y, gelu_tanh));
+        __nv_bfloat162 lo = __floats2bfloat162_rn(v.x * a.x, v.y * a.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(v.z * e.x, v.w * e.y);
         *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + (int64_t)m * ldo + col) =
             make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
       }
+    };
+    if (row0 + 32 <= M) {  // every row of this warp exists: no per-row branch
+#pragma unroll
+      for (int i = 0; i < 8; ++i) row(i);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (row0 + rq + 4 * i < M) row(i);
     }
   }
   return true;
@@ -588,7 +606,9 @@ __device__ inline int64_t gemm_run(const KParams& kp, int64_t t_first, GemmShare
       if (warp == 4 && lane == 0 && synced) {
         mbar_arrive(q_empty0 + 8 * slot);
         if (t != kp.skip_release) {
-          __threadfence();
+          // the tile's stores by all four warps precede this thread's acquire on
+          // the group sync; the release add below makes them visible at gpu scope
+          // (and the proxy fence to the consumers' TMA loads)
           fence_proxy_async_global();
           red_release_add_u64(kp.counters + kp.tasks[t].sig, 1ull);
           if (kp.tasks[t].sig2 >= 0) red_release_add_u64(kp.counters + kp.tasks[t].sig2, 1ull);

@@ -45,12 +45,43 @@ def run(name, M, N, K, a_mn, b_mn, reps=3):
     return best, 2.0 * M * N * K / best / 1e9
 
 
+EPILOGUES = [("f32", None), ("store", B.EPI_STORE), ("residual", B.EPI_RESID), ("gelu", B.EPI_GELU),
+             ("gelu-bwd", B.EPI_GELU_BWD)]
+
+
+def run_epilogues(M, N, K, reps=3):
+    """Each fused epilogue on one shape: ms, TFLOP/s and the implied time per tile."""
+    g = torch.Generator(device="cuda").manual_seed(1)
+    A = torch.randn(M, K, device="cuda", generator=g).bfloat16()
+    Bm = torch.randn(N, K, device="cuda", generator=g).bfloat16()
+    bias = torch.randn(N, device="cuda", generator=g)
+    resid = torch.randn(M, N, device="cuda", generator=g)
+    aux = torch.randn(M, N, device="cuda", generator=g).bfloat16()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    print(f"epilogues on M={M} N={N} K={K} ({sms} SMs)")
+    for name, epi in EPILOGUES:
+        best = float("inf")
+        for _ in range(reps):
+            if epi is None:
+                _, ms = B.test_gemm(A, Bm, 0, 0, M, N, K, timing=True)
+            else:
+                src = resid if epi == B.EPI_RESID else (aux if epi == B.EPI_GELU_BWD else None)
+                ms = B.test_gemm_epilogue(A, Bm, 0, 0, M, N, K, epi, bias=bias, src=src, timing=True)[-1]
+            best = min(best, ms)
+        print(f"  {name:10s} {best:8.3f} ms {2.0 * M * N * K / best / 1e9:8.1f} TF/s")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--config", default="main")
     ap.add_argument("--only", default=None, help="M,N,K,a_mn,b_mn")
+    ap.add_argument("--epilogues", default=None, help="M,N,K: time every fused epilogue on this shape")
+    ap.add_argument("--reps", type=int, default=3, help="launches per epilogue (--epilogues)")
     args = ap.parse_args()
     B.load()
+    if args.epilogues:
+        run_epilogues(*(int(x) for x in args.epilogues.split(",")), reps=args.reps)
+        return
     todo = shapes(I.CONFIGS[args.config])
     if args.only:
         M, N, K, a, b = (int(x) for x in args.only.split(","))

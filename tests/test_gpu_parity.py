@@ -85,6 +85,46 @@ def test_gemm_bf16_ksplit():
     assert (C.double().sum(0) - ref).abs().max().item() <= 1e-3 * math.sqrt(K)
 
 
+@pytest.mark.parametrize("M,N,K", [(256, 320, 256), (384, 3072, 768), (200, 128, 128)])
+@pytest.mark.parametrize("epi", [B.EPI_STORE, B.EPI_RESID, B.EPI_GELU, B.EPI_GELU_BWD])
+@pytest.mark.parametrize("gelu_tanh", [True, False])
+def test_gemm_fused_epilogues(M, N, K, epi, gelu_tanh):
+    """Each fused epilogue of the step's GEMMs against its definition applied to
+    a float64 product (GELU and its derivative from the oracle's definitions)."""
+    if not gelu_tanh and epi not in (B.EPI_GELU, B.EPI_GELU_BWD):
+        pytest.skip("the GELU form only matters to the GELU epilogues")
+    g = torch.Generator(device="cuda").manual_seed(M + 3 * N + K + epi)
+    Am = torch.randn(M, K, device="cuda", generator=g).bfloat16()
+    Bm = torch.randn(N, K, device="cuda", generator=g).bfloat16()
+    bias = torch.randn(N, device="cuda", generator=g)
+    acc = Am.double() @ Bm.double().t()
+    src = None
+    if epi == B.EPI_RESID:
+        src = torch.randn(M, N, device="cuda", generator=g)
+    elif epi == B.EPI_GELU_BWD:
+        x = 2 * torch.randn(M, N, device="cuda", generator=g).double()
+        src = torch.from_numpy(O.gelu_grad(x.cpu().numpy(), gelu_tanh)).cuda().bfloat16()
+    got = B.test_gemm_epilogue(Am, Bm, 0, 0, M, N, K, epi, bias=bias, src=src, gelu_tanh=gelu_tanh)
+    b = bias.double()
+    if epi == B.EPI_STORE:
+        ref = acc + b
+        assert (got.double() - ref).abs().max().item() <= 8e-3 * ref.abs().max().item()
+    elif epi == B.EPI_RESID:
+        ref = src.double() + acc + b
+        assert got.dtype == torch.float32
+        assert (got.double() - ref).abs().max().item() <= 1e-4 * math.sqrt(K)
+    elif epi == B.EPI_GELU:
+        dgelu, act = got
+        pre = (acc + b).cpu().numpy()
+        refd = torch.from_numpy(O.gelu_grad(pre, gelu_tanh)).cuda()
+        refg = torch.from_numpy(O.gelu(pre, gelu_tanh)).cuda()
+        assert (dgelu.double() - refd).abs().max().item() <= 1e-2 * refd.abs().max().item()
+        assert (act.double() - refg).abs().max().item() <= 1e-2 * refg.abs().max().item()
+    else:
+        ref = acc * src.double()
+        assert (got.double() - ref).abs().max().item() <= 1e-2 * ref.abs().max().item()
+
+
 # ----------------------------------------------------------------- attention unit tests
 
 def _attn_reference(qkv, dout, B, T, H, d):

@@ -249,7 +249,7 @@ typedef struct gpt_task_info {
 
 /*
  * Host-only: builds the step's task graph for cfg (as if on a GPU with num_sms
- * SMs; <= 0 means 148) without device memory, and reports it: *n_tasks tasks in
+ * SMs; <= 0 means 152, a GB300) without device memory, and reports it: *n_tasks tasks in
  * ticket order (the first max_tasks copied to HOST tasks[], may be NULL) and
  * *n_ops operations (type and task count of the first max_ops into HOST
  * op_types[] / op_tasks[], and into op_dims[6*i .. 6*i+5]: for GEMM

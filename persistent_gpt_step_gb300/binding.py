@@ -362,7 +362,7 @@ def init_params_host(cfg, seed: int, n: int) -> np.ndarray:
     return out
 
 
-def describe_graph(cfg, num_sms: int = 148, dims: bool = False):
+def describe_graph(cfg, num_sms: int = 152, dims: bool = False):
     """The step's task graph, built on the host.
 
     Returns (tasks, op_types, op_tasks[, op_dims]): tasks in ticket order as

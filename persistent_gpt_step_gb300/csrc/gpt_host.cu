@@ -267,7 +267,7 @@ bool ce_staged(const gpt_config& c) {
 constexpr int kRowsEmb = 32;      // rows per embedding task
 constexpr int kVocabRows = 64;    // vocabulary rows per embedding-backward task
 constexpr int kColsColsum = 64;   // columns per column-sum task
-constexpr int64_t kAdamChunk = 32768;
+constexpr int64_t kAdamChunk = 65536;
 
 int ln_tasks(int N) { return (N + kRowsLn - 1) / kRowsLn; }
 
@@ -897,7 +897,7 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
                     kRowsEmb, nullptr, nullptr, nullptr};
   const int op_wpe = bld.add(o, {op_dres});
   adam(h->t_wpe, {op_wpe});
-  bld.finish(h->num_sms > 0 ? h->num_sms : 148);
+  bld.finish(h->num_sms > 0 ? h->num_sms : 152);
   (void)op_lm; (void)op_qkv; (void)op_attn; (void)op_atto; (void)op_ln2; (void)op_up; (void)op_down;
   return GPT_OK;
 }
@@ -1056,7 +1056,7 @@ size_t gpt_arena_bytes(const gpt_config* cfg) {
   gpt tmp;
   tmp.cfg = *cfg;
   build_table(&tmp);
-  int dev = 0, sms = 148;
+  int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   return make_layout(*cfg, tmp.nparams, lm_ksplit_for(*cfg, sms)).total;
 }
@@ -1540,7 +1540,7 @@ int gpt_graph_describe(const gpt_config* cfg, int32_t num_sms, int64_t* n_tasks,
   gpt h;
   h.cfg = *cfg;
   h.describe_only = true;
-  h.num_sms = num_sms > 0 ? num_sms : 148;
+  h.num_sms = num_sms > 0 ? num_sms : 152;
   h.D = Dims{cfg->n_layer, cfg->d_model, cfg->n_head, cfg->d_model / cfg->n_head, cfg->d_mlp, cfg->vocab,
              cfg->seq_len, cfg->batch, cfg->batch * cfg->seq_len};
   build_table(&h);

@@ -29,8 +29,8 @@ constexpr int kTcStageBytes = kTcStageA + kTcStageB;  // 48 KB
 constexpr int kTcSmemBytes = kTcStages * kTcStageBytes;
 constexpr int kEpiStageBytes = 32 * 64 * 4;            // per epilogue warp: 32 rows x 64 fp32
 constexpr int kTmemCols = 512;            // two fp32 accumulators of up to 128 x 256
-constexpr int kAdamSub = 2048;            // AdamW: parameters per bulk-copied sub-chunk
-constexpr int kAdamStages = 4;            // AdamW: sub-chunks in flight
+constexpr int kAdamSub = 4096;            // AdamW: parameters per bulk-copied sub-chunk
+constexpr int kAdamStages = 3;            // AdamW: staging buffers (sub-chunks in flight + 1)
 constexpr int kAdamStageBytes = kAdamSub * (4 * 4 + 2);  // p, g, m, v fp32 + bf16 copy
 constexpr int kThreads = 256;     // threads of every persistent block
 constexpr int kWarps = kThreads / 32;

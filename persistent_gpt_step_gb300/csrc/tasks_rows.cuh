@@ -739,9 +739,9 @@ __device__ inline void task_embed_bwd_wpe(const EmbedArgs& a, int idx) {
 // p -= lr (m / bc1) / (sqrt(v / bc2) + eps); bf16 copy of p written if requested.
 // The chunk streams through shared memory in sub-chunks of kAdamSub parameters:
 // one thread issues 1-D bulk copies (cp.async.bulk, completion counted on an
-// mbarrier) of p, g, m and v for up to kAdamStages sub-chunks ahead, all threads
+// mbarrier) of p, g, m and v for kAdamStages - 1 sub-chunks ahead, all threads
 // update a staged sub-chunk in place, and bulk stores write p, m, v and the bf16
-// copy back — about 128 KB in flight per SM without spending registers on it.
+// copy back — about 180 KB in flight per SM without spending registers on it.
 // iter: this block's count of sub-chunks so far (stage = iter mod kAdamStages,
 // phase = (iter / kAdamStages) mod 2), shared by the block's threads.
 __device__ inline void task_adamw(const KParams& kp, const AdamArgs& a, int idx, uint8_t* smem, uint64_t* bars,
@@ -772,10 +772,15 @@ __device__ inline void task_adamw(const KParams& kp, const AdamArgs& a, int idx,
     bulk_load(buf + kAdamSub * 8, a.m + base, bytes, bar);
     bulk_load(buf + kAdamSub * 12, a.v + base, bytes, bar);
   };
+  // Sub-chunk s lives in stage (iter + s) mod kAdamStages.  Loads run
+  // kAdamStages - 1 sub-chunks ahead: the load of s + kAdamStages - 1 goes into
+  // the stage that sub-chunk s - 1 used, whose bulk stores (committed one
+  // iteration earlier) have normally finished reading it already.
+  constexpr int kAhead = kAdamStages - 1;
   if (threadIdx.x == 0) {
     bulk_wait_read_all();  // earlier bulk stores have finished reading these buffers
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    for (int s = 0; s < min(nsub, kAdamStages); ++s) issue(s);
+    for (int s = 0; s < min(nsub, kAhead); ++s) issue(s);
   }
   const float decay = 1.0f - kp.lr * kp.wd * a.decay;
   const float b1 = kp.beta1, b2 = kp.beta2, ib1 = 1.0f - kp.beta1, ib2 = 1.0f - kp.beta2;
@@ -823,15 +828,17 @@ __device__ inline void task_adamw(const KParams& kp, const AdamArgs& a, int idx,
       bulk_store(a.v + base, sb + kAdamSub * 12, bytes);
       if (a.shadow) bulk_store(a.shadow + base, sb + kAdamSub * 16, bytes / 2);
       bulk_commit();
-      if (s + kAdamStages < nsub) {
-        bulk_wait_read_all();  // this stage's stores have read the buffer
-        issue(s + kAdamStages);
+      if (s + kAhead < nsub) {
+        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // sub-chunk s - 1's stores have read its stage
+        issue(s + kAhead);
       }
     }
   }
   if (threadIdx.x == 0) {
-    bulk_wait_all();  // writes complete before the task's release
-    asm volatile("fence.proxy.async.global;" ::: "memory");
+    // Nothing later in the step reads an AdamW result, so only the staging
+    // buffers need to be free before the next task; the stores to global memory
+    // drain in the background (the kernel waits for them before it exits).
+    bulk_wait_read_all();
     *iter = it0 + (uint32_t)nsub;
   }
 }

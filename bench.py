@@ -37,6 +37,35 @@ METRIC = "train tokens/s & ms/step, 162M GPT seq512 b8 on 1 GB300; % bf16 tensor
 UNIT = "tokens/s"
 
 
+def kernel_source_digest() -> str:
+    """sha256 over the kernel's sources (csrc/ and the C header), to tell whether a
+    stored ncu measurement still describes the kernel that runs."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "persistent_gpt_step_gb300", "csrc")
+    files = sorted(os.path.join(csrc, f) for f in os.listdir(csrc)) + [os.path.join(ROOT, "include", "gpt.h")]
+    for f in files:
+        h.update(os.path.relpath(f, ROOT).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes (read + write) of one step launch from the committed ncu capture
+    (profiles/step_kernel_main_traffic.json), or None when that capture was taken
+    on another workload or on kernel sources that have changed since."""
+    path = os.path.join(ROOT, "profiles", "step_kernel_main_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("workload") != workload or rec.get("kernel_source_sha256") != kernel_source_digest():
+        return None
+    return int(rec["dram_bytes_read"]) + int(rec["dram_bytes_write"])
+
+
 def model_flops(cfg, n_params: int) -> float:
     """6 * params * tokens + causal attention (fwd + bwd = 3x fwd; fwd = 2 T^2 d per head)."""
     N = cfg.batch * cfg.seq_len
@@ -286,7 +315,8 @@ def main():
                    "params": n_params, "l2": "working set (~7 GB) > L2; no flush",
                    "tokens": "Zipf(1.1) synthetic, 64 pre-uploaded batches"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tf if peak_tf else None, "traffic": None,
+                     "frac": achieved / peak_tf if peak_tf else None,
+                     "traffic": measured_traffic(workload_name(cfg)),
                      "peak_kind": f"{peak_kind} bf16 burst",
                      "flops_per_launch": flops, "matmul_flops_per_launch": matmul_flops(cfg),
                      "kernel": "pgs::gpt_step_kernel<bf16> (the whole step)",

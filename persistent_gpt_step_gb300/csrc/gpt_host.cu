@@ -909,6 +909,7 @@ size_t smem_needed(const gpt* h) {
   s = std::max(s, (size_t)(2 * 16 * (kSimtTile + 4) * 4));                     // SIMT GEMM
   s = std::max(s, (size_t)(2 * kWarps * D.C * 4));                             // LN backward partials
   s = std::max(s, (size_t)D.N * 16 + 256 * 4);                                 // token sort
+  s = std::max(s, (size_t)(D.N + 3) / 4 * 16 + (size_t)kWarps * D.C * 4);      // embedding backward (wte)
   s = std::max(s, (size_t)(qblock * D.d + 64 * (D.d + 1) + qblock * D.T) * 4); // attention forward
   s = std::max(s, (size_t)(2 * qblock * D.d + 64 * (D.d + 1) + qblock * D.T + qblock) * 4);  // backward
   s = std::max(s, (size_t)kThreads * 4);

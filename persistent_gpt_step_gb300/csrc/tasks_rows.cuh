@@ -674,31 +674,86 @@ __device__ __forceinline__ int lower_bound_i32(const int* a, int n, int key) {
   return lo;
 }
 
+// dwte[v] = sum of dx0 over the occurrences of token v, for a block of vocabulary
+// rows [v0, v1), from the task's slice of the token-sorted positions (stok: the
+// slice's token ids in shared memory).  Rows with fewer than kHotRow occurrences
+// are summed by one warp each, four occurrences in flight; a hot row (Zipf-
+// distributed tokens put hundreds of occurrences on the first few ids) is split
+// over all warps in contiguous slices whose partial sums are then added in warp
+// order — a fixed order, so the result is the same in every step.
+constexpr int kHotRow = 32;
+
 template <int NV>
-__device__ __forceinline__ void wte_rows(const EmbedArgs& a, int v0, int v1, int i0, const int* stok, int nseg) {
+__device__ __forceinline__ void wte_row_sum(const EmbedArgs& a, int i0, int j0, int j1, int lane, float4* acc) {
+#pragma unroll
+  for (int i = 0; i < NV; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  int j = j0;
+  for (; j + 4 <= j1; j += 4) {  // four rows' loads in flight, added in order
+    const float4* s0 = reinterpret_cast<const float4*>(a.dx0 + (int64_t)a.sorted_pos[i0 + j] * a.C);
+    const float4* s1 = reinterpret_cast<const float4*>(a.dx0 + (int64_t)a.sorted_pos[i0 + j + 1] * a.C);
+    const float4* s2 = reinterpret_cast<const float4*>(a.dx0 + (int64_t)a.sorted_pos[i0 + j + 2] * a.C);
+    const float4* s3 = reinterpret_cast<const float4*>(a.dx0 + (int64_t)a.sorted_pos[i0 + j + 3] * a.C);
+    float4 x0[NV], x1[NV], x2[NV], x3[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      x0[i] = s0[lane + 32 * i]; x1[i] = s1[lane + 32 * i]; x2[i] = s2[lane + 32 * i]; x3[i] = s3[lane + 32 * i];
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      acc[i].x += x0[i].x; acc[i].y += x0[i].y; acc[i].z += x0[i].z; acc[i].w += x0[i].w;
+      acc[i].x += x1[i].x; acc[i].y += x1[i].y; acc[i].z += x1[i].z; acc[i].w += x1[i].w;
+      acc[i].x += x2[i].x; acc[i].y += x2[i].y; acc[i].z += x2[i].z; acc[i].w += x2[i].w;
+      acc[i].x += x3[i].x; acc[i].y += x3[i].y; acc[i].z += x3[i].z; acc[i].w += x3[i].w;
+    }
+  }
+  for (; j < j1; ++j) {
+    const float4* src = reinterpret_cast<const float4*>(a.dx0 + (int64_t)a.sorted_pos[i0 + j] * a.C);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const float4 x = src[lane + 32 * i];
+      acc[i].x += x.x; acc[i].y += x.y; acc[i].z += x.z; acc[i].w += x.w;
+    }
+  }
+}
+
+template <int NV>
+__device__ __forceinline__ void wte_rows(const EmbedArgs& a, int v0, int v1, int i0, const int* stok, int nseg,
+                                         float* part) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int v = v0 + warp; v < v1; v += kWarps) {
-    float4 acc[NV > 0 ? NV : 1];
+  if constexpr (NV > 0) {
+    for (int v = v0 + warp; v < v1; v += kWarps) {
+      const int j0 = lower_bound_i32(stok, nseg, v), j1 = lower_bound_i32(stok, nseg, v + 1);
+      if (j1 - j0 >= kHotRow) continue;  // below, by the whole block
+      float4 acc[NV];
+      wte_row_sum<NV>(a, i0, j0, j1, lane, acc);
+      float4* dst = reinterpret_cast<float4*>(a.dwte + (int64_t)v * a.C);
 #pragma unroll
-    for (int i = 0; i < (NV > 0 ? NV : 1); ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    int j = lower_bound_i32(stok, nseg, v);
-    float* dst = a.dwte + (int64_t)v * a.C;
-    if constexpr (NV > 0) {
-      for (; j < nseg && stok[j] == v; ++j) {
-        const float4* src = reinterpret_cast<const float4*>(a.dx0 + (int64_t)a.sorted_pos[i0 + j] * a.C);
+      for (int i = 0; i < NV; ++i) dst[lane + 32 * i] = acc[i];
+    }
+    for (int v = v0; v < v1; ++v) {  // every thread sees the same counts: uniform branches
+      const int j0 = lower_bound_i32(stok, nseg, v), j1 = lower_bound_i32(stok, nseg, v + 1);
+      if (j1 - j0 < kHotRow) continue;
+      const int per = (j1 - j0 + kWarps - 1) / kWarps;
+      const int w0 = min(j1, j0 + warp * per), w1 = min(j1, w0 + per);
+      float4 acc[NV];
+      wte_row_sum<NV>(a, i0, w0, w1, lane, acc);
 #pragma unroll
-        for (int i = 0; i < NV; ++i) {
-          const float4 x = src[lane + 32 * i];
-          acc[i].x += x.x; acc[i].y += x.y; acc[i].z += x.z; acc[i].w += x.w;
-        }
+      for (int i = 0; i < NV; ++i) reinterpret_cast<float4*>(part + warp * a.C)[lane + 32 * i] = acc[i];
+      __syncthreads();
+      for (int c = threadIdx.x; c < a.C; c += kThreads) {
+        float s = part[c];
+        for (int w = 1; w < kWarps; ++w) s += part[w * a.C + c];
+        a.dwte[(int64_t)v * a.C + c] = s;
       }
-#pragma unroll
-      for (int i = 0; i < NV; ++i) reinterpret_cast<float4*>(dst)[lane + 32 * i] = acc[i];
-    } else {
-      const int jb = j;
+      __syncthreads();
+    }
+  } else {
+    for (int v = v0 + warp; v < v1; v += kWarps) {
+      const int jb = lower_bound_i32(stok, nseg, v);
+      float* dst = a.dwte + (int64_t)v * a.C;
       for (int c = lane; c < a.C; c += 32) {
         float s = 0.f;
-        for (j = jb; j < nseg && stok[j] == v; ++j) s += a.dx0[(int64_t)a.sorted_pos[i0 + j] * a.C + c];
+        for (int j = jb; j < nseg && stok[j] == v; ++j) s += a.dx0[(int64_t)a.sorted_pos[i0 + j] * a.C + c];
         dst[c] = s;
       }
     }
@@ -710,14 +765,15 @@ __device__ inline void task_embed_bwd_wte(const KParams& kp, const EmbedArgs& a,
   const int v0 = idx * a.rows_per_task, v1 = min(v0 + a.rows_per_task, a.V);
   const int i0 = a.block_start[idx], nseg = a.block_start[idx + 1] - i0;
   int* stok = smem;
+  float* part = reinterpret_cast<float*>(smem + ((a.N + 3) & ~3));  // [kWarps][C], after a slice of at most N ids
   for (int j = threadIdx.x; j < nseg; j += kThreads) stok[j] = a.sorted_tok[i0 + j];
   __syncthreads();
   switch ((a.C & 127) ? 0 : a.C >> 7) {
-    case 2: wte_rows<2>(a, v0, v1, i0, stok, nseg); break;
-    case 4: wte_rows<4>(a, v0, v1, i0, stok, nseg); break;
-    case 6: wte_rows<6>(a, v0, v1, i0, stok, nseg); break;
-    case 8: wte_rows<8>(a, v0, v1, i0, stok, nseg); break;
-    default: wte_rows<0>(a, v0, v1, i0, stok, nseg); break;
+    case 2: wte_rows<2>(a, v0, v1, i0, stok, nseg, part); break;
+    case 4: wte_rows<4>(a, v0, v1, i0, stok, nseg, part); break;
+    case 6: wte_rows<6>(a, v0, v1, i0, stok, nseg, part); break;
+    case 8: wte_rows<8>(a, v0, v1, i0, stok, nseg, part); break;
+    default: wte_rows<0>(a, v0, v1, i0, stok, nseg, part); break;
   }
 }
 

@@ -123,6 +123,26 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// One AdamW step of one parameter (decoupled weight decay first):
+// p *= decay; m = b1 m + (1-b1) g; v = b2 v + (1-b2) g^2;
+// p -= lr (m / bc1) / (sqrt(v / bc2) + eps).  Shared by the AdamW task and the
+// fused weight-gradient epilogue so both produce the same bits.
+struct AdamHyper {
+  float lr, b1, b2, ib1, ib2, rbc1, rbc2, eps;
+};
+__device__ __forceinline__ AdamHyper adam_hyper(const KParams& kp) {
+  return AdamHyper{kp.lr, kp.beta1, kp.beta2, 1.0f - kp.beta1, 1.0f - kp.beta2, 1.0f / kp.bc1, 1.0f / kp.bc2,
+                   kp.eps};
+}
+__device__ __forceinline__ void adamw_elem(const AdamHyper& hp, float decay, float g, float& p, float& m,
+                                           float& v) {
+  p *= decay;
+  m = hp.b1 * m + hp.ib1 * g;
+  v = hp.b2 * v + hp.ib2 * g * g;
+  const float mh = m * hp.rbc1, vh = v * hp.rbc2;
+  p -= hp.lr * mh / (sqrtf(vh) + hp.eps);
+}
+
 // GELU, tanh form 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) or erf form.
 __device__ __forceinline__ float gelu_f(float x, bool tanh_form) {
   if (tanh_form) {

@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~(uintptr_t)1023);
   const int warp = threadIdx.x >> 5;
-  TcState st = {0u, 0u, 0u, 0u, 0u, 0u, 0u};
+  TcState st = {0u, 0u, 0u, 0u, 0u, 0u};
   if (blockIdx.x == 0 && threadIdx.x == 0) kp.tickets[(kp.epoch + 1ull) & 1ull] = 0ull;  // next launch's
   if (threadIdx.x == 0) {
     for (int i = 0; i < kAdamStages; ++i) mbar_init(smem_u32(&sh.adam_bars[i]), 1);
@@ -48,13 +48,15 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
         mbar_init(smem_u32(&sh.gemm.stage_full[i]), 1);   // producer arrive + tx bytes
         mbar_init(smem_u32(&sh.gemm.stage_empty[i]), 1);  // one MMA commit
       }
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < kQSlots; ++i) {
         mbar_init(smem_u32(&sh.gemm.q_full[i]), 1);     // scheduler publishes a queue entry
-        mbar_init(smem_u32(&sh.gemm.q_empty[i]), 3);    // producer, MMA, epilogue leader took it
+        mbar_init(smem_u32(&sh.gemm.q_empty[i]), 3);    // producer, MMA and releaser are done with it
+        mbar_init(smem_u32(&sh.gemm.tile_done[i]), 4);  // each epilogue warp finished the slot's tile
+      }
+      for (int i = 0; i < 2; ++i) {
         mbar_init(smem_u32(&sh.gemm.acc_full[i]), 1);   // MMA commit: accumulator complete
         mbar_init(smem_u32(&sh.gemm.acc_empty[i]), 4);  // each epilogue warp drained it
       }
-      mbar_init(smem_u32(&sh.gemm.epi_sync), 4);
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }

@@ -839,8 +839,7 @@ __device__ inline void task_adamw(const KParams& kp, const AdamArgs& a, int idx,
     for (int s = 0; s < min(nsub, kAhead); ++s) issue(s);
   }
   const float decay = 1.0f - kp.lr * kp.wd * a.decay;
-  const float b1 = kp.beta1, b2 = kp.beta2, ib1 = 1.0f - kp.beta1, ib2 = 1.0f - kp.beta2;
-  const float rbc1 = 1.0f / kp.bc1, rbc2 = 1.0f / kp.bc2;
+  const AdamHyper hp = adam_hyper(kp);
   for (int s = 0; s < nsub; ++s) {
     const uint32_t st = stage_of(s);
     const uint32_t phase = ((it0 + (uint32_t)s) / kAdamStages) & 1u;
@@ -857,13 +856,7 @@ __device__ inline void task_adamw(const KParams& kp, const AdamArgs& a, int idx,
       float pp[4] = {p.x, p.y, p.z, p.w}, gg[4] = {g.x, g.y, g.z, g.w};
       float mm[4] = {m.x, m.y, m.z, m.w}, vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        pp[e] *= decay;
-        mm[e] = b1 * mm[e] + ib1 * gg[e];
-        vv[e] = b2 * vv[e] + ib2 * gg[e] * gg[e];
-        const float mh = mm[e] * rbc1, vh = vv[e] * rbc2;
-        pp[e] -= kp.lr * mh / (sqrtf(vh) + kp.eps);
-      }
+      for (int e = 0; e < 4; ++e) adamw_elem(hp, decay, gg[e], pp[e], mm[e], vv[e]);
       P[i] = make_float4(pp[0], pp[1], pp[2], pp[3]);
       Mo[i] = make_float4(mm[0], mm[1], mm[2], mm[3]);
       Vo[i] = make_float4(vv[0], vv[1], vv[2], vv[3]);

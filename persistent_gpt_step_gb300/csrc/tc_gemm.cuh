@@ -17,14 +17,13 @@ namespace pgs {
 
 // Pipeline state a block carries across its GEMM runs for the whole launch.
 // Each role thread keeps its own copy and advances only its own fields; the
-// queue, accumulator and epilogue-sync mbarriers are initialised once per
-// launch and these counts give every wait its slot and phase parity.
+// queue, tile-done and accumulator mbarriers are initialised once per launch
+// and these counts give every wait its slot and phase parity.
 struct TcState {
   uint32_t prod_stage, prod_phase;   // producer thread: operand stage ring
   uint32_t mma_stage, mma_phase;     // MMA thread: operand stage ring
   uint32_t q_seq;                    // queue entries published (scheduler) / taken (consumers)
   uint32_t acc_seq;                  // accumulators filled (MMA) / drained (epilogue)
-  uint32_t e_seq;                    // epilogue group syncs (epilogue warps)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -366,44 +365,40 @@ __device__ __forceinline__ bool epilogue_tile(const KParams& kp, const GemmArgs&
 // While a block's current task is a GEMM, its warps split into roles that each
 // loop over the same sequence of GEMM tasks:
 //   warp 2 lane 0  scheduler: claims the next ticket ahead of time, waits for
-//                  its dependencies, hands it over through a 2-slot queue;
+//                  its dependencies, copies the op's arguments into a queue slot
+//                  in shared memory (kQSlots slots);
 //   warp 0 lane 0  TMA producer: k-blocks of A and B into the stage ring;
 //   warp 1 lane 0  MMA issuer: tcgen05.mma into one of two TMEM accumulators;
 //   warps 4..7     epilogue: TMEM -> registers -> fused epilogue -> global,
-//                  then the task's release.
-// Tile i+1's loads and MMAs therefore overlap tile i's epilogue.  The run ends
-// when the scheduler claims a task that is not a GEMM (or the graph ends); that
-// ticket goes back to the main loop, dependencies not yet waited.
+//                  each warp on its own 32 rows, without waiting for the others;
+//   warp 3 lane 0  releaser: once the four epilogue warps are done with a tile,
+//                  publishes it (proxy fence + release add) and frees its slot.
+// Tile i+1's loads and MMAs therefore overlap tile i's epilogue, and no
+// epilogue warp waits for a release to drain its stores.  The run ends when the
+// scheduler claims a task that is not a GEMM (or the graph ends); that ticket
+// goes back to the main loop, dependencies not yet waited.
+constexpr int kQSlots = 2;
+
 struct GemmShared {
   uint64_t stage_full[kTcStages], stage_empty[kTcStages];
   uint64_t acc_full[2], acc_empty[2];
-  uint64_t q_full[2], q_empty[2];
-  uint64_t epi_sync;  // the four epilogue warps meet here after each tile
-  int64_t q_task[2];
+  uint64_t q_full[kQSlots], q_empty[kQSlots];
+  uint64_t tile_done[kQSlots];  // the four epilogue warps finished the slot's tile
+  int64_t q_task[kQSlots];
+  int32_t q_idx[kQSlots], q_sig[kQSlots], q_sig2[kQSlots];
+  GemmArgs q_args[kQSlots];     // the op's arguments, read by every role from here
   int64_t next;
 };
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-// The four epilogue warps meet on an mbarrier (one arrival per warp) rather
-// than a named hardware barrier: the wait is bounded, so a warp that left its
-// loop after a failed wait cannot leave the other three blocked for good.
-// n counts this warp's syncs in the current run (the phase parity).
-__device__ __forceinline__ bool epi_group_sync(const KParams& kp, uint32_t bar, uint32_t& n) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-  const bool ok = mbar_wait(kp, bar, n & 1u);
-  ++n;
-  __syncwarp();
-  return ok;
-}
 
-// The queue slots are rewritten by the scheduler as soon as every role has
-// signalled "slot empty"; a role must therefore read its slot exactly once,
-// before that signal.  Volatile accesses keep the compiler from re-reading
-// the slot later (a plain load may legally be repeated under register
-// pressure, and a repeat after the signal would see the next task).
+// The queue slots are rewritten by the scheduler once the producer, the MMA
+// issuer and the releaser have signalled "slot empty" (the releaser does so only
+// after the epilogue warps finished the slot's tile).  A role reads the slot's
+// task word exactly once; volatile accesses keep the compiler from re-reading it
+// later (a plain load may legally be repeated under register pressure).
 __device__ __forceinline__ int64_t q_read(const int64_t* slot) { return *reinterpret_cast<const volatile int64_t*>(slot); }
 __device__ __forceinline__ void q_write(int64_t* slot, int64_t v) { *reinterpret_cast<volatile int64_t*>(slot) = v; }
 
@@ -421,202 +416,343 @@ __device__ __forceinline__ void role_note(const KParams& kp, int role, uint32_t 
         ((unsigned long long)kind << 56) | ((unsigned long long)(i & 0xffffffu) << 32) | (uint32_t)t;
 }
 
-// Runs GEMM tasks starting with t_first (claimed, dependencies satisfied) and
-// returns the next claimed ticket (not a GEMM, or >= ntasks).
-__device__ inline int64_t gemm_run(const KParams& kp, int64_t t_first, GemmShared& gs, uint8_t* smem_tiles,
-                                   uint32_t tmem_base, TcState& st, bool gelu_tanh) {
+// Queue position of entry seq: its slot and the phase parity of that slot's use.
+__device__ __forceinline__ uint32_t q_slot(uint32_t seq) { return seq % kQSlots; }
+__device__ __forceinline__ uint32_t q_parity(uint32_t seq) { return (seq / kQSlots) & 1u; }
+
+// The epilogue warps' part of a GEMM run (warps 4..7 read TMEM lane quarters
+// 0..3): for each queue entry, wait for the tile's accumulator, run the fused
+// epilogue on the warp's 32 rows, hand the accumulator back to the MMA issuer
+// and tell the releaser the warp is done.  Out of line, so the live state
+// around the epilogue calls is this loop's alone (the epilogue bodies keep their
+// registers).  Returns the updated queue and accumulator sequence counts.
+static __device__ __noinline__ uint2 epilogue_role(const KParams* const kpp, GemmShared& gs, const uint32_t tmem_base,
+                                                   uint8_t* const smem_tiles, uint32_t q_seq, uint32_t acc_seq,
+                                                   const bool gelu_tanh) {
+  const KParams kp = *kpp;  // a value copy: fields stay in registers across asm memory clobbers
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t q_full0 = smem_u32(&gs.q_full[0]), done0 = smem_u32(&gs.tile_done[0]);
+  const uint32_t acc_full0 = smem_u32(&gs.acc_full[0]), acc_empty0 = smem_u32(&gs.acc_empty[0]);
+  const int q = warp & 3;
+  for (uint32_t i = 0;; ++i) {
+    const uint32_t seq = q_seq, slot = q_slot(seq);
+    if (lane == 0) role_note(kp, 3 + q, RW_EPI_QFULL, i, -1);
+    if (!mbar_wait(kp, q_full0 + 8 * slot, q_parity(seq))) break;
+    const int64_t t = q_read(&gs.q_task[slot]);
+    ++q_seq;
+    if (t < 0) {
+      // every use of a slot completes one tile-done phase, the run's last
+      // (non-GEMM) entry included, so the phase parities follow the queue's
+      __syncwarp();
+      if (lane == 0) mbar_arrive(done0 + 8 * slot);
+      break;
+    }
+    const uint32_t acc = acc_seq, buf = acc & 1;
+    ++acc_seq;
+    const GemmArgs& g = gs.q_args[slot];  // valid until the releaser frees the slot, after this tile
+    int tm, tn, split;
+    gemm_coords(g, gs.q_idx[slot], tm, tn, split);
+    if (lane == 0) role_note(kp, 3 + q, RW_EPI_TILE, i, t);
+    const bool ok = epilogue_tile(kp, g, split, tm * kTcBM + q * 32, tn * g.BN,
+                                  tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256,
+                                  smem_tiles + kTcSmemBytes + (warp - 4) * kEpiStageBytes, gelu_tanh,
+                                  acc_full0 + 8 * buf, (acc >> 1) & 1);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(acc_empty0 + 8 * buf);
+      mbar_arrive(done0 + 8 * slot);  // release (CTA scope): this warp's stores precede it
+      role_note(kp, 3 + q, RW_EPI_SYNC, i, t);
+    }
+    if (!ok) break;
+  }
+  return make_uint2(q_seq, acc_seq);
+}
+
+// Scheduler role (warp 2): claims tickets ahead and fills the queue.
+static __device__ __noinline__ TcState scheduler_role(const KParams* const kpp, GemmShared& gs,
+                                                 uint8_t* const smem_tiles, const uint32_t tmem_base, TcState st,
+                                                 const int64_t t_first) {
+  const KParams kp = *kpp;  // a value copy: fields stay in registers across asm memory clobbers
+  const int lane = threadIdx.x & 31;
+  (void)lane;
   const uint32_t q_full0 = smem_u32(&gs.q_full[0]), q_empty0 = smem_u32(&gs.q_empty[0]);
+  const uint32_t done0 = smem_u32(&gs.tile_done[0]);
   const uint32_t acc_full0 = smem_u32(&gs.acc_full[0]), acc_empty0 = smem_u32(&gs.acc_empty[0]);
   const uint32_t full0 = smem_u32(&gs.stage_full[0]), empty0 = smem_u32(&gs.stage_empty[0]);
   const uint32_t tiles0 = smem_u32(smem_tiles);
   const uint8_t* maps = reinterpret_cast<const uint8_t*>(kp.tmaps);  // 128-byte CUtensorMaps
+  (void)q_full0; (void)q_empty0; (void)done0; (void)acc_full0; (void)acc_empty0; (void)full0; (void)empty0;
+  (void)tiles0; (void)maps; (void)tmem_base; (void)t_first;
+  // ---- scheduler: publishes t_first, then claims ahead.  Lane 0 claims and
+  // waits; the whole warp copies the op's arguments into the slot (one 8-byte
+  // word per lane, so no thread holds the whole struct in registers). ----
+  static_assert(sizeof(GemmArgs) % 8 == 0 && sizeof(GemmArgs) <= 32 * 8, "GemmArgs copy");
+  for (uint32_t i = 0;; ++i) {
+    int64_t t = t_first;
+    int gemm = 1, stop = 0;
+    uint32_t slot = 0;
+    if (lane == 0) {
+      const uint32_t seq = st.q_seq;
+      slot = q_slot(seq);
+      role_note(kp, 0, RW_SCHED_QEMPTY, i, t);
+      if (seq >= kQSlots && !mbar_wait(kp, q_empty0 + 8 * slot, q_parity(seq) ^ 1u)) {
+        gs.next = kp.ntasks;
+        stop = 1;
+      }
+      if (!stop && i > 0) {  // claim only once the slot is free: no ticket is held longer than needed
+        t = kp.ntasks;
+        gemm = 0;
+        if (ld_volatile_u32(&kp.err[0]) == 0u) {
+          t = claim_task(kp);
+          if (t < kp.ntasks && kp.ops[kp.tasks[t].op].type == OP_GEMM) {
+            const uint64_t t_claim = kp.trace ? globaltimer_ns() : 0;
+            role_note(kp, 0, RW_SCHED_READY, i, t);
+            gemm = task_ready(kp, t) ? 1 : 0;
+            if (!gemm) t = kp.ntasks;  // a wait failed: stop the run, the main loop drains
+            else if (kp.trace) {
+              kp.trace[4 * t + 0] = t_claim;
+              kp.trace[4 * t + 1] = globaltimer_ns();
+              uint32_t smid;
+              asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+              kp.trace[4 * t + 3] = smid | ((unsigned long long)blockIdx.x << 32);
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    stop = __shfl_sync(0xffffffffu, stop, 0);
+    if (stop) break;
+    gemm = __shfl_sync(0xffffffffu, gemm, 0);
+    t = __shfl_sync(0xffffffffu, t, 0);
+    slot = __shfl_sync(0xffffffffu, slot, 0);
+    if (gemm) {
+      const TaskDesc& d = kp.tasks[t];
+      if (lane < (int)(sizeof(GemmArgs) / 8))
+        reinterpret_cast<uint64_t*>(&gs.q_args[slot])[lane] =
+            reinterpret_cast<const uint64_t*>(&kp.ops[d.op].gemm)[lane];
+      if (lane == 0) {
+        gs.q_idx[slot] = d.idx;
+        gs.q_sig[slot] = d.sig;
+        gs.q_sig2[slot] = d.sig2;
+      }
+    }
+    __syncwarp();  // every lane's copy precedes lane 0's arrival
+    if (lane == 0) {
+      q_write(&gs.q_task[slot], gemm ? t : -2 - t);
+      mbar_arrive(q_full0 + 8 * slot);  // release: the slot's contents precede the arrival
+      ++st.q_seq;
+      if (!gemm) gs.next = t;
+    }
+    if (!gemm) break;
+  }
+  return st;
+}
+
+// TMA producer role (warp 0 lane 0): streams each tile's k-blocks of A and B.
+static __device__ __forceinline__ TcState producer_role(const KParams* const kpp, GemmShared& gs,
+                                                 uint8_t* const smem_tiles, const uint32_t tmem_base, TcState st,
+                                                 const int64_t t_first) {
+  const KParams kp = *kpp;  // a value copy: fields stay in registers across asm memory clobbers
+  const int lane = threadIdx.x & 31;
+  (void)lane;
+  const uint32_t q_full0 = smem_u32(&gs.q_full[0]), q_empty0 = smem_u32(&gs.q_empty[0]);
+  const uint32_t done0 = smem_u32(&gs.tile_done[0]);
+  const uint32_t acc_full0 = smem_u32(&gs.acc_full[0]), acc_empty0 = smem_u32(&gs.acc_empty[0]);
+  const uint32_t full0 = smem_u32(&gs.stage_full[0]), empty0 = smem_u32(&gs.stage_empty[0]);
+  const uint32_t tiles0 = smem_u32(smem_tiles);
+  const uint8_t* maps = reinterpret_cast<const uint8_t*>(kp.tmaps);  // 128-byte CUtensorMaps
+  (void)q_full0; (void)q_empty0; (void)done0; (void)acc_full0; (void)acc_empty0; (void)full0; (void)empty0;
+  (void)tiles0; (void)maps; (void)tmem_base; (void)t_first;
+  if (lane == 0) {
+    // ---- TMA producer ----
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // smem last written by generic stores
+    for (uint32_t i = 0;; ++i) {
+      const uint32_t seq = st.q_seq, slot = q_slot(seq);
+      role_note(kp, 1, RW_PROD_QFULL, i, -1);
+      if (!mbar_wait(kp, q_full0 + 8 * slot, q_parity(seq))) break;
+      const int64_t t = q_read(&gs.q_task[slot]);
+      ++st.q_seq;
+      if (t < 0) {
+        mbar_arrive(q_empty0 + 8 * slot);
+        break;
+      }
+      const GemmArgs& g = gs.q_args[slot];
+      int tm, tn, split;
+      gemm_coords(g, gs.q_idx[slot], tm, tn, split);
+      const int kchunk = (g.K + g.ksplit - 1) / g.ksplit;
+      const int k0 = split * kchunk;
+      const int nkb = (min(g.K, k0 + kchunk) - k0 + kTcBK - 1) / kTcBK;
+      const int m0 = tm * kTcBM, n0 = tn * g.BN;
+      const void* amap = maps + 128 * g.a_map;
+      const void* bmap = maps + 128 * g.b_map;
+      const uint32_t bytes = kTcStageA + (uint32_t)g.BN * kTcBK * 2;
+      const int a_mn = g.a_mn, b_mn = g.b_mn, bn64 = g.BN / 64;
+      mbar_arrive(q_empty0 + 8 * slot);  // everything needed is in registers now
+      role_note(kp, 1, RW_PROD_STAGE, i, t);
+      fence_proxy_async_global();  // operands written by other blocks' generic stores
+      bool ok = true;
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        ok = mbar_wait(kp, empty0 + 8 * st.prod_stage, st.prod_phase ^ 1u);
+        if (!ok) break;
+        const uint32_t full = full0 + 8 * st.prod_stage;
+        mbar_arrive_expect_tx(full, bytes);
+        const uint32_t sa = tiles0 + st.prod_stage * kTcStageBytes;
+        const uint32_t sb = sa + kTcStageA;
+        const int kk = k0 + kb * kTcBK;
+        if (!a_mn) {
+          tma_load_2d(sa, amap, kk, m0, full);
+        } else {
+          tma_load_2d(sa, amap, m0, kk, full);
+          tma_load_2d(sa + 8192, amap, m0 + 64, kk, full);
+        }
+        if (!b_mn) {
+          tma_load_2d(sb, bmap, kk, n0, full);
+        } else {
+          for (int j = 0; j < bn64; ++j) tma_load_2d(sb + 8192 * j, bmap, n0 + 64 * j, kk, full);
+        }
+        if (++st.prod_stage == kTcStages) { st.prod_stage = 0; st.prod_phase ^= 1u; }
+      }
+      if (!ok) break;
+    }
+  }
+  return st;
+}
+
+// MMA issuer role (warp 1 lane 0): one tcgen05.mma chain per tile.
+static __device__ __forceinline__ TcState mma_role(const KParams* const kpp, GemmShared& gs,
+                                                 uint8_t* const smem_tiles, const uint32_t tmem_base, TcState st,
+                                                 const int64_t t_first) {
+  const KParams kp = *kpp;  // a value copy: fields stay in registers across asm memory clobbers
+  const int lane = threadIdx.x & 31;
+  (void)lane;
+  const uint32_t q_full0 = smem_u32(&gs.q_full[0]), q_empty0 = smem_u32(&gs.q_empty[0]);
+  const uint32_t done0 = smem_u32(&gs.tile_done[0]);
+  const uint32_t acc_full0 = smem_u32(&gs.acc_full[0]), acc_empty0 = smem_u32(&gs.acc_empty[0]);
+  const uint32_t full0 = smem_u32(&gs.stage_full[0]), empty0 = smem_u32(&gs.stage_empty[0]);
+  const uint32_t tiles0 = smem_u32(smem_tiles);
+  const uint8_t* maps = reinterpret_cast<const uint8_t*>(kp.tmaps);  // 128-byte CUtensorMaps
+  (void)q_full0; (void)q_empty0; (void)done0; (void)acc_full0; (void)acc_empty0; (void)full0; (void)empty0;
+  (void)tiles0; (void)maps; (void)tmem_base; (void)t_first;
+  if (lane == 0) {
+    // ---- MMA issuer ----
+    for (uint32_t i = 0;; ++i) {
+      const uint32_t seq = st.q_seq, slot = q_slot(seq);
+      role_note(kp, 2, RW_MMA_QFULL, i, -1);
+      if (!mbar_wait(kp, q_full0 + 8 * slot, q_parity(seq))) break;
+      const int64_t t = q_read(&gs.q_task[slot]);
+      ++st.q_seq;
+      if (t < 0) {
+        mbar_arrive(q_empty0 + 8 * slot);
+        break;
+      }
+      const GemmArgs& g = gs.q_args[slot];
+      int tm, tn, split;
+      gemm_coords(g, gs.q_idx[slot], tm, tn, split);
+      const int kchunk = (g.K + g.ksplit - 1) / g.ksplit;
+      const int k0 = split * kchunk;
+      const int nkb = (min(g.K, k0 + kchunk) - k0 + kTcBK - 1) / kTcBK;
+      const uint32_t idesc = idesc_bf16(kTcBM, g.BN, g.a_mn, g.b_mn);
+      const int a_mn = g.a_mn, b_mn = g.b_mn;
+      mbar_arrive(q_empty0 + 8 * slot);
+      role_note(kp, 2, RW_MMA_ACC, i, t);
+      const uint32_t acc = st.acc_seq, buf = acc & 1;
+      if (acc >= 2 && !mbar_wait(kp, acc_empty0 + 8 * buf, ((acc >> 1) - 1) & 1)) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + buf * 256;
+      bool ok = true;
+      role_note(kp, 2, RW_MMA_STAGE, i, t);
+      for (int kb = 0; kb < nkb; ++kb) {
+        ok = mbar_wait(kp, full0 + 8 * st.mma_stage, st.mma_phase);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sa = tiles0 + st.mma_stage * kTcStageBytes;
+        const uint32_t sb = sa + kTcStageA;
+#pragma unroll
+        for (int k = 0; k < kTcBK / 16; ++k) {
+          const uint64_t ad = a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
+                                   : smem_desc_sw128(sa + k * 32, 16, 1024);
+          const uint64_t bd = b_mn ? smem_desc_sw128(sb + k * 2048, 8192, 1024)
+                                   : smem_desc_sw128(sb + k * 32, 16, 1024);
+          tc_mma(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+        }
+        tc_commit(empty0 + 8 * st.mma_stage);  // frees the stage once these MMAs have read it
+        if (++st.mma_stage == kTcStages) { st.mma_stage = 0; st.mma_phase ^= 1u; }
+      }
+      if (!ok) break;
+      tc_commit(acc_full0 + 8 * buf);  // accumulator complete
+      ++st.acc_seq;
+    }
+  }
+  return st;
+}
+
+// Releaser role (warp 3 lane 0): publishes each finished tile and frees its slot.
+static __device__ __noinline__ TcState releaser_role(const KParams* const kpp, GemmShared& gs,
+                                                 uint8_t* const smem_tiles, const uint32_t tmem_base, TcState st,
+                                                 const int64_t t_first) {
+  const KParams kp = *kpp;  // a value copy: fields stay in registers across asm memory clobbers
+  const int lane = threadIdx.x & 31;
+  (void)lane;
+  const uint32_t q_full0 = smem_u32(&gs.q_full[0]), q_empty0 = smem_u32(&gs.q_empty[0]);
+  const uint32_t done0 = smem_u32(&gs.tile_done[0]);
+  const uint32_t acc_full0 = smem_u32(&gs.acc_full[0]), acc_empty0 = smem_u32(&gs.acc_empty[0]);
+  const uint32_t full0 = smem_u32(&gs.stage_full[0]), empty0 = smem_u32(&gs.stage_empty[0]);
+  const uint32_t tiles0 = smem_u32(smem_tiles);
+  const uint8_t* maps = reinterpret_cast<const uint8_t*>(kp.tmaps);  // 128-byte CUtensorMaps
+  (void)q_full0; (void)q_empty0; (void)done0; (void)acc_full0; (void)acc_empty0; (void)full0; (void)empty0;
+  (void)tiles0; (void)maps; (void)tmem_base; (void)t_first;
+  if (lane == 0) {
+    // ---- releaser: publishes finished tiles in order and frees their slots ----
+    for (uint32_t i = 0;; ++i) {
+      const uint32_t seq = st.q_seq, slot = q_slot(seq);
+      if (!mbar_wait(kp, q_full0 + 8 * slot, q_parity(seq))) break;
+      const int64_t t = q_read(&gs.q_task[slot]);
+      ++st.q_seq;
+      if (t < 0) {  // the epilogue warps' arrivals for this entry complete before the run ends
+        mbar_arrive(q_empty0 + 8 * slot);
+        break;
+      }
+      if (!mbar_wait(kp, done0 + 8 * slot, q_parity(seq))) break;
+      if (t != kp.skip_release) {
+        // the four warps' stores precede their arrivals, which this thread has
+        // acquired; the release add makes them visible at gpu scope (and the
+        // proxy fence to the consumers' TMA loads)
+        fence_proxy_async_global();
+        red_release_add_u64(kp.counters + gs.q_sig[slot], 1ull);
+        if (gs.q_sig2[slot] >= 0) red_release_add_u64(kp.counters + gs.q_sig2[slot], 1ull);
+      }
+      if (kp.trace) kp.trace[4 * t + 2] = globaltimer_ns();
+      mbar_arrive(q_empty0 + 8 * slot);
+    }
+  }
+  return st;
+}
+
+// Runs GEMM tasks starting with t_first (claimed, dependencies satisfied) and
+// returns the next claimed ticket (not a GEMM, or >= ntasks).  Every role runs
+// out of line, so each role loop is register-allocated on its own and not
+// together with the rest of the persistent kernel.
+__device__ inline int64_t gemm_run(const KParams& kp, int64_t t_first, GemmShared& gs, uint8_t* smem_tiles,
+                                   uint32_t tmem_base, TcState& st, bool gelu_tanh) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (kp.trace && threadIdx.x == 0) {  // spare role word: runs so far on this block and this run's first task
     unsigned long long* w = kp.trace + 4 * kp.ntasks + 8 * blockIdx.x + 7;
     *w = ((((*w >> 32) & 0xffffffull) + 1) << 32) | (uint32_t)t_first;
   }
-
   if (warp == 2) {
-    if (lane == 0) {
-      // ---- scheduler: publishes t_first, then claims ahead ----
-      for (uint32_t i = 0;; ++i) {
-        int64_t t = t_first;
-        bool gemm = true;
-        if (i > 0) {
-          t = kp.ntasks;
-          gemm = false;
-          if (ld_volatile_u32(&kp.err[0]) == 0u) {
-            t = claim_task(kp);
-            if (t < kp.ntasks && kp.ops[kp.tasks[t].op].type == OP_GEMM) {
-              const uint64_t t_claim = kp.trace ? globaltimer_ns() : 0;
-              role_note(kp, 0, RW_SCHED_READY, i, t);
-              gemm = task_ready(kp, t);
-              if (!gemm) t = kp.ntasks;  // a wait failed: stop the run, the main loop drains
-              else if (kp.trace) {
-                kp.trace[4 * t + 0] = t_claim;
-                kp.trace[4 * t + 1] = globaltimer_ns();
-                uint32_t smid;
-                asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-                kp.trace[4 * t + 3] = smid | ((unsigned long long)blockIdx.x << 32);
-              }
-            }
-          }
-        }
-        const uint32_t seq = st.q_seq, slot = seq & 1;
-        role_note(kp, 0, RW_SCHED_QEMPTY, i, t);
-        if (seq >= 2 && !mbar_wait(kp, q_empty0 + 8 * slot, ((seq >> 1) - 1) & 1)) {
-          gs.next = kp.ntasks;
-          break;
-        }
-        q_write(&gs.q_task[slot], gemm ? t : -2 - t);
-        mbar_arrive(q_full0 + 8 * slot);
-        ++st.q_seq;
-        if (!gemm) {
-          gs.next = t;
-          break;
-        }
-      }
-    }
+    st = scheduler_role(&kp, gs, smem_tiles, tmem_base, st, t_first);
   } else if (warp == 0) {
-    if (lane == 0) {
-      // ---- TMA producer ----
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // smem last written by generic stores
-      for (uint32_t i = 0;; ++i) {
-        const uint32_t seq = st.q_seq, slot = seq & 1;
-        role_note(kp, 1, RW_PROD_QFULL, i, -1);
-        if (!mbar_wait(kp, q_full0 + 8 * slot, (seq >> 1) & 1)) break;
-        const int64_t t = q_read(&gs.q_task[slot]);
-        mbar_arrive(q_empty0 + 8 * slot);
-        ++st.q_seq;
-        if (t < 0) break;
-        role_note(kp, 1, RW_PROD_STAGE, i, t);
-        fence_proxy_async_global();  // operands written by other blocks' generic stores
-        const GemmArgs g = kp.ops[kp.tasks[t].op].gemm;
-        int tm, tn, split;
-        gemm_coords(g, kp.tasks[t].idx, tm, tn, split);
-        const int kchunk = (g.K + g.ksplit - 1) / g.ksplit;
-        const int k0 = split * kchunk;
-        const int nkb = (min(g.K, k0 + kchunk) - k0 + kTcBK - 1) / kTcBK;
-        const int m0 = tm * kTcBM, n0 = tn * g.BN;
-        const void* amap = maps + 128 * g.a_map;
-        const void* bmap = maps + 128 * g.b_map;
-        const uint32_t bytes = kTcStageA + (uint32_t)g.BN * kTcBK * 2;
-        bool ok = true;
-        for (int kb = 0; kb < nkb && ok; ++kb) {
-          ok = mbar_wait(kp, empty0 + 8 * st.prod_stage, st.prod_phase ^ 1u);
-          if (!ok) break;
-          const uint32_t full = full0 + 8 * st.prod_stage;
-          mbar_arrive_expect_tx(full, bytes);
-          const uint32_t sa = tiles0 + st.prod_stage * kTcStageBytes;
-          const uint32_t sb = sa + kTcStageA;
-          const int kk = k0 + kb * kTcBK;
-          if (!g.a_mn) {
-            tma_load_2d(sa, amap, kk, m0, full);
-          } else {
-            tma_load_2d(sa, amap, m0, kk, full);
-            tma_load_2d(sa + 8192, amap, m0 + 64, kk, full);
-          }
-          if (!g.b_mn) {
-            tma_load_2d(sb, bmap, kk, n0, full);
-          } else {
-            for (int j = 0; j < g.BN / 64; ++j) tma_load_2d(sb + 8192 * j, bmap, n0 + 64 * j, kk, full);
-          }
-          if (++st.prod_stage == kTcStages) { st.prod_stage = 0; st.prod_phase ^= 1u; }
-        }
-        if (!ok) break;
-      }
-    }
+    st = producer_role(&kp, gs, smem_tiles, tmem_base, st, t_first);
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ---- MMA issuer ----
-      for (uint32_t i = 0;; ++i) {
-        const uint32_t seq = st.q_seq, slot = seq & 1;
-        role_note(kp, 2, RW_MMA_QFULL, i, -1);
-        if (!mbar_wait(kp, q_full0 + 8 * slot, (seq >> 1) & 1)) break;
-        const int64_t t = q_read(&gs.q_task[slot]);
-        mbar_arrive(q_empty0 + 8 * slot);
-        ++st.q_seq;
-        if (t < 0) break;
-        role_note(kp, 2, RW_MMA_ACC, i, t);
-        const uint32_t acc = st.acc_seq, buf = acc & 1;
-        if (acc >= 2 && !mbar_wait(kp, acc_empty0 + 8 * buf, ((acc >> 1) - 1) & 1)) break;
-        tc_fence_after();
-        const GemmArgs g = kp.ops[kp.tasks[t].op].gemm;
-        int tm, tn, split;
-        gemm_coords(g, kp.tasks[t].idx, tm, tn, split);
-        const int kchunk = (g.K + g.ksplit - 1) / g.ksplit;
-        const int k0 = split * kchunk;
-        const int nkb = (min(g.K, k0 + kchunk) - k0 + kTcBK - 1) / kTcBK;
-        const uint32_t idesc = idesc_bf16(kTcBM, g.BN, g.a_mn, g.b_mn);
-        const uint32_t d_tmem = tmem_base + buf * 256;
-        bool ok = true;
-        role_note(kp, 2, RW_MMA_STAGE, i, t);
-        for (int kb = 0; kb < nkb; ++kb) {
-          ok = mbar_wait(kp, full0 + 8 * st.mma_stage, st.mma_phase);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t sa = tiles0 + st.mma_stage * kTcStageBytes;
-          const uint32_t sb = sa + kTcStageA;
-#pragma unroll
-          for (int k = 0; k < kTcBK / 16; ++k) {
-            const uint64_t ad = g.a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
-                                       : smem_desc_sw128(sa + k * 32, 16, 1024);
-            const uint64_t bd = g.b_mn ? smem_desc_sw128(sb + k * 2048, 8192, 1024)
-                                       : smem_desc_sw128(sb + k * 32, 16, 1024);
-            tc_mma(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-          }
-          tc_commit(empty0 + 8 * st.mma_stage);  // frees the stage once these MMAs have read it
-          if (++st.mma_stage == kTcStages) { st.mma_stage = 0; st.mma_phase ^= 1u; }
-        }
-        if (!ok) break;
-        tc_commit(acc_full0 + 8 * buf);  // accumulator complete
-        ++st.acc_seq;
-      }
-    }
+    st = mma_role(&kp, gs, smem_tiles, tmem_base, st, t_first);
   } else if (warp >= 4) {
-    // ---- epilogue (warps 4..7 read TMEM lane quarters 0..3) ----
-    const int q = warp & 3;
-    const uint32_t esync = smem_u32(&gs.epi_sync);
-    for (uint32_t i = 0;; ++i) {
-      const uint32_t seq = st.q_seq, slot = seq & 1;
-      if (lane == 0) role_note(kp, 3 + q, RW_EPI_QFULL, i, -1);
-      if (!mbar_wait(kp, q_full0 + 8 * slot, (seq >> 1) & 1)) break;
-      const int64_t t = q_read(&gs.q_task[slot]);
-      ++st.q_seq;
-      if (t < 0) {
-        epi_group_sync(kp, esync, st.e_seq);
-        if (warp == 4 && lane == 0) mbar_arrive(q_empty0 + 8 * slot);
-        break;
-      }
-      const uint32_t acc = st.acc_seq, buf = acc & 1;
-      ++st.acc_seq;
-      const GemmArgs g = kp.ops[kp.tasks[t].op].gemm;
-      int tm, tn, split;
-      gemm_coords(g, kp.tasks[t].idx, tm, tn, split);
-      if (lane == 0) role_note(kp, 3 + q, RW_EPI_TILE, i, t);
-      const bool ok = epilogue_tile(kp, g, split, tm * kTcBM + q * 32, tn * g.BN,
-                                    tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256,
-                                    smem_tiles + kTcSmemBytes + (warp - 4) * kEpiStageBytes, gelu_tanh,
-                                    acc_full0 + 8 * buf, (acc >> 1) & 1);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty0 + 8 * buf);
-      if (lane == 0) role_note(kp, 3 + q, RW_EPI_SYNC, i, t);
-      const bool synced = epi_group_sync(kp, esync, st.e_seq);
-      if (warp == 4 && lane == 0 && synced) {
-        mbar_arrive(q_empty0 + 8 * slot);
-        if (t != kp.skip_release) {
-          // the tile's stores by all four warps precede this thread's acquire on
-          // the group sync; the release add below makes them visible at gpu scope
-          // (and the proxy fence to the consumers' TMA loads)
-          fence_proxy_async_global();
-          red_release_add_u64(kp.counters + kp.tasks[t].sig, 1ull);
-          if (kp.tasks[t].sig2 >= 0) red_release_add_u64(kp.counters + kp.tasks[t].sig2, 1ull);
-        }
-        if (kp.trace) kp.trace[4 * t + 2] = globaltimer_ns();
-      }
-      if (!ok || !synced) break;
-    }
+    const uint2 seqs = epilogue_role(&kp, gs, tmem_base, smem_tiles, st.q_seq, st.acc_seq, gelu_tanh);
+    st.q_seq = seqs.x;
+    st.acc_seq = seqs.y;
+  } else {
+    st = releaser_role(&kp, gs, smem_tiles, tmem_base, st, t_first);
   }
   if (lane == 0 && warp != 3 && ld_volatile_u32(&kp.err[0]) == 0u)  // a failed role keeps its last wait
     role_note(kp, warp < 3 ? (warp == 2 ? 0 : warp + 1) : 3 + (warp & 3), RW_DONE, 0, -1);

@@ -278,8 +278,50 @@ def test_checkpoint_resume_is_bitwise():
     assert np.array_equal(pa, pc)
 
 
-def test_bad_token_skips_update():
-    cfg = I.CONFIGS["tiny"]
+def _adamw_reference(cfg, p, m, v, g, t):
+    """AdamW (decoupled decay first, bias correction, weight decay on 2-D
+    tensors only) of the given state with the given gradient, in float64."""
+    p, m, v, g = (x.astype(np.float64) for x in (p, m, v, g))
+    decay = np.ones_like(p)
+    off = 0
+    for _, shape, _ in O.param_table(cfg):
+        n = int(np.prod(shape))
+        if len(shape) == 2 or cfg.wd_on_1d:
+            decay[off:off + n] = 1.0 - cfg.lr * cfg.weight_decay
+        off += n
+    p = p * decay
+    m = cfg.beta1 * m + (1 - cfg.beta1) * g
+    v = cfg.beta2 * v + (1 - cfg.beta2) * g * g
+    mh, vh = m / (1 - cfg.beta1 ** t), v / (1 - cfg.beta2 ** t)
+    return p - cfg.lr * mh / (np.sqrt(vh) + cfg.eps), m, v
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_update_is_adamw_of_the_step_gradients(name):
+    """Every parameter after step 2 is the AdamW update of the state after step 1
+    with step 2's own gradients (bias correction for t = 2, decay on matrices)."""
+    cfg = I.CONFIGS[name]
+    with B.GPT(cfg, seed=21) as mdl:
+        mdl.train_step(*(_dev(x) for x in I.batch(cfg, 21, 0)))
+        p1 = mdl.params()
+        m1, v1, _ = mdl.opt_state()
+        mdl.train_step(*(_dev(x) for x in I.batch(cfg, 21, 1)))
+        g2 = mdl.grads()
+        p2 = mdl.params()
+        m2, v2, t = mdl.opt_state()
+    assert t == 2
+    pe, me, ve = _adamw_reference(cfg, p1, m1, v1, g2, 2)
+    # fp32 rounding, measured against the size of the terms each result is the
+    # sum of (m = b1 m + (1 - b1) g may cancel; v and p may not)
+    m_scale = cfg.beta1 * np.abs(m1.astype(np.float64)) + (1 - cfg.beta1) * np.abs(g2.astype(np.float64))
+    assert np.all(np.abs(m2 - me) <= 1e-6 * m_scale + 1e-30)
+    np.testing.assert_allclose(v2, ve, rtol=1e-5, atol=1e-30)
+    np.testing.assert_allclose(p2, pe, rtol=1e-6, atol=1e-9)
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_bad_token_skips_update(name):
+    cfg = I.CONFIGS[name]
     tok, tgt = I.batch(cfg, 1, 0)
     tok = tok.copy()
     tok[1, 5] = cfg.vocab + 3

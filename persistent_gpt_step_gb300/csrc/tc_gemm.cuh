@@ -388,6 +388,7 @@ struct GemmShared {
   int32_t q_idx[kQSlots], q_sig[kQSlots], q_sig2[kQSlots];
   GemmArgs q_args[kQSlots];     // the op's arguments, read by every role from here
   int64_t next;
+  uint32_t prod_half;           // queue entries whose first half of k-blocks the producer has issued
 };
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -501,6 +502,11 @@ static __device__ __noinline__ TcState scheduler_role(const KParams* const kpp, 
         stop = 1;
       }
       if (!stop && i > 0) {  // claim only once the slot is free: no ticket is held longer than needed
+        // ... and the producer is half-way through the previous entry's k-blocks
+        const uint64_t t0 = globaltimer_ns();
+        while (*reinterpret_cast<volatile uint32_t*>(&gs.prod_half) < st.q_seq) {
+          if (globaltimer_ns() - t0 > kp.timeout_ns) break;  // no error: claiming late is only slower
+        }
         t = kp.ntasks;
         gemm = 0;
         if (ld_volatile_u32(&kp.err[0]) == 0u) {
@@ -594,6 +600,7 @@ static __device__ __forceinline__ TcState producer_role(const KParams* const kpp
       fence_proxy_async_global();  // operands written by other blocks' generic stores
       bool ok = true;
       for (int kb = 0; kb < nkb && ok; ++kb) {
+        if (kb == (3 * nkb) / 4) *reinterpret_cast<volatile uint32_t*>(&gs.prod_half) = st.q_seq;
         ok = mbar_wait(kp, empty0 + 8 * st.prod_stage, st.prod_phase ^ 1u);
         if (!ok) break;
         const uint32_t full = full0 + 8 * st.prod_stage;

@@ -40,11 +40,12 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
+  // the thread may sleep up to 1 us in the instruction until the phase completes
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(1000u)
       : "memory");
   return ok != 0;
 }
@@ -505,6 +506,7 @@ static __device__ __noinline__ TcState scheduler_role(const KParams* const kpp, 
         // ... and the producer is half-way through the previous entry's k-blocks
         const uint64_t t0 = globaltimer_ns();
         while (*reinterpret_cast<volatile uint32_t*>(&gs.prod_half) < st.q_seq) {
+          __nanosleep(64);  // leave the issue slots to the epilogue warp of this sub-partition
           if (globaltimer_ns() - t0 > kp.timeout_ns) break;  // no error: claiming late is only slower
         }
         t = kp.ntasks;

@@ -380,6 +380,50 @@ int make_tmap(gpt* h, const void* base, int64_t inner, int64_t outer, int64_t ld
   return (int)h->tmaps.size() - 1;
 }
 
+// Output map of a GEMM's TMA-store epilogue: rows x cols of bf16 (64-byte
+// swizzle) or fp32 (128-byte swizzle), 32 x 32 boxes (one epilogue warp's rows,
+// one 32-column group).  -1 when the output does not meet the TMA rules (16-byte
+// aligned base and row pitch); the epilogue then stores with generic stores.
+int make_tmap_out(gpt* h, void* base, bool f32, int64_t cols, int64_t rows, int64_t ld) {
+  const int64_t es = f32 ? 4 : 2;
+  if (((uintptr_t)base & 15) || (ld * es) % 16 || cols < 1 || rows < 1) return -1;
+  if (h->describe_only) {
+    h->tmaps.push_back(std::vector<uint8_t>(128, 0));
+    return (int)h->tmaps.size() - 1;
+  }
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return -1;
+  std::vector<uint8_t> buf(128, 0);
+  CUtensorMap* m = reinterpret_cast<CUtensorMap*>(buf.data());
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(ld * es)};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return -1;
+  h->tmaps.push_back(buf);
+  return (int)h->tmaps.size() - 1;
+}
+
+// Gives a tensor-core GEMM op the output map of the TMA-store epilogue where it
+// has one (bf16 store or fp32 store; with a K split the splits' outputs must be
+// stacked row blocks of whole 128-row tiles).
+void set_out_map(gpt* h, OpDesc& op) {
+  if (op.type != OP_GEMM) return;  // (the arguments are a union: only a GEMM op has c_map)
+  GemmArgs& g = op.gemm;
+  g.c_map = -1;
+  if (!is_bf16(h->cfg) || !g.out) return;
+  if (g.epi == EPI_STORE) {
+    g.c_map = make_tmap_out(h, g.out, false, g.N, g.M, g.ldo);
+  } else if (g.epi == EPI_F32) {
+    if (g.ksplit > 1 && (g.M % kTcBM || g.split_stride != (int64_t)g.M * g.ldo)) return;
+    g.c_map = make_tmap_out(h, g.out, true, g.n_real, (int64_t)g.M * g.ksplit, g.ldo);
+  }
+}
+
 // ----------------------------------------------------------------------------
 // Graph builder
 // ----------------------------------------------------------------------------
@@ -469,8 +513,10 @@ struct Builder {
     }
   }
 
-  int add(const OpDesc& op, std::initializer_list<int> deps) {
+  int add(const OpDesc& op_in, std::initializer_list<int> deps) {
     const int id = (int)h->ops.size();
+    OpDesc op = op_in;
+    set_out_map(h, op);
     h->ops.push_back(op);
     int dl[kMaxWaits], nd = 0;
     for (int d : deps) {
@@ -643,7 +689,7 @@ int gemm_op(gpt* h, OpDesc* op, int M, int N, int K, Operand A, Operand B, int e
   g.ksplit = ksplit;
   g.n_real = N;
   g.bias_grad = nullptr;
-  g.a_map = g.b_map = -1;
+  g.a_map = g.b_map = g.c_map = -1;
   if (is_bf16(h->cfg)) {
     g.BM = kTcBM;
     g.BN = pick_bn(M, N, h->num_sms);

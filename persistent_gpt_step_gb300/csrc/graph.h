@@ -74,6 +74,9 @@ struct GemmArgs {
   const void* B; int64_t sbn, sbk;
   // tensor-core path: tensor-map indices and operand majorness (1 = MN-major)
   int32_t a_map, b_map, a_mn, b_mn;
+  // output tensor map for the TMA-store epilogue (EPI_STORE / EPI_F32): 32 x 32
+  // boxes of out, rows split * M + m; -1 = the epilogue stores with generic stores
+  int32_t c_map;
   int32_t epi;
   void* out;  int64_t ldo;   // with ksplit > 1 split s writes out + s * split_stride
   int64_t split_stride;

@@ -82,6 +82,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
+// Stores a 32 x 32 box from shared memory (bulk async-group of this thread).
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t c0, int32_t c1, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(tmap), "r"(c0),
+               "r"(c1), "r"(src)
+               : "memory");
+}
+
 // ---- tcgen05 -----------------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
@@ -240,7 +247,7 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
                                              const float* const bias, const void* const src, const int64_t lds,
                                              const bool gelu_tanh, const int n_real, float* const bias_grad,
                                              const uint32_t acc_bar, const uint32_t acc_parity, uint32_t* const err,
-                                             const uint64_t timeout_ns) {
+                                             const uint64_t timeout_ns, const void* const cmap, const int crow0) {
   constexpr bool kSrc = EPI == EPI_RESID || EPI == EPI_GELU_BWD;
   using SrcT = typename EpiSrc<EPI>::T;
   const int lane = threadIdx.x & 31;
@@ -254,6 +261,72 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
   __syncwarp();  // lanes leave the poll loop separately; tcgen05.ld below is warp-aligned
   if (!acc_ok) return false;
   tc_fence_after();
+  if constexpr (EPI == EPI_STORE || EPI == EPI_F32) {
+    if (cmap) {
+      // TMA-store path: each lane holds its own row's 32 columns, writes them
+      // (bias added and rounded to bf16, or fp32) into a swizzled 32 x 32 box in
+      // the warp's staging area (two boxes, alternating), and lane 0 stores the
+      // box with one bulk tensor copy — one pass through shared memory and no
+      // per-row global stores.
+      const uint32_t sbase = smem_u32(stage);
+      int gi = 0;
+      for (int c = 0; c < cend; c += 32, ++gi) {
+        const int n = n0 + c;
+        uint32_t r[2][16];
+        tmem_ld16_issue(tbase + (uint32_t)c, r[0]);
+        tmem_ld16_issue(tbase + (uint32_t)(c + 16), r[1]);
+        tmem_ld_wait16(r[0]);
+        tmem_ld_wait16(r[1]);
+        if constexpr (EPI == EPI_F32) {
+          if (n >= n_real) {  // the padded columns: the first is the bias gradient, the rest are dropped
+            if (n == n_real && bias_grad && row0 + lane < M) bias_grad[row0 + lane] = __uint_as_float(r[0][0]);
+            continue;
+          }
+        }
+        const uint32_t buf = sbase + (uint32_t)(gi & 1) * 4096u;
+        if (gi >= 2 && lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncwarp();  // the box written two groups ago has been read by its store
+        if constexpr (EPI == EPI_F32) {
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)  // 128-byte rows, 16-byte chunk ch at ch ^ (row mod 8)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 128 + ((ch ^ (lane & 7)) << 4)),
+                         "r"(r[ch >> 2][4 * (ch & 3)]), "r"(r[ch >> 2][4 * (ch & 3) + 1]),
+                         "r"(r[ch >> 2][4 * (ch & 3) + 2]), "r"(r[ch >> 2][4 * (ch & 3) + 3])
+                         : "memory");
+        } else {
+          uint32_t w[16];
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (bias) b = reinterpret_cast<const float4*>(bias + n)[q4];
+            const uint32_t* x = &r[q4 >> 2][4 * (q4 & 3)];
+            __nv_bfloat162 lo = __floats2bfloat162_rn(__uint_as_float(x[0]) + b.x, __uint_as_float(x[1]) + b.y);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(__uint_as_float(x[2]) + b.z, __uint_as_float(x[3]) + b.w);
+            w[2 * q4] = *reinterpret_cast<uint32_t*>(&lo);
+            w[2 * q4 + 1] = *reinterpret_cast<uint32_t*>(&hi);
+          }
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch)  // 64-byte rows, 16-byte chunk ch at ch ^ ((row / 2) mod 4)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
+                         ::"r"(buf + lane * 64 + ((ch ^ ((lane >> 1) & 3)) << 4)), "r"(w[4 * ch]),
+                         "r"(w[4 * ch + 1]), "r"(w[4 * ch + 2]), "r"(w[4 * ch + 3])
+                         : "memory");
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic smem writes -> the bulk copy
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(cmap, n, crow0, buf);
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+      }
+      if (lane == 0) {  // the tile's stores are complete before the warp reports it done
+        asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        fence_proxy_async_global();
+      }
+      __syncwarp();
+      return true;
+    }
+  }
   for (int c = 0; c < cend; c += 32) {
     const int n = n0 + c;
     {
@@ -340,24 +413,26 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
 __device__ __forceinline__ bool epilogue_tile(const KParams& kp, const GemmArgs& g, int split, int row0, int n0,
                                               uint32_t tbase, uint8_t* stage, bool gelu_tanh, uint32_t acc_bar,
                                               uint32_t acc_parity) {
+  const void* const cmap = g.c_map >= 0 ? reinterpret_cast<const uint8_t*>(kp.tmaps) + 128 * g.c_map : nullptr;
+  const int crow0 = row0 + split * g.M;
   switch (g.epi) {
     case EPI_STORE:
       return epi_tile<EPI_STORE>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, g.bias, nullptr,
-                                 0, gelu_tanh, g.N, nullptr, acc_bar, acc_parity, kp.err, kp.timeout_ns);
+                                 0, gelu_tanh, g.N, nullptr, acc_bar, acc_parity, kp.err, kp.timeout_ns, cmap, crow0);
     case EPI_RESID:
       return epi_tile<EPI_RESID>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, g.bias, g.resid,
-                                 g.ldr, gelu_tanh, g.N, nullptr, acc_bar, acc_parity, kp.err, kp.timeout_ns);
+                                 g.ldr, gelu_tanh, g.N, nullptr, acc_bar, acc_parity, kp.err, kp.timeout_ns, cmap, crow0);
     case EPI_GELU:
       return epi_tile<EPI_GELU>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, g.out2, g.ldo2, g.bias,
-                                nullptr, 0, gelu_tanh, g.N, nullptr, acc_bar, acc_parity, kp.err, kp.timeout_ns);
+                                nullptr, 0, gelu_tanh, g.N, nullptr, acc_bar, acc_parity, kp.err, kp.timeout_ns, cmap, crow0);
     case EPI_F32:
       return epi_tile<EPI_F32>(g.M, g.N, g.BN, row0, n0, tbase, stage,
                                reinterpret_cast<float*>(g.out) + split * g.split_stride, g.ldo, nullptr, 0, nullptr,
                                nullptr, 0, gelu_tanh, g.n_real, g.bias_grad, acc_bar, acc_parity, kp.err,
-                               kp.timeout_ns);
+                               kp.timeout_ns, cmap, crow0);
     default:
       return epi_tile<EPI_GELU_BWD>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, nullptr, g.aux,
-                                    g.ldaux, gelu_tanh, g.N, nullptr, acc_bar, acc_parity, kp.err, kp.timeout_ns);
+                                    g.ldaux, gelu_tanh, g.N, nullptr, acc_bar, acc_parity, kp.err, kp.timeout_ns, cmap, crow0);
   }
 }
 

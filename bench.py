@@ -7,7 +7,7 @@ backward and AdamW of the whole model as one persistent kernel launch.  Inputs
 are seeded synthetic Zipf(1.1) token batches (64 distinct batches, pre-uploaded),
 standing in for the tokenized TinyStories stream of the pages; weights are the
 seeded N(0, 0.02) initialisation.  The step's working set (fp32 master weights,
-moments, gradients and activations, ~7 GB) is far larger than L2, so no L2 flush
+moments, gradients and activations: 7 GB for the 162M model) is far larger than L2, so no L2 flush
 is inserted between steps.
 
 Multi-GPU: the step does not shard here (no collective is in scope), so N > 1
@@ -248,6 +248,7 @@ def main():
     dev_batches = [(torch.from_numpy(t).to(dev), torch.from_numpy(g).to(dev)) for t, g in host_batches]
     stream = torch.cuda.current_stream(dev)
     model = B.GPT(cfg, seed=args.seed, stream=stream)
+    arena_gb = model.arena_bytes / 1e9
     n_params = model.n_params
     N = cfg.batch * cfg.seq_len
 
@@ -312,7 +313,7 @@ def main():
         "data": "synthetic",
         "config": {"workload": workload_name(cfg), "global_batch": cfg.batch * world, "seq_len": cfg.seq_len,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
-                   "params": n_params, "l2": "working set (~7 GB) > L2; no flush",
+                   "params": n_params, "l2": f"working set ({arena_gb:.1f} GB arena) > L2; no flush",
                    "tokens": "Zipf(1.1) synthetic, 64 pre-uploaded batches"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": achieved / peak_tf if peak_tf else None,

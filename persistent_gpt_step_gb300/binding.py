@@ -157,6 +157,7 @@ class GPT:
         nbytes = lib.gpt_arena_bytes(byref(self._c))
         if nbytes == 0:
             raise GptError(-1, "invalid or unsupported config")
+        self.arena_bytes = int(nbytes)
         self._arena = torch.empty(nbytes, dtype=torch.uint8, device="cuda") if torch_arena else None
         h = c_void_p()
         rc = lib.gpt_create(byref(self._c), c_uint64(seed), c_void_p(self.stream.cuda_stream),

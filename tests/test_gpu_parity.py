@@ -235,6 +235,15 @@ def test_main_bf16_parity_first_steps():
     assert (np.abs(losses - refs) / np.abs(refs)).max() <= 0.01
 
 
+def test_350m_bf16_parity_first_step():
+    """The 350M scale-up (24 layers, d 1024, 16 heads, seq 1024 x batch 8): step-1 loss
+    within 2e-3 of the fp32 oracle and per-tensor gradient cosine >= 0.999 (one step:
+    the oracle's fp32 step of 8,192 tokens takes about a minute on the host)."""
+    cfg = I.CONFIGS["350m"]
+    losses, refs = _bf16_parity(cfg, 1234, 1, oracle_dtype=np.float32)
+    assert abs(losses[0] - refs[0]) <= 2e-3 * abs(refs[0])
+
+
 # ----------------------------------------------------------------- properties
 
 @pytest.mark.parametrize("name", ["tiny", "small"])

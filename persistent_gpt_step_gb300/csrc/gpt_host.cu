@@ -1087,12 +1087,17 @@ void gpt_default_config(gpt_config* c) {
 
 static int lm_ksplit_for(const gpt_config& c, int num_sms) {
   if (!is_bf16(c)) return 1;
-  // the vocabulary-long reduction of the LM-head input gradient is split so
-  // that its tiles fill at least one wave
+  // The vocabulary-long reduction of the LM-head input gradient (which the
+  // whole backward waits for) is split into the largest number of whole
+  // k-block ranges, at most 8, whose tiles still fit in two waves: for the
+  // 162M step 3 splits (288 tiles) measured 7.92 ms against 8.01 with 2 and
+  // 7.95 with 6.
   const int N = c.batch * c.seq_len;
   const int tiles = (N / kTcBM) * ((c.d_model + 255) / 256);
+  const int kblocks = c.vocab / kTcBK;
   int ks = 1;
-  while (tiles * ks < num_sms && ks < 8 && (c.vocab / kTcBK) % (ks * 2) == 0) ks *= 2;
+  for (int k = 2; k <= 8; ++k)
+    if (kblocks % k == 0 && tiles * k <= 2 * num_sms) ks = k;
   return ks;
 }
 

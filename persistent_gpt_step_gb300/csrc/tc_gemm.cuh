@@ -1,9 +1,10 @@
 // tc_gemm.cuh — bf16 GEMM task on the 5th-generation tensor cores (sm_103a):
 // TMA (cp.async.bulk.tensor, 128-byte swizzle) stages A and B tiles through a
 // multi-stage shared-memory ring guarded by mbarriers; one thread issues
-// tcgen05.mma (kind::f16, bf16 x bf16 -> fp32) into a TMEM accumulator; the
-// block's eight warps read the accumulator back with tcgen05.ld and run the
-// fused epilogue (bias, residual add, GELU, GELU', fp32 or bf16 stores).
+// tcgen05.mma (kind::f16, bf16 x bf16 -> fp32) into one of two TMEM
+// accumulators; four epilogue warps read the other back with tcgen05.ld and run
+// the fused epilogue (bias, residual add, GELU, GELU', fp32 or bf16 stores — the
+// plain stores as bulk tensor copies of 32 x 32 boxes).
 //
 // Operand majorness comes from the UMMA descriptors, not from transposes:
 //   forward       C = X  W^T   A = X  [M,K] K-major,   B = W [N,K] K-major
@@ -485,7 +486,7 @@ __device__ __forceinline__ void q_write(int64_t* slot, int64_t v) { *reinterpret
 // step the host reads where every block's pipeline stopped.
 enum RoleWait : uint32_t {
   RW_SCHED_READY = 1, RW_SCHED_QEMPTY, RW_PROD_QFULL, RW_PROD_STAGE, RW_MMA_QFULL, RW_MMA_ACC, RW_MMA_STAGE,
-  RW_EPI_QFULL, RW_EPI_TILE, RW_EPI_SYNC, RW_DONE
+  RW_EPI_QFULL, RW_EPI_TILE, RW_EPI_DONE, RW_DONE
 };
 __device__ __forceinline__ void role_note(const KParams& kp, int role, uint32_t kind, uint32_t i, int64_t t) {
   if (kp.trace)
@@ -539,7 +540,7 @@ static __device__ __noinline__ uint2 epilogue_role(const KParams* const kpp, Gem
     if (lane == 0) {
       mbar_arrive(acc_empty0 + 8 * buf);
       mbar_arrive(done0 + 8 * slot);  // release (CTA scope): this warp's stores precede it
-      role_note(kp, 3 + q, RW_EPI_SYNC, i, t);
+      role_note(kp, 3 + q, RW_EPI_DONE, i, t);
     }
     if (!ok) break;
   }

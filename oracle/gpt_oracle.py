@@ -369,11 +369,32 @@ class OracleState:
             self.v = np.zeros_like(self.params)
 
 
-def train_step(state: OracleState, tokens, targets) -> float:
-    """Forward, backward and AdamW; returns the pre-update mean loss."""
+def lr_at(step, lr_max, lr_min, warmup, total):
+    """Learning rate of update number ``step`` (1-based) under a linear warmup then
+    cosine decay.
+
+    The record mentions a 4,000-step learning-rate schedule without giving its
+    form ("Open Flapping Airplanes" record, section "Reproducibility needs inputs
+    and an environment record"); the reading here is the common one: for
+    step <= warmup the rate rises linearly, lr_max * step / warmup; from there
+    to ``total`` it follows half a cosine period from lr_max down to lr_min,
+    lr_min + (lr_max - lr_min) (1 + cos(pi (step - warmup) / (total - warmup))) / 2;
+    after ``total`` it stays at lr_min.
+    """
+    if warmup > 0 and step <= warmup:
+        return lr_max * step / warmup
+    if step >= total:
+        return lr_min
+    frac = (step - warmup) / (total - warmup)
+    return lr_min + 0.5 * (lr_max - lr_min) * (1.0 + math.cos(math.pi * frac))
+
+
+def train_step(state: OracleState, tokens, targets, lr=None) -> float:
+    """Forward, backward and AdamW (at learning rate ``lr``, default the config's);
+    returns the pre-update mean loss."""
     loss, cache = forward(state.cfg, state.params, tokens, targets, dtype=state.dtype)
     g = backward(state.cfg, state.params, cache, dtype=state.dtype)
     state.step += 1
-    adamw(state.cfg, state.params, g, state.m, state.v, state.step)
+    adamw(state.cfg, state.params, g, state.m, state.v, state.step, lr=lr)
     state.last_grad = g
     return loss

@@ -281,6 +281,48 @@ def test_adamw_first_two_steps_closed_form():
     assert np.allclose(p, p2, rtol=1e-13, atol=1e-16)
 
 
+def test_adamw_first_two_steps_closed_form_with_scheduled_rates():
+    """The same closed form with a different rate on each step (the rate scales both
+    the decoupled decay and the Adam step of that update only)."""
+    cfg = MICRO
+    rng = np.random.default_rng(9)
+    n = O.num_params(cfg)
+    p0 = rng.normal(0, 1, n)
+    g1, g2 = rng.normal(0, 1e-2, n), rng.normal(0, 1e-2, n)
+    wd, b1, b2, eps = cfg.weight_decay, cfg.beta1, cfg.beta2, cfg.eps
+    lr1, lr2 = 2.5e-4, 7.5e-4
+    dec = O.decay_mask(cfg)
+    p, m, v = p0.copy(), np.zeros(n), np.zeros(n)
+    O.adamw(cfg, p, g1, m, v, 1, lr=lr1)
+    p1 = p0 * (1 - lr1 * wd * dec) - lr1 * g1 / (np.abs(g1) + eps)
+    assert np.allclose(p, p1, rtol=1e-14, atol=1e-16)
+    O.adamw(cfg, p, g2, m, v, 2, lr=lr2)
+    m2 = b1 * (1 - b1) * g1 + (1 - b1) * g2
+    v2 = b2 * (1 - b2) * g1 ** 2 + (1 - b2) * g2 ** 2
+    p2 = p1 * (1 - lr2 * wd * dec) - lr2 * (m2 / (1 - b1 ** 2)) / (np.sqrt(v2 / (1 - b2 ** 2)) + eps)
+    assert np.allclose(p, p2, rtol=1e-13, atol=1e-16)
+
+
+def test_lr_schedule_closed_forms():
+    """Warmup + cosine: linear ramp values, lr_max at the end of the warmup, the mean
+    of lr_max and lr_min half-way through the decay, lr_min at and after the end,
+    the half-period symmetry of the cosine about that midpoint, monotone decay."""
+    hi, lo, w, tot = 6e-4, 6e-5, 100, 4000
+    for t in (1, 37, 100):
+        assert O.lr_at(t, hi, lo, w, tot) == pytest.approx(hi * t / w, rel=1e-15)
+    assert O.lr_at(w, hi, lo, w, tot) == pytest.approx(hi, rel=1e-15)
+    assert O.lr_at(w + (tot - w) // 2, hi, lo, w, tot) == pytest.approx((hi + lo) / 2, rel=1e-12)
+    assert O.lr_at(tot, hi, lo, w, tot) == lo and O.lr_at(tot + 5, hi, lo, w, tot) == lo
+    for x in (1, 250, 1234):
+        a = O.lr_at(w + x, hi, lo, w, tot) - lo
+        b = hi - O.lr_at(tot - x, hi, lo, w, tot)
+        assert a == pytest.approx(b, rel=1e-9)
+    seq = [O.lr_at(t, hi, lo, w, tot) for t in range(w, tot + 1)]
+    assert all(x >= y for x, y in zip(seq, seq[1:]))
+    # no warmup: the first update already follows the cosine, just below lr_max
+    assert lo < O.lr_at(1, hi, lo, 0, tot) < hi
+
+
 def test_decay_mask_is_two_dimensional_tensors():
     cfg = MICRO
     mask = O.decay_mask(cfg)

@@ -286,6 +286,20 @@ def main():
     torch.cuda.synchronize(dev)
     barrier(world)
     t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1000.0, world, dev)
+
+    # ---- the same K steps as one multi-step call (no host sync between steps) ---
+    ring = [dev_batches[(args.warmup + s) % n_batches] for s in range(args.steps)]
+    ring_tok = torch.stack([t for t, _ in ring]).contiguous()
+    ring_tgt = torch.stack([g for _, g in ring]).contiguous()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    m0.record(stream)
+    model.train_steps(ring_tok, ring_tgt)
+    m1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t_multi = max_over_ranks(m0.elapsed_time(m1) / 1000.0, world, dev)
     model.close()
 
     if rank != 0:
@@ -324,6 +338,8 @@ def main():
                      "kernel_ms": 1000 * kern_s},
         "e2e": {"value": world * args.steps * N / t_e2e, "unit": UNIT,
                 "h2d_bytes_per_step": 2 * N * 4, "d2h_bytes_per_step": 4 * 4 + 4},
+        "multi_step_call": {"value": world * args.steps * N / t_multi, "unit": UNIT, "steps_per_call": args.steps,
+                            "ms_per_step": 1000.0 * t_multi / args.steps},
         "gpu_launches": args.steps,
         "clocks": clk,
         "loss_first_last": [losses[0], losses[-1]],

@@ -143,6 +143,49 @@ int gpt_train_step(gpt* h, const int32_t* tokens, const int32_t* targets, float*
  */
 int gpt_train_step_host(gpt* h, const int32_t* tokens, const int32_t* targets, float* loss);
 
+/*
+ * Learning-rate schedule of a multi-step call.  The record mentions a 4,000-step
+ * learning-rate schedule without giving its form ("Open Flapping Airplanes"
+ * record, section "Reproducibility needs inputs and an environment record"); the
+ * reading implemented is linear warmup then cosine decay:
+ *   kind GPT_LR_CONSTANT: every update uses cfg.lr;
+ *   kind GPT_LR_WARMUP_COSINE: update t (1-based count of applied updates) uses
+ *     lr_max * t / warmup_steps              for t <= warmup_steps,
+ *     lr_min + (lr_max - lr_min) (1 + cos(pi (t - warmup_steps) /
+ *                                   (total_steps - warmup_steps))) / 2   up to total_steps,
+ *     lr_min                                 after total_steps.
+ */
+enum { GPT_LR_CONSTANT = 0, GPT_LR_WARMUP_COSINE = 1 };
+typedef struct {
+  int32_t kind;
+  int32_t warmup_steps;  /* >= 0 */
+  int64_t total_steps;   /* > warmup_steps */
+  float lr_max, lr_min;  /* lr_max >= lr_min >= 0 */
+} gpt_lr_schedule;
+
+/*
+ * Host-only: the rate sched gives update number step (>= 1); base_lr is used
+ * for GPT_LR_CONSTANT.  Returns a negative value for an invalid schedule.
+ */
+float gpt_lr_at(const gpt_lr_schedule* sched, float base_lr, int64_t step);
+
+/*
+ * k training steps in one call ("K steps per launch"): step j reads DEVICE
+ * tokens + j*batch*seq_len and targets + j*batch*seq_len (int32 [k, batch,
+ * seq_len], row-major, caller-owned, valid until the call returns) and updates
+ * with the rate sched gives its update number (NULL: cfg.lr).  The k launches
+ * of the persistent kernel are queued back to back on the handle's stream with
+ * no host synchronisation between them: each writes its loss and status into a
+ * device ring, and the host reads the ring once at the end (once every 256
+ * steps for longer calls).  losses: HOST float[k] (may be NULL) receives every
+ * step's pre-update loss.  Errors as gpt_train_step; on BAD_TOKEN or NONFINITE
+ * at step j the steps before j are applied, step j and every later step of the
+ * call leave parameters, moments and the step count unchanged (their losses are
+ * still computed and returned), and gpt_last_error names j.
+ */
+int gpt_train_steps(gpt* h, const int32_t* tokens, const int32_t* targets, int32_t k,
+                    const gpt_lr_schedule* sched, float* losses);
+
 /* Number of parameters (length of every flat parameter-sized vector). */
 size_t gpt_num_params(const gpt* h);
 

@@ -46,6 +46,19 @@ class gpt_config(ctypes.Structure):
     ]
 
 
+class gpt_lr_schedule(ctypes.Structure):
+    _fields_ = [("kind", c_int32), ("warmup_steps", c_int32), ("total_steps", c_int64),
+                ("lr_max", c_float), ("lr_min", c_float)]
+
+
+GPT_LR_CONSTANT, GPT_LR_WARMUP_COSINE = 0, 1
+
+
+def lr_schedule(warmup_steps: int, total_steps: int, lr_max: float, lr_min: float) -> gpt_lr_schedule:
+    """A linear-warmup + cosine-decay schedule for GPT.train_steps."""
+    return gpt_lr_schedule(GPT_LR_WARMUP_COSINE, warmup_steps, total_steps, lr_max, lr_min)
+
+
 class gpt_task_info(ctypes.Structure):
     _fields_ = [("op", c_int32), ("idx", c_int32), ("sig", c_int32), ("sig2", c_int32), ("nwait", c_int32),
                 ("wait_first", c_int32 * 3), ("wait_count", c_int32 * 3), ("wait_need", c_int32 * 3)]
@@ -60,6 +73,8 @@ SIGNATURES = [
     ("gpt_create", c_int, [POINTER(gpt_config), c_uint64, c_void_p, c_void_p, c_size_t, POINTER(c_void_p)]),
     ("gpt_train_step", c_int, [c_void_p, c_void_p, c_void_p, POINTER(c_float)]),
     ("gpt_train_step_host", c_int, [c_void_p, c_void_p, c_void_p, POINTER(c_float)]),
+    ("gpt_lr_at", c_float, [POINTER(gpt_lr_schedule), c_float, c_int64]),
+    ("gpt_train_steps", c_int, [c_void_p, c_void_p, c_void_p, c_int32, POINTER(gpt_lr_schedule), c_void_p]),
     ("gpt_num_params", c_size_t, [c_void_p]),
     ("gpt_num_tensors", c_int, [c_void_p]),
     ("gpt_tensor_info", c_int, [c_void_p, c_int, POINTER(c_char_p), POINTER(c_int64), POINTER(c_size_t)]),
@@ -216,6 +231,25 @@ class GPT:
                                                c_void_p(tgt.ctypes.data), byref(loss))
         self._check(rc)
         return float(loss.value)
+
+    def train_steps(self, tokens, targets, schedule: gpt_lr_schedule | None = None) -> np.ndarray:
+        """k training steps in one call (no host synchronisation between them).
+
+        tokens, targets: CUDA int32 tensors [k, batch, seq_len]; schedule: a
+        gpt_lr_schedule (None: the config's constant rate).  Returns the k
+        pre-update losses; raises GptError as train_step does (the error names
+        the first failing step; the steps before it are applied)."""
+        assert tokens.is_cuda and targets.is_cuda
+        assert tokens.dtype == self._torch.int32 and targets.dtype == self._torch.int32
+        assert tokens.is_contiguous() and targets.is_contiguous() and tokens.shape == targets.shape
+        k = int(tokens.shape[0])
+        out = np.zeros(k, np.float32)
+        rc = self._lib.gpt_train_steps(self._h, c_void_p(tokens.data_ptr()), c_void_p(targets.data_ptr()), k,
+                                       byref(schedule) if schedule is not None else None,
+                                       c_void_p(out.ctypes.data))
+        self.last_losses = out
+        self._check(rc)
+        return out
 
     # -- state ----------------------------------------------------------------
     def params(self) -> np.ndarray:

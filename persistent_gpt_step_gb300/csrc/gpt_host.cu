@@ -93,6 +93,8 @@ struct Dims {
 // ----------------------------------------------------------------------------
 // The handle
 // ----------------------------------------------------------------------------
+constexpr int kStepRing = 256;  // steps of a multi-step call between host reads of the loss ring
+
 struct gpt {
   gpt_config cfg;
   Dims D;
@@ -143,7 +145,15 @@ struct gpt {
   float last_kernel_ms = 0.f;
   unsigned long long* d_trace = nullptr;  // optional per-task timestamps (gpt_trace_enable)
   // host staging (pinned) for the per-step status
-  struct Status { uint32_t err[4]; float loss; uint32_t pad[3]; };
+  struct Status {
+    uint32_t err[4];
+    float loss;
+    uint32_t pad[3];
+    float ring_loss[kStepRing];        // multi-step calls: per-step losses ...
+    uint32_t ring_status[kStepRing];   // ... and soft error bits, read back once per chunk
+  };
+  float* d_loss_ring = nullptr;        // device rings of kStepRing slots (in the metadata allocation)
+  uint32_t* d_status_ring = nullptr;
   Status* h_status = nullptr;
   std::string err;
 };
@@ -1015,8 +1025,11 @@ int reset_counters(gpt* h) {
   return GPT_OK;
 }
 
-int launch_step(gpt* h, const int32_t* tokens, const int32_t* targets, float* loss) {
-  if (h->poisoned) return fail(h, GPT_ERR_POISONED, "handle poisoned by an earlier timeout; call gpt_reset");
+// Queues one launch of the step kernel on the handle's stream (no
+// synchronisation): epoch = launch number, lr and the bias corrections of update
+// number t; loss_out / status_out: ring slots of a multi-step call (or null).
+int enqueue_step(gpt* h, const int32_t* tokens, const int32_t* targets, unsigned long long epoch, float lr,
+                 int64_t t, float* loss_out, uint32_t* status_out) {
   KParams kp;
   std::memset(&kp, 0, sizeof kp);
   kp.tasks = h->d_tasks;
@@ -1024,7 +1037,7 @@ int launch_step(gpt* h, const int32_t* tokens, const int32_t* targets, float* lo
   kp.ops = h->d_ops;
   kp.counters = h->d_counters;
   kp.tickets = h->d_ticket;
-  kp.epoch = h->launches + 1;
+  kp.epoch = epoch;
   kp.err = h->d_err;
   kp.timeout_ns = (uint64_t)(h->cfg.wait_timeout_ms ? h->cfg.wait_timeout_ms : 2000) * 1000000ull;
   kp.skip_release = h->skip_release;
@@ -1032,18 +1045,26 @@ int launch_step(gpt* h, const int32_t* tokens, const int32_t* targets, float* lo
   kp.tokens = tokens;
   kp.targets = targets;
   kp.trace = h->d_trace;
-  kp.lr = h->cfg.lr; kp.beta1 = h->cfg.beta1; kp.beta2 = h->cfg.beta2; kp.eps = h->cfg.eps;
+  kp.loss_out = loss_out;
+  kp.status_out = status_out;
+  kp.lr = lr; kp.beta1 = h->cfg.beta1; kp.beta2 = h->cfg.beta2; kp.eps = h->cfg.eps;
   kp.wd = h->cfg.weight_decay;
-  const double t = (double)(h->opt_step + 1);
-  kp.bc1 = (float)(1.0 - std::pow((double)h->cfg.beta1, t));
-  kp.bc2 = (float)(1.0 - std::pow((double)h->cfg.beta2, t));
+  kp.bc1 = (float)(1.0 - std::pow((double)h->cfg.beta1, (double)t));
+  kp.bc2 = (float)(1.0 - std::pow((double)h->cfg.beta2, (double)t));
   int32_t gelu_tanh = h->cfg.gelu_tanh;
   void* args[2] = {&kp, &gelu_tanh};
   h->skip_release = -1;
-  if (h->ev0) CUDA_TRY(h, cudaEventRecord(h->ev0, h->stream));
   cudaError_t e = cudaLaunchCooperativeKernel(h->kernel, dim3(h->grid), dim3(kThreads), args, h->smem_bytes,
                                               h->stream);
   if (e != cudaSuccess) return fail(h, GPT_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+  return GPT_OK;
+}
+
+int launch_step(gpt* h, const int32_t* tokens, const int32_t* targets, float* loss) {
+  if (h->poisoned) return fail(h, GPT_ERR_POISONED, "handle poisoned by an earlier timeout; call gpt_reset");
+  if (h->ev0) CUDA_TRY(h, cudaEventRecord(h->ev0, h->stream));
+  int rc = enqueue_step(h, tokens, targets, h->launches + 1, h->cfg.lr, h->opt_step + 1, nullptr, nullptr);
+  if (rc != GPT_OK) return rc;
   if (h->ev1) CUDA_TRY(h, cudaEventRecord(h->ev1, h->stream));
   CUDA_TRY(h, cudaMemcpyAsync(h->h_status->err, h->d_err, 4 * sizeof(uint32_t), cudaMemcpyDeviceToHost, h->stream));
   CUDA_TRY(h, cudaMemcpyAsync(&h->h_status->loss, h->loss_dev, sizeof(float), cudaMemcpyDeviceToHost, h->stream));
@@ -1064,6 +1085,77 @@ int launch_step(gpt* h, const int32_t* tokens, const int32_t* targets, float* lo
     return fail(h, GPT_ERR_NONFINITE, "non-finite loss %g", (double)h->h_status->loss);
   }
   h->opt_step++;
+  h->err.clear();
+  return GPT_OK;
+}
+
+bool schedule_ok(const gpt_lr_schedule* s) {
+  if (!s) return true;
+  if (s->kind == GPT_LR_CONSTANT) return true;
+  if (s->kind != GPT_LR_WARMUP_COSINE) return false;
+  return s->warmup_steps >= 0 && s->total_steps > s->warmup_steps && std::isfinite(s->lr_max) &&
+         std::isfinite(s->lr_min) && s->lr_min >= 0.f && s->lr_max >= s->lr_min;
+}
+
+double schedule_lr(const gpt_lr_schedule* s, double base_lr, int64_t t) {
+  if (!s || s->kind == GPT_LR_CONSTANT) return base_lr;
+  if (s->warmup_steps > 0 && t <= s->warmup_steps) return (double)s->lr_max * (double)t / s->warmup_steps;
+  if (t >= s->total_steps) return s->lr_min;
+  const double frac = (double)(t - s->warmup_steps) / (double)(s->total_steps - s->warmup_steps);
+  return s->lr_min + 0.5 * ((double)s->lr_max - s->lr_min) * (1.0 + std::cos(M_PI * frac));
+}
+
+// k steps, queued in chunks of kStepRing launches with one host read per chunk.
+int train_steps(gpt* h, const int32_t* tokens, const int32_t* targets, int32_t k, const gpt_lr_schedule* sched,
+                float* losses) {
+  if (h->poisoned) return fail(h, GPT_ERR_POISONED, "handle poisoned by an earlier timeout; call gpt_reset");
+  const int64_t n = (int64_t)h->D.N;
+  for (int32_t j0 = 0; j0 < k; j0 += kStepRing) {
+    const int32_t kc = std::min<int32_t>(kStepRing, k - j0);
+    if (h->ev0) CUDA_TRY(h, cudaEventRecord(h->ev0, h->stream));
+    for (int32_t j = 0; j < kc; ++j) {
+      const int64_t t = h->opt_step + 1 + j;
+      const int rc = enqueue_step(h, tokens + (j0 + j) * n, targets + (j0 + j) * n, h->launches + 1 + j,
+                                  (float)schedule_lr(sched, h->cfg.lr, t), t, h->d_loss_ring + j,
+                                  h->d_status_ring + j);
+      if (rc != GPT_OK) {  // launches already queued still run: wait for them, then report
+        cudaStreamSynchronize(h->stream);
+        h->poisoned = true;
+        return rc;
+      }
+    }
+    if (h->ev1) CUDA_TRY(h, cudaEventRecord(h->ev1, h->stream));
+    CUDA_TRY(h, cudaMemcpyAsync(h->h_status->err, h->d_err, 4 * sizeof(uint32_t), cudaMemcpyDeviceToHost,
+                                h->stream));
+    CUDA_TRY(h, cudaMemcpyAsync(h->h_status->ring_loss, h->d_loss_ring, kc * sizeof(float),
+                                cudaMemcpyDeviceToHost, h->stream));
+    CUDA_TRY(h, cudaMemcpyAsync(h->h_status->ring_status, h->d_status_ring, kc * sizeof(uint32_t),
+                                cudaMemcpyDeviceToHost, h->stream));
+    CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+    if (h->ev0 && h->ev1) cudaEventElapsedTime(&h->last_kernel_ms, h->ev0, h->ev1);
+    const uint32_t fatal = h->h_status->err[0];
+    if (fatal) {
+      h->poisoned = true;
+      return fail(h, GPT_ERR_TIMEOUT, "device wait timed out in steps %d..%d of the call (code %u, task %u, "
+                  "counter/barrier %u)", j0, j0 + kc - 1, fatal, h->h_status->err[2], h->h_status->err[3]);
+    }
+    h->launches += kc;
+    if (losses) std::memcpy(losses + j0, h->h_status->ring_loss, kc * sizeof(float));
+    int32_t good = kc;
+    for (int32_t j = 0; j < kc; ++j)
+      if (h->h_status->ring_status[j]) { good = j; break; }
+    h->opt_step += good;
+    if (good < kc) {  // the soft flag stayed raised for the rest of the chunk: no later update applied
+      const uint32_t soft = h->h_status->ring_status[good];
+      CUDA_TRY(h, cudaMemsetAsync(h->d_err + 1, 0, sizeof(uint32_t), h->stream));
+      CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+      if (soft & kSoftBadToken)
+        return fail(h, GPT_ERR_BAD_TOKEN, "token or target id outside [0, vocab) at step %d of the call",
+                    j0 + good);
+      return fail(h, GPT_ERR_NONFINITE, "non-finite loss %g at step %d of the call",
+                  (double)h->h_status->ring_loss[good], j0 + good);
+    }
+  }
   h->err.clear();
   return GPT_OK;
 }
@@ -1179,6 +1271,7 @@ int gpt_create(const gpt_config* cfg, uint64_t seed, void* cuda_stream, void* ar
   const size_t o_tic = mb.take(2 * sizeof(unsigned long long));
   const size_t o_err = mb.take(4 * sizeof(uint32_t));
   const size_t o_tok = mb.take(2 * (size_t)h->D.N * sizeof(int32_t));
+  const size_t o_ring = mb.take((size_t)kStepRing * (sizeof(float) + sizeof(uint32_t)));
   h->meta_bytes = mb.off;
   if (cudaMalloc(&h->meta, h->meta_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -1192,6 +1285,8 @@ int gpt_create(const gpt_config* cfg, uint64_t seed, void* cuda_stream, void* ar
   h->d_ticket = reinterpret_cast<unsigned long long*>(h->meta + o_tic);
   h->d_err = reinterpret_cast<uint32_t*>(h->meta + o_err);
   h->d_tok_stage = reinterpret_cast<int32_t*>(h->meta + o_tok);
+  h->d_loss_ring = reinterpret_cast<float*>(h->meta + o_ring);
+  h->d_status_ring = reinterpret_cast<uint32_t*>(h->meta + o_ring + (size_t)kStepRing * sizeof(float));
   if (cudaMallocHost(&h->h_status, sizeof(gpt::Status)) != cudaSuccess) {
     cudaGetLastError();
     fail(h, GPT_ERR_OOM, "pinned host allocation failed");
@@ -1261,6 +1356,19 @@ int gpt_train_step_host(gpt* h, const int32_t* tokens, const int32_t* targets, f
   CUDA_TRY(h, cudaMemcpyAsync(h->d_tok_stage, tokens, n * 4, cudaMemcpyHostToDevice, h->stream));
   CUDA_TRY(h, cudaMemcpyAsync(h->d_tok_stage + n, targets, n * 4, cudaMemcpyHostToDevice, h->stream));
   return launch_step(h, h->d_tok_stage, h->d_tok_stage + n, loss);
+}
+
+float gpt_lr_at(const gpt_lr_schedule* sched, float base_lr, int64_t step) {
+  if (!schedule_ok(sched) || step < 1) return -1.0f;
+  return (float)schedule_lr(sched, base_lr, step);
+}
+
+int gpt_train_steps(gpt* h, const int32_t* tokens, const int32_t* targets, int32_t k,
+                    const gpt_lr_schedule* sched, float* losses) {
+  if (!h) return GPT_ERR_INVALID_ARG;
+  if (!tokens || !targets || k < 1) return fail(h, GPT_ERR_INVALID_ARG, "tokens/targets must be device pointers, k >= 1");
+  if (!schedule_ok(sched)) return fail(h, GPT_ERR_INVALID_ARG, "invalid learning-rate schedule");
+  return train_steps(h, tokens, targets, k, sched, losses);
 }
 
 size_t gpt_num_params(const gpt* h) { return h ? h->nparams : 0; }

@@ -204,6 +204,8 @@ struct KParams {
   const int32_t* tokens; const int32_t* targets;
   float lr, beta1, beta2, eps, wd, bc1, bc2;
   unsigned long long* trace;       // optional [ntasks][4]: claim, start, end (globaltimer ns), SM id
+  float* loss_out;                 // multi-step calls: this launch's slot of the loss ring (else null)
+  uint32_t* status_out;            // ... and of the status ring (the soft error bits after the loss)
 };
 
 }  // namespace pgs

@@ -534,6 +534,10 @@ __device__ inline void task_loss(const KParams& kp, const LossArgs& a, float* sm
     const float loss = smem[0] / (float)a.N;
     *a.loss = loss;
     if (!isfinite(loss)) set_soft(kp, kSoftNonFinite);
+    // multi-step calls: the loss and the soft error bits of this step (every
+    // cross-entropy row, which raises them, precedes this task) into the rings
+    if (kp.loss_out) *kp.loss_out = loss;
+    if (kp.status_out) *kp.status_out = ld_volatile_u32(&kp.err[1]);
   }
 }
 

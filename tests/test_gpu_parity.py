@@ -244,6 +244,67 @@ def test_350m_bf16_parity_first_step():
     assert abs(losses[0] - refs[0]) <= 2e-3 * abs(refs[0])
 
 
+def _ring(cfg, seed, steps):
+    """k steps of (tokens, targets) as [k, B, T] CUDA tensors."""
+    b = [I.batch(cfg, seed, s) for s in range(steps)]
+    return _dev(np.stack([x[0] for x in b])), _dev(np.stack([x[1] for x in b])), b
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_multi_step_call_equals_single_steps(name):
+    """k steps in one call (constant rate) give bitwise the losses and state of k
+    single-step calls."""
+    cfg = I.CONFIGS[name]
+    tok, tgt, b = _ring(cfg, 17, 4)
+    with B.GPT(cfg, seed=17) as a, B.GPT(cfg, seed=17) as c:
+        la = [a.train_step(_dev(t), _dev(g)) for t, g in b]
+        lc = c.train_steps(tok, tgt)
+        assert [float(x) for x in lc] == la
+        assert np.array_equal(a.params(), c.params())
+        assert a.opt_state()[2] == c.opt_state()[2] == 4
+        ma, va, _ = a.opt_state()
+        mc, vc, _ = c.opt_state()
+        assert np.array_equal(ma, mc) and np.array_equal(va, vc)
+
+
+def test_multi_step_schedule_parity_tiny_fp32():
+    """Ten steps in one call under warmup + cosine (3 warmup updates, decay to 1e-4
+    at update 10) against the fp64 oracle with the same schedule: per-step loss
+    within 1e-4 relative, parameters within 1e-4 after the ten steps."""
+    cfg = I.CONFIGS["tiny"]
+    seed, k, w, hi, lo = 1234, 10, 3, 1e-3, 1e-4
+    params = I.init_params(O.param_table(cfg), seed)
+    st = O.OracleState(cfg, params, dtype=np.float64)
+    tok, tgt, b = _ring(cfg, seed, k)
+    with B.GPT(cfg, seed=seed) as m:
+        m.set_params(params)
+        losses = m.train_steps(tok, tgt, B.lr_schedule(w, k, hi, lo))
+        p = m.params()
+        assert m.opt_state()[2] == k
+    hi32, lo32 = float(np.float32(hi)), float(np.float32(lo))
+    for s, (t, g) in enumerate(b):
+        ref = O.train_step(st, t, g, lr=O.lr_at(s + 1, hi32, lo32, w, k))
+        assert abs(losses[s] - ref) <= 1e-4 * abs(ref), (s, losses[s], ref)
+    assert np.abs(p - st.params).max() <= 1e-4
+
+
+def test_multi_step_bad_token_stops_updates_at_that_step():
+    cfg = I.CONFIGS["tiny"]
+    tok, tgt, b = _ring(cfg, 5, 4)
+    tok[2, 1, 7] = cfg.vocab + 1  # step 2 of the call
+    with B.GPT(cfg, seed=5) as a, B.GPT(cfg, seed=5) as c:
+        for t, g in b[:2]:
+            a.train_step(_dev(t), _dev(g))
+        with pytest.raises(B.GptError) as e:
+            c.train_steps(tok, tgt)
+        assert e.value.name == "BAD_TOKEN" and "step 2" in str(e.value)
+        assert c.opt_state()[2] == 2
+        assert np.array_equal(a.params(), c.params())
+        assert np.isfinite(c.last_losses).all()
+        c.train_step(_dev(b[3][0]), _dev(b[3][1]))  # the handle stays usable
+        assert c.opt_state()[2] == 3
+
+
 # ----------------------------------------------------------------- properties
 
 @pytest.mark.parametrize("name", ["tiny", "small"])

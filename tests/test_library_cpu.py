@@ -120,6 +120,26 @@ def test_library_tensor_table_and_host_init_match_spec(lib, name):
         assert ulp.max() <= 1
 
 
+def test_library_lr_schedule_matches_oracle(lib):
+    """The host-side schedule the multi-step call uses against the oracle's
+    (independently written) warmup + cosine schedule, and invalid schedules."""
+    from ctypes import byref
+    from oracle import gpt_oracle as O
+    hi, lo, w, tot = 6e-4, 6e-5, 100, 4000
+    s = B.lr_schedule(w, tot, hi, lo)
+    hi32, lo32 = float(np.float32(hi)), float(np.float32(lo))
+    for t in list(range(1, 130)) + [1000, 2050, 3998, 3999, 4000, 4001, 10 ** 6]:
+        want = O.lr_at(t, hi32, lo32, w, tot)
+        assert lib.gpt_lr_at(byref(s), 1.0, t) == pytest.approx(want, rel=2e-7, abs=1e-12), t
+    assert lib.gpt_lr_at(None, 2.5e-4, 7) == pytest.approx(2.5e-4, rel=1e-7)
+    assert lib.gpt_lr_at(byref(B.gpt_lr_schedule(B.GPT_LR_CONSTANT, 0, 1, 0.0, 0.0)), 1e-3, 3) == \
+        pytest.approx(1e-3, rel=1e-7)
+    for bad in (B.gpt_lr_schedule(7, 0, 10, 1e-3, 0.0), B.gpt_lr_schedule(1, 10, 10, 1e-3, 0.0),
+                B.gpt_lr_schedule(1, 1, 10, 1e-4, 1e-3), B.gpt_lr_schedule(1, -1, 10, 1e-3, 0.0)):
+        assert lib.gpt_lr_at(byref(bad), 1e-3, 1) < 0
+    assert lib.gpt_lr_at(byref(s), 1e-3, 0) < 0
+
+
 def test_init_statistics():
     w = I.normal_fp32(42, 3, 200000)
     assert abs(w.mean()) < 0.02 * 0.02

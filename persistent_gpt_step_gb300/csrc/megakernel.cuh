@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
         mbar_init(smem_u32(&sh.gemm.acc_full[i]), 1);   // MMA commit: accumulator complete
         mbar_init(smem_u32(&sh.gemm.acc_empty[i]), 4);  // each epilogue warp drained it
       }
-      sh.gemm.prod_half = 0;
+      sh.gemm.prod_claim = 0;
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }

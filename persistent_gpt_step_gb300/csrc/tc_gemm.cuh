@@ -441,9 +441,11 @@ __device__ __forceinline__ bool epilogue_tile(const KParams& kp, const GemmArgs&
 //
 // While a block's current task is a GEMM, its warps split into roles that each
 // loop over the same sequence of GEMM tasks:
-//   warp 2 lane 0  scheduler: claims the next ticket ahead of time, waits for
-//                  its dependencies, copies the op's arguments into a queue slot
-//                  in shared memory (kQSlots slots);
+//   warp 2         scheduler: lane 0 claims the next ticket once a queue slot
+//                  is free and the producer has issued three quarters of the
+//                  current tile's k-blocks (a ticket held but not started is work
+//                  no other block can take), waits for its dependencies, and the
+//                  warp copies the op's arguments into the slot in shared memory;
 //   warp 0 lane 0  TMA producer: k-blocks of A and B into the stage ring;
 //   warp 1 lane 0  MMA issuer: tcgen05.mma into one of two TMEM accumulators;
 //   warps 4..7     epilogue: TMEM -> registers -> fused epilogue -> global,
@@ -465,7 +467,7 @@ struct GemmShared {
   int32_t q_idx[kQSlots], q_sig[kQSlots], q_sig2[kQSlots];
   GemmArgs q_args[kQSlots];     // the op's arguments, read by every role from here
   int64_t next;
-  uint32_t prod_half;           // queue entries whose first half of k-blocks the producer has issued
+  uint32_t prod_claim;          // queue entries for which the producer has passed the claim point
 };
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -579,9 +581,9 @@ static __device__ __noinline__ TcState scheduler_role(const KParams* const kpp, 
         stop = 1;
       }
       if (!stop && i > 0) {  // claim only once the slot is free: no ticket is held longer than needed
-        // ... and the producer is half-way through the previous entry's k-blocks
+        // ... and the producer has issued three quarters of the previous entry's k-blocks
         const uint64_t t0 = globaltimer_ns();
-        while (*reinterpret_cast<volatile uint32_t*>(&gs.prod_half) < st.q_seq) {
+        while (*reinterpret_cast<volatile uint32_t*>(&gs.prod_claim) < st.q_seq) {
           __nanosleep(64);  // leave the issue slots to the epilogue warp of this sub-partition
           if (globaltimer_ns() - t0 > kp.timeout_ns) break;  // no error: claiming late is only slower
         }
@@ -678,7 +680,7 @@ static __device__ __forceinline__ TcState producer_role(const KParams* const kpp
       fence_proxy_async_global();  // operands written by other blocks' generic stores
       bool ok = true;
       for (int kb = 0; kb < nkb && ok; ++kb) {
-        if (kb == (3 * nkb) / 4) *reinterpret_cast<volatile uint32_t*>(&gs.prod_half) = st.q_seq;
+        if (kb == (3 * nkb) / 4) *reinterpret_cast<volatile uint32_t*>(&gs.prod_claim) = st.q_seq;
         ok = mbar_wait(kp, empty0 + 8 * st.prod_stage, st.prod_phase ^ 1u);
         if (!ok) break;
         const uint32_t full = full0 + 8 * st.prod_stage;

@@ -30,9 +30,18 @@ b_qkv [3C], w_o [C,C], b_o [C], ln2_g, ln2_b, w_1 [F,C], b_1 [F], w_2 [C,F],
 b_2 [C]; then lnf_g, lnf_b, w_lm [V,C].  Weight matrices are stored
 [out_features, in_features]; a linear layer computes y = x W^T + b.
 
+The RTX 3090 page's 57.7M model ("Coppelius training on the RTX 3090": RoPE on
+q/k, gated-GELU FFN, tied embedding and LM head) is the same model with three
+switches: ``rope`` rotates each head's dimension pairs (2i, 2i+1) of q and k by
+t * 10000^(-2i/d) at position t and drops wpe; ``gated_mlp`` replaces w_1 / b_1
+by w_gu [2F,C] / b_gu [2F] whose rows 2f and 2f+1 are the gate and up
+projections of feature f, the MLP output being GELU(gate) * up; and
+``tie_embeddings`` drops w_lm, the LM head using wte.
+
 Pins (see tests/test_oracle.py): central finite differences in float64 on the
-tiny model, an independent float64 autograd re-derivation with PyTorch CPU
-operators, the know-nothing loss ln V printed on the Coppelius page, loss near
+tiny model and its gated / RoPE / tied variant, an independent float64 autograd
+re-derivation with PyTorch CPU operators (rotary embedding as a complex
+product), the rotary embedding's norm and relative-position properties, the know-nothing loss ln V printed on the Coppelius page, loss near
 ln V at initialisation, softmax rows summing to one, the closed form of the
 first two AdamW steps, causality, T = 1 attention, LayerNorm moments, and the
 parameter counts printed on the pages.
@@ -64,7 +73,12 @@ def param_table(cfg):
     Airplanes" record, "What ran" and "Reproduce the run").
     """
     C, F, V, T = cfg.d_model, cfg.d_mlp, cfg.vocab, cfg.seq_len
-    tab = [("wte", (V, C), "normal"), ("wpe", (T, C), "normal")]
+    rope = getattr(cfg, "rope", False)
+    gated = getattr(cfg, "gated_mlp", False)
+    tied = getattr(cfg, "tie_embeddings", False)
+    tab = [("wte", (V, C), "normal")]
+    if not rope:
+        tab.append(("wpe", (T, C), "normal"))
     for l in range(cfg.n_layer):
         p = f"h{l}."
         tab.append((p + "ln1_g", (C,), "ones"))
@@ -79,16 +93,20 @@ def param_table(cfg):
         tab.append((p + "ln2_g", (C,), "ones"))
         if cfg.ln_bias:
             tab.append((p + "ln2_b", (C,), "zeros"))
-        tab.append((p + "w_1", (F, C), "normal"))
+        if gated:  # rows 2f and 2f+1: gate and up projection of feature f
+            tab.append((p + "w_gu", (2 * F, C), "normal"))
+        else:
+            tab.append((p + "w_1", (F, C), "normal"))
         if cfg.linear_bias:
-            tab.append((p + "b_1", (F,), "zeros"))
+            tab.append((p + ("b_gu" if gated else "b_1"), (2 * F if gated else F,), "zeros"))
         tab.append((p + "w_2", (C, F), "normal"))
         if cfg.linear_bias:
             tab.append((p + "b_2", (C,), "zeros"))
     tab.append(("lnf_g", (C,), "ones"))
     if cfg.ln_bias:
         tab.append(("lnf_b", (C,), "zeros"))
-    tab.append(("w_lm", (V, C), "normal"))
+    if not tied:
+        tab.append(("w_lm", (V, C), "normal"))
     return tab
 
 
@@ -215,6 +233,23 @@ def cross_entropy(z, targets):
 # Forward / backward of the whole model
 # --------------------------------------------------------------------------- #
 
+def rope_angles(T, d, base=10000.0):
+    """theta[t, i] = t * base^(-2i/d): the rotation angle of pair i at position t
+    (rotary position embedding, pairs (2i, 2i+1) of each head's dimensions)."""
+    i = np.arange(d // 2, dtype=np.float64)
+    return np.arange(T, dtype=np.float64)[:, None] * base ** (-2.0 * i / d)[None, :]
+
+
+def rope_rotate(x, theta, sign=1.0):
+    """Rotates pairs (2i, 2i+1) of the last axis of x [..., T, d] by sign * theta[T, d/2]."""
+    c, s = np.cos(theta), sign * np.sin(theta)
+    x0, x1 = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = x0 * c - x1 * s
+    out[..., 1::2] = x0 * s + x1 * c
+    return out
+
+
 def _split_heads(x, B, T, H):
     # [B*T, C] -> [B, H, T, d]
     d = x.shape[1] // H
@@ -237,10 +272,16 @@ def forward(cfg, params: np.ndarray, tokens: np.ndarray, targets: np.ndarray,
     assert T <= cfg.seq_len
     C, H = cfg.d_model, cfg.n_head
     P = param_views(cfg, np.asarray(params, dtype=dtype))
+    rope = getattr(cfg, "rope", False)
+    gated = getattr(cfg, "gated_mlp", False)
+    tied = getattr(cfg, "tie_embeddings", False)
     tok = tokens.reshape(-1)
     pos = np.tile(np.arange(T), B)
-    x = P["wte"][tok] + P["wpe"][pos]
-    cache = {"x0": x, "tok": tok, "pos": pos, "B": B, "T": T, "layers": []}
+    x = P["wte"][tok]
+    if not rope:
+        x = x + P["wpe"][pos]
+    theta = rope_angles(T, C // H) if rope else None
+    cache = {"x0": x, "tok": tok, "pos": pos, "B": B, "T": T, "layers": [], "theta": theta}
     for l in range(cfg.n_layer):
         p = f"h{l}."
         lc = {"x_in": x}
@@ -249,6 +290,8 @@ def forward(cfg, params: np.ndarray, tokens: np.ndarray, targets: np.ndarray,
         if cfg.linear_bias:
             qkv = qkv + P[p + "b_qkv"]
         q, k, v = (_split_heads(qkv[:, i * C:(i + 1) * C], B, T, H) for i in range(3))
+        if rope:
+            q, k = rope_rotate(q, theta), rope_rotate(k, theta)
         o, pr = causal_attention(q, k, v)
         o = _merge_heads(o)
         y = o @ P[p + "w_o"].T
@@ -256,10 +299,17 @@ def forward(cfg, params: np.ndarray, tokens: np.ndarray, targets: np.ndarray,
             y = y + P[p + "b_o"]
         x_mid = x + y
         a2, lc["xhat2"], lc["rstd2"] = layernorm(x_mid, P[p + "ln2_g"], P.get(p + "ln2_b"), cfg.ln_eps)
-        h = a2 @ P[p + "w_1"].T
-        if cfg.linear_bias:
-            h = h + P[p + "b_1"]
-        g = gelu(h, cfg.gelu_tanh)
+        if gated:
+            hg = a2 @ P[p + "w_gu"].T
+            if cfg.linear_bias:
+                hg = hg + P[p + "b_gu"]
+            h = hg               # [N, 2F]: gate (even columns) and up (odd columns)
+            g = gelu(hg[:, 0::2], cfg.gelu_tanh) * hg[:, 1::2]
+        else:
+            h = a2 @ P[p + "w_1"].T
+            if cfg.linear_bias:
+                h = h + P[p + "b_1"]
+            g = gelu(h, cfg.gelu_tanh)
         y2 = g @ P[p + "w_2"].T
         if cfg.linear_bias:
             y2 = y2 + P[p + "b_2"]
@@ -268,7 +318,7 @@ def forward(cfg, params: np.ndarray, tokens: np.ndarray, targets: np.ndarray,
         if keep:
             cache["layers"].append(lc)
     af, cache["xhatf"], cache["rstdf"] = layernorm(x, P["lnf_g"], P.get("lnf_b"), cfg.ln_eps)
-    z = af @ P["w_lm"].T
+    z = af @ P["wte" if tied else "w_lm"].T
     loss, rows, dz = cross_entropy(z, targets.reshape(-1))
     cache.update(af=af, z=z, rows=rows, dz=dz, x_final=x)
     return float(loss), (cache if keep else None)
@@ -280,9 +330,13 @@ def backward(cfg, params: np.ndarray, cache, dtype=np.float64) -> np.ndarray:
     grad = np.zeros(num_params(cfg), dtype=dtype)
     G = param_views(cfg, grad)
     B, T, C, H = cache["B"], cache["T"], cfg.d_model, cfg.n_head
+    rope = getattr(cfg, "rope", False)
+    gated = getattr(cfg, "gated_mlp", False)
+    tied = getattr(cfg, "tie_embeddings", False)
     dz = cache["dz"]
-    G["w_lm"][...] = dz.T @ cache["af"]
-    daf = dz @ P["w_lm"]
+    lm = "wte" if tied else "w_lm"
+    G[lm][...] += dz.T @ cache["af"]
+    daf = dz @ P[lm]
     dx, dg, db = layernorm_backward(daf, cache["xhatf"], cache["rstdf"], P["lnf_g"])
     G["lnf_g"][...] = dg
     if cfg.ln_bias:
@@ -295,11 +349,19 @@ def backward(cfg, params: np.ndarray, cache, dtype=np.float64) -> np.ndarray:
         if cfg.linear_bias:
             G[p + "b_2"][...] = dx.sum(0)
         dgl = dx @ P[p + "w_2"]
-        dh = dgl * gelu_grad(lc["h"], cfg.gelu_tanh)
-        G[p + "w_1"][...] = dh.T @ lc["a2"]
+        if gated:  # g = GELU(gate) * up
+            gate, up = lc["h"][:, 0::2], lc["h"][:, 1::2]
+            dh = np.empty_like(lc["h"])
+            dh[:, 0::2] = dgl * up * gelu_grad(gate, cfg.gelu_tanh)
+            dh[:, 1::2] = dgl * gelu(gate, cfg.gelu_tanh)
+            w1 = "w_gu"
+        else:
+            dh = dgl * gelu_grad(lc["h"], cfg.gelu_tanh)
+            w1 = "w_1"
+        G[p + w1][...] = dh.T @ lc["a2"]
         if cfg.linear_bias:
-            G[p + "b_1"][...] = dh.sum(0)
-        da2 = dh @ P[p + "w_1"]
+            G[p + ("b_gu" if gated else "b_1")][...] = dh.sum(0)
+        da2 = dh @ P[p + w1]
         dxm, dg, db = layernorm_backward(da2, lc["xhat2"], lc["rstd2"], P[p + "ln2_g"])
         G[p + "ln2_g"][...] = dg
         if cfg.ln_bias:
@@ -311,6 +373,8 @@ def backward(cfg, params: np.ndarray, cache, dtype=np.float64) -> np.ndarray:
             G[p + "b_o"][...] = dx_mid.sum(0)
         do = _split_heads(dx_mid @ P[p + "w_o"], B, T, H)
         dq, dk, dv = causal_attention_backward(lc["q"], lc["k"], lc["v"], lc["p"], do)
+        if rope:  # q, k were rotated by theta: their gradients rotate back by -theta
+            dq, dk = rope_rotate(dq, cache["theta"], -1.0), rope_rotate(dk, cache["theta"], -1.0)
         dqkv = np.concatenate([_merge_heads(dq), _merge_heads(dk), _merge_heads(dv)], axis=1)
         G[p + "w_qkv"][...] = dqkv.T @ lc["a1"]
         if cfg.linear_bias:
@@ -323,7 +387,8 @@ def backward(cfg, params: np.ndarray, cache, dtype=np.float64) -> np.ndarray:
         dx = dx_mid + dxi
     # embeddings: x0 = wte[tok] + wpe[pos]
     np.add.at(G["wte"], cache["tok"], dx)
-    np.add.at(G["wpe"], cache["pos"], dx)
+    if not rope:
+        np.add.at(G["wpe"], cache["pos"], dx)
     return grad
 
 

@@ -68,6 +68,9 @@ class GPTConfig:
     linear_bias: bool = True
     ln_bias: bool = True
     gelu_tanh: bool = True
+    rope: bool = False            # rotary position embedding on q, k (no learned position table)
+    gated_mlp: bool = False       # gated-GELU MLP: GELU(x W_g^T) * (x W_u^T), then W_2
+    tie_embeddings: bool = False  # the LM head is the token embedding
     lr: float = 6e-4
     beta1: float = 0.9
     beta2: float = 0.95
@@ -97,6 +100,13 @@ CONFIGS = {
     "small": GPTConfig("small", 4, 256, 4, 1024, 4096, 256, 8, lr=6e-4, steps=100),
     "main": GPTConfig("main", 12, 768, 12, 3072, 50304, 512, 8, lr=6e-4, steps=4000),
     "350m": GPTConfig("350m", 24, 1024, 16, 4096, 50304, 1024, 8, lr=6e-4, steps=500),
+    # the RTX 3090 page's 57.7M model: RoPE, gated-GELU FFN 1408, tied embeddings,
+    # no linear biases, one 1,024-token sequence per step
+    "57m": GPTConfig("57m", 16, 512, 8, 1408, 12288, 1024, 1, lr=6e-4, steps=2000, linear_bias=False,
+                     rope=True, gated_mlp=True, tie_embeddings=True),
+    # the same architecture at a size the parity tests run quickly
+    "small_gated": GPTConfig("small_gated", 4, 256, 4, 704, 4096, 256, 4, lr=6e-4, steps=50, linear_bias=False,
+                             rope=True, gated_mlp=True, tie_embeddings=True),
 }
 
 

@@ -50,8 +50,34 @@ def test_param_counts_match_pages():
 def test_param_count_closed_form():
     for cfg in I.CONFIGS.values():
         L, C, V, T, F = cfg.n_layer, cfg.d_model, cfg.vocab, cfg.seq_len, cfg.d_mlp
-        per_layer = 4 * C + (3 * C * C + 3 * C) + (C * C + C) + (F * C + F) + (C * F + C)
-        assert O.num_params(cfg) == L * per_layer + 2 * V * C + T * C + 2 * C
+        lb, nb = int(cfg.linear_bias), int(cfg.ln_bias)
+        fw = 2 * F if cfg.gated_mlp else F     # rows of the first MLP matrix
+        per_layer = (2 + 2 * nb) * C + (3 * C * C + lb * 3 * C) + (C * C + lb * C) + (fw * C + lb * fw) \
+            + (C * F + lb * C)
+        emb = V * C + (0 if cfg.rope else T * C) + (0 if cfg.tie_embeddings else V * C)
+        assert O.num_params(cfg) == L * per_layer + emb + (1 + nb) * C, cfg.name
+
+
+def test_gated_rope_tied_model_is_the_pages_57_7m():
+    """The RTX 3090 page's model: 57.7M parameters (its config list and summary)."""
+    assert round(O.num_params(I.CONFIGS["57m"]) / 1e5) / 10 == 57.7
+
+
+def test_rope_rotation_preserves_pairs_and_depends_on_offsets_only():
+    """Rotary embedding: each (2i, 2i+1) pair keeps its length, rotating by -theta undoes
+    it, and the score of a query at position m with a key at n depends only on m - n."""
+    rng = np.random.default_rng(3)
+    T, d = 40, 16
+    th = O.rope_angles(T, d)
+    q, k = rng.normal(size=(T, d)), rng.normal(size=(T, d))
+    rq = O.rope_rotate(q, th)
+    assert np.allclose(rq[:, 0::2] ** 2 + rq[:, 1::2] ** 2, q[:, 0::2] ** 2 + q[:, 1::2] ** 2, rtol=1e-12)
+    assert np.allclose(O.rope_rotate(rq, th, -1.0), q, rtol=1e-12, atol=1e-14)
+    qv, kv = rng.normal(size=d), rng.normal(size=d)
+    Q, K = O.rope_rotate(np.tile(qv, (T, 1)), th), O.rope_rotate(np.tile(kv, (T, 1)), th)
+    for m, n, shift in ((9, 3, 17), (20, 20, 11), (5, 1, 30)):
+        assert Q[m] @ K[n] == pytest.approx(Q[m + shift] @ K[n + shift], rel=1e-10)
+    assert np.allclose(th[0], 0.0) and th[1, 0] == 1.0 and th[3, 1] == pytest.approx(3 * 10000 ** (-2 / d))
 
 
 def test_know_nothing_loss_is_ln_vocab():
@@ -169,20 +195,25 @@ def _one_blas_thread():
         return contextlib.nullcontext()
 
 
-def test_finite_differences_tiny_fp64():
+GATED = TINY.replace(name="tiny_gated", rope=True, gated_mlp=True, tie_embeddings=True, d_mlp=96)
+
+
+@pytest.mark.parametrize("variant", ["gpt2", "gated_rope_tied", "gated_rope_tied_bias"])
+def test_finite_differences_tiny_fp64(variant):
     """Central differences on >=200 scalars per tensor (all of the small ones)."""
+    cfg = {"gpt2": TINY, "gated_rope_tied": GATED.replace(linear_bias=False),
+           "gated_rope_tied_bias": GATED}[variant]
     with _one_blas_thread():
-        _finite_differences_tiny_fp64()
+        _finite_differences_tiny_fp64(cfg)
 
 
-def _finite_differences_tiny_fp64():
-    cfg = TINY
+def _finite_differences_tiny_fp64(cfg):
     params, tok, tgt = _tiny_inputs(cfg, seed=11)
     # non-trivial LN/bias values so their gradients are exercised
     rng = np.random.default_rng(12)
     views = O.param_views(cfg, params)
     for name, arr in views.items():
-        if name.endswith(("_b", "_g", "b_qkv", "b_o", "b_1", "b_2")):
+        if name.endswith(("_b", "_g", "b_qkv", "b_o", "b_1", "b_2", "b_gu")):
             arr += rng.normal(0, 0.1, arr.shape)
     _, cache = O.forward(cfg, params, tok, tgt)
     grad = O.backward(cfg, params, cache)
@@ -224,31 +255,49 @@ def _torch_loss(cfg, params, tok, tgt):
     B, T = tok.shape
     C, H = cfg.d_model, cfg.n_head
     tk = torch.tensor(tok, dtype=torch.long)
-    x = F.embedding(tk, views["wte"]) + views["wpe"][:T][None]
+    x = F.embedding(tk, views["wte"])
+    if not cfg.rope:
+        x = x + views["wpe"][:T][None]
+    d = C // H
+    # rotary embedding as a complex product: pair (2i, 2i+1) times exp(j t w_i)
+    w = 1.0 / (10000.0 ** (torch.arange(0, d, 2, dtype=torch.float64) / d))
+    rot = torch.polar(torch.ones(T, d // 2, dtype=torch.float64), torch.arange(T, dtype=torch.float64)[:, None] * w)
+
+    def rope(u):  # [B, H, T, d]
+        c = torch.view_as_complex(u.reshape(B, H, T, d // 2, 2).contiguous())
+        return torch.view_as_real(c * rot).reshape(B, H, T, d)
+
     for l in range(cfg.n_layer):
         p = f"h{l}."
         a = F.layer_norm(x, (C,), views[p + "ln1_g"], views.get(p + "ln1_b"), cfg.ln_eps)
         qkv = F.linear(a, views[p + "w_qkv"], views.get(p + "b_qkv"))
         q, k, v = qkv.split(C, dim=-1)
         q, k, v = (u.view(B, T, H, C // H).transpose(1, 2) for u in (q, k, v))
+        if cfg.rope:
+            q, k = rope(q), rope(k)
         o = F.scaled_dot_product_attention(q, k, v, is_causal=True)
         o = o.transpose(1, 2).reshape(B, T, C)
         x = x + F.linear(o, views[p + "w_o"], views.get(p + "b_o"))
         a = F.layer_norm(x, (C,), views[p + "ln2_g"], views.get(p + "ln2_b"), cfg.ln_eps)
-        h = F.gelu(F.linear(a, views[p + "w_1"], views.get(p + "b_1")),
-                   approximate="tanh" if cfg.gelu_tanh else "none")
+        approx = "tanh" if cfg.gelu_tanh else "none"
+        if cfg.gated_mlp:
+            gu = F.linear(a, views[p + "w_gu"], views.get(p + "b_gu"))
+            h = F.gelu(gu[..., 0::2], approximate=approx) * gu[..., 1::2]
+        else:
+            h = F.gelu(F.linear(a, views[p + "w_1"], views.get(p + "b_1")), approximate=approx)
         x = x + F.linear(h, views[p + "w_2"], views.get(p + "b_2"))
     x = F.layer_norm(x, (C,), views["lnf_g"], views.get("lnf_b"), cfg.ln_eps)
-    z = F.linear(x, views["w_lm"])
+    z = F.linear(x, views["wte" if cfg.tie_embeddings else "w_lm"])
     loss = F.cross_entropy(z.view(B * T, -1), torch.tensor(tgt, dtype=torch.long).view(-1))
     loss.backward()
     return float(loss), t.grad.numpy()
 
 
-@pytest.mark.parametrize("variant", ["tiny", "nobias_erf"])
+@pytest.mark.parametrize("variant", ["tiny", "nobias_erf", "gated_rope_tied", "gated_rope_tied_erf_bias"])
 def test_against_torch_autograd_fp64(variant):
-    cfg = TINY if variant == "tiny" else TINY.replace(linear_bias=False, ln_bias=False,
-                                                      gelu_tanh=False)
+    cfg = {"tiny": TINY, "nobias_erf": TINY.replace(linear_bias=False, ln_bias=False, gelu_tanh=False),
+           "gated_rope_tied": GATED.replace(linear_bias=False),
+           "gated_rope_tied_erf_bias": GATED.replace(gelu_tanh=False)}[variant]
     params, tok, tgt = _tiny_inputs(cfg, seed=5)
     rng = np.random.default_rng(6)
     params = params + rng.normal(0, 0.05, params.shape)   # move LN / biases off their init

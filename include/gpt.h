@@ -90,6 +90,14 @@ typedef struct gpt_config {
   int32_t deterministic;     /* accepted for compatibility: every reduction of this
                                 library has a fixed order, so steps are always
                                 bitwise repeatable                                  */
+  /* Model variant of the RTX 3090 page's 57.7M model (bf16 only; "Coppelius
+   * training on the RTX 3090": RoPE on q/k, gated-GELU FFN, tied embedding):
+   *   rope: rotate pairs (2i, 2i+1) of every head's q and k by t * 10000^(-2i/64)
+   *     at position t; no learned position table;
+   *   gated_mlp: the first MLP matrix is w_gu [2F, C] (rows 2f, 2f+1 = gate and
+   *     up of feature f), the MLP output GELU(gate) * up (needs linear_bias 0);
+   *   tie_embeddings (above): the LM head is wte.                               */
+  int32_t rope, gated_mlp;
 } gpt_config;
 
 typedef struct gpt gpt;  /* opaque handle; owns every device buffer it allocates */

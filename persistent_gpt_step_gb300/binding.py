@@ -43,6 +43,7 @@ class gpt_config(ctypes.Structure):
         ("lr", c_float), ("beta1", c_float), ("beta2", c_float), ("eps", c_float),
         ("weight_decay", c_float), ("ln_eps", c_float),
         ("wd_on_1d", c_int32), ("wait_timeout_ms", c_uint32), ("deterministic", c_int32),
+        ("rope", c_int32), ("gated_mlp", c_int32),
     ]
 
 
@@ -138,6 +139,9 @@ def make_config(cfg, wait_timeout_ms: int = 2000) -> gpt_config:
     c.linear_bias = int(bool(getattr(cfg, "linear_bias", True)))
     c.ln_bias = int(bool(getattr(cfg, "ln_bias", True)))
     c.gelu_tanh = int(bool(getattr(cfg, "gelu_tanh", True)))
+    c.tie_embeddings = int(bool(getattr(cfg, "tie_embeddings", False)))
+    c.rope = int(bool(getattr(cfg, "rope", False)))
+    c.gated_mlp = int(bool(getattr(cfg, "gated_mlp", False)))
     for f in ("lr", "beta1", "beta2", "eps", "weight_decay", "ln_eps"):
         if hasattr(cfg, f):
             setattr(c, f, float(getattr(cfg, f)))

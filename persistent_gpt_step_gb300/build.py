@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgpt.so")
-SOURCES = ["gpt_host.cu", "kernel_fp32.cu", "kernel_bf16.cu"]
+SOURCES = ["gpt_host.cu", "kernel_fp32.cu", "kernel_bf16.cu", "kernel_bf16_ext.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
          "-I" + os.path.join(ROOT, "include")]

@@ -121,6 +121,20 @@ __device__ __forceinline__ void mma_pb(float (*acc)[4], const uint32_t (*pa)[4],
   }
 }
 
+// Packs the pair (x0, x1) of head dimensions (c, c+1) at position t into bf16,
+// rotated back by the rotary angle (the gradient of a rotated q or k w.r.t. the
+// projection before the rotation) when kRope.
+template <bool kRope>
+__device__ __forceinline__ uint32_t pack_unrotate(const float2* rope, int t, int c, float x0, float x1) {
+  if constexpr (kRope) {
+    const float2 cs = rope[t * 32 + (c >> 1)];
+    const float y0 = x0 * cs.x + x1 * cs.y, y1 = x1 * cs.x - x0 * cs.y;
+    x0 = y0;
+    x1 = y1;
+  }
+  return pack_bf16x2(x0, x1);
+}
+
 __device__ __forceinline__ void zero_acc(float (*acc)[4]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
@@ -280,6 +294,7 @@ __device__ inline void task_attn_bwd_pre(const AttnArgs& a, int idx) {
 }
 
 // ---- backward dK/dV -------------------------------------------------------------
+template <bool kRope>
 __device__ inline void task_attn_bwd_kv_tc(const AttnArgs& a, int idx, uint8_t* smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = a.T / kAttK;
@@ -364,14 +379,15 @@ __device__ inline void task_attn_bwd_kv_tc(const AttnArgs& a, int idx, uint8_t* 
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
     const int c = nt * 8 + 2 * (lane & 3);
-    *reinterpret_cast<uint32_t*>(dq + (int64_t)ka * ld + a.C + c) = pack_bf16x2(dk[nt][0], dk[nt][1]);
-    *reinterpret_cast<uint32_t*>(dq + (int64_t)kbr * ld + a.C + c) = pack_bf16x2(dk[nt][2], dk[nt][3]);
+    *reinterpret_cast<uint32_t*>(dq + (int64_t)ka * ld + a.C + c) = pack_unrotate<kRope>(a.rope, ka, c, dk[nt][0], dk[nt][1]);
+    *reinterpret_cast<uint32_t*>(dq + (int64_t)kbr * ld + a.C + c) = pack_unrotate<kRope>(a.rope, kbr, c, dk[nt][2], dk[nt][3]);
     *reinterpret_cast<uint32_t*>(dq + (int64_t)ka * ld + 2 * a.C + c) = pack_bf16x2(dv[nt][0], dv[nt][1]);
     *reinterpret_cast<uint32_t*>(dq + (int64_t)kbr * ld + 2 * a.C + c) = pack_bf16x2(dv[nt][2], dv[nt][3]);
   }
 }
 
 // ---- backward dQ ------------------------------------------------------------------
+template <bool kRope>
 __device__ inline void task_attn_bwd_q_tc(const AttnArgs& a, int idx, uint8_t* smem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = a.T / kAttQ;
@@ -444,8 +460,8 @@ __device__ inline void task_attn_bwd_q_tc(const AttnArgs& a, int idx, uint8_t* s
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
     const int c = nt * 8 + 2 * (lane & 3);
-    *reinterpret_cast<uint32_t*>(dqp + (int64_t)ra * ld + c) = pack_bf16x2(dq[nt][0], dq[nt][1]);
-    *reinterpret_cast<uint32_t*>(dqp + (int64_t)rb * ld + c) = pack_bf16x2(dq[nt][2], dq[nt][3]);
+    *reinterpret_cast<uint32_t*>(dqp + (int64_t)ra * ld + c) = pack_unrotate<kRope>(a.rope, ra, c, dq[nt][0], dq[nt][1]);
+    *reinterpret_cast<uint32_t*>(dqp + (int64_t)rb * ld + c) = pack_unrotate<kRope>(a.rope, rb, c, dq[nt][2], dq[nt][3]);
   }
 }
 

@@ -185,7 +185,11 @@ int validate(const gpt_config& c, std::string* why) {
       c.batch < 1)
     return bad("every size must be positive (vocab >= 2)");
   if (c.dtype != GPT_DTYPE_FP32 && c.dtype != GPT_DTYPE_BF16) return bad("dtype must be 0 (fp32) or 1 (bf16)");
-  if (c.tie_embeddings) { *why = "tied embeddings are not supported"; return GPT_ERR_UNSUPPORTED; }
+  if ((c.tie_embeddings || c.rope || c.gated_mlp) && !is_bf16(c)) {
+    *why = "rotary embedding, the gated MLP and tied embeddings are built for the bf16 path only";
+    return GPT_ERR_UNSUPPORTED;
+  }
+  if (c.gated_mlp && c.linear_bias) { *why = "the gated MLP has no linear biases (linear_bias 0)"; return GPT_ERR_UNSUPPORTED; }
   if (c.d_model % c.n_head) return bad("d_model must be a multiple of n_head");
   const int hd = c.d_model / c.n_head;
   if (c.d_model % 64 || c.d_model > 1024) { *why = "d_model must be a multiple of 64 and <= 1024"; return GPT_ERR_UNSUPPORTED; }
@@ -215,7 +219,7 @@ void build_table(gpt* h) {
     return (int)h->tensors.size() - 1;
   };
   h->t_wte = add("wte", V, C, 2, INIT_NORMAL);
-  h->t_wpe = add("wpe", T, C, 2, INIT_NORMAL);
+  h->t_wpe = c.rope ? -1 : add("wpe", T, C, 2, INIT_NORMAL);
   for (int l = 0; l < c.n_layer; ++l) {
     const std::string p = "h" + std::to_string(l) + ".";
     TensorIds id{};
@@ -227,7 +231,7 @@ void build_table(gpt* h) {
     id.b_o = c.linear_bias ? add(p + "b_o", C, 1, 1, INIT_ZEROS) : -1;
     id.ln2_g = add(p + "ln2_g", C, 1, 1, INIT_ONES);
     id.ln2_b = c.ln_bias ? add(p + "ln2_b", C, 1, 1, INIT_ZEROS) : -1;
-    id.w_1 = add(p + "w_1", F, C, 2, INIT_NORMAL);
+    id.w_1 = c.gated_mlp ? add(p + "w_gu", 2 * F, C, 2, INIT_NORMAL) : add(p + "w_1", F, C, 2, INIT_NORMAL);
     id.b_1 = c.linear_bias ? add(p + "b_1", F, 1, 1, INIT_ZEROS) : -1;
     id.w_2 = add(p + "w_2", C, F, 2, INIT_NORMAL);
     id.b_2 = c.linear_bias ? add(p + "b_2", C, 1, 1, INIT_ZEROS) : -1;
@@ -235,7 +239,7 @@ void build_table(gpt* h) {
   }
   h->t_lnf_g = add("lnf_g", C, 1, 1, INIT_ONES);
   h->t_lnf_b = c.ln_bias ? add("lnf_b", C, 1, 1, INIT_ZEROS) : -1;
-  h->t_wlm = add("w_lm", V, C, 2, INIT_NORMAL);
+  h->t_wlm = c.tie_embeddings ? h->t_wte : add("w_lm", V, C, 2, INIT_NORMAL);
 }
 
 // ----------------------------------------------------------------------------
@@ -262,6 +266,7 @@ struct Layout {
   std::vector<size_t> ln1_gp, ln1_bp, ln2_gp, ln2_bp;
   size_t lnf_gp, lnf_bp;
   size_t sorted_tok, sorted_pos, block_start;
+  size_t rope;  // rotary embedding (cos, sin) [T][32] fp32 pairs (rope configs)
   size_t total;
 };
 
@@ -311,7 +316,8 @@ Layout make_layout(const gpt_config& c, size_t nparams, int lm_ksplit) {
     Lo.ln2.push_back(b.take(N * Lo.ldc * act));
     Lo.ln2_mu.push_back(b.take(N * 4));
     Lo.ln2_rs.push_back(b.take(N * 4));
-    Lo.dgelu.push_back(b.take(N * F * act));  // GELU'(pre-activation), for the backward
+    // GELU'(pre-activation), or for the gated MLP the (gate, up) pairs [N, 2F], for the backward
+    Lo.dgelu.push_back(b.take(N * F * (c.gated_mlp ? 2 : 1) * act));
     Lo.gact.push_back(b.take(N * Lo.ldf * act));
   }
   Lo.lnf = b.take(N * C * act);
@@ -328,7 +334,7 @@ Layout make_layout(const gpt_config& c, size_t nparams, int lm_ksplit) {
   for (int l = 0; l < L; ++l) {
     Lo.dxm.push_back(b.take(N * C * 4));
     Lo.dxm_act.push_back(b.take(N * C * act));
-    Lo.dh.push_back(b.take(N * F * act));
+    Lo.dh.push_back(b.take(N * F * (c.gated_mlp ? 2 : 1) * act));
     Lo.da2.push_back(b.take(N * C * 4));
     Lo.dO.push_back(b.take(N * C * act));
     Lo.dqkv.push_back(b.take(N * 3 * C * act));
@@ -341,6 +347,7 @@ Layout make_layout(const gpt_config& c, size_t nparams, int lm_ksplit) {
   }
   Lo.lnf_gp = b.take(nrb * C * 4);
   Lo.lnf_bp = b.take(nrb * C * 4);
+  Lo.rope = c.rope ? b.take((size_t)c.seq_len * 32 * 8) : 0;
   Lo.sorted_tok = b.take(N * 4);
   Lo.sorted_pos = b.take(N * 4);
   Lo.block_start = b.take((V / 64 + 2) * 4);
@@ -426,7 +433,7 @@ void set_out_map(gpt* h, OpDesc& op) {
   GemmArgs& g = op.gemm;
   g.c_map = -1;
   if (!is_bf16(h->cfg) || !g.out) return;
-  if (g.epi == EPI_STORE) {
+  if (g.epi == EPI_STORE || g.epi == EPI_STORE_ROPE) {
     g.c_map = make_tmap_out(h, g.out, false, g.N, g.M, g.ldo);
   } else if (g.epi == EPI_F32) {
     if (g.ksplit > 1 && (g.M % kTcBM || g.split_stride != (int64_t)g.M * g.ldo)) return;
@@ -742,6 +749,9 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
   Builder bld{h};
   const int N = D.N, C = D.C, F = D.F, V = D.V, L = D.L;
   const int LDC = (int)Lo.ldc, LDF = (int)Lo.ldf;  // padded pitches (bias-gradient column)
+  const bool gated = c.gated_mlp != 0, tied = c.tie_embeddings != 0;
+  const int F2 = gated ? 2 * F : F;  // rows of the first MLP matrix (gate and up interleaved)
+  const float2* rope_cs = c.rope ? reinterpret_cast<const float2*>(A + Lo.rope) : nullptr;
   int rc;
 
   // ---------------- forward ----------------
@@ -758,9 +768,11 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
                       F32(Lo.ln1_rs[l]), N, C, kRowsLn, c.ln_eps, LDC};
     op_ln1[l] = bld.add(o, {prev});
     // qkv = ln1 . Wqkv^T + b
-    if ((rc = gemm_op(h, &o, N, 3 * C, C, {ACT(Lo.ln1[l]), LDC, false}, {W(id.w_qkv), C, false}, EPI_STORE, 1)))
+    if ((rc = gemm_op(h, &o, N, 3 * C, C, {ACT(Lo.ln1[l]), LDC, false}, {W(id.w_qkv), C, false},
+                      rope_cs ? EPI_STORE_ROPE : EPI_STORE, 1)))
       return rc;
     o.gemm.out = ACT(Lo.qkv[l]); o.gemm.ldo = 3 * C; o.gemm.bias = P(id.b_qkv);
+    o.gemm.rope = rope_cs; o.gemm.rope_T = D.T;
     op_qkv[l] = bld.add(o, {op_ln1[l]});
     o = blank(OP_ATTN_FWD, bf ? D.B * D.H * (D.T / 128) : D.B * D.H * ((D.T + qblock - 1) / qblock));
     o.attn = AttnArgs{ACT(Lo.qkv[l]), ACT(Lo.atto[l]), F32(Lo.lse[l]), nullptr, nullptr, nullptr,
@@ -777,9 +789,11 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
                       F32(Lo.ln2_rs[l]), N, C, kRowsLn, c.ln_eps, LDC};
     op_ln2[l] = bld.add(o, {op_atto[l]});
     // h = ln2 . W1^T + b1 ; g = GELU(h)
-    if ((rc = gemm_op(h, &o, N, F, C, {ACT(Lo.ln2[l]), LDC, false}, {W(id.w_1), C, false}, EPI_GELU, 1)))
+    // gated: [gate, up] pairs kept for the backward, GELU(gate) * up to the next GEMM
+    if ((rc = gemm_op(h, &o, N, F2, C, {ACT(Lo.ln2[l]), LDC, false}, {W(id.w_1), C, false},
+                      gated ? EPI_GEGLU : EPI_GELU, 1)))
       return rc;
-    o.gemm.out = ACT(Lo.dgelu[l]); o.gemm.ldo = F; o.gemm.out2 = ACT(Lo.gact[l]); o.gemm.ldo2 = LDF;
+    o.gemm.out = ACT(Lo.dgelu[l]); o.gemm.ldo = F2; o.gemm.out2 = ACT(Lo.gact[l]); o.gemm.ldo2 = LDF;
     o.gemm.bias = P(id.b_1);
     op_up[l] = bld.add(o, {op_ln2[l]});
     // x_{l+1} = xm + g . W2^T + b2
@@ -833,7 +847,7 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
   if ((rc = gemm_op(h, &o, V, C, N, {ACT(Lo.logits), V, true}, {ACT(Lo.lnf), C, true}, EPI_F32, 1))) return rc;
   o.gemm.out = G(h->t_wlm); o.gemm.ldo = C;
   const int op_lm_dw = bld.add(o, {op_ce});
-  adam(h->t_wlm, {op_lm_dw, op_lm_dx});
+  if (!tied) adam(h->t_wlm, {op_lm_dw, op_lm_dx});  // tied: wte's update follows the embedding gradient
   // final LayerNorm backward
   const int nrb = ln_tasks(N);
   o = blank(OP_LN_BWD, nrb);
@@ -852,9 +866,11 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
   for (int l = L - 1; l >= 0; --l) {
     const TensorIds& id = h->lid[l];
     // MLP down: dg = dx . W2 (then * GELU'(h)) ; dW2 = dx^T . g ; db2 = dx^T . 1
-    if ((rc = gemm_op(h, &o, N, F, C, {ACT(Lo.dx_act[l + 1]), C, false}, {W(id.w_2), F, true}, EPI_GELU_BWD, 1)))
+    // (gated: dh becomes the (gate, up) gradient pairs [N, 2F] from the stored pairs)
+    if ((rc = gemm_op(h, &o, N, F, C, {ACT(Lo.dx_act[l + 1]), C, false}, {W(id.w_2), F, true},
+                      gated ? EPI_GEGLU_BWD : EPI_GELU_BWD, 1)))
       return rc;
-    o.gemm.out = ACT(Lo.dh[l]); o.gemm.ldo = F; o.gemm.aux = ACT(Lo.dgelu[l]); o.gemm.ldaux = F;
+    o.gemm.out = ACT(Lo.dh[l]); o.gemm.ldo = F2; o.gemm.aux = ACT(Lo.dgelu[l]); o.gemm.ldaux = F2;
     const int op_down_dx = bld.add(o, {op_dres});
     // [dW2 | db2] = dx^T . [g | 1]
     if ((rc = gemm_op(h, &o, C, LDF, N, {ACT(Lo.dx_act[l + 1]), C, true}, {ACT(Lo.gact[l]), LDF, true}, EPI_F32, 1)))
@@ -864,11 +880,11 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
     if (id.b_2 >= 0) adam(id.b_2, {op_down_dw});
     adam(id.w_2, {op_down_dw, op_down_dx});
     // MLP up: da2 = dh . W1 ; dW1 = dh^T . ln2 ; db1 = dh^T . 1
-    if ((rc = gemm_op(h, &o, N, C, F, {ACT(Lo.dh[l]), F, false}, {W(id.w_1), C, true}, EPI_F32, 1))) return rc;
+    if ((rc = gemm_op(h, &o, N, C, F2, {ACT(Lo.dh[l]), F2, false}, {W(id.w_1), C, true}, EPI_F32, 1))) return rc;
     o.gemm.out = F32(Lo.da2[l]); o.gemm.ldo = C;
     const int op_up_dx = bld.add(o, {op_down_dx});
     // [dW1 | db1] = dh^T . [ln2 | 1]
-    if ((rc = gemm_op(h, &o, F, LDC, N, {ACT(Lo.dh[l]), F, true}, {ACT(Lo.ln2[l]), LDC, true}, EPI_F32, 1)))
+    if ((rc = gemm_op(h, &o, F2, LDC, N, {ACT(Lo.dh[l]), F2, true}, {ACT(Lo.ln2[l]), LDC, true}, EPI_F32, 1)))
       return rc;
     o.gemm.out = G(id.w_1); o.gemm.ldo = C; o.gemm.n_real = C; o.gemm.bias_grad = G(id.b_1);
     const int op_up_dw = bld.add(o, {op_down_dx});
@@ -896,7 +912,8 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
     adam(id.w_o, {op_atto_dw, op_atto_dx});
     // attention backward -> dqkv
     const AttnArgs att{ACT(Lo.qkv[l]), ACT(Lo.atto[l]), F32(Lo.lse[l]), ACT(Lo.dO[l]), ACT(Lo.dqkv[l]),
-                       F32(Lo.att_scr[l]), D.B, D.T, D.H, D.d, C, qblock, 1.0f / std::sqrt((float)D.d), LDC};
+                       F32(Lo.att_scr[l]), D.B, D.T, D.H, D.d, C, qblock, 1.0f / std::sqrt((float)D.d), LDC,
+                       rope_cs};
     int op_attb, op_attb2 = -1;
     if (bf) {
       o = blank(OP_ATTN_BWD_PRE, N / 64);
@@ -945,14 +962,17 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
   const int op_sort = bld.add(o, {});
   o = blank(OP_EMBED_BWD_WTE, (V + kVocabRows - 1) / kVocabRows);
   o.emb = EmbedArgs{nullptr, nullptr, nullptr, F32(Lo.dx[0]), G(h->t_wte), G(h->t_wpe), N, D.B, D.T, C, V,
-                    kVocabRows, stok, spos, bstart};
-  const int op_wte = bld.add(o, {op_dres, op_sort});
+                    kVocabRows, stok, spos, bstart, tied ? 1 : 0};
+  // tied: the LM head's weight gradient is written first, the scatter adds to it
+  const int op_wte = bld.add(o, {op_dres, op_sort, tied ? op_lm_dw : -1});
   adam(h->t_wte, {op_wte});
-  o = blank(OP_EMBED_BWD_WPE, (D.T + kRowsEmb - 1) / kRowsEmb);
-  o.emb = EmbedArgs{nullptr, nullptr, nullptr, F32(Lo.dx[0]), G(h->t_wte), G(h->t_wpe), N, D.B, D.T, C, V,
-                    kRowsEmb, nullptr, nullptr, nullptr};
-  const int op_wpe = bld.add(o, {op_dres});
-  adam(h->t_wpe, {op_wpe});
+  if (h->t_wpe >= 0) {
+    o = blank(OP_EMBED_BWD_WPE, (D.T + kRowsEmb - 1) / kRowsEmb);
+    o.emb = EmbedArgs{nullptr, nullptr, nullptr, F32(Lo.dx[0]), G(h->t_wte), G(h->t_wpe), N, D.B, D.T, C, V,
+                      kRowsEmb, nullptr, nullptr, nullptr};
+    const int op_wpe = bld.add(o, {op_dres});
+    adam(h->t_wpe, {op_wpe});
+  }
   bld.finish(h->num_sms > 0 ? h->num_sms : 152);
   (void)op_lm; (void)op_qkv; (void)op_attn; (void)op_atto; (void)op_ln2; (void)op_up; (void)op_down;
   return GPT_OK;
@@ -1321,11 +1341,23 @@ int gpt_create(const gpt_config* cfg, uint64_t seed, void* cuda_stream, void* ar
     if (rc != GPT_OK) return bail(rc);
   }
   if (init_bias_pads(h, Lo) != GPT_OK) return bail(GPT_ERR_CUDA);
+  if (c.rope) {  // rotary embedding table: (cos, sin) of t * 10000^(-2i/64), computed in double
+    std::vector<float> cs((size_t)c.seq_len * 64);
+    for (int t = 0; t < c.seq_len; ++t)
+      for (int i = 0; i < 32; ++i) {
+        const double th = (double)t * std::pow(10000.0, -2.0 * i / 64.0);
+        cs[(size_t)t * 64 + 2 * i] = (float)std::cos(th);
+        cs[(size_t)t * 64 + 2 * i + 1] = (float)std::sin(th);
+      }
+    CREATE_TRY(cudaMemcpyAsync(h->arena + Lo.rope, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice, h->stream));
+    CREATE_TRY(cudaStreamSynchronize(h->stream));
+  }
   CREATE_TRY(cudaMemsetAsync(h->grads, 0, h->nparams * 4, h->stream));
   CREATE_TRY(cudaMemsetAsync(h->m, 0, h->nparams * 4, h->stream));
   CREATE_TRY(cudaMemsetAsync(h->v, 0, h->nparams * 4, h->stream));
   // kernel + grid: every block must be resident (cooperative launch checks it)
-  h->kernel = is_bf16(c) ? step_kernel_bf16() : step_kernel_fp32();
+  h->kernel = !is_bf16(c) ? step_kernel_fp32()
+              : (c.rope || c.gated_mlp || c.tie_embeddings) ? step_kernel_bf16_ext() : step_kernel_bf16();
   h->smem_bytes = smem_needed(h);
   CREATE_TRY(cudaFuncSetAttribute(h->kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->smem_bytes));
   int per_sm = 0;

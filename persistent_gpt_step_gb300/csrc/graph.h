@@ -62,6 +62,11 @@ enum Epilogue : int32_t {
   EPI_GELU,          // out(act)  = GELU'(acc + bias) ; out2(act) = GELU(acc + bias)
   EPI_F32,           // out(f32)  = acc                   (dX partials, weight gradients)
   EPI_GELU_BWD,      // out(act)  = acc * aux(act)        (aux: the GELU' the forward stored)
+  EPI_STORE_ROPE,    // out(act)  = acc (+ bias), q and k columns rotated (rotary embedding; see rope below)
+  EPI_GEGLU,         // gated MLP up: columns (2f, 2f+1) = (gate, up) of feature f;
+                     // out(act) [., 2N/2] = acc (kept for the backward), out2(act) [., N/2] = GELU(gate) * up
+  EPI_GEGLU_BWD,     // gated MLP: acc = dh [., F]; aux(act) = stored (gate, up) [., 2F];
+                     // out(act) [., 2F] = (dh * up * GELU'(gate), dh * GELU(gate)) per feature
 };
 
 struct GemmArgs {
@@ -77,6 +82,11 @@ struct GemmArgs {
   // output tensor map for the TMA-store epilogue (EPI_STORE / EPI_F32): 32 x 32
   // boxes of out, rows split * M + m; -1 = the epilogue stores with generic stores
   int32_t c_map;
+  // EPI_STORE_ROPE (the QKV projection with rotary embedding): columns < 2 N / 3 (q and
+  // k) rotate pair (2i, 2i+1) of each 64-wide head by the angle of row m's
+  // position m mod rope_T: rope[(m mod rope_T) * 32 + i] = (cos, sin); null = none
+  const float2* rope;
+  int32_t rope_T;
   int32_t epi;
   void* out;  int64_t ldo;   // with ksplit > 1 split s writes out + s * split_stride
   int64_t split_stride;
@@ -119,6 +129,7 @@ struct AttnArgs {
   int32_t B, T, H, d, C, q_block;
   float scale;
   int32_t ld_o;     // row pitch of o (>= C)
+  const float2* rope;  // rotary embedding (cos, sin) [T][d/2]: the backward rotates dq, dk back; null = none
 };
 
 struct CeArgs {
@@ -144,6 +155,7 @@ struct EmbedArgs {
   int32_t N, B, T, C, V, rows_per_task;
   int32_t* sorted_tok; int32_t* sorted_pos;   // token ids in increasing order, stable
   int32_t* block_start;  // [V / rows_per_task + 1]: first sorted entry of each vocabulary block
+  int32_t accumulate;    // token-embedding backward: add into dwte (tied LM head wrote it first)
 };
 
 struct AdamArgs {

@@ -6,4 +6,5 @@
 namespace pgs {
 const void* step_kernel_fp32();  // SIMT, fp32 everywhere
 const void* step_kernel_bf16();  // tcgen05 GEMMs, bf16 operands, fp32 accumulation
+const void* step_kernel_bf16_ext();  // the same with rotary embedding and the gated MLP
 }  // namespace pgs

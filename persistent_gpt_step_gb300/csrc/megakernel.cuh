@@ -26,7 +26,9 @@ struct KernelShared {
   int64_t task;
 };
 
-template <typename act_t, bool kTC>
+// kExt: the rotary-embedding / gated-MLP model variant (its extra epilogues
+// and the rotation in the attention backward are compiled into this instance only).
+template <typename act_t, bool kTC, bool kExt = false>
 __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_constant__ KParams kp,
                                                                int32_t gelu_tanh) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -100,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
     const int idx = d.idx;
     if constexpr (kTC) {
       if (op.type == OP_GEMM) {
-        pending = gemm_run(kp, t, sh.gemm, smem, sh.tmem_base, st, gelu_tanh != 0);
+        pending = gemm_run<kExt>(kp, t, sh.gemm, smem, sh.tmem_base, st, gelu_tanh != 0);
         continue;  // the run released its tasks
       }
     }
@@ -124,10 +126,10 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
         if constexpr (kTC) { const AttnArgs a = op.attn; task_attn_bwd_pre(a, idx); }
         break;
       case OP_ATTN_BWD_KV:
-        if constexpr (kTC) { const AttnArgs a = op.attn; task_attn_bwd_kv_tc(a, idx, smem); }
+        if constexpr (kTC) { const AttnArgs a = op.attn; task_attn_bwd_kv_tc<kExt>(a, idx, smem); }
         break;
       case OP_ATTN_BWD_Q:
-        if constexpr (kTC) { const AttnArgs a = op.attn; task_attn_bwd_q_tc(a, idx, smem); }
+        if constexpr (kTC) { const AttnArgs a = op.attn; task_attn_bwd_q_tc<kExt>(a, idx, smem); }
         break;
       case OP_CE:
         {

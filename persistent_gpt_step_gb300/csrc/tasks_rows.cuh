@@ -38,11 +38,15 @@ __device__ inline void task_embed(const KParams& kp, const EmbedArgs& a, int idx
       tok = tok < 0 ? 0 : a.V - 1;
     }
     const float4* we = reinterpret_cast<const float4*>(a.wte + (int64_t)tok * a.C);
-    const float4* pe = reinterpret_cast<const float4*>(a.wpe + (int64_t)(r % a.T) * a.C);
     float4* xo = reinterpret_cast<float4*>(a.x0 + (int64_t)r * a.C);
-    for (int c = lane; c < a.C / 4; c += 32) {
-      float4 u = we[c], w = pe[c];
-      xo[c] = make_float4(u.x + w.x, u.y + w.y, u.z + w.z, u.w + w.w);
+    if (a.wpe) {
+      const float4* pe = reinterpret_cast<const float4*>(a.wpe + (int64_t)(r % a.T) * a.C);
+      for (int c = lane; c < a.C / 4; c += 32) {
+        float4 u = we[c], w = pe[c];
+        xo[c] = make_float4(u.x + w.x, u.y + w.y, u.z + w.z, u.w + w.w);
+      }
+    } else {  // rotary position embedding instead of a learned position table
+      for (int c = lane; c < a.C / 4; c += 32) xo[c] = we[c];
     }
   }
 }
@@ -728,11 +732,18 @@ __device__ __forceinline__ void wte_rows(const EmbedArgs& a, int v0, int v1, int
     for (int v = v0 + warp; v < v1; v += kWarps) {
       const int j0 = lower_bound_i32(stok, nseg, v), j1 = lower_bound_i32(stok, nseg, v + 1);
       if (j1 - j0 >= kHotRow) continue;  // below, by the whole block
+      if (a.accumulate && j1 == j0) continue;  // no occurrence: the LM-head part stays as it is
       float4 acc[NV];
       wte_row_sum<NV>(a, i0, j0, j1, lane, acc);
       float4* dst = reinterpret_cast<float4*>(a.dwte + (int64_t)v * a.C);
 #pragma unroll
-      for (int i = 0; i < NV; ++i) dst[lane + 32 * i] = acc[i];
+      for (int i = 0; i < NV; ++i) {
+        if (a.accumulate) {
+          const float4 o = dst[lane + 32 * i];
+          acc[i].x += o.x; acc[i].y += o.y; acc[i].z += o.z; acc[i].w += o.w;
+        }
+        dst[lane + 32 * i] = acc[i];
+      }
     }
     for (int v = v0; v < v1; ++v) {  // every thread sees the same counts: uniform branches
       const int j0 = lower_bound_i32(stok, nseg, v), j1 = lower_bound_i32(stok, nseg, v + 1);
@@ -747,6 +758,7 @@ __device__ __forceinline__ void wte_rows(const EmbedArgs& a, int v0, int v1, int
       for (int c = threadIdx.x; c < a.C; c += kThreads) {
         float s = part[c];
         for (int w = 1; w < kWarps; ++w) s += part[w * a.C + c];
+        if (a.accumulate) s += a.dwte[(int64_t)v * a.C + c];
         a.dwte[(int64_t)v * a.C + c] = s;
       }
       __syncthreads();
@@ -755,10 +767,11 @@ __device__ __forceinline__ void wte_rows(const EmbedArgs& a, int v0, int v1, int
     for (int v = v0 + warp; v < v1; v += kWarps) {
       const int jb = lower_bound_i32(stok, nseg, v);
       float* dst = a.dwte + (int64_t)v * a.C;
+      if (a.accumulate && (jb >= nseg || stok[jb] != v)) continue;  // no occurrence
       for (int c = lane; c < a.C; c += 32) {
         float s = 0.f;
         for (int j = jb; j < nseg && stok[j] == v; ++j) s += a.dx0[(int64_t)a.sorted_pos[i0 + j] * a.C + c];
-        dst[c] = s;
+        dst[c] = a.accumulate ? dst[c] + s : s;
       }
     }
   }

@@ -228,14 +228,19 @@ template <>
 struct EpiSrc<EPI_RESID> {
   using T = float4;  // four fp32 residual-stream values
 };
+template <>
+struct EpiSrc<EPI_GEGLU_BWD> {
+  using T = uint4;  // the (gate, up) bf16 pairs of four features
+};
 
 template <int EPI>
 __device__ __forceinline__ void epi_load_src(typename EpiSrc<EPI>::T* dst, const void* src, int64_t lds, int M,
                                              int r0, int col) {
   using T = typename EpiSrc<EPI>::T;
-  const T* p = reinterpret_cast<const T*>(reinterpret_cast<const char*>(src) +
-                                          ((int64_t)r0 * lds + col) * (EPI == EPI_RESID ? 4 : 2));
-  const int64_t step = 4 * lds * (EPI == EPI_RESID ? 4 : 2) / (int64_t)sizeof(T);
+  constexpr int64_t es = EPI == EPI_RESID ? 4 : 2;           // element bytes of the source
+  constexpr int64_t cw = EPI == EPI_GEGLU_BWD ? 2 : 1;       // source columns per output column
+  const T* p = reinterpret_cast<const T*>(reinterpret_cast<const char*>(src) + ((int64_t)r0 * lds + cw * col) * es);
+  const int64_t step = 4 * lds * es / (int64_t)sizeof(T);
 #pragma unroll
   for (int i = 0; i < 8; ++i)
     if (r0 + 4 * i < M) dst[i] = p[i * step];
@@ -249,7 +254,7 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
                                              const bool gelu_tanh, const int n_real, float* const bias_grad,
                                              const uint32_t acc_bar, const uint32_t acc_parity, uint32_t* const err,
                                              const uint64_t timeout_ns, const void* const cmap, const int crow0) {
-  constexpr bool kSrc = EPI == EPI_RESID || EPI == EPI_GELU_BWD;
+  constexpr bool kSrc = EPI == EPI_RESID || EPI == EPI_GELU_BWD || EPI == EPI_GEGLU_BWD;
   using SrcT = typename EpiSrc<EPI>::T;
   const int lane = threadIdx.x & 31;
   const int cu = 4 * (lane & 7);     // this thread's first column within the group
@@ -262,7 +267,7 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
   __syncwarp();  // lanes leave the poll loop separately; tcgen05.ld below is warp-aligned
   if (!acc_ok) return false;
   tc_fence_after();
-  if constexpr (EPI == EPI_STORE || EPI == EPI_F32) {
+  if constexpr (EPI == EPI_STORE || EPI == EPI_STORE_ROPE || EPI == EPI_F32) {
     if (cmap) {
       // TMA-store path: each lane holds its own row's 32 columns, writes them
       // (bias added and rounded to bf16, or fp32) into a swizzled 32 x 32 box in
@@ -296,13 +301,26 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
                          : "memory");
         } else {
           uint32_t w[16];
+          // rotary embedding of q and k (src: the (cos, sin) table of period lds)
+          const float2* cs = (EPI == EPI_STORE_ROPE && n < 2 * (N / 3))
+                                 ? reinterpret_cast<const float2*>(src) + (int64_t)((row0 + lane) % (int)lds) * 32 +
+                                       ((n & 63) >> 1)
+                                 : nullptr;
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
             float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
             if (bias) b = reinterpret_cast<const float4*>(bias + n)[q4];
             const uint32_t* x = &r[q4 >> 2][4 * (q4 & 3)];
-            __nv_bfloat162 lo = __floats2bfloat162_rn(__uint_as_float(x[0]) + b.x, __uint_as_float(x[1]) + b.y);
-            __nv_bfloat162 hi = __floats2bfloat162_rn(__uint_as_float(x[2]) + b.z, __uint_as_float(x[3]) + b.w);
+            float y0 = __uint_as_float(x[0]) + b.x, y1 = __uint_as_float(x[1]) + b.y;
+            float y2 = __uint_as_float(x[2]) + b.z, y3 = __uint_as_float(x[3]) + b.w;
+            if (cs) {
+              const float2 c0 = cs[2 * q4], c1 = cs[2 * q4 + 1];
+              const float t0 = y0 * c0.x - y1 * c0.y, t1 = y0 * c0.y + y1 * c0.x;
+              const float t2 = y2 * c1.x - y3 * c1.y, t3 = y2 * c1.y + y3 * c1.x;
+              y0 = t0; y1 = t1; y2 = t2; y3 = t3;
+            }
+            __nv_bfloat162 lo = __floats2bfloat162_rn(y0, y1);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(y2, y3);
             w[2 * q4] = *reinterpret_cast<uint32_t*>(&lo);
             w[2 * q4 + 1] = *reinterpret_cast<uint32_t*>(&hi);
           }
@@ -355,13 +373,23 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
     }
     const int col = n + cu;
     float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (EPI != EPI_F32 && EPI != EPI_GELU_BWD && bias) b = *reinterpret_cast<const float4*>(bias + col);
+    if (EPI != EPI_F32 && EPI != EPI_GELU_BWD && EPI != EPI_GEGLU_BWD && bias)
+      b = *reinterpret_cast<const float4*>(bias + col);
     auto row = [&](const int i) {
       const int rl = rq + 4 * i;
       const int m = row0 + rl;
       float4 v = *reinterpret_cast<const float4*>(stage + rl * 128 + (((lane & 7) ^ (rl & 7)) << 4));
       v.x += b.x; v.y += b.y; v.z += b.z; v.w += b.w;
-      if constexpr (EPI == EPI_STORE) {
+      if constexpr (EPI == EPI_STORE || EPI == EPI_STORE_ROPE) {
+        if constexpr (EPI == EPI_STORE_ROPE) {
+          if (n < 2 * (N / 3)) {  // rotary embedding of q and k (src: the (cos, sin) table, lds: its period)
+            const float2* cs =
+                reinterpret_cast<const float2*>(src) + (int64_t)(m % (int)lds) * 32 + ((col & 63) >> 1);
+            const float2 c0 = cs[0], c1 = cs[1];
+            v = make_float4(v.x * c0.x - v.y * c0.y, v.x * c0.y + v.y * c0.x, v.z * c1.x - v.w * c1.y,
+                            v.z * c1.y + v.w * c1.x);
+          }
+        }
         __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
         *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + (int64_t)m * ldo + col) =
             make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
@@ -388,6 +416,31 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
         } else {
           *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (int64_t)m * ldo + col) = v;
         }
+      } else if constexpr (EPI == EPI_GEGLU) {  // out = (gate, up) kept; out2 = GELU(gate) * up
+        __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + (int64_t)m * ldo + col) =
+            make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+        float g0, g1, d0, d1;
+        gelu_pair_bf(v.x, gelu_tanh, g0, d0);
+        gelu_pair_bf(v.z, gelu_tanh, g1, d1);
+        (void)d0; (void)d1;
+        __nv_bfloat162 hv = __floats2bfloat162_rn(g0 * v.y, g1 * v.w);
+        *reinterpret_cast<__nv_bfloat162*>(reinterpret_cast<__nv_bfloat16*>(out2) + (int64_t)m * ldo2 + (col >> 1)) = hv;
+      } else if constexpr (EPI == EPI_GEGLU_BWD) {  // v = dh of features col..col+3
+        const uint4 gu = cur[i];
+        const uint32_t w[4] = {gu.x, gu.y, gu.z, gu.w};
+        const float dh[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));  // (gate, up)
+          float g, dg;
+          gelu_pair_bf(a.x, gelu_tanh, g, dg);
+          __nv_bfloat162 t = __floats2bfloat162_rn(dh[j] * a.y * dg, dh[j] * g);
+          o[j] = *reinterpret_cast<uint32_t*>(&t);
+        }
+        *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out) + (int64_t)m * ldo + 2 * col) =
+            make_uint4(o[0], o[1], o[2], o[3]);
       } else if constexpr (EPI == EPI_GELU_BWD) {
         const uint2 hv = cur[i];  // GELU'(pre-activation), stored by the forward
         const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hv.x));
@@ -411,6 +464,9 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
 }
 
 // Waits for the tile's accumulator and runs its epilogue (false: the wait failed).
+// kExt: the kernel of the rotary / gated-MLP model variant, which alone carries
+// those epilogues (the plain model's kernel keeps its register allocation).
+template <bool kExt>
 __device__ __forceinline__ bool epilogue_tile(const KParams& kp, const GemmArgs& g, int split, int row0, int n0,
                                               uint32_t tbase, uint8_t* stage, bool gelu_tanh, uint32_t acc_bar,
                                               uint32_t acc_parity) {
@@ -420,6 +476,24 @@ __device__ __forceinline__ bool epilogue_tile(const KParams& kp, const GemmArgs&
     case EPI_STORE:
       return epi_tile<EPI_STORE>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, g.bias, nullptr,
                                  0, gelu_tanh, g.N, nullptr, acc_bar, acc_parity, kp.err, kp.timeout_ns, cmap, crow0);
+    case EPI_STORE_ROPE:  // second operand: the rotary table and its period
+      if constexpr (kExt)
+        return epi_tile<EPI_STORE_ROPE>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, g.bias,
+                                        g.rope, g.rope_T, gelu_tanh, g.N, nullptr, acc_bar, acc_parity, kp.err,
+                                        kp.timeout_ns, cmap, crow0);
+      return false;
+    case EPI_GEGLU:
+      if constexpr (kExt)
+        return epi_tile<EPI_GEGLU>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, g.out2, g.ldo2, g.bias,
+                                   nullptr, 0, gelu_tanh, g.N, nullptr, acc_bar, acc_parity, kp.err, kp.timeout_ns,
+                                   nullptr, crow0);
+      return false;
+    case EPI_GEGLU_BWD:
+      if constexpr (kExt)
+        return epi_tile<EPI_GEGLU_BWD>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, nullptr,
+                                       g.aux, g.ldaux, gelu_tanh, g.N, nullptr, acc_bar, acc_parity, kp.err,
+                                       kp.timeout_ns, nullptr, crow0);
+      return false;
     case EPI_RESID:
       return epi_tile<EPI_RESID>(g.M, g.N, g.BN, row0, n0, tbase, stage, g.out, g.ldo, nullptr, 0, g.bias, g.resid,
                                  g.ldr, gelu_tanh, g.N, nullptr, acc_bar, acc_parity, kp.err, kp.timeout_ns, cmap, crow0);
@@ -506,6 +580,7 @@ __device__ __forceinline__ uint32_t q_parity(uint32_t seq) { return (seq / kQSlo
 // and tell the releaser the warp is done.  Out of line, so the live state
 // around the epilogue calls is this loop's alone (the epilogue bodies keep their
 // registers).  Returns the updated queue and accumulator sequence counts.
+template <bool kExt>
 static __device__ __noinline__ uint2 epilogue_role(const KParams* const kpp, GemmShared& gs, const uint32_t tmem_base,
                                                    uint8_t* const smem_tiles, uint32_t q_seq, uint32_t acc_seq,
                                                    const bool gelu_tanh) {
@@ -533,7 +608,7 @@ static __device__ __noinline__ uint2 epilogue_role(const KParams* const kpp, Gem
     int tm, tn, split;
     gemm_coords(g, gs.q_idx[slot], tm, tn, split);
     if (lane == 0) role_note(kp, 3 + q, RW_EPI_TILE, i, t);
-    const bool ok = epilogue_tile(kp, g, split, tm * kTcBM + q * 32, tn * g.BN,
+    const bool ok = epilogue_tile<kExt>(kp, g, split, tm * kTcBM + q * 32, tn * g.BN,
                                   tmem_base + ((uint32_t)(q * 32) << 16) + buf * 256,
                                   smem_tiles + kTcSmemBytes + (warp - 4) * kEpiStageBytes, gelu_tanh,
                                   acc_full0 + 8 * buf, (acc >> 1) & 1);
@@ -821,6 +896,7 @@ static __device__ __noinline__ TcState releaser_role(const KParams* const kpp, G
 // returns the next claimed ticket (not a GEMM, or >= ntasks).  Every role runs
 // out of line, so each role loop is register-allocated on its own and not
 // together with the rest of the persistent kernel.
+template <bool kExt>
 __device__ inline int64_t gemm_run(const KParams& kp, int64_t t_first, GemmShared& gs, uint8_t* smem_tiles,
                                    uint32_t tmem_base, TcState& st, bool gelu_tanh) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -835,7 +911,7 @@ __device__ inline int64_t gemm_run(const KParams& kp, int64_t t_first, GemmShare
   } else if (warp == 1) {
     st = mma_role(&kp, gs, smem_tiles, tmem_base, st, t_first);
   } else if (warp >= 4) {
-    const uint2 seqs = epilogue_role(&kp, gs, tmem_base, smem_tiles, st.q_seq, st.acc_seq, gelu_tanh);
+    const uint2 seqs = epilogue_role<kExt>(&kp, gs, tmem_base, smem_tiles, st.q_seq, st.acc_seq, gelu_tanh);
     st.q_seq = seqs.x;
     st.acc_seq = seqs.y;
   } else {

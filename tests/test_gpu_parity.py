@@ -235,6 +235,26 @@ def test_main_bf16_parity_first_steps():
     assert (np.abs(losses - refs) / np.abs(refs)).max() <= 0.01
 
 
+def test_gated_rope_tied_bf16_parity_20_steps():
+    """The RTX 3090 page's model variant (rotary embedding, gated-GELU MLP, tied
+    embedding and LM head) at a small size: step-1 loss within 2e-3 and per-tensor
+    gradient cosine >= 0.999 against the fp64 oracle, loss curve within 1 % over
+    20 steps."""
+    cfg = I.CONFIGS["small_gated"]
+    losses, refs = _bf16_parity(cfg, 1234, 20)
+    assert (np.abs(losses - refs) / np.abs(refs)).max() <= 0.01
+    assert losses[-1] < losses[0]
+
+
+def test_57m_bf16_parity_first_step():
+    """The 57.7M model itself (16 layers, d 512, F 1408, vocab 12288, one 1,024-token
+    sequence): step-1 loss within 2e-3 and per-tensor gradient cosine >= 0.999
+    against the fp32 oracle."""
+    cfg = I.CONFIGS["57m"]
+    losses, refs = _bf16_parity(cfg, 1234, 1, oracle_dtype=np.float32)
+    assert abs(losses[0] - refs[0]) <= 2e-3 * abs(refs[0])
+
+
 def test_350m_bf16_parity_first_step():
     """The 350M scale-up (24 layers, d 1024, 16 heads, seq 1024 x batch 8): step-1 loss
     within 2e-3 of the fp32 oracle and per-tensor gradient cosine >= 0.999 (one step:
@@ -307,7 +327,7 @@ def test_multi_step_bad_token_stops_updates_at_that_step():
 
 # ----------------------------------------------------------------- properties
 
-@pytest.mark.parametrize("name", ["tiny", "small"])
+@pytest.mark.parametrize("name", ["tiny", "small", "small_gated"])
 def test_steps_are_bitwise_repeatable(name):
     cfg = I.CONFIGS[name]
     runs = []

@@ -104,7 +104,7 @@ def test_create_without_gpu_fails_cleanly(lib):
     assert lib.gpt_last_error(None)
 
 
-@pytest.mark.parametrize("name", ["tiny", "small"])
+@pytest.mark.parametrize("name", ["tiny", "small", "small_gated", "57m"])
 def test_library_tensor_table_and_host_init_match_spec(lib, name):
     """The C++ implementation of the init spec equals the test-side one."""
     cfg = I.CONFIGS[name]
@@ -181,7 +181,7 @@ def test_zipf_frequencies():
 
 # ----------------------------------------------------------------- task graph
 
-@pytest.mark.parametrize("name", ["tiny", "small", "main", "350m"])
+@pytest.mark.parametrize("name", ["tiny", "small", "main", "350m", "small_gated", "57m"])
 def test_task_graph_is_topological(lib, name):
     """Every counter a task waits on is signalled only by earlier tickets, as
     many times as the wait needs (the no-deadlock condition of the ticket loop)."""

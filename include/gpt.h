@@ -262,7 +262,8 @@ int gpt_trace_enable(gpt* h, int32_t on);
 int gpt_get_trace(gpt* h, uint64_t* dst, size_t n);
 
 /* Device time of the last step's kernel launch in milliseconds, from CUDA
- * events the library records on the handle's stream around the launch. */
+ * events the library records on the handle's stream around the launch (after
+ * gpt_train_steps: around the last chunk of its launches, up to 256 steps). */
 int gpt_last_kernel_ms(const gpt* h, float* ms);
 
 /* Text of the handle's last error ("" if none).  h may be NULL (last create

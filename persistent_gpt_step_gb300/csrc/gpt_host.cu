@@ -488,7 +488,7 @@ struct Builder {
     switch (o.type) {
       case OP_EMBED: rows_task(o.emb.rows_per_task, 12.0 * D.C); break;
       case OP_LN_FWD: rows_task(o.lnf.rows_per_task, 6.0 * D.C); break;
-      case OP_LN_BWD: rows_task(o.lnb.rows_per_task, 18.0 * D.C); break;
+      case OP_LN_BWD: rows_task(o.lnb.rows_per_task, 36.0 * D.C); break;  // 18C bytes a row, at half the stream rate (traced)
       case OP_CE: rows_task(o.ce.rows_per_task, 6.0 * D.V); break;
       case OP_ATTN_BWD_PRE: rows_task(64, 4.0 * D.C); break;
       case OP_GEMM: {
@@ -506,7 +506,8 @@ struct Builder {
           blk = (b * D.T + qb * 128) / kRowBlock;
           lo = o.type == OP_ATTN_FWD ? b * D.T / kRowBlock : blk;
           hi = blk;
-          us = 1.0 + (o.type == OP_ATTN_FWD ? 4.0 : 6.0) * 128.0 * (qb * 128 + 128) * D.d / 3e6;
+          // (mma.sync attention runs near 1.25 FLOP per ns per SM: traced task times)
+          us = 1.0 + (o.type == OP_ATTN_FWD ? 4.0 : 6.0) * 128.0 * (qb * 128 + 128) * D.d / 1.25e6;
         } else {
           us = 1.0 + 4.0 * D.T * D.T * D.d / 1e5;
         }
@@ -517,7 +518,7 @@ struct Builder {
           blk = (b * D.T + kb * 128) / kRowBlock;
           lo = blk;
           hi = (b * D.T + D.T) / kRowBlock - 1;
-          us = 1.0 + 8.0 * 128.0 * (D.T - kb * 128) * D.d / 3e6;
+          us = 1.0 + 8.0 * 128.0 * (D.T - kb * 128) * D.d / 1.25e6;
         }
         break;
       case OP_ATTN_BWD: us = 1.0 + 12.0 * D.T * D.T * D.d / 1e5; break;

@@ -7,8 +7,12 @@ backward and AdamW of the whole model as one persistent kernel launch.  Inputs
 are seeded synthetic Zipf(1.1) token batches (64 distinct batches, pre-uploaded),
 standing in for the tokenized TinyStories stream of the pages; weights are the
 seeded N(0, 0.02) initialisation.  The step's working set (fp32 master weights,
-moments, gradients and activations: 7 GB for the 162M model) is far larger than L2, so no L2 flush
-is inserted between steps.
+moments, gradients and activations: 6.5 GB for the 162M model) is far larger than
+L2, so no L2 flush is inserted between steps.
+
+Besides the device-timed steps (value) the line carries the same steps through
+the host-buffer entry point (e2e) and as one multi-step call (multi_step_call).
+--config selects another workload of inputs.CONFIGS (350m, 57m, ...).
 
 Multi-GPU: the step does not shard here (no collective is in scope), so N > 1
 runs N independent replicas, one per rank, and reports the aggregate tokens/s

@@ -41,10 +41,12 @@ projections of feature f, the MLP output being GELU(gate) * up; and
 Pins (see tests/test_oracle.py): central finite differences in float64 on the
 tiny model and its gated / RoPE / tied variant, an independent float64 autograd
 re-derivation with PyTorch CPU operators (rotary embedding as a complex
-product), the rotary embedding's norm and relative-position properties, the know-nothing loss ln V printed on the Coppelius page, loss near
-ln V at initialisation, softmax rows summing to one, the closed form of the
-first two AdamW steps, causality, T = 1 attention, LayerNorm moments, and the
-parameter counts printed on the pages.
+product), the rotary embedding's norm and relative-position properties, the
+know-nothing loss ln V printed on the Coppelius page, loss near ln V at
+initialisation, softmax rows summing to one, the closed form of the first two
+AdamW steps (also with per-step rates), the learning-rate schedule's closed
+forms, causality, T = 1 attention, LayerNorm moments, and the parameter counts
+printed on the pages.
 """
 
 from __future__ import annotations

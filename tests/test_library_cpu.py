@@ -205,6 +205,27 @@ def test_task_graph_is_topological(lib, name):
     assert sum(1 for t in types if t == 11) == len(O.param_table(I.CONFIGS[name]))
 
 
+@pytest.mark.parametrize("name", ["small_gated", "57m"])
+def test_variant_graph_structure(lib, name):
+    """The rotary / gated / tied variant: no position-table gradient op, the gated MLP's
+    GEMMs are 2F wide, and (tied embedding) the token-embedding gradient op waits for
+    the LM head's weight-gradient GEMM, whose result it adds to."""
+    cfg = I.CONFIGS[name]
+    tasks, types, ntk, dims = B.describe_graph(cfg, dims=True)
+    N, C, F, V = cfg.batch * cfg.seq_len, cfg.d_model, cfg.d_mlp, cfg.vocab
+    assert 10 not in types                                   # no position-embedding backward
+    gemm = [(o, d) for o, (t, d) in enumerate(zip(types, dims)) if t == 2]
+    shapes = {(d[0], d[1], d[2]) for _, d in gemm}
+    assert (N, 2 * F, C) in shapes                           # up projection, gate and up interleaved
+    assert (2 * F, C, N) in shapes and (N, C, 2 * F) in shapes  # its weight and input gradients
+    lm_dw = [o for o, d in gemm if (d[0], d[1], d[2]) == (V, C, N)]
+    assert len(lm_dw) == 1
+    ctr0, nctr = dims[lm_dw[0]][4], dims[lm_dw[0]][5]
+    wte_op = types.index(9)
+    waited = {c for (op, _, _, waits, _) in tasks if op == wte_op for (f, n, _) in waits for c in range(f, f + n)}
+    assert waited & set(range(ctr0, ctr0 + nctr))
+
+
 def test_row_blocks_make_the_forward_a_wavefront(lib):
     """On the bf16 path a QKV tile waits only for its own 128-row block of LN1."""
     tasks, types, ntk, dims = B.describe_graph(I.CONFIGS["main"], dims=True)

@@ -1,6 +1,8 @@
 """Per-family time table of one training step from the in-kernel trace.
 
-python -m persistent_gpt_step_gb300.trace [--config main] [--steps 3]
+python -m persistent_gpt_step_gb300.trace [--config main] [--steps 3] [--save t.npz]
+                                          [--windows 0,1.85,2.55,7.0,8.0]
+python -m persistent_gpt_step_gb300.trace --load t.npz --windows ...   (no GPU needed)
 
 The kernel stamps every task's claim, start (after its dependency waits) and
 end (after its release) with %globaltimer.  Per operation family this prints
@@ -44,6 +46,33 @@ def family_table(trace: np.ndarray, task_ops: np.ndarray, op_types, grid: int):
     return rows, total
 
 
+def window_shares(trace: np.ndarray, task_ops: np.ndarray, op_types, grid: int, bounds_ms):
+    """Per window [bounds_ms[i], bounds_ms[i+1]) of the launch (ms from its first
+    claim) and per family: the share of the grid's time its tasks executed (start to
+    end) and waited (claim to start) inside the window.  Tasks of one GEMM run
+    overlap (tile i+1's mainloop runs under tile i's epilogue), so a window's GEMM
+    share counts that overlap twice.  Returns [(lo, hi, {family: (exec, wait)})]."""
+    claim = trace[:, 0].astype(np.int64)
+    start = trace[:, 1].astype(np.int64)
+    end = trace[:, 2].astype(np.int64)
+    t0 = claim.min()
+    c, s, e = (claim - t0) / 1e6, (start - t0) / 1e6, (end - t0) / 1e6
+    fam = np.asarray(op_types)[task_ops]
+    out = []
+    for lo, hi in zip(bounds_ms[:-1], bounds_ms[1:]):
+        cap = (hi - lo) * grid
+        ex = np.clip(np.minimum(e, hi) - np.maximum(s, lo), 0, None)
+        wt = np.clip(np.minimum(s, hi) - np.maximum(c, lo), 0, None)
+        shares = {}
+        for f in sorted(set(fam.tolist())):
+            sel = fam == f
+            x, w = ex[sel].sum() / cap, wt[sel].sum() / cap
+            if x > 0 or w > 0:
+                shares[FAMILIES[f]] = (float(x), float(w))
+        out.append((lo, hi, shares))
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--config", default="main")
@@ -51,7 +80,21 @@ def main():
     ap.add_argument("--json", default=None)
     ap.add_argument("--ops", action="store_true", help="print every op's first start / last end")
     ap.add_argument("--save", default=None, help="write the raw trace and the task graph to this .npz")
+    ap.add_argument("--load", default=None, help="analyse a trace saved with --save instead of running (no GPU)")
+    ap.add_argument("--windows", default=None,
+                    help="comma-separated window bounds in ms from the launch start: per-window family shares")
     args = ap.parse_args()
+    if args.load:
+        d = np.load(args.load)
+        tr, task_ops, op_types, grid = d["trace"], d["task_ops"], list(d["op_types"]), int(d["grid"])
+        rows, total = family_table(tr, task_ops, op_types, grid)
+        print(f"saved trace: {len(tr)} tasks, grid {grid}, kernel {float(d['kernel_ms']):.3f} ms, "
+              f"traced span {total:.3f} ms")
+        for r in sorted(rows, key=lambda r: -r[2]):
+            print(f"{r[0]:20s} {r[1]:7d} {r[2]:9.3f} {r[3]:9.3f} {r[4]:9.3f} {r[5]:8.3f} {r[6]:8.3f}")
+        if args.windows:
+            print_windows(window_shares(tr, task_ops, op_types, grid, [float(x) for x in args.windows.split(",")]))
+        return 0
     import torch
 
     from . import binding as B
@@ -106,8 +149,17 @@ def main():
                          (end[sel] - start[sel]).sum() / 1e6 / grid))
         for st, o, ty, nt, en, busy in sorted(rows):
             print(f"{o:5d} {FAMILIES[ty]:20s} {nt:6d} {st:8.3f} {en:8.3f} {busy:9.4f}")
+    if args.windows:
+        print_windows(window_shares(tr, task_ops, op_types, grid, [float(x) for x in args.windows.split(",")]))
     if args.json:
         json.dump({"config": args.config, "kernel_ms": kms, "grid": grid, "rows": rows}, open(args.json, "w"))
+
+
+def print_windows(wins):
+    for lo, hi, shares in wins:
+        print(f"\nwindow {lo:.2f}-{hi:.2f} ms")
+        for f, (x, w) in sorted(shares.items(), key=lambda kv: -kv[1][0]):
+            print(f"  {f:20s} exec {100 * x:5.1f} %  wait {100 * w:5.1f} %")
 
 
 if __name__ == "__main__":

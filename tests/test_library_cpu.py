@@ -297,3 +297,20 @@ def test_scheduler_simulation_skipped_release_times_out(lib):
     tasks, types, ntk, dims = B.describe_graph(I.CONFIGS["tiny"], dims=True)
     counters, done, failed = _simulate(tasks, _n_counters(dims), 8, skip=0, timeout=0.5)
     assert failed
+
+
+def test_trace_window_shares_synthetic():
+    """The trace tool's window table on a hand-made trace: grid 2, one GEMM task
+    (claim 0, start 1 ms, end 3 ms) and one AdamW task (claim 2, start 2.5, end 4)."""
+    from persistent_gpt_step_gb300 import trace as T
+    ms = 1_000_000
+    tr = np.array([[0, 1 * ms, 3 * ms, 0], [2 * ms, int(2.5 * ms), 4 * ms, 1]], dtype=np.uint64)
+    ops = np.array([0, 1])
+    types = [2, 11]  # gemm, adamw
+    w = T.window_shares(tr, ops, types, 2, [0.0, 2.0, 4.0])
+    (lo0, hi0, s0), (lo1, hi1, s1) = w
+    assert s0["gemm"] == pytest.approx((1.0 / 4.0, 1.0 / 4.0))   # exec 1-2, wait 0-1 of 2 x 2 ms
+    assert "adamw" not in s0
+    assert s1["gemm"] == pytest.approx((1.0 / 4.0, 0.0))
+    assert s1["adamw"] == pytest.approx((1.5 / 4.0, 0.5 / 4.0))
+

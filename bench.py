@@ -209,10 +209,13 @@ def run_reference(args, cfg):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": workload_name(cfg), "global_batch": 1, "seq_len": cfg.seq_len,
-                       "sample": "one sequence per step (CPU oracle)"},
+            # the workload of our arm's line; each timed step samples one of its sequences
+            "config": {"workload": workload_name(cfg), "global_batch": cfg.batch, "seq_len": cfg.seq_len,
+                       "parallelism": "single-gpu", "params": O.num_params(cfg),
+                       "tokens": "Zipf(1.1) synthetic" if cfg.tokens == "zipf" else "uniform synthetic"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": f"{args.steps} oracle steps on 1 x {sub.seq_len} tokens"},
+                             "sample": f"{args.steps} oracle steps (fp64 numpy), each on 1 of the {cfg.batch} "
+                                       f"sequences of a batch ({sub.seq_len} tokens)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

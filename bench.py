@@ -100,12 +100,12 @@ class ClockSampler:
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, interval_ms: int = 50):
         self.proc = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(interval_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
 
@@ -209,9 +209,10 @@ def run_reference(args, cfg):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            # the workload of our arm's line; each timed step samples one of its sequences
-            "config": {"workload": workload_name(cfg), "global_batch": cfg.batch, "seq_len": cfg.seq_len,
-                       "parallelism": "single-gpu", "params": O.num_params(cfg),
+            # what this arm runs: the same model, one sequence of the workload's batch per step
+            "config": {"workload": workload_name(sub), "global_batch": sub.batch, "seq_len": sub.seq_len,
+                       "parallelism": "host cores", "params": O.num_params(cfg),
+                       "sample_of": workload_name(cfg),
                        "tokens": "Zipf(1.1) synthetic" if cfg.tokens == "zipf" else "uniform synthetic"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                              "sample": f"{args.steps} oracle steps (fp64 numpy), each on 1 of the {cfg.batch} "
@@ -276,7 +277,6 @@ def main():
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
-    clk = clocks.stop() if clocks else None
     t_dev = max_over_ranks(ev0.elapsed_time(ev1) / 1000.0, world, dev)
 
     # ---- end to end: host buffers through the C ABI (H2D/D2H inside) ----------
@@ -306,6 +306,8 @@ def main():
     m1.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
+    # the sampler ran through the three timed regions (device, end-to-end, multi-step)
+    clk = clocks.stop() if clocks else None
     t_multi = max_over_ranks(m0.elapsed_time(m1) / 1000.0, world, dev)
     model.close()
 

@@ -110,6 +110,11 @@ void gpt_default_config(gpt_config* cfg);
  * invalid config. */
 size_t gpt_arena_bytes(const gpt_config* cfg);
 
+/* Host-only: number of parameters of a model with this config (the length of
+ * every flat parameter-sized vector; "What ran" prints the 162M model's count).
+ * 0 on an invalid config.  Needs no GPU. */
+size_t gpt_param_count(const gpt_config* cfg);
+
 /*
  * Creates a handle on the current CUDA device.  Weights are initialised on the
  * host from `seed` ("What ran": seeded initial weights; "Reproduce the run":
@@ -194,10 +199,14 @@ float gpt_lr_at(const gpt_lr_schedule* sched, float base_lr, int64_t step);
 int gpt_train_steps(gpt* h, const int32_t* tokens, const int32_t* targets, int32_t k,
                     const gpt_lr_schedule* sched, float* losses);
 
-/* Number of parameters (length of every flat parameter-sized vector). */
+/* Number of parameters (length of every flat parameter-sized vector): the
+ * count "What ran" prints for its model (162,417,408; this library's 162M model
+ * keeps linear and LayerNorm biases and has 162,716,160).  0 for a NULL handle. */
 size_t gpt_num_params(const gpt* h);
 
-/* Number of tensors in the canonical order. */
+/* Number of tensors in the canonical order (the model of "What ran": token and
+ * position embeddings, per layer two LayerNorms, QKV, attention-out and two MLP
+ * linears, the final LayerNorm and the LM head).  0 for a NULL handle. */
 int gpt_num_tensors(const gpt* h);
 
 /*
@@ -208,19 +217,35 @@ int gpt_num_tensors(const gpt* h);
  */
 int gpt_tensor_info(const gpt* h, int i, const char** name, int64_t shape[2], size_t* offset);
 
-/* Copies the fp32 master parameters to HOST dst[0..n), n == gpt_num_params. */
+/* Copies the fp32 master parameters to HOST dst[0..n), n == gpt_num_params:
+ * the parameter half of a checkpoint ("Coppelius training on the RTX 3090",
+ * section "Checkpoint lineage": each invocation resumes the checkpoint the one
+ * before wrote).  Synchronises the handle's stream.  INVALID_ARG for a NULL
+ * handle or dst or a wrong n; CUDA if the copy fails. */
 int gpt_get_params(gpt* h, float* dst, size_t n);
 
 /* Overwrites the fp32 master parameters (and the bf16 copies the kernels read)
- * from HOST src[0..n).  Optimizer state is unchanged. */
+ * from HOST src[0..n), n == gpt_num_params: resuming a checkpoint ("Checkpoint
+ * lineage", as above).  Optimizer state is unchanged.  The values are not
+ * checked: a non-finite parameter makes the next step's loss non-finite, and
+ * that step returns NONFINITE without updating anything.  INVALID_ARG for a
+ * NULL handle or src or a wrong n; CUDA if the copy fails. */
 int gpt_set_params(gpt* h, const float* src, size_t n);
 
 /* Copies the gradient computed by the last step (fp32, canonical order) to
- * HOST dst[0..n). */
+ * HOST dst[0..n), n == gpt_num_params ("Coppelius training on the RTX 3090",
+ * section "Optimizer internals": the last step's embedding gradient is
+ * inspected after each invocation; here every tensor's is available, for
+ * parity checks).  Also valid after a BAD_TOKEN or NONFINITE step.  INVALID_ARG
+ * for a NULL handle or dst or a wrong n; CUDA if the copy fails. */
 int gpt_get_grads(gpt* h, float* dst, size_t n);
 
-/* AdamW state: first and second moments (HOST float[n] each, either may be
- * NULL) and the number of updates applied so far. */
+/* AdamW state: first and second moments (HOST float[gpt_num_params] each,
+ * either may be NULL) and the number of updates applied so far (bias
+ * correction of the next update uses step + 1).  The optimizer half of a
+ * checkpoint ("Checkpoint lineage"; "Optimizer internals": AdamW's first moment
+ * after each invocation).  INVALID_ARG for a NULL handle, a NULL step pointer
+ * (get) or a negative step (set); CUDA if a copy fails. */
 int gpt_get_opt_state(gpt* h, float* m, float* v, int64_t* step);
 int gpt_set_opt_state(gpt* h, const float* m, const float* v, int64_t step);
 
@@ -266,8 +291,12 @@ int gpt_get_trace(gpt* h, uint64_t* dst, size_t n);
  * gpt_train_steps: around the last chunk of its launches, up to 256 steps). */
 int gpt_last_kernel_ms(const gpt* h, float* ms);
 
-/* Text of the handle's last error ("" if none).  h may be NULL (last create
- * error of this thread). */
+/* Text of the handle's last error ("" if none): the error notifier of
+ * "Coppelius training on the RTX 3090", section "Channel health" (each
+ * invocation's exit status, error notifier and finite-loss check).  h may be
+ * NULL: the last error of gpt_create or of a handle-less call (test hooks,
+ * gpt_train_step_static) in this process.  The string stays valid until the
+ * next call on the same handle. */
 const char* gpt_last_error(const gpt* h);
 
 /* Releases every resource of the handle.  gpt_destroy(NULL) is a no-op. */
@@ -322,32 +351,40 @@ int gpt_graph_describe(const gpt_config* cfg, int32_t num_sms, int64_t* n_tasks,
 
 /*
  * Training step that allocates nothing (the pages have no counterpart: this is
- * an addition of this library).  It is meant for callers that cannot allocate
- * device memory: code that issues the step while a stream is being captured
- * into a CUDA graph, runtimes whose device memory belongs to a pool that does
- * not allow side allocations, and hosts that must not allocate after start-up.
- * The same persistent kernel runs the same task graph as gpt_train_step, with
- * GPT_DTYPE_FP32 arithmetic; every piece of scratch (gradients, activations,
- * the task graph, counters, error words) lives in one 16 MiB file-scope device
- * array that every GPU which loads libgpt.so holds until the process exits.
- * No cudaMalloc, cudaFree, pinned or library allocation is made; the task list
- * is built in ordinary host heap memory and copied into the array.
+ * an addition of this library).  It is for callers that cannot allocate device
+ * memory: runtimes whose device memory is owned by a pool allocator that
+ * allows no side allocations (a cudaMalloc next to the pool would break its
+ * reservation or fragment it), and embedded or real-time hosts that must not
+ * allocate after start-up (an allocation can block the calling thread for an
+ * unbounded time).  The same persistent kernel runs the same task graph as
+ * gpt_train_step, with GPT_DTYPE_FP32 arithmetic; every piece of scratch
+ * (gradients, activations, the task graph, counters, error words) lives in one
+ * 16 MiB file-scope device array that every GPU which loads libgpt.so holds
+ * until the process exits.  No cudaMalloc, cudaFree, pinned or library
+ * allocation is made; the task list is built in ordinary host heap memory and
+ * copied into the array from pageable memory.
  *   cfg: GPT_DTYPE_FP32 only; models whose scratch exceeds 16 MiB (the tiny
- *     configuration needs about 7 MiB) are rejected with GPT_ERR_INVALID_ARG
- *     and a message giving the size they need.
- *   params, m, v: DEVICE fp32 [gpt_num_params] in the canonical order: the
- *     parameters and AdamW moments, read and updated in place.
+ *     configuration needs about 5.6 MiB) are rejected with GPT_ERR_INVALID_ARG
+ *     and a message giving the size they need, before anything is written to
+ *     the array.
+ *   params, m, v: DEVICE fp32 [gpt_param_count(cfg)] in the canonical order:
+ *     the parameters and AdamW moments, read and updated in place.  The library
+ *     cannot check their length: shorter buffers are read and written past
+ *     their end.
  *   step: AdamW updates applied so far (bias correction uses step + 1); on
  *     GPT_OK the caller counts one more.
  *   tokens, targets: DEVICE int32 [batch, seq_len]; loss: HOST float*, may be
- *     NULL.  Runs on cuda_stream and synchronises it.
+ *     NULL.  Runs on cuda_stream; the call copies the graph from host memory,
+ *     writes the activation pads, launches the kernel and synchronises the
+ *     stream before it returns.
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit: make that
- * first call before any stream capture.  Every call shares the one array and
- * starts by rewriting its graph and zeroing its counters, so calls whose work
- * overlaps on the GPU (other threads, other streams) race and must not be made.
- * Errors as gpt_train_step (BAD_TOKEN / NONFINITE leave params, m, v as they
- * were), plus UNSUPPORTED for bf16; text via gpt_last_error(NULL).
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call sets the kernel's shared-memory limit (cudaFuncSetAttribute).
+ * Every call shares the one array: it rewrites the graph and the pads and zeroes
+ * the counters, the ticket and the error words before its launch, so calls whose
+ * work overlaps on the GPU (other threads, other streams) race and must not be
+ * made.  Errors as gpt_train_step (BAD_TOKEN / NONFINITE leave params, m, v as
+ * they were), plus UNSUPPORTED for bf16; text via gpt_last_error(NULL).
  */
 int gpt_train_step_static(const gpt_config* cfg, float* params, float* m, float* v, int64_t step,
                           const int32_t* tokens, const int32_t* targets, float* loss, void* cuda_stream);

@@ -71,6 +71,7 @@ _lib = None
 SIGNATURES = [
     ("gpt_default_config", None, [POINTER(gpt_config)]),
     ("gpt_arena_bytes", c_size_t, [POINTER(gpt_config)]),
+    ("gpt_param_count", c_size_t, [POINTER(gpt_config)]),
     ("gpt_create", c_int, [POINTER(gpt_config), c_uint64, c_void_p, c_void_p, c_size_t, POINTER(c_void_p)]),
     ("gpt_train_step", c_int, [c_void_p, c_void_p, c_void_p, POINTER(c_float)]),
     ("gpt_train_step_host", c_int, [c_void_p, c_void_p, c_void_p, POINTER(c_float)]),
@@ -428,12 +429,47 @@ def describe_graph(cfg, num_sms: int = 152, dims: bool = False):
     return out, list(types), list(ntk)
 
 
+def param_count(cfg) -> int:
+    """Number of parameters of a model with this workload definition (host only)."""
+    n = int(load().gpt_param_count(byref(make_config(cfg))))
+    if n == 0:
+        raise GptError(-1, "invalid config")
+    return n
+
+
+def _check_device_tensor(name, t, dtype, numel=None, shape=None):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise GptError(-1, f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        raise GptError(-1, f"{name} is on cuda:{t.device.index}, not the current device")
+    if t.dtype != dtype:
+        raise GptError(-1, f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise GptError(-1, f"{name} must be contiguous")
+    if numel is not None and t.numel() != numel:
+        raise GptError(-1, f"{name} has {t.numel()} elements, the model needs {numel}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise GptError(-1, f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
 def train_step_static(cfg, params, m, v, step: int, tokens, targets, stream=None,
                       wait_timeout_ms: int = 2000) -> float:
-    """gpt_train_step_static on CUDA tensors (fp32 params/m/v updated in place)."""
+    """gpt_train_step_static on CUDA tensors (fp32 params/m/v updated in place).
+
+    The C call cannot check buffer lengths, so every tensor's device, dtype,
+    contiguity and size is checked here before any launch; a mismatch raises
+    GptError(INVALID_ARG).  Invalid configs and bf16 (which the call rejects by
+    itself, before touching any buffer) reach the library unchanged."""
     import torch
     lib = load()
     c = make_config(cfg, wait_timeout_ms)
+    n = int(lib.gpt_param_count(byref(c)))
+    if n > 0 and c.dtype == DTYPE_FP32:
+        for name, t in (("params", params), ("m", m), ("v", v)):
+            _check_device_tensor(name, t, torch.float32, numel=n)
+        for name, t in (("tokens", tokens), ("targets", targets)):
+            _check_device_tensor(name, t, torch.int32, shape=(c.batch, c.seq_len))
     s = stream if stream is not None else torch.cuda.current_stream()
     loss = c_float()
     rc = lib.gpt_train_step_static(byref(c), c_void_p(params.data_ptr()), c_void_p(m.data_ptr()),

@@ -286,7 +286,9 @@ constexpr int64_t kAdamChunk = 65536;
 
 int ln_tasks(int N) { return (N + kRowsLn - 1) / kRowsLn; }
 
-Layout make_layout(const gpt_config& c, size_t nparams, int lm_ksplit) {
+// own_state = false: the caller owns the parameters and AdamW moments (the
+// allocation-free step), so the arena holds no regions for them.
+Layout make_layout(const gpt_config& c, size_t nparams, int lm_ksplit, bool own_state = true) {
   Layout Lo;
   Bump b;
   const size_t N = (size_t)c.batch * c.seq_len, C = c.d_model, F = c.d_mlp, V = c.vocab;
@@ -299,10 +301,10 @@ Layout make_layout(const gpt_config& c, size_t nparams, int lm_ksplit) {
   const size_t pad = c.linear_bias ? 64 : 0;
   Lo.ldc = C + pad;
   Lo.ldf = F + pad;
-  Lo.params = b.take(nparams * 4);
+  Lo.params = own_state ? b.take(nparams * 4) : 0;
   Lo.grads = b.take(nparams * 4);
-  Lo.m = b.take(nparams * 4);
-  Lo.v = b.take(nparams * 4);
+  Lo.m = own_state ? b.take(nparams * 4) : 0;
+  Lo.v = own_state ? b.take(nparams * 4) : 0;
   Lo.shadow = is_bf16(c) ? b.take(nparams * 2) : 0;
   for (int l = 0; l <= L; ++l) Lo.x.push_back(b.take(N * C * 4));
   for (int l = 0; l < L; ++l) {
@@ -1226,6 +1228,16 @@ size_t gpt_arena_bytes(const gpt_config* cfg) {
   return make_layout(*cfg, tmp.nparams, lm_ksplit_for(*cfg, sms)).total;
 }
 
+size_t gpt_param_count(const gpt_config* cfg) {
+  if (!cfg) return 0;
+  std::string why;
+  if (validate(*cfg, &why) != GPT_OK) return 0;
+  gpt tmp;
+  tmp.cfg = *cfg;
+  build_table(&tmp);
+  return tmp.nparams;
+}
+
 int gpt_create(const gpt_config* cfg, uint64_t seed, void* cuda_stream, void* arena, size_t arena_bytes, gpt** out) {
   g_create_error.clear();
   if (!cfg || !out) return fail(nullptr, GPT_ERR_INVALID_ARG, "cfg and out must be non-NULL");
@@ -1783,10 +1795,9 @@ int64_t gpt_task_budget(int64_t iterations, int64_t tasks_per_iteration) {
 // Training step without any allocation.
 //
 // For callers that cannot allocate device memory themselves or through us:
-// code that runs while a stream is being captured into a CUDA graph (where an
-// allocation would break or serialise the capture), runtimes whose memory is
-// owned by a pool that forbids side allocations, and embedded or real-time
-// hosts that must not allocate after start-up.  The step's scratch (gradients,
+// runtimes whose memory is owned by a pool allocator that forbids side
+// allocations, and embedded or real-time hosts that must not allocate after
+// start-up (an allocation can block for an unbounded time).  The step's scratch (gradients,
 // activations, the task graph, counters and error words) lives in one
 // file-scope device array; the caller passes parameters, AdamW moments, tokens
 // and targets.  Only the fp32 arithmetic is offered (the bf16 path would have to
@@ -1844,11 +1855,11 @@ extern "C" int gpt_train_step_static(const gpt_config* cfg, float* params, float
   cudaDeviceGetAttribute(&h.num_sms, cudaDevAttrMultiProcessorCount, h.device);
   build_table(&h);
   const int lm_ks = lm_ksplit_for(h.cfg, h.num_sms);
-  const Layout Lo = make_layout(h.cfg, h.nparams, lm_ks);
+  const Layout Lo = make_layout(h.cfg, h.nparams, lm_ks, /*own_state=*/false);
   uint8_t* scratch = nullptr;
   rc = static_scratch_address(h.device, &scratch);
   if (rc != GPT_OK) return rc;
-  // scratch: the arena layout (its params/m/v regions stay unused: the
+  // scratch: the arena layout without parameter and moment regions (the
   // caller's buffers take their place), then the graph and the sync words
   h.arena = scratch;
   h.params = params;
@@ -1860,19 +1871,20 @@ extern "C" int gpt_train_step_static(const gpt_config* cfg, float* params, float
   if (rc != GPT_OK) { g_create_error = h.err; return rc; }
   Bump mb;
   mb.off = Lo.total;
-  if (mb.off <= kStaticScratchBytes && init_bias_pads(&h, Lo) != GPT_OK) {
-    g_create_error = h.err;
-    return GPT_ERR_CUDA;
-  }
   const size_t o_tasks = mb.take(h.tasks.size() * sizeof(TaskDesc));
   const size_t o_ops = mb.take(h.ops.size() * sizeof(OpDesc));
   const size_t o_ctr = mb.take((size_t)h.n_counters * sizeof(unsigned long long));
   const size_t o_tic = mb.take(2 * sizeof(unsigned long long));
   const size_t o_err = mb.take(4 * sizeof(uint32_t));
+  // the whole footprint is checked before anything is written to the array
   if (mb.off > kStaticScratchBytes)
     return fail(nullptr, GPT_ERR_INVALID_ARG,
                 "gpt_train_step_static: this model needs %zu bytes of scratch, above the %zu-byte static maximum",
                 mb.off, kStaticScratchBytes);
+  if (init_bias_pads(&h, Lo) != GPT_OK) {
+    g_create_error = h.err;
+    return GPT_ERR_CUDA;
+  }
   h.d_tasks = reinterpret_cast<TaskDesc*>(scratch + o_tasks);
   h.d_ops = reinterpret_cast<OpDesc*>(scratch + o_ops);
   h.d_counters = reinterpret_cast<unsigned long long*>(scratch + o_ctr);

@@ -1,12 +1,13 @@
 """The training step that allocates nothing (gpt_train_step_static).
 
-Callers that cannot allocate device memory (a stream being captured into a
-CUDA graph, a runtime whose memory belongs to a pool that allows no side
-allocations, a host that must not allocate after start-up) get this entry
-point: its scratch is a static device array inside libgpt.so, and the caller
-passes parameters, AdamW moments, tokens and targets.  It must give the same
-results as the ordinary handle-based step.  This file is collected last so a
-run that stops at its first failure has run every other test before it.
+Callers that cannot allocate device memory (a runtime whose memory belongs to a
+pool allocator that allows no side allocations, an embedded or real-time host
+that must not allocate after start-up, where an allocation can block for an
+unbounded time) get this entry point: its scratch is a static device array
+inside libgpt.so, and the caller passes parameters, AdamW moments, tokens and
+targets.  It must give the same results as the ordinary handle-based step.
+This file is collected last so a run that stops at its first failure has run
+every other test before it.
 """
 
 import numpy as np
@@ -62,11 +63,35 @@ def test_static_step_matches_handle_step_on_two_calls():
 
 def test_static_step_rejects_models_beyond_its_scratch():
     cfg = I.CONFIGS["small"].replace(dtype="fp32")
-    P = torch.zeros(1, device="cuda")   # never touched: the size check comes first
+    n = B.param_count(cfg)
+    P, M, V = (torch.full((n,), 7.0, device="cuda") for _ in range(3))
     tok = torch.zeros(cfg.batch, cfg.seq_len, dtype=torch.int32, device="cuda")
     with pytest.raises(B.GptError) as e:
-        B.train_step_static(cfg, P, P, P, 0, tok, tok)
+        B.train_step_static(cfg, P, M, V, 0, tok, tok)
     assert e.value.name == "INVALID_ARG" and "static maximum" in str(e.value)
+    assert bool((P == 7.0).all()) and bool((M == 7.0).all())  # rejected before any launch
+    one = torch.zeros(1, device="cuda")
     with pytest.raises(B.GptError) as e:
-        B.train_step_static(I.CONFIGS["tiny"].replace(dtype="bf16"), P, P, P, 0, tok, tok)
+        B.train_step_static(I.CONFIGS["tiny"].replace(dtype="bf16"), one, one, one, 0, tok, tok)
     assert e.value.name == "UNSUPPORTED"
+
+
+def test_static_step_binding_rejects_wrong_buffers_before_any_launch():
+    """The C call cannot see buffer lengths: the binding checks every tensor's
+    size, dtype and device first, so a short parameter vector never reaches the
+    kernel (which would read and write past its end)."""
+    cfg = I.CONFIGS["tiny"]
+    n = B.param_count(cfg)
+    tok, tgt = (_dev(x) for x in I.batch(cfg, 3, 0))
+    good = [torch.zeros(n, device="cuda") for _ in range(3)]
+    short = torch.zeros(n - 1, device="cuda")
+    for bad_args, word in (((short, good[1], good[2]), "elements"),
+                           ((good[0], good[1].double(), good[2]), "float32"),
+                           ((good[0], good[1], good[2].cpu()), "CUDA")):
+        with pytest.raises(B.GptError) as e:
+            B.train_step_static(cfg, *bad_args, 0, tok, tgt)
+        assert e.value.name == "INVALID_ARG" and word in str(e.value)
+    with pytest.raises(B.GptError) as e:
+        B.train_step_static(cfg, *good, 0, tok[:, :-1].contiguous(), tgt)
+    assert e.value.name == "INVALID_ARG" and "shape" in str(e.value)
+    assert not any(bool(g.any()) for g in good)  # nothing ran

@@ -261,6 +261,28 @@ int gpt_debug_skip_release(gpt* h, int64_t task_index);
  * and optimizer state are kept. */
 int gpt_reset(gpt* h);
 
+/*
+ * Measurement hook (per-phase timing, after the per-family table of
+ * "Coppelius training on the RTX 3090", section "Where a step's time goes"):
+ * runs the operations op_first .. op_first + op_count - 1 of the handle's step
+ * graph (the order gpt_graph_describe reports for this config and this GPU's SM
+ * count) as their own launch of the persistent kernel, `reps` times back to
+ * back, on whatever the arena holds (run a step first so the activations are
+ * real).  Their tasks keep the step's ticket order and their dependencies on
+ * each other; dependencies on operations outside the range are dropped.
+ * Operations that update in place act again: the cross-entropy rewrites the
+ * logits buffer (which after a step holds the logit gradients), AdamW updates
+ * the parameters and moments with the next update's bias correction (the update
+ * count is not advanced).  tokens, targets: DEVICE int32 [batch, seq_len], as
+ * gpt_train_step.  kernel_ms (HOST, may be NULL): mean device time of one
+ * launch, from CUDA events on the handle's stream around each launch.
+ * Errors: INVALID_ARG (range, reps outside 1..1000), POISONED, OOM (its small
+ * task/counter buffer), CUDA, TIMEOUT (a wait inside the range gave up; the
+ * handle is not poisoned).
+ */
+int gpt_run_ops(gpt* h, int32_t op_first, int32_t op_count, const int32_t* tokens, const int32_t* targets,
+                int32_t reps, float* kernel_ms);
+
 /* Size of the step's task graph: number of tasks, and the grid (resident
  * blocks) the persistent kernel is launched with.  Any pointer may be NULL. */
 int gpt_graph_info(const gpt* h, int64_t* n_tasks, int32_t* grid, int32_t* block);

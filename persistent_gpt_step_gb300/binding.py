@@ -87,6 +87,7 @@ SIGNATURES = [
     ("gpt_set_opt_state", c_int, [c_void_p, c_void_p, c_void_p, c_int64]),
     ("gpt_debug_skip_release", c_int, [c_void_p, c_int64]),
     ("gpt_reset", c_int, [c_void_p]),
+    ("gpt_run_ops", c_int, [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_int32, POINTER(c_float)]),
     ("gpt_graph_info", c_int, [c_void_p, POINTER(c_int64), POINTER(c_int32), POINTER(c_int32)]),
     ("gpt_trace_enable", c_int, [c_void_p, c_int32]),
     ("gpt_get_trace", c_int, [c_void_p, c_void_p, c_size_t]),
@@ -338,6 +339,17 @@ class GPT:
 
     def reset(self):
         self._check(self._lib.gpt_reset(self._h))
+
+    def run_ops(self, op_first: int, op_count: int, tokens, targets, reps: int = 1) -> float:
+        """gpt_run_ops: operations [op_first, op_first + op_count) of the step graph
+        as their own launch, ``reps`` times; returns the mean milliseconds per launch.
+        tokens, targets: CUDA int32 tensors [batch, seq_len]."""
+        assert tokens.is_cuda and targets.is_cuda
+        assert tokens.dtype == self._torch.int32 and targets.dtype == self._torch.int32
+        ms = c_float()
+        self._check(self._lib.gpt_run_ops(self._h, op_first, op_count, c_void_p(tokens.data_ptr()),
+                                          c_void_p(targets.data_ptr()), reps, byref(ms)))
+        return float(ms.value)
 
 
 def task_budget(iterations: int, tasks_per_iteration: int) -> int:

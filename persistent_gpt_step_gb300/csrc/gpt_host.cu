@@ -1051,8 +1051,8 @@ int reset_counters(gpt* h) {
 // Queues one launch of the step kernel on the handle's stream (no
 // synchronisation): epoch = launch number, lr and the bias corrections of update
 // number t; loss_out / status_out: ring slots of a multi-step call (or null).
-int enqueue_step(gpt* h, const int32_t* tokens, const int32_t* targets, unsigned long long epoch, float lr,
-                 int64_t t, float* loss_out, uint32_t* status_out) {
+KParams step_params(gpt* h, const int32_t* tokens, const int32_t* targets, unsigned long long epoch, float lr,
+                    int64_t t) {
   KParams kp;
   std::memset(&kp, 0, sizeof kp);
   kp.tasks = h->d_tasks;
@@ -1068,19 +1068,29 @@ int enqueue_step(gpt* h, const int32_t* tokens, const int32_t* targets, unsigned
   kp.tokens = tokens;
   kp.targets = targets;
   kp.trace = h->d_trace;
-  kp.loss_out = loss_out;
-  kp.status_out = status_out;
   kp.lr = lr; kp.beta1 = h->cfg.beta1; kp.beta2 = h->cfg.beta2; kp.eps = h->cfg.eps;
   kp.wd = h->cfg.weight_decay;
   kp.bc1 = (float)(1.0 - std::pow((double)h->cfg.beta1, (double)t));
   kp.bc2 = (float)(1.0 - std::pow((double)h->cfg.beta2, (double)t));
+  return kp;
+}
+
+int launch_kernel(gpt* h, KParams& kp) {
   int32_t gelu_tanh = h->cfg.gelu_tanh;
   void* args[2] = {&kp, &gelu_tanh};
-  h->skip_release = -1;
   cudaError_t e = cudaLaunchCooperativeKernel(h->kernel, dim3(h->grid), dim3(kThreads), args, h->smem_bytes,
                                               h->stream);
   if (e != cudaSuccess) return fail(h, GPT_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
   return GPT_OK;
+}
+
+int enqueue_step(gpt* h, const int32_t* tokens, const int32_t* targets, unsigned long long epoch, float lr,
+                 int64_t t, float* loss_out, uint32_t* status_out) {
+  KParams kp = step_params(h, tokens, targets, epoch, lr, t);
+  kp.loss_out = loss_out;
+  kp.status_out = status_out;
+  h->skip_release = -1;
+  return launch_kernel(h, kp);
 }
 
 int launch_step(gpt* h, const int32_t* tokens, const int32_t* targets, float* loss) {
@@ -1461,6 +1471,88 @@ int gpt_set_opt_state(gpt* h, const float* m, const float* v, int64_t step) {
   CUDA_TRY(h, cudaStreamSynchronize(h->stream));
   h->opt_step = step;
   return GPT_OK;
+}
+
+int gpt_run_ops(gpt* h, int32_t op_first, int32_t op_count, const int32_t* tokens, const int32_t* targets,
+                int32_t reps, float* kernel_ms) {
+  if (!h) return GPT_ERR_INVALID_ARG;
+  const int nops = (int)h->ops.size();
+  if (!tokens || !targets || op_first < 0 || op_count < 1 || reps < 1 || reps > 1000 ||
+      (int64_t)op_first + op_count > nops)
+    return fail(h, GPT_ERR_INVALID_ARG, "need device tokens/targets, 0 <= op_first, op_first + op_count <= %d, "
+                "1 <= reps <= 1000", nops);
+  if (h->poisoned) return fail(h, GPT_ERR_POISONED, "handle poisoned by an earlier timeout; call gpt_reset");
+  // the range's tasks in the step's ticket order; the range owns the contiguous
+  // counters [c_lo, c_hi), and waits on counters outside it are dropped (those
+  // producers' outputs are taken as the arena holds them)
+  const int last = op_first + op_count - 1;
+  const int c_lo = h->op_ctr0[op_first], c_hi = h->op_ctr0[last] + h->op_nblk[last];
+  std::vector<TaskDesc> sub;
+  for (const TaskDesc& t : h->tasks) {
+    if (t.op < op_first || t.op > last) continue;
+    TaskDesc u = t;
+    u.nwait = 0;
+    for (int w = 0; w < t.nwait; ++w)
+      if (t.wait[w].first >= c_lo && t.wait[w].first < c_hi) u.wait[u.nwait++] = t.wait[w];
+    sub.push_back(u);
+  }
+  Bump mb;
+  const size_t o_tasks = mb.take(sub.size() * sizeof(TaskDesc));
+  const size_t o_ctr = mb.take((size_t)h->n_counters * sizeof(unsigned long long));
+  const size_t o_tic = mb.take(2 * sizeof(unsigned long long));
+  const size_t o_err = mb.take(4 * sizeof(uint32_t));
+  uint8_t* d = nullptr;
+  if (cudaMalloc(&d, mb.off) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(h, GPT_ERR_OOM, "cudaMalloc of %zu bytes failed", mb.off);
+  }
+  std::vector<cudaEvent_t> ev(2 * (size_t)reps, nullptr);
+  int rc = GPT_OK;
+  uint32_t err[4] = {0, 0, 0, 0};
+  do {
+    if (cudaMemcpyAsync(d + o_tasks, sub.data(), sub.size() * sizeof(TaskDesc), cudaMemcpyHostToDevice, h->stream) ||
+        cudaMemsetAsync(d + o_ctr, 0, mb.off - o_ctr, h->stream)) {
+      rc = fail(h, GPT_ERR_CUDA, "set-up copies failed");
+      break;
+    }
+    for (auto& e : ev)
+      if (cudaEventCreate(&e) != cudaSuccess) rc = fail(h, GPT_ERR_CUDA, "cudaEventCreate failed");
+    if (rc != GPT_OK) break;
+    for (int r = 0; r < reps && rc == GPT_OK; ++r) {
+      // epochs 1..reps on counters that start at zero: no reset between launches
+      KParams kp = step_params(h, tokens, targets, (unsigned long long)r + 1, h->cfg.lr, h->opt_step + 1);
+      kp.tasks = reinterpret_cast<const TaskDesc*>(d + o_tasks);
+      kp.ntasks = (int64_t)sub.size();
+      kp.counters = reinterpret_cast<unsigned long long*>(d + o_ctr);
+      kp.tickets = reinterpret_cast<unsigned long long*>(d + o_tic);
+      kp.err = reinterpret_cast<uint32_t*>(d + o_err);
+      kp.skip_release = -1;
+      kp.trace = nullptr;
+      cudaEventRecord(ev[2 * r], h->stream);
+      rc = launch_kernel(h, kp);
+      cudaEventRecord(ev[2 * r + 1], h->stream);
+    }
+    if (cudaMemcpyAsync(err, d + o_err, sizeof err, cudaMemcpyDeviceToHost, h->stream) ||
+        cudaStreamSynchronize(h->stream))
+      rc = fail(h, GPT_ERR_CUDA, "run of the op range failed");
+  } while (0);
+  if (rc == GPT_OK && err[0])
+    rc = fail(h, GPT_ERR_TIMEOUT, "a wait timed out in the op range (code %u, task %u, counter %u)", err[0], err[2],
+              err[3]);
+  if (rc == GPT_OK && kernel_ms) {
+    double sum = 0.0;
+    for (int r = 0; r < reps; ++r) {
+      float ms = 0.f;
+      cudaEventElapsedTime(&ms, ev[2 * r], ev[2 * r + 1]);
+      sum += ms;
+    }
+    *kernel_ms = (float)(sum / reps);
+  }
+  for (auto& e : ev)
+    if (e) cudaEventDestroy(e);
+  cudaStreamSynchronize(h->stream);
+  cudaFree(d);
+  return rc;
 }
 
 int gpt_debug_skip_release(gpt* h, int64_t task_index) {

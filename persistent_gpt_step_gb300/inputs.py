@@ -104,6 +104,9 @@ CONFIGS = {
     # no linear biases, one 1,024-token sequence per step
     "57m": GPTConfig("57m", 16, 512, 8, 1408, 12288, 1024, 1, lr=6e-4, steps=2000, linear_bias=False,
                      rope=True, gated_mlp=True, tie_embeddings=True),
+    # the 162M model's shapes with two layers: profiling captures of one operation
+    # at the step's own sizes with a few GB on the device
+    "main_2l": GPTConfig("main_2l", 2, 768, 12, 3072, 50304, 512, 8, lr=6e-4, steps=10),
     # the same architecture at a size the parity tests run quickly
     "small_gated": GPTConfig("small_gated", 4, 256, 4, 704, 4096, 256, 4, lr=6e-4, steps=50, linear_bias=False,
                              rope=True, gated_mlp=True, tie_embeddings=True),

@@ -8,6 +8,7 @@ of the oracle's over the first 50 steps.
 
 import math
 import os
+import sys
 
 import numpy as np
 import pytest
@@ -15,6 +16,9 @@ import pytest
 from oracle import gpt_oracle as O
 from persistent_gpt_step_gb300 import binding as B
 from persistent_gpt_step_gb300 import inputs as I
+
+sys.path.insert(0, os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden"))
+from make_loss_curves import SEED as GOLDEN_SEED, read_curve  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -141,20 +145,29 @@ def _attn_reference(qkv, dout, B, T, H, d):
 
 
 @pytest.mark.parametrize("dt,Bn,T,H,d", [("bf16", 2, 256, 3, 64), ("bf16", 1, 512, 2, 64),
-                                         ("bf16", 1, 1024, 1, 64), ("fp32", 2, 64, 4, 16),
+                                         ("bf16", 1, 1024, 1, 64), ("bf16", 3, 128, 2, 64),
+                                         ("bf16", 1, 1024, 12, 64), ("fp32", 2, 64, 4, 16),
                                          ("fp32", 1, 192, 2, 64)])
 def test_attention_tasks_match_autograd(dt, Bn, T, H, d):
+    """Every element of o, LSE and dqkv against float64 autograd on the same
+    (bf16-rounded) inputs: |got - ref| <= tol * max|ref| per output, so a wrong
+    row block (the diagonal block, the last key block) fails even when the norm
+    of the error over the whole tensor is small.  bf16 tolerances: o and dqkv are
+    stored in bf16 (relative rounding 2^-9) after fp32 accumulation over products
+    of bf16-rounded P and dS (another 2^-9 each); LSE is fp32."""
     g = torch.Generator(device="cuda").manual_seed(T + H)
     dtype = torch.bfloat16 if dt == "bf16" else torch.float32
     qkv = torch.randn(Bn * T, 3 * H * d, device="cuda", generator=g).to(dtype)
     dout = torch.randn(Bn * T, H * d, device="cuda", generator=g).to(dtype)
     o, lse, dqkv = B.test_attention(qkv, dout, Bn, T, H, d)
     ro, rlse, rd = _attn_reference(qkv, dout, Bn, T, H, d)
-    tol = 2e-2 if dt == "bf16" else 1e-5
+    tols = {"o": 1e-2, "lse": 1e-3, "dqkv": 2e-2} if dt == "bf16" else {"o": 1e-5, "lse": 1e-6, "dqkv": 1e-5}
     for got, ref, name in ((o, ro, "o"), (lse, rlse, "lse"), (dqkv, rd, "dqkv")):
-        err = (got.double() - ref).norm().item() / ref.norm().item()
-        assert err <= tol, (name, err)
-        assert torch.isfinite(got).all()
+        assert torch.isfinite(got).all(), name
+        err = (got.double() - ref).abs()
+        scale = ref.abs().max().item()
+        worst = err.max().item()
+        assert worst <= tols[name] * scale, (name, worst / scale, divmod(int(err.argmax()), ref.shape[-1]))
 
 
 # ----------------------------------------------------------------- model parity
@@ -226,13 +239,47 @@ def test_small_bf16_parity_50_steps():
     assert losses[-1] < losses[0]
 
 
-def test_main_bf16_parity_first_steps():
+def test_main_bf16_parity_first_step():
     """The 162M workload, in the launch configuration the benchmark times: step-1
-    loss and per-tensor gradient cosine, then two more steps of the loss curve
-    (the oracle runs in fp32 here to bound its CPU time)."""
+    loss within 2e-3 and per-tensor gradient cosine >= 0.999 against the fp32
+    oracle run here."""
     cfg = I.CONFIGS["main"]
-    losses, refs = _bf16_parity(cfg, 1234, 3, oracle_dtype=np.float32)
-    assert (np.abs(losses - refs) / np.abs(refs)).max() <= 0.01
+    _bf16_parity(cfg, GOLDEN_SEED, 1, oracle_dtype=np.float32)
+
+
+def _golden_curve_parity(name, steps):
+    """`steps` GPU steps of configuration `name` (seed and batches of the golden
+    file) against the fp32 oracle's loss curve committed in tests/golden/, written
+    by tests/golden/make_loss_curves.py: every step within 1 % relative."""
+    cfg = I.CONFIGS[name]
+    ref = read_curve(name, steps)
+    params = I.init_params(O.param_table(cfg), GOLDEN_SEED)
+    with B.GPT(cfg, seed=GOLDEN_SEED) as m:
+        m.set_params(params)
+        got = np.array([m.train_step(*(_dev(x) for x in I.batch(cfg, GOLDEN_SEED, s))) for s in range(steps)])
+    rel = np.abs(got - ref) / np.abs(ref)
+    assert rel.max() <= 0.01, (int(rel.argmax()), rel.max(), got[rel.argmax()], ref[rel.argmax()])
+    assert got[-1] < got[0]
+    return got, ref
+
+
+def test_main_bf16_loss_curve_50_steps():
+    """The bf16 loss curve of the 162M model over its first 50 steps within 1 % of
+    the fp32 oracle's (the step the pages train for 4,000 steps)."""
+    _golden_curve_parity("main", 50)
+
+
+def test_57m_bf16_loss_curve_50_steps():
+    """The 57.7M gated / rotary / tied model's loss curve over 50 steps within 1 %
+    of the fp32 oracle's."""
+    _golden_curve_parity("57m", 50)
+
+
+def test_350m_bf16_loss_curve_10_steps():
+    """The 350M scale-up's loss curve over its first 10 steps within 1 % of the fp32
+    oracle's (ten fp32 oracle steps of 8,192 tokens are about twenty minutes of CPU,
+    run once when the golden file was written)."""
+    _golden_curve_parity("350m", 10)
 
 
 def test_gated_rope_tied_bf16_parity_20_steps():
@@ -425,6 +472,56 @@ def test_bad_token_skips_update(name):
         tok[1, 5] = 0
         m.train_step(_dev(tok), _dev(tgt))      # the handle stays usable
         assert m.opt_state()[2] == 1
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_nonfinite_loss_skips_update_and_keeps_the_handle(name):
+    """An infinite LM-head weight makes the loss non-finite: the step returns
+    NONFINITE, parameters, moments and the update count stay as they were, and
+    after the weights are restored the handle trains on ("Channel health": a
+    non-finite loss is reported, not applied)."""
+    cfg = I.CONFIGS[name]
+    tok, tgt = (_dev(x) for x in I.batch(cfg, 4, 0))
+    with B.GPT(cfg, seed=4) as m:
+        m.train_step(tok, tgt)  # one good update: the moments are non-zero
+        p1 = m.params()
+        m1, v1, s1 = m.opt_state()
+        off = {n: o for n, _, o in m.tensor_table()}["w_lm"]
+        bad = p1.copy()
+        bad[off + 5] = np.inf
+        m.set_params(bad)
+        with pytest.raises(B.GptError) as e:
+            m.train_step(tok, tgt)
+        assert e.value.name == "NONFINITE", str(e.value)
+        assert np.array_equal(m.params(), bad)
+        m2, v2, s2 = m.opt_state()
+        assert s2 == s1 == 1 and np.array_equal(m2, m1) and np.array_equal(v2, v1)
+        m.set_params(p1)
+        loss = m.train_step(tok, tgt)
+        assert math.isfinite(loss) and m.opt_state()[2] == 2
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_run_ops_of_the_whole_graph_equals_a_step(name):
+    """The per-phase measurement hook runs a range of the step graph as its own
+    launch: over every operation it is one training step (bitwise the parameters
+    of gpt_train_step from the same state), and one operation run again on its
+    own inputs (a layer's LayerNorm) leaves the step's results unchanged."""
+    cfg = I.CONFIGS[name]
+    tok, tgt = (_dev(x) for x in I.batch(cfg, 8, 0))
+    _, types, _ = B.describe_graph(cfg, torch.cuda.get_device_properties(0).multi_processor_count)
+    with B.GPT(cfg, seed=8) as a, B.GPT(cfg, seed=8) as b:
+        a.train_step(tok, tgt)
+        ms = b.run_ops(0, len(types), tok, tgt, reps=1)
+        assert ms > 0
+        assert np.array_equal(a.params(), b.params())
+        assert np.array_equal(a.grads(), b.grads())
+        ln = types.index(1)  # the first LayerNorm forward: reads x0, writes its own output only
+        b.run_ops(ln, 1, tok, tgt, reps=3)
+        assert np.array_equal(a.params(), b.params())
+        with pytest.raises(B.GptError) as e:
+            b.run_ops(len(types), 1, tok, tgt)
+        assert e.value.name == "INVALID_ARG"
 
 
 def test_skipped_release_times_out_without_hanging():

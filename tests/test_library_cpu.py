@@ -92,6 +92,17 @@ def test_arena_bytes_and_invalid_configs(lib):
     assert lib.gpt_arena_bytes(ctypes.byref(bad)) == 0
 
 
+@pytest.mark.parametrize("name", ["tiny", "small", "main", "350m", "57m", "small_gated"])
+def test_param_count_matches_oracle_table(lib, name):
+    cfg = I.CONFIGS[name]
+    assert B.param_count(cfg) == O.num_params(cfg)
+
+
+def test_param_count_rejects_invalid_config(lib):
+    with pytest.raises(B.GptError):
+        B.param_count(I.CONFIGS["tiny"].replace(d_model=65))
+
+
 def test_create_without_gpu_fails_cleanly(lib):
     import torch
     if torch.cuda.is_available():

@@ -372,14 +372,70 @@ def test_lr_schedule_closed_forms():
     assert lo < O.lr_at(1, hi, lo, 0, tot) < hi
 
 
-def test_decay_mask_is_two_dimensional_tensors():
-    cfg = MICRO
+def _decays_by_name(name: str) -> bool:
+    """GPT-2 convention written from parameter names alone: weight decay on the
+    weight matrices and embeddings (w_*, wte, wpe, w_lm), none on biases or
+    LayerNorm gains and biases."""
+    leaf = name.split(".")[-1]
+    return leaf in ("wte", "wpe", "w_lm") or leaf.startswith("w_")
+
+
+@pytest.mark.parametrize("variant", ["tiny", "gated_rope_tied"])
+def test_adamw_matches_torch_optim_adamw(variant):
+    """Three AdamW updates of the oracle against torch.optim.AdamW (float64, CPU),
+    with two parameter groups built from the parameter names (decay / no decay)
+    and a different learning rate on each update: a decayed LayerNorm gain or
+    bias, an undecayed matrix, a wrong bias correction or a wrong moment update
+    each fails this."""
+    torch = pytest.importorskip("torch")
+    cfg = MICRO if variant == "tiny" else MICRO.replace(rope=True, gated_mlp=True, tie_embeddings=True,
+                                                         linear_bias=False)
+    table = O.param_table(cfg)
+    rng = np.random.default_rng(31)
+    n = O.num_params(cfg)
+    p0 = rng.normal(0, 0.5, n)
+    grads = [rng.normal(0, 1e-2, n) for _ in range(3)]
+    rates = [3e-3, 1e-3, 2e-3]
+    # torch: one tensor per parameter, grouped by name
+    tensors, off = [], 0
+    for name, shape, _ in table:
+        k = int(np.prod(shape))
+        tensors.append((name, off, k, torch.tensor(p0[off:off + k], dtype=torch.float64, requires_grad=True)))
+        off += k
+    decay = [t for name, _, _, t in tensors if _decays_by_name(name)]
+    no_decay = [t for name, _, _, t in tensors if not _decays_by_name(name)]
+    assert decay and no_decay
+    opt = torch.optim.AdamW([{"params": decay, "weight_decay": cfg.weight_decay},
+                             {"params": no_decay, "weight_decay": 0.0}],
+                            lr=rates[0], betas=(cfg.beta1, cfg.beta2), eps=cfg.eps)
+    p, m, v = p0.copy(), np.zeros(n), np.zeros(n)
+    for step, (g, lr) in enumerate(zip(grads, rates), start=1):
+        for grp in opt.param_groups:
+            grp["lr"] = lr
+        for _, o, k, t in tensors:
+            t.grad = torch.tensor(g[o:o + k], dtype=torch.float64)
+        opt.step()
+        O.adamw(cfg, p, g, m, v, step, lr=lr)
+        ref = np.concatenate([t.detach().numpy() for _, _, _, t in tensors])
+        assert np.allclose(p, ref, rtol=1e-13, atol=1e-15), (step, np.abs(p - ref).max())
+        ref_m = np.concatenate([opt.state[t]["exp_avg"].numpy() for _, _, _, t in tensors])
+        ref_v = np.concatenate([opt.state[t]["exp_avg_sq"].numpy() for _, _, _, t in tensors])
+        assert np.allclose(m, ref_m, rtol=1e-13, atol=1e-18)
+        assert np.allclose(v, ref_v, rtol=1e-13, atol=1e-20)
+
+
+@pytest.mark.parametrize("gated", [False, True])
+def test_decay_mask_follows_parameter_names(gated):
+    """The decay mask against the GPT-2 naming rule (matrices and embeddings
+    decay; biases and LayerNorm parameters do not), not against tensor ranks."""
+    cfg = MICRO.replace(rope=gated, gated_mlp=gated, tie_embeddings=gated, linear_bias=not gated)
     mask = O.decay_mask(cfg)
     off = 0
     for name, shape, _ in O.param_table(cfg):
         n = int(np.prod(shape))
-        assert (mask[off:off + n] == (1.0 if len(shape) == 2 else 0.0)).all(), name
+        assert (mask[off:off + n] == (1.0 if _decays_by_name(name) else 0.0)).all(), name
         off += n
+    assert off == mask.size
     assert (O.decay_mask(cfg.replace(wd_on_1d=True)) == 1).all()
 
 

@@ -1,23 +1,37 @@
-// attn_tc.cuh — causal flash attention on tensor cores (bf16 operands, fp32
-// accumulation), forward and backward, as tasks of the persistent kernel.
+// attn_tc.cuh — causal flash attention on the 5th-generation tensor cores
+// (tcgen05, sm_103a), forward and backward, as tasks of the persistent kernel.
 //
-// Head dimension 64, sequence length a multiple of 128.  Tiles move global ->
-// shared with cp.async into 128-byte rows whose 16-byte chunks are XOR-swizzled
-// by (row mod 8), so ldmatrix reads are bank-conflict free.  Products use
-// mma.sync m16n8k16 (bf16 x bf16 -> fp32); the softmax runs on the accumulator
-// fragments in registers with the running-max ("online") rescaling, in base 2.
+// Head dimension 64, sequence length a multiple of 128.  Every operand tile is a
+// 128-row x 64-column bf16 block (one head of 128 tokens) that TMA copies from
+// the [tokens, 3C] qkv buffer (or the [tokens, C] output gradient) into shared
+// memory with the 128-byte swizzle; the products run as tcgen05.mma (kind::f16,
+// M = 128) issued by one thread, with fp32 accumulators in tensor memory
+// (TMEM), and the softmax reads them back with tcgen05.ld: each of the 8 warps
+// owns 32 rows (its TMEM lane quarter) and one half of the columns, one row per
+// thread.  Probabilities and score gradients go back to shared memory as bf16
+// in the K-major swizzled layout the next product reads.
 //
-//   forward, task (b, h, 128 queries):  S = q k^T * scale, causal mask,
-//       running max m and sum l per row, O = sum_j exp(S - m) v / l,
-//       LSE = m + ln l (natural log) saved for the backward pass.
+//   forward, task (b, h, 128 queries), key blocks j = 0 .. diagonal:
+//       S_j = Q K_j^T (TMEM, two buffers: S_{j+1} is computed while S_j is
+//       reduced), running row max m and sum l in registers (base 2), P_j =
+//       exp2(S_j * scale * log2 e - m) to shared memory, O_j = P_j V_j into one of
+//       two TMEM buffers; the thread adds O_j to its 32 output columns, rescaled
+//       by exp2(m_old - m_new), while the next block's probabilities are formed.
+//       O = sum / l, LSE = ln 2 (m + log2 l) saved for the backward pass.
 //   backward pre-pass, task (64 rows):  D_i = sum_c dO_ic O_ic per head.
-//   backward dK/dV, task (b, h, 128 keys): for every query block at or after
-//       the keys: P^T = exp(S^T - LSE), dV += P^T dO, dP^T = V dO^T,
-//       dS^T = P^T (dP^T - D) * scale, dK += dS^T Q.
-//   backward dQ, task (b, h, 128 queries): for every key block up to the
-//       diagonal: P, dP = dO V^T, dS = P (dP - D) * scale, dQ += dS K.
+//   backward dK/dV, task (b, h, 128 keys), query blocks i at or after the keys:
+//       S^T = K Q_i^T and dP^T = V dO_i^T (TMEM), P^T = exp2(S^T scale log2 e -
+//       LSE log2 e), dS^T = P^T (dP^T - D) scale, then dV += P^T dO_i and
+//       dK += dS^T Q_i accumulate in TMEM across the query blocks.
+//   backward dQ, task (b, h, 128 queries), key blocks up to the diagonal:
+//       S = Q K_j^T, dP = dO V_j^T, dS = P (dP - D) scale, dQ += dS K_j in TMEM.
 // dQ and dK/dV are separate tasks (recomputing P) so every output has exactly
 // one writer and the step stays deterministic (no atomics).
+//
+// Algorithm: the online-softmax attention of Dao et al. ("FlashAttention",
+// 2022) in the forward and its recomputation-based backward; the method's
+// pages name the families (attention-forward, attention-key, attention-query:
+// "Coppelius training on the RTX 3090", section "Where a step's time goes").
 #pragma once
 #include "device.cuh"
 #include "tasks_rows.cuh"
@@ -25,100 +39,34 @@
 
 namespace pgs {
 
-constexpr int kAttQ = 128;   // query rows per forward / dQ task (8 warps x 16)
-constexpr int kAttK = 128;   // key rows per dK/dV task (8 warps x 16)
-constexpr int kAttSub = 64;  // rows of the streamed blocks
+constexpr int kAttBlk = 128;                 // rows of every attention tile (queries or keys)
+constexpr uint32_t kAttTile = kAttBlk * 128;  // bytes of a 128 x 64 bf16 tile
+constexpr int kAttPreRows = 64;               // token rows of a backward pre-pass task
 
-__device__ __forceinline__ void cp_async16(uint32_t smem, const void* gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+// mbarriers of the attention tasks (initialised once per launch, phases counted
+// in use[]): Q (or K/V of a dK/dV task) loaded; the streamed pair of tiles of
+// buffer 0/1 loaded; scores of buffer 0/1 complete; products of buffer 0/1 complete.
+enum AttBar : int { AB_FIXED = 0, AB_LD0 = 1, AB_S0 = 3, AB_O0 = 5, AB_NUM = 7 };
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-// d += a (16x16, row) * b (16x8, col)
-__device__ __forceinline__ void mma16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
+struct AttnShared {
+  uint64_t bar[AB_NUM];
+  uint32_t use[AB_NUM];          // phases of each barrier completed so far in this launch
+};
+
+// Small per-task arrays in the dynamic shared memory, above every task's tiles
+// (at most 10 tiles = 160 KB): values exchanged between the two column halves
+// of a row, and the dK/dV task's LSE (base 2) and D of a query block, two buffers.
+constexpr uint32_t kAttScratchOff = 12 * kAttTile;
+struct AttnScratch {
+  float red[2][kAttBlk];
+  float ld[2][2][kAttBlk];
+};
+static_assert(kAttScratchOff + sizeof(AttnScratch) <= (uint32_t)(kTcSmemBytes + 4 * kEpiStageBytes),
+              "attention scratch beyond the dynamic shared memory");
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// byte offset of 16-byte chunk `ch` (0..7) of row r in a swizzled [rows][64] bf16 tile
-__device__ __forceinline__ uint32_t swz(int r, int ch) { return (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4)); }
-
-// rows x 64 bf16 tile from global (row pitch ld elements) into a swizzled smem tile
-__device__ __forceinline__ void tile_load_async(uint32_t s, const __nv_bfloat16* g, int64_t ld, int rows) {
-  for (int e = threadIdx.x; e < rows * 8; e += kThreads) {
-    const int r = e >> 3, ch = e & 7;
-    cp_async16(s + swz(r, ch), g + (int64_t)r * ld + ch * 8);
-  }
-}
-
-// A fragments (16 rows from r0, 64 columns = 4 k-steps) of a swizzled tile
-__device__ __forceinline__ void load_a_frags(uint32_t s, int r0, uint32_t (*f)[4]) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk) ldsm_x4(s + swz(r0 + (lane & 15), kk * 2 + (lane >> 4)), f[kk]);
-}
-
-// acc[8][4] (16 x 64) += A (16 x 64, k = 64 columns of the A fragments) * B^T
-// with B stored [n][k] (64 n-rows x 64 k) in a swizzled tile.
-__device__ __forceinline__ void mma_abt(float (*acc)[4], const uint32_t (*af)[4], uint32_t sb) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-    for (int np = 0; np < 4; ++np) {
-      uint32_t b[4];
-      ldsm_x4(sb + swz(np * 16 + (lane & 7) + ((lane >> 4) << 3), kk * 2 + ((lane >> 3) & 1)), b);
-      mma16816(acc[2 * np], af[kk], b[0], b[1]);
-      mma16816(acc[2 * np + 1], af[kk], b[2], b[3]);
-    }
-}
-
-// Packs a 16 x 64 fp32 accumulator tile into bf16 A fragments (4 k-steps of 16).
-__device__ __forceinline__ void pack_a(const float (*p)[4], uint32_t (*pa)[4]) {
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    pa[t][0] = pack_bf16x2(p[2 * t][0], p[2 * t][1]);
-    pa[t][1] = pack_bf16x2(p[2 * t][2], p[2 * t][3]);
-    pa[t][2] = pack_bf16x2(p[2 * t + 1][0], p[2 * t + 1][1]);
-    pa[t][3] = pack_bf16x2(p[2 * t + 1][2], p[2 * t + 1][3]);
-  }
-}
-
-// acc[8][4] (16 x 64) += A (16 x 64, packed bf16 fragments, k = 64) * B
-// with B stored [k][n] (64 k-rows x 64 n) in a swizzled tile.
-__device__ __forceinline__ void mma_pb(float (*acc)[4], const uint32_t (*pa)[4], uint32_t sb) {
-  const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-#pragma unroll
-    for (int np = 0; np < 4; ++np) {
-      uint32_t b[4];
-      ldsm_x4_t(sb + swz(t * 16 + (lane & 7) + (((lane >> 3) & 1) << 3), np * 2 + (lane >> 4)), b);
-      mma16816(acc[2 * np], pa[t], b[0], b[1]);
-      mma16816(acc[2 * np + 1], pa[t], b[2], b[3]);
-    }
-  }
 }
 
 // Packs the pair (x0, x1) of head dimensions (c, c+1) at position t into bf16,
@@ -135,104 +83,219 @@ __device__ __forceinline__ uint32_t pack_unrotate(const float2* rope, int t, int
   return pack_bf16x2(x0, x1);
 }
 
-__device__ __forceinline__ void zero_acc(float (*acc)[4]) {
+// 32 lanes x 32 consecutive fp32 columns of TMEM (thread i: lane base + i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Row `row` of a 128-row K-major bf16 operand tile in the 128-byte swizzled
+// layout: 32 values (columns 32 q .. 32 q + 31 of the 64 the tile holds) as four
+// 16-byte chunks; chunk c of a row lives at (c ^ (row mod 8)) * 16.
+__device__ __forceinline__ void st_row32_sw128(uint32_t tile, int row, int q, const float* v) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int ch = 4 * q + c;
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(tile + row * 128 + ((ch ^ (row & 7)) << 4)),
+                 "r"(pack_bf16x2(v[8 * c], v[8 * c + 1])), "r"(pack_bf16x2(v[8 * c + 2], v[8 * c + 3])),
+                 "r"(pack_bf16x2(v[8 * c + 4], v[8 * c + 5])), "r"(pack_bf16x2(v[8 * c + 6], v[8 * c + 7]))
+                 : "memory");
+  }
+}
+
+// Descriptors of the operand tiles: K-major (rows = M or N, 64 K-values in a
+// 128-byte row; k-step kk of 16 advances 32 bytes inside the row, a second
+// 64-wide K atom lies kAttTile further) and MN-major (rows = K, 64 N-values in a
+// 128-byte row; k-step kk advances 16 rows = 2048 bytes).
+__device__ __forceinline__ uint64_t att_desc_k(uint32_t tile, int kk) {
+  return smem_desc_sw128(tile + (uint32_t)(kk >> 2) * kAttTile + (uint32_t)(kk & 3) * 32u, 16, 1024);
+}
+__device__ __forceinline__ uint64_t att_desc_mn(uint32_t tile, int kk) {
+  return smem_desc_sw128(tile + (uint32_t)kk * 2048u, 8192, 1024);
+}
+// d (+)= A B^T over K = 16 nk: A K-major [128, K], B K-major [N, K]
+__device__ __forceinline__ void att_mma_kk(uint32_t d, uint32_t a, uint32_t b, int nk, uint32_t idesc, bool acc) {
+#pragma unroll 1
+  for (int kk = 0; kk < nk; ++kk) tc_mma(d, att_desc_k(a, kk), att_desc_k(b, kk), idesc, (acc || kk > 0) ? 1u : 0u);
+}
+// d (+)= A B over K = 16 nk: A K-major [128, K], B MN-major [K, N]
+__device__ __forceinline__ void att_mma_kmn(uint32_t d, uint32_t a, uint32_t b, int nk, uint32_t idesc, bool acc) {
+#pragma unroll 1
+  for (int kk = 0; kk < nk; ++kk) tc_mma(d, att_desc_k(a, kk), att_desc_mn(b, kk), idesc, (acc || kk > 0) ? 1u : 0u);
+}
+
+// Phase bookkeeping: use u (from 0, counted over the launch) of barrier b has parity u & 1.
+struct AttPhases {
+  uint32_t use[AB_NUM];
+  __device__ __forceinline__ void load(const AttnShared& as) {
+#pragma unroll
+    for (int i = 0; i < AB_NUM; ++i) use[i] = *reinterpret_cast<const volatile uint32_t*>(&as.use[i]);
+  }
+  // parity of the k-th use of barrier b in this task
+  __device__ __forceinline__ uint32_t par(int b, int k) const { return (use[b] + (uint32_t)k) & 1u; }
+};
+
+// Number of j in [0, n) with j mod 2 == b.
+__device__ __forceinline__ uint32_t n_parity(int n, int b) { return (uint32_t)((n - b + 1) >> 1); }
+
+// Bounded wait of every calling thread; a failure is recorded in the error words
+// and later waits return at once, so every thread keeps the same control flow.
+__device__ __forceinline__ void att_wait(const KParams& kp, uint32_t bar, uint32_t parity) {
+  (void)mbar_wait(kp, bar, parity);
+}
+
+// Pair barrier of the two warps that share a TMEM lane quarter (column halves).
+__device__ __forceinline__ void pair_sync(int quarter) {
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory");
 }
 
 // ---- forward ----------------------------------------------------------------
-__device__ inline void task_attn_fwd_tc(const AttnArgs& a, int idx, uint8_t* smem) {
+__device__ inline void task_attn_fwd_tc(const KParams& kp, const AttnArgs& a, int idx, uint8_t* smem,
+                                        AttnShared& as, uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nqb = a.T / kAttQ;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int nqb = a.T / kAttBlk;
   const int qb = nqb - 1 - idx % nqb;  // longest blocks are claimed first
   const int h = (idx / nqb) % a.H, b = idx / (nqb * a.H);
-  const int q0 = qb * kAttQ;
-  const int64_t ld = 3 * (int64_t)a.C;
-  const __nv_bfloat16* base = reinterpret_cast<const __nv_bfloat16*>(a.qkv) + (int64_t)b * a.T * ld + h * 64;
-  const uint32_t sQ = smem_u32(smem), sK = sQ + kAttQ * 128, sV = sK + 2 * kAttSub * 128;
-  tile_load_async(sQ, base + (int64_t)q0 * ld, ld, kAttQ);
-  tile_load_async(sK, base + a.C, ld, kAttSub);
-  tile_load_async(sV, base + 2 * a.C, ld, kAttSub);
-  cp_async_commit();
-  const int nkv = (q0 + kAttQ) / kAttSub;
+  const int q0 = qb * kAttBlk, nkb = qb + 1, row0 = b * a.T;
+  const void* map = reinterpret_cast<const uint8_t*>(kp.tmaps) + 128 * a.qkv_map;
+  const uint32_t sQ = smem_u32(smem), sK = sQ + kAttTile, sV = sQ + 3 * kAttTile, sP = sQ + 5 * kAttTile;
+  const uint32_t bar0 = smem_u32(&as.bar[0]);
+  AttnScratch& sc = *reinterpret_cast<AttnScratch*>(smem + kAttScratchOff);
+  AttPhases ph;
+  ph.load(as);
+  const bool leader = threadIdx.x == 0;
+  const int r = quarter * 32 + lane;                        // this thread's query row (TMEM lane)
+  const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+  const uint32_t id_s = idesc_bf16(128, 128, 0, 0), id_o = idesc_bf16(128, 64, 0, 1);
+  auto load_kv = [&](int j) {
+    const int buf = j & 1;
+    const uint32_t bar = bar0 + 8 * (AB_LD0 + buf);
+    mbar_arrive_expect_tx(bar, 2 * kAttTile);
+    tma_load_2d(sK + buf * kAttTile, map, a.C + h * 64, row0 + j * kAttBlk, bar);
+    tma_load_2d(sV + buf * kAttTile, map, 2 * a.C + h * 64, row0 + j * kAttBlk, bar);
+  };
+  auto issue_s = [&](int j) {  // leader: S_j = Q K_j^T into TMEM columns 128 (j & 1)
+    const int buf = j & 1;
+    att_wait(kp, bar0 + 8 * (AB_LD0 + buf), ph.par(AB_LD0 + buf, j >> 1));
+    tc_fence_after();
+    att_mma_kk(tmem + 128u * buf, sQ, sK + buf * kAttTile, 4, id_s, false);
+    tc_commit(bar0 + 8 * (AB_S0 + buf));
+  };
+  if (leader) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier generic writes of this memory
+    mbar_arrive_expect_tx(bar0 + 8 * AB_FIXED, kAttTile);
+    tma_load_2d(sQ, map, h * 64, row0 + q0, bar0 + 8 * AB_FIXED);
+    for (int j = 0; j < min(2, nkb); ++j) load_kv(j);
+    att_wait(kp, bar0 + 8 * AB_FIXED, ph.par(AB_FIXED, 0));
+    issue_s(0);
+  }
+  __syncwarp();
   const float sl2 = a.scale * 1.4426950408889634f;
-  const int row0 = q0 + warp * 16;
-  const int ra = row0 + (lane >> 2), rb = ra + 8;  // this thread's two query rows
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float o[8][4];
-  zero_acc(o);
-  uint32_t qf[4][4];
-  for (int j = 0; j < nkv; ++j) {
-    if (j + 1 < nkv) {
-      const int nb = (j + 1) & 1;
-      tile_load_async(sK + nb * kAttSub * 128, base + a.C + (int64_t)(j + 1) * kAttSub * ld, ld, kAttSub);
-      tile_load_async(sV + nb * kAttSub * 128, base + 2 * a.C + (int64_t)(j + 1) * kAttSub * ld, ld, kAttSub);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+  float o[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) o[i] = 0.f;
+  float m_run = -INFINITY, l_run = 0.f, alpha_pend = 0.f;
+  for (int j = 0; j < nkb; ++j) {
+    const int buf = j & 1;
+    if (leader && j + 1 < nkb) issue_s(j + 1);  // its buffer was last read before the previous block barrier
+    __syncwarp();
+    att_wait(kp, bar0 + 8 * (AB_S0 + buf), ph.par(AB_S0 + buf, j >> 1));
+    __syncwarp();
+    tc_fence_after();
+    float s[64];
+    tmem_ld32(trow + 128u * buf + 64u * half, s);
+    tmem_ld32(trow + 128u * buf + 64u * half + 32u, s + 32);
+    const bool diag = j == nkb - 1;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+      s[i] = (diag && half * 64 + i > r) ? -INFINITY : s[i] * sl2;
+      mx = fmaxf(mx, s[i]);
     }
-    __syncthreads();
-    if (j == 0) load_a_frags(sQ, warp * 16, qf);
-    const int k0 = j * kAttSub;
-    if (k0 <= row0 + 15) {
-      const uint32_t kb = sK + (j & 1) * kAttSub * 128, vb = sV + (j & 1) * kAttSub * 128;
-      float s[8][4];
-      zero_acc(s);
-      mma_abt(s, qf, kb);
-      float mx0 = m0, mx1 = m1;
+    sc.red[half][r] = mx;
+    pair_sync(quarter);
+    const float m_new = fmaxf(m_run, fmaxf(sc.red[0][r], sc.red[1][r]));
+    const float alpha = exp2f(m_run - m_new);
+    float ls = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const int c = k0 + nt * 8 + 2 * (lane & 3);
-        s[nt][0] = c <= ra ? s[nt][0] * sl2 : -INFINITY;
-        s[nt][1] = c + 1 <= ra ? s[nt][1] * sl2 : -INFINITY;
-        s[nt][2] = c <= rb ? s[nt][2] * sl2 : -INFINITY;
-        s[nt][3] = c + 1 <= rb ? s[nt][3] * sl2 : -INFINITY;
-        mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
-        mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
-      }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float al0 = exp2f(m0 - mx0), al1 = exp2f(m1 - mx1);
-      m0 = mx0;
-      m1 = mx1;
-      l0 *= al0;
-      l1 *= al1;
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        o[nt][0] *= al0; o[nt][1] *= al0; o[nt][2] *= al1; o[nt][3] *= al1;
-        s[nt][0] = exp2f(s[nt][0] - mx0);
-        s[nt][1] = exp2f(s[nt][1] - mx0);
-        s[nt][2] = exp2f(s[nt][2] - mx1);
-        s[nt][3] = exp2f(s[nt][3] - mx1);
-        l0 += s[nt][0] + s[nt][1];
-        l1 += s[nt][2] + s[nt][3];
-      }
-      uint32_t pa[4][4];
-      pack_a(s, pa);
-      mma_pb(o, pa, vb);
+    for (int i = 0; i < 64; ++i) {
+      s[i] = exp2f(s[i] - m_new);
+      ls += s[i];
     }
+    l_run = l_run * alpha + ls;
+    m_run = m_new;
+    // P_j (bf16) into buffer buf: its previous reader (the product of block j - 2) completed
+    // before the partial of block j - 2 was added to o in the previous iteration
+    const uint32_t pt = sP + (uint32_t)buf * 2u * kAttTile + (uint32_t)half * kAttTile;
+    st_row32_sw128(pt, r, 0, s);
+    st_row32_sw128(pt, r, 1, s + 32);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic smem writes -> tensor core reads
+    tc_fence_before();
     __syncthreads();
-  }
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  const float i0 = 1.0f / l0, i1 = 1.0f / l1;
-  __nv_bfloat16* O = reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)b * a.T * a.ld_o + h * 64;
+    if (leader) {
+      tc_fence_after();
+      att_mma_kmn(tmem + 256u + 64u * buf, pt - (uint32_t)half * kAttTile, sV + buf * kAttTile, 8, id_o, false);
+      tc_commit(bar0 + 8 * (AB_O0 + buf));
+      if (j + 2 < nkb) {  // K_j and V_j are no longer read: stream in block j + 2
+        att_wait(kp, bar0 + 8 * (AB_O0 + buf), ph.par(AB_O0 + buf, j >> 1));
+        load_kv(j + 2);
+      }
+    }
+    __syncwarp();
+    if (j >= 1) {  // add the partial of block j - 1, rescaled from its running max to this one
+      const int pb = (j - 1) & 1;
+      att_wait(kp, bar0 + 8 * (AB_O0 + pb), ph.par(AB_O0 + pb, (j - 1) >> 1));
+      __syncwarp();
+      tc_fence_after();
+      float part[32];
+      tmem_ld32(trow + 256u + 64u * pb + 32u * half, part);
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-    const int c = nt * 8 + 2 * (lane & 3);
-    *reinterpret_cast<uint32_t*>(O + (int64_t)ra * a.ld_o + c) = pack_bf16x2(o[nt][0] * i0, o[nt][1] * i0);
-    *reinterpret_cast<uint32_t*>(O + (int64_t)rb * a.ld_o + c) = pack_bf16x2(o[nt][2] * i1, o[nt][3] * i1);
+      for (int i = 0; i < 32; ++i) o[i] = o[i] * alpha_pend + part[i];
+    }
+    alpha_pend = alpha;
   }
-  if ((lane & 3) == 0) {
-    float* L = a.lse + ((int64_t)b * a.H + h) * a.T;
-    const float ln2 = 0.6931471805599453f;
-    L[ra] = (m0 + log2f(l0)) * ln2;
-    L[rb] = (m1 + log2f(l1)) * ln2;
+  {
+    const int pb = (nkb - 1) & 1;
+    att_wait(kp, bar0 + 8 * (AB_O0 + pb), ph.par(AB_O0 + pb, (nkb - 1) >> 1));
+    __syncwarp();
+    tc_fence_after();
+    float part[32];
+    tmem_ld32(trow + 256u + 64u * pb + 32u * half, part);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o[i] = o[i] * alpha_pend + part[i];
+  }
+  sc.red[half][r] = l_run;  // every earlier read of red[] came before the last block barrier
+  pair_sync(quarter);
+  const float L = sc.red[0][r] + sc.red[1][r];
+  const float inv = 1.0f / L;
+  uint4* O = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) + (int64_t)(row0 + q0 + r) * a.ld_o +
+                                      h * 64 + half * 32);
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    O[c] = make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv), pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+                      pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv), pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+  if (half == 0) a.lse[((int64_t)b * a.H + h) * a.T + q0 + r] = (m_run + log2f(L)) * 0.6931471805599453f;
+  tc_fence_before();
+  __syncthreads();  // every TMEM read and red[] use of this task is done
+  if (leader) {
+    as.use[AB_FIXED] = ph.use[AB_FIXED] + 1u;
+#pragma unroll
+    for (int bb = 0; bb < 2; ++bb) {
+      as.use[AB_LD0 + bb] = ph.use[AB_LD0 + bb] + n_parity(nkb, bb);
+      as.use[AB_S0 + bb] = ph.use[AB_S0 + bb] + n_parity(nkb, bb);
+      as.use[AB_O0 + bb] = ph.use[AB_O0 + bb] + n_parity(nkb, bb);
+    }
   }
 }
 
@@ -245,7 +308,7 @@ __device__ inline void task_attn_bwd_pre(const AttnArgs& a, int idx) {
   constexpr int kRG = 2, kHG = 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int N = a.B * a.T;
-  const int r0 = idx * kAttSub, r1 = min(r0 + kAttSub, N);
+  const int r0 = idx * kAttPreRows, r1 = min(r0 + kAttPreRows, N);
   const int sub = lane & 7;
   const __nv_bfloat16* dO = reinterpret_cast<const __nv_bfloat16*>(a.dout);
   const __nv_bfloat16* O = reinterpret_cast<const __nv_bfloat16*>(a.o);
@@ -295,173 +358,240 @@ __device__ inline void task_attn_bwd_pre(const AttnArgs& a, int idx) {
 
 // ---- backward dK/dV -------------------------------------------------------------
 template <bool kRope>
-__device__ inline void task_attn_bwd_kv_tc(const AttnArgs& a, int idx, uint8_t* smem) {
+__device__ inline void task_attn_bwd_kv_tc(const KParams& kp, const AttnArgs& a, int idx, uint8_t* smem,
+                                           AttnShared& as, uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nkb = a.T / kAttK;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int nkb = a.T / kAttBlk;
   const int kb = idx % nkb;  // earliest keys see the most queries: claimed first
   const int h = (idx / nkb) % a.H, b = idx / (nkb * a.H);
-  const int k0 = kb * kAttK;
-  const int64_t ld = 3 * (int64_t)a.C;
-  const __nv_bfloat16* base = reinterpret_cast<const __nv_bfloat16*>(a.qkv) + (int64_t)b * a.T * ld + h * 64;
-  const __nv_bfloat16* dOb = reinterpret_cast<const __nv_bfloat16*>(a.dout) + (int64_t)b * a.T * a.C + h * 64;
-  const float* L = a.lse + ((int64_t)b * a.H + h) * a.T;
-  const float* Dv = a.scratch + ((int64_t)b * a.H + h) * a.T;
-  const uint32_t sK = smem_u32(smem), sV = sK + kAttK * 128, sQ = sV + kAttK * 128,
-                 sO = sQ + 2 * kAttSub * 128;
-  float* sL = reinterpret_cast<float*>(smem + (sO - sK) + 2 * kAttSub * 128);  // [2][64] LSE, [2][64] D
-  tile_load_async(sK, base + a.C + (int64_t)k0 * ld, ld, kAttK);
-  tile_load_async(sV, base + 2 * a.C + (int64_t)k0 * ld, ld, kAttK);
-  const int i_first = k0 / kAttSub, nq = a.T / kAttSub;
-  auto load_q = [&](int i, int buf) {
-    tile_load_async(sQ + buf * kAttSub * 128, base + (int64_t)i * kAttSub * ld, ld, kAttSub);
-    tile_load_async(sO + buf * kAttSub * 128, dOb + (int64_t)i * kAttSub * a.C, a.C, kAttSub);
-    for (int e = threadIdx.x; e < 2 * kAttSub; e += kThreads) {
-      const int which = e / kAttSub, r = e % kAttSub;
-      sL[(which * 2 + buf) * kAttSub + r] = which == 0 ? L[i * kAttSub + r] : Dv[i * kAttSub + r];
-    }
+  const int k0 = kb * kAttBlk, row0 = b * a.T, nq = nkb - kb;  // query blocks kb .. nkb - 1
+  const void* qmap = reinterpret_cast<const uint8_t*>(kp.tmaps) + 128 * a.qkv_map;
+  const void* dmap = reinterpret_cast<const uint8_t*>(kp.tmaps) + 128 * a.do_map;
+  const uint32_t sK = smem_u32(smem), sV = sK + kAttTile, sQ = sK + 2 * kAttTile, sO = sK + 4 * kAttTile,
+                 sPt = sK + 6 * kAttTile, sDs = sK + 8 * kAttTile;
+  const uint32_t bar0 = smem_u32(&as.bar[0]);
+  AttnScratch& sc = *reinterpret_cast<AttnScratch*>(smem + kAttScratchOff);
+  AttPhases ph;
+  ph.load(as);
+  const bool leader = threadIdx.x == 0;
+  const int r = quarter * 32 + lane;  // this thread's key row (TMEM lane)
+  const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+  const uint32_t id_s = idesc_bf16(128, 128, 0, 0), id_o = idesc_bf16(128, 64, 0, 1);
+  const float* Lg = a.lse + ((int64_t)b * a.H + h) * a.T;
+  const float* Dg = a.scratch + ((int64_t)b * a.H + h) * a.T;
+  const float log2e = 1.4426950408889634f, sl2 = a.scale * log2e;
+  auto load_qo = [&](int it) {  // leader: Q and dO of query block kb + it into buffer it & 1
+    const int buf = it & 1, i = kb + it;
+    const uint32_t bar = bar0 + 8 * (AB_LD0 + buf);
+    mbar_arrive_expect_tx(bar, 2 * kAttTile);
+    tma_load_2d(sQ + buf * kAttTile, qmap, h * 64, row0 + i * kAttBlk, bar);
+    tma_load_2d(sO + buf * kAttTile, dmap, h * 64, row0 + i * kAttBlk, bar);
   };
-  load_q(i_first, 0);
-  cp_async_commit();
-  const float sl2 = a.scale * 1.4426950408889634f;
-  const float log2e = 1.4426950408889634f;
-  const int key0 = k0 + warp * 16;
-  const int ka = key0 + (lane >> 2), kbr = ka + 8;  // this thread's two key rows
-  float dk[8][4], dv[8][4];
-  zero_acc(dk);
-  zero_acc(dv);
-  for (int i = i_first; i < nq; ++i) {
-    const int buf = (i - i_first) & 1;
-    if (i + 1 < nq) {
-      load_q(i + 1, buf ^ 1);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    const int qi0 = i * kAttSub;
-    if (qi0 + kAttSub - 1 >= key0) {
-      const uint32_t qb_s = sQ + buf * kAttSub * 128, ob_s = sO + buf * kAttSub * 128;
-      const float* lseb = sL + (0 * 2 + buf) * kAttSub;
-      const float* Db = sL + (1 * 2 + buf) * kAttSub;
-      float p[8][4], dp[8][4];
-      uint32_t af[4][4];           // A fragments reloaded from shared memory (register budget)
-      load_a_frags(sK, warp * 16, af);
-      zero_acc(p);
-      mma_abt(p, af, qb_s);        // S^T = K Q^T
-      load_a_frags(sV, warp * 16, af);
-      zero_acc(dp);
-      mma_abt(dp, af, ob_s);       // dP^T = V dO^T
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const int cq = nt * 8 + 2 * (lane & 3);  // query column within the block
-        const float l0 = lseb[cq] * log2e, l1 = lseb[cq + 1] * log2e;
-        const float d0 = Db[cq], d1 = Db[cq + 1];
-        const int q = qi0 + cq;
-        p[nt][0] = q >= ka ? exp2f(p[nt][0] * sl2 - l0) : 0.f;
-        p[nt][1] = q + 1 >= ka ? exp2f(p[nt][1] * sl2 - l1) : 0.f;
-        p[nt][2] = q >= kbr ? exp2f(p[nt][2] * sl2 - l0) : 0.f;
-        p[nt][3] = q + 1 >= kbr ? exp2f(p[nt][3] * sl2 - l1) : 0.f;
-        dp[nt][0] = p[nt][0] * (dp[nt][0] - d0) * a.scale;
-        dp[nt][1] = p[nt][1] * (dp[nt][1] - d1) * a.scale;
-        dp[nt][2] = p[nt][2] * (dp[nt][2] - d0) * a.scale;
-        dp[nt][3] = p[nt][3] * (dp[nt][3] - d1) * a.scale;
-      }
-      uint32_t pa[4][4], pd[4][4];  // P^T and dS^T as bf16 fragments (the fp32 tiles die here)
-      pack_a(p, pa);
-      pack_a(dp, pd);
-      mma_pb(dv, pa, ob_s);  // dV += P^T dO
-      mma_pb(dk, pd, qb_s);  // dK += dS^T Q
-    }
-    __syncthreads();
+  auto stage_ld = [&](int it) {  // all threads: LSE (base 2) and D of query block kb + it
+    const int i = kb + it, c = threadIdx.x & (kAttBlk - 1), w = threadIdx.x >> 7;
+    const float v = w == 0 ? Lg[i * kAttBlk + c] * log2e : Dg[i * kAttBlk + c];
+    sc.ld[it & 1][w][c] = v;
+  };
+  if (leader) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive_expect_tx(bar0 + 8 * AB_FIXED, 2 * kAttTile);
+    tma_load_2d(sK, qmap, a.C + h * 64, row0 + k0, bar0 + 8 * AB_FIXED);
+    tma_load_2d(sV, qmap, 2 * a.C + h * 64, row0 + k0, bar0 + 8 * AB_FIXED);
+    for (int it = 0; it < min(2, nq); ++it) load_qo(it);
   }
-  __nv_bfloat16* dq = reinterpret_cast<__nv_bfloat16*>(a.dqkv) + (int64_t)b * a.T * ld + h * 64;
+  __syncwarp();
+  stage_ld(0);
+  __syncthreads();
+  for (int it = 0; it < nq; ++it) {
+    const int buf = it & 1;
+    if (leader) {  // S^T = K Q_i^T and dP^T = V dO_i^T (their TMEM columns were read before the last block barrier)
+      if (it == 0) att_wait(kp, bar0 + 8 * AB_FIXED, ph.par(AB_FIXED, 0));
+      att_wait(kp, bar0 + 8 * (AB_LD0 + buf), ph.par(AB_LD0 + buf, it >> 1));
+      tc_fence_after();
+      att_mma_kk(tmem, sK, sQ + buf * kAttTile, 4, id_s, false);
+      att_mma_kk(tmem + 128u, sV, sO + buf * kAttTile, 4, id_s, false);
+      tc_commit(bar0 + 8 * AB_S0);
+    }
+    __syncwarp();
+    if (it + 1 < nq) stage_ld(it + 1);  // read after this block's barrier; its buffer was last read before the previous one
+    att_wait(kp, bar0 + 8 * AB_S0, ph.par(AB_S0, it));
+    if (it >= 1) att_wait(kp, bar0 + 8 * AB_O0, ph.par(AB_O0, it - 1));  // the previous products no longer read P^T, dS^T
+    __syncwarp();
+    tc_fence_after();
+    const bool diag = it == 0;  // the key block's own query block: queries before a key are masked
+    const float* lse2 = sc.ld[buf][0];
+    const float* dd = sc.ld[buf][1];
+#pragma unroll 1
+    for (int q = 0; q < 2; ++q) {  // 32 query columns at a time
+      float s[32], dp[32];
+      const int c0 = half * 64 + q * 32;
+      tmem_ld32(trow + (uint32_t)c0, s);
+      tmem_ld32(trow + 128u + (uint32_t)c0, dp);
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-    const int c = nt * 8 + 2 * (lane & 3);
-    *reinterpret_cast<uint32_t*>(dq + (int64_t)ka * ld + a.C + c) = pack_unrotate<kRope>(a.rope, ka, c, dk[nt][0], dk[nt][1]);
-    *reinterpret_cast<uint32_t*>(dq + (int64_t)kbr * ld + a.C + c) = pack_unrotate<kRope>(a.rope, kbr, c, dk[nt][2], dk[nt][3]);
-    *reinterpret_cast<uint32_t*>(dq + (int64_t)ka * ld + 2 * a.C + c) = pack_bf16x2(dv[nt][0], dv[nt][1]);
-    *reinterpret_cast<uint32_t*>(dq + (int64_t)kbr * ld + 2 * a.C + c) = pack_bf16x2(dv[nt][2], dv[nt][3]);
+      for (int e = 0; e < 32; ++e) {
+        const int c = c0 + e;
+        const float p = (diag && c < r) ? 0.f : exp2f(s[e] * sl2 - lse2[c]);
+        s[e] = p;
+        dp[e] = p * (dp[e] - dd[c]) * a.scale;
+      }
+      st_row32_sw128(sPt + (uint32_t)half * kAttTile, r, q, s);
+      st_row32_sw128(sDs + (uint32_t)half * kAttTile, r, q, dp);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    if (leader) {  // dV += P^T dO_i, dK += dS^T Q_i
+      tc_fence_after();
+      att_mma_kmn(tmem + 256u, sPt, sO + buf * kAttTile, 8, id_o, it > 0);
+      att_mma_kmn(tmem + 320u, sDs, sQ + buf * kAttTile, 8, id_o, it > 0);
+      tc_commit(bar0 + 8 * AB_O0);
+      if (it + 2 < nq) {  // Q_i and dO_i are no longer read: stream in block i + 2
+        att_wait(kp, bar0 + 8 * AB_O0, ph.par(AB_O0, it));
+        load_qo(it + 2);
+      }
+    }
+    __syncwarp();
+  }
+  att_wait(kp, bar0 + 8 * AB_O0, ph.par(AB_O0, nq - 1));
+  __syncwarp();
+  tc_fence_after();
+  const int64_t ld = 3 * (int64_t)a.C;
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.dqkv) + (int64_t)(row0 + k0 + r) * ld + h * 64 + half * 32;
+  {
+    float v[32];
+    tmem_ld32(trow + 256u + 32u * half, v);  // dV
+    uint4* dst = reinterpret_cast<uint4*>(out + 2 * a.C);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      dst[c] = make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]), pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                          pack_bf16x2(v[8 * c + 4], v[8 * c + 5]), pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
+    tmem_ld32(trow + 320u + 32u * half, v);  // dK (rotated back to the projection's frame with rotary embedding)
+    const int t = k0 + r;
+    uint32_t w[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) w[e] = pack_unrotate<kRope>(a.rope, t, half * 32 + 2 * e, v[2 * e], v[2 * e + 1]);
+    dst = reinterpret_cast<uint4*>(out + a.C);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (leader) {
+    as.use[AB_FIXED] = ph.use[AB_FIXED] + 1u;
+    as.use[AB_LD0] = ph.use[AB_LD0] + n_parity(nq, 0);
+    as.use[AB_LD0 + 1] = ph.use[AB_LD0 + 1] + n_parity(nq, 1);
+    as.use[AB_S0] = ph.use[AB_S0] + (uint32_t)nq;
+    as.use[AB_O0] = ph.use[AB_O0] + (uint32_t)nq;
   }
 }
 
 // ---- backward dQ ------------------------------------------------------------------
 template <bool kRope>
-__device__ inline void task_attn_bwd_q_tc(const AttnArgs& a, int idx, uint8_t* smem) {
+__device__ inline void task_attn_bwd_q_tc(const KParams& kp, const AttnArgs& a, int idx, uint8_t* smem,
+                                          AttnShared& as, uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nqb = a.T / kAttQ;
+  const int quarter = warp & 3, half = warp >> 2;
+  const int nqb = a.T / kAttBlk;
   const int qb = nqb - 1 - idx % nqb;
   const int h = (idx / nqb) % a.H, b = idx / (nqb * a.H);
-  const int q0 = qb * kAttQ;
-  const int64_t ld = 3 * (int64_t)a.C;
-  const __nv_bfloat16* base = reinterpret_cast<const __nv_bfloat16*>(a.qkv) + (int64_t)b * a.T * ld + h * 64;
-  const __nv_bfloat16* dOb = reinterpret_cast<const __nv_bfloat16*>(a.dout) + (int64_t)b * a.T * a.C + h * 64;
-  const uint32_t sQ = smem_u32(smem), sO = sQ + kAttQ * 128, sK = sO + kAttQ * 128,
-                 sV = sK + 2 * kAttSub * 128;
-  tile_load_async(sQ, base + (int64_t)q0 * ld, ld, kAttQ);
-  tile_load_async(sO, dOb + (int64_t)q0 * a.C, a.C, kAttQ);
-  tile_load_async(sK, base + a.C, ld, kAttSub);
-  tile_load_async(sV, base + 2 * a.C, ld, kAttSub);
-  cp_async_commit();
-  const int nkv = (q0 + kAttQ) / kAttSub;
-  const float sl2 = a.scale * 1.4426950408889634f;
-  const float log2e = 1.4426950408889634f;
-  const int row0 = q0 + warp * 16;
-  const int ra = row0 + (lane >> 2), rb = ra + 8;
-  const float* L = a.lse + ((int64_t)b * a.H + h) * a.T;
-  const float* Dv = a.scratch + ((int64_t)b * a.H + h) * a.T;
-  const float la = L[ra] * log2e, lb = L[rb] * log2e, da = Dv[ra], db = Dv[rb];
-  float dq[8][4];
-  zero_acc(dq);
-  uint32_t qf[4][4], of[4][4];
-  for (int j = 0; j < nkv; ++j) {
-    if (j + 1 < nkv) {
-      const int nb = (j + 1) & 1;
-      tile_load_async(sK + nb * kAttSub * 128, base + a.C + (int64_t)(j + 1) * kAttSub * ld, ld, kAttSub);
-      tile_load_async(sV + nb * kAttSub * 128, base + 2 * a.C + (int64_t)(j + 1) * kAttSub * ld, ld, kAttSub);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    if (j == 0) {
-      load_a_frags(sQ, warp * 16, qf);
-      load_a_frags(sO, warp * 16, of);
-    }
-    const int k0 = j * kAttSub;
-    if (k0 <= row0 + 15) {
-      const uint32_t kb = sK + (j & 1) * kAttSub * 128, vb = sV + (j & 1) * kAttSub * 128;
-      float p[8][4], dp[8][4];
-      zero_acc(p);
-      mma_abt(p, qf, kb);   // S = Q K^T
-      zero_acc(dp);
-      mma_abt(dp, of, vb);  // dP = dO V^T
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const int c = k0 + nt * 8 + 2 * (lane & 3);
-        p[nt][0] = c <= ra ? exp2f(p[nt][0] * sl2 - la) : 0.f;
-        p[nt][1] = c + 1 <= ra ? exp2f(p[nt][1] * sl2 - la) : 0.f;
-        p[nt][2] = c <= rb ? exp2f(p[nt][2] * sl2 - lb) : 0.f;
-        p[nt][3] = c + 1 <= rb ? exp2f(p[nt][3] * sl2 - lb) : 0.f;
-        p[nt][0] *= (dp[nt][0] - da) * a.scale;
-        p[nt][1] *= (dp[nt][1] - da) * a.scale;
-        p[nt][2] *= (dp[nt][2] - db) * a.scale;
-        p[nt][3] *= (dp[nt][3] - db) * a.scale;
-      }
-      uint32_t pa[4][4];
-      pack_a(p, pa);
-      mma_pb(dq, pa, kb);  // dQ += dS K
-    }
-    __syncthreads();
+  const int q0 = qb * kAttBlk, row0 = b * a.T, nkb = qb + 1;
+  const void* qmap = reinterpret_cast<const uint8_t*>(kp.tmaps) + 128 * a.qkv_map;
+  const void* dmap = reinterpret_cast<const uint8_t*>(kp.tmaps) + 128 * a.do_map;
+  const uint32_t sQ = smem_u32(smem), sO = sQ + kAttTile, sK = sQ + 2 * kAttTile, sV = sQ + 4 * kAttTile,
+                 sDs = sQ + 6 * kAttTile;
+  const uint32_t bar0 = smem_u32(&as.bar[0]);
+  AttPhases ph;
+  ph.load(as);
+  const bool leader = threadIdx.x == 0;
+  const int r = quarter * 32 + lane;  // this thread's query row (TMEM lane)
+  const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+  const uint32_t id_s = idesc_bf16(128, 128, 0, 0), id_o = idesc_bf16(128, 64, 0, 1);
+  const float log2e = 1.4426950408889634f, sl2 = a.scale * log2e;
+  const float lse2 = a.lse[((int64_t)b * a.H + h) * a.T + q0 + r] * log2e;
+  const float dd = a.scratch[((int64_t)b * a.H + h) * a.T + q0 + r];
+  auto load_kv = [&](int j) {
+    const int buf = j & 1;
+    const uint32_t bar = bar0 + 8 * (AB_LD0 + buf);
+    mbar_arrive_expect_tx(bar, 2 * kAttTile);
+    tma_load_2d(sK + buf * kAttTile, qmap, a.C + h * 64, row0 + j * kAttBlk, bar);
+    tma_load_2d(sV + buf * kAttTile, qmap, 2 * a.C + h * 64, row0 + j * kAttBlk, bar);
+  };
+  if (leader) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive_expect_tx(bar0 + 8 * AB_FIXED, 2 * kAttTile);
+    tma_load_2d(sQ, qmap, h * 64, row0 + q0, bar0 + 8 * AB_FIXED);
+    tma_load_2d(sO, dmap, h * 64, row0 + q0, bar0 + 8 * AB_FIXED);
+    for (int j = 0; j < min(2, nkb); ++j) load_kv(j);
   }
-  __nv_bfloat16* dqp = reinterpret_cast<__nv_bfloat16*>(a.dqkv) + (int64_t)b * a.T * ld + h * 64;
+  __syncwarp();
+  for (int j = 0; j < nkb; ++j) {
+    const int buf = j & 1;
+    if (leader) {  // S = Q K_j^T, dP = dO V_j^T (their TMEM columns were read before the last block barrier)
+      if (j == 0) att_wait(kp, bar0 + 8 * AB_FIXED, ph.par(AB_FIXED, 0));
+      att_wait(kp, bar0 + 8 * (AB_LD0 + buf), ph.par(AB_LD0 + buf, j >> 1));
+      tc_fence_after();
+      att_mma_kk(tmem, sQ, sK + buf * kAttTile, 4, id_s, false);
+      att_mma_kk(tmem + 128u, sO, sV + buf * kAttTile, 4, id_s, false);
+      tc_commit(bar0 + 8 * AB_S0);
+    }
+    __syncwarp();
+    att_wait(kp, bar0 + 8 * AB_S0, ph.par(AB_S0, j));
+    if (j >= 1) att_wait(kp, bar0 + 8 * AB_O0, ph.par(AB_O0, j - 1));  // the previous product no longer reads dS
+    __syncwarp();
+    tc_fence_after();
+    const bool diag = j == nkb - 1;  // keys after a query are masked
+#pragma unroll 1
+    for (int q = 0; q < 2; ++q) {
+      float s[32], dp[32];
+      const int c0 = half * 64 + q * 32;
+      tmem_ld32(trow + (uint32_t)c0, s);
+      tmem_ld32(trow + 128u + (uint32_t)c0, dp);
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-    const int c = nt * 8 + 2 * (lane & 3);
-    *reinterpret_cast<uint32_t*>(dqp + (int64_t)ra * ld + c) = pack_unrotate<kRope>(a.rope, ra, c, dq[nt][0], dq[nt][1]);
-    *reinterpret_cast<uint32_t*>(dqp + (int64_t)rb * ld + c) = pack_unrotate<kRope>(a.rope, rb, c, dq[nt][2], dq[nt][3]);
+      for (int e = 0; e < 32; ++e) {
+        const int c = c0 + e;
+        const float p = (diag && c > r) ? 0.f : exp2f(s[e] * sl2 - lse2);
+        dp[e] = p * (dp[e] - dd) * a.scale;
+      }
+      st_row32_sw128(sDs + (uint32_t)half * kAttTile, r, q, dp);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    if (leader) {  // dQ += dS K_j
+      tc_fence_after();
+      att_mma_kmn(tmem + 256u, sDs, sK + buf * kAttTile, 8, id_o, j > 0);
+      tc_commit(bar0 + 8 * AB_O0);
+      if (j + 2 < nkb) {  // K_j and V_j are no longer read: stream in block j + 2
+        att_wait(kp, bar0 + 8 * AB_O0, ph.par(AB_O0, j));
+        load_kv(j + 2);
+      }
+    }
+    __syncwarp();
+  }
+  att_wait(kp, bar0 + 8 * AB_O0, ph.par(AB_O0, nkb - 1));
+  __syncwarp();
+  tc_fence_after();
+  {
+    float v[32];
+    tmem_ld32(trow + 256u + 32u * half, v);
+    const int t = q0 + r;
+    uint32_t w[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) w[e] = pack_unrotate<kRope>(a.rope, t, half * 32 + 2 * e, v[2 * e], v[2 * e + 1]);
+    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.dqkv) +
+                                          (int64_t)(row0 + t) * 3 * a.C + h * 64 + half * 32);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (leader) {
+    as.use[AB_FIXED] = ph.use[AB_FIXED] + 1u;
+    as.use[AB_LD0] = ph.use[AB_LD0] + n_parity(nkb, 0);
+    as.use[AB_LD0 + 1] = ph.use[AB_LD0 + 1] + n_parity(nkb, 1);
+    as.use[AB_S0] = ph.use[AB_S0] + (uint32_t)nkb;
+    as.use[AB_O0] = ph.use[AB_O0] + (uint32_t)nkb;
   }
 }
 

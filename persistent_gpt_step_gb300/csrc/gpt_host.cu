@@ -286,6 +286,23 @@ constexpr int64_t kAdamChunk = 65536;
 
 int ln_tasks(int N) { return (N + kRowsLn - 1) / kRowsLn; }
 
+// Rows per LayerNorm-backward task.  On the bf16 path (C = 128 NV, NV <= 8) a
+// task stages its rows of `arrays` fp32 [rows, C] inputs in shared memory (dy
+// and its split-K partials, x, the incoming residual gradient): 16 rows when
+// they fit beside nothing else (the GEMM ring's space), else 8; otherwise the
+// register path with kRowsLn rows.
+int ln_bwd_rows(const gpt_config& c, int arrays) {
+  if (c.dtype != GPT_DTYPE_BF16 || c.d_model % 128 || c.d_model > 1024) return kRowsLn;
+  const size_t budget = (size_t)kTcSmemBytes + 4 * kEpiStageBytes;
+  for (int rows : {16, 8})
+    if ((size_t)arrays * rows * c.d_model * 4 <= budget) return rows;
+  return kRowsLn;
+}
+bool ln_bwd_staged(const gpt_config& c, int arrays) { return ln_bwd_rows(c, arrays) != kRowsLn; }
+// arrays a LayerNorm backward reads: a layer's (dy, x, dres_in); the final one's (dy splits, x)
+int ln_bwd_arrays_layer() { return 3; }
+int ln_bwd_arrays_final(int lm_ksplit) { return lm_ksplit + 1; }
+
 // own_state = false: the caller owns the parameters and AdamW moments (the
 // allocation-free step), so the arena holds no regions for them.
 Layout make_layout(const gpt_config& c, size_t nparams, int lm_ksplit, bool own_state = true) {
@@ -295,7 +312,10 @@ Layout make_layout(const gpt_config& c, size_t nparams, int lm_ksplit, bool own_
   const size_t act = is_bf16(c) ? 2 : 4;
   const int L = c.n_layer;
   const size_t BHT = (size_t)c.batch * c.n_head * c.seq_len;
-  const size_t nrb = ln_tasks((int)N);
+  // gain / bias partials: one row per LayerNorm-backward task
+  const size_t nrb = (N + ln_bwd_rows(c, ln_bwd_arrays_layer()) - 1) / ln_bwd_rows(c, ln_bwd_arrays_layer());
+  const size_t nrb_f = (N + ln_bwd_rows(c, ln_bwd_arrays_final(lm_ksplit)) - 1) /
+                       ln_bwd_rows(c, ln_bwd_arrays_final(lm_ksplit));
   // activations a weight-gradient GEMM reads as its second operand carry a
   // 64-column pad whose first column is 1 (bias gradients come out of the GEMM)
   const size_t pad = c.linear_bias ? 64 : 0;
@@ -347,8 +367,8 @@ Layout make_layout(const gpt_config& c, size_t nparams, int lm_ksplit, bool own_
     Lo.ln2_gp.push_back(b.take(nrb * C * 4));
     Lo.ln2_bp.push_back(b.take(nrb * C * 4));
   }
-  Lo.lnf_gp = b.take(nrb * C * 4);
-  Lo.lnf_bp = b.take(nrb * C * 4);
+  Lo.lnf_gp = b.take(nrb_f * C * 4);
+  Lo.lnf_bp = b.take(nrb_f * C * 4);
   Lo.rope = c.rope ? b.take((size_t)c.seq_len * 32 * 8) : 0;
   Lo.sorted_tok = b.take(N * 4);
   Lo.sorted_pos = b.take(N * 4);
@@ -490,7 +510,9 @@ struct Builder {
     switch (o.type) {
       case OP_EMBED: rows_task(o.emb.rows_per_task, 12.0 * D.C); break;
       case OP_LN_FWD: rows_task(o.lnf.rows_per_task, 6.0 * D.C); break;
-      case OP_LN_BWD: rows_task(o.lnb.rows_per_task, 36.0 * D.C); break;  // 18C bytes a row, at half the stream rate (traced)
+      case OP_LN_BWD:  // 18C bytes a row; the register path streams at half the rate (traced)
+        rows_task(o.lnb.rows_per_task, (o.lnb.staged ? 18.0 : 36.0) * D.C);
+        break;
       case OP_CE: rows_task(o.ce.rows_per_task, 6.0 * D.V); break;
       case OP_ATTN_BWD_PRE: rows_task(64, 4.0 * D.C); break;
       case OP_GEMM: {
@@ -763,6 +785,7 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
                     N, D.B, D.T, C, V, kRowsEmb, nullptr, nullptr, nullptr};
   int prev = bld.add(o, {});
   std::vector<int> op_ln1(L), op_qkv(L), op_attn(L), op_atto(L), op_ln2(L), op_up(L), op_down(L);
+  std::vector<int> qkv_maps(L, -1);
   const int qblock = D.T <= 512 ? 64 : 32;
   for (int l = 0; l < L; ++l) {
     const TensorIds& id = h->lid[l];
@@ -779,7 +802,11 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
     op_qkv[l] = bld.add(o, {op_ln1[l]});
     o = blank(OP_ATTN_FWD, bf ? D.B * D.H * (D.T / 128) : D.B * D.H * ((D.T + qblock - 1) / qblock));
     o.attn = AttnArgs{ACT(Lo.qkv[l]), ACT(Lo.atto[l]), F32(Lo.lse[l]), nullptr, nullptr, nullptr,
-                      D.B, D.T, D.H, D.d, C, qblock, 1.0f / std::sqrt((float)D.d), LDC};
+                      D.B, D.T, D.H, D.d, C, qblock, 1.0f / std::sqrt((float)D.d), LDC, nullptr, -1, -1};
+    if (bf) {  // the attention tasks' TMA boxes: one head (64 columns) of 128 tokens
+      o.attn.qkv_map = qkv_maps[l] = make_tmap(h, Lo.qkv[l] + A, 3 * C, N, 3 * C, 128);
+      if (qkv_maps[l] < 0) return fail(h, GPT_ERR_CUDA, "cuTensorMapEncodeTiled failed (qkv)");
+    }
     op_attn[l] = bld.add(o, {op_qkv[l]});
     // xm = x + o . Wo^T + b
     if ((rc = gemm_op(h, &o, N, C, C, {ACT(Lo.atto[l]), LDC, false}, {W(id.w_o), C, false}, EPI_RESID, 1)))
@@ -852,17 +879,22 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
   const int op_lm_dw = bld.add(o, {op_ce});
   if (!tied) adam(h->t_wlm, {op_lm_dw, op_lm_dx});  // tied: wte's update follows the embedding gradient
   // final LayerNorm backward
-  const int nrb = ln_tasks(N);
-  o = blank(OP_LN_BWD, nrb);
+  const int rows_f = ln_bwd_rows(c, ln_bwd_arrays_final(lm_ksplit));
+  const int nrb_f = (N + rows_f - 1) / rows_f;
+  o = blank(OP_LN_BWD, nrb_f);
   o.lnb = LnBwdArgs{F32(Lo.daf), lm_ksplit, (int64_t)N * C, F32(Lo.x[L]), F32(Lo.lnf_mu), F32(Lo.lnf_rs),
                     P(h->t_lnf_g), nullptr, F32(Lo.dx[L]), ACT(Lo.dx_act[L]), F32(Lo.lnf_gp),
-                    h->t_lnf_b >= 0 ? F32(Lo.lnf_bp) : nullptr, N, C, kRowsLn};
+                    h->t_lnf_b >= 0 ? F32(Lo.lnf_bp) : nullptr, N, C, rows_f,
+                    ln_bwd_staged(c, ln_bwd_arrays_final(lm_ksplit)) ? 1 : 0};
   int op_dres = bld.add(o, {op_lm_dx});
+  const int rows_l = ln_bwd_rows(c, ln_bwd_arrays_layer());
+  const int nrb = (N + rows_l - 1) / rows_l;
+  const int staged_l = ln_bwd_staged(c, ln_bwd_arrays_layer()) ? 1 : 0;
   {
-    const int r1 = colsum(F32(Lo.lnf_gp), true, C, nrb, C, G(h->t_lnf_g), op_dres);
+    const int r1 = colsum(F32(Lo.lnf_gp), true, C, nrb_f, C, G(h->t_lnf_g), op_dres);
     adam(h->t_lnf_g, {r1});
     if (h->t_lnf_b >= 0) {
-      const int r2 = colsum(F32(Lo.lnf_bp), true, C, nrb, C, G(h->t_lnf_b), op_dres);
+      const int r2 = colsum(F32(Lo.lnf_bp), true, C, nrb_f, C, G(h->t_lnf_b), op_dres);
       adam(h->t_lnf_b, {r2});
     }
   }
@@ -897,7 +929,7 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
     o = blank(OP_LN_BWD, nrb);
     o.lnb = LnBwdArgs{F32(Lo.da2[l]), 1, 0, F32(Lo.xm[l]), F32(Lo.ln2_mu[l]), F32(Lo.ln2_rs[l]), P(id.ln2_g),
                       F32(Lo.dx[l + 1]), F32(Lo.dxm[l]), ACT(Lo.dxm_act[l]), F32(Lo.ln2_gp[l]),
-                      id.ln2_b >= 0 ? F32(Lo.ln2_bp[l]) : nullptr, N, C, kRowsLn};
+                      id.ln2_b >= 0 ? F32(Lo.ln2_bp[l]) : nullptr, N, C, rows_l, staged_l};
     const int op_ln2b = bld.add(o, {op_up_dx, op_dres});
     adam(id.ln2_g, {colsum(F32(Lo.ln2_gp[l]), true, C, nrb, C, G(id.ln2_g), op_ln2b)});
     if (id.ln2_b >= 0) adam(id.ln2_b, {colsum(F32(Lo.ln2_bp[l]), true, C, nrb, C, G(id.ln2_b), op_ln2b)});
@@ -914,9 +946,14 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
     if (id.b_o >= 0) adam(id.b_o, {op_atto_dw});
     adam(id.w_o, {op_atto_dw, op_atto_dx});
     // attention backward -> dqkv
-    const AttnArgs att{ACT(Lo.qkv[l]), ACT(Lo.atto[l]), F32(Lo.lse[l]), ACT(Lo.dO[l]), ACT(Lo.dqkv[l]),
-                       F32(Lo.att_scr[l]), D.B, D.T, D.H, D.d, C, qblock, 1.0f / std::sqrt((float)D.d), LDC,
-                       rope_cs};
+    AttnArgs att{ACT(Lo.qkv[l]), ACT(Lo.atto[l]), F32(Lo.lse[l]), ACT(Lo.dO[l]), ACT(Lo.dqkv[l]),
+                 F32(Lo.att_scr[l]), D.B, D.T, D.H, D.d, C, qblock, 1.0f / std::sqrt((float)D.d), LDC,
+                 rope_cs, -1, -1};
+    if (bf) {
+      att.qkv_map = qkv_maps[l];
+      att.do_map = make_tmap(h, Lo.dO[l] + A, C, N, C, 128);
+      if (att.do_map < 0) return fail(h, GPT_ERR_CUDA, "cuTensorMapEncodeTiled failed (dO)");
+    }
     int op_attb, op_attb2 = -1;
     if (bf) {
       o = blank(OP_ATTN_BWD_PRE, N / 64);
@@ -950,7 +987,7 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
     o = blank(OP_LN_BWD, nrb);
     o.lnb = LnBwdArgs{F32(Lo.da1[l]), 1, 0, F32(Lo.x[l]), F32(Lo.ln1_mu[l]), F32(Lo.ln1_rs[l]), P(id.ln1_g),
                       F32(Lo.dxm[l]), F32(Lo.dx[l]), ACT(Lo.dx_act[l]), F32(Lo.ln1_gp[l]),
-                      id.ln1_b >= 0 ? F32(Lo.ln1_bp[l]) : nullptr, N, C, kRowsLn};
+                      id.ln1_b >= 0 ? F32(Lo.ln1_bp[l]) : nullptr, N, C, rows_l, staged_l};
     op_dres = bld.add(o, {op_qkv_dx, op_ln2b});
     adam(id.ln1_g, {colsum(F32(Lo.ln1_gp[l]), true, C, nrb, C, G(id.ln1_g), op_dres)});
     if (id.ln1_b >= 0) adam(id.ln1_b, {colsum(F32(Lo.ln1_bp[l]), true, C, nrb, C, G(id.ln1_b), op_dres)});
@@ -1783,8 +1820,13 @@ int gpt_test_attention(int32_t dtype, int32_t B, int32_t T, int32_t H, int32_t d
   cudaDeviceGetAttribute(&h.num_sms, cudaDevAttrMultiProcessorCount, h.device);
   h.D = Dims{1, H * d, H, d, 64, 64, T, B, B * T};
   const int qblock = T <= 512 ? 64 : 32;
-  const AttnArgs att{qkv, o, lse, dout, dqkv, scratch, B, T, H, d, H * d, qblock, 1.0f / std::sqrt((float)d),
-                     H * d};
+  AttnArgs att{qkv, o, lse, dout, dqkv, scratch, B, T, H, d, H * d, qblock, 1.0f / std::sqrt((float)d),
+               H * d, nullptr, -1, -1};
+  if (dtype == GPT_DTYPE_BF16) {  // TMA boxes of one head (64 columns) x 128 tokens
+    att.qkv_map = make_tmap(&h, qkv, 3 * H * d, (int64_t)B * T, 3 * H * d, 128);
+    att.do_map = make_tmap(&h, dout, H * d, (int64_t)B * T, H * d, 128);
+    if (att.qkv_map < 0 || att.do_map < 0) return fail(nullptr, GPT_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  }
   Builder bld{&h};
   OpDesc op = blank(OP_ATTN_FWD, dtype == GPT_DTYPE_BF16 ? B * H * (T / 128) : B * H * ((T + qblock - 1) / qblock));
   op.attn = att;

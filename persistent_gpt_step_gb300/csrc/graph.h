@@ -117,6 +117,7 @@ struct LnBwdArgs {
   float* dres_out; void* dres_act;
   float* dg_part; float* db_part;   // [tasks, C]; db_part may be null
   int32_t rows, C, rows_per_task;
+  int32_t staged;   // bf16 path: the task's rows of dy, x, dres_in are bulk-copied into shared memory
 };
 
 struct AttnArgs {
@@ -130,6 +131,9 @@ struct AttnArgs {
   float scale;
   int32_t ld_o;     // row pitch of o (>= C)
   const float2* rope;  // rotary embedding (cos, sin) [T][d/2]: the backward rotates dq, dk back; null = none
+  // tensor-core path: tensor maps (indices into KParams::tmaps) of qkv [B*T, 3C] and
+  // dout [B*T, C], 64-column x 128-row boxes with the 128-byte swizzle; -1 = none
+  int32_t qkv_map, do_map;
 };
 
 struct CeArgs {

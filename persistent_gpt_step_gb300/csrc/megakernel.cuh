@@ -19,6 +19,7 @@ namespace pgs {
 
 struct KernelShared {
   GemmShared gemm;
+  AttnShared att;
   uint64_t adam_bars[kAdamStages];
   uint32_t adam_iter;
   uint32_t tmem_base;
@@ -60,6 +61,10 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
         mbar_init(smem_u32(&sh.gemm.acc_empty[i]), 4);  // each epilogue warp drained it
       }
       sh.gemm.prod_claim = 0;
+      for (int i = 0; i < AB_NUM; ++i) {
+        mbar_init(smem_u32(&sh.att.bar[i]), 1);  // one arrival: a TMA expect-tx or a tcgen05 commit
+        sh.att.use[i] = 0;
+      }
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -118,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
       case OP_ATTN_FWD:
         {
           const AttnArgs a = op.attn;
-          if constexpr (kTC) task_attn_fwd_tc(a, idx, smem);
+          if constexpr (kTC) task_attn_fwd_tc(kp, a, idx, smem, sh.att, sh.tmem_base);
           else task_attn_fwd_simt<act_t>(a, idx, reinterpret_cast<float*>(smem));
         }
         break;
@@ -126,10 +131,10 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
         if constexpr (kTC) { const AttnArgs a = op.attn; task_attn_bwd_pre(a, idx); }
         break;
       case OP_ATTN_BWD_KV:
-        if constexpr (kTC) { const AttnArgs a = op.attn; task_attn_bwd_kv_tc<kExt>(a, idx, smem); }
+        if constexpr (kTC) { const AttnArgs a = op.attn; task_attn_bwd_kv_tc<kExt>(kp, a, idx, smem, sh.att, sh.tmem_base); }
         break;
       case OP_ATTN_BWD_Q:
-        if constexpr (kTC) { const AttnArgs a = op.attn; task_attn_bwd_q_tc<kExt>(a, idx, smem); }
+        if constexpr (kTC) { const AttnArgs a = op.attn; task_attn_bwd_q_tc<kExt>(kp, a, idx, smem, sh.att, sh.tmem_base); }
         break;
       case OP_CE:
         {
@@ -144,7 +149,11 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
         }
         break;
       case OP_LOSS: { const LossArgs a = op.loss; task_loss(kp, a, reinterpret_cast<float*>(smem)); } break;
-      case OP_LN_BWD: { const LnBwdArgs a = op.lnb; task_ln_bwd<act_t>(a, idx, reinterpret_cast<float*>(smem)); } break;
+      case OP_LN_BWD: {
+        const LnBwdArgs a = op.lnb;
+        if (kTC && a.staged) task_ln_bwd_staged_any<act_t>(kp, a, idx, smem, sh.adam_bars, &sh.adam_iter);
+        else task_ln_bwd<act_t>(a, idx, reinterpret_cast<float*>(smem));
+      } break;
       case OP_COLSUM: { const ColsumArgs a = op.colsum; task_colsum<act_t>(a, idx, reinterpret_cast<float*>(smem)); } break;
       case OP_ATTN_BWD: { const AttnArgs a = op.attn; task_attn_bwd_simt<act_t>(a, idx, reinterpret_cast<float*>(smem)); } break;
       case OP_EMBED_BWD_WTE: { const EmbedArgs a = op.emb; task_embed_bwd_wte(kp, a, idx, reinterpret_cast<int*>(smem)); } break;

@@ -298,6 +298,121 @@ __device__ inline void task_ln_bwd(const LnBwdArgs& a, int idx, float* smem) {
   }
 }
 
+// LayerNorm backward of a block of rows (same formulas as task_ln_bwd) with
+// every input staged in shared memory first: thread 0 issues one bulk copy per
+// array (dy and its split-K partials, x, the incoming residual gradient: the
+// task's rows of each are contiguous), all in flight together, so the task
+// waits about one memory latency instead of one per row a warp handles.  A
+// warp then reduces its rows (C = 128 NV; lane holds float4 lane + 32 i) from
+// shared memory and writes dres_out and its act copy with coalesced stores.
+// The gain / bias partials of a warp's rows are summed in registers in row
+// order, then across warps in warp order (a fixed order: steps stay bitwise
+// repeatable).  Shared memory: (dy_splits + 1 + [dres_in]) x rows x C x 4 bytes.
+template <typename act_t, int NV>
+__device__ inline void task_ln_bwd_staged(const KParams& kp, const LnBwdArgs& a, int idx, uint8_t* smem,
+                                          uint64_t* bars, uint32_t* iter) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r0 = idx * a.rows_per_task, r1 = min(r0 + a.rows_per_task, a.rows);
+  const int nr = r1 - r0;
+  const int S = a.dy_splits;
+  const uint32_t blk = (uint32_t)nr * (uint32_t)a.C * 4u;   // bytes of one array's rows (a multiple of 512)
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t it = *iter;
+  const uint32_t bar = smem_u32(bars) + 8u * (it % kAdamStages);
+  const uint32_t phase = (it / kAdamStages) & 1u;
+  if (threadIdx.x == 0) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier generic use of this memory
+    const uint32_t total = blk * (uint32_t)(S + 1 + (a.dres_in ? 1 : 0));
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(total) : "memory");
+    const int64_t off = (int64_t)r0 * a.C;
+    for (int sp = 0; sp < S; ++sp) bulk_load(sbase + sp * blk, a.dy + sp * a.dy_split_stride + off, blk, bar);
+    bulk_load(sbase + S * blk, a.x + off, blk, bar);
+    if (a.dres_in) bulk_load(sbase + (S + 1) * blk, a.dres_in + off, blk, bar);
+  }
+  float4 g[NV], pg[NV], pb[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    g[i] = *reinterpret_cast<const float4*>(a.g + 4 * (lane + 32 * i));
+    pg[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    pb[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const bool ok = __syncthreads_and(mbar_wait(kp, bar, phase));
+  if (threadIdx.x == 0) *iter = it + 1u;  // this stage's phase is used (read by the next task after the block barrier)
+  if (!ok) return;  // every thread leaves together
+  const float invC = 1.0f / (float)a.C;
+  act_t* dact = reinterpret_cast<act_t*>(a.dres_act);
+  const float* sdy = reinterpret_cast<const float*>(smem);
+  const float* sx = reinterpret_cast<const float*>(smem + S * blk);
+  const float* sin = reinterpret_cast<const float*>(smem + (S + 1) * blk);
+  for (int k = warp; k < nr; k += kWarps) {
+    const int r = r0 + k;
+    const float mean = a.mean[r], rstd = a.rstd[r];
+    float4 dy[NV], xh[NV];
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int c = 4 * (lane + 32 * i);
+      float4 d = *reinterpret_cast<const float4*>(sdy + (int64_t)k * a.C + c);
+      for (int sp = 1; sp < S; ++sp) {
+        const float4 e = *reinterpret_cast<const float4*>(sdy + (int64_t)sp * (blk / 4) + (int64_t)k * a.C + c);
+        d.x += e.x; d.y += e.y; d.z += e.z; d.w += e.w;
+      }
+      dy[i] = d;
+      const float4 xv = *reinterpret_cast<const float4*>(sx + (int64_t)k * a.C + c);
+      xh[i] = make_float4((xv.x - mean) * rstd, (xv.y - mean) * rstd, (xv.z - mean) * rstd, (xv.w - mean) * rstd);
+      const float a0 = d.x * g[i].x, a1 = d.y * g[i].y, a2 = d.z * g[i].z, a3 = d.w * g[i].w;
+      s1 += (a0 + a1) + (a2 + a3);
+      s2 += (a0 * xh[i].x + a1 * xh[i].y) + (a2 * xh[i].z + a3 * xh[i].w);
+      pg[i].x += d.x * xh[i].x; pg[i].y += d.y * xh[i].y; pg[i].z += d.z * xh[i].z; pg[i].w += d.w * xh[i].w;
+      pb[i].x += d.x; pb[i].y += d.y; pb[i].z += d.z; pb[i].w += d.w;
+    }
+    s1 = warp_sum(s1) * invC;
+    s2 = warp_sum(s2) * invC;
+    float* out = a.dres_out + (int64_t)r * a.C;
+    act_t* oa = dact + (int64_t)r * a.C;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int c = 4 * (lane + 32 * i);
+      float4 din = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (a.dres_in) din = *reinterpret_cast<const float4*>(sin + (int64_t)k * a.C + c);
+      const float4 o = make_float4(rstd * (dy[i].x * g[i].x - s1 - xh[i].x * s2) + din.x,
+                                   rstd * (dy[i].y * g[i].y - s1 - xh[i].y * s2) + din.y,
+                                   rstd * (dy[i].z * g[i].z - s1 - xh[i].z * s2) + din.z,
+                                   rstd * (dy[i].w * g[i].w - s1 - xh[i].w * s2) + din.w);
+      *reinterpret_cast<float4*>(out + c) = o;
+      store4<act_t>(oa + c, o.x, o.y, o.z, o.w);
+    }
+  }
+  __syncthreads();  // every read of the staged rows is done: the area holds the warps' partials now
+  float* wg = reinterpret_cast<float*>(smem);            // [kWarps][C]
+  float* wb = wg + kWarps * a.C;                         // [kWarps][C]
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int c = 4 * (lane + 32 * i);
+    *reinterpret_cast<float4*>(wg + warp * a.C + c) = pg[i];
+    *reinterpret_cast<float4*>(wb + warp * a.C + c) = pb[i];
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < a.C; c += kThreads) {
+    float sg = 0.f, sb = 0.f;
+    for (int w = 0; w < kWarps; ++w) { sg += wg[w * a.C + c]; sb += wb[w * a.C + c]; }
+    a.dg_part[(int64_t)idx * a.C + c] = sg;
+    if (a.db_part) a.db_part[(int64_t)idx * a.C + c] = sb;
+  }
+}
+
+template <typename act_t>
+__device__ inline void task_ln_bwd_staged_any(const KParams& kp, const LnBwdArgs& a, int idx, uint8_t* smem,
+                                              uint64_t* bars, uint32_t* iter) {
+  switch (a.C >> 7) {  // the host stages only C = 128 NV, NV <= 8
+    case 2: task_ln_bwd_staged<act_t, 2>(kp, a, idx, smem, bars, iter); break;
+    case 4: task_ln_bwd_staged<act_t, 4>(kp, a, idx, smem, bars, iter); break;
+    case 6: task_ln_bwd_staged<act_t, 6>(kp, a, idx, smem, bars, iter); break;
+    case 8: task_ln_bwd_staged<act_t, 8>(kp, a, idx, smem, bars, iter); break;
+    default: break;
+  }
+}
+
 // Softmax cross-entropy of a block of rows, one warp per row:
 // lse = log sum_j exp z_j (max subtracted), loss_n = lse - z[t_n],
 // dz_j = (exp(z_j - lse) - [j = t_n]) / N written over the logits.

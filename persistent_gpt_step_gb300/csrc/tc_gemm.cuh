@@ -375,10 +375,20 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
     float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
     if (EPI != EPI_F32 && EPI != EPI_GELU_BWD && EPI != EPI_GEGLU_BWD && bias)
       b = *reinterpret_cast<const float4*>(bias + col);
+    // the thread's 8 rows are read from the staging tile before any of them is
+    // processed: the global stores below may alias the staging pointer as far as
+    // the compiler knows, so reads interleaved with them would run one row at a
+    // time; read first, the 32 values' arithmetic chains are independent
+    float4 vr[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int rl = rq + 4 * i;
+      vr[i] = *reinterpret_cast<const float4*>(stage + rl * 128 + (((lane & 7) ^ (rl & 7)) << 4));
+    }
     auto row = [&](const int i) {
       const int rl = rq + 4 * i;
       const int m = row0 + rl;
-      float4 v = *reinterpret_cast<const float4*>(stage + rl * 128 + (((lane & 7) ^ (rl & 7)) << 4));
+      float4 v = vr[i];
       v.x += b.x; v.y += b.y; v.z += b.z; v.w += b.w;
       if constexpr (EPI == EPI_STORE || EPI == EPI_STORE_ROPE) {
         if constexpr (EPI == EPI_STORE_ROPE) {

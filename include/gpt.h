@@ -183,18 +183,22 @@ typedef struct {
 float gpt_lr_at(const gpt_lr_schedule* sched, float base_lr, int64_t step);
 
 /*
- * k training steps in one call ("K steps per launch"): step j reads DEVICE
- * tokens + j*batch*seq_len and targets + j*batch*seq_len (int32 [k, batch,
- * seq_len], row-major, caller-owned, valid until the call returns) and updates
- * with the rate sched gives its update number (NULL: cfg.lr).  The k launches
- * of the persistent kernel are queued back to back on the handle's stream with
- * no host synchronisation between them: each writes its loss and status into a
- * device ring, and the host reads the ring once at the end (once every 256
- * steps for longer calls).  losses: HOST float[k] (may be NULL) receives every
- * step's pre-update loss.  Errors as gpt_train_step; on BAD_TOKEN or NONFINITE
- * at step j the steps before j are applied, step j and every later step of the
- * call leave parameters, moments and the step count unchanged (their losses are
- * still computed and returned), and gpt_last_error names j.
+ * k training steps in one call ("K steps per launch": the "Open Flapping
+ * Airplanes" record times its whole run inside one kernel interval, section
+ * "Measured results"): step j reads DEVICE tokens + j*batch*seq_len and targets
+ * + j*batch*seq_len (int32 [k, batch, seq_len], row-major, caller-owned, valid
+ * until the call returns) and updates with the rate sched gives its update
+ * number (NULL: cfg.lr).  Up to 256 steps run inside ONE launch of the
+ * persistent kernel: after each step every block passes a grid barrier (a
+ * device counter, bounded wait) and starts the next step with the next epoch,
+ * its rate and bias corrections taken from a device table the call uploads
+ * first; each step writes its loss and status into a device ring that the host
+ * reads once per launch.  Longer calls use one launch per 256 steps.
+ * losses: HOST float[k] (may be NULL) receives every step's pre-update loss.
+ * Errors as gpt_train_step; on BAD_TOKEN or NONFINITE at step j the steps
+ * before j are applied, step j and every later step of the call leave
+ * parameters, moments and the step count unchanged (their losses are still
+ * computed and returned), and gpt_last_error names j.
  */
 int gpt_train_steps(gpt* h, const int32_t* tokens, const int32_t* targets, int32_t k,
                     const gpt_lr_schedule* sched, float* losses);
@@ -310,7 +314,7 @@ int gpt_get_trace(gpt* h, uint64_t* dst, size_t n);
 
 /* Device time of the last step's kernel launch in milliseconds, from CUDA
  * events the library records on the handle's stream around the launch (after
- * gpt_train_steps: around the last chunk of its launches, up to 256 steps). */
+ * gpt_train_steps: around its last launch, which ran up to 256 steps). */
 int gpt_last_kernel_ms(const gpt* h, float* ms);
 
 /* Text of the handle's last error ("" if none): the error notifier of

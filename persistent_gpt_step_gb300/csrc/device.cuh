@@ -43,6 +43,29 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 // the aligned __syncthreads() is used (it keeps more registers free).
 __device__ __forceinline__ void cta_sync() { asm volatile("barrier.sync 0;" ::: "memory"); }
 
+// Step of a multi-step launch that this block is running (0 for a one-step
+// launch).  Thread 0 writes it at the start of each step, before a block
+// barrier; every task body reads the step's epoch, inputs, rates and ring
+// slots through the helpers below.
+static __shared__ int32_t g_step;
+
+__device__ __forceinline__ unsigned long long step_epoch(const KParams& kp) {
+  return kp.epoch + (unsigned long long)g_step;
+}
+__device__ __forceinline__ const int32_t* step_tokens(const KParams& kp) {
+  return kp.tokens + (int64_t)g_step * kp.tok_stride;
+}
+__device__ __forceinline__ const int32_t* step_targets(const KParams& kp) {
+  return kp.targets + (int64_t)g_step * kp.tok_stride;
+}
+__device__ __forceinline__ float step_lr(const KParams& kp) { return kp.step_hyper ? kp.step_hyper[3 * g_step] : kp.lr; }
+__device__ __forceinline__ float step_bc1(const KParams& kp) {
+  return kp.step_hyper ? kp.step_hyper[3 * g_step + 1] : kp.bc1;
+}
+__device__ __forceinline__ float step_bc2(const KParams& kp) {
+  return kp.step_hyper ? kp.step_hyper[3 * g_step + 2] : kp.bc2;
+}
+
 __device__ __forceinline__ void set_fatal(const KParams& kp, uint32_t code, uint32_t task,
                                           uint32_t ctr) {
   if (atomicCAS(&kp.err[0], 0u, code) == 0u) {
@@ -84,7 +107,7 @@ __device__ __forceinline__ bool task_ready(const KParams& kp, int64_t t) {
   const TaskDesc& d = kp.tasks[t];
   for (int w = 0; w < d.nwait; ++w) {
     const WaitSpec ws = d.wait[w];
-    const unsigned long long target = kp.epoch * (unsigned long long)ws.need;
+    const unsigned long long target = step_epoch(kp) * (unsigned long long)ws.need;
     for (int c = 0; c < ws.count; ++c)
       if (!wait_counter(kp, ws.first + c, target, (uint32_t)t)) return false;
   }
@@ -96,7 +119,7 @@ __device__ __forceinline__ bool task_ready(const KParams& kp, int64_t t) {
 // are a 64-bit counter per launch parity; the previous launch zeroed this one.
 __device__ __forceinline__ int64_t claim_task(const KParams& kp) {
   if (ld_volatile_u32(&kp.err[0]) != 0u) return kp.ntasks;
-  const int64_t t = (int64_t)atomicAdd(kp.tickets + (kp.epoch & 1ull), 1ull);
+  const int64_t t = (int64_t)atomicAdd(kp.tickets + (step_epoch(kp) & 1ull), 1ull);
   return t < kp.ntasks ? t : kp.ntasks;
 }
 
@@ -131,8 +154,8 @@ struct AdamHyper {
   float lr, b1, b2, ib1, ib2, rbc1, rbc2, eps;
 };
 __device__ __forceinline__ AdamHyper adam_hyper(const KParams& kp) {
-  return AdamHyper{kp.lr, kp.beta1, kp.beta2, 1.0f - kp.beta1, 1.0f - kp.beta2, 1.0f / kp.bc1, 1.0f / kp.bc2,
-                   kp.eps};
+  return AdamHyper{step_lr(kp), kp.beta1, kp.beta2, 1.0f - kp.beta1, 1.0f - kp.beta2, 1.0f / step_bc1(kp),
+                   1.0f / step_bc2(kp), kp.eps};
 }
 __device__ __forceinline__ void adamw_elem(const AdamHyper& hp, float decay, float g, float& p, float& m,
                                            float& v) {

@@ -151,9 +151,12 @@ struct gpt {
     uint32_t pad[3];
     float ring_loss[kStepRing];        // multi-step calls: per-step losses ...
     uint32_t ring_status[kStepRing];   // ... and soft error bits, read back once per chunk
+    float ring_hyper[3 * kStepRing];   // ... and the (lr, bc1, bc2) table uploaded before the launch
   };
   float* d_loss_ring = nullptr;        // device rings of kStepRing slots (in the metadata allocation)
   uint32_t* d_status_ring = nullptr;
+  float* d_step_hyper = nullptr;       // multi-step launch: (lr, bc1, bc2) of each step, kStepRing x 3
+  unsigned long long* d_grid_bar = nullptr;  // grid barrier between the steps of a launch
   Status* h_status = nullptr;
   std::string err;
 };
@@ -1079,6 +1082,7 @@ int reset_counters(gpt* h) {
   CUDA_TRY(h, cudaMemsetAsync(h->d_counters, 0, nctr * sizeof(unsigned long long), h->stream));
   CUDA_TRY(h, cudaMemsetAsync(h->d_ticket, 0, 2 * sizeof(unsigned long long), h->stream));
   CUDA_TRY(h, cudaMemsetAsync(h->d_err, 0, 4 * sizeof(uint32_t), h->stream));
+  if (h->d_grid_bar) CUDA_TRY(h, cudaMemsetAsync(h->d_grid_bar, 0, sizeof(unsigned long long), h->stream));
   CUDA_TRY(h, cudaStreamSynchronize(h->stream));
   h->launches = 0;
   h->poisoned = false;
@@ -1104,6 +1108,9 @@ KParams step_params(gpt* h, const int32_t* tokens, const int32_t* targets, unsig
   kp.tmaps = h->d_tmaps;
   kp.tokens = tokens;
   kp.targets = targets;
+  kp.nsteps = 1;
+  kp.tok_stride = (int64_t)h->D.N;
+  kp.grid_bar = h->d_grid_bar;
   kp.trace = h->d_trace;
   kp.lr = lr; kp.beta1 = h->cfg.beta1; kp.beta2 = h->cfg.beta2; kp.eps = h->cfg.eps;
   kp.wd = h->cfg.weight_decay;
@@ -1182,13 +1189,26 @@ int train_steps(gpt* h, const int32_t* tokens, const int32_t* targets, int32_t k
   const int64_t n = (int64_t)h->D.N;
   for (int32_t j0 = 0; j0 < k; j0 += kStepRing) {
     const int32_t kc = std::min<int32_t>(kStepRing, k - j0);
-    if (h->ev0) CUDA_TRY(h, cudaEventRecord(h->ev0, h->stream));
+    // the chunk's kc steps run inside ONE launch of the persistent kernel: step j has
+    // epoch launches + 1 + j, its rate and bias corrections come from this table
     for (int32_t j = 0; j < kc; ++j) {
       const int64_t t = h->opt_step + 1 + j;
-      const int rc = enqueue_step(h, tokens + (j0 + j) * n, targets + (j0 + j) * n, h->launches + 1 + j,
-                                  (float)schedule_lr(sched, h->cfg.lr, t), t, h->d_loss_ring + j,
-                                  h->d_status_ring + j);
-      if (rc != GPT_OK) {  // launches already queued still run: wait for them, then report
+      h->h_status->ring_hyper[3 * j] = (float)schedule_lr(sched, h->cfg.lr, t);
+      h->h_status->ring_hyper[3 * j + 1] = (float)(1.0 - std::pow((double)h->cfg.beta1, (double)t));
+      h->h_status->ring_hyper[3 * j + 2] = (float)(1.0 - std::pow((double)h->cfg.beta2, (double)t));
+    }
+    CUDA_TRY(h, cudaMemcpyAsync(h->d_step_hyper, h->h_status->ring_hyper, 3 * kc * sizeof(float),
+                                cudaMemcpyHostToDevice, h->stream));
+    if (h->ev0) CUDA_TRY(h, cudaEventRecord(h->ev0, h->stream));
+    {
+      KParams kp = step_params(h, tokens + j0 * n, targets + j0 * n, h->launches + 1, h->cfg.lr, h->opt_step + 1);
+      kp.nsteps = kc;
+      kp.step_hyper = h->d_step_hyper;
+      kp.loss_out = h->d_loss_ring;
+      kp.status_out = h->d_status_ring;
+      h->skip_release = -1;
+      const int rc = launch_kernel(h, kp);
+      if (rc != GPT_OK) {
         cudaStreamSynchronize(h->stream);
         h->poisoned = true;
         return rc;
@@ -1352,6 +1372,8 @@ int gpt_create(const gpt_config* cfg, uint64_t seed, void* cuda_stream, void* ar
   const size_t o_err = mb.take(4 * sizeof(uint32_t));
   const size_t o_tok = mb.take(2 * (size_t)h->D.N * sizeof(int32_t));
   const size_t o_ring = mb.take((size_t)kStepRing * (sizeof(float) + sizeof(uint32_t)));
+  const size_t o_hyper = mb.take((size_t)kStepRing * 3 * sizeof(float));
+  const size_t o_bar = mb.take(sizeof(unsigned long long));
   h->meta_bytes = mb.off;
   if (cudaMalloc(&h->meta, h->meta_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -1367,6 +1389,8 @@ int gpt_create(const gpt_config* cfg, uint64_t seed, void* cuda_stream, void* ar
   h->d_tok_stage = reinterpret_cast<int32_t*>(h->meta + o_tok);
   h->d_loss_ring = reinterpret_cast<float*>(h->meta + o_ring);
   h->d_status_ring = reinterpret_cast<uint32_t*>(h->meta + o_ring + (size_t)kStepRing * sizeof(float));
+  h->d_step_hyper = reinterpret_cast<float*>(h->meta + o_hyper);
+  h->d_grid_bar = reinterpret_cast<unsigned long long*>(h->meta + o_bar);
   if (cudaMallocHost(&h->h_status, sizeof(gpt::Status)) != cudaSuccess) {
     cudaGetLastError();
     fail(h, GPT_ERR_OOM, "pinned host allocation failed");
@@ -1565,6 +1589,7 @@ int gpt_run_ops(gpt* h, int32_t op_first, int32_t op_count, const int32_t* token
       kp.err = reinterpret_cast<uint32_t*>(d + o_err);
       kp.skip_release = -1;
       kp.trace = nullptr;
+      kp.grid_bar = nullptr;  // the handle's step barrier counts the handle's own steps only
       cudaEventRecord(ev[2 * r], h->stream);
       rc = launch_kernel(h, kp);
       cudaEventRecord(ev[2 * r + 1], h->stream);

@@ -220,8 +220,17 @@ struct KParams {
   const int32_t* tokens; const int32_t* targets;
   float lr, beta1, beta2, eps, wd, bc1, bc2;
   unsigned long long* trace;       // optional [ntasks][4]: claim, start, end (globaltimer ns), SM id
-  float* loss_out;                 // multi-step calls: this launch's slot of the loss ring (else null)
-  uint32_t* status_out;            // ... and of the status ring (the soft error bits after the loss)
+  float* loss_out;                 // multi-step launches: the loss ring, one slot per step (else null)
+  uint32_t* status_out;            // ... and the status ring (the soft error bits after the loss)
+  // K steps in one launch: step s (0-based) has epoch epoch + s, reads tokens and
+  // targets + s * tok_stride, updates with step_hyper[3 s .. 3 s + 2] = (lr, bc1, bc2)
+  // (null: the fields above), and writes loss_out[s], status_out[s].  Between two
+  // steps every block passes a grid barrier on grid_bar, which every block adds 1
+  // to after each step (after the step of epoch e it holds e * gridDim.x).
+  int32_t nsteps;                  // <= 1: one step
+  int64_t tok_stride;
+  const float* step_hyper;
+  unsigned long long* grid_bar;    // null: no step barrier (one-step launches of test graphs)
 };
 
 }  // namespace pgs

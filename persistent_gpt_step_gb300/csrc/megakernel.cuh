@@ -24,6 +24,7 @@ struct KernelShared {
   uint32_t adam_iter;
   uint32_t tmem_base;
   int32_t ok;
+  int32_t step_ok;   // the grid barrier after a step of a multi-step launch passed
   int64_t task;
 };
 
@@ -38,7 +39,6 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
                                              ~(uintptr_t)1023);
   const int warp = threadIdx.x >> 5;
   TcState st = {0u, 0u, 0u, 0u, 0u, 0u};
-  if (blockIdx.x == 0 && threadIdx.x == 0) kp.tickets[(kp.epoch + 1ull) & 1ull] = 0ull;  // next launch's
   if (threadIdx.x == 0) {
     for (int i = 0; i < kAdamStages; ++i) mbar_init(smem_u32(&sh.adam_bars[i]), 1);
     sh.adam_iter = 0;
@@ -75,6 +75,15 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
     tc_fence_after();
   }
 
+  const int nsteps = kp.nsteps > 1 ? kp.nsteps : 1;
+  for (int step = 0; step < nsteps; ++step) {
+  if (threadIdx.x == 0) {
+    g_step = step;
+    // the ticket of the next step (or launch): its last user, the previous step, has
+    // ended on every block (grid barrier below, or the end of the previous launch)
+    if (blockIdx.x == 0) kp.tickets[(kp.epoch + (unsigned long long)step + 1ull) & 1ull] = 0ull;
+  }
+  __syncthreads();
   int64_t pending = -1;  // ticket claimed by a GEMM run, dependencies not yet waited
   for (;;) {
     if (threadIdx.x == 0) {
@@ -86,6 +95,9 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
           ok = 1;
           const uint64_t t_claim = kp.trace ? globaltimer_ns() : 0;
           ok = task_ready(kp, t);
+          // this thread issues the bulk / tensor copies of row and attention tasks:
+          // order the producers' writes it has acquired before those async-proxy reads
+          fence_proxy_async_global();
           if (kp.trace) {
             uint32_t smid;
             asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
@@ -174,6 +186,42 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
     }
     if (threadIdx.x == 0 && kp.trace) kp.trace[4 * t + 2] = globaltimer_ns();
   }
+  // End of this block's share of the step: its AdamW bulk stores complete and are
+  // published, and the block arrives at the grid barrier (after the step of
+  // epoch e the barrier holds e * gridDim.x).  Between two steps of the launch
+  // every block waits there, so the next step reads the updated weights.
+  if (threadIdx.x == 0) {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    if (kp.grid_bar) {
+      fence_proxy_async_global();
+      __threadfence();
+      red_release_add_u64(kp.grid_bar, 1ull);
+    }
+  }
+  if (step + 1 < nsteps) {
+    if (threadIdx.x == 0) {
+      const unsigned long long target = (kp.epoch + (unsigned long long)step) * (unsigned long long)gridDim.x;
+      int ok = 1;
+      if (ld_volatile_u32(&kp.err[0]) == 0u) {
+        const uint64_t t0 = globaltimer_ns();
+        const uint64_t max_iters = kp.timeout_ns / 30 + 1024;
+        ok = 0;
+        for (uint64_t it = 0; it < max_iters; ++it) {
+          if (ld_acquire_u64(kp.grid_bar) >= target) { ok = 1; break; }
+          __nanosleep(128);
+          if ((it & 15) == 15) {
+            if (ld_volatile_u32(&kp.err[0]) != 0u) break;
+            if (globaltimer_ns() - t0 > kp.timeout_ns) { set_fatal(kp, kFatalTimeout, 0xFFFFFFFFu, 0xFFFFFFFFu); break; }
+          }
+        }
+        fence_proxy_async_global();  // later tensor copies read the other blocks' updates
+      }
+      sh.step_ok = ok && ld_volatile_u32(&kp.err[0]) == 0u;
+    }
+    __syncthreads();
+    if (!*reinterpret_cast<volatile int32_t*>(&sh.step_ok)) break;  // every thread reads the same word
+  }
+  }  // steps
 
   if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   if constexpr (kTC) {

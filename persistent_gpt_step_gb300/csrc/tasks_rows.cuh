@@ -32,7 +32,7 @@ __device__ inline void task_embed(const KParams& kp, const EmbedArgs& a, int idx
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r0 = idx * a.rows_per_task, r1 = min(r0 + a.rows_per_task, a.N);
   for (int r = r0 + warp; r < r1; r += kWarps) {
-    int tok = kp.tokens[r];
+    int tok = step_tokens(kp)[r];
     if (tok < 0 || tok >= a.V) {
       if (lane == 0) set_soft(kp, kSoftBadToken);
       tok = tok < 0 ? 0 : a.V - 1;
@@ -424,7 +424,7 @@ __device__ inline void task_ce(const KParams& kp, const CeArgs& a, int idx) {
   const float invN = 1.0f / (float)a.N;
   for (int r = r0 + warp; r < r1; r += kWarps) {
     act_t* z = L + (int64_t)r * a.V;
-    int t = kp.targets[r];
+    int t = step_targets(kp)[r];
     if (t < 0 || t >= a.V) {
       if (lane == 0) set_soft(kp, kSoftBadToken);
       t = t < 0 ? 0 : a.V - 1;
@@ -486,7 +486,7 @@ __device__ inline void task_ce_bf16_vec(const KParams& kp, const CeArgs& a, int 
   for (int r = r0 + warp; r < r1; r += kWarps) {
     __nv_bfloat16* zr = reinterpret_cast<__nv_bfloat16*>(a.logits) + (int64_t)r * a.V;
     uint4* z = reinterpret_cast<uint4*>(zr);
-    int t = kp.targets[r];
+    int t = step_targets(kp)[r];
     if (t < 0 || t >= a.V) {
       if (lane == 0) set_soft(kp, kSoftBadToken);
       t = t < 0 ? 0 : a.V - 1;
@@ -580,7 +580,7 @@ __device__ inline void task_ce_bf16_staged(const KParams& kp, const CeArgs& a, i
     // behind at a later barrier of this task)
     if (!__syncthreads_and(mbar_wait(kp, bar0 + 8 * st, phase))) return;
     const uint4* z = reinterpret_cast<const uint4*>(smem + (k & 1) * buf_stride);
-    int t = kp.targets[r];
+    int t = step_targets(kp)[r];
     if (t < 0 || t >= a.V) {
       if (threadIdx.x == 0) set_soft(kp, kSoftBadToken);
       t = t < 0 ? 0 : a.V - 1;
@@ -655,8 +655,8 @@ __device__ inline void task_loss(const KParams& kp, const LossArgs& a, float* sm
     if (!isfinite(loss)) set_soft(kp, kSoftNonFinite);
     // multi-step calls: the loss and the soft error bits of this step (every
     // cross-entropy row, which raises them, precedes this task) into the rings
-    if (kp.loss_out) *kp.loss_out = loss;
-    if (kp.status_out) *kp.status_out = ld_volatile_u32(&kp.err[1]);
+    if (kp.loss_out) kp.loss_out[g_step] = loss;
+    if (kp.status_out) kp.status_out[g_step] = ld_volatile_u32(&kp.err[1]);
   }
 }
 
@@ -732,7 +732,7 @@ __device__ inline void task_token_sort(const KParams& kp, const EmbedArgs& a, in
   int* vb = kb + N;
   int* hist = vb + N;  // [256]
   for (int n = threadIdx.x; n < N; n += kThreads) {
-    int t = kp.tokens[n];
+    int t = step_tokens(kp)[n];
     ka[n] = t < 0 ? 0 : (t >= a.V ? a.V - 1 : t);
     va[n] = n;
   }
@@ -970,7 +970,7 @@ __device__ inline void task_adamw(const KParams& kp, const AdamArgs& a, int idx,
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     for (int s = 0; s < min(nsub, kAhead); ++s) issue(s);
   }
-  const float decay = 1.0f - kp.lr * kp.wd * a.decay;
+  const float decay = 1.0f - step_lr(kp) * kp.wd * a.decay;
   const AdamHyper hp = adam_hyper(kp);
   for (int s = 0; s < nsub; ++s) {
     const uint32_t st = stage_of(s);

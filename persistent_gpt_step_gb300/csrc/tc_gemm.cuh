@@ -186,12 +186,13 @@ __device__ __forceinline__ void gelu_pair_bf(float x, bool tanh_form, float& g, 
     dg = gelu_grad_f(x, false);
     return;
   }
-  const float k0 = 0.7978845608028654f;
+  // k0 (x + c x^3) = x (k0 + c k0 x^2); k0 (1 + 3 c x^2) = k0 + 3 c k0 x^2 (constants folded)
+  const float k0 = 0.7978845608028654f, ck0 = 0.044715f * 0.7978845608028654f;
   const float x2 = x * x;
-  const float t = tanh_sfu(k0 * (x + 0.044715f * x2 * x));
+  const float t = tanh_sfu(x * fmaf(ck0, x2, k0));
   const float h = 0.5f * x;
-  g = h + h * t;
-  dg = 0.5f + 0.5f * t + h * (1.0f - t * t) * k0 * (1.0f + 3.0f * 0.044715f * x2);
+  g = fmaf(h, t, h);
+  dg = fmaf(h * fmaf(-t, t, 1.0f), fmaf(3.0f * ck0, x2, k0), fmaf(0.5f, t, 0.5f));
 }
 
 __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float* v) {

@@ -59,7 +59,7 @@ import numpy as np
 __all__ = [
     "param_table", "num_params", "param_views", "decay_mask", "forward", "backward",
     "adamw", "train_step", "OracleState", "layernorm", "gelu", "gelu_grad",
-    "causal_attention", "softmax_rows", "cross_entropy",
+    "causal_attention", "softmax_rows", "cross_entropy", "next_token_logits", "greedy_decode",
 ]
 
 
@@ -454,6 +454,33 @@ def lr_at(step, lr_max, lr_min, warmup, total):
         return lr_min
     frac = (step - warmup) / (total - warmup)
     return lr_min + 0.5 * (lr_max - lr_min) * (1.0 + math.cos(math.pi * frac))
+
+
+def next_token_logits(cfg, params, seq, dtype=np.float64) -> np.ndarray:
+    """Logits [V] of the token that follows the 1-D id sequence ``seq`` (its last
+    position's row of the LM head output), from a full forward pass over ``seq``."""
+    tok = np.asarray(seq, dtype=np.int64)[None, :]
+    _, cache = forward(cfg, params, tok, np.zeros_like(tok), dtype=dtype)
+    return cache["z"][-1]
+
+
+def greedy_decode(cfg, params, prompt, n_new, dtype=np.float64):
+    """Autoregressive greedy generation (serving: "autoregressive text generation
+    from the changing model", "Open Flapping Airplanes" record, section "What
+    ran", table of SM roles; one generated token releases the next, "How one
+    persistent kernel runs three jobs").  Each new token is the argmax of the next
+    token's logits (the smallest id among equal maxima) given everything so far,
+    recomputed by a full forward pass over the sequence (no cache).  Returns the
+    n_new generated ids and the logits each was chosen from ([n_new, V])."""
+    seq = [int(t) for t in prompt]
+    out, zs = [], []
+    for _ in range(n_new):
+        z = next_token_logits(cfg, params, seq, dtype=dtype)
+        t = int(np.argmax(z))
+        out.append(t)
+        zs.append(z)
+        seq.append(t)
+    return np.array(out, dtype=np.int64), np.array(zs)
 
 
 def train_step(state: OracleState, tokens, targets, lr=None) -> float:

@@ -247,6 +247,17 @@ def _torch_loss(cfg, params, tok, tgt):
     import torch
     import torch.nn.functional as F
     t = torch.tensor(params, dtype=torch.float64, requires_grad=True)
+    B, T = tok.shape
+    z = _torch_logits(cfg, t, tok)
+    loss = F.cross_entropy(z.view(B * T, -1), torch.tensor(tgt, dtype=torch.long).view(-1))
+    loss.backward()
+    return float(loss), t.grad.numpy()
+
+
+def _torch_logits(cfg, t, tok):
+    """Logits [B, T, V] of the same re-statement; t: the float64 parameter tensor."""
+    import torch
+    import torch.nn.functional as F
     views, off = {}, 0
     for name, shape, _ in O.param_table(cfg):
         n = int(np.prod(shape))
@@ -287,10 +298,30 @@ def _torch_loss(cfg, params, tok, tgt):
             h = F.gelu(F.linear(a, views[p + "w_1"], views.get(p + "b_1")), approximate=approx)
         x = x + F.linear(h, views[p + "w_2"], views.get(p + "b_2"))
     x = F.layer_norm(x, (C,), views["lnf_g"], views.get("lnf_b"), cfg.ln_eps)
-    z = F.linear(x, views["wte" if cfg.tie_embeddings else "w_lm"])
-    loss = F.cross_entropy(z.view(B * T, -1), torch.tensor(tgt, dtype=torch.long).view(-1))
-    loss.backward()
-    return float(loss), t.grad.numpy()
+    return F.linear(x, views["wte" if cfg.tie_embeddings else "w_lm"])
+
+
+@pytest.mark.parametrize("variant", ["tiny", "gated_rope_tied"])
+def test_greedy_decode_against_torch_restatement(variant):
+    """Every token of the oracle's greedy generation is the argmax of the PyTorch
+    re-statement's next-token logits over the same prefix, and the logits it was
+    chosen from match that re-statement; generation stops at no fixed point (the
+    oracle recomputes the whole prefix for every token)."""
+    torch = pytest.importorskip("torch")
+    cfg = TINY if variant == "tiny" else GATED.replace(linear_bias=False)
+    params, tok, _ = _tiny_inputs(cfg, seed=12)
+    rng = np.random.default_rng(13)
+    params = params + rng.normal(0, 0.3, params.shape)   # a model with strong preferences: no near-ties
+    prompt = tok[0, :5]
+    gen, zs = O.greedy_decode(cfg, params, prompt, 12)
+    seq = list(prompt)
+    t = torch.tensor(params, dtype=torch.float64)
+    for i, g in enumerate(gen):
+        z = _torch_logits(cfg, t, np.array([seq]))[0, -1].numpy()
+        assert int(np.argmax(z)) == int(g), i
+        assert np.allclose(zs[i], z, rtol=1e-10, atol=1e-10)
+        seq.append(int(g))
+    assert len(gen) == 12 and len(set(gen.tolist())) > 1
 
 
 @pytest.mark.parametrize("variant", ["tiny", "nobias_erf", "gated_rope_tied", "gated_rope_tied_erf_bias"])

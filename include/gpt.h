@@ -266,6 +266,44 @@ int gpt_debug_skip_release(gpt* h, int64_t task_index);
 int gpt_reset(gpt* h);
 
 /*
+ * Serving partition: greedy generation (batch 1) from the live weights on a
+ * reserved set of blocks of the persistent kernel, next to the training step
+ * ("Open Flapping Airplanes" record, section "What ran": 17 of the A100's SMs
+ * serve "autoregressive text generation from the changing model"; "How one
+ * persistent kernel runs three jobs": static block roles, serving claims tasks
+ * through its own ticket counter, one token releases the next).  A decode step
+ * takes the token at position s (the prompt, then the generated ones) through
+ * the model with the keys and values of positions < s kept in an fp32 cache,
+ * and the next token is the argmax of its logits (the smallest id among equal
+ * logits); activations are fp32, weights the bf16 copy that training updates.
+ * bf16 model with learned positions, a GELU MLP and an untied LM head only
+ * (UNSUPPORTED otherwise).  The step's ticket and every counter are 64-bit ("A
+ * longer run exposed a scheduler overflow": a task budget of 4,194,304 x 2,225
+ * wrapped at 32 bits); first_step starts the session's counters as if that many
+ * steps had run before (a boundary test of the budget), 0 normally.
+ *
+ * gpt_serve_begin: HOST prompt[n_prompt] (ids in [0, vocab)), max_new >= 1 new
+ *   tokens, n_prompt + max_new <= seq_len; `blocks` (1 .. grid-1) blocks serve
+ *   during every later training launch, each of which runs up to
+ *   tokens_per_step decode steps per training step (0: serve only in
+ *   gpt_serve_run).  Allocates the session's device state (about 2 x layers x
+ *   seq_len x d_model fp32 of cache); an earlier session is ended first.
+ *   Errors: INVALID_ARG, BAD_TOKEN, UNSUPPORTED, OOM, CUDA.
+ * gpt_serve_run: a launch in which only the serving blocks work (no training
+ *   step, no epoch consumed) for up to max_steps decode steps; kernel_ms (HOST,
+ *   may be NULL) receives its device time.  Errors: INVALID_ARG, POISONED,
+ *   TIMEOUT, CUDA.
+ * gpt_serve_tokens: the tokens generated so far (*n of them; the first
+ *   min(*n, cap) are copied to HOST dst, which may be NULL).
+ * gpt_serve_end: frees the session (no-op without one).
+ */
+int gpt_serve_begin(gpt* h, const int32_t* prompt, int32_t n_prompt, int32_t max_new, int32_t blocks,
+                    int32_t tokens_per_step, int64_t first_step);
+int gpt_serve_run(gpt* h, int32_t max_steps, float* kernel_ms);
+int gpt_serve_tokens(gpt* h, int32_t* dst, int32_t cap, int32_t* n);
+int gpt_serve_end(gpt* h);
+
+/*
  * Measurement hook (per-phase timing, after the per-family table of
  * "Coppelius training on the RTX 3090", section "Where a step's time goes"):
  * runs the operations op_first .. op_first + op_count - 1 of the handle's step

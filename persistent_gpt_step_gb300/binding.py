@@ -88,6 +88,10 @@ SIGNATURES = [
     ("gpt_debug_skip_release", c_int, [c_void_p, c_int64]),
     ("gpt_reset", c_int, [c_void_p]),
     ("gpt_run_ops", c_int, [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_int32, POINTER(c_float)]),
+    ("gpt_serve_begin", c_int, [c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int64]),
+    ("gpt_serve_run", c_int, [c_void_p, c_int32, POINTER(c_float)]),
+    ("gpt_serve_tokens", c_int, [c_void_p, c_void_p, c_int32, POINTER(c_int32)]),
+    ("gpt_serve_end", c_int, [c_void_p]),
     ("gpt_graph_info", c_int, [c_void_p, POINTER(c_int64), POINTER(c_int32), POINTER(c_int32)]),
     ("gpt_trace_enable", c_int, [c_void_p, c_int32]),
     ("gpt_get_trace", c_int, [c_void_p, c_void_p, c_size_t]),
@@ -339,6 +343,33 @@ class GPT:
 
     def reset(self):
         self._check(self._lib.gpt_reset(self._h))
+
+    # -- serving partition ----------------------------------------------------
+    def serve_begin(self, prompt, max_new: int, blocks: int = 16, tokens_per_step: int = 0,
+                    first_step: int = 0):
+        """gpt_serve_begin: greedy generation from the live weights on `blocks`
+        reserved blocks (prompt: host int ids)."""
+        p = np.ascontiguousarray(prompt, dtype=np.int32)
+        self._check(self._lib.gpt_serve_begin(self._h, c_void_p(p.ctypes.data), int(p.size), int(max_new),
+                                              int(blocks), int(tokens_per_step), c_int64(first_step)))
+
+    def serve_run(self, max_steps: int) -> float:
+        """gpt_serve_run: a serving-only launch of up to max_steps decode steps;
+        returns its device milliseconds."""
+        ms = c_float()
+        self._check(self._lib.gpt_serve_run(self._h, int(max_steps), byref(ms)))
+        return float(ms.value)
+
+    def serve_tokens(self) -> np.ndarray:
+        """The tokens generated so far."""
+        n = c_int32()
+        self._check(self._lib.gpt_serve_tokens(self._h, None, 0, byref(n)))
+        out = np.zeros(max(int(n.value), 1), np.int32)
+        self._check(self._lib.gpt_serve_tokens(self._h, c_void_p(out.ctypes.data), out.size, byref(n)))
+        return out[:int(n.value)]
+
+    def serve_end(self):
+        self._check(self._lib.gpt_serve_end(self._h))
 
     def run_ops(self, op_first: int, op_count: int, tokens, targets, reps: int = 1) -> float:
         """gpt_run_ops: operations [op_first, op_first + op_count) of the step graph

@@ -144,6 +144,18 @@ struct gpt {
   cudaEvent_t ev0 = nullptr, ev1 = nullptr;  // bracket the kernel of the last step
   float last_kernel_ms = 0.f;
   unsigned long long* d_trace = nullptr;  // optional per-task timestamps (gpt_trace_enable)
+  unsigned long long bar_count = 0;       // grid-barrier arrivals so far (reset with the counters)
+  // serving session (gpt_serve_begin): device state in serve_mem, ServeParams at d_serve
+  struct Serve {
+    bool active = false;
+    int32_t blocks = 0, n_prompt = 0, n_new = 0, per_step = 0;
+    int64_t steps_total = 0, steps_done = 0;
+    unsigned long long base = 0;
+    int32_t P = 0;
+    uint8_t* mem = nullptr;
+    ServeParams* d_params = nullptr;
+    ServeParams host{};  // the device copy's contents (limit and ticket are refreshed per launch)
+  } serve;
   // host staging (pinned) for the per-step status
   struct Status {
     uint32_t err[4];
@@ -1085,6 +1097,7 @@ int reset_counters(gpt* h) {
   if (h->d_grid_bar) CUDA_TRY(h, cudaMemsetAsync(h->d_grid_bar, 0, sizeof(unsigned long long), h->stream));
   CUDA_TRY(h, cudaStreamSynchronize(h->stream));
   h->launches = 0;
+  h->bar_count = 0;
   h->poisoned = false;
   return GPT_OK;
 }
@@ -1119,12 +1132,33 @@ KParams step_params(gpt* h, const int32_t* tokens, const int32_t* targets, unsig
   return kp;
 }
 
+// Serving blocks of an active session for a launch that trains `steps` steps
+// (0: a serving-only launch): the session's step limit for this launch and its
+// ticket are written to the device, and the training blocks' count is set.
+int serve_prepare(gpt* h, KParams& kp, int64_t steps_budget) {
+  gpt::Serve& sv = h->serve;
+  if (!sv.active || sv.steps_done >= sv.steps_total || steps_budget <= 0) return GPT_OK;
+  const int64_t limit = std::min<int64_t>(sv.steps_total, sv.steps_done + steps_budget);
+  sv.host.limit = limit;
+  const unsigned long long ticket = (sv.base + (unsigned long long)sv.steps_done) * (unsigned long long)sv.P;
+  CUDA_TRY(h, cudaMemcpyAsync(sv.d_params, &sv.host, sizeof(ServeParams), cudaMemcpyHostToDevice, h->stream));
+  CUDA_TRY(h, cudaMemcpyAsync(sv.host.ticket, &ticket, sizeof ticket, cudaMemcpyHostToDevice, h->stream));
+  kp.serve = sv.d_params;
+  kp.train_blocks = h->grid - sv.blocks;
+  return GPT_OK;
+}
+
 int launch_kernel(gpt* h, KParams& kp) {
+  if (kp.grid_bar) kp.bar_base = h->bar_count;
   int32_t gelu_tanh = h->cfg.gelu_tanh;
   void* args[2] = {&kp, &gelu_tanh};
   cudaError_t e = cudaLaunchCooperativeKernel(h->kernel, dim3(h->grid), dim3(kThreads), args, h->smem_bytes,
                                               h->stream);
   if (e != cudaSuccess) return fail(h, GPT_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+  if (kp.grid_bar && kp.ntasks > 0)  // every training block arrives once per step
+    h->bar_count += (unsigned long long)(kp.nsteps > 1 ? kp.nsteps : 1) *
+                    (unsigned long long)(kp.serve ? kp.train_blocks : h->grid);
+  if (kp.serve) h->serve.steps_done = h->serve.host.limit;  // every step below the limit completes in the launch
   return GPT_OK;
 }
 
@@ -1134,6 +1168,8 @@ int enqueue_step(gpt* h, const int32_t* tokens, const int32_t* targets, unsigned
   kp.loss_out = loss_out;
   kp.status_out = status_out;
   h->skip_release = -1;
+  const int rc = serve_prepare(h, kp, h->serve.per_step);
+  if (rc != GPT_OK) return rc;
   return launch_kernel(h, kp);
 }
 
@@ -1207,7 +1243,8 @@ int train_steps(gpt* h, const int32_t* tokens, const int32_t* targets, int32_t k
       kp.loss_out = h->d_loss_ring;
       kp.status_out = h->d_status_ring;
       h->skip_release = -1;
-      const int rc = launch_kernel(h, kp);
+      int rc = serve_prepare(h, kp, (int64_t)h->serve.per_step * kc);
+      if (rc == GPT_OK) rc = launch_kernel(h, kp);
       if (rc != GPT_OK) {
         cudaStreamSynchronize(h->stream);
         h->poisoned = true;
@@ -1534,6 +1571,196 @@ int gpt_set_opt_state(gpt* h, const float* m, const float* v, int64_t step) {
   return GPT_OK;
 }
 
+int gpt_serve_end(gpt* h) {
+  if (!h) return GPT_ERR_INVALID_ARG;
+  if (h->serve.mem) {
+    cudaStreamSynchronize(h->stream);
+    cudaFree(h->serve.mem);
+  }
+  h->serve = gpt::Serve{};
+  return GPT_OK;
+}
+
+int gpt_serve_begin(gpt* h, const int32_t* prompt, int32_t n_prompt, int32_t max_new, int32_t blocks,
+                    int32_t tokens_per_step, int64_t first_step) {
+  if (!h) return GPT_ERR_INVALID_ARG;
+  const gpt_config& c = h->cfg;
+  const Dims& D = h->D;
+  if (!is_bf16(c) || c.rope || c.gated_mlp || c.tie_embeddings)
+    return fail(h, GPT_ERR_UNSUPPORTED, "serving runs the bf16 model with learned positions, a GELU MLP and an "
+                "untied LM head");
+  if (!prompt || n_prompt < 1 || max_new < 1 || (int64_t)n_prompt + max_new > D.T || blocks < 1 ||
+      blocks >= h->grid || tokens_per_step < 0 || first_step < 0 || first_step > ((int64_t)1 << 40))
+    return fail(h, GPT_ERR_INVALID_ARG, "need a prompt of >= 1 token, max_new >= 1, n_prompt + max_new <= %d, "
+                "1 <= blocks < %d, tokens_per_step >= 0, 0 <= first_step <= 2^40", D.T, h->grid);
+  for (int32_t i = 0; i < n_prompt; ++i)
+    if (prompt[i] < 0 || prompt[i] >= D.V) return fail(h, GPT_ERR_BAD_TOKEN, "prompt token %d outside [0, vocab)", i);
+  gpt_serve_end(h);
+  gpt::Serve& sv = h->serve;
+  const int C = D.C, F = D.F, L = D.L, T = D.T, V = D.V;
+  const int n_slices = (V + kServeRows - 1) / kServeRows;
+  // ops of one step, in chain order
+  std::vector<ServeOp> ops;
+  Bump mb;
+  const size_t o_kv = mb.take((size_t)L * 2 * T * C * 4);
+  const size_t o_x = mb.take((size_t)C * 4), o_a = mb.take((size_t)C * 4), o_q = mb.take((size_t)C * 4);
+  const size_t o_o = mb.take((size_t)C * 4), o_h = mb.take((size_t)F * 4);
+  const size_t o_pm = mb.take((size_t)n_slices * 4), o_pi = mb.take((size_t)n_slices * 4);
+  const size_t o_seq = mb.take((size_t)T * 4);
+  const size_t o_tic = mb.take(8);
+  const int nops = 1 + 7 * L + 3;
+  const size_t o_ctr = mb.take((size_t)nops * 8);
+  const size_t o_ops = mb.take((size_t)nops * sizeof(ServeOp));
+  const size_t o_par = mb.take(sizeof(ServeParams));
+  // tasks per step
+  int P = 0;
+  std::vector<int32_t> task_op, task_idx;
+  const size_t o_task = mb.take((size_t)(1 + L * (2 + 3 * C / kServeRows + D.H + C / kServeRows + F / kServeRows +
+                                                 C / kServeRows) + 2 + n_slices + 8) * 8);
+  if (cudaMalloc(&sv.mem, mb.off) != cudaSuccess) {
+    cudaGetLastError();
+    sv.mem = nullptr;
+    return fail(h, GPT_ERR_OOM, "cudaMalloc of %zu serving bytes failed", mb.off);
+  }
+  uint8_t* M = sv.mem;
+  auto F32 = [&](size_t off) { return reinterpret_cast<float*>(M + off); };
+  float* kv = F32(o_kv);
+  auto Wt = [&](int t) { return t < 0 ? nullptr : h->shadow + h->tensors[t].offset; };
+  auto Pt = [&](int t) { return t < 0 ? (const float*)nullptr : (const float*)(h->params + h->tensors[t].offset); };
+  auto add = [&](int type, int ntasks, int epi, int K, int N, const uint16_t* W, const float* bias, const float* in,
+                 float* out, float* kc, float* vc, const float* g, const float* b) {
+    ServeOp o{type, ntasks, epi, K, N, W, bias, in, out, kc, vc, g, b};
+    for (int i = 0; i < ntasks; ++i) {
+      task_op.push_back((int32_t)ops.size());
+      task_idx.push_back(i);
+    }
+    ops.push_back(o);
+  };
+  auto rows = [](int N) { return (N + kServeRows - 1) / kServeRows; };
+  add(SV_EMBED, 1, SE_STORE, 0, C, nullptr, nullptr, nullptr, F32(o_x), nullptr, nullptr, nullptr, nullptr);
+  for (int l = 0; l < L; ++l) {
+    const TensorIds& id = h->lid[l];
+    float* kc = kv + (size_t)l * 2 * T * C;
+    float* vc = kc + (size_t)T * C;
+    add(SV_LN, 1, SE_STORE, 0, C, nullptr, nullptr, F32(o_x), F32(o_a), nullptr, nullptr, Pt(id.ln1_g), Pt(id.ln1_b));
+    add(SV_GEMV, rows(3 * C), SE_QKV, C, 3 * C, Wt(id.w_qkv), Pt(id.b_qkv), F32(o_a), F32(o_q), kc, vc, nullptr,
+        nullptr);
+    add(SV_ATTN, D.H, SE_STORE, 0, C, nullptr, nullptr, F32(o_q), F32(o_o), kc, vc, nullptr, nullptr);
+    add(SV_GEMV, rows(C), SE_RESID, C, C, Wt(id.w_o), Pt(id.b_o), F32(o_o), F32(o_x), nullptr, nullptr, nullptr,
+        nullptr);
+    add(SV_LN, 1, SE_STORE, 0, C, nullptr, nullptr, F32(o_x), F32(o_a), nullptr, nullptr, Pt(id.ln2_g), Pt(id.ln2_b));
+    add(SV_GEMV, rows(F), SE_GELU, C, F, Wt(id.w_1), Pt(id.b_1), F32(o_a), F32(o_h), nullptr, nullptr, nullptr,
+        nullptr);
+    add(SV_GEMV, rows(C), SE_RESID, F, C, Wt(id.w_2), Pt(id.b_2), F32(o_h), F32(o_x), nullptr, nullptr, nullptr,
+        nullptr);
+  }
+  add(SV_LN, 1, SE_STORE, 0, C, nullptr, nullptr, F32(o_x), F32(o_a), nullptr, nullptr, Pt(h->t_lnf_g),
+      Pt(h->t_lnf_b));
+  add(SV_GEMV, n_slices, SE_LOGITS, C, V, Wt(h->t_wlm), nullptr, F32(o_a), nullptr, nullptr, nullptr, nullptr,
+      nullptr);
+  add(SV_ARGMAX, 1, SE_STORE, 0, 0, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr);
+  P = (int)task_op.size();
+  if ((int)ops.size() != nops || (size_t)P * 8 > mb.off - o_task) {
+    gpt_serve_end(h);
+    return fail(h, GPT_ERR_UNSUPPORTED, "serving graph size mismatch");
+  }
+  ServeParams& sp = sv.host;
+  std::memset(&sp, 0, sizeof sp);
+  sp.ops = reinterpret_cast<const ServeOp*>(M + o_ops);
+  sp.nops = nops;
+  sp.task_op = reinterpret_cast<const int32_t*>(M + o_task);
+  sp.task_idx = reinterpret_cast<const int32_t*>(M + o_task) + P;
+  sp.P = P;
+  sp.counters = reinterpret_cast<unsigned long long*>(M + o_ctr);
+  sp.ticket = reinterpret_cast<unsigned long long*>(M + o_tic);
+  sp.base = (unsigned long long)first_step;
+  sp.limit = 0;
+  sp.seq = reinterpret_cast<int32_t*>(M + o_seq);
+  sp.n_prompt = n_prompt;
+  sp.C = C; sp.H = D.H; sp.T = T; sp.V = V;
+  sp.ln_eps = c.ln_eps;
+  sp.gelu_tanh = c.gelu_tanh;
+  sp.wte = Pt(h->t_wte);
+  sp.wpe = Pt(h->t_wpe);
+  sp.part_max = F32(o_pm);
+  sp.part_idx = reinterpret_cast<int32_t*>(M + o_pi);
+  sp.n_slices = n_slices;
+  // counters as if first_step steps had completed: op o at first_step x its tasks
+  std::vector<unsigned long long> ctr(nops);
+  for (int o = 0; o < nops; ++o) ctr[o] = (unsigned long long)first_step * (unsigned long long)ops[o].ntasks;
+  std::vector<int32_t> seq(T, 0);
+  std::memcpy(seq.data(), prompt, (size_t)n_prompt * 4);
+  std::vector<int32_t> tasks(task_op);
+  tasks.insert(tasks.end(), task_idx.begin(), task_idx.end());
+  sv.d_params = reinterpret_cast<ServeParams*>(M + o_par);
+  cudaError_t e = cudaMemsetAsync(M, 0, mb.off, h->stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(M + o_ops, ops.data(), ops.size() * sizeof(ServeOp), cudaMemcpyHostToDevice, h->stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(M + o_task, tasks.data(), tasks.size() * 4, cudaMemcpyHostToDevice, h->stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(M + o_ctr, ctr.data(), ctr.size() * 8, cudaMemcpyHostToDevice, h->stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(M + o_seq, seq.data(), seq.size() * 4, cudaMemcpyHostToDevice, h->stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(sv.d_params, &sp, sizeof sp, cudaMemcpyHostToDevice, h->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(h->stream);
+  if (e != cudaSuccess) {
+    gpt_serve_end(h);
+    return fail(h, GPT_ERR_CUDA, "serving set-up failed: %s", cudaGetErrorString(e));
+  }
+  sv.active = true;
+  sv.blocks = blocks;
+  sv.n_prompt = n_prompt;
+  sv.n_new = max_new;
+  sv.per_step = tokens_per_step;
+  sv.steps_total = (int64_t)n_prompt - 1 + max_new;
+  sv.steps_done = 0;
+  sv.base = (unsigned long long)first_step;
+  sv.P = P;
+  return GPT_OK;
+}
+
+int gpt_serve_run(gpt* h, int32_t max_steps, float* kernel_ms) {
+  if (!h) return GPT_ERR_INVALID_ARG;
+  if (!h->serve.active) return fail(h, GPT_ERR_INVALID_ARG, "no serving session (gpt_serve_begin)");
+  if (max_steps < 1) return fail(h, GPT_ERR_INVALID_ARG, "max_steps must be >= 1");
+  if (h->poisoned) return fail(h, GPT_ERR_POISONED, "handle poisoned by an earlier timeout; call gpt_reset");
+  if (h->serve.steps_done >= h->serve.steps_total) return GPT_OK;
+  // a launch whose training blocks have no task: only the serving blocks work, and no
+  // training epoch, ticket or grid-barrier arrival is consumed
+  KParams kp = step_params(h, h->d_tok_stage, h->d_tok_stage, h->launches + 1, h->cfg.lr, h->opt_step + 1);
+  kp.ntasks = 0;
+  kp.grid_bar = nullptr;
+  kp.trace = nullptr;
+  kp.skip_release = -1;
+  int rc = serve_prepare(h, kp, max_steps);
+  if (rc != GPT_OK) return rc;
+  if (h->ev0) CUDA_TRY(h, cudaEventRecord(h->ev0, h->stream));
+  rc = launch_kernel(h, kp);
+  if (rc != GPT_OK) return rc;
+  if (h->ev1) CUDA_TRY(h, cudaEventRecord(h->ev1, h->stream));
+  uint32_t err[4] = {0, 0, 0, 0};
+  CUDA_TRY(h, cudaMemcpyAsync(err, h->d_err, sizeof err, cudaMemcpyDeviceToHost, h->stream));
+  CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  if (h->ev0 && h->ev1) cudaEventElapsedTime(&h->last_kernel_ms, h->ev0, h->ev1);
+  if (kernel_ms) *kernel_ms = h->last_kernel_ms;
+  if (err[0]) {
+    h->poisoned = true;
+    return fail(h, GPT_ERR_TIMEOUT, "serving wait timed out (code %u, task %u, counter %u)", err[0], err[2], err[3]);
+  }
+  return GPT_OK;
+}
+
+int gpt_serve_tokens(gpt* h, int32_t* dst, int32_t cap, int32_t* n) {
+  if (!h || !n) return GPT_ERR_INVALID_ARG;
+  if (!h->serve.active) return fail(h, GPT_ERR_INVALID_ARG, "no serving session (gpt_serve_begin)");
+  const gpt::Serve& sv = h->serve;
+  const int64_t produced = std::max<int64_t>(0, sv.steps_done + 1 - sv.n_prompt);
+  *n = (int32_t)produced;
+  if (dst && produced > 0) {
+    const int32_t m = (int32_t)std::min<int64_t>(produced, cap);
+    CUDA_TRY(h, cudaMemcpyAsync(dst, sv.host.seq + sv.n_prompt, (size_t)m * 4, cudaMemcpyDeviceToHost, h->stream));
+    CUDA_TRY(h, cudaStreamSynchronize(h->stream));
+  }
+  return GPT_OK;
+}
+
 int gpt_run_ops(gpt* h, int32_t op_first, int32_t op_count, const int32_t* tokens, const int32_t* targets,
                 int32_t reps, float* kernel_ms) {
   if (!h) return GPT_ERR_INVALID_ARG;
@@ -1680,6 +1907,7 @@ void gpt_destroy(gpt* h) {
   if (h->own_arena && h->arena) cudaFree(h->arena);
   if (h->h_status) cudaFreeHost(h->h_status);
   if (h->d_trace) cudaFree(h->d_trace);
+  if (h->serve.mem) cudaFree(h->serve.mem);
   if (h->ev0) cudaEventDestroy(h->ev0);
   if (h->ev1) cudaEventDestroy(h->ev1);
   delete h;

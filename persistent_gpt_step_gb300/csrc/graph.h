@@ -207,6 +207,46 @@ constexpr uint32_t kSoftNonFinite = 2u;
 constexpr uint32_t kFatalTimeout = 1u;
 constexpr uint32_t kFatalMbarTimeout = 2u;
 
+// ---- serving partition: greedy generation from the live weights --------------
+// A reserved set of blocks runs one decode step per token: embedding, per layer
+// LayerNorm, QKV (q kept, k and v appended to the cache), attention over the
+// cache, attention-out (+ residual), LayerNorm, MLP up (+ GELU), MLP down (+
+// residual), final LayerNorm, LM head in 64-row slices (each slice keeps its
+// best logit), argmax.  The ops of a step form a chain; a step's embedding waits
+// for the previous step's argmax ("one token releases the next").  Activations
+// are fp32, weights the bf16 copy the training step keeps current.
+enum ServeOpType : int32_t { SV_EMBED = 0, SV_LN, SV_GEMV, SV_ATTN, SV_ARGMAX };
+enum ServeEpi : int32_t { SE_STORE = 0, SE_QKV, SE_RESID, SE_GELU, SE_LOGITS };
+constexpr int kServeRows = 64;  // output rows of a GEMV task
+
+struct ServeOp {
+  int32_t type, ntasks, epi, K, N;
+  const uint16_t* W;          // SV_GEMV: bf16 [N, K] (row-major, y = W x + b)
+  const float* bias;          // [N] or null
+  const float* in;            // [K] input vector (SV_LN, SV_GEMV, SV_ATTN: q)
+  float* out;                 // output vector (SE_RESID: the residual stream, added to)
+  float* kc; float* vc;       // SE_QKV / SV_ATTN: this layer's key and value cache [T, C] fp32
+  const float* g; const float* b;  // SV_LN gain and bias (b may be null)
+};
+
+struct ServeParams {
+  const ServeOp* ops; int32_t nops;
+  const int32_t* task_op; const int32_t* task_idx;  // [P]: op and index of task k of a step
+  int32_t P;                     // tasks per step
+  unsigned long long* counters;  // [nops]: tasks of each op completed, over all steps
+  unsigned long long* ticket;    // next serving ticket: step (ticket / P) - base, task ticket % P
+  unsigned long long base;       // steps completed before this session started (counters start at base x ntasks)
+  int64_t limit;                 // this launch serves steps < limit (the host restores the ticket per launch)
+  int32_t* seq;                  // [T]: the prompt, then the generated tokens
+  int32_t n_prompt;
+  int32_t C, H, T, V;
+  float ln_eps;
+  int32_t gelu_tanh;
+  const float* wte; const float* wpe;   // fp32 master embeddings (the training step keeps them current)
+  float* part_max; int32_t* part_idx;   // [n_slices]: best logit of each LM-head slice and its id
+  int32_t n_slices;
+};
+
 struct KParams {
   const TaskDesc* tasks; int64_t ntasks;
   const OpDesc* ops;
@@ -225,12 +265,18 @@ struct KParams {
   // K steps in one launch: step s (0-based) has epoch epoch + s, reads tokens and
   // targets + s * tok_stride, updates with step_hyper[3 s .. 3 s + 2] = (lr, bc1, bc2)
   // (null: the fields above), and writes loss_out[s], status_out[s].  Between two
-  // steps every block passes a grid barrier on grid_bar, which every block adds 1
-  // to after each step (after the step of epoch e it holds e * gridDim.x).
+  // steps every training block passes a grid barrier on grid_bar, which every
+  // training block adds 1 to after each step (after step s of this launch it
+  // holds bar_base + (s + 1) * the number of training blocks).
   int32_t nsteps;                  // <= 1: one step
   int64_t tok_stride;
   const float* step_hyper;
   unsigned long long* grid_bar;    // null: no step barrier (one-step launches of test graphs)
+  // serving partition: blocks >= train_blocks serve (greedy generation) instead of
+  // training; the grid barrier counts the training blocks only
+  const ServeParams* serve;        // null: every block trains
+  int32_t train_blocks;
+  unsigned long long bar_base;     // grid-barrier arrivals before this launch (each step adds train_blocks)
 };
 
 }  // namespace pgs

@@ -14,6 +14,7 @@
 #include "tasks_simt.cuh"
 #include "tc_gemm.cuh"
 #include "attn_tc.cuh"
+#include "serve.cuh"
 
 namespace pgs {
 
@@ -75,7 +76,10 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
     tc_fence_after();
   }
 
-  const int nsteps = kp.nsteps > 1 ? kp.nsteps : 1;
+  const bool serving = kp.serve != nullptr && (int)blockIdx.x >= kp.train_blocks;
+  if (serving) serve_loop(kp, smem, &sh.task, &sh.ok);  // a serving role for the whole launch
+  const unsigned long long nbar = kp.serve ? (unsigned long long)kp.train_blocks : (unsigned long long)gridDim.x;
+  const int nsteps = serving || kp.ntasks == 0 ? 0 : (kp.nsteps > 1 ? kp.nsteps : 1);
   for (int step = 0; step < nsteps; ++step) {
   if (threadIdx.x == 0) {
     g_step = step;
@@ -187,9 +191,10 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
     if (threadIdx.x == 0 && kp.trace) kp.trace[4 * t + 2] = globaltimer_ns();
   }
   // End of this block's share of the step: its AdamW bulk stores complete and are
-  // published, and the block arrives at the grid barrier (after the step of
-  // epoch e the barrier holds e * gridDim.x).  Between two steps of the launch
-  // every block waits there, so the next step reads the updated weights.
+  // published, and the block arrives at the grid barrier (after step s of the
+  // launch it holds bar_base + (s + 1) x the training blocks).  Between two steps
+  // of the launch every training block waits there, so the next step reads the
+  // updated weights.
   if (threadIdx.x == 0) {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     if (kp.grid_bar) {
@@ -200,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) gpt_step_kernel(const __grid_cons
   }
   if (step + 1 < nsteps) {
     if (threadIdx.x == 0) {
-      const unsigned long long target = (kp.epoch + (unsigned long long)step) * (unsigned long long)gridDim.x;
+      const unsigned long long target = kp.bar_base + (unsigned long long)(step + 1) * nbar;
       int ok = 1;
       if (ld_volatile_u32(&kp.err[0]) == 0u) {
         const uint64_t t0 = globaltimer_ns();

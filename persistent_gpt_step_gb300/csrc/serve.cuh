@@ -59,33 +59,55 @@ __device__ inline void serve_ln(const ServeParams& sp, const ServeOp& op, float*
 // Rows [64 idx, 64 idx + 64) of y = W in + b with the op's epilogue.  The input
 // vector is staged in shared memory; each warp reduces 8 rows, its lanes
 // reading 16-byte chunks (8 bf16) of a row, so a warp reads whole 512-byte spans.
+// The loads of all 8 rows over a 768-wide slice of K are issued before any is
+// reduced: one memory latency per slice instead of one per row.
 __device__ inline void serve_gemv(const ServeParams& sp, const ServeOp& op, int idx, int64_t s, float* sx,
                                   float* red) {
+  constexpr int kR = kServeRows / kWarps;  // rows of a warp
+  constexpr int kU = 3;                    // 16-byte chunks of a row per lane per slice (3 x 32 x 8 = 768)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int k = threadIdx.x; k < op.K; k += kThreads) sx[k] = op.in[k];
   __syncthreads();
-  const int r0 = idx * kServeRows;
-  float best = -INFINITY;
-  int best_i = 0x7fffffff;
-  for (int rr = 0; rr < kServeRows / kWarps; ++rr) {
-    const int r = r0 + warp * (kServeRows / kWarps) + rr;
-    float acc = 0.f;
-    if (r < op.N) {
-      const uint4* w = reinterpret_cast<const uint4*>(op.W + (int64_t)r * op.K);
-      for (int c = lane; c < op.K / 8; c += 32) {
-        const uint4 u = w[c];
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-        const float4 x0 = *reinterpret_cast<const float4*>(sx + 8 * c);
-        const float4 x1 = *reinterpret_cast<const float4*>(sx + 8 * c + 4);
-        const float2 a0 = __bfloat1622float2(h[0]), a1 = __bfloat1622float2(h[1]);
-        const float2 a2 = __bfloat1622float2(h[2]), a3 = __bfloat1622float2(h[3]);
-        acc += a0.x * x0.x + a0.y * x0.y + a1.x * x0.z + a1.y * x0.w + a2.x * x1.x + a2.y * x1.y + a3.x * x1.z +
-               a3.y * x1.w;
+  const int r0 = idx * kServeRows + warp * kR;
+  const int nch = op.K / 8;  // 16-byte chunks of a row
+  float acc[kR];
+#pragma unroll
+  for (int i = 0; i < kR; ++i) acc[i] = 0.f;
+  for (int c0 = 0; c0 < nch; c0 += kU * 32) {
+    uint4 u[kR][kU];
+#pragma unroll
+    for (int i = 0; i < kR; ++i)
+#pragma unroll
+      for (int j = 0; j < kU; ++j) {
+        const int c = c0 + j * 32 + lane;
+        u[i][j] = (r0 + i < op.N && c < nch)
+                      ? reinterpret_cast<const uint4*>(op.W + (int64_t)(r0 + i) * op.K)[c]
+                      : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+    for (int j = 0; j < kU; ++j) {
+      const int c = c0 + j * 32 + lane;
+      if (c >= nch) break;
+      const float4 x0 = *reinterpret_cast<const float4*>(sx + 8 * c);
+      const float4 x1 = *reinterpret_cast<const float4*>(sx + 8 * c + 4);
+#pragma unroll
+      for (int i = 0; i < kR; ++i) {
+        const __nv_bfloat162* hh = reinterpret_cast<const __nv_bfloat162*>(&u[i][j]);
+        const float2 a0 = __bfloat1622float2(hh[0]), a1 = __bfloat1622float2(hh[1]);
+        const float2 a2 = __bfloat1622float2(hh[2]), a3 = __bfloat1622float2(hh[3]);
+        acc[i] += a0.x * x0.x + a0.y * x0.y + a1.x * x0.z + a1.y * x0.w + a2.x * x1.x + a2.y * x1.y + a3.x * x1.z +
+                  a3.y * x1.w;
       }
     }
-    acc = warp_sum(acc);
+  }
+  float best = -INFINITY;
+  int best_i = 0x7fffffff;
+#pragma unroll
+  for (int i = 0; i < kR; ++i) {
+    const int r = r0 + i;
+    const float sum = warp_sum(acc[i]);
     if (r < op.N && lane == 0) {
-      const float y = acc + (op.bias ? op.bias[r] : 0.f);
+      const float y = sum + (op.bias ? op.bias[r] : 0.f);
       switch (op.epi) {
         case SE_QKV:  // q | k | v: k and v are this position's cache rows
           if (r < sp.C) op.out[r] = y;
@@ -119,22 +141,35 @@ __device__ inline void serve_gemv(const ServeParams& sp, const ServeOp& op, int 
 }
 
 // One head of causal attention for the query at position s over the cached
-// keys and values of positions 0..s: softmax(q k_j / sqrt(d)) v.
+// keys and values of positions 0..s: softmax(q k_j / sqrt(d)) v (d = 64).
+// Scores: one thread per key, its key row loaded whole (16 x 16 bytes in
+// flight).  Output: warp w accumulates p_j v_j over the keys j = w mod 8, a lane
+// holding two of the 64 columns, the loads of four keys in flight; the warps'
+// partial rows are added in warp order.
 __device__ inline void serve_attn(const ServeParams& sp, const ServeOp& op, int h, int64_t s, float* sm,
                                   float* red) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int d = sp.C / sp.H;
-  const float scale = rsqrtf((float)d);
-  float* sc = sm;  // [T] scores, then probabilities
-  for (int j = warp; j <= (int)s; j += kWarps) {
-    float acc = 0.f;
-    for (int e = lane; e < d; e += 32) acc += op.in[h * d + e] * op.kc[(int64_t)j * sp.C + h * d + e];
-    acc = warp_sum(acc);
-    if (lane == 0) sc[j] = acc * scale;
-  }
+  constexpr int d = 64;
+  const float scale = 0.125f;  // 1 / sqrt(64)
+  float* sq = sm;              // [64] the query
+  float* sc = sm + 64;         // [T] scores, then probabilities
+  float* po = sc + sp.T;       // [kWarps][64] partial outputs
+  const int n = (int)s + 1;
+  if (threadIdx.x < d) sq[threadIdx.x] = op.in[h * d + threadIdx.x];
   __syncthreads();
   float m = -INFINITY;
-  for (int j = threadIdx.x; j <= (int)s; j += kThreads) m = fmaxf(m, sc[j]);
+  for (int j = threadIdx.x; j < n; j += kThreads) {
+    const float4* kr = reinterpret_cast<const float4*>(op.kc + (int64_t)j * sp.C + h * d);
+    float4 kv[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) kv[i] = kr[i];
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      acc += kv[i].x * sq[4 * i] + kv[i].y * sq[4 * i + 1] + kv[i].z * sq[4 * i + 2] + kv[i].w * sq[4 * i + 3];
+    sc[j] = acc * scale;
+    m = fmaxf(m, acc * scale);
+  }
   m = warp_max(m);
   if (lane == 0) red[warp] = m;
   __syncthreads();
@@ -142,25 +177,39 @@ __device__ inline void serve_attn(const ServeParams& sp, const ServeOp& op, int 
   for (int w = 1; w < kWarps; ++w) m = fmaxf(m, red[w]);
   __syncthreads();
   float acc = 0.f;
-  for (int j = threadIdx.x; j <= (int)s; j += kThreads) {
+  for (int j = threadIdx.x; j < n; j += kThreads) {
     const float p = expf(sc[j] - m);
     sc[j] = p;
     acc += p;
   }
-  const float l = block_sum(acc, red);
-  // o[e] = sum_j p_j v_j[e] / l: thread (e, part) sums positions j = part mod 4
-  float* po = sm + sp.T;  // [4][d] partial sums
-  const int e = threadIdx.x % 64, part = threadIdx.x / 64;
-  if (e < d) {
-    float o = 0.f;
-    for (int j = part; j <= (int)s; j += kThreads / 64) o += sc[j] * op.vc[(int64_t)j * sp.C + h * d + e];
-    po[part * 64 + e] = o;
+  const float l = block_sum(acc, red);  // (its barrier also orders the probabilities before their use)
+  float2 o = make_float2(0.f, 0.f);
+  const float* vb = op.vc + h * d + 2 * lane;
+  int j = warp;
+  for (; j + 3 * kWarps < n; j += 4 * kWarps) {
+    float2 v4[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v4[u] = *reinterpret_cast<const float2*>(vb + (int64_t)(j + u * kWarps) * sp.C);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float p = sc[j + u * kWarps];
+      o.x += p * v4[u].x;
+      o.y += p * v4[u].y;
+    }
   }
+  for (; j < n; j += kWarps) {
+    const float2 v = *reinterpret_cast<const float2*>(vb + (int64_t)j * sp.C);
+    const float p = sc[j];
+    o.x += p * v.x;
+    o.y += p * v.y;
+  }
+  po[warp * 64 + 2 * lane] = o.x;
+  po[warp * 64 + 2 * lane + 1] = o.y;
   __syncthreads();
   if (threadIdx.x < d) {
-    float o = 0.f;
-    for (int p = 0; p < kThreads / 64; ++p) o += po[p * 64 + threadIdx.x];
-    op.out[h * d + threadIdx.x] = o / l;
+    float r = 0.f;
+    for (int w = 0; w < kWarps; ++w) r += po[w * 64 + threadIdx.x];
+    op.out[h * d + threadIdx.x] = r / l;
   }
 }
 

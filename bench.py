@@ -70,6 +70,26 @@ def measured_traffic(workload: str):
     return int(rec["dram_bytes_read"]) + int(rec["dram_bytes_write"])
 
 
+def ptxas_report():
+    """Registers, stack and spill bytes of each step-kernel instance, from the
+    build's -Xptxas -v report (persistent_gpt_step_gb300/_build/ptxas.txt)."""
+    import re
+    path = os.path.join(ROOT, "persistent_gpt_step_gb300", "_build", "ptxas.txt")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    out = {}
+    names = {"I13__nv_bfloat16Lb1ELb0": "bf16", "I13__nv_bfloat16Lb1ELb1": "bf16_variant", "IfLb0ELb0": "fp32"}
+    for key, label in names.items():
+        m = re.search(r"Function properties for _ZN3pgs15gpt_step_kernel" + key + r"\S*\n\s*(\d+) bytes stack frame, "
+                      r"(\d+) bytes spill stores, (\d+) bytes spill loads\n[^\n]*Used (\d+) registers", text)
+        if m:
+            out[label] = {"registers": int(m.group(4)), "stack_bytes": int(m.group(1)),
+                          "spill_stores": int(m.group(2)), "spill_loads": int(m.group(3))}
+    return out or None
+
+
 def model_flops(cfg, n_params: int) -> float:
     """6 * params * tokens + causal attention (fwd + bwd = 3x fwd; fwd = 2 T^2 d per head)."""
     N = cfg.batch * cfg.seq_len
@@ -350,6 +370,7 @@ def main():
         "multi_step_call": {"value": world * args.steps * N / t_multi, "unit": UNIT, "steps_per_call": args.steps,
                             "ms_per_step": 1000.0 * t_multi / args.steps},
         "gpu_launches": args.steps,
+        "ptxas": ptxas_report(),
         "clocks": clk,
         "loss_first_last": [losses[0], losses[-1]],
     }

@@ -45,8 +45,15 @@ constexpr int kAttPreRows = 64;               // token rows of a backward pre-pa
 
 // mbarriers of the attention tasks (initialised once per launch, phases counted
 // in use[]): Q (or K/V of a dK/dV task) loaded; the streamed pair of tiles of
-// buffer 0/1 loaded; scores of buffer 0/1 complete; products of buffer 0/1 complete.
-enum AttBar : int { AB_FIXED = 0, AB_LD0 = 1, AB_S0 = 3, AB_O0 = 5, AB_NUM = 7 };
+// stage 0..3 loaded; scores of buffer 0/1 complete; products of buffer 0/1 complete.
+//
+// The streamed pairs (K_j, V_j, or Q_i, dO_i) go through a ring of kAttStages
+// stages (three in the dK/dV task, whose two resident tiles leave less room):
+// at 512 tokens every block of a task is requested when the task starts, and a
+// stage is refilled as soon as the product that last read it is known complete,
+// which the threads wait for anyway, so no thread ever blocks on a refill.
+constexpr int kAttStages = 4, kAttStagesKV = 3;
+enum AttBar : int { AB_FIXED = 0, AB_LD0 = 1, AB_S0 = AB_LD0 + kAttStages, AB_O0 = AB_S0 + 2, AB_NUM = AB_O0 + 2 };
 
 struct AttnShared {
   uint64_t bar[AB_NUM];
@@ -54,9 +61,9 @@ struct AttnShared {
 };
 
 // Small per-task arrays in the dynamic shared memory, above every task's tiles
-// (at most 10 tiles = 160 KB): values exchanged between the two column halves
+// (at most 13 tiles = 208 KB): values exchanged between the two column halves
 // of a row, and the dK/dV task's LSE (base 2) and D of a query block, two buffers.
-constexpr uint32_t kAttScratchOff = 12 * kAttTile;
+constexpr uint32_t kAttScratchOff = 13 * kAttTile;
 struct AttnScratch {
   float red[2][kAttBlk];
   float ld[2][2][kAttBlk];
@@ -145,8 +152,8 @@ struct AttPhases {
   __device__ __forceinline__ uint32_t par(int b, int k) const { return (use[b] + (uint32_t)k) & 1u; }
 };
 
-// Number of j in [0, n) with j mod 2 == b.
-__device__ __forceinline__ uint32_t n_parity(int n, int b) { return (uint32_t)((n - b + 1) >> 1); }
+// Number of j in [0, n) with j mod m == b (0 <= b < m, n >= 0).
+__device__ __forceinline__ uint32_t n_mod(int n, int b, int m) { return (uint32_t)((n - b + m - 1) / m); }
 
 // Bounded wait of every calling thread; a failure is recorded in the error words
 // and later waits return at once, so every thread keeps the same control flow.
@@ -169,7 +176,9 @@ __device__ inline void task_attn_fwd_tc(const KParams& kp, const AttnArgs& a, in
   const int h = (idx / nqb) % a.H, b = idx / (nqb * a.H);
   const int q0 = qb * kAttBlk, nkb = qb + 1, row0 = b * a.T;
   const void* map = reinterpret_cast<const uint8_t*>(kp.tmaps) + 128 * a.qkv_map;
-  const uint32_t sQ = smem_u32(smem), sK = sQ + kAttTile, sV = sQ + 3 * kAttTile, sP = sQ + 5 * kAttTile;
+  // tiles: Q | K stages 0..3 | V stages 0..3 | P buffers 0, 1 (two tiles each)
+  const uint32_t sQ = smem_u32(smem), sK = sQ + kAttTile, sV = sK + kAttStages * kAttTile,
+                 sP = sV + kAttStages * kAttTile;
   const uint32_t bar0 = smem_u32(&as.bar[0]);
   AttnScratch& sc = *reinterpret_cast<AttnScratch*>(smem + kAttScratchOff);
   AttPhases ph;
@@ -178,25 +187,25 @@ __device__ inline void task_attn_fwd_tc(const KParams& kp, const AttnArgs& a, in
   const int r = quarter * 32 + lane;                        // this thread's query row (TMEM lane)
   const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
   const uint32_t id_s = idesc_bf16(128, 128, 0, 0), id_o = idesc_bf16(128, 64, 0, 1);
-  auto load_kv = [&](int j) {
-    const int buf = j & 1;
-    const uint32_t bar = bar0 + 8 * (AB_LD0 + buf);
+  auto load_kv = [&](int j) {  // leader: K_j and V_j into stage j mod kAttStages
+    const int st = j % kAttStages;
+    const uint32_t bar = bar0 + 8 * (AB_LD0 + st);
     mbar_arrive_expect_tx(bar, 2 * kAttTile);
-    tma_load_2d(sK + buf * kAttTile, map, a.C + h * 64, row0 + j * kAttBlk, bar);
-    tma_load_2d(sV + buf * kAttTile, map, 2 * a.C + h * 64, row0 + j * kAttBlk, bar);
+    tma_load_2d(sK + st * kAttTile, map, a.C + h * 64, row0 + j * kAttBlk, bar);
+    tma_load_2d(sV + st * kAttTile, map, 2 * a.C + h * 64, row0 + j * kAttBlk, bar);
   };
   auto issue_s = [&](int j) {  // leader: S_j = Q K_j^T into TMEM columns 128 (j & 1)
-    const int buf = j & 1;
-    att_wait(kp, bar0 + 8 * (AB_LD0 + buf), ph.par(AB_LD0 + buf, j >> 1));
+    const int buf = j & 1, st = j % kAttStages;
+    att_wait(kp, bar0 + 8 * (AB_LD0 + st), ph.par(AB_LD0 + st, j / kAttStages));
     tc_fence_after();
-    att_mma_kk(tmem + 128u * buf, sQ, sK + buf * kAttTile, 4, id_s, false);
+    att_mma_kk(tmem + 128u * buf, sQ, sK + st * kAttTile, 4, id_s, false);
     tc_commit(bar0 + 8 * (AB_S0 + buf));
   };
   if (leader) {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier generic writes of this memory
     mbar_arrive_expect_tx(bar0 + 8 * AB_FIXED, kAttTile);
     tma_load_2d(sQ, map, h * 64, row0 + q0, bar0 + 8 * AB_FIXED);
-    for (int j = 0; j < min(2, nkb); ++j) load_kv(j);
+    for (int j = 0; j < min(kAttStages, nkb); ++j) load_kv(j);
     att_wait(kp, bar0 + 8 * AB_FIXED, ph.par(AB_FIXED, 0));
     issue_s(0);
   }
@@ -245,17 +254,16 @@ __device__ inline void task_attn_fwd_tc(const KParams& kp, const AttnArgs& a, in
     __syncthreads();
     if (leader) {
       tc_fence_after();
-      att_mma_kmn(tmem + 256u + 64u * buf, pt - (uint32_t)half * kAttTile, sV + buf * kAttTile, 8, id_o, false);
+      att_mma_kmn(tmem + 256u + 64u * buf, pt - (uint32_t)half * kAttTile, sV + (j % kAttStages) * kAttTile, 8,
+                  id_o, false);
       tc_commit(bar0 + 8 * (AB_O0 + buf));
-      if (j + 2 < nkb) {  // K_j and V_j are no longer read: stream in block j + 2
-        att_wait(kp, bar0 + 8 * (AB_O0 + buf), ph.par(AB_O0 + buf, j >> 1));
-        load_kv(j + 2);
-      }
     }
     __syncwarp();
     if (j >= 1) {  // add the partial of block j - 1, rescaled from its running max to this one
       const int pb = (j - 1) & 1;
       att_wait(kp, bar0 + 8 * (AB_O0 + pb), ph.par(AB_O0 + pb, (j - 1) >> 1));
+      // K_{j-1} and V_{j-1} are no longer read (every earlier product is complete): refill their stage
+      if (leader && j - 1 + kAttStages < nkb) load_kv(j - 1 + kAttStages);
       __syncwarp();
       tc_fence_after();
       float part[32];
@@ -291,10 +299,11 @@ __device__ inline void task_attn_fwd_tc(const KParams& kp, const AttnArgs& a, in
   if (leader) {
     as.use[AB_FIXED] = ph.use[AB_FIXED] + 1u;
 #pragma unroll
+    for (int st = 0; st < kAttStages; ++st) as.use[AB_LD0 + st] = ph.use[AB_LD0 + st] + n_mod(nkb, st, kAttStages);
+#pragma unroll
     for (int bb = 0; bb < 2; ++bb) {
-      as.use[AB_LD0 + bb] = ph.use[AB_LD0 + bb] + n_parity(nkb, bb);
-      as.use[AB_S0 + bb] = ph.use[AB_S0 + bb] + n_parity(nkb, bb);
-      as.use[AB_O0 + bb] = ph.use[AB_O0 + bb] + n_parity(nkb, bb);
+      as.use[AB_S0 + bb] = ph.use[AB_S0 + bb] + n_mod(nkb, bb, 2);
+      as.use[AB_O0 + bb] = ph.use[AB_O0 + bb] + n_mod(nkb, bb, 2);
     }
   }
 }
@@ -368,8 +377,9 @@ __device__ inline void task_attn_bwd_kv_tc(const KParams& kp, const AttnArgs& a,
   const int k0 = kb * kAttBlk, row0 = b * a.T, nq = nkb - kb;  // query blocks kb .. nkb - 1
   const void* qmap = reinterpret_cast<const uint8_t*>(kp.tmaps) + 128 * a.qkv_map;
   const void* dmap = reinterpret_cast<const uint8_t*>(kp.tmaps) + 128 * a.do_map;
-  const uint32_t sK = smem_u32(smem), sV = sK + kAttTile, sQ = sK + 2 * kAttTile, sO = sK + 4 * kAttTile,
-                 sPt = sK + 6 * kAttTile, sDs = sK + 8 * kAttTile;
+  // tiles: K | V | Q stages 0..2 | dO stages 0..2 | P^T (two tiles) | dS^T (two tiles)
+  const uint32_t sK = smem_u32(smem), sV = sK + kAttTile, sQ = sK + 2 * kAttTile,
+                 sO = sQ + kAttStagesKV * kAttTile, sPt = sO + kAttStagesKV * kAttTile, sDs = sPt + 2 * kAttTile;
   const uint32_t bar0 = smem_u32(&as.bar[0]);
   AttnScratch& sc = *reinterpret_cast<AttnScratch*>(smem + kAttScratchOff);
   AttPhases ph;
@@ -381,12 +391,12 @@ __device__ inline void task_attn_bwd_kv_tc(const KParams& kp, const AttnArgs& a,
   const float* Lg = a.lse + ((int64_t)b * a.H + h) * a.T;
   const float* Dg = a.scratch + ((int64_t)b * a.H + h) * a.T;
   const float log2e = 1.4426950408889634f, sl2 = a.scale * log2e;
-  auto load_qo = [&](int it) {  // leader: Q and dO of query block kb + it into buffer it & 1
-    const int buf = it & 1, i = kb + it;
-    const uint32_t bar = bar0 + 8 * (AB_LD0 + buf);
+  auto load_qo = [&](int it) {  // leader: Q and dO of query block kb + it into stage it mod kAttStagesKV
+    const int st = it % kAttStagesKV, i = kb + it;
+    const uint32_t bar = bar0 + 8 * (AB_LD0 + st);
     mbar_arrive_expect_tx(bar, 2 * kAttTile);
-    tma_load_2d(sQ + buf * kAttTile, qmap, h * 64, row0 + i * kAttBlk, bar);
-    tma_load_2d(sO + buf * kAttTile, dmap, h * 64, row0 + i * kAttBlk, bar);
+    tma_load_2d(sQ + st * kAttTile, qmap, h * 64, row0 + i * kAttBlk, bar);
+    tma_load_2d(sO + st * kAttTile, dmap, h * 64, row0 + i * kAttBlk, bar);
   };
   auto stage_ld = [&](int it) {  // all threads: LSE (base 2) and D of query block kb + it
     const int i = kb + it, c = threadIdx.x & (kAttBlk - 1), w = threadIdx.x >> 7;
@@ -398,25 +408,28 @@ __device__ inline void task_attn_bwd_kv_tc(const KParams& kp, const AttnArgs& a,
     mbar_arrive_expect_tx(bar0 + 8 * AB_FIXED, 2 * kAttTile);
     tma_load_2d(sK, qmap, a.C + h * 64, row0 + k0, bar0 + 8 * AB_FIXED);
     tma_load_2d(sV, qmap, 2 * a.C + h * 64, row0 + k0, bar0 + 8 * AB_FIXED);
-    for (int it = 0; it < min(2, nq); ++it) load_qo(it);
+    for (int it = 0; it < min(kAttStagesKV, nq); ++it) load_qo(it);
   }
   __syncwarp();
   stage_ld(0);
   __syncthreads();
   for (int it = 0; it < nq; ++it) {
-    const int buf = it & 1;
+    const int buf = it & 1, st = it % kAttStagesKV;
     if (leader) {  // S^T = K Q_i^T and dP^T = V dO_i^T (their TMEM columns were read before the last block barrier)
       if (it == 0) att_wait(kp, bar0 + 8 * AB_FIXED, ph.par(AB_FIXED, 0));
-      att_wait(kp, bar0 + 8 * (AB_LD0 + buf), ph.par(AB_LD0 + buf, it >> 1));
+      att_wait(kp, bar0 + 8 * (AB_LD0 + st), ph.par(AB_LD0 + st, it / kAttStagesKV));
       tc_fence_after();
-      att_mma_kk(tmem, sK, sQ + buf * kAttTile, 4, id_s, false);
-      att_mma_kk(tmem + 128u, sV, sO + buf * kAttTile, 4, id_s, false);
+      att_mma_kk(tmem, sK, sQ + st * kAttTile, 4, id_s, false);
+      att_mma_kk(tmem + 128u, sV, sO + st * kAttTile, 4, id_s, false);
       tc_commit(bar0 + 8 * AB_S0);
     }
     __syncwarp();
     if (it + 1 < nq) stage_ld(it + 1);  // read after this block's barrier; its buffer was last read before the previous one
     att_wait(kp, bar0 + 8 * AB_S0, ph.par(AB_S0, it));
-    if (it >= 1) att_wait(kp, bar0 + 8 * AB_O0, ph.par(AB_O0, it - 1));  // the previous products no longer read P^T, dS^T
+    if (it >= 1) {  // the previous products no longer read P^T, dS^T, nor Q_{i-1}, dO_{i-1}: refill that stage
+      att_wait(kp, bar0 + 8 * AB_O0, ph.par(AB_O0, it - 1));
+      if (leader && it - 1 + kAttStagesKV < nq) load_qo(it - 1 + kAttStagesKV);
+    }
     __syncwarp();
     tc_fence_after();
     const bool diag = it == 0;  // the key block's own query block: queries before a key are masked
@@ -443,13 +456,9 @@ __device__ inline void task_attn_bwd_kv_tc(const KParams& kp, const AttnArgs& a,
     __syncthreads();
     if (leader) {  // dV += P^T dO_i, dK += dS^T Q_i
       tc_fence_after();
-      att_mma_kmn(tmem + 256u, sPt, sO + buf * kAttTile, 8, id_o, it > 0);
-      att_mma_kmn(tmem + 320u, sDs, sQ + buf * kAttTile, 8, id_o, it > 0);
+      att_mma_kmn(tmem + 256u, sPt, sO + st * kAttTile, 8, id_o, it > 0);
+      att_mma_kmn(tmem + 320u, sDs, sQ + st * kAttTile, 8, id_o, it > 0);
       tc_commit(bar0 + 8 * AB_O0);
-      if (it + 2 < nq) {  // Q_i and dO_i are no longer read: stream in block i + 2
-        att_wait(kp, bar0 + 8 * AB_O0, ph.par(AB_O0, it));
-        load_qo(it + 2);
-      }
     }
     __syncwarp();
   }
@@ -479,8 +488,8 @@ __device__ inline void task_attn_bwd_kv_tc(const KParams& kp, const AttnArgs& a,
   __syncthreads();
   if (leader) {
     as.use[AB_FIXED] = ph.use[AB_FIXED] + 1u;
-    as.use[AB_LD0] = ph.use[AB_LD0] + n_parity(nq, 0);
-    as.use[AB_LD0 + 1] = ph.use[AB_LD0 + 1] + n_parity(nq, 1);
+#pragma unroll
+    for (int st = 0; st < kAttStagesKV; ++st) as.use[AB_LD0 + st] = ph.use[AB_LD0 + st] + n_mod(nq, st, kAttStagesKV);
     as.use[AB_S0] = ph.use[AB_S0] + (uint32_t)nq;
     as.use[AB_O0] = ph.use[AB_O0] + (uint32_t)nq;
   }
@@ -498,8 +507,9 @@ __device__ inline void task_attn_bwd_q_tc(const KParams& kp, const AttnArgs& a, 
   const int q0 = qb * kAttBlk, row0 = b * a.T, nkb = qb + 1;
   const void* qmap = reinterpret_cast<const uint8_t*>(kp.tmaps) + 128 * a.qkv_map;
   const void* dmap = reinterpret_cast<const uint8_t*>(kp.tmaps) + 128 * a.do_map;
-  const uint32_t sQ = smem_u32(smem), sO = sQ + kAttTile, sK = sQ + 2 * kAttTile, sV = sQ + 4 * kAttTile,
-                 sDs = sQ + 6 * kAttTile;
+  // tiles: Q | dO | K stages 0..3 | V stages 0..3 | dS (two tiles)
+  const uint32_t sQ = smem_u32(smem), sO = sQ + kAttTile, sK = sQ + 2 * kAttTile, sV = sK + kAttStages * kAttTile,
+                 sDs = sV + kAttStages * kAttTile;
   const uint32_t bar0 = smem_u32(&as.bar[0]);
   AttPhases ph;
   ph.load(as);
@@ -510,34 +520,37 @@ __device__ inline void task_attn_bwd_q_tc(const KParams& kp, const AttnArgs& a, 
   const float log2e = 1.4426950408889634f, sl2 = a.scale * log2e;
   const float lse2 = a.lse[((int64_t)b * a.H + h) * a.T + q0 + r] * log2e;
   const float dd = a.scratch[((int64_t)b * a.H + h) * a.T + q0 + r];
-  auto load_kv = [&](int j) {
-    const int buf = j & 1;
-    const uint32_t bar = bar0 + 8 * (AB_LD0 + buf);
+  auto load_kv = [&](int j) {  // leader: K_j and V_j into stage j mod kAttStages
+    const int st = j % kAttStages;
+    const uint32_t bar = bar0 + 8 * (AB_LD0 + st);
     mbar_arrive_expect_tx(bar, 2 * kAttTile);
-    tma_load_2d(sK + buf * kAttTile, qmap, a.C + h * 64, row0 + j * kAttBlk, bar);
-    tma_load_2d(sV + buf * kAttTile, qmap, 2 * a.C + h * 64, row0 + j * kAttBlk, bar);
+    tma_load_2d(sK + st * kAttTile, qmap, a.C + h * 64, row0 + j * kAttBlk, bar);
+    tma_load_2d(sV + st * kAttTile, qmap, 2 * a.C + h * 64, row0 + j * kAttBlk, bar);
   };
   if (leader) {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_arrive_expect_tx(bar0 + 8 * AB_FIXED, 2 * kAttTile);
     tma_load_2d(sQ, qmap, h * 64, row0 + q0, bar0 + 8 * AB_FIXED);
     tma_load_2d(sO, dmap, h * 64, row0 + q0, bar0 + 8 * AB_FIXED);
-    for (int j = 0; j < min(2, nkb); ++j) load_kv(j);
+    for (int j = 0; j < min(kAttStages, nkb); ++j) load_kv(j);
   }
   __syncwarp();
   for (int j = 0; j < nkb; ++j) {
-    const int buf = j & 1;
+    const int st = j % kAttStages;
     if (leader) {  // S = Q K_j^T, dP = dO V_j^T (their TMEM columns were read before the last block barrier)
       if (j == 0) att_wait(kp, bar0 + 8 * AB_FIXED, ph.par(AB_FIXED, 0));
-      att_wait(kp, bar0 + 8 * (AB_LD0 + buf), ph.par(AB_LD0 + buf, j >> 1));
+      att_wait(kp, bar0 + 8 * (AB_LD0 + st), ph.par(AB_LD0 + st, j / kAttStages));
       tc_fence_after();
-      att_mma_kk(tmem, sQ, sK + buf * kAttTile, 4, id_s, false);
-      att_mma_kk(tmem + 128u, sO, sV + buf * kAttTile, 4, id_s, false);
+      att_mma_kk(tmem, sQ, sK + st * kAttTile, 4, id_s, false);
+      att_mma_kk(tmem + 128u, sO, sV + st * kAttTile, 4, id_s, false);
       tc_commit(bar0 + 8 * AB_S0);
     }
     __syncwarp();
     att_wait(kp, bar0 + 8 * AB_S0, ph.par(AB_S0, j));
-    if (j >= 1) att_wait(kp, bar0 + 8 * AB_O0, ph.par(AB_O0, j - 1));  // the previous product no longer reads dS
+    if (j >= 1) {  // the previous product no longer reads dS, nor K_{j-1}, V_{j-1}: refill that stage
+      att_wait(kp, bar0 + 8 * AB_O0, ph.par(AB_O0, j - 1));
+      if (leader && j - 1 + kAttStages < nkb) load_kv(j - 1 + kAttStages);
+    }
     __syncwarp();
     tc_fence_after();
     const bool diag = j == nkb - 1;  // keys after a query are masked
@@ -560,12 +573,8 @@ __device__ inline void task_attn_bwd_q_tc(const KParams& kp, const AttnArgs& a, 
     __syncthreads();
     if (leader) {  // dQ += dS K_j
       tc_fence_after();
-      att_mma_kmn(tmem + 256u, sDs, sK + buf * kAttTile, 8, id_o, j > 0);
+      att_mma_kmn(tmem + 256u, sDs, sK + st * kAttTile, 8, id_o, j > 0);
       tc_commit(bar0 + 8 * AB_O0);
-      if (j + 2 < nkb) {  // K_j and V_j are no longer read: stream in block j + 2
-        att_wait(kp, bar0 + 8 * AB_O0, ph.par(AB_O0, j));
-        load_kv(j + 2);
-      }
     }
     __syncwarp();
   }
@@ -588,8 +597,8 @@ __device__ inline void task_attn_bwd_q_tc(const KParams& kp, const AttnArgs& a, 
   __syncthreads();
   if (leader) {
     as.use[AB_FIXED] = ph.use[AB_FIXED] + 1u;
-    as.use[AB_LD0] = ph.use[AB_LD0] + n_parity(nkb, 0);
-    as.use[AB_LD0 + 1] = ph.use[AB_LD0 + 1] + n_parity(nkb, 1);
+#pragma unroll
+    for (int st = 0; st < kAttStages; ++st) as.use[AB_LD0 + st] = ph.use[AB_LD0 + st] + n_mod(nkb, st, kAttStages);
     as.use[AB_S0] = ph.use[AB_S0] + (uint32_t)nkb;
     as.use[AB_O0] = ph.use[AB_O0] + (uint32_t)nkb;
   }

@@ -183,7 +183,11 @@ __device__ inline void task_attn_fwd_tc(const KParams& kp, const AttnArgs& a, in
   AttnScratch& sc = *reinterpret_cast<AttnScratch*>(smem + kAttScratchOff);
   AttPhases ph;
   ph.load(as);
-  const bool leader = threadIdx.x == 0;
+  // One thread of three different warps each: the copies, the score products, the
+  // value products.  Issuing a product takes its thread about as long as the tensor
+  // pipe needs for the products queued before it, so the issue work is spread over
+  // warps that otherwise do the same share of the softmax.
+  const bool leader = threadIdx.x == 0, s_issuer = threadIdx.x == 32, o_issuer = threadIdx.x == 64;
   const int r = quarter * 32 + lane;                        // this thread's query row (TMEM lane)
   const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
   const uint32_t id_s = idesc_bf16(128, 128, 0, 0), id_o = idesc_bf16(128, 64, 0, 1);
@@ -194,7 +198,7 @@ __device__ inline void task_attn_fwd_tc(const KParams& kp, const AttnArgs& a, in
     tma_load_2d(sK + st * kAttTile, map, a.C + h * 64, row0 + j * kAttBlk, bar);
     tma_load_2d(sV + st * kAttTile, map, 2 * a.C + h * 64, row0 + j * kAttBlk, bar);
   };
-  auto issue_s = [&](int j) {  // leader: S_j = Q K_j^T into TMEM columns 128 (j & 1)
+  auto issue_s = [&](int j) {  // s_issuer: S_j = Q K_j^T into TMEM columns 128 (j & 1)
     const int buf = j & 1, st = j % kAttStages;
     att_wait(kp, bar0 + 8 * (AB_LD0 + st), ph.par(AB_LD0 + st, j / kAttStages));
     tc_fence_after();
@@ -206,6 +210,8 @@ __device__ inline void task_attn_fwd_tc(const KParams& kp, const AttnArgs& a, in
     mbar_arrive_expect_tx(bar0 + 8 * AB_FIXED, kAttTile);
     tma_load_2d(sQ, map, h * 64, row0 + q0, bar0 + 8 * AB_FIXED);
     for (int j = 0; j < min(kAttStages, nkb); ++j) load_kv(j);
+  }
+  if (s_issuer) {
     att_wait(kp, bar0 + 8 * AB_FIXED, ph.par(AB_FIXED, 0));
     issue_s(0);
   }
@@ -217,7 +223,7 @@ __device__ inline void task_attn_fwd_tc(const KParams& kp, const AttnArgs& a, in
   float m_run = -INFINITY, l_run = 0.f, alpha_pend = 0.f;
   for (int j = 0; j < nkb; ++j) {
     const int buf = j & 1;
-    if (leader && j + 1 < nkb) issue_s(j + 1);  // its buffer was last read before the previous block barrier
+    if (s_issuer && j + 1 < nkb) issue_s(j + 1);  // its buffer was last read before the previous block barrier
     __syncwarp();
     att_wait(kp, bar0 + 8 * (AB_S0 + buf), ph.par(AB_S0 + buf, j >> 1));
     __syncwarp();
@@ -252,7 +258,7 @@ __device__ inline void task_attn_fwd_tc(const KParams& kp, const AttnArgs& a, in
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic smem writes -> tensor core reads
     tc_fence_before();
     __syncthreads();
-    if (leader) {
+    if (o_issuer) {
       tc_fence_after();
       att_mma_kmn(tmem + 256u + 64u * buf, pt - (uint32_t)half * kAttTile, sV + (j % kAttStages) * kAttTile, 8,
                   id_o, false);
@@ -384,7 +390,9 @@ __device__ inline void task_attn_bwd_kv_tc(const KParams& kp, const AttnArgs& a,
   AttnScratch& sc = *reinterpret_cast<AttnScratch*>(smem + kAttScratchOff);
   AttPhases ph;
   ph.load(as);
-  const bool leader = threadIdx.x == 0;
+  // the copies, and each of the four products, issued by one thread of a different warp
+  const bool leader = threadIdx.x == 0, st_issuer = threadIdx.x == 32, dpt_issuer = threadIdx.x == 64,
+             dv_issuer = threadIdx.x == 96, dk_issuer = threadIdx.x == 160;
   const int r = quarter * 32 + lane;  // this thread's key row (TMEM lane)
   const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
   const uint32_t id_s = idesc_bf16(128, 128, 0, 0), id_o = idesc_bf16(128, 64, 0, 1);
@@ -415,19 +423,22 @@ __device__ inline void task_attn_bwd_kv_tc(const KParams& kp, const AttnArgs& a,
   __syncthreads();
   for (int it = 0; it < nq; ++it) {
     const int buf = it & 1, st = it % kAttStagesKV;
-    if (leader) {  // S^T = K Q_i^T and dP^T = V dO_i^T (their TMEM columns were read before the last block barrier)
+    // S^T = K Q_i^T and dP^T = V dO_i^T (their TMEM columns were read before the last block barrier)
+    if (st_issuer || dpt_issuer) {
       if (it == 0) att_wait(kp, bar0 + 8 * AB_FIXED, ph.par(AB_FIXED, 0));
       att_wait(kp, bar0 + 8 * (AB_LD0 + st), ph.par(AB_LD0 + st, it / kAttStagesKV));
       tc_fence_after();
-      att_mma_kk(tmem, sK, sQ + st * kAttTile, 4, id_s, false);
-      att_mma_kk(tmem + 128u, sV, sO + st * kAttTile, 4, id_s, false);
-      tc_commit(bar0 + 8 * AB_S0);
+      if (st_issuer) att_mma_kk(tmem, sK, sQ + st * kAttTile, 4, id_s, false);
+      else att_mma_kk(tmem + 128u, sV, sO + st * kAttTile, 4, id_s, false);
+      tc_commit(bar0 + 8 * (AB_S0 + (st_issuer ? 0 : 1)));
     }
     __syncwarp();
     if (it + 1 < nq) stage_ld(it + 1);  // read after this block's barrier; its buffer was last read before the previous one
     att_wait(kp, bar0 + 8 * AB_S0, ph.par(AB_S0, it));
+    att_wait(kp, bar0 + 8 * (AB_S0 + 1), ph.par(AB_S0 + 1, it));
     if (it >= 1) {  // the previous products no longer read P^T, dS^T, nor Q_{i-1}, dO_{i-1}: refill that stage
       att_wait(kp, bar0 + 8 * AB_O0, ph.par(AB_O0, it - 1));
+      att_wait(kp, bar0 + 8 * (AB_O0 + 1), ph.par(AB_O0 + 1, it - 1));
       if (leader && it - 1 + kAttStagesKV < nq) load_qo(it - 1 + kAttStagesKV);
     }
     __syncwarp();
@@ -454,15 +465,16 @@ __device__ inline void task_attn_bwd_kv_tc(const KParams& kp, const AttnArgs& a,
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
     __syncthreads();
-    if (leader) {  // dV += P^T dO_i, dK += dS^T Q_i
+    if (dv_issuer || dk_issuer) {  // dV += P^T dO_i, dK += dS^T Q_i
       tc_fence_after();
-      att_mma_kmn(tmem + 256u, sPt, sO + st * kAttTile, 8, id_o, it > 0);
-      att_mma_kmn(tmem + 320u, sDs, sQ + st * kAttTile, 8, id_o, it > 0);
-      tc_commit(bar0 + 8 * AB_O0);
+      if (dv_issuer) att_mma_kmn(tmem + 256u, sPt, sO + st * kAttTile, 8, id_o, it > 0);
+      else att_mma_kmn(tmem + 320u, sDs, sQ + st * kAttTile, 8, id_o, it > 0);
+      tc_commit(bar0 + 8 * (AB_O0 + (dv_issuer ? 0 : 1)));
     }
     __syncwarp();
   }
   att_wait(kp, bar0 + 8 * AB_O0, ph.par(AB_O0, nq - 1));
+  att_wait(kp, bar0 + 8 * (AB_O0 + 1), ph.par(AB_O0 + 1, nq - 1));
   __syncwarp();
   tc_fence_after();
   const int64_t ld = 3 * (int64_t)a.C;
@@ -490,8 +502,11 @@ __device__ inline void task_attn_bwd_kv_tc(const KParams& kp, const AttnArgs& a,
     as.use[AB_FIXED] = ph.use[AB_FIXED] + 1u;
 #pragma unroll
     for (int st = 0; st < kAttStagesKV; ++st) as.use[AB_LD0 + st] = ph.use[AB_LD0 + st] + n_mod(nq, st, kAttStagesKV);
-    as.use[AB_S0] = ph.use[AB_S0] + (uint32_t)nq;
-    as.use[AB_O0] = ph.use[AB_O0] + (uint32_t)nq;
+#pragma unroll
+    for (int bb = 0; bb < 2; ++bb) {
+      as.use[AB_S0 + bb] = ph.use[AB_S0 + bb] + (uint32_t)nq;
+      as.use[AB_O0 + bb] = ph.use[AB_O0 + bb] + (uint32_t)nq;
+    }
   }
 }
 
@@ -513,7 +528,9 @@ __device__ inline void task_attn_bwd_q_tc(const KParams& kp, const AttnArgs& a, 
   const uint32_t bar0 = smem_u32(&as.bar[0]);
   AttPhases ph;
   ph.load(as);
-  const bool leader = threadIdx.x == 0;
+  // the copies, and each of the three products, issued by one thread of a different warp
+  const bool leader = threadIdx.x == 0, s_issuer = threadIdx.x == 32, dp_issuer = threadIdx.x == 64,
+             dq_issuer = threadIdx.x == 96;
   const int r = quarter * 32 + lane;  // this thread's query row (TMEM lane)
   const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
   const uint32_t id_s = idesc_bf16(128, 128, 0, 0), id_o = idesc_bf16(128, 64, 0, 1);
@@ -537,16 +554,18 @@ __device__ inline void task_attn_bwd_q_tc(const KParams& kp, const AttnArgs& a, 
   __syncwarp();
   for (int j = 0; j < nkb; ++j) {
     const int st = j % kAttStages;
-    if (leader) {  // S = Q K_j^T, dP = dO V_j^T (their TMEM columns were read before the last block barrier)
+    // S = Q K_j^T, dP = dO V_j^T (their TMEM columns were read before the last block barrier)
+    if (s_issuer || dp_issuer) {
       if (j == 0) att_wait(kp, bar0 + 8 * AB_FIXED, ph.par(AB_FIXED, 0));
       att_wait(kp, bar0 + 8 * (AB_LD0 + st), ph.par(AB_LD0 + st, j / kAttStages));
       tc_fence_after();
-      att_mma_kk(tmem, sQ, sK + st * kAttTile, 4, id_s, false);
-      att_mma_kk(tmem + 128u, sO, sV + st * kAttTile, 4, id_s, false);
-      tc_commit(bar0 + 8 * AB_S0);
+      if (s_issuer) att_mma_kk(tmem, sQ, sK + st * kAttTile, 4, id_s, false);
+      else att_mma_kk(tmem + 128u, sO, sV + st * kAttTile, 4, id_s, false);
+      tc_commit(bar0 + 8 * (AB_S0 + (s_issuer ? 0 : 1)));
     }
     __syncwarp();
     att_wait(kp, bar0 + 8 * AB_S0, ph.par(AB_S0, j));
+    att_wait(kp, bar0 + 8 * (AB_S0 + 1), ph.par(AB_S0 + 1, j));
     if (j >= 1) {  // the previous product no longer reads dS, nor K_{j-1}, V_{j-1}: refill that stage
       att_wait(kp, bar0 + 8 * AB_O0, ph.par(AB_O0, j - 1));
       if (leader && j - 1 + kAttStages < nkb) load_kv(j - 1 + kAttStages);
@@ -571,7 +590,7 @@ __device__ inline void task_attn_bwd_q_tc(const KParams& kp, const AttnArgs& a, 
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     tc_fence_before();
     __syncthreads();
-    if (leader) {  // dQ += dS K_j
+    if (dq_issuer) {  // dQ += dS K_j
       tc_fence_after();
       att_mma_kmn(tmem + 256u, sDs, sK + st * kAttTile, 8, id_o, j > 0);
       tc_commit(bar0 + 8 * AB_O0);
@@ -600,6 +619,7 @@ __device__ inline void task_attn_bwd_q_tc(const KParams& kp, const AttnArgs& a, 
 #pragma unroll
     for (int st = 0; st < kAttStages; ++st) as.use[AB_LD0 + st] = ph.use[AB_LD0 + st] + n_mod(nkb, st, kAttStages);
     as.use[AB_S0] = ph.use[AB_S0] + (uint32_t)nkb;
+    as.use[AB_S0 + 1] = ph.use[AB_S0 + 1] + (uint32_t)nkb;
     as.use[AB_O0] = ph.use[AB_O0] + (uint32_t)nkb;
   }
 }

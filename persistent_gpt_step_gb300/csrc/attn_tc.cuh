@@ -14,7 +14,7 @@
 //   forward, task (b, h, 128 queries), key blocks j = 0 .. diagonal:
 //       S_j = Q K_j^T (TMEM, two buffers: S_{j+1} is computed while S_j is
 //       reduced), running row max m and sum l in registers (base 2), P_j =
-//       exp2(S_j * scale * log2 e - m) to shared memory, O_j = P_j V_j into one of
+//       exp2(S_j * scale * log2 e - m) (the SFU's approximate 2^x) to shared memory, O_j = P_j V_j into one of
 //       two TMEM buffers; the thread adds O_j to its 32 output columns, rescaled
 //       by exp2(m_old - m_new), while the next block's probabilities are formed.
 //       O = sum / l, LSE = ln 2 (m + log2 l) saved for the backward pass.
@@ -241,11 +241,11 @@ __device__ inline void task_attn_fwd_tc(const KParams& kp, const AttnArgs& a, in
     sc.red[half][r] = mx;
     pair_sync(quarter);
     const float m_new = fmaxf(m_run, fmaxf(sc.red[0][r], sc.red[1][r]));
-    const float alpha = exp2f(m_run - m_new);
+    const float alpha = ex2_sfu(m_run - m_new);
     float ls = 0.f;
 #pragma unroll
     for (int i = 0; i < 64; ++i) {
-      s[i] = exp2f(s[i] - m_new);
+      s[i] = ex2_sfu(s[i] - m_new);
       ls += s[i];
     }
     l_run = l_run * alpha + ls;
@@ -455,7 +455,7 @@ __device__ inline void task_attn_bwd_kv_tc(const KParams& kp, const AttnArgs& a,
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const int c = c0 + e;
-        const float p = (diag && c < r) ? 0.f : exp2f(s[e] * sl2 - lse2[c]);
+        const float p = (diag && c < r) ? 0.f : ex2_sfu(fmaf(s[e], sl2, -lse2[c]));
         s[e] = p;
         dp[e] = p * (dp[e] - dd[c]) * a.scale;
       }
@@ -582,7 +582,7 @@ __device__ inline void task_attn_bwd_q_tc(const KParams& kp, const AttnArgs& a, 
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const int c = c0 + e;
-        const float p = (diag && c > r) ? 0.f : exp2f(s[e] * sl2 - lse2);
+        const float p = (diag && c > r) ? 0.f : ex2_sfu(fmaf(s[e], sl2, -lse2));
         dp[e] = p * (dp[e] - dd) * a.scale;
       }
       st_row32_sw128(sDs + (uint32_t)half * kAttTile, r, q, dp);

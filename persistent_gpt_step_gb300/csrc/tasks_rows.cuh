@@ -455,21 +455,29 @@ __device__ inline void task_ce(const KParams& kp, const CeArgs& a, int idx) {
 }
 
 // Vectorised variant for bf16 logits with V % 8 == 0: 16-byte loads, 4 in flight.
+// bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32 word.
 __device__ __forceinline__ void bf16x8_to_f(const uint4& u, float* f) {
-  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    float2 t = __bfloat1622float2(h[i]);
-    f[2 * i] = t.x;
-    f[2 * i + 1] = t.y;
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
   }
 }
+__device__ __forceinline__ uint32_t f2_to_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
 __device__ __forceinline__ uint4 f_to_bf16x8(const float* f) {
-  uint4 u;
-  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-  return u;
+  return make_uint4(f2_to_bf16x2(f[0], f[1]), f2_to_bf16x2(f[2], f[3]), f2_to_bf16x2(f[4], f[5]),
+                    f2_to_bf16x2(f[6], f[7]));
+}
+// 2^x with the SFU's approximate base-2 exponential (relative error ~2^-22,
+// subnormal results flushed to zero): one instruction.
+__device__ __forceinline__ float ex2_sfu(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ inline void task_ce_bf16_vec(const KParams& kp, const CeArgs& a, int idx) {
@@ -544,9 +552,9 @@ __device__ inline void task_ce_bf16_vec(const KParams& kp, const CeArgs& a, int 
 
 // Staged variant (bf16, two rows of V logits fit in shared memory): one thread
 // bulk-copies each row into one of two buffers, the next row while this one is
-// processed; the whole block reduces the row (online max / sum of exp, then a
-// fixed-order combination of the eight warps) and writes dz back with 16-byte
-// coalesced stores.  A logit is read from memory once instead of twice.
+// processed; the whole block reduces the row (its maximum, then the sum of
+// exp(z - max), each combined over the eight warps in a fixed order) and writes dz
+// back with 16-byte coalesced stores.  A logit is read from memory once instead of twice.
 // The row copies complete on the bars shared with AdamW (iter counts their
 // phases); every copy issued here is also waited for here.
 __device__ inline void task_ce_bf16_staged(const KParams& kp, const CeArgs& a, int idx, uint8_t* smem,
@@ -585,46 +593,59 @@ __device__ inline void task_ce_bf16_staged(const KParams& kp, const CeArgs& a, i
       if (threadIdx.x == 0) set_soft(kp, kSoftBadToken);
       t = t < 0 ? 0 : a.V - 1;
     }
-    float m = -INFINITY, s = 0.f;
+    // Three passes over the staged row, each with independent per-lane work (no
+    // loop-carried chain through an exponential): the row maximum, the sum of
+    // exp(z - max) in eight accumulators, then the gradient below.  Reductions run
+    // in a fixed order (xor tree in the warp, warps in order).
+    float m8[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 4
     for (int j = threadIdx.x; j < nvec; j += kThreads) {
       float f[8];
       bf16x8_to_f(z[j], f);
-      float lm = f[0];
 #pragma unroll
-      for (int e = 1; e < 8; ++e) lm = fmaxf(lm, f[e]);
-      if (lm > m) { s *= __expf(m - lm); m = lm; }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) s += __expf(f[e] - m);
+      for (int e = 0; e < 8; ++e) m8[e & 3] = fmaxf(m8[e & 3], f[e]);
     }
-    // warp, then block: (m, s) pairs combined in a fixed order
+    float m = fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3]));
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
-      const float mm = fmaxf(m, m2);
-      s = (m == -INFINITY ? 0.f : s * __expf(m - mm)) + (m2 == -INFINITY ? 0.f : s2 * __expf(m2 - mm));
-      m = mm;
-    }
-    if (lane == 0) red[warp] = make_float2(m, s);
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) red[warp].x = m;
     __syncthreads();
     float M = red[0].x;
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) M = fmaxf(M, red[w].x);
+    constexpr float kLog2e = 1.4426950408889634f;
+    const float M2 = M * kLog2e;  // exp(z - M) = 2^(z log2 e - M log2 e)
+    float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int j = threadIdx.x; j < nvec; j += kThreads) {
+      float f[8];
+      bf16x8_to_f(z[j], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) s8[e] += ex2_sfu(fmaf(f[e], kLog2e, -M2));
+    }
+    float s = ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) red[warp].y = s;
+    __syncthreads();
     float S = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) S += red[w].x == -INFINITY ? 0.f : red[w].y * __expf(red[w].x - M);
+    for (int w = 0; w < kWarps; ++w) S += red[w].y;
     const float lse = M + logf(S);
+    const float lse2 = lse * kLog2e;
     if (threadIdx.x == 0) {
       const float zt = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(z)[t]);
       a.row_loss[r] = lse - zt;
       if (!isfinite(lse - zt)) set_soft(kp, kSoftNonFinite);
     }
     uint4* dz = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.logits) + (int64_t)r * a.V);
+#pragma unroll 4
     for (int j = threadIdx.x; j < nvec; j += kThreads) {
       float f[8];
       bf16x8_to_f(z[j], f);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        float p = __expf(f[e] - lse);
+        float p = ex2_sfu(fmaf(f[e], kLog2e, -lse2));
         if (j * 8 + e == t) p -= 1.0f;
         f[e] = p * invN;
       }

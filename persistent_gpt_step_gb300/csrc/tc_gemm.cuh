@@ -195,6 +195,48 @@ __device__ __forceinline__ void gelu_pair_bf(float x, bool tanh_form, float& g, 
   dg = fmaf(h * fmaf(-t, t, 1.0f), fmaf(3.0f * ck0, x2, k0), fmaf(0.5f, t, 0.5f));
 }
 
+// Two-wide fp32 arithmetic (fma / mul / add .rn.f32x2, sm_100 and later): one
+// instruction for two independent lanes, each rounded as the scalar operation is.
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+      " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+// The tanh-form GELU pair of two inputs with the two-wide instructions; the same
+// roundings as gelu_pair_bf (1 - t^2 and k0 + 3 c k0 x^2 are formed negated, which
+// is exact), so the results are bitwise those of two scalar calls.
+__device__ __forceinline__ void gelu_pair_tanh2(float2 x, float2& g, float2& dg) {
+  constexpr float k0 = 0.7978845608028654f, ck0 = 0.044715f * 0.7978845608028654f;
+  const float2 x2 = f2_mul(x, x);
+  const float2 arg = f2_mul(x, f2_fma(make_float2(ck0, ck0), x2, make_float2(k0, k0)));
+  const float2 t = make_float2(tanh_sfu(arg.x), tanh_sfu(arg.y));
+  const float2 h = f2_mul(make_float2(0.5f, 0.5f), x);
+  g = f2_fma(h, t, h);
+  const float2 p = f2_fma(make_float2(0.5f, 0.5f), t, make_float2(0.5f, 0.5f));
+  const float2 nq = f2_fma(make_float2(-3.0f * ck0, -3.0f * ck0), x2, make_float2(-k0, -k0));  // -(k0 + 3 c k0 x^2)
+  const float2 w = f2_mul(h, f2_fma(t, t, make_float2(-1.0f, -1.0f)));                        // -h (1 - t^2)
+  dg = f2_fma(w, nq, p);
+}
+
 __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float* v) {
   uint4 u0, u1;
   __nv_bfloat162* h0 = reinterpret_cast<__nv_bfloat162*>(&u0);
@@ -406,10 +448,18 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
             make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
       } else if constexpr (EPI == EPI_GELU) {  // out = GELU'(v) for the backward, out2 = GELU(v)
         float g[4], dg[4];
-        gelu_pair_bf(v.x, gelu_tanh, g[0], dg[0]);
-        gelu_pair_bf(v.y, gelu_tanh, g[1], dg[1]);
-        gelu_pair_bf(v.z, gelu_tanh, g[2], dg[2]);
-        gelu_pair_bf(v.w, gelu_tanh, g[3], dg[3]);
+        if (gelu_tanh) {
+          float2 g01, d01, g23, d23;
+          gelu_pair_tanh2(make_float2(v.x, v.y), g01, d01);
+          gelu_pair_tanh2(make_float2(v.z, v.w), g23, d23);
+          g[0] = g01.x; g[1] = g01.y; g[2] = g23.x; g[3] = g23.y;
+          dg[0] = d01.x; dg[1] = d01.y; dg[2] = d23.x; dg[3] = d23.y;
+        } else {
+          gelu_pair_bf(v.x, false, g[0], dg[0]);
+          gelu_pair_bf(v.y, false, g[1], dg[1]);
+          gelu_pair_bf(v.z, false, g[2], dg[2]);
+          gelu_pair_bf(v.w, false, g[3], dg[3]);
+        }
         __nv_bfloat162 lo = __floats2bfloat162_rn(dg[0], dg[1]), hi = __floats2bfloat162_rn(dg[2], dg[3]);
         *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + (int64_t)m * ldo + col) =
             make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));

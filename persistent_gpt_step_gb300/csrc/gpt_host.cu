@@ -464,13 +464,16 @@ int make_tmap_out(gpt* h, void* base, bool f32, int64_t cols, int64_t rows, int6
 
 // Gives a tensor-core GEMM op the output map of the TMA-store epilogue where it
 // has one (bf16 store or fp32 store; with a K split the splits' outputs must be
-// stacked row blocks of whole 128-row tiles).
+// stacked row blocks of whole 128-row tiles; a residual GEMM without a separate
+// residual operand adds into its output, which already holds the residual).
 void set_out_map(gpt* h, OpDesc& op) {
   if (op.type != OP_GEMM) return;  // (the arguments are a union: only a GEMM op has c_map)
   GemmArgs& g = op.gemm;
   g.c_map = -1;
   if (!is_bf16(h->cfg) || !g.out) return;
-  if (g.epi == EPI_STORE || g.epi == EPI_STORE_ROPE) {
+  if (g.epi == EPI_RESID && !g.resid) {
+    g.c_map = make_tmap_out(h, g.out, true, g.N, g.M, g.ldo);
+  } else if (g.epi == EPI_STORE || g.epi == EPI_STORE_ROPE) {
     g.c_map = make_tmap_out(h, g.out, false, g.N, g.M, g.ldo);
   } else if (g.epi == EPI_F32) {
     if (g.ksplit > 1 && (g.M % kTcBM || g.split_stride != (int64_t)g.M * g.ldo)) return;
@@ -804,9 +807,11 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
   const int qblock = D.T <= 512 ? 64 : 32;
   for (int l = 0; l < L; ++l) {
     const TensorIds& id = h->lid[l];
+    // bf16 path: LayerNorm also copies its input (the residual stream) into the
+    // next residual GEMM's output, and that GEMM's epilogue adds its product in
     o = blank(OP_LN_FWD, ln_tasks(N));
     o.lnf = LnFwdArgs{F32(Lo.x[l]), P(id.ln1_g), P(id.ln1_b), ACT(Lo.ln1[l]), F32(Lo.ln1_mu[l]),
-                      F32(Lo.ln1_rs[l]), N, C, kRowsLn, c.ln_eps, LDC};
+                      F32(Lo.ln1_rs[l]), N, C, kRowsLn, c.ln_eps, LDC, bf ? F32(Lo.xm[l]) : nullptr};
     op_ln1[l] = bld.add(o, {prev});
     // qkv = ln1 . Wqkv^T + b
     if ((rc = gemm_op(h, &o, N, 3 * C, C, {ACT(Lo.ln1[l]), LDC, false}, {W(id.w_qkv), C, false},
@@ -827,11 +832,12 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
     if ((rc = gemm_op(h, &o, N, C, C, {ACT(Lo.atto[l]), LDC, false}, {W(id.w_o), C, false}, EPI_RESID, 1)))
       return rc;
     o.gemm.out = F32(Lo.xm[l]); o.gemm.ldo = C; o.gemm.bias = P(id.b_o);
-    o.gemm.resid = F32(Lo.x[l]); o.gemm.ldr = C;
+    o.gemm.resid = bf ? nullptr : F32(Lo.x[l]); o.gemm.ldr = C;
     op_atto[l] = bld.add(o, {op_attn[l]});
+    if (bf && h->ops[op_atto[l]].gemm.c_map < 0) return fail(h, GPT_ERR_CUDA, "cuTensorMapEncodeTiled failed (residual)");
     o = blank(OP_LN_FWD, ln_tasks(N));
     o.lnf = LnFwdArgs{F32(Lo.xm[l]), P(id.ln2_g), P(id.ln2_b), ACT(Lo.ln2[l]), F32(Lo.ln2_mu[l]),
-                      F32(Lo.ln2_rs[l]), N, C, kRowsLn, c.ln_eps, LDC};
+                      F32(Lo.ln2_rs[l]), N, C, kRowsLn, c.ln_eps, LDC, bf ? F32(Lo.x[l + 1]) : nullptr};
     op_ln2[l] = bld.add(o, {op_atto[l]});
     // h = ln2 . W1^T + b1 ; g = GELU(h)
     // gated: [gate, up] pairs kept for the backward, GELU(gate) * up to the next GEMM
@@ -845,8 +851,9 @@ int build_graph(gpt* h, const Layout& Lo, int lm_ksplit) {
     if ((rc = gemm_op(h, &o, N, C, F, {ACT(Lo.gact[l]), LDF, false}, {W(id.w_2), F, false}, EPI_RESID, 1)))
       return rc;
     o.gemm.out = F32(Lo.x[l + 1]); o.gemm.ldo = C; o.gemm.bias = P(id.b_2);
-    o.gemm.resid = F32(Lo.xm[l]); o.gemm.ldr = C;
+    o.gemm.resid = bf ? nullptr : F32(Lo.xm[l]); o.gemm.ldr = C;
     op_down[l] = prev = bld.add(o, {op_up[l]});
+    if (bf && h->ops[op_down[l]].gemm.c_map < 0) return fail(h, GPT_ERR_CUDA, "cuTensorMapEncodeTiled failed (residual)");
   }
   o = blank(OP_LN_FWD, ln_tasks(N));
   o.lnf = LnFwdArgs{F32(Lo.x[L]), P(h->t_lnf_g), P(h->t_lnf_b), ACT(Lo.lnf), F32(Lo.lnf_mu), F32(Lo.lnf_rs),
@@ -2035,10 +2042,17 @@ int gpt_test_gemm_epilogue(int32_t M, int32_t N, int32_t K, const void* A, int64
   o.gemm.out = out; o.gemm.ldo = ldo;
   o.gemm.out2 = out2; o.gemm.ldo2 = ldo2;
   o.gemm.bias = epi == EPI_GELU_BWD ? nullptr : bias;
-  if (epi == EPI_RESID) { o.gemm.resid = static_cast<const float*>(src); o.gemm.ldr = lds; }
+  if (epi == EPI_RESID) {  // the output holds the residual first; the epilogue adds into it
+    if (cudaMemcpy2DAsync(out, (size_t)ldo * 4, src, (size_t)lds * 4, (size_t)N * 4, (size_t)M,
+                          cudaMemcpyDeviceToDevice, h.stream) != cudaSuccess)
+      return fail(nullptr, GPT_ERR_CUDA, "residual copy failed");
+    o.gemm.resid = nullptr;
+  }
   if (epi == EPI_GELU_BWD) { o.gemm.aux = src; o.gemm.ldaux = lds; }
   Builder bld{&h};
-  bld.add(o, {});
+  const int op_id = bld.add(o, {});
+  if (epi == EPI_RESID && h.ops[op_id].gemm.c_map < 0)
+    return fail(nullptr, GPT_ERR_UNSUPPORTED, "residual epilogue: output not TMA-addressable (16-byte aligned base)");
   bld.finish(h.num_sms);
   if (kernel_ms) {
     cudaEventCreate(&h.ev0);

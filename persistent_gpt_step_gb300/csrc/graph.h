@@ -108,6 +108,8 @@ struct LnFwdArgs {
   int32_t rows, C, rows_per_task;
   float eps;
   int32_t ldy;      // row pitch of y (>= C)
+  float* copy;      // may be null: x is also copied here (pitch C), the residual
+                    // GEMM's output, which its epilogue then adds its product into
 };
 
 struct LnBwdArgs {

@@ -117,6 +117,10 @@ __device__ __forceinline__ void ln_fwd_rows(const LnFwdArgs& a, int r0, int r1) 
         store4<act_t>(yr + c, (v[i].x - mean) * rstd * g[i].x + bb[i].x, (v[i].y - mean) * rstd * g[i].y + bb[i].y,
                       (v[i].z - mean) * rstd * g[i].z + bb[i].z, (v[i].w - mean) * rstd * g[i].w + bb[i].w);
       }
+      if (a.copy) {
+#pragma unroll
+        for (int i = 0; i < NV; ++i) reinterpret_cast<float4*>(a.copy + (int64_t)r * a.C)[lane + 32 * i] = v[i];
+      }
       if (lane == 0) { a.mean[r] = mean; a.rstd[r] = rstd; }
     }
   } else {
@@ -133,6 +137,7 @@ __device__ __forceinline__ void ln_fwd_rows(const LnFwdArgs& a, int r0, int r1) 
         float o = (x[c] - mean) * rstd * a.g[c];
         if (a.b) o += a.b[c];
         yr[c] = from_f<act_t>(o);
+        if (a.copy) a.copy[(int64_t)r * a.C + c] = x[c];
       }
       if (lane == 0) { a.mean[r] = mean; a.rstd[r] = rstd; }
     }

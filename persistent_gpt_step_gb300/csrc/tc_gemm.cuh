@@ -89,6 +89,14 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, int32_t c0, int32
                "r"(c1), "r"(src)
                : "memory");
 }
+// Adds a 32 x 32 fp32 box from shared memory into global memory (element-wise,
+// performed at L2; bulk async-group of this thread).
+__device__ __forceinline__ void tma_reduce_add_2d(const void* tmap, int32_t c0, int32_t c1, uint32_t src) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   tmap),
+               "r"(c0), "r"(c1), "r"(src)
+               : "memory");
+}
 
 // ---- tcgen05 -----------------------------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -254,11 +262,11 @@ __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float* v
 // all BN columns, in 32-column groups.  The accumulators go TMEM -> registers
 // -> a per-warp 32 x 32 fp32 staging tile in shared memory (16-byte chunks
 // XOR-swizzled by row) -> back to registers in a row-contiguous layout: thread
-// u owns columns 4 (u mod 8) .. +3 of rows 4i + u / 8, so bias, residual,
-// GELU and the stores touch whole 64- or 128-byte row segments.
+// u owns columns 4 (u mod 8) .. +3 of rows 4i + u / 8, so bias, GELU and
+// the stores touch whole 64- or 128-byte row segments.
 //
-// An epilogue that reads a second operand (the residual stream, the stored
-// GELU derivative) issues all 8 of a group's loads at once: the first group's
+// An epilogue that reads a second operand (the stored GELU derivative, the
+// gated MLP's pairs) issues all 8 of a group's loads at once: the first group's
 // before waiting for the accumulator (they land while the MMAs still run), each
 // next group's before the current one is processed, so a tile pays about one
 // memory latency instead of one per few rows.  Returns false when the wait for
@@ -266,10 +274,6 @@ __device__ __forceinline__ void store_bf16x16(__nv_bfloat16* dst, const float* v
 template <int EPI>
 struct EpiSrc {
   using T = uint2;  // EPI_GELU_BWD: four bf16 GELU derivatives
-};
-template <>
-struct EpiSrc<EPI_RESID> {
-  using T = float4;  // four fp32 residual-stream values
 };
 template <>
 struct EpiSrc<EPI_GEGLU_BWD> {
@@ -280,7 +284,7 @@ template <int EPI>
 __device__ __forceinline__ void epi_load_src(typename EpiSrc<EPI>::T* dst, const void* src, int64_t lds, int M,
                                              int r0, int col) {
   using T = typename EpiSrc<EPI>::T;
-  constexpr int64_t es = EPI == EPI_RESID ? 4 : 2;           // element bytes of the source
+  constexpr int64_t es = 2;                                  // element bytes of the source (bf16)
   constexpr int64_t cw = EPI == EPI_GEGLU_BWD ? 2 : 1;       // source columns per output column
   const T* p = reinterpret_cast<const T*>(reinterpret_cast<const char*>(src) + ((int64_t)r0 * lds + cw * col) * es);
   const int64_t step = 4 * lds * es / (int64_t)sizeof(T);
@@ -297,7 +301,7 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
                                              const bool gelu_tanh, const int n_real, float* const bias_grad,
                                              const uint32_t acc_bar, const uint32_t acc_parity, uint32_t* const err,
                                              const uint64_t timeout_ns, const void* const cmap, const int crow0) {
-  constexpr bool kSrc = EPI == EPI_RESID || EPI == EPI_GELU_BWD || EPI == EPI_GEGLU_BWD;
+  constexpr bool kSrc = EPI == EPI_GELU_BWD || EPI == EPI_GEGLU_BWD;
   using SrcT = typename EpiSrc<EPI>::T;
   const int lane = threadIdx.x & 31;
   const int cu = 4 * (lane & 7);     // this thread's first column within the group
@@ -310,13 +314,17 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
   __syncwarp();  // lanes leave the poll loop separately; tcgen05.ld below is warp-aligned
   if (!acc_ok) return false;
   tc_fence_after();
-  if constexpr (EPI == EPI_STORE || EPI == EPI_STORE_ROPE || EPI == EPI_F32) {
+  if constexpr (EPI == EPI_STORE || EPI == EPI_STORE_ROPE || EPI == EPI_F32 || EPI == EPI_RESID) {
     if (cmap) {
       // TMA-store path: each lane holds its own row's 32 columns, writes them
       // (bias added and rounded to bf16, or fp32) into a swizzled 32 x 32 box in
       // the warp's staging area (two boxes, alternating), and lane 0 stores the
       // box with one bulk tensor copy — one pass through shared memory and no
-      // per-row global stores.
+      // per-row global stores.  The residual epilogue (its output already holds
+      // the residual stream, copied there by the LayerNorm that read it) adds the
+      // box (accumulator + bias, fp32) into the output with a bulk tensor
+      // reduction instead: out = residual + (acc + bias), one rounding, as the
+      // row path computes it.
       const uint32_t sbase = smem_u32(stage);
       int gi = 0;
       for (int c = 0; c < cend; c += 32, ++gi) {
@@ -342,6 +350,17 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
                          "r"(r[ch >> 2][4 * (ch & 3)]), "r"(r[ch >> 2][4 * (ch & 3) + 1]),
                          "r"(r[ch >> 2][4 * (ch & 3) + 2]), "r"(r[ch >> 2][4 * (ch & 3) + 3])
                          : "memory");
+        } else if constexpr (EPI == EPI_RESID) {
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch) {  // the same 128-byte swizzled rows, bias added
+            float4 b = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (bias) b = reinterpret_cast<const float4*>(bias + n)[ch];
+            const uint32_t* x = &r[ch >> 2][4 * (ch & 3)];
+            asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(buf + lane * 128 + ((ch ^ (lane & 7)) << 4)),
+                         "f"(__uint_as_float(x[0]) + b.x), "f"(__uint_as_float(x[1]) + b.y),
+                         "f"(__uint_as_float(x[2]) + b.z), "f"(__uint_as_float(x[3]) + b.w)
+                         : "memory");
+          }
         } else {
           uint32_t w[16];
           // rotary embedding of q and k (src: the (cos, sin) table of period lds)
@@ -377,7 +396,8 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic smem writes -> the bulk copy
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(cmap, n, crow0, buf);
+          if constexpr (EPI == EPI_RESID) tma_reduce_add_2d(cmap, n, crow0, buf);
+          else tma_store_2d(cmap, n, crow0, buf);
           asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
       }
@@ -389,6 +409,7 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
       return true;
     }
   }
+  if constexpr (EPI == EPI_RESID) return false;  // the residual epilogue has only the reduction path
   for (int c = 0; c < cend; c += 32) {
     const int n = n0 + c;
     {
@@ -467,10 +488,6 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
         hi = __floats2bfloat162_rn(g[2], g[3]);
         *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out2) + (int64_t)m * ldo2 + col) =
             make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
-      } else if constexpr (EPI == EPI_RESID) {
-        const float4 rr = cur[i];
-        *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (int64_t)m * ldo + col) =
-            make_float4(rr.x + v.x, rr.y + v.y, rr.z + v.z, rr.w + v.w);
       } else if constexpr (EPI == EPI_F32) {
         if (n >= n_real) {  // the padded columns: the first is the bias gradient
           if (n == n_real && cu == 0 && bias_grad) bias_grad[m] = v.x;

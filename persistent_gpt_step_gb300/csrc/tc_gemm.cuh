@@ -409,7 +409,9 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
       return true;
     }
   }
-  if constexpr (EPI == EPI_RESID) return false;  // the residual epilogue has only the reduction path
+  if constexpr (EPI == EPI_RESID) {
+    return false;  // the residual epilogue has only the reduction path
+  } else {
   for (int c = 0; c < cend; c += 32) {
     const int n = n0 + c;
     {
@@ -539,6 +541,7 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
     }
   }
   return true;
+  }
 }
 
 // Waits for the tile's accumulator and runs its epilogue (false: the wait failed).

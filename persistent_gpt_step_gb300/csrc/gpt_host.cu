@@ -720,8 +720,13 @@ struct Operand {
   bool mn_major;
 };
 
-int pick_bn(int M, int N, int num_sms) {
-  // prefer wide tiles, but not at the price of badly filled waves
+int pick_bn(int M, int N, int num_sms, bool weight_grad) {
+  // Weight-gradient GEMMs (both operands MN-major, K = tokens) run beside the
+  // input-gradient chain of the backward, so what they cost is SM time, not a
+  // wave of their own: 256-wide tiles do about twice the work per SM-second of
+  // 128-wide ones there (traced in the 162M step).
+  if (weight_grad && N >= 256 && N % 64 == 0) return 256;
+  // otherwise prefer wide tiles, but not at the price of badly filled waves
   const int tm = (M + kTcBM - 1) / kTcBM;
   int best = 64;
   double best_eff = -1;
@@ -752,7 +757,7 @@ int gemm_op(gpt* h, OpDesc* op, int M, int N, int K, Operand A, Operand B, int e
   g.a_map = g.b_map = g.c_map = -1;
   if (is_bf16(h->cfg)) {
     g.BM = kTcBM;
-    g.BN = pick_bn(M, N, h->num_sms);
+    g.BN = pick_bn(M, N, h->num_sms, A.mn_major && B.mn_major && epi == EPI_F32);
     g.BK = kTcBK;
     g.a_map = A.mn_major ? make_tmap(h, A.p, M, K, A.ld, 64) : make_tmap(h, A.p, K, M, A.ld, kTcBM);
     g.b_map = B.mn_major ? make_tmap(h, B.p, N, K, B.ld, 64) : make_tmap(h, B.p, K, N, B.ld, g.BN);

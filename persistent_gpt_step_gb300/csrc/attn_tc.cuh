@@ -234,9 +234,12 @@ __device__ inline void task_attn_fwd_tc(const KParams& kp, const AttnArgs& a, in
     const bool diag = j == nkb - 1;
     float mx = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      s[i] = (diag && half * 64 + i > r) ? -INFINITY : s[i] * sl2;
+    for (int i = 0; i < 64; i += 2) {  // the scale two columns per instruction
+      const float2 v = f2_mul(make_float2(s[i], s[i + 1]), make_float2(sl2, sl2));
+      s[i] = (diag && half * 64 + i > r) ? -INFINITY : v.x;
+      s[i + 1] = (diag && half * 64 + i + 1 > r) ? -INFINITY : v.y;
       mx = fmaxf(mx, s[i]);
+      mx = fmaxf(mx, s[i + 1]);
     }
     sc.red[half][r] = mx;
     pair_sync(quarter);
@@ -244,9 +247,12 @@ __device__ inline void task_attn_fwd_tc(const KParams& kp, const AttnArgs& a, in
     const float alpha = ex2_sfu(m_run - m_new);
     float ls = 0.f;
 #pragma unroll
-    for (int i = 0; i < 64; ++i) {
-      s[i] = ex2_sfu(s[i] - m_new);
+    for (int i = 0; i < 64; i += 2) {
+      const float2 d = f2_add(make_float2(s[i], s[i + 1]), make_float2(-m_new, -m_new));
+      s[i] = ex2_sfu(d.x);
+      s[i + 1] = ex2_sfu(d.y);
       ls += s[i];
+      ls += s[i + 1];
     }
     l_run = l_run * alpha + ls;
     m_run = m_new;
@@ -406,10 +412,10 @@ __device__ inline void task_attn_bwd_kv_tc(const KParams& kp, const AttnArgs& a,
     tma_load_2d(sQ + st * kAttTile, qmap, h * 64, row0 + i * kAttBlk, bar);
     tma_load_2d(sO + st * kAttTile, dmap, h * 64, row0 + i * kAttBlk, bar);
   };
-  auto stage_ld = [&](int it) {  // all threads: LSE (base 2) and D of query block kb + it
+  auto stage_ld = [&](int it) {  // all threads: -LSE (base 2) and -D of query block kb + it
     const int i = kb + it, c = threadIdx.x & (kAttBlk - 1), w = threadIdx.x >> 7;
     const float v = w == 0 ? Lg[i * kAttBlk + c] * log2e : Dg[i * kAttBlk + c];
-    sc.ld[it & 1][w][c] = v;
+    sc.ld[it & 1][w][c] = -v;
   };
   if (leader) {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -444,20 +450,29 @@ __device__ inline void task_attn_bwd_kv_tc(const KParams& kp, const AttnArgs& a,
     __syncwarp();
     tc_fence_after();
     const bool diag = it == 0;  // the key block's own query block: queries before a key are masked
-    const float* lse2 = sc.ld[buf][0];
-    const float* dd = sc.ld[buf][1];
+    const float4* nlse2 = reinterpret_cast<const float4*>(sc.ld[buf][0]);  // -LSE log2 e per query column
+    const float4* ndd = reinterpret_cast<const float4*>(sc.ld[buf][1]);    // -D per query column
+    const float2 sl2v = make_float2(sl2, sl2), scv = make_float2(a.scale, a.scale);
 #pragma unroll 1
     for (int q = 0; q < 2; ++q) {  // 32 query columns at a time
       float s[32], dp[32];
       const int c0 = half * 64 + q * 32;
       tmem_ld32(trow + (uint32_t)c0, s);
       tmem_ld32(trow + 128u + (uint32_t)c0, dp);
+      // two columns per instruction: p = 2^(s sl2 - lse2), ds = p (dp - D) scale
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int c = c0 + e;
-        const float p = (diag && c < r) ? 0.f : ex2_sfu(fmaf(s[e], sl2, -lse2[c]));
-        s[e] = p;
-        dp[e] = p * (dp[e] - dd[c]) * a.scale;
+      for (int e4 = 0; e4 < 8; ++e4) {
+        const float4 nl = nlse2[(c0 >> 2) + e4], nd = ndd[(c0 >> 2) + e4];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int e = 4 * e4 + 2 * k, c = c0 + e;
+          const float2 arg = f2_fma(make_float2(s[e], s[e + 1]), sl2v, k ? make_float2(nl.z, nl.w) : make_float2(nl.x, nl.y));
+          const float2 p = make_float2((diag && c < r) ? 0.f : ex2_sfu(arg.x), (diag && c + 1 < r) ? 0.f : ex2_sfu(arg.y));
+          const float2 t = f2_add(make_float2(dp[e], dp[e + 1]), k ? make_float2(nd.z, nd.w) : make_float2(nd.x, nd.y));
+          const float2 ds = f2_mul(f2_mul(p, t), scv);
+          s[e] = p.x; s[e + 1] = p.y;
+          dp[e] = ds.x; dp[e + 1] = ds.y;
+        }
       }
       st_row32_sw128(sPt + (uint32_t)half * kAttTile, r, q, s);
       st_row32_sw128(sDs + (uint32_t)half * kAttTile, r, q, dp);
@@ -580,10 +595,13 @@ __device__ inline void task_attn_bwd_q_tc(const KParams& kp, const AttnArgs& a, 
       tmem_ld32(trow + (uint32_t)c0, s);
       tmem_ld32(trow + 128u + (uint32_t)c0, dp);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
+      for (int e = 0; e < 32; e += 2) {  // two columns per instruction
         const int c = c0 + e;
-        const float p = (diag && c > r) ? 0.f : ex2_sfu(fmaf(s[e], sl2, -lse2));
-        dp[e] = p * (dp[e] - dd) * a.scale;
+        const float2 arg = f2_fma(make_float2(s[e], s[e + 1]), make_float2(sl2, sl2), make_float2(-lse2, -lse2));
+        const float2 p = make_float2((diag && c > r) ? 0.f : ex2_sfu(arg.x), (diag && c + 1 > r) ? 0.f : ex2_sfu(arg.y));
+        const float2 t = f2_add(make_float2(dp[e], dp[e + 1]), make_float2(-dd, -dd));
+        const float2 ds = f2_mul(f2_mul(p, t), make_float2(a.scale, a.scale));
+        dp[e] = ds.x; dp[e + 1] = ds.y;
       }
       st_row32_sw128(sDs + (uint32_t)half * kAttTile, r, q, dp);
     }

@@ -308,8 +308,32 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
   const int rq = lane >> 3;          // first row (of 4)
   const int r0 = row0 + rq;
   const int cend = min(BN, N - n0);  // N is a multiple of 64
-  SrcT nxt[kSrc ? 8 : 1];
-  if constexpr (kSrc) epi_load_src<EPI>(nxt, src, lds, M, r0, n0 + cu);
+  // The stored GELU derivative is staged with cp.async two column groups ahead,
+  // each thread's own eight 8-byte pieces in the upper half of the warp's staging
+  // area ([slot][row i][lane], 2 KB a group): no registers are held while the
+  // copies are in flight.  The gated pairs keep the one-group register prefetch.
+  constexpr bool kAsync = EPI == EPI_GELU_BWD;
+  constexpr bool kSrcReg = kSrc && !kAsync;
+  SrcT nxt[kSrcReg ? 8 : 1];
+  if constexpr (kSrcReg) epi_load_src<EPI>(nxt, src, lds, M, r0, n0 + cu);
+  const uint32_t aslot = smem_u32(stage) + 4096u;
+  auto async_src = [&](int c, uint32_t slot) {
+    const int col = n0 + c + cu;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = r0 + 4 * i;
+      const char* g = r < M ? reinterpret_cast<const char*>(src) + ((int64_t)r * lds + col) * 2
+                            : reinterpret_cast<const char*>(src);
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(aslot + slot * 2048u + (uint32_t)(i * 32 + lane) * 8u),
+                   "l"(g), "r"(r < M ? 8 : 0)
+                   : "memory");
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  if constexpr (kAsync) {
+    async_src(0, 0u);
+    if (32 < cend) async_src(32, 1u);
+  }
   const bool acc_ok = mbar_wait_e(err, timeout_ns, acc_bar, acc_parity);
   __syncwarp();  // lanes leave the poll loop separately; tcgen05.ld below is warp-aligned
   if (!acc_ok) return false;
@@ -432,7 +456,20 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
       __syncwarp();
     }
     SrcT cur[kSrc ? 8 : 1];
-    if constexpr (kSrc) {
+    if constexpr (kAsync) {
+      const uint32_t slot = (uint32_t)(c >> 5) & 1u;
+      if (c + 32 < cend) asm volatile("cp.async.wait_group 1;" ::: "memory");  // this group's copies landed
+      else asm volatile("cp.async.wait_group 0;" ::: "memory");
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t x, y;
+        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(x), "=r"(y)
+                     : "r"(aslot + slot * 2048u + (uint32_t)(i * 32 + lane) * 8u)
+                     : "memory");
+        cur[i] = make_uint2(x, y);
+      }
+      if (c + 64 < cend) async_src(c + 64, slot);  // the slot just read (by this thread alone)
+    } else if constexpr (kSrc) {
 #pragma unroll
       for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
       if (c + 32 < cend) epi_load_src<EPI>(nxt, src, lds, M, r0, n + 32 + cu);

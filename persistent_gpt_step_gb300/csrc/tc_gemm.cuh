@@ -308,31 +308,33 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
   const int rq = lane >> 3;          // first row (of 4)
   const int r0 = row0 + rq;
   const int cend = min(BN, N - n0);  // N is a multiple of 64
-  // The stored GELU derivative is staged with cp.async two column groups ahead,
-  // each thread's own eight 8-byte pieces in the upper half of the warp's staging
-  // area ([slot][row i][lane], 2 KB a group): no registers are held while the
-  // copies are in flight.  The gated pairs keep the one-group register prefetch.
-  constexpr bool kAsync = EPI == EPI_GELU_BWD;
-  constexpr bool kSrcReg = kSrc && !kAsync;
-  SrcT nxt[kSrcReg ? 8 : 1];
-  if constexpr (kSrcReg) epi_load_src<EPI>(nxt, src, lds, M, r0, n0 + cu);
+  // The second operand (the stored GELU derivative, the gated pairs) is staged
+  // with cp.async, each thread's own eight pieces in the upper half of the warp's
+  // staging area ([slot][row i][lane]): two 2 KB slots, two column groups ahead,
+  // for the 8-byte derivative pieces; one 4 KB slot, one group ahead, for the
+  // 16-byte pairs.  No registers are held while the copies are in flight.
+  constexpr int kPiece = (int)sizeof(SrcT);
+  constexpr int kSlots = EPI == EPI_GELU_BWD ? 2 : 1;
+  constexpr uint32_t kSlotBytes = 8u * 32u * (uint32_t)kPiece;
+  constexpr int64_t kCw = EPI == EPI_GEGLU_BWD ? 2 : 1;  // source columns per output column
   const uint32_t aslot = smem_u32(stage) + 4096u;
   auto async_src = [&](int c, uint32_t slot) {
     const int col = n0 + c + cu;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int r = r0 + 4 * i;
-      const char* g = r < M ? reinterpret_cast<const char*>(src) + ((int64_t)r * lds + col) * 2
+      const char* g = r < M ? reinterpret_cast<const char*>(src) + ((int64_t)r * lds + kCw * col) * 2
                             : reinterpret_cast<const char*>(src);
-      asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(aslot + slot * 2048u + (uint32_t)(i * 32 + lane) * 8u),
-                   "l"(g), "r"(r < M ? 8 : 0)
+      asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;" ::"r"(aslot + slot * kSlotBytes +
+                                                                         (uint32_t)(i * 32 + lane) * (uint32_t)kPiece),
+                   "l"(g), "n"(kPiece), "r"(r < M ? kPiece : 0)
                    : "memory");
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
   };
-  if constexpr (kAsync) {
+  if constexpr (kSrc) {
     async_src(0, 0u);
-    if (32 < cend) async_src(32, 1u);
+    if (kSlots == 2 && 32 < cend) async_src(32, 1u);
   }
   const bool acc_ok = mbar_wait_e(err, timeout_ns, acc_bar, acc_parity);
   __syncwarp();  // lanes leave the poll loop separately; tcgen05.ld below is warp-aligned
@@ -456,23 +458,28 @@ static __device__ __noinline__ bool epi_tile(const int M, const int N, const int
       __syncwarp();
     }
     SrcT cur[kSrc ? 8 : 1];
-    if constexpr (kAsync) {
-      const uint32_t slot = (uint32_t)(c >> 5) & 1u;
-      if (c + 32 < cend) asm volatile("cp.async.wait_group 1;" ::: "memory");  // this group's copies landed
+    if constexpr (kSrc) {
+      const uint32_t slot = kSlots == 2 ? ((uint32_t)(c >> 5) & 1u) : 0u;
+      if (kSlots == 2 && c + 32 < cend) asm volatile("cp.async.wait_group 1;" ::: "memory");  // this group landed
       else asm volatile("cp.async.wait_group 0;" ::: "memory");
+      const uint32_t sp = aslot + slot * kSlotBytes + (uint32_t)lane * (uint32_t)kPiece;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        uint32_t x, y;
-        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(x), "=r"(y)
-                     : "r"(aslot + slot * 2048u + (uint32_t)(i * 32 + lane) * 8u)
-                     : "memory");
-        cur[i] = make_uint2(x, y);
+        const uint32_t ad = sp + (uint32_t)(i * 32 * kPiece);
+        if constexpr (kPiece == 8) {
+          uint2 v;
+          asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(ad) : "memory");
+          cur[i] = *reinterpret_cast<SrcT*>(&v);
+        } else {
+          uint4 v;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(ad)
+                       : "memory");
+          cur[i] = *reinterpret_cast<SrcT*>(&v);
+        }
       }
-      if (c + 64 < cend) async_src(c + 64, slot);  // the slot just read (by this thread alone)
-    } else if constexpr (kSrc) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) cur[i] = nxt[i];
-      if (c + 32 < cend) epi_load_src<EPI>(nxt, src, lds, M, r0, n + 32 + cu);
+      // refill the slot just read (by this thread alone)
+      if (kSlots == 2 && c + 64 < cend) async_src(c + 64, slot);
+      if (kSlots == 1 && c + 32 < cend) async_src(c + 32, 0u);
     }
     const int col = n + cu;
     float4 b = make_float4(0.f, 0.f, 0.f, 0.f);

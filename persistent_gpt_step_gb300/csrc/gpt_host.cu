@@ -538,7 +538,9 @@ struct Builder {
         int tm, tn, sp;
         gemm_coords_host(g, i, tm, tn, sp);
         const double k = (double)g.K / g.ksplit;
-        us = 1.5 + 2.0 * g.BM * g.BN * k / 7e6;
+        // traced in the 162M step: a tile costs ~6 us beyond its MMA work at ~7 TFLOP/s
+        // per SM (loads in flight, epilogue, release), the GELU epilogue ~6 us more
+        us = 6.0 + 2.0 * g.BM * g.BN * k / 7e6 + (g.epi == EPI_GELU ? 6.0 : 0.0);
         if (rowed && !g.a_mn && g.M == D.N) { blk = tm; lo = hi = tm; }  // token-major output rows
       } break;
       case OP_ATTN_FWD:

@@ -170,6 +170,35 @@ def test_attention_tasks_match_autograd(dt, Bn, T, H, d):
         assert worst <= tols[name] * scale, (name, worst / scale, divmod(int(err.argmax()), ref.shape[-1]))
 
 
+def test_attention_forward_rescales_when_the_max_jumps():
+    """Keys whose norms grow block by block (x1, x3, x5, x7 over the 128-token key
+    blocks, queries x3): every later key block's score max exceeds the running max
+    by far more than 8 (base 2), so the forward's running max and its rescaling of
+    the accumulated output and sum act at every block, with probabilities of very
+    different magnitudes.  Element-wise against float64 autograd, as above."""
+    Bn, T, H, d = 2, 512, 2, 64
+    g = torch.Generator(device="cuda").manual_seed(4242)
+    qkv = torch.randn(Bn * T, 3 * H * d, device="cuda", generator=g)
+    grow = 1.0 + 2.0 * ((torch.arange(Bn * T, device="cuda") % T) // 128).float()
+    qkv[:, :H * d] *= 3.0
+    qkv[:, H * d:2 * H * d] *= grow[:, None]
+    qkv = qkv.to(torch.bfloat16)
+    dout = torch.randn(Bn * T, H * d, device="cuda", generator=g).to(torch.bfloat16)
+    o, lse, dqkv = B.test_attention(qkv, dout, Bn, T, H, d)
+    ro, rlse, rd = _attn_reference(qkv, dout, Bn, T, H, d)
+    for got, ref, name, tol in ((o, ro, "o", 1e-2), (lse, rlse, "lse", 1e-3), (dqkv, rd, "dqkv", 2e-2)):
+        assert torch.isfinite(got).all(), name
+        err = (got.double() - ref).abs()
+        worst = err.max().item()
+        assert worst <= tol * ref.abs().max().item(), (name, worst, divmod(int(err.argmax()), ref.shape[-1]))
+    # the scores do jump: block maxima (base 2) of the last query block differ by more than 8
+    q = qkv[:, :H * d].double().view(Bn, T, H, d)[0, 384:, 0]
+    k = qkv[:, H * d:2 * H * d].double().view(Bn, T, H, d)[0, :, 0]
+    s2 = (q @ k.T) / math.sqrt(d) * 1.4426950408889634
+    blk = torch.stack([s2[:, 128 * j:128 * (j + 1)].max(dim=1).values for j in range(3)])
+    assert ((blk[1:] - blk[:-1]) > 8).float().mean() > 0.9
+
+
 # ----------------------------------------------------------------- model parity
 
 def test_create_initialises_from_spec():

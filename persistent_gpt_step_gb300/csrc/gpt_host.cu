@@ -550,7 +550,8 @@ struct Builder {
           blk = (b * D.T + qb * 128) / kRowBlock;
           lo = o.type == OP_ATTN_FWD ? b * D.T / kRowBlock : blk;
           hi = blk;
-          // (mma.sync attention runs near 1.25 FLOP per ns per SM: traced task times)
+          // (scaled to traced task times; the forward's fixed part is underestimated, which
+          // measured better in the list order than costs fitted to the trace)
           us = 1.0 + (o.type == OP_ATTN_FWD ? 4.0 : 6.0) * 128.0 * (qb * 128 + 128) * D.d / 1.25e6;
         } else {
           us = 1.0 + 4.0 * D.T * D.T * D.d / 1e5;

@@ -14,9 +14,10 @@
 //   forward, task (b, h, 128 queries), key blocks j = 0 .. diagonal:
 //       S_j = Q K_j^T (TMEM, two buffers: S_{j+1} is computed while S_j is
 //       reduced), running row max m and sum l in registers (base 2), P_j =
-//       exp2(S_j * scale * log2 e - m) (the SFU's approximate 2^x) to shared memory, O_j = P_j V_j into one of
-//       two TMEM buffers; the thread adds O_j to its 32 output columns, rescaled
-//       by exp2(m_old - m_new), while the next block's probabilities are formed.
+//       exp2(S_j * scale * log2 e - m) (the SFU's approximate 2^x) to shared
+//       memory, O_j = P_j V_j into one of two TMEM buffers; the thread adds O_j
+//       to its 32 output columns, rescaled by exp2(m_old - m_new), while the
+//       next block's probabilities are formed.
 //       O = sum / l, LSE = ln 2 (m + log2 l) saved for the backward pass.
 //   backward pre-pass, task (64 rows):  D_i = sum_c dO_ic O_ic per head.
 //   backward dK/dV, task (b, h, 128 keys), query blocks i at or after the keys:

@@ -4,7 +4,8 @@
 // tcgen05.mma (kind::f16, bf16 x bf16 -> fp32) into one of two TMEM
 // accumulators; four epilogue warps read the other back with tcgen05.ld and run
 // the fused epilogue (bias, residual add, GELU, GELU', fp32 or bf16 stores — the
-// plain stores as bulk tensor copies of 32 x 32 boxes).
+// plain stores as bulk tensor copies of 32 x 32 boxes, the residual add as a bulk
+// tensor reduction into the output, which already holds the residual stream).
 //
 // Operand majorness comes from the UMMA descriptors, not from transposes:
 //   forward       C = X  W^T   A = X  [M,K] K-major,   B = W [N,K] K-major
